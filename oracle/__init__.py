@@ -145,7 +145,8 @@ def bt_dense(D, O):
 def pcg(D, O, Pd, Po, gamma, eps, max_iters, lambda0=None, stop_rule=0):
     """PCG on S lambda = gamma; returns (lambda [N][n], iterations, converged).
 
-    stop_rule 0: ||r|| <= eps ||gamma||;  1: r^T Phi^-1 r <= eps^2 eta0."""
+    stop_rule 0: ||r|| <= eps ||gamma||;  1: r^T Phi^-1 r <= eps^2 eta0;
+    2: r^T D^-1 r <= eps^2 gamma^T D^-1 gamma (D = blockdiag(S))."""
     L = _load()
     N, n = D.shape[0], D.shape[1]
     args = [_f64(x) for x in (D, O, Pd, Po, gamma)]

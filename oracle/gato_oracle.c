@@ -402,13 +402,29 @@ void oracle_bt_dense(int N, int n, const double *Dg, const double *Off, double *
  * iteration):
  *   stop_rule 0: relative residual  ||r||_2 <= eps ||gamma||_2
  *   stop_rule 1: preconditioned     r^T Phi^-1 r <= eps^2 eta0
+ *   stop_rule 2: block-Jacobi-scaled residual r^T D^-1 r <= eps^2 gamma^T D^-1 gamma,
+ *                D^-1 = Pd, the diagonal blocks of Phi^-1
  * Returns 0 if converged, 1 if max_iters was reached; *iters = iterations run.
  * With eps = 0 and max_iters = k the result is exactly the k-th iterate.
  */
-static int pcg_converged(int rule, int d, const double *rv, double eta,
-                         double eta0, double gg, double eps)
+/* x^T blockdiag(Pd) x */
+static double dinv_norm2(int N, int n, const double *Pd, const double *x)
 {
-    if (rule == 0) return dot(d, rv, rv) <= eps * eps * gg;
+    double s = 0.0;
+    double *t = malloc(sizeof(double) * n);
+    for (int j = 0; j < N; ++j) {
+        gemv(n, n, Pd + j * n * n, 0, x + j * n, t);
+        s += dot(n, x + j * n, t);
+    }
+    free(t);
+    return s;
+}
+
+static int pcg_converged(int rule, int N, int n, const double *Pd, const double *rv,
+                         double eta, double eta0, double ref, double eps)
+{
+    if (rule == 0) return dot(N * n, rv, rv) <= eps * eps * ref;
+    if (rule == 2) return dinv_norm2(N, n, Pd, rv) <= eps * eps * ref;
     return eta <= eps * eps * eta0;
 }
 
@@ -426,8 +442,9 @@ int oracle_pcg(int N, int n, const double *Dg, const double *Off, const double *
     bt_matvec(N, n, Pd, Po, rv, z);
     memcpy(p, z, sizeof(double) * d);
     double eta = dot(d, rv, z);
-    const double eta0 = eta, gg = dot(d, gamma, gamma);
-    int done = pcg_converged(stop_rule, d, rv, eta, eta0, gg, eps);
+    const double eta0 = eta;
+    const double ref = stop_rule == 2 ? dinv_norm2(N, n, Pd, gamma) : dot(d, gamma, gamma);
+    int done = pcg_converged(stop_rule, N, n, Pd, rv, eta, eta0, ref, eps);
     while (!done && it < max_iters) {
         ++it;
         bt_matvec(N, n, Dg, Off, p, v);
@@ -435,7 +452,7 @@ int oracle_pcg(int N, int n, const double *Dg, const double *Off, const double *
         for (int i = 0; i < d; ++i) { lambda[i] += alpha * p[i]; rv[i] -= alpha * v[i]; }
         bt_matvec(N, n, Pd, Po, rv, z);
         double eta_new = dot(d, rv, z);
-        done = pcg_converged(stop_rule, d, rv, eta_new, eta0, gg, eps);
+        done = pcg_converged(stop_rule, N, n, Pd, rv, eta_new, eta0, ref, eps);
         if (done) break;
         double beta = eta_new / eta;
         for (int i = 0; i < d; ++i) p[i] = z[i] + beta * p[i];

@@ -222,7 +222,7 @@ def test_pcg_iterates_match_scipy(k):
     assert rel(lam, ref) < 1e-9
 
 
-@pytest.mark.parametrize("stop_rule", [0, 1])
+@pytest.mark.parametrize("stop_rule", [0, 1, 2])
 @pytest.mark.parametrize("w", [0, 1, 2, 4])
 def test_pcg_tight_tolerance_reaches_direct(w, stop_rule):
     prob = oracle.solve_one(make_batch(WORKLOADS[w], M=1, N=min(WORKLOADS[w].N, 32)), 0)
