@@ -1,0 +1,339 @@
+"""Benchmark: batched KKT solves per second on one GB300 (or N replicas).
+
+A step is one gato_solve_kkt call over the whole batch: Schur complement and
+stair preconditioner formation, batched PCG with dz recovery, and the
+8-candidate L1-merit line search.  The workload is the 256-solve batch of
+128-knot problems (n = 14 states, m = 7 controls, fp32) with synthetic,
+seeded data; inputs are resident in HBM when the timed region starts and L2
+is flushed (256 MB write) before every timed step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  With --impl reference the fp64 CPU oracle is
+timed on the host cores on the same workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KKT solves/sec and PCG iters/sec at batch M; % of GB300 HBM/L2 roofline"
+UNIT = "solves/s"
+WORKLOAD_INDEX = 4  # M=256, N=128, n=14, m=7
+
+# DRAM traffic of one PCG launch from an ncu capture, valid only for the kernel
+# source it was taken on (sha256 prefix of csrc/pcg.cu); null otherwise.
+PCG_TRAFFIC = {"pcg_sha": None, "bytes_per_launch": None}
+
+
+def _src_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 6:
+                self.rows.append(parts)
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[2 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """fp64 oracle on the host cores, same workload, bounded per step."""
+    if rank != 0:
+        return
+    import multiprocessing as mp
+
+    import oracle
+    from trajectory_optimization_kkt_gb300.workloads import WORKLOADS, make_batch
+    w = WORKLOADS[WORKLOAD_INDEX]
+    cores = os.cpu_count() or 1
+    per_step = max(cores, 16)  # solves per timed step: a bounded sample of the batch
+    prob = make_batch(w, M=per_step)
+    oracle.build()
+    solves = [oracle.solve_one(prob, j) for j in range(per_step)]
+    kw = dict(eps=w.pcg_eps, max_iters=w.pcg_max_iters, n_alpha=w.n_alpha, beta=w.beta, mu=w.mu)
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        for _ in range(args.warmup):
+            pool.starmap(_oracle_solve, [(s, kw) for s in solves])
+        times, iters = [], 0
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            res = pool.starmap(_oracle_solve, [(s, kw) for s in solves])
+            times.append(time.perf_counter() - t0)
+            iters += sum(r[0] for r in res)
+    sec = sum(times)
+    value = per_step * args.steps / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * sec / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "pcg_iters_per_sec": iters / sec,
+        "config": _config(w, per_step_solves=per_step),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} of the {w.M} solves per step, spawn pool of {cores}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _oracle_solve(prob, kw):
+    import oracle
+    out = oracle.solve_kkt(prob, **kw)
+    return out["iters"], out["best"]
+
+
+def _config(w, **extra):
+    c = {"workload": w.name, "M": w.M, "N": w.N, "n": w.n, "m": w.m, "pcg_eps": w.pcg_eps,
+         "pcg_max_iters": w.pcg_max_iters, "stop_rule": "relative residual ||r||<=eps||gamma||",
+         "n_alpha": w.n_alpha, "beta": w.beta, "mu": w.mu,
+         "refine_steps": w.refine_steps, "refine_eps": w.refine_eps,
+         "l2": "flushed before every timed step (256 MB write)"}
+    c.update(extra)
+    return c
+
+
+def _cpu_baseline(w, budget_s=12.0):
+    """Oracle on a bounded sample of the workload, spawn pool on all cores."""
+    import multiprocessing as mp
+
+    import oracle
+    from trajectory_optimization_kkt_gb300.workloads import make_batch
+    cores = os.cpu_count() or 1
+    oracle.build()
+    kw = dict(eps=w.pcg_eps, max_iters=w.pcg_max_iters, n_alpha=w.n_alpha, beta=w.beta, mu=w.mu)
+    sample = min(w.M, max(cores, 16))
+    prob = make_batch(w, M=sample)
+    solves = [oracle.solve_one(prob, j) for j in range(sample)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        pool.starmap(_oracle_solve, [(s, kw) for s in solves[:cores]])  # start-up
+        t0 = time.perf_counter()
+        res = pool.starmap(_oracle_solve, [(s, kw) for s in solves])
+        sec = time.perf_counter() - t0
+    return {"value": sample / sec, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {sample} of the {w.M} solves, fp64 C oracle, spawn pool",
+            "pcg_iters_per_sec": sum(r[0] for r in res) / sec}
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+
+    from trajectory_optimization_kkt_gb300 import _build, gato
+    from trajectory_optimization_kkt_gb300.workloads import WORKLOADS, make_batch
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    _build.build()
+    w = WORKLOADS[WORKLOAD_INDEX]
+    M = w.M
+    prob = make_batch(w, M=M, first_solve=rank * M) if rank else make_batch(w, M=M)
+    dev = torch.device("cuda", local)
+    d = {k: torch.from_numpy(v).to(dev) for k, v in prob.items()}
+    s = gato.Solver(M, w.N, w.n, w.m)
+    out = s.outputs(w.n_alpha)
+    p = gato.default_params(pcg_eps=w.pcg_eps, pcg_max_iters=w.pcg_max_iters,
+                            n_alpha=w.n_alpha, beta=w.beta, mu=w.mu,
+                            refine_steps=w.refine_steps, refine_eps=w.refine_eps)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    # 3 formation + 1 right-hand side + 1 PCG + 2 merit, and per refinement
+    # round 1 residual + 1 right-hand side + 1 PCG + 1 accumulate
+    launches_per_step = 7 + 4 * w.refine_steps
+
+    def step():
+        out["status"].zero_()
+        s.solve_kkt(p, d, out["dX"], out["dU"], out["lam"], out["iters"], out["merit"],
+                    out["best"], out["status"], stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- device-resident timing: per-step events, L2 flushed in between ----
+    s.set_timing(True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    pcg_us, form_us, merit_us, iters_total = [], [], [], 0
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for k in range(args.steps):
+            flush.fill_(float(k))
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+            st = s.get_stats()  # synchronises on this step's last event
+            pcg_us.append(st.pcg_us)
+            form_us.append(st.form_us)
+            merit_us.append(st.merit_us)
+            iters_total += int(out["iters"].sum())
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    s.set_timing(False)
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    status_bad = int((out["status"] != 0).sum())
+
+    # ---- end to end through the C ABI with host buffers ----
+    host = {k: torch.from_numpy(v).pin_memory() for k, v in prob.items()}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for k in range(args.steps):
+        flush.fill_(float(k))
+        e_start.record(stream)
+        for key, v in host.items():
+            d[key].copy_(v, non_blocking=True)
+        step()
+        for key, v in out.items():
+            host_out[key].copy_(v, non_blocking=True)
+        e_end.record(stream)
+        e_end.synchronize()
+        e2e_ms += e_start.elapsed_time(e_end)
+
+    # ---- max over ranks ----
+    t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = float(t[0]), float(t[1])
+    solves = M * world * args.steps
+    value = solves / (total_ms / 1000.0)
+
+    # ---- roofline of the dominant kernel (PCG) ----
+    # algorithmic bytes per solve-iteration: packed S (N n(n+1)/2 + (N-1) n^2
+    # floats) plus packed Phi^-1 (same count)
+    N, n = w.N, w.n
+    unit_bytes = 2 * (N * n * (n + 1) // 2 + (N - 1) * n * n) * 4
+    iters_per_step = iters_total / args.steps
+    pcg_mean_us = statistics.mean(pcg_us)
+    achieved = unit_bytes * iters_per_step / (pcg_mean_us * 1e-6) / 1e9
+    peak, peak_kind = _peaks()
+    sha = _src_sha(os.path.join(_build.CSRC, "pcg.cu"))
+    traffic = PCG_TRAFFIC["bytes_per_launch"] if PCG_TRAFFIC["pcg_sha"] == sha else None
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded generator, workload recipe of the benchmark configs)",
+            "config": _config(w),
+            "pcg_iters_per_sec": iters_per_step * world / (total_ms / args.steps / 1000.0),
+            "pcg_iters_per_solve": iters_per_step / M,
+            "stage_us": {"form": statistics.mean(form_us), "pcg": pcg_mean_us,
+                         "merit": statistics.mean(merit_us)},
+            "status_nonzero_solves": status_bad,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic, "kernel": "k_pcg",
+                         "peak_kind": peak_kind,
+                         "algorithmic_bytes_per_launch": unit_bytes * iters_per_step},
+            "e2e": {"value": solves / (e2e_ms / 1000.0), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = _cpu_baseline(w)
+        print(json.dumps(line), flush=True)
+    s.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gato", choices=["gato", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = _dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_gpu(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+/*
+ * gato.h -- C ABI of the GB300 (sm_103a) batched KKT solver.
+ *
+ * The solver takes a batch of M independent linear-quadratic trajectory
+ * subproblems (GATO paper, "GATO: GPU-Accelerated and Batched Trajectory
+ * Optimization for Scalable Edge Model Predictive Control", Sec. II eq. (1))
+ * and runs the data-parallel half of one SQP iteration on the GPU:
+ *
+ *   gato_form_schur   Schur complement S = C G^-1 C^T, gamma and the symmetric
+ *                     stair preconditioner Phi^-1 (Sec. II eqs. (4)-(6)),
+ *   gato_pcg_solve    batched preconditioned CG on S lambda = gamma (Sec. II)
+ *                     and recovery of dz = -G^-1 (g + C^T lambda) (eq. (4)),
+ *   gato_linesearch   the parallel line search over alpha = beta^-i with the
+ *                     L1 merit J + mu ||c||_1 (Sec. III-A),
+ *   gato_solve_kkt    all of the above, in order, on one stream,
+ *   gato_apply_step   the update Z <- Z + alpha* dZ (Sec. III-A).
+ *
+ * Problem layout (all pointers are fp32 DEVICE memory, dense row-major,
+ * solve-major then knot-major, no padding; the caller owns every buffer):
+ *   Q  [M][N][n][n]    state cost Hessians (symmetric positive definite)
+ *   R  [M][N-1][m][m]  control cost Hessians (symmetric positive definite)
+ *   q  [M][N][n]       state cost gradients
+ *   r  [M][N-1][m]     control cost gradients
+ *   A  [M][N-1][n][n]  dynamics Jacobians wrt x
+ *   B  [M][N-1][n][m]  dynamics Jacobians wrt u
+ *   e  [M][N-1][n]     defects f(x_k, u_k) - x_{k+1}
+ *   s0 [M][n]          initial-state error x_s - x_0
+ * N counts state knots x_0..x_{N-1}; there are N-1 controls.  When N == 1
+ * the [N-1] arrays are empty and their pointers may be NULL.
+ *
+ * Constraints of the QP:  dx_0 = s0,  A_k dx_k + B_k du_k + e_k = dx_{k+1}.
+ * Multipliers follow  G dz + C^T lambda = -g  with C's row for dx_0 equal to
+ * -I, so lambda_0 = Q_0 dx_0 + q_0 + A_0^T lambda_1 and so on.
+ *
+ * Streams and errors: every call is asynchronous on `stream` (a cudaStream_t
+ * passed as void*, NULL = legacy default stream) and never synchronises the
+ * device.  Return values: GATO_OK, or a negative call-level error (nothing
+ * was launched unless the error is GATO_ERR_CUDA).  Per-solve outcomes are
+ * OR-ed into the caller's device array `status[M]` (uint32, not cleared by
+ * the library: zero it before the first call); see GATO_STATUS_*.
+ * Device code never traps and every loop is bounded.
+ */
+#ifndef GATO_H
+#define GATO_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* call-level return codes */
+#define GATO_OK 0
+#define GATO_ERR_INVALID_ARG (-1)  /* NULL pointer, M/N/n/m out of range      */
+#define GATO_ERR_UNSUPPORTED (-2)  /* sizes beyond the kernels' limits         */
+#define GATO_ERR_CUDA (-3)         /* a CUDA call or kernel launch failed     */
+#define GATO_ERR_NO_MEMORY (-4)    /* workspace allocation failed             */
+
+/* per-solve status bits (device array status[M]) */
+#define GATO_STATUS_PCG_MAX_ITERS 1u      /* PCG stopped at pcg_max_iters          */
+#define GATO_STATUS_NONPOSITIVE_PIVOT 2u  /* a Cholesky pivot of Q_k, R_k or S_jj
+                                             was <= 0 or not finite: flagged, not
+                                             repaired (the pivot is replaced by 1
+                                             so that the arithmetic stays finite) */
+#define GATO_STATUS_LINESEARCH_FAILED 4u  /* no candidate beat M(0); best = -1     */
+#define GATO_STATUS_NONFINITE 8u          /* a NaN/Inf reached a PCG reduction or
+                                             a merit value                          */
+
+/* PCG stopping rules (GATO paper Sec. II: "up to tolerance eps") */
+#define GATO_STOP_RESIDUAL 0       /* ||gamma - S lambda||_2 <= eps ||gamma||_2   */
+#define GATO_STOP_PRECOND 1        /* r^T Phi^-1 r <= eps^2 (r0^T Phi^-1 r0)      */
+#define GATO_STOP_SCALED 2         /* ||r||_{D^-1} <= eps ||gamma||_{D^-1}, D the
+                                      block diagonal of S                         */
+
+/* PCG kernel selection (gato_set_pcg_kernel) */
+#define GATO_PCG_AUTO 0            /* register-tiled kernel when 7 <= n <= 16 and
+                                      N <= 128, else the generic kernel            */
+#define GATO_PCG_GENERIC 1         /* always the generic kernel                   */
+
+/* Limits of this build. */
+#define GATO_MAX_STATE 64          /* n <= 64 */
+#define GATO_MAX_CONTROL 64        /* m <= 64 */
+#define GATO_MAX_ALPHA 31          /* n_alpha <= 31 */
+
+typedef struct gato_params {
+    float pcg_eps;       /* PCG tolerance eps (default 1e-6)                     */
+    int pcg_max_iters;   /* PCG iteration cap (default 200)                       */
+    int stop_rule;       /* GATO_STOP_* (default GATO_STOP_RESIDUAL)              */
+    int refine_steps;    /* gato_solve_kkt only: rounds of iterative refinement of
+                            the KKT solution, residual in fp64 (default 0)         */
+    int n_alpha;         /* line-search candidates A (default 8)                  */
+    float beta;          /* alpha_i = beta^-i, beta > 1 (default 2)               */
+    float mu;            /* L1 penalty weight (default 10)                        */
+    int merit_threads;   /* threads per merit block, 32..256, multiple of 32
+                            (default 64); results are bit-identical at any size   */
+    float refine_eps;    /* PCG tolerance of each refinement correction; 0 means
+                            pcg_eps (default 0.1: a correction only needs a digit) */
+} gato_params;
+
+typedef struct gato_stats {
+    float form_us;       /* device time of the last call's stages (microseconds), */
+    float pcg_us;        /* filled only when timing was enabled with              */
+    float merit_us;      /* gato_set_timing; -1 for a stage that did not run      */
+    float total_us;
+} gato_stats;
+
+typedef struct gato_handle gato_handle;
+
+/* Default parameters (values above). */
+void gato_default_params(gato_params* p);
+
+/* Creates a solver for M solves of N knots, n states and m controls on the
+ * current CUDA device and allocates its device workspace (cudaMalloc; about
+ * 4 (7 n^2 + m^2 + 2 n m + 4 n + m) N M bytes).  *h receives the handle, which the
+ * caller releases with gato_destroy.  Errors: INVALID_ARG (h NULL, M, N, n or
+ * m < 1), UNSUPPORTED (n or m above the limits), NO_MEMORY, CUDA. */
+int gato_create(gato_handle** h, int M, int N, int n, int m);
+
+/* Frees the workspace and the handle (waits for nothing: the caller must make
+ * sure no call using the handle is still running). NULL is ignored. */
+void gato_destroy(gato_handle* h);
+
+/* Turns per-stage CUDA-event timing on (1) or off (0).  When on, calls record
+ * events on their stream; gato_get_stats synchronises on the last one. */
+int gato_set_timing(gato_handle* h, int on);
+
+/* Stage times of the last call (see gato_stats). */
+int gato_get_stats(gato_handle* h, gato_stats* out);
+
+/* Chooses the PCG kernel (GATO_PCG_AUTO or GATO_PCG_GENERIC) for later calls.
+ * Both give the same PCG iterates up to rounding; the generic kernel covers
+ * every supported size.  Errors: INVALID_ARG. */
+int gato_set_pcg_kernel(gato_handle* h, int kind);
+
+/* a1 + a2.  Forms, per solve and knot (GATO paper Sec. II, eqs. (4)-(6)):
+ *   S_00 = Q_0^-1, S_jj = A_{j-1} Q_{j-1}^-1 A_{j-1}^T + B_{j-1} R_{j-1}^-1 B_{j-1}^T + Q_j^-1,
+ *   S_{j,j-1} = -A_{j-1} Q_{j-1}^-1,
+ *   gamma_0 = s0 + Q_0^-1 q_0,
+ *   gamma_j = e_{j-1} - A_{j-1} Q_{j-1}^-1 q_{j-1} - B_{j-1} R_{j-1}^-1 r_{j-1} + Q_j^-1 q_j,
+ * and the symmetric stair preconditioner
+ *   Phi^-1 = D^-1 - D^-1 (L + L^T) D^-1   (D = blockdiag(S), L = S's lower blocks)
+ * in the factored form the PCG kernel uses (Cholesky factors of S_jj and the
+ * scaled coupling blocks L_j^-1 S_{j,j-1} L_{j-1}^-T).  Everything goes to
+ * the handle's workspace; inputs are read only during this call.
+ * Inputs as in the layout above; status[M] as above. */
+int gato_form_schur(gato_handle* h, const float* Q, const float* R, const float* q,
+                    const float* r, const float* A, const float* B, const float* e,
+                    const float* s0, uint32_t* status, void* stream);
+
+/* Copies the explicit blocks formed by the last gato_form_schur into caller
+ * buffers (any may be NULL): S_diag [M][N][n][n], S_off [M][N-1][n][n] (block
+ * (j, j-1) at index j-1), gamma [M][N][n], Phi_diag [M][N][n][n], Phi_off
+ * [M][N-1][n][n].  Device-to-device copies on `stream`. */
+int gato_get_schur(gato_handle* h, float* S_diag, float* S_off, float* gamma,
+                   float* Phi_diag, float* Phi_off, void* stream);
+
+/* a3 + a4.  Batched PCG on S lambda = gamma with Phi^-1 (GATO paper Sec. II),
+ * one thread block per solve, from lambda0 [M][N][n] (NULL = zero), stopping
+ * by p->stop_rule at p->pcg_eps or after p->pcg_max_iters iterations; then
+ *   dx_k = -Q_k^-1 (q_k - lambda_k + A_k^T lambda_{k+1}),
+ *   du_k = -R_k^-1 (r_k + B_k^T lambda_{k+1})            (eq. (4)).
+ * Outputs: lambda [M][N][n], dX [M][N][n], dU [M][N-1][m], iters [M] (int32).
+ * Requires a preceding gato_form_schur on the same handle (stream-ordered).
+ * p->refine_steps is ignored here (see gato_solve_kkt). */
+int gato_pcg_solve(gato_handle* h, const gato_params* p, const float* lambda0,
+                   float* lambda, float* dX, float* dU, int32_t* iters,
+                   uint32_t* status, void* stream);
+
+/* a5 + a6.  Parallel line search (GATO paper Sec. III-A): for alpha = 0 and
+ * alpha_i = beta^-i (i = 0..n_alpha-1), with x = alpha dx, u = alpha du,
+ *   M(alpha) = sum_k 1/2 x_k^T Q_k x_k + q_k^T x_k + 1/2 u_k^T R_k u_k + r_k^T u_k
+ *            + mu (||x_0 - s0||_1 + sum_k ||A_k x_k + B_k u_k + e_k - x_{k+1}||_1),
+ * one thread block per (knot, candidate), knot sums in a fixed order.
+ * merit [M][n_alpha+1]: merit[.][0] is alpha = 0, merit[.][1+i] is beta^-i.
+ * best [M]: argmin_i merit[1+i] (lowest i on ties) if it is below merit[0],
+ * else -1 with GATO_STATUS_LINESEARCH_FAILED. */
+int gato_linesearch(gato_handle* h, const gato_params* p, const float* Q, const float* R,
+                    const float* q, const float* r, const float* A, const float* B,
+                    const float* e, const float* s0, const float* dX, const float* dU,
+                    float* merit, int32_t* best, uint32_t* status, void* stream);
+
+/* gato_form_schur + gato_pcg_solve + gato_linesearch on one stream.  With
+ * p->refine_steps = k > 0 the KKT solution is refined k times: the residual of
+ * the full KKT system is formed in fp64 from the inputs, the correction is
+ * solved with the same S and Phi^-1, and added to dz and lambda; iters then
+ * counts PCG iterations over all solves of the refinement.  Each correction is
+ * solved to p->refine_eps (relative residual of the correction system). */
+int gato_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const float* R,
+                   const float* q, const float* r, const float* A, const float* B,
+                   const float* e, const float* s0, float* dX, float* dU, float* lambda,
+                   int32_t* iters, float* merit, int32_t* best, uint32_t* status,
+                   void* stream);
+
+/* The update Z <- Z + alpha* dZ (GATO paper Sec. III-A): X [M][N][n] and
+ * U [M][N-1][m] are updated in place with alpha* = beta^-best per solve;
+ * solves with best < 0 are left unchanged. */
+int gato_apply_step(gato_handle* h, const gato_params* p, const int32_t* best,
+                    const float* dX, const float* dU, float* X, float* U, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GATO_H */

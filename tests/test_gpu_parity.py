@@ -1,0 +1,385 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances
+  dz          relative L2 of the stacked dz = (dX, dU) per solve <= 1e-4 against
+              the oracle's direct fp64 solution, PCG stopped at eps = 1e-6
+  merit       |merit_gpu - merit_oracle| <= 1e-5 max|merit| per solve, the oracle
+              evaluating the GPU's own dz
+  best        identical, unless the oracle's two best candidates are within
+              1e-5 |M_best| of each other (then either of the two)
+  S, Phi, gamma  relative Frobenius error per solve <= 1e-5 (fp32 formation:
+              about 20 n u with u = 2^-24 for the sizes here)
+The workloads use their own refinement setting (one correction solved to
+0.1, or 0.01 for workload 3): in fp32 the formation of S alone moves dz by
+4e-5 to 1.3e-4 (up to 3e-3 for workload 3), so the unrefined solve sits at
+the tolerance; refinement brings it near 1e-5.  A test below also checks
+the unrefined solve of workload 4.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+from trajectory_optimization_kkt_gb300 import gato  # noqa: E402
+from trajectory_optimization_kkt_gb300.workloads import WORKLOADS, make_batch, random_lq  # noqa: E402
+
+TOL_DZ = 1e-4
+TOL_MERIT = 1e-5
+TOL_FORM = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def rel(a, b):
+    a, b = np.ravel(a), np.ravel(b)
+    return np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300)
+
+
+def params_for(w, **kw):
+    p = dict(pcg_eps=w.pcg_eps, pcg_max_iters=w.pcg_max_iters, n_alpha=w.n_alpha,
+             beta=w.beta, mu=w.mu, refine_steps=w.refine_steps, refine_eps=w.refine_eps)
+    p.update(kw)
+    return gato.default_params(**p)
+
+
+def solve(prob, params, kernel=gato.GATO_PCG_AUTO):
+    M, N, n = prob["Q"].shape[:3]
+    m = prob["B"].shape[-1]
+    d = gato.to_device(prob)
+    with gato.Solver(M, N, n, m) as s:
+        s.set_pcg_kernel(kernel)
+        out = s.outputs(params.n_alpha)
+        s.solve_kkt(params, d, out["dX"], out["dU"], out["lam"], out["iters"], out["merit"],
+                    out["best"], out["status"])
+        torch.cuda.synchronize()
+        return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def check_solution(prob, out, solves, n_alpha=8, beta=2.0, mu=10.0, tol_dz=TOL_DZ):
+    for j in solves:
+        pj = oracle.solve_one(prob, j)
+        dX, dU, lam = oracle.direct_solve(pj)
+        z = np.concatenate([out["dX"][j].ravel(), out["dU"][j].ravel()])
+        zr = np.concatenate([dX.ravel(), dU.ravel()])
+        assert rel(z, zr) <= tol_dz, (j, rel(z, zr))
+        check_merit(pj, out["dX"][j], out["dU"][j], out["merit"][j], out["best"][j],
+                    n_alpha, beta, mu)
+
+
+def check_merit(pj, dX, dU, merit, best, n_alpha, beta, mu):
+    ref, ref_best = oracle.linesearch(pj, dX, dU, n_alpha, beta, mu)
+    scale = np.abs(ref).max()
+    assert np.abs(merit - ref).max() <= TOL_MERIT * scale, (merit, ref)
+    cand = ref[1:]
+    order = np.argsort(cand, kind="stable")
+    gap = cand[order[1]] - cand[order[0]] if len(cand) > 1 else np.inf
+    if ref_best >= 0 and gap > TOL_MERIT * abs(cand[order[0]]):
+        assert int(best) == ref_best
+    elif ref_best >= 0:
+        assert int(best) in (int(order[0]), int(order[1]))
+
+
+# --------------------------------------------------------------------------
+# formation (a1, a2)
+# --------------------------------------------------------------------------
+
+def form(prob):
+    M, N, n = prob["Q"].shape[:3]
+    m = prob["B"].shape[-1]
+    d = gato.to_device(prob)
+    f = dict(device="cuda", dtype=torch.float32)
+    out = dict(D=torch.empty(M, N, n, n, **f), O=torch.empty(M, max(N - 1, 0), n, n, **f),
+               g=torch.empty(M, N, n, **f), Pd=torch.empty(M, N, n, n, **f),
+               Po=torch.empty(M, max(N - 1, 0), n, n, **f))
+    status = torch.zeros(M, dtype=torch.int32, device="cuda")
+    with gato.Solver(M, N, n, m) as s:
+        s.form_schur(d, status)
+        s.get_schur(out["D"], out["O"] if N > 1 else None, out["g"], out["Pd"],
+                    out["Po"] if N > 1 else None)
+        torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}, status.cpu().numpy()
+
+
+FORM_CASES = [(w.name, make_batch(w, M=min(w.M, 6))) for w in WORKLOADS] + [
+    ("ragged_N37_n13_m5", random_lq(3, 37, 13, 5, seed=501)),
+    ("N1_n14", random_lq(2, 1, 14, 7, seed=502)),
+    ("n3_m2", random_lq(2, 11, 3, 2, seed=503)),
+    ("n64_m64", random_lq(1, 4, 64, 64, seed=504)),
+]
+
+
+@pytest.mark.parametrize("name,prob", FORM_CASES, ids=[c[0] for c in FORM_CASES])
+def test_form_schur_matches_oracle(name, prob):
+    got, status = form(prob)
+    assert not status.any()
+    N = prob["Q"].shape[1]
+    for j in range(prob["Q"].shape[0]):
+        D, O, g, rc = oracle.schur(oracle.solve_one(prob, j))
+        Pd, Po, rc2 = oracle.stair(D, O)
+        assert rc == 0 and rc2 == 0
+        refs = dict(D=D, g=g, Pd=Pd)
+        if N > 1:
+            refs.update(O=O, Po=Po)
+        for k, ref in refs.items():
+            assert rel(got[k][j], ref) <= TOL_FORM, (name, j, k, rel(got[k][j], ref))
+
+
+# --------------------------------------------------------------------------
+# whole path (a1..a6) on the five workloads (subsets) and ragged sizes
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("w", WORKLOADS, ids=lambda w: w.name)
+def test_solve_kkt_matches_oracle(w):
+    M = min(w.M, 8)
+    prob = make_batch(w, M=M)
+    out = solve(prob, params_for(w))
+    # workloads 0 and 2 state their caps (200, 500), which fp32 PCG can reach
+    assert not (out["status"] & ~gato.GATO_STATUS_PCG_MAX_ITERS).any(), out["status"]
+    if w.index not in (0, 2):
+        assert not out["status"].any()
+    check_solution(prob, out, range(M), w.n_alpha, w.beta, w.mu)
+
+
+def test_unrefined_solve_of_workload4():
+    w = WORKLOADS[4]
+    prob = make_batch(w, M=8)
+    out = solve(prob, params_for(w, refine_steps=0))
+    assert not out["status"].any()
+    check_solution(prob, out, range(8), w.n_alpha, w.beta, w.mu)
+
+
+CUSTOM = [
+    ("ragged_N37_n13_m5", 3, 37, 13, 5, 1),
+    ("N1_n14_m7", 2, 1, 14, 7, 0),
+    ("N2_n7_m3", 3, 2, 7, 3, 0),
+    ("N9_n16_m8", 2, 9, 16, 8, 1),
+    ("N11_n3_m2_generic", 2, 11, 3, 2, 1),
+    ("N6_n40_m12_generic", 2, 6, 40, 12, 1),
+    ("N130_n14_m7_generic", 1, 130, 14, 7, 1),
+    ("N128_n12_m6_tile", 2, 128, 12, 6, 1),
+]
+
+
+@pytest.mark.parametrize("name,M,N,n,m,refine", CUSTOM, ids=[c[0] for c in CUSTOM])
+def test_solve_kkt_custom_sizes(name, M, N, n, m, refine):
+    prob = random_lq(M, N, n, m, seed=600 + N + n)
+    p = gato.default_params(pcg_max_iters=3000, refine_steps=refine)
+    out = solve(prob, p)
+    assert not out["status"].any(), out["status"]
+    check_solution(prob, out, range(M))
+
+
+@pytest.mark.parametrize("w", [WORKLOADS[1], WORKLOADS[4]], ids=lambda w: w.name)
+def test_tile_and_generic_kernels_agree(w):
+    prob = make_batch(w, M=4)
+    a = solve(prob, params_for(w), gato.GATO_PCG_AUTO)
+    b = solve(prob, params_for(w), gato.GATO_PCG_GENERIC)
+    assert np.abs(a["iters"] - b["iters"]).max() <= 0.05 * b["iters"].max() + 2
+    for j in range(4):
+        assert rel(a["dX"][j], b["dX"][j]) < 1e-3
+    check_solution(prob, b, range(4), w.n_alpha, w.beta, w.mu)
+
+
+@pytest.mark.parametrize("rule", [gato.GATO_STOP_PRECOND, gato.GATO_STOP_SCALED])
+def test_other_stop_rules(rule):
+    w = WORKLOADS[1]
+    prob = make_batch(w, M=3)
+    out = solve(prob, params_for(w, stop_rule=rule, refine_steps=1))
+    assert not out["status"].any()
+    check_solution(prob, out, range(3), w.n_alpha, w.beta, w.mu)
+    for j in range(3):
+        D, O, g, _ = oracle.schur(oracle.solve_one(prob, j))
+        Pd, Po, _ = oracle.stair(D, O)
+        _, it, ok = oracle.pcg(D, O, Pd, Po, g, w.pcg_eps, 5000, stop_rule=rule)
+        # the same stopping quantity: fp32 iterations of the first solve track
+        # the fp64 count (the refinement adds a short second solve)
+        assert ok and it * 0.9 - 3 <= int(out["iters"][j]) <= it * 1.2 + 150
+
+
+# --------------------------------------------------------------------------
+# full sizes, launch configuration of the benchmark, sampled solves
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("w", [WORKLOADS[2], WORKLOADS[3], WORKLOADS[4]], ids=lambda w: w.name)
+def test_full_size_sampled(w):
+    prob = make_batch(w)
+    out = solve(prob, params_for(w))
+    if w.index == 2:  # stated cap of 500 iterations
+        assert not (out["status"] & ~gato.GATO_STATUS_PCG_MAX_ITERS).any()
+    else:
+        assert not out["status"].any(), np.nonzero(out["status"])
+    samples = sorted(set(np.linspace(0, w.M - 1, 12).astype(int).tolist()))
+    check_solution(prob, out, samples, w.n_alpha, w.beta, w.mu)
+    assert (out["best"] >= 0).all()
+
+
+# --------------------------------------------------------------------------
+# invariance gates
+# --------------------------------------------------------------------------
+
+def test_merit_bit_identical_across_block_sizes():
+    w = WORKLOADS[1]
+    prob = make_batch(w, M=4)
+    ref = None
+    for mt in (32, 64, 128, 256):
+        out = solve(prob, params_for(w, merit_threads=mt))
+        if ref is None:
+            ref = out
+        assert np.array_equal(out["merit"], ref["merit"])
+        assert np.array_equal(out["best"], ref["best"])
+
+
+def test_deterministic_and_batch_position_invariant():
+    w = WORKLOADS[4]
+    prob = make_batch(w, M=6)
+    a = solve(prob, params_for(w))
+    b = solve(prob, params_for(w))
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+    one = solve({k: v[3:4] for k, v in prob.items()}, params_for(w))
+    for k in ("dX", "dU", "lam", "merit", "best", "iters"):
+        assert np.array_equal(one[k][0], a[k][3]), k
+
+
+def test_separate_entry_points_equal_solve_kkt():
+    w = WORKLOADS[1]
+    prob = make_batch(w, M=3)
+    p = params_for(w, refine_steps=0)
+    full = solve(prob, p)
+    d = gato.to_device(prob)
+    with gato.Solver(3, w.N, w.n, w.m) as s:
+        o = s.outputs(p.n_alpha)
+        s.form_schur(d, o["status"])
+        s.pcg_solve(p, o["lam"], o["dX"], o["dU"], o["iters"], o["status"])
+        s.linesearch(p, d, o["dX"], o["dU"], o["merit"], o["best"], o["status"])
+        torch.cuda.synchronize()
+        for k in ("dX", "dU", "lam", "merit", "best", "iters", "status"):
+            assert np.array_equal(o[k].cpu().numpy(), full[k]), k
+
+
+# --------------------------------------------------------------------------
+# line search on given steps, update, warm start
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("scale", [2.5, 6.0, -1.0])
+def test_linesearch_on_scaled_steps(scale):
+    w = WORKLOADS[1]
+    prob = make_batch(w, M=4)
+    d = gato.to_device(prob)
+    dX = np.stack([oracle.direct_solve(oracle.solve_one(prob, j))[0] for j in range(4)])
+    dU = np.stack([oracle.direct_solve(oracle.solve_one(prob, j))[1] for j in range(4)])
+    dXt = torch.tensor(scale * dX, dtype=torch.float32, device="cuda")
+    dUt = torch.tensor(scale * dU, dtype=torch.float32, device="cuda")
+    p = params_for(w)
+    with gato.Solver(4, w.N, w.n, w.m) as s:
+        o = s.outputs(p.n_alpha)
+        s.linesearch(p, d, dXt, dUt, o["merit"], o["best"], o["status"])
+        torch.cuda.synchronize()
+        merit, best, status = (o[k].cpu().numpy() for k in ("merit", "best", "status"))
+    for j in range(4):
+        pj = oracle.solve_one(prob, j)
+        check_merit(pj, dXt[j].cpu().numpy(), dUt[j].cpu().numpy(), merit[j], best[j],
+                    p.n_alpha, p.beta, p.mu)
+        if scale < 0:
+            assert best[j] == -1 and status[j] & gato.GATO_STATUS_LINESEARCH_FAILED
+        else:
+            assert best[j] > 0 and status[j] == 0
+
+
+def test_apply_step():
+    w = WORKLOADS[1]
+    prob = make_batch(w, M=3)
+    out = solve(prob, params_for(w))
+    X0 = np.random.default_rng(1).standard_normal(out["dX"].shape).astype(np.float32)
+    U0 = np.random.default_rng(2).standard_normal(out["dU"].shape).astype(np.float32)
+    best = np.array([0, 2, -1], dtype=np.int32)
+    X, U = torch.tensor(X0, device="cuda"), torch.tensor(U0, device="cuda")
+    p = params_for(w)
+    with gato.Solver(3, w.N, w.n, w.m) as s:
+        s.apply_step(p, torch.tensor(best, device="cuda"), torch.tensor(out["dX"], device="cuda"),
+                     torch.tensor(out["dU"], device="cuda"), X, U)
+        torch.cuda.synchronize()
+    alpha = np.array([1.0, 0.25, 0.0], dtype=np.float32)
+    np.testing.assert_array_equal(X.cpu().numpy(), X0 + alpha[:, None, None] * out["dX"])
+    np.testing.assert_array_equal(U.cpu().numpy(), U0 + alpha[:, None, None] * out["dU"])
+
+
+def test_warm_start_at_solution_needs_no_iterations():
+    w = WORKLOADS[1]
+    prob = make_batch(w, M=2)
+    lam = np.stack([oracle.direct_solve(oracle.solve_one(prob, j))[2] for j in range(2)])
+    d = gato.to_device(prob)
+    p = params_for(w, pcg_eps=1e-3)
+    with gato.Solver(2, w.N, w.n, w.m) as s:
+        o = s.outputs(p.n_alpha)
+        s.form_schur(d, o["status"])
+        s.pcg_solve(p, o["lam"], o["dX"], o["dU"], o["iters"], o["status"],
+                    lambda0=torch.tensor(lam, dtype=torch.float32, device="cuda"))
+        torch.cuda.synchronize()
+        assert (o["iters"].cpu().numpy() == 0).all()
+        for j in range(2):
+            assert rel(o["lam"][j].cpu().numpy(), lam[j]) < 1e-4
+
+
+# --------------------------------------------------------------------------
+# failure detection (host-made faults; flags, never traps)
+# --------------------------------------------------------------------------
+
+def test_iteration_cap_is_flagged():
+    w = WORKLOADS[1]
+    prob = make_batch(w, M=2)
+    out = solve(prob, params_for(w, pcg_max_iters=5, refine_steps=0))
+    assert (out["iters"] == 5).all()
+    assert (out["status"] & gato.GATO_STATUS_PCG_MAX_ITERS).all()
+
+
+def test_indefinite_Q_is_flagged():
+    w = WORKLOADS[0]
+    prob = make_batch(w, M=2)
+    prob["Q"] = prob["Q"].copy()
+    prob["Q"][1, 3] = -np.eye(w.n, dtype=np.float32)
+    out = solve(prob, params_for(w, pcg_max_iters=50))
+    assert out["status"][1] & gato.GATO_STATUS_NONPOSITIVE_PIVOT
+    assert not out["status"][0] & gato.GATO_STATUS_NONPOSITIVE_PIVOT
+
+
+def test_nan_input_is_flagged():
+    w = WORKLOADS[0]
+    prob = make_batch(w, M=2)
+    prob["q"] = prob["q"].copy()
+    prob["q"][0, 2, 1] = np.nan
+    out = solve(prob, params_for(w, pcg_max_iters=50))
+    assert out["status"][0] & gato.GATO_STATUS_NONFINITE
+    assert not out["status"][1] & gato.GATO_STATUS_NONFINITE
+
+
+def test_invalid_parameters_rejected():
+    w = WORKLOADS[0]
+    prob = make_batch(w, M=1)
+    for bad in (dict(merit_threads=48), dict(n_alpha=0), dict(beta=1.0), dict(stop_rule=7),
+                dict(pcg_max_iters=-1)):
+        with pytest.raises(gato.GatoError) as e:
+            solve(prob, params_for(w, **bad))
+        assert e.value.code == gato.GATO_ERR_INVALID_ARG
+
+
+def test_stage_timing():
+    w = WORKLOADS[1]
+    prob = make_batch(w, M=4)
+    d = gato.to_device(prob)
+    p = params_for(w)
+    with gato.Solver(4, w.N, w.n, w.m) as s:
+        o = s.outputs(p.n_alpha)
+        s.set_timing(True)
+        s.solve_kkt(p, d, o["dX"], o["dU"], o["lam"], o["iters"], o["merit"], o["best"], o["status"])
+        st = s.get_stats()
+    assert st.form_us > 0 and st.pcg_us > 0 and st.merit_us > 0
+    assert st.total_us >= st.pcg_us

@@ -1,0 +1,233 @@
+// form_schur.cu -- Schur complement S, gamma and the symmetric stair
+// preconditioner (GATO paper, Sec. II eqs. (4)-(6); Sec. III: block-local
+// formation with one grid-wide synchronisation before Phi^-1 is final).
+//
+// One warp per knot; each warp keeps its knot's small matrices in its own
+// slice of shared memory.  Three launches, whose boundaries are the grid-wide
+// synchronisations the block-local formation needs:
+//   k_form_inv   knot k:  Q_k^-1, R_k^-1, S_{k+1,k} = -A_k Q_k^-1, V_k = B_k R_k^-1
+//   k_form_diag  row j:   S_jj = Q_j^-1 + A_{j-1} Q_{j-1}^-1 A_{j-1}^T + V_{j-1} B_{j-1}^T,
+//                         its Cholesky factor L_j, L_j^-1, S_jj^-1 and the
+//                         eigenvalue bound 1 / ||L_j^-1||_F^2
+//   k_form_off   row j:   Nhat_j = L_j^-1 S_{j,j-1} L_{j-1}^-T and the explicit
+//                         Phi^-1 block -S_jj^-1 S_{j,j-1} S_{j-1,j-1}^-1
+// and a fourth for the right-hand side (also used by iterative refinement):
+//   k_form_rhs   row j:   gamma_j, L_j^-1 gamma_j, -Q_j^-1 q_j, -R_j^-1 r_j
+#include "gato_internal.cuh"
+
+namespace gato {
+namespace {
+
+__global__ void k_form_inv(Work w, const float* __restrict__ Q, const float* __restrict__ R,
+                           const float* __restrict__ A, const float* __restrict__ B,
+                           uint32_t* status)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int n = w.n, m = w.m, N = w.N;
+    const int nn = n * n, mm = m * m, nm = n * m;
+    const int warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+    const long g = (long)blockIdx.x * wpb + warp;
+    if (g >= (long)w.M * N) return;
+    const int sol = (int)(g / N), k = (int)(g % N);
+    float* sQ = sm + (size_t)warp * (3 * nn + 3 * mm + nm);
+    float* sT = sQ + nn;
+    float* sQi = sT + nn;
+    float* sR = sQi + nn;
+    float* sRt = sR + mm;
+    float* sRi = sRt + mm;
+    float* sB = sRi + mm;
+
+    warp_copy(sQ, Q + ((size_t)sol * N + k) * nn, nn);
+    bool ok = warp_cholesky(sQ, n);
+    warp_lower_inverse(sQ, sT, n);
+    warp_gram_lower(sT, sQi, n);
+    warp_copy(w.Qinv + sol * w.sNnn + (size_t)k * nn, sQi, nn);
+    if (k < N - 1) {
+        const size_t K = (size_t)(N - 1);
+        warp_copy(sR, R + ((size_t)sol * K + k) * mm, mm);
+        ok = warp_cholesky(sR, m) && ok;
+        warp_lower_inverse(sR, sRt, m);
+        warp_gram_lower(sRt, sRi, m);
+        warp_copy(w.Rinv + sol * w.sKmm + (size_t)k * mm, sRi, mm);
+        warp_copy(sQ, A + ((size_t)sol * K + k) * nn, nn);  // sQ now holds A_k
+        warp_copy(sB, B + ((size_t)sol * K + k) * nm, nm);
+        __syncwarp();
+        warp_gemm<false, false>(n, n, n, sQ, sQi, w.O + sol * w.sKnn + (size_t)k * nn, -1.f, false);
+        warp_gemm<false, false>(n, m, m, sB, sRi, w.V + sol * w.sKnm + (size_t)k * nm, 1.f, false);
+    }
+    if (!ok && lane_id() == 0) atomicOr(status + sol, GATO_STATUS_NONPOSITIVE_PIVOT);
+}
+
+__global__ void k_form_diag(Work w, const float* __restrict__ A, const float* __restrict__ B,
+                            uint32_t* status)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int n = w.n, m = w.m, N = w.N;
+    const int nn = n * n, nm = n * m;
+    const int warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+    const long g = (long)blockIdx.x * wpb + warp;
+    if (g >= (long)w.M * N) return;
+    const int sol = (int)(g / N), j = (int)(g % N);
+    float* sD = sm + (size_t)warp * (4 * nn + 2 * nm);
+    float* sO = sD + nn;
+    float* sA = sO + nn;
+    float* sL = sA + nn;
+    float* sV = sL + nn;
+    float* sB = sV + nm;
+
+    warp_copy(sD, w.Qinv + sol * w.sNnn + (size_t)j * nn, nn);
+    if (j > 0) {
+        const size_t K = (size_t)(N - 1);
+        warp_copy(sO, w.O + sol * w.sKnn + (size_t)(j - 1) * nn, nn);
+        warp_copy(sA, A + ((size_t)sol * K + (j - 1)) * nn, nn);
+        warp_copy(sV, w.V + sol * w.sKnm + (size_t)(j - 1) * nm, nm);
+        warp_copy(sB, B + ((size_t)sol * K + (j - 1)) * nm, nm);
+        __syncwarp();
+        // theta: A Q^-1 A^T = -S_{j,j-1} A^T, plus B R^-1 B^T = V B^T
+        warp_gemm<false, true>(n, n, n, sO, sA, sD, -1.f, true);
+        warp_gemm<false, true>(n, n, m, sV, sB, sD, 1.f, true);
+    }
+    __syncwarp();
+    const size_t off = sol * w.sNnn + (size_t)j * nn;
+    warp_copy(w.D + off, sD, nn);
+    warp_copy(sL, sD, nn);
+    const bool ok = warp_cholesky(sL, n);
+    warp_copy(w.L + off, sL, nn);
+    warp_lower_inverse(sL, sA, n);
+    warp_copy(w.Linv + off, sA, nn);
+    {
+        // ||L_j^-1||_F^2 = trace(S_jj^-1) >= 1 / lambda_min(S_jj)
+        float f = 0.f;
+        for (int t = lane_id(); t < nn; t += 32) f += sA[t] * sA[t];
+        f = warp_sum(f);
+        if (lane_id() == 0) w.dlow[sol * w.sN + j] = 1.f / f;
+    }
+    warp_gram_lower(sA, sO, n);
+    warp_copy(w.Pd + off, sO, nn);
+    if (!ok && lane_id() == 0) atomicOr(status + sol, GATO_STATUS_NONPOSITIVE_PIVOT);
+}
+
+__global__ void k_form_off(Work w)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int n = w.n, N = w.N, K = N - 1;
+    const int nn = n * n;
+    const int warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+    const long g = (long)blockIdx.x * wpb + warp;
+    if (K < 1 || g >= (long)w.M * K) return;
+    const int sol = (int)(g / K), j = 1 + (int)(g % K);
+    float* s1 = sm + (size_t)warp * 4 * nn;
+    float* s2 = s1 + nn;
+    float* s3 = s2 + nn;
+    float* s4 = s3 + nn;
+    const size_t dj = sol * w.sNnn + (size_t)j * nn, dp = dj - nn;
+    const size_t oj = sol * w.sKnn + (size_t)(j - 1) * nn;
+
+    warp_copy(s1, w.Linv + dj, nn);
+    warp_copy(s2, w.O + oj, nn);
+    warp_copy(s3, w.Linv + dp, nn);
+    __syncwarp();
+    warp_gemm<false, false>(n, n, n, s1, s2, s4, 1.f, false);
+    warp_gemm<false, true>(n, n, n, s4, s3, w.Nh + oj, 1.f, false);
+    warp_copy(s1, w.Pd + dj, nn);
+    warp_copy(s3, w.Pd + dp, nn);
+    __syncwarp();
+    warp_gemm<false, false>(n, n, n, s1, s2, s4, 1.f, false);
+    warp_gemm<false, false>(n, n, n, s4, s3, w.Po + oj, -1.f, false);
+}
+
+// Right-hand side for (q, r, e, s0); s0 of solve i starts at s0 + i * s0_stride.
+__global__ void k_form_rhs(Work w, Rhs out, const float* __restrict__ q,
+                           const float* __restrict__ r, const float* __restrict__ e,
+                           const float* __restrict__ s0, size_t s0_stride)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int n = w.n, m = w.m, N = w.N;
+    const int nn = n * n;
+    const int warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+    const long g = (long)blockIdx.x * wpb + warp;
+    if (g >= (long)w.M * N) return;
+    const int sol = (int)(g / N), j = (int)(g % N);
+    const size_t K = (size_t)(N - 1);
+    float* sg = sm + (size_t)warp * n;
+    const float* Qi = w.Qinv + sol * w.sNnn + (size_t)j * nn;
+    const float* qj = q + ((size_t)sol * N + j) * n;
+
+    if (j == 0) {
+        warp_copy(sg, s0 + sol * s0_stride, n);
+        __syncwarp();
+        warp_gemv<false>(n, n, Qi, qj, sg, 1.f, true);
+    } else {
+        warp_copy(sg, e + ((size_t)sol * K + (j - 1)) * n, n);
+        __syncwarp();
+        warp_gemv<false>(n, n, w.O + sol * w.sKnn + (size_t)(j - 1) * nn,
+                         q + ((size_t)sol * N + (j - 1)) * n, sg, 1.f, true);
+        warp_gemv<false>(n, m, w.V + sol * w.sKnm + (size_t)(j - 1) * n * m,
+                         r + ((size_t)sol * K + (j - 1)) * m, sg, -1.f, true);
+        warp_gemv<false>(n, n, Qi, qj, sg, 1.f, true);
+    }
+    warp_copy(out.gamma + sol * w.sNn + (size_t)j * n, sg, n);
+    warp_gemv<false>(n, n, w.Linv + sol * w.sNnn + (size_t)j * nn, sg,
+                     out.ghat + sol * w.sNn + (size_t)j * n, 1.f, false);
+    warp_gemv<false>(n, n, Qi, qj, out.avec + sol * w.sNn + (size_t)j * n, -1.f, false);
+    if (j < N - 1)
+        warp_gemv<false>(m, m, w.Rinv + sol * w.sKmm + (size_t)j * m * m,
+                         r + ((size_t)sol * K + j) * m, out.bvec + sol * w.sKm + (size_t)j * m,
+                         -1.f, false);
+}
+
+// warps per block so that the per-warp slices fit in `budget` bytes
+int warps_for(size_t per_warp_bytes, size_t budget)
+{
+    size_t w = per_warp_bytes ? budget / per_warp_bytes : 8;
+    if (w > 8) w = 8;
+    if (w < 1) w = 1;
+    return (int)w;
+}
+
+template <typename K, typename... Args>
+cudaError_t launch_warp_per_item(K kernel, long items, size_t per_warp_bytes,
+                                 const gato_handle* h, cudaStream_t st, Args... args)
+{
+    if (items <= 0) return cudaSuccess;
+    const int wpb = warps_for(per_warp_bytes, 48 * 1024);
+    const size_t smem = (size_t)wpb * per_warp_bytes;
+    if (smem > (size_t)h->smem_optin) return cudaErrorInvalidConfiguration;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    const long blocks = (items + wpb - 1) / wpb;
+    kernel<<<(unsigned)blocks, wpb * 32, smem, st>>>(args...);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_form_matrices(gato_handle* h, const float* Q, const float* R,
+                                 const float* A, const float* B, uint32_t* status,
+                                 cudaStream_t st)
+{
+    const Work& w = h->w;
+    const size_t n = w.n, m = w.m, f = sizeof(float);
+    const long knots = (long)w.M * w.N;
+    cudaError_t e;
+    e = launch_warp_per_item(k_form_inv, knots, (3 * n * n + 3 * m * m + n * m) * f, h, st,
+                             w, Q, R, A, B, status);
+    if (e != cudaSuccess) return e;
+    e = launch_warp_per_item(k_form_diag, knots, (4 * n * n + 2 * n * m) * f, h, st, w, A, B,
+                             status);
+    if (e != cudaSuccess) return e;
+    return launch_warp_per_item(k_form_off, (long)w.M * (w.N - 1), 4 * n * n * f, h, st, w);
+}
+
+cudaError_t launch_form_rhs(gato_handle* h, int set, const float* q, const float* r,
+                            const float* e, const float* s0, size_t s0_stride, cudaStream_t st)
+{
+    const Work& w = h->w;
+    return launch_warp_per_item(k_form_rhs, (long)w.M * w.N, (size_t)w.n * sizeof(float), h,
+                                st, w, w.rhs[set], q, r, e, s0, s0_stride);
+}
+
+}  // namespace gato

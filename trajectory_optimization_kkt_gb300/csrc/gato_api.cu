@@ -1,0 +1,302 @@
+// gato_api.cu -- the extern "C" entry points declared in include/gato.h:
+// argument checks, the workspace allocation, stage ordering on the caller's
+// stream and the optional per-stage CUDA-event timing.
+#include <stdlib.h>
+#include <string.h>
+
+#include "gato_internal.cuh"
+
+using gato::Work;
+
+namespace {
+
+size_t round64(size_t x)
+{
+    const size_t r = (x + 63) / 64 * 64;
+    return r ? r : 64;
+}
+
+int cuda_fail(cudaError_t e) { return e == cudaSuccess ? GATO_OK : GATO_ERR_CUDA; }
+
+bool params_ok(const gato_params* p)
+{
+    if (!p) return false;
+    if (!(p->pcg_eps >= 0.f) || p->pcg_max_iters < 0) return false;
+    if (p->stop_rule < GATO_STOP_RESIDUAL || p->stop_rule > GATO_STOP_SCALED) return false;
+    if (p->refine_steps < 0 || p->refine_steps > 16) return false;
+    if (p->n_alpha < 1 || p->n_alpha > GATO_MAX_ALPHA) return false;
+    if (!(p->beta > 1.f) || !(p->mu >= 0.f)) return false;
+    if (p->merit_threads < 32 || p->merit_threads > 256 || p->merit_threads % 32) return false;
+    if (!(p->refine_eps >= 0.f)) return false;
+    return true;
+}
+
+// the [N-1] arrays may be NULL only when N == 1
+bool lq_ok(const gato_handle* h, const float* Q, const float* R, const float* q,
+           const float* r, const float* A, const float* B, const float* e, const float* s0)
+{
+    if (!Q || !q || !s0) return false;
+    if (h->w.N > 1 && (!R || !r || !A || !B || !e)) return false;
+    return true;
+}
+
+void record(gato_handle* h, int i, cudaStream_t st)
+{
+    if (!h->timing) return;
+    cudaEventRecord(h->ev[i], st);
+    h->ev_used[i] = 1;
+}
+
+void begin_timing(gato_handle* h, cudaStream_t st)
+{
+    if (!h->timing) return;
+    for (int i = 0; i < 5; ++i) h->ev_used[i] = 0;
+    record(h, 0, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+void gato_default_params(gato_params* p)
+{
+    if (!p) return;
+    p->pcg_eps = 1e-6f;
+    p->pcg_max_iters = 200;
+    p->stop_rule = GATO_STOP_RESIDUAL;
+    p->refine_steps = 0;
+    p->n_alpha = 8;
+    p->beta = 2.f;
+    p->mu = 10.f;
+    p->merit_threads = 64;
+    p->refine_eps = 0.1f;
+}
+
+int gato_create(gato_handle** out, int M, int N, int n, int m)
+{
+    if (!out) return GATO_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (M < 1 || N < 1 || n < 1 || m < 1) return GATO_ERR_INVALID_ARG;
+    if (n > GATO_MAX_STATE || m > GATO_MAX_CONTROL) return GATO_ERR_UNSUPPORTED;
+    gato_handle* h = (gato_handle*)calloc(1, sizeof(gato_handle));
+    if (!h) return GATO_ERR_NO_MEMORY;
+    if (cudaGetDevice(&h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                               h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) !=
+            cudaSuccess) {
+        free(h);
+        return GATO_ERR_CUDA;
+    }
+    Work& w = h->w;
+    w.M = M; w.N = N; w.n = n; w.m = m;
+    const size_t K = (size_t)(N - 1);
+    w.sNnn = round64((size_t)N * n * n);
+    w.sKnn = round64(K * n * n);
+    w.sKmm = round64(K * m * m);
+    w.sKnm = round64(K * n * m);
+    w.sNn = round64((size_t)N * n);
+    w.sN = round64((size_t)N);
+    w.sKm = round64(K * m);
+    w.sK2 = (size_t)N * (GATO_MAX_ALPHA + 1);  // float2 units
+    // carve one allocation: (count of per-solve floats) x M
+    float** fields[] = {&w.Qinv, &w.Rinv, &w.O, &w.V, &w.D, &w.L, &w.Linv, &w.Pd, &w.Po, &w.Nh,
+                        &w.dlow,
+                        &w.rhs[0].gamma, &w.rhs[0].ghat, &w.rhs[0].avec, &w.rhs[0].bvec,
+                        &w.rhs[1].gamma, &w.rhs[1].ghat, &w.rhs[1].avec, &w.rhs[1].bvec,
+                        &w.q2, &w.r2, &w.e2, &w.s02, &w.dlam, &w.ddX, &w.ddU};
+    const size_t strides[] = {w.sNnn, w.sKmm, w.sKnn, w.sKnm, w.sNnn, w.sNnn, w.sNnn,
+                              w.sNnn, w.sKnn, w.sKnn, w.sN, w.sNn, w.sNn, w.sNn, w.sKm,
+                              w.sNn, w.sNn, w.sNn, w.sKm,
+                              w.sNn, w.sKm, w.sNn, w.sNn, w.sNn, w.sNn, w.sKm};
+    const int nf = (int)(sizeof(strides) / sizeof(strides[0]));
+    size_t total = 0;
+    for (int i = 0; i < nf; ++i) total += strides[i] * (size_t)M;
+    total += 2 * w.sK2 * (size_t)M;  // merit partials
+    h->bytes = total * sizeof(float);
+    if (cudaMalloc(&h->base, h->bytes) != cudaSuccess) {
+        cudaGetLastError();
+        free(h);
+        return GATO_ERR_NO_MEMORY;
+    }
+    float* cur = (float*)h->base;
+    for (int i = 0; i < nf; ++i) {
+        *fields[i] = cur;
+        cur += strides[i] * (size_t)M;
+    }
+    w.mpart = (float2*)cur;
+    for (int i = 0; i < 5; ++i) {
+        if (cudaEventCreate(&h->ev[i]) != cudaSuccess) {
+            for (int j = 0; j < i; ++j) cudaEventDestroy(h->ev[j]);
+            cudaFree(h->base);
+            free(h);
+            return GATO_ERR_CUDA;
+        }
+    }
+    h->last.form_us = h->last.pcg_us = h->last.merit_us = h->last.total_us = -1.f;
+    *out = h;
+    return GATO_OK;
+}
+
+void gato_destroy(gato_handle* h)
+{
+    if (!h) return;
+    for (int i = 0; i < 5; ++i) cudaEventDestroy(h->ev[i]);
+    cudaFree(h->base);
+    free(h);
+}
+
+int gato_set_timing(gato_handle* h, int on)
+{
+    if (!h) return GATO_ERR_INVALID_ARG;
+    h->timing = on ? 1 : 0;
+    return GATO_OK;
+}
+
+int gato_set_pcg_kernel(gato_handle* h, int kind)
+{
+    if (!h || (kind != GATO_PCG_AUTO && kind != GATO_PCG_GENERIC)) return GATO_ERR_INVALID_ARG;
+    h->force_generic_pcg = kind == GATO_PCG_GENERIC;
+    return GATO_OK;
+}
+
+int gato_get_stats(gato_handle* h, gato_stats* out)
+{
+    if (!h || !out) return GATO_ERR_INVALID_ARG;
+    gato_stats s;
+    s.form_us = s.pcg_us = s.merit_us = s.total_us = -1.f;
+    if (h->timing && h->ev_used[0]) {
+        int last = 0;
+        for (int i = 4; i > 0; --i)
+            if (h->ev_used[i]) { last = i; break; }
+        if (cudaEventSynchronize(h->ev[last]) != cudaSuccess) return GATO_ERR_CUDA;
+        float ms;
+        // stage i runs between the previous recorded event and event i
+        int prev = 0;
+        float* dst[5] = {nullptr, &s.form_us, &s.pcg_us, &s.merit_us, nullptr};
+        for (int i = 1; i < 5; ++i) {
+            if (!h->ev_used[i]) continue;
+            if (dst[i] && cudaEventElapsedTime(&ms, h->ev[prev], h->ev[i]) == cudaSuccess)
+                *dst[i] = 1000.f * ms;
+            prev = i;
+        }
+        if (cudaEventElapsedTime(&ms, h->ev[0], h->ev[last]) == cudaSuccess)
+            s.total_us = 1000.f * ms;
+    }
+    h->last = s;
+    *out = s;
+    return GATO_OK;
+}
+
+int gato_form_schur(gato_handle* h, const float* Q, const float* R, const float* q,
+                    const float* r, const float* A, const float* B, const float* e,
+                    const float* s0, uint32_t* status, void* stream)
+{
+    if (!h || !status || !lq_ok(h, Q, R, q, r, A, B, e, s0)) return GATO_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    begin_timing(h, st);
+    cudaError_t err = gato::launch_form_matrices(h, Q, R, A, B, status, st);
+    if (err == cudaSuccess) err = gato::launch_form_rhs(h, 0, q, r, e, s0, (size_t)h->w.n, st);
+    record(h, 1, st);
+    if (err == cudaErrorInvalidConfiguration) return GATO_ERR_UNSUPPORTED;
+    return cuda_fail(err);
+}
+
+int gato_get_schur(gato_handle* h, float* S_diag, float* S_off, float* gamma,
+                   float* Phi_diag, float* Phi_off, void* stream)
+{
+    if (!h) return GATO_ERR_INVALID_ARG;
+    const Work& w = h->w;
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t f = sizeof(float), K = (size_t)(w.N - 1);
+    struct Item { float* dst; const float* src; size_t width, stride; } items[] = {
+        {S_diag, w.D, (size_t)w.N * w.n * w.n, w.sNnn},
+        {S_off, w.O, K * w.n * w.n, w.sKnn},
+        {gamma, w.rhs[0].gamma, (size_t)w.N * w.n, w.sNn},
+        {Phi_diag, w.Pd, (size_t)w.N * w.n * w.n, w.sNnn},
+        {Phi_off, w.Po, K * w.n * w.n, w.sKnn},
+    };
+    for (const Item& it : items) {
+        if (!it.dst || it.width == 0) continue;
+        cudaError_t e = cudaMemcpy2DAsync(it.dst, it.width * f, it.src, it.stride * f,
+                                          it.width * f, (size_t)w.M, cudaMemcpyDeviceToDevice, st);
+        if (e != cudaSuccess) return GATO_ERR_CUDA;
+    }
+    return GATO_OK;
+}
+
+int gato_pcg_solve(gato_handle* h, const gato_params* p, const float* lambda0, float* lambda,
+                   float* dX, float* dU, int32_t* iters, uint32_t* status, void* stream)
+{
+    if (!h || !params_ok(p) || !lambda || !dX || !iters || !status) return GATO_ERR_INVALID_ARG;
+    if (h->w.N > 1 && !dU) return GATO_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    begin_timing(h, st);
+    cudaError_t err = gato::launch_pcg(h, p, lambda0, lambda, dX, dU, iters, status, st);
+    record(h, 2, st);
+    if (err == cudaErrorInvalidConfiguration) return GATO_ERR_UNSUPPORTED;
+    return cuda_fail(err);
+}
+
+int gato_linesearch(gato_handle* h, const gato_params* p, const float* Q, const float* R,
+                    const float* q, const float* r, const float* A, const float* B,
+                    const float* e, const float* s0, const float* dX, const float* dU,
+                    float* merit, int32_t* best, uint32_t* status, void* stream)
+{
+    if (!h || !params_ok(p) || !lq_ok(h, Q, R, q, r, A, B, e, s0) || !dX || !merit || !best ||
+        !status)
+        return GATO_ERR_INVALID_ARG;
+    if (h->w.N > 1 && !dU) return GATO_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    begin_timing(h, st);
+    cudaError_t err =
+        gato::launch_merit(h, p, Q, R, q, r, A, B, e, s0, dX, dU, merit, best, status, st);
+    record(h, 3, st);
+    return cuda_fail(err);
+}
+
+int gato_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const float* R,
+                   const float* q, const float* r, const float* A, const float* B,
+                   const float* e, const float* s0, float* dX, float* dU, float* lambda,
+                   int32_t* iters, float* merit, int32_t* best, uint32_t* status,
+                   void* stream)
+{
+    if (!h || !params_ok(p) || !lq_ok(h, Q, R, q, r, A, B, e, s0) || !dX || !lambda ||
+        !iters || !merit || !best || !status)
+        return GATO_ERR_INVALID_ARG;
+    if (h->w.N > 1 && !dU) return GATO_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    Work& w = h->w;
+    begin_timing(h, st);
+    cudaError_t err = gato::launch_form_matrices(h, Q, R, A, B, status, st);
+    if (err == cudaSuccess) err = gato::launch_form_rhs(h, 0, q, r, e, s0, (size_t)w.n, st);
+    record(h, 1, st);
+    if (err == cudaSuccess)
+        err = gato::launch_pcg_ex(h, p, 0, nullptr, lambda, dX, dU, iters, 0, status, st);
+    gato_params pc = *p;  // corrections are solved to refine_eps
+    if (p->refine_eps > 0.f) pc.pcg_eps = p->refine_eps;
+    for (int k = 0; k < p->refine_steps && err == cudaSuccess; ++k) {
+        err = gato::launch_kkt_residual(h, Q, R, q, r, A, B, e, s0, dX, dU, lambda, st);
+        if (err == cudaSuccess)
+            err = gato::launch_form_rhs(h, 1, w.q2, w.r2, w.e2, w.s02, (size_t)w.n, st);
+        if (err == cudaSuccess)
+            err = gato::launch_pcg_ex(h, &pc, 1, nullptr, w.dlam, w.ddX, w.ddU, iters, 1, status, st);
+        if (err == cudaSuccess) err = gato::launch_accumulate(h, lambda, dX, dU, iters, st);
+    }
+    record(h, 2, st);
+    if (err == cudaSuccess)
+        err = gato::launch_merit(h, p, Q, R, q, r, A, B, e, s0, dX, dU, merit, best, status, st);
+    record(h, 3, st);
+    if (err == cudaErrorInvalidConfiguration) return GATO_ERR_UNSUPPORTED;
+    return cuda_fail(err);
+}
+
+int gato_apply_step(gato_handle* h, const gato_params* p, const int32_t* best, const float* dX,
+                    const float* dU, float* X, float* U, void* stream)
+{
+    if (!h || !params_ok(p) || !best || !dX || !X) return GATO_ERR_INVALID_ARG;
+    if (h->w.N > 1 && (!dU || !U)) return GATO_ERR_INVALID_ARG;
+    return cuda_fail(gato::launch_apply_step(h, p, best, dX, dU, X, U, (cudaStream_t)stream));
+}
+
+}  // extern "C"

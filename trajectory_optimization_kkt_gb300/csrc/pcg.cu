@@ -1,0 +1,734 @@
+// pcg.cu -- batched preconditioned conjugate gradient on S lambda = gamma with
+// the symmetric stair preconditioner, and recovery of dz (GATO paper, Sec. II
+// and eq. (4); Sec. III: one thread block per linear system, no inter-block
+// coordination, block-tridiagonal matrix-vector products, warp-shuffle
+// reductions).
+//
+// Both kernels run PCG in the block-Jacobi-scaled variables
+//     lambda_hat_j = L_j^T lambda_j,   S_jj = L_j L_j^T,
+// where S_hat = L^-1 S L^-T = I + Nhat with Nhat block-tridiagonal, zero
+// diagonal blocks and coupling blocks Nhat_j = L_j^-1 S_{j,j-1} L_{j-1}^-T,
+// and the stair preconditioner becomes L^T Phi^-1 L = I - Nhat.  PCG is
+// invariant under this congruence: its iterates map one to one onto those of
+// PCG on (S, Phi^-1), eta = r^T Phi^-1 r is unchanged, and the true residual
+// is r = L r_hat.  Both operator applications per iteration are products with
+// the one matrix Nhat.
+//
+// k_pcg_tile<H>  (7 <= n <= 16, N <= 128): every coupling block Nhat_j is
+//     split into 2 x 2 tiles of H x H (H = ceil(n/2)); four threads hold one
+//     block's tiles in registers for the whole solve, so a product with Nhat
+//     reads only the two vector halves each tile touches from shared memory
+//     and does 2 H^2 FMAs per thread (row sums for knot j, column sums for
+//     knot j-1).  Vector elements are owned by threads in registers; the two
+//     inner products of an iteration are folded into the barriers that the
+//     products need anyway (x^T S_hat x = x^T x + 2 sum_j x_j^T Nhat_j x_{j-1}),
+//     four block barriers per iteration.
+// k_pcg_generic  (any n <= 64): Nhat in shared memory when it fits (else read
+//     from global memory), one thread per vector element.
+#include "gato_internal.cuh"
+
+namespace gato {
+namespace {
+
+struct PcgArgs {
+    Work w;
+    Rhs rhs;
+    const float* lambda0;  // original variables, [M][N][n], may be NULL
+    float* lambda;
+    float* dX;
+    float* dU;
+    int32_t* iters;
+    uint32_t* status;
+    float eps;
+    int max_iters;
+    int rule;
+    int nh_smem;     // generic kernel: Nhat staged in shared memory
+    int l_smem;      // packed L staged in shared memory (rule 0 only)
+    int acc_iters;   // add to iters instead of storing
+};
+
+__host__ __device__ __forceinline__ size_t round4(size_t x) { return (x + 3) & ~(size_t)3; }
+
+template <int K>
+__device__ __forceinline__ void block_sum(float (&v)[K], float4* buf)
+{
+    static_assert(K >= 1 && K <= 3, "block_sum reduces up to three values");
+#pragma unroll
+    for (int k = 0; k < K; ++k) v[k] = warp_sum(v[k]);
+    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (lane_id() == 0) {
+        float4 t = make_float4(v[0], 0.f, 0.f, 0.f);
+        if (K > 1) t.y = v[K > 1 ? 1 : 0];
+        if (K > 2) t.z = v[K > 2 ? 2 : 0];
+        buf[w] = t;
+    }
+    __syncthreads();
+    float s[3] = {0.f, 0.f, 0.f};
+    for (int q = 0; q < nw; ++q) {
+        const float4 t = buf[q];
+        s[0] += t.x;
+        s[1] += t.y;
+        s[2] += t.z;
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) v[k] = s[k];
+}
+
+// Warp partial sums written before a barrier and summed by every thread after
+// it (deterministic).  buf holds 32 float2.
+__device__ __forceinline__ void post2(float a, float b, float2* buf)
+{
+    a = warp_sum(a);
+    b = warp_sum(b);
+    if (lane_id() == 0) buf[threadIdx.x >> 5] = make_float2(a, b);
+}
+
+__device__ __forceinline__ float2 collect2(const float2* buf)
+{
+    // lane q reads warp q's partials; the xor butterfly gives every lane of
+    // every warp the same, order-fixed total
+    const int q = lane_id();
+    const float2 t = q < (int)(blockDim.x >> 5) ? buf[q] : make_float2(0.f, 0.f);
+    return make_float2(warp_sum(t.x), warp_sum(t.y));
+}
+
+// ---------------------------------------------------------------------------
+// epilogue shared by both kernels: lambda = L^-T lambda_hat and recovery of
+// dz.  lhat(j, a) reads lambda_hat; lsm is an N n scratch in shared memory.
+// ---------------------------------------------------------------------------
+template <typename LhatFn>
+__device__ __forceinline__ void recover_dz(const PcgArgs& g, LhatFn lhat, float* lsm)
+{
+    const Work& w = g.w;
+    const int N = w.N, n = w.n, m = w.m, Nn = N * n, T = blockDim.x, tid = threadIdx.x;
+    const int sol = blockIdx.x;
+    const float* gLi = w.Linv + sol * w.sNnn;
+    for (int i = tid; i < Nn; i += T) {
+        const int j = i / n, a = i - j * n;
+        const float* Li = gLi + (size_t)j * n * n;
+        float x = 0.f;
+        for (int b = a; b < n; ++b) x += Li[b * n + a] * lhat(j, b);
+        g.lambda[(size_t)sol * Nn + i] = x;
+        lsm[i] = x;
+    }
+    __syncthreads();
+    const float* Qi = w.Qinv + sol * w.sNnn;
+    const float* Ob = w.O + sol * w.sKnn;
+    const float* av = g.rhs.avec + sol * w.sNn;
+    for (int i = tid; i < Nn; i += T) {
+        const int k = i / n, a = i - k * n;
+        float x = av[i];
+        const float* Qrow = Qi + (size_t)k * n * n + a * n;
+        float t = 0.f;
+        for (int b = 0; b < n; ++b) t += Qrow[b] * lsm[k * n + b];
+        x += t;
+        if (k < N - 1) {
+            const float* Oc = Ob + (size_t)k * n * n + a;  // S_{k+1,k}, column a
+            float u = 0.f;
+            for (int b = 0; b < n; ++b) u += Oc[b * n] * lsm[(k + 1) * n + b];
+            x += u;
+        }
+        g.dX[(size_t)sol * Nn + i] = x;
+    }
+    const int Km = (N - 1) * m;
+    const float* Vb = w.V + sol * w.sKnm;
+    const float* bv = g.rhs.bvec + sol * w.sKm;
+    for (int t = tid; t < Km; t += T) {
+        const int k = t / m, c = t - k * m;
+        const float* Vc = Vb + (size_t)k * n * m + c;  // column c of B_k R_k^-1
+        float u = 0.f;
+        for (int b = 0; b < n; ++b) u += Vc[b * m] * lsm[(k + 1) * n + b];
+        g.dU[(size_t)sol * Km + t] = bv[t] - u;
+    }
+}
+
+__device__ __forceinline__ void finish(const PcgArgs& g, int it, bool done, bool nonfinite)
+{
+    if (threadIdx.x == 0) {
+        const int sol = blockIdx.x;
+        if (g.acc_iters)
+            g.iters[sol] += it;
+        else
+            g.iters[sol] = it;
+        uint32_t st = 0;
+        if (!done && !nonfinite) st |= GATO_STATUS_PCG_MAX_ITERS;
+        if (nonfinite) st |= GATO_STATUS_NONFINITE;
+        if (st) atomicOr(g.status + sol, st);
+    }
+}
+
+// ===========================================================================
+// generic kernel
+// ===========================================================================
+
+// (Nhat x)_i for element i = (knot j, row a):
+//   sum_b Nhat_j[a][b] x_{j-1}[b] + sum_b Nhat_{j+1}[b][a] x_{j+1}[b]
+__device__ __forceinline__ float nhat_row(const float* Nh, const float* x, int i, int n, int N)
+{
+    const int j = i / n, a = i - j * n;
+    float s = 0.f;
+    if (j > 0) {
+        const float* blk = Nh + (size_t)(j - 1) * n * n + a * n;
+        const float* xv = x + (j - 1) * n;
+        for (int b = 0; b < n; ++b) s += blk[b] * xv[b];
+    }
+    if (j < N - 1) {
+        const float* blk = Nh + (size_t)j * n * n + a;
+        const float* xv = x + (j + 1) * n;
+        for (int b = 0; b < n; ++b) s += blk[b * n] * xv[b];
+    }
+    return s;
+}
+
+// (L x)_i: packed lower rows (row a of knot j at j*tri + a(a+1)/2) or the
+// full n x n factor in global memory.
+__device__ __forceinline__ float lrow(const float* Lp, const float* Lg, bool packed,
+                                      const float* x, int i, int n)
+{
+    const int j = i / n, a = i - j * n;
+    const float* xv = x + j * n;
+    const float* row = packed ? Lp + (size_t)j * (n * (n + 1) / 2) + a * (a + 1) / 2
+                              : Lg + (size_t)j * n * n + a * n;
+    float s = 0.f;
+    for (int b = 0; b <= a; ++b) s += row[b] * xv[b];
+    return s;
+}
+
+// All PCG vectors live in shared memory; thread t owns elements t, t + T, ...
+// and is the only one to write them.
+__global__ void __launch_bounds__(512) k_pcg_generic(PcgArgs g)
+{
+    extern __shared__ __align__(16) float sm[];
+    const Work& w = g.w;
+    const int N = w.N, n = w.n, Nn = N * n, T = blockDim.x, tid = threadIdx.x;
+    const int sol = blockIdx.x;
+    const int tri = n * (n + 1) / 2;
+    const size_t nh_count = (size_t)(N - 1) * n * n;
+
+    size_t off = 0;
+    float* sNh = sm + off;
+    if (g.nh_smem) off += round4(nh_count);
+    float* sLp = sm + off;
+    const bool lpacked = g.rule == GATO_STOP_RESIDUAL && g.l_smem;
+    if (lpacked) off += round4((size_t)N * tri);
+    float* lam = sm + off;
+    off += round4(Nn);
+    float* r = sm + off;
+    off += round4(Nn);
+    float* p = sm + off;
+    off += round4(Nn);
+    float* v = sm + off;  // S_hat p, then z
+    off += round4(Nn);
+    float4* redA = reinterpret_cast<float4*>(sm + off);
+    float4* redB = redA + 32;
+
+    const float* gNh = w.Nh + sol * w.sKnn;
+    const float* gL = w.L + sol * w.sNnn;
+    if (g.nh_smem) {
+        for (size_t t = tid; t < nh_count; t += T) sNh[t] = gNh[t];
+    }
+    if (lpacked) {
+        for (int t = tid; t < Nn; t += T) {
+            const int j = t / n, a = t - j * n;
+            const float* src = gL + (size_t)j * n * n + a * n;
+            float* dst = sLp + (size_t)j * tri + a * (a + 1) / 2;
+            for (int b = 0; b <= a; ++b) dst[b] = src[b];
+        }
+    }
+    const float* Nh = g.nh_smem ? sNh : gNh;
+    const float* ghat = g.rhs.ghat + sol * w.sNn;
+    const float* gam = g.rhs.gamma + sol * w.sNn;
+
+    // initial point lambda_hat = L^T lambda0
+    for (int i = tid; i < Nn; i += T) {
+        float x = 0.f;
+        if (g.lambda0) {
+            const int j = i / n, a = i - j * n;
+            const float* Lj = gL + (size_t)j * n * n;
+            const float* l0 = g.lambda0 + (size_t)sol * Nn + j * n;
+            for (int b = a; b < n; ++b) x += Lj[b * n + a] * l0[b];
+        }
+        lam[i] = x;
+    }
+    __syncthreads();
+    for (int i = tid; i < Nn; i += T) r[i] = ghat[i] - lam[i] - nhat_row(Nh, lam, i, n, N);
+    __syncthreads();
+    float red3[3] = {0.f, 0.f, 0.f};
+    for (int i = tid; i < Nn; i += T) {
+        const float z = r[i] - nhat_row(Nh, r, i, n, N);
+        p[i] = z;
+        red3[0] += r[i] * z;
+        if (g.rule == GATO_STOP_RESIDUAL) {
+            const float t = lrow(sLp, gL, lpacked, r, i, n);
+            red3[1] += t * t;
+            red3[2] += gam[i] * gam[i];
+        } else if (g.rule == GATO_STOP_SCALED) {
+            red3[1] += r[i] * r[i];
+            red3[2] += ghat[i] * ghat[i];
+        }
+    }
+    block_sum<3>(red3, redA);
+    float eta = red3[0];
+    const float ref = g.rule == GATO_STOP_PRECOND ? eta : red3[2];
+    const float thr = g.eps * g.eps * ref;
+    bool done = (g.rule == GATO_STOP_PRECOND ? eta : red3[1]) <= thr;
+    bool nonfinite = !isfinite(eta);
+
+    int it = 0;
+    while (!done && !nonfinite && it < g.max_iters) {
+        ++it;
+        float pv[1] = {0.f};
+        for (int i = tid; i < Nn; i += T) {
+            const float x = p[i] + nhat_row(Nh, p, i, n, N);
+            v[i] = x;
+            pv[0] += p[i] * x;
+        }
+        block_sum<1>(pv, redA);
+        const float alpha = eta / pv[0];
+        for (int i = tid; i < Nn; i += T) {
+            lam[i] += alpha * p[i];
+            r[i] -= alpha * v[i];
+        }
+        __syncthreads();
+        float red2[2] = {0.f, 0.f};
+        for (int i = tid; i < Nn; i += T) {
+            const float z = r[i] - nhat_row(Nh, r, i, n, N);
+            v[i] = z;
+            red2[0] += r[i] * z;
+            if (g.rule == GATO_STOP_RESIDUAL) {
+                const float t = lrow(sLp, gL, lpacked, r, i, n);
+                red2[1] += t * t;
+            } else if (g.rule == GATO_STOP_SCALED) {
+                red2[1] += r[i] * r[i];
+            }
+        }
+        block_sum<2>(red2, redB);
+        const float eta_new = red2[0];
+        if (!isfinite(eta_new) || !isfinite(pv[0])) {
+            nonfinite = true;
+            break;
+        }
+        done = (g.rule == GATO_STOP_PRECOND ? eta_new : red2[1]) <= thr;
+        if (done) break;
+        const float beta = eta_new / eta;
+        for (int i = tid; i < Nn; i += T) p[i] = v[i] + beta * p[i];
+        eta = eta_new;
+        __syncthreads();
+    }
+    __syncthreads();
+    recover_dz(g, [&](int j, int b) { return lam[j * n + b]; }, r);
+    finish(g, it, done, nonfinite);
+}
+
+// ===========================================================================
+// register-tiled kernel
+// ===========================================================================
+//
+// Shared-memory layouts (floats), knot stride 16 ("padded"): element (j, a)
+// sits at j*16 + (a / H)*8 + a % H, so each half of a knot's vector starts on
+// a 32-byte boundary; the padding slots stay exactly zero.
+//   XP, XR [N][16]          the vectors multiplied by Nhat (p, r)
+//   YR0, YR1 [N][16]        row sums of block j, one copy per column tile
+//   YC0, YC1 [N][16]        column sums of block j+1, one copy per row tile
+//                           (each copy offset by 4 floats from the previous
+//                           one so that the two tiles' stores use different
+//                           banks)
+//   red [5][32] float2      warp partial sums
+//   DL [N]                  1 / ||L_j^-1||_F^2 (eigenvalue lower bounds)
+//   LP [N][n(n+1)/2]        packed Cholesky factors (stopping rule 0)
+// Thread t owns the four padded elements 4t .. 4t+3 (one knot half, one
+// float4) and keeps them in registers; the launch uses T >= 4 N threads.
+
+template <int H>
+struct Tile {
+    float t[H][H];
+};
+
+// One product with Nhat for the tile (j, rt, ct) held in registers: writes
+// the row and column partial sums and returns x_j^T Nhat_j(tile) x_{j-1}.
+template <int H>
+__device__ __forceinline__ float tile_matvec(const Tile<H>& T, int j, int rt, int ct,
+                                             const float* X, float* yr_base, float* yc_base)
+{
+    float xc[8], xr[8];
+    const float4* pc = reinterpret_cast<const float4*>(X + (j - 1) * 16 + ct * 8);
+    const float4* pr = reinterpret_cast<const float4*>(X + j * 16 + rt * 8);
+    {
+        const float4 a0 = pc[0], a1 = pc[1], b0 = pr[0], b1 = pr[1];
+        xc[0] = a0.x; xc[1] = a0.y; xc[2] = a0.z; xc[3] = a0.w;
+        xc[4] = a1.x; xc[5] = a1.y; xc[6] = a1.z; xc[7] = a1.w;
+        xr[0] = b0.x; xr[1] = b0.y; xr[2] = b0.z; xr[3] = b0.w;
+        xr[4] = b1.x; xr[5] = b1.y; xr[6] = b1.z; xr[7] = b1.w;
+    }
+    float rs[8], cs[8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a) rs[a] = cs[a] = 0.f;
+#pragma unroll
+    for (int a = 0; a < H; ++a)
+#pragma unroll
+        for (int b = 0; b < H; ++b) {
+            rs[a] += T.t[a][b] * xc[b];
+            cs[b] += T.t[a][b] * xr[a];
+        }
+    float q = 0.f;
+#pragma unroll
+    for (int a = 0; a < H; ++a) q += xr[a] * rs[a];
+    float4* yr = reinterpret_cast<float4*>(yr_base + j * 16 + rt * 8);
+    float4* yc = reinterpret_cast<float4*>(yc_base + (j - 1) * 16 + ct * 8);
+    yr[0] = make_float4(rs[0], rs[1], rs[2], rs[3]);
+    yr[1] = make_float4(rs[4], rs[5], rs[6], rs[7]);
+    yc[0] = make_float4(cs[0], cs[1], cs[2], cs[3]);
+    yc[1] = make_float4(cs[4], cs[5], cs[6], cs[7]);
+    return q;
+}
+
+struct Y4 {
+    const float* r0;
+    const float* r1;
+    const float* c0;
+    const float* c1;
+};
+
+// (Nhat x) at the four padded elements e0..e0+3, partial sums in a fixed order
+__device__ __forceinline__ void ysum4(const Y4& y, int e0, float (&o)[4])
+{
+    const float4 a = *reinterpret_cast<const float4*>(y.r0 + e0);
+    const float4 b = *reinterpret_cast<const float4*>(y.r1 + e0);
+    const float4 c = *reinterpret_cast<const float4*>(y.c0 + e0);
+    const float4 d = *reinterpret_cast<const float4*>(y.c1 + e0);
+    o[0] = a.x + b.x + c.x + d.x;
+    o[1] = a.y + b.y + c.y + d.y;
+    o[2] = a.z + b.z + c.z + d.z;
+    o[3] = a.w + b.w + c.w + d.w;
+}
+
+__device__ __forceinline__ void store4(float* X, int e0, const float (&v)[4])
+{
+    *reinterpret_cast<float4*>(X + e0) = make_float4(v[0], v[1], v[2], v[3]);
+}
+
+// ||L_j r_hat_j||^2 contribution of row a of knot j
+template <int H>
+__device__ __forceinline__ float lrow_tile(const float* LP, const float* gL, bool lpacked,
+                                          const float* XR, int j, int a, int n, int tri)
+{
+    const float* row = lpacked ? LP + (size_t)j * tri + a * (a + 1) / 2
+                               : gL + (size_t)j * n * n + a * n;
+    const float* xv = XR + j * 16;
+    float t = 0.f;
+    for (int b = 0; b <= a; ++b) t += row[b] * xv[(b / H) * 8 + b % H];
+    return t * t;
+}
+
+template <int H>
+__global__ void __launch_bounds__(512, 1) k_pcg_tile(PcgArgs g)
+{
+    extern __shared__ __align__(16) float sm[];
+    const Work& w = g.w;
+    const int N = w.N, n = w.n, T = blockDim.x, tid = threadIdx.x;
+    const int sol = blockIdx.x;
+    const int E = N * 16;  // padded elements
+    const int tri = n * (n + 1) / 2;
+    const bool rule0 = g.rule == GATO_STOP_RESIDUAL;
+    const bool lpacked = rule0 && g.l_smem;
+
+    float* XP = sm;
+    float* XR = XP + E;
+    float* YR0 = XR + E;
+    float* YR1 = YR0 + E + 4;
+    float* YC0 = YR1 + E + 4;
+    float* YC1 = YC0 + E + 4;
+    const int zero_count = 6 * E + 12;
+    float2* redA = reinterpret_cast<float2*>(sm + zero_count);
+    float2* redB = redA + 32;
+    float2* redC = redA + 64;
+    float2* redD = redA + 96;
+    float2* redE = redA + 128;
+    float* DL = reinterpret_cast<float*>(redA + 160);
+    float* LP = DL + ((N + 3) & ~3);
+    const Y4 Y{YR0, YR1, YC0, YC1};
+
+    // zero vectors and partial sums (padding and missing blocks stay 0)
+    for (int i = tid; i < zero_count; i += T) sm[i] = 0.f;
+    for (int j = tid; j < N; j += T) DL[j] = w.dlow[sol * w.sN + j];
+    const float* gL = w.L + sol * w.sNnn;
+    if (lpacked) {
+        for (int t = tid; t < N * n; t += T) {
+            const int j = t / n, a = t - j * n;
+            const float* src = gL + (size_t)j * n * n + a * n;
+            float* dst = LP + (size_t)j * tri + a * (a + 1) / 2;
+            for (int b = 0; b <= a; ++b) dst[b] = src[b];
+        }
+    }
+
+    // the tile this thread holds: block jb = 1 + tid/4, tile (rt, ct)
+    const int jb = 1 + (tid >> 2), rt = (tid >> 1) & 1, ct = tid & 1;
+    const bool has_tile = jb <= N - 1;
+    float* yr_base = ct ? YR1 : YR0;
+    float* yc_base = rt ? YC1 : YC0;
+    Tile<H> tile;
+    {
+        const float* blk = w.Nh + sol * w.sKnn + (size_t)(has_tile ? jb - 1 : 0) * n * n;
+#pragma unroll
+        for (int a = 0; a < H; ++a)
+#pragma unroll
+            for (int b = 0; b < H; ++b) {
+                const int ra = rt * H + a, cb = ct * H + b;
+                tile.t[a][b] = (has_tile && ra < n && cb < n) ? blk[ra * n + cb] : 0.f;
+            }
+    }
+
+    // owned elements e0 + u (u < 4): knot jo, rows ao + u; valid when in range
+    const int e0 = 4 * tid;
+    const bool owner = e0 < E;
+    const int jo = e0 >> 4, k0 = e0 & 7;
+    const int ao = ((e0 >> 3) & 1) * H + k0;
+    bool valid[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) valid[u] = owner && k0 + u < H && ao + u < n;
+    const int gi0 = jo * n + ao;  // unpadded index of element u is gi0 + u
+    const float* ghat = g.rhs.ghat + sol * w.sNn;
+    const float* gam = g.rhs.gamma + sol * w.sNn;
+    const float dl = owner ? DL[jo] : 0.f;
+    float lam[4], r[4], p[4], y[4] = {0.f, 0.f, 0.f, 0.f};
+    __syncthreads();
+
+    // lambda_hat0 = L^T lambda0
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        lam[u] = 0.f;
+        if (valid[u] && g.lambda0) {
+            const int a = ao + u;
+            const float* Lj = gL + (size_t)jo * n * n;
+            const float* l0 = g.lambda0 + (size_t)sol * N * n + jo * n;
+            float x = 0.f;
+            for (int b = a; b < n; ++b) x += Lj[b * n + a] * l0[b];
+            lam[u] = x;
+        }
+    }
+    if (owner) store4(XP, e0, lam);
+    __syncthreads();
+    if (has_tile) tile_matvec<H>(tile, jb, rt, ct, XP, yr_base, yc_base);
+    __syncthreads();
+    // r_hat = ghat - S_hat lambda_hat
+    float rr = 0.f, gg = 0.f;
+    if (owner) ysum4(Y, e0, y);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        r[u] = 0.f;
+        if (valid[u]) {
+            const int i = gi0 + u;
+            r[u] = ghat[i] - lam[u] - y[u];
+            rr += r[u] * r[u];
+            gg += rule0 ? gam[i] * gam[i] : ghat[i] * ghat[i];
+        }
+    }
+    if (owner) store4(XR, e0, r);
+    post2(rr, 0.f, redB);
+    post2(gg, 0.f, redE);
+    __syncthreads();
+    float q = has_tile ? tile_matvec<H>(tile, jb, rt, ct, XR, yr_base, yc_base) : 0.f;
+    float lsq = 0.f;
+    if (rule0) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (valid[u]) lsq += lrow_tile<H>(LP, gL, lpacked, XR, jo, ao + u, n, tri);
+    }
+    post2(q, lsq, redC);
+    __syncthreads();
+    float2 sB = collect2(redB), sC = collect2(redC);
+    float eta = sB.x - 2.f * sC.x;  // r^T (I - Nhat) r
+    const float ref = g.rule == GATO_STOP_PRECOND ? eta : collect2(redE).x;
+    const float thr = g.eps * g.eps * ref;
+    float stopq = g.rule == GATO_STOP_RESIDUAL ? sC.y : (g.rule == GATO_STOP_SCALED ? sB.x : eta);
+    bool done = stopq <= thr;
+    bool nonfinite = !isfinite(eta) || !isfinite(stopq);
+    float pp = 0.f;
+    if (owner) ysum4(Y, e0, y);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        p[u] = valid[u] ? r[u] - y[u] : 0.f;  // z = (I - Nhat) r
+        pp += p[u] * p[u];
+    }
+    if (owner) store4(XP, e0, p);
+    post2(pp, 0.f, redD);
+    __syncthreads();
+
+    int it = 0;
+    while (!done && !nonfinite && it < g.max_iters) {
+        ++it;
+        // A: Nhat p (tiles) and p^T Nhat p partials
+        q = has_tile ? tile_matvec<H>(tile, jb, rt, ct, XP, yr_base, yc_base) : 0.f;
+        post2(q, 0.f, redA);
+        __syncthreads();
+        // B: alpha = eta / p^T S_hat p; lambda and r updates (owners)
+        const float pv = collect2(redD).x + 2.f * collect2(redA).x;
+        const float alpha = eta / pv;
+        rr = 0.f;
+        if (owner) ysum4(Y, e0, y);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float v = p[u] + y[u];
+            lam[u] += alpha * p[u];
+            r[u] = valid[u] ? r[u] - alpha * v : 0.f;
+            rr += r[u] * r[u];
+        }
+        if (owner) store4(XR, e0, r);
+        // sum_j lambda_min-bound_j ||r_hat_j||^2 <= ||L r_hat||^2
+        post2(rr, dl * rr, redB);
+        __syncthreads();
+        // C: Nhat r (tiles), r^T Nhat r partials; ||L r_hat||^2 (owners), only
+        // when its lower bound does not already rule convergence out
+        q = has_tile ? tile_matvec<H>(tile, jb, rt, ct, XR, yr_base, yc_base) : 0.f;
+        lsq = 0.f;
+        sB = collect2(redB);
+        const bool exact = rule0 && sB.y * 0.999f <= thr;
+        if (exact) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (valid[u]) lsq += lrow_tile<H>(LP, gL, lpacked, XR, jo, ao + u, n, tri);
+        }
+        post2(q, lsq, redC);
+        __syncthreads();
+        // D: eta' = r^T (I - Nhat) r, convergence, p = z + beta p (owners)
+        sC = collect2(redC);
+        const float eta_new = sB.x - 2.f * sC.x;
+        stopq = g.rule == GATO_STOP_RESIDUAL ? sC.y : (g.rule == GATO_STOP_SCALED ? sB.x : eta_new);
+        if (!isfinite(eta_new) || !isfinite(pv) || !isfinite(stopq) || !isfinite(sB.y)) {
+            nonfinite = true;
+            break;
+        }
+        done = (!rule0 || exact) && stopq <= thr;
+        if (done) break;
+        const float beta = eta_new / eta;
+        pp = 0.f;
+        if (owner) ysum4(Y, e0, y);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            p[u] = valid[u] ? (r[u] - y[u]) + beta * p[u] : 0.f;
+            pp += p[u] * p[u];
+        }
+        if (owner) store4(XP, e0, p);
+        post2(pp, 0.f, redD);
+        eta = eta_new;
+        __syncthreads();
+    }
+    __syncthreads();
+    if (owner) store4(XP, e0, lam);
+    __syncthreads();
+    recover_dz(g, [&](int j, int b) { return XP[j * 16 + (b / H) * 8 + b % H]; }, YR0);
+    finish(g, it, done, nonfinite);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+size_t generic_smem_bytes(const Work& w, int nh_smem, int l_smem)
+{
+    const size_t n = w.n, N = w.N;
+    size_t f = 0;
+    if (nh_smem) f += round4((N - 1) * n * n);
+    if (l_smem) f += round4(N * (n * (n + 1) / 2));
+    f += 4 * round4(N * n);  // lambda_hat, r_hat, p, v
+    f += 64 * 4;             // two float4[32] reduction buffers
+    return f * sizeof(float);
+}
+
+size_t tile_smem_bytes(const Work& w, int l_smem)
+{
+    const size_t n = w.n, N = w.N;
+    size_t f = 6 * 16 * N + 12;  // XP, XR, YR0/1, YC0/1
+    f += 5 * 32 * 2;        // five float2[32] reduction buffers
+    f += round4(N);         // DL
+    if (l_smem) f += N * (n * (n + 1) / 2);
+    return f * sizeof(float);
+}
+
+template <typename K>
+cudaError_t launch_k(K kernel, const PcgArgs& a, int T, size_t smem, cudaStream_t st)
+{
+    if (smem > 48 * 1024) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    kernel<<<a.w.M, T, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const float* lambda0,
+                          float* lambda, float* dX, float* dU, int32_t* iters, int acc_iters,
+                          uint32_t* status, cudaStream_t st)
+{
+    const Work& w = h->w;
+    PcgArgs a;
+    a.w = w;
+    a.rhs = w.rhs[set];
+    a.lambda0 = lambda0;
+    a.lambda = lambda;
+    a.dX = dX;
+    a.dU = dU;
+    a.iters = iters;
+    a.status = status;
+    a.eps = p->pcg_eps;
+    a.max_iters = p->pcg_max_iters;
+    a.rule = p->stop_rule;
+    a.acc_iters = acc_iters;
+    const size_t limit = (size_t)h->smem_optin;
+    const int want_l = p->stop_rule == GATO_STOP_RESIDUAL;
+
+    // register-tiled kernel: 7 <= n <= 16, four threads per coupling block
+    const int H = (w.n + 1) / 2;
+    int T = ((4 * w.N + 31) / 32) * 32;
+    if (T < 64) T = 64;
+    if (!h->force_generic_pcg && w.n >= 7 && w.n <= 16 && T <= 512) {
+        a.nh_smem = 0;
+        a.l_smem = want_l;
+        size_t smem = tile_smem_bytes(w, a.l_smem);
+        if (smem > limit) {
+            a.l_smem = 0;
+            smem = tile_smem_bytes(w, 0);
+        }
+        if (smem <= limit) {
+            switch (H) {
+                case 4: return launch_k(k_pcg_tile<4>, a, T, smem, st);
+                case 5: return launch_k(k_pcg_tile<5>, a, T, smem, st);
+                case 6: return launch_k(k_pcg_tile<6>, a, T, smem, st);
+                case 7: return launch_k(k_pcg_tile<7>, a, T, smem, st);
+                case 8: return launch_k(k_pcg_tile<8>, a, T, smem, st);
+                default: break;
+            }
+        }
+    }
+
+    // generic kernel
+    a.nh_smem = 1;
+    a.l_smem = want_l;
+    size_t smem = generic_smem_bytes(w, a.nh_smem, a.l_smem);
+    if (smem > limit && want_l) {
+        a.l_smem = 0;
+        smem = generic_smem_bytes(w, a.nh_smem, a.l_smem);
+    }
+    if (smem > limit) {
+        a.nh_smem = 0;
+        smem = generic_smem_bytes(w, a.nh_smem, a.l_smem);
+    }
+    if (smem > limit) return cudaErrorInvalidConfiguration;
+    const int Nn = w.N * w.n;
+    T = ((Nn + 1) / 2 + 31) / 32 * 32;
+    if (T < 64) T = 64;
+    if (T > 512) T = 512;
+    return launch_k(k_pcg_generic, a, T, smem, st);
+}
+
+cudaError_t launch_pcg(gato_handle* h, const gato_params* p, const float* lambda0,
+                       float* lambda, float* dX, float* dU, int32_t* iters,
+                       uint32_t* status, cudaStream_t st)
+{
+    return launch_pcg_ex(h, p, 0, lambda0, lambda, dX, dU, iters, 0, status, st);
+}
+
+}  // namespace gato

@@ -1,0 +1,235 @@
+"""Thin ctypes binding of the C ABI in include/gato.h.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library (``_build/libgato.so``).  Tensors must be contiguous float32 (int32 /
+uint32-as-int32 for iters, best and status) CUDA tensors on the handle's
+device.  If the library is missing, loading raises instead of falling back.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import _build
+
+GATO_OK = 0
+GATO_ERR_INVALID_ARG = -1
+GATO_ERR_UNSUPPORTED = -2
+GATO_ERR_CUDA = -3
+GATO_ERR_NO_MEMORY = -4
+
+GATO_STATUS_PCG_MAX_ITERS = 1
+GATO_STATUS_NONPOSITIVE_PIVOT = 2
+GATO_STATUS_LINESEARCH_FAILED = 4
+GATO_STATUS_NONFINITE = 8
+
+GATO_PCG_AUTO = 0
+GATO_PCG_GENERIC = 1
+
+GATO_STOP_RESIDUAL = 0
+GATO_STOP_PRECOND = 1
+GATO_STOP_SCALED = 2
+
+_ERRORS = {GATO_ERR_INVALID_ARG: "invalid argument", GATO_ERR_UNSUPPORTED: "unsupported sizes",
+           GATO_ERR_CUDA: "CUDA error", GATO_ERR_NO_MEMORY: "out of device memory"}
+
+
+class GatoParams(ctypes.Structure):
+    _fields_ = [("pcg_eps", ctypes.c_float), ("pcg_max_iters", ctypes.c_int),
+                ("stop_rule", ctypes.c_int), ("refine_steps", ctypes.c_int),
+                ("n_alpha", ctypes.c_int), ("beta", ctypes.c_float), ("mu", ctypes.c_float),
+                ("merit_threads", ctypes.c_int), ("refine_eps", ctypes.c_float)]
+
+
+class GatoStats(ctypes.Structure):
+    _fields_ = [("form_us", ctypes.c_float), ("pcg_us", ctypes.c_float),
+                ("merit_us", ctypes.c_float), ("total_us", ctypes.c_float)]
+
+
+class GatoError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {_ERRORS.get(code, 'error')} ({code})")
+        self.code = code
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: Optional[str] = None):
+    """Load libgato.so (built by __graft_entry__.build()); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing (run build())")
+    lib = ctypes.CDLL(path)
+    vp, ip, fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    P = ctypes.POINTER(GatoParams)
+    lib.gato_default_params.argtypes = [P]
+    lib.gato_default_params.restype = None
+    lib.gato_create.argtypes = [ctypes.POINTER(vp), ip, ip, ip, ip]
+    lib.gato_destroy.argtypes = [vp]
+    lib.gato_destroy.restype = None
+    lib.gato_set_timing.argtypes = [vp, ip]
+    lib.gato_set_pcg_kernel.argtypes = [vp, ip]
+    lib.gato_get_stats.argtypes = [vp, ctypes.POINTER(GatoStats)]
+    lib.gato_form_schur.argtypes = [vp] + [vp] * 8 + [vp, vp]
+    lib.gato_get_schur.argtypes = [vp] + [vp] * 5 + [vp]
+    lib.gato_pcg_solve.argtypes = [vp, P] + [vp] * 6 + [vp]
+    lib.gato_linesearch.argtypes = [vp, P] + [vp] * 8 + [vp] * 5 + [vp]
+    lib.gato_solve_kkt.argtypes = [vp, P] + [vp] * 8 + [vp] * 7 + [vp]
+    lib.gato_apply_step.argtypes = [vp, P] + [vp] * 5 + [vp]
+    for fn in ("gato_create", "gato_set_timing", "gato_set_pcg_kernel", "gato_get_stats", "gato_form_schur",
+               "gato_get_schur", "gato_pcg_solve", "gato_linesearch", "gato_solve_kkt",
+               "gato_apply_step"):
+        getattr(lib, fn).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, rc: int):
+    if rc != GATO_OK:
+        raise GatoError(fn, rc)
+
+
+def default_params(**overrides) -> GatoParams:
+    p = GatoParams()
+    load().gato_default_params(ctypes.byref(p))
+    for k, v in overrides.items():
+        setattr(p, k, v)
+    return p
+
+
+def _ptr(t, dtype=None, what="tensor"):
+    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    import torch
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    want = dtype or torch.float32
+    if t.dtype != want:
+        raise ValueError(f"{what} must be {want}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+_LQ = ("Q", "R", "q", "r", "A", "B", "e", "s0")
+
+
+class Solver:
+    """Owns a gato_handle; methods mirror the C entry points one to one."""
+
+    def __init__(self, M: int, N: int, n: int, m: int):
+        import torch
+        self.lib = load()
+        self.M, self.N, self.n, self.m = M, N, n, m
+        self.device = torch.cuda.current_device()
+        h = ctypes.c_void_p()
+        _check("gato_create", self.lib.gato_create(ctypes.byref(h), M, N, n, m))
+        self.h = h
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.gato_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # -- helpers --------------------------------------------------------------
+    def _lq(self, prob):
+        return [_ptr(prob.get(k), what=k) for k in _LQ]
+
+    # -- entry points ---------------------------------------------------------
+    def set_timing(self, on: bool):
+        _check("gato_set_timing", self.lib.gato_set_timing(self.h, 1 if on else 0))
+
+    def set_pcg_kernel(self, kind: int):
+        _check("gato_set_pcg_kernel", self.lib.gato_set_pcg_kernel(self.h, kind))
+
+    def get_stats(self) -> GatoStats:
+        s = GatoStats()
+        _check("gato_get_stats", self.lib.gato_get_stats(self.h, ctypes.byref(s)))
+        return s
+
+    def form_schur(self, prob, status, stream=None):
+        import torch
+        _check("gato_form_schur", self.lib.gato_form_schur(
+            self.h, *self._lq(prob), _ptr(status, torch.int32, "status"), _stream(stream)))
+
+    def get_schur(self, S_diag=None, S_off=None, gamma=None, Phi_diag=None, Phi_off=None,
+                  stream=None):
+        _check("gato_get_schur", self.lib.gato_get_schur(
+            self.h, _ptr(S_diag), _ptr(S_off), _ptr(gamma), _ptr(Phi_diag), _ptr(Phi_off),
+            _stream(stream)))
+
+    def pcg_solve(self, params, lam, dX, dU, iters, status, lambda0=None, stream=None):
+        import torch
+        _check("gato_pcg_solve", self.lib.gato_pcg_solve(
+            self.h, ctypes.byref(params), _ptr(lambda0), _ptr(lam), _ptr(dX), _ptr(dU),
+            _ptr(iters, torch.int32, "iters"), _ptr(status, torch.int32, "status"),
+            _stream(stream)))
+
+    def linesearch(self, params, prob, dX, dU, merit, best, status, stream=None):
+        import torch
+        _check("gato_linesearch", self.lib.gato_linesearch(
+            self.h, ctypes.byref(params), *self._lq(prob), _ptr(dX), _ptr(dU), _ptr(merit),
+            _ptr(best, torch.int32, "best"), _ptr(status, torch.int32, "status"),
+            _stream(stream)))
+
+    def solve_kkt(self, params, prob, dX, dU, lam, iters, merit, best, status, stream=None):
+        import torch
+        _check("gato_solve_kkt", self.lib.gato_solve_kkt(
+            self.h, ctypes.byref(params), *self._lq(prob), _ptr(dX), _ptr(dU), _ptr(lam),
+            _ptr(iters, torch.int32, "iters"), _ptr(merit), _ptr(best, torch.int32, "best"),
+            _ptr(status, torch.int32, "status"), _stream(stream)))
+
+    def apply_step(self, params, best, dX, dU, X, U, stream=None):
+        import torch
+        _check("gato_apply_step", self.lib.gato_apply_step(
+            self.h, ctypes.byref(params), _ptr(best, torch.int32, "best"), _ptr(dX), _ptr(dU),
+            _ptr(X), _ptr(U), _stream(stream)))
+
+    # -- convenience ------------------------------------------------------------
+    def outputs(self, n_alpha: int = 8):
+        """Freshly allocated output tensors for solve_kkt (status zeroed)."""
+        import torch
+        M, N, n, m = self.M, self.N, self.n, self.m
+        dev = torch.device("cuda", self.device)
+        f = dict(device=dev, dtype=torch.float32)
+        return dict(dX=torch.empty(M, N, n, **f), dU=torch.empty(M, max(N - 1, 0), m, **f),
+                    lam=torch.empty(M, N, n, **f),
+                    iters=torch.zeros(M, device=dev, dtype=torch.int32),
+                    merit=torch.empty(M, n_alpha + 1, **f),
+                    best=torch.empty(M, device=dev, dtype=torch.int32),
+                    status=torch.zeros(M, device=dev, dtype=torch.int32))
+
+
+def to_device(prob, device="cuda"):
+    """numpy workload dict -> contiguous float32 CUDA tensors."""
+    import torch
+    return {k: torch.as_tensor(v, dtype=torch.float32).contiguous().to(device) for k, v in prob.items()}
