@@ -81,6 +81,7 @@ extern "C" {
 #define GATO_MAX_STATE 64          /* n <= 64 */
 #define GATO_MAX_CONTROL 64        /* m <= 64 */
 #define GATO_MAX_ALPHA 31          /* n_alpha <= 31 */
+#define GATO_NOALLOC_MAX_BYTES (32u * 1024u * 1024u) /* scratch of gato_solve_kkt_noalloc */
 
 typedef struct gato_params {
     float pcg_eps;       /* PCG tolerance eps (default 1e-6)                     */
@@ -111,7 +112,7 @@ void gato_default_params(gato_params* p);
 
 /* Creates a solver for M solves of N knots, n states and m controls on the
  * current CUDA device and allocates its device workspace (cudaMalloc; about
- * 4 (7 n^2 + m^2 + 2 n m + 4 n + m) N M bytes).  *h receives the handle, which the
+ * 4 M (8 N n^2 + (N-1)(m^2 + n m) + 11 N n + 4 (N-1) m + 65 N) bytes).  *h receives the handle, which the
  * caller releases with gato_destroy.  Errors: INVALID_ARG (h NULL, M, N, n or
  * m < 1), UNSUPPORTED (n or m above the limits), NO_MEMORY, CUDA. */
 int gato_create(gato_handle** h, int M, int N, int n, int m);
@@ -196,6 +197,30 @@ int gato_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const f
  * solves with best < 0 are left unchanged. */
 int gato_apply_step(gato_handle* h, const gato_params* p, const int32_t* best,
                     const float* dX, const float* dU, float* X, float* U, void* stream);
+
+/* gato_solve_kkt without a handle and without allocating anything.  The
+ * paper has no counterpart: this entry point exists for callers that cannot
+ * allocate device memory while they run, such as a real-time MPC loop whose
+ * memory is fixed at start-up, or a host framework that owns every device
+ * allocation.  Arguments are those of gato_solve_kkt plus the sizes (M, N,
+ * n, m); the caller still provides every input and output.  The solver's
+ * scratch is one static device array of GATO_NOALLOC_MAX_BYTES that every GPU
+ * loading this library holds until the process exits; a problem needs about
+ * 4 M (8 N n^2 + (N-1)(m^2 + n m) + 11 N n + 4 (N-1) m + 65 N) bytes of it
+ * (each array rounded up to 64 floats), and larger problems are rejected
+ * with GATO_ERR_UNSUPPORTED before
+ * anything is launched (use gato_create for those).  The first call on each
+ * device looks up the array's device address; make that first call before
+ * any stream capture.  All calls share the array and it keeps the previous
+ * call's contents (every entry is written before it is read, so nothing needs
+ * clearing); calls that overlap on the GPU race on it, so the caller must
+ * serialise them.  Never calls cudaMalloc, cudaFree or any allocating
+ * routine. */
+int gato_solve_kkt_noalloc(const gato_params* p, int M, int N, int n, int m, const float* Q,
+                           const float* R, const float* q, const float* r, const float* A,
+                           const float* B, const float* e, const float* s0, float* dX,
+                           float* dU, float* lambda, int32_t* iters, float* merit,
+                           int32_t* best, uint32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

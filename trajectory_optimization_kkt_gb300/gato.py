@@ -85,9 +85,10 @@ def load(path: Optional[str] = None):
     lib.gato_linesearch.argtypes = [vp, P] + [vp] * 8 + [vp] * 5 + [vp]
     lib.gato_solve_kkt.argtypes = [vp, P] + [vp] * 8 + [vp] * 7 + [vp]
     lib.gato_apply_step.argtypes = [vp, P] + [vp] * 5 + [vp]
+    lib.gato_solve_kkt_noalloc.argtypes = [P, ip, ip, ip, ip] + [vp] * 8 + [vp] * 7 + [vp]
     for fn in ("gato_create", "gato_set_timing", "gato_set_pcg_kernel", "gato_get_stats", "gato_form_schur",
                "gato_get_schur", "gato_pcg_solve", "gato_linesearch", "gato_solve_kkt",
-               "gato_apply_step"):
+               "gato_apply_step", "gato_solve_kkt_noalloc"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -227,6 +228,18 @@ class Solver:
                     merit=torch.empty(M, n_alpha + 1, **f),
                     best=torch.empty(M, device=dev, dtype=torch.int32),
                     status=torch.zeros(M, device=dev, dtype=torch.int32))
+
+
+def solve_kkt_noalloc(params, prob, dX, dU, lam, iters, merit, best, status, stream=None):
+    """gato_solve_kkt_noalloc: the whole solve with the library's static scratch
+    (no handle, no device allocation by the library)."""
+    import torch
+    M, N, n = prob["Q"].shape[:3]
+    m = prob["B"].shape[-1]
+    _check("gato_solve_kkt_noalloc", load().gato_solve_kkt_noalloc(
+        ctypes.byref(params), M, N, n, m, *[_ptr(prob.get(k), what=k) for k in _LQ],
+        _ptr(dX), _ptr(dU), _ptr(lam), _ptr(iters, torch.int32, "iters"), _ptr(merit),
+        _ptr(best, torch.int32, "best"), _ptr(status, torch.int32, "status"), _stream(stream)))
 
 
 def to_device(prob, device="cuda"):
