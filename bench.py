@@ -31,9 +31,12 @@ METRIC = "KKT solves/sec and PCG iters/sec at batch M; % of GB300 HBM/L2 rooflin
 UNIT = "solves/s"
 WORKLOAD_INDEX = 4  # M=256, N=128, n=14, m=7
 
-# DRAM traffic of one PCG launch from an ncu capture, valid only for the kernel
-# source it was taken on (sha256 prefix of csrc/pcg.cu); null otherwise.
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one PCG
+# launch at this workload, from an ncu capture; valid only for the kernel
+# source it was taken on (sha256 prefix of csrc/pcg.cu), null otherwise.
 PCG_TRAFFIC = {"pcg_sha": None, "bytes_per_launch": None}
+
+FP32_LANES_PER_SM = 128  # FFMA lanes per SM (4 sub-partitions x 32)
 
 
 def _src_sha(path):
@@ -42,13 +45,14 @@ def _src_sha(path):
 
 
 def _peaks():
+    """(HBM GB/s, kind, max SM MHz) from MEASURED_PEAKS.json, else the fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d["hbm_gbs"]), "measured", float(d.get("sm_max_mhz", 2070.0))
     except Exception:
-        return 6800.0, "fallback"
+        return 6800.0, "fallback", 2070.0
 
 
 class ClockSampler:
@@ -200,6 +204,8 @@ def run_gpu(args, world, rank, local):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     _build.build()
     w = WORKLOADS[WORKLOAD_INDEX]
+    if args.batch:
+        w = w.with_batch(args.batch)
     M = w.M
     prob = make_batch(w, M=M, first_solve=rank * M) if rank else make_batch(w, M=M)
     dev = torch.device("cuda", local)
@@ -228,7 +234,7 @@ def run_gpu(args, world, rank, local):
     s.set_timing(True)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    pcg_us, form_us, merit_us, iters_total = [], [], [], 0
+    pcg_us, refine_us, form_us, merit_us, iters_total = [], [], [], [], 0
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -240,6 +246,7 @@ def run_gpu(args, world, rank, local):
             ends[k].record(stream)
             st = s.get_stats()  # synchronises on this step's last event
             pcg_us.append(st.pcg_us)
+            refine_us.append(max(st.refine_us, 0.0))
             form_us.append(st.form_us)
             merit_us.append(st.merit_us)
             iters_total += int(out["iters"].sum())
@@ -259,7 +266,7 @@ def run_gpu(args, world, rank, local):
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
-    for k in range(args.steps):
+    for k in range(0 if args.no_e2e else args.steps):
         flush.fill_(float(k))
         e_start.record(stream)
         for key, v in host.items():
@@ -280,14 +287,24 @@ def run_gpu(args, world, rank, local):
     value = solves / (total_ms / 1000.0)
 
     # ---- roofline of the dominant kernel (PCG) ----
-    # algorithmic bytes per solve-iteration: packed S (N n(n+1)/2 + (N-1) n^2
-    # floats) plus packed Phi^-1 (same count)
+    # The PCG kernel keeps the operator on chip (registers and shared memory),
+    # so its bound is the SM's fp32 FMA throughput.  Algorithmic flops per
+    # solve-iteration are those of the method's iteration on the explicit
+    # block-tridiagonal S and Phi^-1: two products with 3N-2 blocks of n^2
+    # (2 flops per entry each) plus 12 N n of vector updates and dots.  Every
+    # PCG iteration of the step (solve and refinement correction) counts; the
+    # time is the two PCG launches plus the refinement's small kernels.
     N, n = w.N, w.n
-    unit_bytes = 2 * (N * n * (n + 1) // 2 + (N - 1) * n * n) * 4
+    flops_it = 2 * 2 * (3 * N - 2) * n * n + 12 * N * n
     iters_per_step = iters_total / args.steps
-    pcg_mean_us = statistics.mean(pcg_us)
-    achieved = unit_bytes * iters_per_step / (pcg_mean_us * 1e-6) / 1e9
-    peak, peak_kind = _peaks()
+    pcg_stage_us = statistics.mean(a + b for a, b in zip(pcg_us, refine_us))
+    achieved_tf = flops_it * iters_per_step / (pcg_stage_us * 1e-6) / 1e12
+    hbm_peak, peak_kind, sm_mhz = _peaks()
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak_tf = n_sm * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    # the pages' streaming model: packed S and Phi^-1 read once per iteration
+    bytes_it = 2 * (N * n * (n + 1) // 2 + (N - 1) * n * n) * 4
+    stream_gbs = bytes_it * iters_per_step / (pcg_stage_us * 1e-6) / 1e9
     sha = _src_sha(os.path.join(_build.CSRC, "pcg.cu"))
     traffic = PCG_TRAFFIC["bytes_per_launch"] if PCG_TRAFFIC["pcg_sha"] == sha else None
 
@@ -300,15 +317,24 @@ def run_gpu(args, world, rank, local):
             "config": _config(w),
             "pcg_iters_per_sec": iters_per_step * world / (total_ms / args.steps / 1000.0),
             "pcg_iters_per_solve": iters_per_step / M,
-            "stage_us": {"form": statistics.mean(form_us), "pcg": pcg_mean_us,
+            "stage_us": {"form": statistics.mean(form_us), "pcg": statistics.mean(pcg_us),
+                         "refine": statistics.mean(refine_us),
                          "merit": statistics.mean(merit_us)},
             "status_nonzero_solves": status_bad,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic, "kernel": "k_pcg",
-                         "peak_kind": peak_kind,
-                         "algorithmic_bytes_per_launch": unit_bytes * iters_per_step},
-            "e2e": {"value": solves / (e2e_ms / 1000.0), "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "roofline": {"bound": "alu", "achieved": achieved_tf, "peak": alu_peak_tf,
+                         "unit": "TFLOP/s", "frac": achieved_tf / alu_peak_tf,
+                         "traffic": traffic, "kernel": "k_pcg_tile (solve + refinement launches)",
+                         "peak_basis": f"{n_sm} SMs x {FP32_LANES_PER_SM} FFMA lanes x 2 flop x "
+                                       f"{sm_mhz:.0f} MHz (max SM clock, {peak_kind})",
+                         "flops_per_solve_iteration": flops_it,
+                         "iterations_per_step": iters_per_step},
+            "hbm_stream_model": {"achieved": stream_gbs, "peak": hbm_peak, "unit": "GB/s",
+                                 "frac": stream_gbs / hbm_peak, "peak_kind": peak_kind,
+                                 "note": "S and Phi^-1 bytes per iteration as if streamed; "
+                                         "the kernel keeps them on chip"},
+            "e2e": None if args.no_e2e else {
+                "value": solves / (e2e_ms / 1000.0), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
         }
@@ -327,6 +353,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gato", choices=["gato", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="solves per GPU (default: the workload's 256); for profiler "
+                         "captures of a smaller case")
     args = ap.parse_args()
     world, rank, local = _dist_env()
     if args.impl == "reference":

@@ -77,6 +77,17 @@ extern "C" {
                                       N <= 128, else the generic kernel            */
 #define GATO_PCG_GENERIC 1         /* always the generic kernel                   */
 
+/* formation kernel selection (gato_set_form_kernel) */
+#define GATO_FORM_AUTO 0           /* register kernels when n, m <= 16, else the
+                                      shared-memory kernels                        */
+#define GATO_FORM_SHARED 1         /* always the shared-memory kernels           */
+
+/* merit kernels (gato_params.merit_kernel) */
+#define GATO_MERIT_FUSED 0         /* one block per solve, knots streamed once,
+                                      candidates in factored form (default)       */
+#define GATO_MERIT_PER_CANDIDATE 1 /* one block of merit_threads per (knot,
+                                      candidate), full formula per candidate      */
+
 /* Limits of this build. */
 #define GATO_MAX_STATE 64          /* n <= 64 */
 #define GATO_MAX_CONTROL 64        /* m <= 64 */
@@ -96,13 +107,15 @@ typedef struct gato_params {
                             (default 64); results are bit-identical at any size   */
     float refine_eps;    /* PCG tolerance of each refinement correction; 0 means
                             pcg_eps (default 0.1: a correction only needs a digit) */
+    int merit_kernel;    /* GATO_MERIT_FUSED (default) or GATO_MERIT_PER_CANDIDATE */
 } gato_params;
 
 typedef struct gato_stats {
     float form_us;       /* device time of the last call's stages (microseconds), */
     float pcg_us;        /* filled only when timing was enabled with              */
-    float merit_us;      /* gato_set_timing; -1 for a stage that did not run      */
-    float total_us;
+    float refine_us;     /* gato_set_timing; -1 for a stage that did not run.     */
+    float merit_us;      /* pcg_us: the PCG launch of the solve; refine_us: every */
+    float total_us;      /* refinement round (residual, right-hand side, PCG).    */
 } gato_stats;
 
 typedef struct gato_handle gato_handle;
@@ -132,6 +145,10 @@ int gato_get_stats(gato_handle* h, gato_stats* out);
  * Both give the same PCG iterates up to rounding; the generic kernel covers
  * every supported size.  Errors: INVALID_ARG. */
 int gato_set_pcg_kernel(gato_handle* h, int kind);
+
+/* Chooses the formation kernels (GATO_FORM_AUTO or GATO_FORM_SHARED) for later
+ * calls; both compute the same blocks up to rounding.  Errors: INVALID_ARG. */
+int gato_set_form_kernel(gato_handle* h, int kind);
 
 /* a1 + a2.  Forms, per solve and knot (GATO paper Sec. II, eqs. (4)-(6)):
  *   S_00 = Q_0^-1, S_jj = A_{j-1} Q_{j-1}^-1 A_{j-1}^T + B_{j-1} R_{j-1}^-1 B_{j-1}^T + Q_j^-1,
@@ -171,7 +188,9 @@ int gato_pcg_solve(gato_handle* h, const gato_params* p, const float* lambda0,
  * alpha_i = beta^-i (i = 0..n_alpha-1), with x = alpha dx, u = alpha du,
  *   M(alpha) = sum_k 1/2 x_k^T Q_k x_k + q_k^T x_k + 1/2 u_k^T R_k u_k + r_k^T u_k
  *            + mu (||x_0 - s0||_1 + sum_k ||A_k x_k + B_k u_k + e_k - x_{k+1}||_1),
- * one thread block per (knot, candidate), knot sums in a fixed order.
+ * with the fused kernel (default) or one thread block per (knot, candidate)
+ * (p->merit_kernel); knot sums in a fixed order, so results are reproducible
+ * and, for the per-candidate kernel, identical at any p->merit_threads.
  * merit [M][n_alpha+1]: merit[.][0] is alpha = 0, merit[.][1+i] is beta^-i.
  * best [M]: argmin_i merit[1+i] (lowest i on ties) if it is below merit[0],
  * else -1 with GATO_STATUS_LINESEARCH_FAILED. */

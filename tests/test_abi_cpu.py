@@ -32,7 +32,7 @@ def test_header_declares_the_abi():
     for fn in ("gato_create", "gato_destroy", "gato_form_schur", "gato_pcg_solve",
                "gato_linesearch", "gato_solve_kkt", "gato_apply_step", "gato_get_schur",
                "gato_default_params", "gato_set_timing", "gato_get_stats",
-               "gato_set_pcg_kernel"):
+               "gato_set_pcg_kernel", "gato_set_form_kernel", "gato_solve_kkt_noalloc"):
         assert fn in names
 
 
@@ -48,6 +48,7 @@ def test_default_params(lib):
         200, 0, 0, 8, 64)
     assert (p.beta, p.mu) == (2.0, 10.0)
     assert p.refine_eps == pytest.approx(0.1)
+    assert p.merit_kernel == gato.GATO_MERIT_FUSED
 
 
 def test_invalid_arguments_rejected_before_cuda(lib):
@@ -64,6 +65,7 @@ def test_invalid_arguments_rejected_before_cuda(lib):
     p = gato.default_params()
     assert lib.gato_set_timing(None, 1) == gato.GATO_ERR_INVALID_ARG
     assert lib.gato_set_pcg_kernel(None, 0) == gato.GATO_ERR_INVALID_ARG
+    assert lib.gato_set_form_kernel(None, 0) == gato.GATO_ERR_INVALID_ARG
     assert lib.gato_get_stats(None, None) == gato.GATO_ERR_INVALID_ARG
     null = [None] * 8
     assert lib.gato_form_schur(None, *null, None, None) == gato.GATO_ERR_INVALID_ARG

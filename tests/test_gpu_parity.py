@@ -50,12 +50,13 @@ def params_for(w, **kw):
     return gato.default_params(**p)
 
 
-def solve(prob, params, kernel=gato.GATO_PCG_AUTO):
+def solve(prob, params, kernel=gato.GATO_PCG_AUTO, form_kind=gato.GATO_FORM_AUTO):
     M, N, n = prob["Q"].shape[:3]
     m = prob["B"].shape[-1]
     d = gato.to_device(prob)
     with gato.Solver(M, N, n, m) as s:
         s.set_pcg_kernel(kernel)
+        s.set_form_kernel(form_kind)
         out = s.outputs(params.n_alpha)
         s.solve_kkt(params, d, out["dX"], out["dU"], out["lam"], out["iters"], out["merit"],
                     out["best"], out["status"])
@@ -91,7 +92,7 @@ def check_merit(pj, dX, dU, merit, best, n_alpha, beta, mu):
 # formation (a1, a2)
 # --------------------------------------------------------------------------
 
-def form(prob):
+def form(prob, kind=gato.GATO_FORM_AUTO):
     M, N, n = prob["Q"].shape[:3]
     m = prob["B"].shape[-1]
     d = gato.to_device(prob)
@@ -101,6 +102,7 @@ def form(prob):
                Po=torch.empty(M, max(N - 1, 0), n, n, **f))
     status = torch.zeros(M, dtype=torch.int32, device="cuda")
     with gato.Solver(M, N, n, m) as s:
+        s.set_form_kernel(kind)
         s.form_schur(d, status)
         s.get_schur(out["D"], out["O"] if N > 1 else None, out["g"], out["Pd"],
                     out["Po"] if N > 1 else None)
@@ -116,9 +118,10 @@ FORM_CASES = [(w.name, make_batch(w, M=min(w.M, 6))) for w in WORKLOADS] + [
 ]
 
 
+@pytest.mark.parametrize("kind", [gato.GATO_FORM_AUTO, gato.GATO_FORM_SHARED])
 @pytest.mark.parametrize("name,prob", FORM_CASES, ids=[c[0] for c in FORM_CASES])
-def test_form_schur_matches_oracle(name, prob):
-    got, status = form(prob)
+def test_form_schur_matches_oracle(name, prob, kind):
+    got, status = form(prob, kind)
     assert not status.any()
     N = prob["Q"].shape[1]
     for j in range(prob["Q"].shape[0]):
@@ -188,6 +191,15 @@ def test_tile_and_generic_kernels_agree(w):
     check_solution(prob, b, range(4), w.n_alpha, w.beta, w.mu)
 
 
+@pytest.mark.parametrize("w", [WORKLOADS[0], WORKLOADS[2]], ids=lambda w: w.name)
+def test_shared_memory_formation_path_solves(w):
+    prob = make_batch(w, M=4)
+    a = solve(prob, params_for(w), form_kind=gato.GATO_FORM_SHARED)
+    b = solve(prob, params_for(w), form_kind=gato.GATO_FORM_AUTO)
+    check_solution(prob, a, range(4), w.n_alpha, w.beta, w.mu)
+    check_solution(prob, b, range(4), w.n_alpha, w.beta, w.mu)
+
+
 @pytest.mark.parametrize("rule", [gato.GATO_STOP_PRECOND, gato.GATO_STOP_SCALED])
 def test_other_stop_rules(rule):
     w = WORKLOADS[1]
@@ -226,15 +238,33 @@ def test_full_size_sampled(w):
 # --------------------------------------------------------------------------
 
 def test_merit_bit_identical_across_block_sizes():
+    """The per-(knot, candidate) kernel sums rows and knots in a fixed order,
+    so its merits are bit-identical at any block size."""
     w = WORKLOADS[1]
     prob = make_batch(w, M=4)
     ref = None
     for mt in (32, 64, 128, 256):
-        out = solve(prob, params_for(w, merit_threads=mt))
+        out = solve(prob, params_for(w, merit_threads=mt,
+                                     merit_kernel=gato.GATO_MERIT_PER_CANDIDATE))
         if ref is None:
             ref = out
         assert np.array_equal(out["merit"], ref["merit"])
         assert np.array_equal(out["best"], ref["best"])
+    check_solution(prob, ref, range(4), w.n_alpha, w.beta, w.mu)
+
+
+@pytest.mark.parametrize("w", [WORKLOADS[0], WORKLOADS[3], WORKLOADS[4]], ids=lambda w: w.name)
+def test_merit_kernels_agree(w):
+    """Fused (factored) and per-candidate (full formula) merit kernels agree
+    within the merit tolerance and pick the same step."""
+    prob = make_batch(w, M=min(w.M, 6))
+    a = solve(prob, params_for(w, merit_kernel=gato.GATO_MERIT_FUSED))
+    b = solve(prob, params_for(w, merit_kernel=gato.GATO_MERIT_PER_CANDIDATE))
+    for j in range(a["merit"].shape[0]):
+        scale = np.abs(b["merit"][j]).max()
+        assert np.abs(a["merit"][j] - b["merit"][j]).max() <= TOL_MERIT * scale
+    np.testing.assert_array_equal(a["best"], b["best"])
+    np.testing.assert_array_equal(a["dX"], b["dX"])
 
 
 def test_deterministic_and_batch_position_invariant():
@@ -269,8 +299,9 @@ def test_separate_entry_points_equal_solve_kkt():
 # line search on given steps, update, warm start
 # --------------------------------------------------------------------------
 
+@pytest.mark.parametrize("kernel", [0, 1])
 @pytest.mark.parametrize("scale", [2.5, 6.0, -1.0])
-def test_linesearch_on_scaled_steps(scale):
+def test_linesearch_on_scaled_steps(scale, kernel):
     w = WORKLOADS[1]
     prob = make_batch(w, M=4)
     d = gato.to_device(prob)
@@ -278,7 +309,7 @@ def test_linesearch_on_scaled_steps(scale):
     dU = np.stack([oracle.direct_solve(oracle.solve_one(prob, j))[1] for j in range(4)])
     dXt = torch.tensor(scale * dX, dtype=torch.float32, device="cuda")
     dUt = torch.tensor(scale * dU, dtype=torch.float32, device="cuda")
-    p = params_for(w)
+    p = params_for(w, merit_kernel=kernel)
     with gato.Solver(4, w.N, w.n, w.m) as s:
         o = s.outputs(p.n_alpha)
         s.linesearch(p, d, dXt, dUt, o["merit"], o["best"], o["status"])
@@ -365,7 +396,7 @@ def test_invalid_parameters_rejected():
     w = WORKLOADS[0]
     prob = make_batch(w, M=1)
     for bad in (dict(merit_threads=48), dict(n_alpha=0), dict(beta=1.0), dict(stop_rule=7),
-                dict(pcg_max_iters=-1)):
+                dict(pcg_max_iters=-1), dict(merit_kernel=5), dict(refine_eps=-1.0)):
         with pytest.raises(gato.GatoError) as e:
             solve(prob, params_for(w, **bad))
         assert e.value.code == gato.GATO_ERR_INVALID_ARG

@@ -1,0 +1,408 @@
+// form_rows.cu -- Schur complement and stair preconditioner formation for
+// n, m <= 16 with the small matrices held in registers (GATO paper, Sec. II
+// eqs. (4)-(6); Sec. III block-local formation with a grid-wide sync before
+// Phi^-1 is final).
+//
+// Each half-warp (16 lanes) works on one knot; lane l holds row l of the
+// current matrix (16 floats, rows >= n are identity rows so that every
+// factorisation acts on diag(M, I)).  Cholesky runs right-looking with
+// half-warp shuffles; finished rows are published to a 16 x 16 scratch in
+// shared memory, from which the other lanes read them with 128-bit loads for
+// the triangular inverse and the small products.  Three launches, as in the
+// shared-memory kernels, with the same outputs:
+//   k_rows_knot  knot k:  Q_k^-1, R_k^-1, S_{k+1,k} = -A_k Q_k^-1,
+//                         V_k = B_k R_k^-1, and theta_k = A_k Q_k^-1 A_k^T +
+//                         V_k B_k^T (stored where S_{k+1,k+1} goes)
+//   k_rows_diag  row j:   S_jj = Q_j^-1 + theta_{j-1}, L_j, L_j^-1, S_jj^-1 and
+//                         the eigenvalue bound 1 / ||L_j^-1||_F^2
+//   k_rows_off   row j:   Nhat_j = L_j^-1 S_{j,j-1} L_{j-1}^-T and the explicit
+//                         Phi^-1 block -S_jj^-1 S_{j,j-1} S_{j-1,j-1}^-1
+#include "gato_internal.cuh"
+
+namespace gato {
+namespace {
+
+constexpr int NP = 16;          // padded order
+constexpr int kKnotsPerBlock = 16;  // 8 warps, two knots each
+
+__device__ __forceinline__ float shfl16(float v, int src)
+{
+    return __shfl_sync(0xffffffffu, v, src, 16);
+}
+
+// a[li] (runtime li) without dynamic register indexing
+__device__ __forceinline__ float pick(const float (&a)[NP], int li)
+{
+    float v = 0.f;
+#pragma unroll
+    for (int j = 0; j < NP; ++j) v = (j == li) ? a[j] : v;
+    return v;
+}
+
+// Row li of a rows x cols row-major global matrix into a (zero beyond cols);
+// rows >= `rows` become identity rows when `ident`, zero rows otherwise.
+__device__ __forceinline__ void load_row(float (&a)[NP], const float* M, int rows, int cols,
+                                         int li, bool ident)
+{
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        float v = 0.f;
+        if (li < rows) {
+            if (j < cols) v = M[li * cols + j];
+        } else if (ident && j == li) {
+            v = 1.f;
+        }
+        a[j] = v;
+    }
+}
+
+__device__ __forceinline__ void store_row(const float (&a)[NP], float* M, int rows, int cols,
+                                          int li, float s = 1.f)
+{
+    if (li < rows) {
+#pragma unroll
+        for (int j = 0; j < NP; ++j)
+            if (j < cols) M[li * cols + j] = s * a[j];
+    }
+}
+
+// publish row li into the 16 x 16 scratch S (row stride 16)
+__device__ __forceinline__ void publish(const float (&a)[NP], float* S, int li)
+{
+    float4* d = reinterpret_cast<float4*>(S + li * NP);
+    d[0] = make_float4(a[0], a[1], a[2], a[3]);
+    d[1] = make_float4(a[4], a[5], a[6], a[7]);
+    d[2] = make_float4(a[8], a[9], a[10], a[11]);
+    d[3] = make_float4(a[12], a[13], a[14], a[15]);
+}
+
+__device__ __forceinline__ void fetch(float (&b)[NP], const float* S, int k)
+{
+    const float4* s = reinterpret_cast<const float4*>(S + k * NP);
+    const float4 s0 = s[0], s1 = s[1], s2 = s[2], s3 = s[3];
+    b[0] = s0.x; b[1] = s0.y; b[2] = s0.z; b[3] = s0.w;
+    b[4] = s1.x; b[5] = s1.y; b[6] = s1.z; b[7] = s1.w;
+    b[8] = s2.x; b[9] = s2.y; b[10] = s2.z; b[11] = s2.w;
+    b[12] = s3.x; b[13] = s3.y; b[14] = s3.z; b[15] = s3.w;
+}
+
+// In-register Cholesky of diag(M, I) (M of order n): a becomes row li of L,
+// strict upper part zeroed.  A pivot <= 0 or not finite is flagged (false)
+// and replaced by 1.
+__device__ bool rows_cholesky(float (&a)[NP], int li, int n)
+{
+    bool ok = true;
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+        if (k < n) {
+            const float d = shfl16(a[k], k);
+            const bool bad = !(d > 0.f) || !isfinite(d);
+            ok = ok && !bad;
+            const float s = bad ? 1.f : sqrtf(d);
+            const float inv = 1.f / s;
+            a[k] = (li == k) ? s : (li > k ? a[k] * inv : a[k]);
+#pragma unroll
+            for (int j = k + 1; j < NP; ++j) {
+                if (j < n) {
+                    const float ljk = shfl16(a[k], j);
+                    if (li >= j) a[j] -= a[k] * ljk;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < NP; ++j)
+        if (j > li) a[j] = 0.f;
+    return ok;
+}
+
+// x = row li of L^-1 (L lower, rows in a); the finished rows of L^-1 end up
+// in the scratch S.
+__device__ void rows_lower_inverse(const float (&a)[NP], float (&x)[NP], int li, int n, float* S)
+{
+#pragma unroll
+    for (int j = 0; j < NP; ++j) x[j] = (j == li) ? 1.f : 0.f;
+    const float inv_diag = 1.f / pick(a, li);
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+        if (k < n) {
+            if (li == k) {
+#pragma unroll
+                for (int j = 0; j < NP; ++j) x[j] *= inv_diag;
+                publish(x, S, k);
+            }
+            __syncwarp();
+            if (li > k) {
+                float xk[NP];
+                fetch(xk, S, k);
+                const float lik = a[k];
+#pragma unroll
+                for (int j = 0; j < NP; ++j) x[j] -= lik * xk[j];
+            }
+        }
+    }
+    if (li >= n) publish(x, S, li);  // identity rows, so S holds all of diag(L^-1, I)
+    __syncwarp();
+}
+
+// c = row li of X^T X, the rows of X in the scratch S (X lower triangular)
+__device__ __forceinline__ void rows_gram_lower(const float* S, float (&c)[NP], int li, int n)
+{
+#pragma unroll
+    for (int j = 0; j < NP; ++j) c[j] = 0.f;
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+        if (k < n && k >= li) {
+            float xk[NP];
+            fetch(xk, S, k);
+            const float xki = pick(xk, li);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) c[j] += xki * xk[j];
+        }
+    }
+}
+
+// c = s * (row li of A) * B, B's rows (kk of them) in the scratch S
+__device__ __forceinline__ void rows_mul(const float (&a)[NP], const float* S, int kk,
+                                         float (&c)[NP], float s)
+{
+#pragma unroll
+    for (int j = 0; j < NP; ++j) c[j] = 0.f;
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+        if (k < kk) {
+            float bk[NP];
+            fetch(bk, S, k);
+            const float ak = s * a[k];
+#pragma unroll
+            for (int j = 0; j < NP; ++j) c[j] += ak * bk[j];
+        }
+    }
+}
+
+// c[j] += s * dot(row li of A, row j of B), B's rows (count of them) in S
+__device__ __forceinline__ void rows_mul_bt(const float (&a)[NP], const float* S, int count,
+                                            float (&c)[NP], float s)
+{
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        if (j < count) {
+            float bj[NP];
+            fetch(bj, S, j);
+            float d = 0.f;
+#pragma unroll
+            for (int k = 0; k < NP; ++k) d += a[k] * bj[k];
+            c[j] += s * d;
+        }
+    }
+}
+
+struct Half {
+    int li;        // lane within the half-warp (row index)
+    long item;     // knot (or block row) index over the batch
+    bool active;
+    float* S0;
+    float* S1;
+};
+
+__device__ __forceinline__ Half half_setup(long items, float* sm)
+{
+    Half h;
+    const int lane = lane_id(), warp = threadIdx.x >> 5;
+    const int half = (warp << 1) | (lane >> 4);
+    h.li = lane & 15;
+    h.item = (long)blockIdx.x * kKnotsPerBlock + half;
+    h.active = h.item < items;
+    h.S0 = sm + (size_t)half * 2 * NP * NP;
+    h.S1 = h.S0 + NP * NP;
+    return h;
+}
+
+__global__ void __launch_bounds__(256) k_rows_knot(Work w, const float* __restrict__ Q,
+                                                   const float* __restrict__ R,
+                                                   const float* __restrict__ A,
+                                                   const float* __restrict__ B, uint32_t* status)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int n = w.n, m = w.m, N = w.N;
+    const Half h = half_setup((long)w.M * N, sm);
+    // inactive halves run the same code on identity data so that every lane
+    // of the warp takes part in the shuffles and barriers; they store nothing
+    const long item = h.active ? h.item : 0;
+    const int sol = (int)(item / N), k = (int)(item % N);
+    const size_t K = (size_t)(N - 1);
+    // the last knot has no control: its half still runs the control part (on
+    // knot 0's data of the same solve, when there is one) so that the warp's
+    // shuffles and barriers stay uniform, but stores nothing from it
+    const bool has_u = k < N - 1;
+    const bool store_u = h.active && has_u && N > 1;
+    const int ku = has_u ? k : 0;
+    const int li = h.li;
+
+    float a[NP], x[NP], c[NP];
+    // Q_k^-1
+    load_row(a, Q + ((size_t)sol * N + k) * n * n, n, n, li, true);
+    bool ok = rows_cholesky(a, li, n);
+    rows_lower_inverse(a, x, li, n, h.S0);
+    rows_gram_lower(h.S0, c, li, n);  // row li of Q_k^-1
+    if (h.active) store_row(c, w.Qinv + sol * w.sNnn + (size_t)k * n * n, n, n, li);
+    __syncwarp();
+    publish(c, h.S1, li);  // Q_k^-1 rows
+    __syncwarp();
+    // O = S_{k+1,k} = -A_k Q_k^-1
+    float arow[NP], o[NP];
+    const bool dyn = N > 1;  // a single-knot problem has no A, B, R
+    if (dyn) {
+        load_row(arow, A + ((size_t)sol * K + ku) * n * n, n, n, li, false);
+    } else {
+#pragma unroll
+        for (int j = 0; j < NP; ++j) arow[j] = 0.f;
+    }
+    rows_mul(arow, h.S1, n, o, -1.f);
+    if (store_u) store_row(o, w.O + sol * w.sKnn + (size_t)k * n * n, n, n, li);
+    // R_k^-1
+    if (dyn) {
+        load_row(a, R + ((size_t)sol * K + ku) * m * m, m, m, li, true);
+    } else {
+#pragma unroll
+        for (int j = 0; j < NP; ++j) a[j] = (j == li) ? 1.f : 0.f;
+    }
+    const bool okr = rows_cholesky(a, li, m);
+    if (has_u) ok = ok && okr;
+    __syncwarp();
+    rows_lower_inverse(a, x, li, m, h.S0);
+    rows_gram_lower(h.S0, c, li, m);  // row li of R_k^-1
+    if (store_u) store_row(c, w.Rinv + sol * w.sKmm + (size_t)k * m * m, m, m, li);
+    __syncwarp();
+    publish(c, h.S1, li);  // R_k^-1 rows
+    __syncwarp();
+    // V = B_k R_k^-1
+    float brow[NP], v[NP];
+    if (dyn) {
+        load_row(brow, B + ((size_t)sol * K + ku) * n * m, n, m, li, false);
+    } else {
+#pragma unroll
+        for (int j = 0; j < NP; ++j) brow[j] = 0.f;
+    }
+    rows_mul(brow, h.S1, m, v, 1.f);
+    if (store_u) store_row(v, w.V + sol * w.sKnm + (size_t)k * n * m, n, m, li);
+    // theta_k = A Q^-1 A^T + V B^T = -O A^T + V B^T  (into S_{k+1,k+1}'s slot)
+    __syncwarp();
+    publish(arow, h.S0, li);
+    publish(brow, h.S1, li);
+    __syncwarp();
+    float t[NP];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) t[j] = 0.f;
+    rows_mul_bt(o, h.S0, n, t, -1.f);
+    rows_mul_bt(v, h.S1, n, t, 1.f);
+    if (store_u) store_row(t, w.D + sol * w.sNnn + (size_t)(k + 1) * n * n, n, n, li);
+    if (h.active && !ok && li == 0) atomicOr(status + sol, GATO_STATUS_NONPOSITIVE_PIVOT);
+}
+
+__global__ void __launch_bounds__(256) k_rows_diag(Work w, uint32_t* status)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int n = w.n, N = w.N;
+    const Half h = half_setup((long)w.M * N, sm);
+    const long item = h.active ? h.item : 0;
+    const int sol = (int)(item / N), j = (int)(item % N);
+    const int li = h.li;
+    const size_t off = sol * w.sNnn + (size_t)j * n * n;
+
+    float d[NP], q[NP];
+    load_row(q, w.Qinv + off, n, n, li, false);
+    if (j > 0) {
+        load_row(d, w.D + off, n, n, li, false);  // theta_{j-1}
+#pragma unroll
+        for (int c = 0; c < NP; ++c) d[c] += q[c];
+    } else {
+#pragma unroll
+        for (int c = 0; c < NP; ++c) d[c] = q[c];
+    }
+    __syncwarp();
+    if (h.active) store_row(d, w.D + off, n, n, li);
+    if (li >= n) {
+#pragma unroll
+        for (int c = 0; c < NP; ++c) d[c] = (c == li) ? 1.f : 0.f;
+    }
+    const bool ok = rows_cholesky(d, li, n);
+    if (h.active) store_row(d, w.L + off, n, n, li);
+    float x[NP], c[NP];
+    rows_lower_inverse(d, x, li, n, h.S0);
+    if (h.active) store_row(x, w.Linv + off, n, n, li);
+    // ||L_j^-1||_F^2 = trace(S_jj^-1) >= 1 / lambda_min(S_jj)
+    float f = 0.f;
+#pragma unroll
+    for (int k = 0; k < NP; ++k) f += (li < n) ? x[k] * x[k] : 0.f;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) f += __shfl_xor_sync(0xffffffffu, f, o, 16);
+    if (h.active && li == 0) w.dlow[sol * w.sN + j] = 1.f / f;
+    rows_gram_lower(h.S0, c, li, n);
+    if (h.active) store_row(c, w.Pd + off, n, n, li);
+    if (h.active && !ok && li == 0) atomicOr(status + sol, GATO_STATUS_NONPOSITIVE_PIVOT);
+}
+
+__global__ void __launch_bounds__(256) k_rows_off(Work w)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int n = w.n, N = w.N, K = N - 1;
+    const Half h = half_setup((long)w.M * K, sm);
+    const long item = h.active ? h.item : 0;
+    const int sol = (int)(item / K), j = 1 + (int)(item % K);
+    const int li = h.li;
+    const size_t dj = sol * w.sNnn + (size_t)j * n * n, dp = dj - (size_t)n * n;
+    const size_t oj = sol * w.sKnn + (size_t)(j - 1) * n * n;
+
+    float a[NP], t[NP], r[NP];
+    // Nhat_j = (L_j^-1 S_{j,j-1}) L_{j-1}^-T
+    load_row(a, w.O + oj, n, n, li, false);
+    publish(a, h.S0, li);  // S_{j,j-1} rows
+    load_row(a, w.Linv + dp, n, n, li, false);
+    publish(a, h.S1, li);  // L_{j-1}^-1 rows
+    __syncwarp();
+    load_row(a, w.Linv + dj, n, n, li, false);
+    rows_mul(a, h.S0, n, t, 1.f);
+#pragma unroll
+    for (int c = 0; c < NP; ++c) r[c] = 0.f;
+    rows_mul_bt(t, h.S1, n, r, 1.f);
+    if (h.active) store_row(r, w.Nh + oj, n, n, li);
+    // Phi^-1 block: -(S_jj^-1 S_{j,j-1}) S_{j-1,j-1}^-1
+    __syncwarp();
+    load_row(a, w.Pd + dp, n, n, li, false);
+    publish(a, h.S1, li);  // S_{j-1,j-1}^-1 rows
+    __syncwarp();
+    load_row(a, w.Pd + dj, n, n, li, false);
+    rows_mul(a, h.S0, n, t, 1.f);
+    // (T S_{j-1,j-1}^-1) row li: sum_k T[li][k] Pd_{j-1}[k][:]
+    rows_mul(t, h.S1, n, r, -1.f);
+    if (h.active) store_row(r, w.Po + oj, n, n, li);
+}
+
+template <typename K, typename... Args>
+cudaError_t launch_rows(K kernel, long items, cudaStream_t st, Args... args)
+{
+    if (items <= 0) return cudaSuccess;
+    const size_t smem = (size_t)kKnotsPerBlock * 2 * NP * NP * sizeof(float);  // 32 KB
+    const long blocks = (items + kKnotsPerBlock - 1) / kKnotsPerBlock;
+    kernel<<<(unsigned)blocks, 256, smem, st>>>(args...);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool rows_formation_supported(const Work& w) { return w.n <= NP && w.m <= NP; }
+
+cudaError_t launch_form_rows(gato_handle* h, const float* Q, const float* R, const float* A,
+                             const float* B, uint32_t* status, cudaStream_t st)
+{
+    const Work& w = h->w;
+    const long knots = (long)w.M * w.N;
+    cudaError_t e = launch_rows(k_rows_knot, knots, st, w, Q, R, A, B, status);
+    if (e != cudaSuccess) return e;
+    e = launch_rows(k_rows_diag, knots, st, w, status);
+    if (e != cudaSuccess) return e;
+    return launch_rows(k_rows_off, (long)w.M * (w.N - 1), st, w);
+}
+
+}  // namespace gato

@@ -28,6 +28,8 @@ bool params_ok(const gato_params* p)
     if (!(p->beta > 1.f) || !(p->mu >= 0.f)) return false;
     if (p->merit_threads < 32 || p->merit_threads > 256 || p->merit_threads % 32) return false;
     if (!(p->refine_eps >= 0.f)) return false;
+    if (p->merit_kernel != GATO_MERIT_FUSED && p->merit_kernel != GATO_MERIT_PER_CANDIDATE)
+        return false;
     return true;
 }
 
@@ -70,6 +72,7 @@ void gato_default_params(gato_params* p)
     p->mu = 10.f;
     p->merit_threads = 64;
     p->refine_eps = 0.1f;
+    p->merit_kernel = GATO_MERIT_FUSED;
 }
 
 int gato_create(gato_handle** out, int M, int N, int n, int m)
@@ -113,6 +116,7 @@ int gato_create(gato_handle** out, int M, int N, int n, int m)
     size_t total = 0;
     for (int i = 0; i < nf; ++i) total += strides[i] * (size_t)M;
     total += 2 * w.sK2 * (size_t)M;  // merit partials
+    total += 64;                     // work counters
     h->bytes = total * sizeof(float);
     if (cudaMalloc(&h->base, h->bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -125,6 +129,7 @@ int gato_create(gato_handle** out, int M, int N, int n, int m)
         cur += strides[i] * (size_t)M;
     }
     w.mpart = (float2*)cur;
+    w.queue = (int*)(cur + 2 * w.sK2 * (size_t)M);
     for (int i = 0; i < 5; ++i) {
         if (cudaEventCreate(&h->ev[i]) != cudaSuccess) {
             for (int j = 0; j < i; ++j) cudaEventDestroy(h->ev[j]);
@@ -133,7 +138,8 @@ int gato_create(gato_handle** out, int M, int N, int n, int m)
             return GATO_ERR_CUDA;
         }
     }
-    h->last.form_us = h->last.pcg_us = h->last.merit_us = h->last.total_us = -1.f;
+    h->last.form_us = h->last.pcg_us = h->last.refine_us = h->last.merit_us = h->last.total_us =
+        -1.f;
     *out = h;
     return GATO_OK;
 }
@@ -160,11 +166,18 @@ int gato_set_pcg_kernel(gato_handle* h, int kind)
     return GATO_OK;
 }
 
+int gato_set_form_kernel(gato_handle* h, int kind)
+{
+    if (!h || (kind != GATO_FORM_AUTO && kind != GATO_FORM_SHARED)) return GATO_ERR_INVALID_ARG;
+    h->force_smem_form = kind == GATO_FORM_SHARED;
+    return GATO_OK;
+}
+
 int gato_get_stats(gato_handle* h, gato_stats* out)
 {
     if (!h || !out) return GATO_ERR_INVALID_ARG;
     gato_stats s;
-    s.form_us = s.pcg_us = s.merit_us = s.total_us = -1.f;
+    s.form_us = s.pcg_us = s.refine_us = s.merit_us = s.total_us = -1.f;
     if (h->timing && h->ev_used[0]) {
         int last = 0;
         for (int i = 4; i > 0; --i)
@@ -173,7 +186,7 @@ int gato_get_stats(gato_handle* h, gato_stats* out)
         float ms;
         // stage i runs between the previous recorded event and event i
         int prev = 0;
-        float* dst[5] = {nullptr, &s.form_us, &s.pcg_us, &s.merit_us, nullptr};
+        float* dst[5] = {nullptr, &s.form_us, &s.pcg_us, &s.refine_us, &s.merit_us};
         for (int i = 1; i < 5; ++i) {
             if (!h->ev_used[i]) continue;
             if (dst[i] && cudaEventElapsedTime(&ms, h->ev[prev], h->ev[i]) == cudaSuccess)
@@ -251,7 +264,7 @@ int gato_linesearch(gato_handle* h, const gato_params* p, const float* Q, const 
     begin_timing(h, st);
     cudaError_t err =
         gato::launch_merit(h, p, Q, R, q, r, A, B, e, s0, dX, dU, merit, best, status, st);
-    record(h, 3, st);
+    record(h, 4, st);
     return cuda_fail(err);
 }
 
@@ -273,6 +286,7 @@ int gato_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const f
     record(h, 1, st);
     if (err == cudaSuccess)
         err = gato::launch_pcg_ex(h, p, 0, nullptr, lambda, dX, dU, iters, 0, status, st);
+    record(h, 2, st);
     gato_params pc = *p;  // corrections are solved to refine_eps
     if (p->refine_eps > 0.f) pc.pcg_eps = p->refine_eps;
     for (int k = 0; k < p->refine_steps && err == cudaSuccess; ++k) {
@@ -283,10 +297,10 @@ int gato_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const f
             err = gato::launch_pcg_ex(h, &pc, 1, nullptr, w.dlam, w.ddX, w.ddU, iters, 1, status, st);
         if (err == cudaSuccess) err = gato::launch_accumulate(h, lambda, dX, dU, iters, st);
     }
-    record(h, 2, st);
+    if (p->refine_steps > 0) record(h, 3, st);
     if (err == cudaSuccess)
         err = gato::launch_merit(h, p, Q, R, q, r, A, B, e, s0, dX, dU, merit, best, status, st);
-    record(h, 3, st);
+    record(h, 4, st);
     if (err == cudaErrorInvalidConfiguration) return GATO_ERR_UNSUPPORTED;
     return cuda_fail(err);
 }

@@ -62,6 +62,7 @@ struct Work {
     float* ddU;    // [N-1][m]
     // line search partial sums
     float2* mpart; // [(A+1)][N] (cost, violation) per knot and candidate
+    int* queue;    // work counters of the persistent kernels (not per solve)
 };
 
 }  // namespace gato
@@ -75,7 +76,8 @@ struct gato_handle {
     size_t bytes;
     int timing;
     int force_generic_pcg;  // GATO_PCG_GENERIC selected by gato_set_pcg_kernel
-    cudaEvent_t ev[5];  // start, after form, after pcg, after merit, end
+    int force_smem_form;    // GATO_FORM_SHARED selected by gato_set_form_kernel
+    cudaEvent_t ev[5];  // start, after form, after PCG, after refinement, after merit
     int ev_used[5];
     gato_stats last;
 };
@@ -88,6 +90,10 @@ namespace gato {
 cudaError_t launch_form_matrices(gato_handle* h, const float* Q, const float* R,
                                  const float* A, const float* B, uint32_t* status,
                                  cudaStream_t st);
+// register formation for n, m <= 16 (form_rows.cu)
+bool rows_formation_supported(const Work& w);
+cudaError_t launch_form_rows(gato_handle* h, const float* Q, const float* R, const float* A,
+                             const float* B, uint32_t* status, cudaStream_t st);
 cudaError_t launch_form_rhs(gato_handle* h, int set, const float* q, const float* r,
                             const float* e, const float* s0, size_t s0_stride, cudaStream_t st);
 cudaError_t launch_pcg(gato_handle* h, const gato_params* p, const float* lambda0,

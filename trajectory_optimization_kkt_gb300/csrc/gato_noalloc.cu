@@ -89,6 +89,8 @@ size_t carve(Work& w, int M, int N, int n, int m, float* base)
     }
     if (base) w.mpart = (float2*)(base + total);
     total += 2 * w.sK2 * (size_t)M;
+    if (base) w.queue = (int*)(base + total);
+    total += 64;  // work counters
     return total * sizeof(float);
 }
 
@@ -102,6 +104,8 @@ bool params_ok(const gato_params* p)
     if (!(p->beta > 1.f) || !(p->mu >= 0.f)) return false;
     if (p->merit_threads < 32 || p->merit_threads > 256 || p->merit_threads % 32) return false;
     if (!(p->refine_eps >= 0.f)) return false;
+    if (p->merit_kernel != GATO_MERIT_FUSED && p->merit_kernel != GATO_MERIT_PER_CANDIDATE)
+        return false;
     return true;
 }
 

@@ -13,6 +13,14 @@
 //                 fixed order (lane-strided partials, xor butterfly), merit =
 //                 cost + mu * violation, argmin with ties to the lower index,
 //                 acceptance against alpha = 0.
+// k_merit_fused   (default) one block per solve: each warp streams a fixed
+//                 set of knots once, lanes over the rows of a knot, and keeps
+//                 the candidate-independent pieces c2 = x^T Q x + u^T R u,
+//                 c1 = q^T x + r^T u and w = A x + B u - x_next of the full
+//                 step; every candidate then costs 1/2 alpha^2 c2 + alpha c1
+//                 + mu sum |e + alpha w| (+ mu sum |alpha x_0 - s0|), the
+//                 factored form of the same merit.  Knot sums in a fixed
+//                 order; the block reduction, argmin and acceptance follow.
 // k_apply_step    X += alpha* dX, U += alpha* dU.
 #include "gato_internal.cuh"
 
@@ -139,6 +147,125 @@ __global__ void k_merit_reduce(Work w, int A1, float mu, float* merit, int32_t* 
     }
 }
 
+constexpr int kMaxA1 = GATO_MAX_ALPHA + 1;
+
+__global__ void __launch_bounds__(512) k_merit_fused(MeritArgs g, float mu, float* merit,
+                                                     int32_t* best, uint32_t* status)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int N = g.w.N, n = g.w.n, m = g.w.m, A1 = g.A1;
+    const int sol = blockIdx.x, lane = lane_id(), warp = threadIdx.x >> 5;
+    const int nw = blockDim.x >> 5;
+    const size_t K = (size_t)(N - 1);
+    float* xv = sm + (size_t)warp * (2 * n + m);  // x_k, x_{k+1}, u_k of this warp's knot
+    float* xn = xv + n;
+    float* uv = xn + n;
+    float* part = sm + (size_t)nw * (2 * n + m);  // [nw][A1 + 2] warp partials
+
+    float alpha[kMaxA1];
+#pragma unroll
+    for (int i = 0; i < kMaxA1; ++i) alpha[i] = i < A1 ? candidate_alpha(i, g.beta) : 0.f;
+    float viol[kMaxA1];
+#pragma unroll
+    for (int i = 0; i < kMaxA1; ++i) viol[i] = 0.f;
+    float c1 = 0.f, c2 = 0.f;
+
+    const float* dXs = g.dX + (size_t)sol * N * n;
+    const float* s0 = g.s0 + (size_t)sol * n;
+    for (int k = warp; k < N; k += nw) {
+        const bool has_u = k < N - 1;
+        for (int i = lane; i < n; i += 32) {
+            xv[i] = dXs[(size_t)k * n + i];
+            xn[i] = has_u ? dXs[(size_t)(k + 1) * n + i] : 0.f;
+        }
+        for (int i = lane; i < m; i += 32)
+            uv[i] = has_u ? g.dU[((size_t)sol * K + k) * m + i] : 0.f;
+        __syncwarp();
+        const float* Qk = g.Q + ((size_t)sol * N + k) * n * n;
+        const float* qk = g.q + ((size_t)sol * N + k) * n;
+        for (int a = lane; a < n; a += 32) {
+            float qx = 0.f;
+            for (int b = 0; b < n; ++b) qx += Qk[a * n + b] * xv[b];
+            c2 += xv[a] * qx;
+            c1 += qk[a] * xv[a];
+            if (has_u) {
+                const float* Ak = g.A + ((size_t)sol * K + k) * n * n;
+                const float* Bk = g.B + ((size_t)sol * K + k) * n * m;
+                const float ea = g.e[((size_t)sol * K + k) * n + a];
+                float wa = -xn[a];
+                for (int b = 0; b < n; ++b) wa += Ak[a * n + b] * xv[b];
+                for (int b = 0; b < m; ++b) wa += Bk[a * m + b] * uv[b];
+#pragma unroll
+                for (int i = 0; i < kMaxA1; ++i)
+                    if (i < A1) viol[i] += fabsf(ea + alpha[i] * wa);
+            }
+            if (k == 0) {
+#pragma unroll
+                for (int i = 0; i < kMaxA1; ++i)
+                    if (i < A1) viol[i] += fabsf(alpha[i] * xv[a] - s0[a]);
+            }
+        }
+        if (has_u) {
+            const float* Rk = g.R + ((size_t)sol * K + k) * m * m;
+            const float* rk = g.r + ((size_t)sol * K + k) * m;
+            for (int c = lane; c < m; c += 32) {
+                float ru = 0.f;
+                for (int b = 0; b < m; ++b) ru += Rk[c * m + b] * uv[b];
+                c2 += uv[c] * ru;
+                c1 += rk[c] * uv[c];
+            }
+        }
+        __syncwarp();
+    }
+    // warp sums, then block sums in warp order
+    c1 = warp_sum(c1);
+    c2 = warp_sum(c2);
+#pragma unroll
+    for (int i = 0; i < kMaxA1; ++i)
+        if (i < A1) viol[i] = warp_sum(viol[i]);
+    if (lane == 0) {
+        float* pw = part + (size_t)warp * (A1 + 2);
+        pw[0] = c1;
+        pw[1] = c2;
+#pragma unroll
+        for (int i = 0; i < kMaxA1; ++i)
+            if (i < A1) pw[2 + i] = viol[i];
+    }
+    __syncthreads();
+    float* smer = part + (size_t)nw * (A1 + 2);  // [A1]
+    if (threadIdx.x < A1) {
+        const int i = threadIdx.x;
+        float C1 = 0.f, C2 = 0.f, V = 0.f;
+        for (int q = 0; q < nw; ++q) {
+            const float* pw = part + (size_t)q * (A1 + 2);
+            C1 += pw[0];
+            C2 += pw[1];
+            V += pw[2 + i];
+        }
+        const float a = candidate_alpha(i, g.beta);
+        const float mv = 0.5f * a * a * C2 + a * C1 + mu * V;
+        smer[i] = mv;
+        merit[(size_t)sol * A1 + i] = mv;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int b = 0;
+        bool finite = isfinite(smer[0]);
+        for (int i = 1; i < A1; ++i) {
+            finite = finite && isfinite(smer[i]);
+            if (smer[i] < smer[1 + b]) b = i - 1;
+        }
+        uint32_t st = 0;
+        if (!finite) st |= GATO_STATUS_NONFINITE;
+        if (!(smer[1 + b] < smer[0])) {
+            b = -1;
+            st |= GATO_STATUS_LINESEARCH_FAILED;
+        }
+        best[sol] = b;
+        if (st) atomicOr(status + sol, st);
+    }
+}
+
 __global__ void k_apply_step(Work w, float beta, const int32_t* best, const float* dX,
                              const float* dU, float* X, float* U)
 {
@@ -169,6 +296,15 @@ cudaError_t launch_merit(gato_handle* h, const gato_params* p, const float* Q,
     a.dX = dX; a.dU = dU;
     a.A1 = p->n_alpha + 1;
     a.beta = p->beta;
+    if (p->merit_kernel == GATO_MERIT_FUSED) {
+        int warps = (w.N + 7) / 8;  // about eight knots per warp
+        if (warps > 16) warps = 16;
+        if (warps < 1) warps = 1;
+        const size_t smem =
+            ((size_t)warps * (2 * w.n + w.m) + (size_t)warps * (a.A1 + 2) + a.A1) * sizeof(float);
+        k_merit_fused<<<w.M, 32 * warps, smem, st>>>(a, p->mu, merit, best, status);
+        return cudaGetLastError();
+    }
     const size_t smem = (size_t)(5 * w.n + 2 * w.m) * sizeof(float);
     dim3 grid(w.N, a.A1, w.M);
     k_merit<<<grid, p->merit_threads, smem, st>>>(a);

@@ -45,6 +45,7 @@ struct PcgArgs {
     int nh_smem;     // generic kernel: Nhat staged in shared memory
     int l_smem;      // packed L staged in shared memory (rule 0 only)
     int acc_iters;   // add to iters instead of storing
+    int* queue;      // tiled kernel: next-solve counter, zero at launch
 };
 
 __host__ __device__ __forceinline__ size_t round4(size_t x) { return (x + 3) & ~(size_t)3; }
@@ -75,21 +76,43 @@ __device__ __forceinline__ void block_sum(float (&v)[K], float4* buf)
 }
 
 // Warp partial sums written before a barrier and summed by every thread after
-// it (deterministic).  buf holds 32 float2.
+// it, in a fixed order (deterministic).  buf holds up to 16 float2 (one per
+// warp).  post2 reduces two values at the cost of one: the first exchange
+// leaves the pair sums of a in the low half-warp and those of b in the high
+// half, the remaining four steps run on one value per lane.
 __device__ __forceinline__ void post2(float a, float b, float2* buf)
 {
+    const int lane = lane_id();
+    const bool hi = lane & 16;
+    float keep = hi ? b : a;
+    keep += __shfl_xor_sync(0xffffffffu, hi ? a : b, 16);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+    float* slot = reinterpret_cast<float*>(buf + (threadIdx.x >> 5));
+    if ((lane & 15) == 0) slot[hi ? 1 : 0] = keep;
+}
+
+// one value into the .x (y = false) or .y (y = true) field of the warp's slot
+__device__ __forceinline__ void post1(float a, float2* buf, bool y)
+{
     a = warp_sum(a);
-    b = warp_sum(b);
-    if (lane_id() == 0) buf[threadIdx.x >> 5] = make_float2(a, b);
+    float* slot = reinterpret_cast<float*>(buf + (threadIdx.x >> 5));
+    if (lane_id() == 0) slot[y ? 1 : 0] = a;
 }
 
 __device__ __forceinline__ float2 collect2(const float2* buf)
 {
-    // lane q reads warp q's partials; the xor butterfly gives every lane of
-    // every warp the same, order-fixed total
-    const int q = lane_id();
-    const float2 t = q < (int)(blockDim.x >> 5) ? buf[q] : make_float2(0.f, 0.f);
-    return make_float2(warp_sum(t.x), warp_sum(t.y));
+    // the low half-warp sums the .x fields of the (at most 16) warp slots,
+    // the high half the .y fields; two broadcasts give every lane both totals
+    const int lane = lane_id(), q = lane & 15;
+    float v = 0.f;
+    if (q < (int)(blockDim.x >> 5)) {
+        const float2 t = buf[q];
+        v = (lane & 16) ? t.y : t.x;
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return make_float2(__shfl_sync(0xffffffffu, v, 0), __shfl_sync(0xffffffffu, v, 16));
 }
 
 // ---------------------------------------------------------------------------
@@ -97,11 +120,10 @@ __device__ __forceinline__ float2 collect2(const float2* buf)
 // dz.  lhat(j, a) reads lambda_hat; lsm is an N n scratch in shared memory.
 // ---------------------------------------------------------------------------
 template <typename LhatFn>
-__device__ __forceinline__ void recover_dz(const PcgArgs& g, LhatFn lhat, float* lsm)
+__device__ __forceinline__ void recover_dz(const PcgArgs& g, int sol, LhatFn lhat, float* lsm)
 {
     const Work& w = g.w;
     const int N = w.N, n = w.n, m = w.m, Nn = N * n, T = blockDim.x, tid = threadIdx.x;
-    const int sol = blockIdx.x;
     const float* gLi = w.Linv + sol * w.sNnn;
     for (int i = tid; i < Nn; i += T) {
         const int j = i / n, a = i - j * n;
@@ -142,10 +164,10 @@ __device__ __forceinline__ void recover_dz(const PcgArgs& g, LhatFn lhat, float*
     }
 }
 
-__device__ __forceinline__ void finish(const PcgArgs& g, int it, bool done, bool nonfinite)
+__device__ __forceinline__ void finish(const PcgArgs& g, int sol, int it, bool done,
+                                       bool nonfinite)
 {
     if (threadIdx.x == 0) {
-        const int sol = blockIdx.x;
         if (g.acc_iters)
             g.iters[sol] += it;
         else
@@ -316,8 +338,8 @@ __global__ void __launch_bounds__(512) k_pcg_generic(PcgArgs g)
         __syncthreads();
     }
     __syncthreads();
-    recover_dz(g, [&](int j, int b) { return lam[j * n + b]; }, r);
-    finish(g, it, done, nonfinite);
+    recover_dz(g, sol, [&](int j, int b) { return lam[j * n + b]; }, r);
+    finish(g, sol, it, done, nonfinite);
 }
 
 // ===========================================================================
@@ -333,7 +355,7 @@ __global__ void __launch_bounds__(512) k_pcg_generic(PcgArgs g)
 //                           (each copy offset by 4 floats from the previous
 //                           one so that the two tiles' stores use different
 //                           banks)
-//   red [5][32] float2      warp partial sums
+//   red [5][32] float2      warp partial sums (three in use)
 //   DL [N]                  1 / ||L_j^-1||_F^2 (eigenvalue lower bounds)
 //   LP [N][n(n+1)/2]        packed Cholesky factors (stopping rule 0)
 // Thread t owns the four padded elements 4t .. 4t+3 (one knot half, one
@@ -421,12 +443,11 @@ __device__ __forceinline__ float lrow_tile(const float* LP, const float* gL, boo
 }
 
 template <int H>
-__global__ void __launch_bounds__(512, 1) k_pcg_tile(PcgArgs g)
+__device__ __forceinline__ void pcg_tile_solve(const PcgArgs& g, int sol)
 {
     extern __shared__ __align__(16) float sm[];
     const Work& w = g.w;
     const int N = w.N, n = w.n, T = blockDim.x, tid = threadIdx.x;
-    const int sol = blockIdx.x;
     const int E = N * 16;  // padded elements
     const int tri = n * (n + 1) / 2;
     const bool rule0 = g.rule == GATO_STOP_RESIDUAL;
@@ -442,8 +463,6 @@ __global__ void __launch_bounds__(512, 1) k_pcg_tile(PcgArgs g)
     float2* redA = reinterpret_cast<float2*>(sm + zero_count);
     float2* redB = redA + 32;
     float2* redC = redA + 64;
-    float2* redD = redA + 96;
-    float2* redE = redA + 128;
     float* DL = reinterpret_cast<float*>(redA + 160);
     float* LP = DL + ((N + 3) & ~3);
     const Y4 Y{YR0, YR1, YC0, YC1};
@@ -524,8 +543,7 @@ __global__ void __launch_bounds__(512, 1) k_pcg_tile(PcgArgs g)
         }
     }
     if (owner) store4(XR, e0, r);
-    post2(rr, 0.f, redB);
-    post2(gg, 0.f, redE);
+    post2(rr, gg, redB);
     __syncthreads();
     float q = has_tile ? tile_matvec<H>(tile, jb, rt, ct, XR, yr_base, yc_base) : 0.f;
     float lsq = 0.f;
@@ -538,7 +556,7 @@ __global__ void __launch_bounds__(512, 1) k_pcg_tile(PcgArgs g)
     __syncthreads();
     float2 sB = collect2(redB), sC = collect2(redC);
     float eta = sB.x - 2.f * sC.x;  // r^T (I - Nhat) r
-    const float ref = g.rule == GATO_STOP_PRECOND ? eta : collect2(redE).x;
+    const float ref = g.rule == GATO_STOP_PRECOND ? eta : sB.y;
     const float thr = g.eps * g.eps * ref;
     float stopq = g.rule == GATO_STOP_RESIDUAL ? sC.y : (g.rule == GATO_STOP_SCALED ? sB.x : eta);
     bool done = stopq <= thr;
@@ -551,7 +569,7 @@ __global__ void __launch_bounds__(512, 1) k_pcg_tile(PcgArgs g)
         pp += p[u] * p[u];
     }
     if (owner) store4(XP, e0, p);
-    post2(pp, 0.f, redD);
+    post1(pp, redA, true);
     __syncthreads();
 
     int it = 0;
@@ -559,10 +577,11 @@ __global__ void __launch_bounds__(512, 1) k_pcg_tile(PcgArgs g)
         ++it;
         // A: Nhat p (tiles) and p^T Nhat p partials
         q = has_tile ? tile_matvec<H>(tile, jb, rt, ct, XP, yr_base, yc_base) : 0.f;
-        post2(q, 0.f, redA);
+        post1(q, redA, false);
         __syncthreads();
         // B: alpha = eta / p^T S_hat p; lambda and r updates (owners)
-        const float pv = collect2(redD).x + 2.f * collect2(redA).x;
+        const float2 sA = collect2(redA);  // (sum_j p_j^T Nhat_j p_{j-1}, p^T p)
+        const float pv = sA.y + 2.f * sA.x;
         const float alpha = eta / pv;
         rr = 0.f;
         if (owner) ysum4(Y, e0, y);
@@ -594,7 +613,7 @@ __global__ void __launch_bounds__(512, 1) k_pcg_tile(PcgArgs g)
         sC = collect2(redC);
         const float eta_new = sB.x - 2.f * sC.x;
         stopq = g.rule == GATO_STOP_RESIDUAL ? sC.y : (g.rule == GATO_STOP_SCALED ? sB.x : eta_new);
-        if (!isfinite(eta_new) || !isfinite(pv) || !isfinite(stopq) || !isfinite(sB.y)) {
+        if (!isfinite(eta_new + pv + stopq + sB.y)) {  // NaN and Inf propagate
             nonfinite = true;
             break;
         }
@@ -609,15 +628,33 @@ __global__ void __launch_bounds__(512, 1) k_pcg_tile(PcgArgs g)
             pp += p[u] * p[u];
         }
         if (owner) store4(XP, e0, p);
-        post2(pp, 0.f, redD);
+        post1(pp, redA, true);
         eta = eta_new;
         __syncthreads();
     }
     __syncthreads();
     if (owner) store4(XP, e0, lam);
     __syncthreads();
-    recover_dz(g, [&](int j, int b) { return XP[j * 16 + (b / H) * 8 + b % H]; }, YR0);
-    finish(g, it, done, nonfinite);
+    recover_dz(g, sol, [&](int j, int b) { return XP[j * 16 + (b / H) * 8 + b % H]; }, YR0);
+    finish(g, sol, it, done, nonfinite);
+}
+
+// Persistent: each block takes the next unsolved system from g.queue until
+// none is left, so the batch is balanced over the resident blocks instead of
+// running in waves that each last as long as their slowest solve.  Every
+// solve's arithmetic is independent of which block runs it.
+template <int H>
+__global__ void __launch_bounds__(512, 1) k_pcg_tile(PcgArgs g)
+{
+    __shared__ int s_sol;
+    for (;;) {
+        if (threadIdx.x == 0) s_sol = atomicAdd(g.queue, 1);
+        __syncthreads();
+        const int sol = s_sol;
+        __syncthreads();
+        if (sol >= g.w.M) break;
+        pcg_tile_solve<H>(g, sol);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -657,6 +694,28 @@ cudaError_t launch_k(K kernel, const PcgArgs& a, int T, size_t smem, cudaStream_
     return cudaGetLastError();
 }
 
+// persistent launch: as many blocks as can be resident, at most one per solve
+template <typename K>
+cudaError_t launch_persistent(K kernel, const PcgArgs& a, int T, size_t smem, int num_sms,
+                              cudaStream_t st)
+{
+    if (smem > 48 * 1024) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, T, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    long grid = (long)per_sm * num_sms;
+    if (grid > a.w.M) grid = a.w.M;
+    e = cudaMemsetAsync(a.queue, 0, sizeof(int), st);
+    if (e != cudaSuccess) return e;
+    kernel<<<(unsigned)grid, T, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const float* lambda0,
@@ -677,6 +736,7 @@ cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const f
     a.max_iters = p->pcg_max_iters;
     a.rule = p->stop_rule;
     a.acc_iters = acc_iters;
+    a.queue = w.queue;
     const size_t limit = (size_t)h->smem_optin;
     const int want_l = p->stop_rule == GATO_STOP_RESIDUAL;
 
@@ -694,11 +754,11 @@ cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const f
         }
         if (smem <= limit) {
             switch (H) {
-                case 4: return launch_k(k_pcg_tile<4>, a, T, smem, st);
-                case 5: return launch_k(k_pcg_tile<5>, a, T, smem, st);
-                case 6: return launch_k(k_pcg_tile<6>, a, T, smem, st);
-                case 7: return launch_k(k_pcg_tile<7>, a, T, smem, st);
-                case 8: return launch_k(k_pcg_tile<8>, a, T, smem, st);
+                case 4: return launch_persistent(k_pcg_tile<4>, a, T, smem, h->num_sms, st);
+                case 5: return launch_persistent(k_pcg_tile<5>, a, T, smem, h->num_sms, st);
+                case 6: return launch_persistent(k_pcg_tile<6>, a, T, smem, h->num_sms, st);
+                case 7: return launch_persistent(k_pcg_tile<7>, a, T, smem, h->num_sms, st);
+                case 8: return launch_persistent(k_pcg_tile<8>, a, T, smem, h->num_sms, st);
                 default: break;
             }
         }

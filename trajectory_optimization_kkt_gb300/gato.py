@@ -27,6 +27,12 @@ GATO_STATUS_NONFINITE = 8
 GATO_PCG_AUTO = 0
 GATO_PCG_GENERIC = 1
 
+GATO_FORM_AUTO = 0
+GATO_FORM_SHARED = 1
+
+GATO_MERIT_FUSED = 0
+GATO_MERIT_PER_CANDIDATE = 1
+
 GATO_STOP_RESIDUAL = 0
 GATO_STOP_PRECOND = 1
 GATO_STOP_SCALED = 2
@@ -39,12 +45,14 @@ class GatoParams(ctypes.Structure):
     _fields_ = [("pcg_eps", ctypes.c_float), ("pcg_max_iters", ctypes.c_int),
                 ("stop_rule", ctypes.c_int), ("refine_steps", ctypes.c_int),
                 ("n_alpha", ctypes.c_int), ("beta", ctypes.c_float), ("mu", ctypes.c_float),
-                ("merit_threads", ctypes.c_int), ("refine_eps", ctypes.c_float)]
+                ("merit_threads", ctypes.c_int), ("refine_eps", ctypes.c_float),
+                ("merit_kernel", ctypes.c_int)]
 
 
 class GatoStats(ctypes.Structure):
     _fields_ = [("form_us", ctypes.c_float), ("pcg_us", ctypes.c_float),
-                ("merit_us", ctypes.c_float), ("total_us", ctypes.c_float)]
+                ("refine_us", ctypes.c_float), ("merit_us", ctypes.c_float),
+                ("total_us", ctypes.c_float)]
 
 
 class GatoError(RuntimeError):
@@ -78,6 +86,7 @@ def load(path: Optional[str] = None):
     lib.gato_destroy.restype = None
     lib.gato_set_timing.argtypes = [vp, ip]
     lib.gato_set_pcg_kernel.argtypes = [vp, ip]
+    lib.gato_set_form_kernel.argtypes = [vp, ip]
     lib.gato_get_stats.argtypes = [vp, ctypes.POINTER(GatoStats)]
     lib.gato_form_schur.argtypes = [vp] + [vp] * 8 + [vp, vp]
     lib.gato_get_schur.argtypes = [vp] + [vp] * 5 + [vp]
@@ -86,7 +95,8 @@ def load(path: Optional[str] = None):
     lib.gato_solve_kkt.argtypes = [vp, P] + [vp] * 8 + [vp] * 7 + [vp]
     lib.gato_apply_step.argtypes = [vp, P] + [vp] * 5 + [vp]
     lib.gato_solve_kkt_noalloc.argtypes = [P, ip, ip, ip, ip] + [vp] * 8 + [vp] * 7 + [vp]
-    for fn in ("gato_create", "gato_set_timing", "gato_set_pcg_kernel", "gato_get_stats", "gato_form_schur",
+    for fn in ("gato_create", "gato_set_timing", "gato_set_pcg_kernel", "gato_set_form_kernel",
+               "gato_get_stats", "gato_form_schur",
                "gato_get_schur", "gato_pcg_solve", "gato_linesearch", "gato_solve_kkt",
                "gato_apply_step", "gato_solve_kkt_noalloc"):
         getattr(lib, fn).restype = ctypes.c_int
@@ -171,6 +181,9 @@ class Solver:
 
     def set_pcg_kernel(self, kind: int):
         _check("gato_set_pcg_kernel", self.lib.gato_set_pcg_kernel(self.h, kind))
+
+    def set_form_kernel(self, kind: int):
+        _check("gato_set_form_kernel", self.lib.gato_set_form_kernel(self.h, kind))
 
     def get_stats(self) -> GatoStats:
         s = GatoStats()
