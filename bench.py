@@ -32,9 +32,11 @@ UNIT = "solves/s"
 WORKLOAD_INDEX = 4  # M=256, N=128, n=14, m=7
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one PCG
-# launch at this workload, from an ncu capture; valid only for the kernel
-# source it was taken on (sha256 prefix of csrc/pcg.cu), null otherwise.
-PCG_TRAFFIC = {"pcg_sha": None, "bytes_per_launch": None}
+# solve launch at this workload, from an ncu capture; valid only for the
+# kernel source it was taken on (sha256 prefix of csrc/pcg.cu), null
+# otherwise.  Captured on 152 solves (one block per SM: 90.51 MB) and scaled
+# by the solves processed to the 256-solve launch.
+PCG_TRAFFIC = {"pcg_sha": "abc92f5045d93132", "bytes_per_launch": 152435874}
 
 FP32_LANES_PER_SM = 128  # FFMA lanes per SM (4 sub-partitions x 32)
 

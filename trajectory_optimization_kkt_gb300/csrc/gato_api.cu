@@ -162,7 +162,7 @@ int gato_set_timing(gato_handle* h, int on)
 int gato_set_pcg_kernel(gato_handle* h, int kind)
 {
     if (!h || (kind != GATO_PCG_AUTO && kind != GATO_PCG_GENERIC)) return GATO_ERR_INVALID_ARG;
-    h->force_generic_pcg = kind == GATO_PCG_GENERIC;
+    h->pcg_kernel = kind;
     return GATO_OK;
 }
 

@@ -75,7 +75,7 @@ struct gato_handle {
     void* base;         // the single workspace allocation
     size_t bytes;
     int timing;
-    int force_generic_pcg;  // GATO_PCG_GENERIC selected by gato_set_pcg_kernel
+    int pcg_kernel;         // GATO_PCG_* selected by gato_set_pcg_kernel
     int force_smem_form;    // GATO_FORM_SHARED selected by gato_set_form_kernel
     cudaEvent_t ev[5];  // start, after form, after PCG, after refinement, after merit
     int ev_used[5];

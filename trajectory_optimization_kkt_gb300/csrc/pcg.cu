@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(512) k_pcg_generic(PcgArgs g)
 //                           (each copy offset by 4 floats from the previous
 //                           one so that the two tiles' stores use different
 //                           banks)
-//   red [5][32] float2      warp partial sums (three in use)
+//   red [5][32] float2      warp partial sums (four in use)
 //   DL [N]                  1 / ||L_j^-1||_F^2 (eigenvalue lower bounds)
 //   LP [N][n(n+1)/2]        packed Cholesky factors (stopping rule 0)
 // Thread t owns the four padded elements 4t .. 4t+3 (one knot half, one
@@ -463,6 +463,7 @@ __device__ __forceinline__ void pcg_tile_solve(const PcgArgs& g, int sol)
     float2* redA = reinterpret_cast<float2*>(sm + zero_count);
     float2* redB = redA + 32;
     float2* redC = redA + 64;
+    float2* redD = redA + 96;  // also used as float4[16] by block_sum
     float* DL = reinterpret_cast<float*>(redA + 160);
     float* LP = DL + ((N + 3) & ~3);
     const Y4 Y{YR0, YR1, YC0, YC1};
@@ -561,74 +562,98 @@ __device__ __forceinline__ void pcg_tile_solve(const PcgArgs& g, int sol)
     float stopq = g.rule == GATO_STOP_RESIDUAL ? sC.y : (g.rule == GATO_STOP_SCALED ? sB.x : eta);
     bool done = stopq <= thr;
     bool nonfinite = !isfinite(eta) || !isfinite(stopq);
-    float pp = 0.f;
     if (owner) ysum4(Y, e0, y);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        p[u] = valid[u] ? r[u] - y[u] : 0.f;  // z = (I - Nhat) r
-        pp += p[u] * p[u];
-    }
+    for (int u = 0; u < 4; ++u) p[u] = valid[u] ? r[u] - y[u] : 0.f;  // z = (I - Nhat) r
     if (owner) store4(XP, e0, p);
-    post1(pp, redA, true);
+    // exact ||L r_hat|| is evaluated in phase C when the previous iteration's
+    // lower bound was within a factor 1.25 of the threshold (the residual
+    // shrinks by about 1-2 % per iteration here); should the bound of
+    // the current residual fall below the threshold without the exact value,
+    // phase D evaluates it there (one extra barrier), so the stopping test is
+    // exact in every iteration.
+    bool exact_next;
+    {
+        float lb = 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) lb += dl * r[u] * r[u];
+        float lbv[1] = {lb};
+        block_sum<1>(lbv, reinterpret_cast<float4*>(redD));
+        exact_next = rule0 && lbv[0] <= 1.25f * thr;
+    }
     __syncthreads();
 
     int it = 0;
     while (!done && !nonfinite && it < g.max_iters) {
         ++it;
-        // A: Nhat p (tiles) and p^T Nhat p partials
+        // A: Nhat p (tiles) with its partial p^T Nhat p, and p^T p (owners)
         q = has_tile ? tile_matvec<H>(tile, jb, rt, ct, XP, yr_base, yc_base) : 0.f;
-        post1(q, redA, false);
+        float pp = 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) pp += p[u] * p[u];
+        post2(q, pp, redA);
         __syncthreads();
         // B: alpha = eta / p^T S_hat p; lambda and r updates (owners)
         const float2 sA = collect2(redA);  // (sum_j p_j^T Nhat_j p_{j-1}, p^T p)
         const float pv = sA.y + 2.f * sA.x;
         const float alpha = eta / pv;
-        rr = 0.f;
         if (owner) ysum4(Y, e0, y);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const float v = p[u] + y[u];
             lam[u] += alpha * p[u];
             r[u] = valid[u] ? r[u] - alpha * v : 0.f;
-            rr += r[u] * r[u];
         }
         if (owner) store4(XR, e0, r);
-        // sum_j lambda_min-bound_j ||r_hat_j||^2 <= ||L r_hat||^2
-        post2(rr, dl * rr, redB);
         __syncthreads();
-        // C: Nhat r (tiles), r^T Nhat r partials; ||L r_hat||^2 (owners), only
-        // when its lower bound does not already rule convergence out
+        // C: Nhat r (tiles) with r^T Nhat r partials; r^T r, the lower bound
+        // sum_j lambda_min-bound_j ||r_hat_j||^2 <= ||L r_hat||^2 and, when
+        // gated in, ||L r_hat||^2 (owners)
         q = has_tile ? tile_matvec<H>(tile, jb, rt, ct, XR, yr_base, yc_base) : 0.f;
-        lsq = 0.f;
-        sB = collect2(redB);
-        const bool exact = rule0 && sB.y * 0.999f <= thr;
+        rr = 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) rr += r[u] * r[u];
+        float lsq = 0.f;
+        const bool exact = exact_next;
         if (exact) {
 #pragma unroll
             for (int u = 0; u < 4; ++u)
                 if (valid[u]) lsq += lrow_tile<H>(LP, gL, lpacked, XR, jo, ao + u, n, tri);
         }
-        post2(q, lsq, redC);
+        post2(q, rr, redB);
+        post2(dl * rr, lsq, redC);
         __syncthreads();
         // D: eta' = r^T (I - Nhat) r, convergence, p = z + beta p (owners)
+        sB = collect2(redB);
         sC = collect2(redC);
-        const float eta_new = sB.x - 2.f * sC.x;
-        stopq = g.rule == GATO_STOP_RESIDUAL ? sC.y : (g.rule == GATO_STOP_SCALED ? sB.x : eta_new);
-        if (!isfinite(eta_new + pv + stopq + sB.y)) {  // NaN and Inf propagate
+        const float eta_new = sB.y - 2.f * sB.x;
+        float lsq_all = sC.y;
+        bool have_exact = exact;
+        if (rule0 && !exact && sC.x * 0.999f <= thr) {
+            // the bound no longer rules convergence out: evaluate ||L r_hat||
+            lsq = 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (valid[u]) lsq += lrow_tile<H>(LP, gL, lpacked, XR, jo, ao + u, n, tri);
+            float lv[1] = {lsq};
+            block_sum<1>(lv, reinterpret_cast<float4*>(redD));
+            lsq_all = lv[0];
+            have_exact = true;
+        }
+        stopq = g.rule == GATO_STOP_RESIDUAL ? lsq_all
+                                             : (g.rule == GATO_STOP_SCALED ? sB.y : eta_new);
+        if (!isfinite(eta_new + pv + stopq + sC.x)) {  // NaN and Inf propagate
             nonfinite = true;
             break;
         }
-        done = (!rule0 || exact) && stopq <= thr;
+        done = (!rule0 || have_exact) && stopq <= thr;
         if (done) break;
+        exact_next = rule0 && sC.x <= 1.25f * thr;
         const float beta = eta_new / eta;
-        pp = 0.f;
         if (owner) ysum4(Y, e0, y);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            p[u] = valid[u] ? (r[u] - y[u]) + beta * p[u] : 0.f;
-            pp += p[u] * p[u];
-        }
+        for (int u = 0; u < 4; ++u) p[u] = valid[u] ? (r[u] - y[u]) + beta * p[u] : 0.f;
         if (owner) store4(XP, e0, p);
-        post1(pp, redA, true);
         eta = eta_new;
         __syncthreads();
     }
@@ -744,7 +769,7 @@ cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const f
     const int H = (w.n + 1) / 2;
     int T = ((4 * w.N + 31) / 32) * 32;
     if (T < 64) T = 64;
-    if (!h->force_generic_pcg && w.n >= 7 && w.n <= 16 && T <= 512) {
+    if (h->pcg_kernel != GATO_PCG_GENERIC && w.n >= 7 && w.n <= 16 && T <= 512) {
         a.nh_smem = 0;
         a.l_smem = want_l;
         size_t smem = tile_smem_bytes(w, a.l_smem);
