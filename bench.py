@@ -40,6 +40,18 @@ PCG_TRAFFIC = {"pcg_sha": "abc92f5045d93132", "bytes_per_launch": 152435874}
 
 FP32_LANES_PER_SM = 128  # FFMA lanes per SM (4 sub-partitions x 32)
 
+# linear solvers of S lambda = gamma (gato_params.linsys)
+LINSYS = {"pcg": 1, "bdsv": 2, "bdsv_chrono": 3}
+
+
+def launches_per_solve(linsys, refine_steps):
+    """Kernel launches of one gato_solve_kkt call: 3 formation + 1 right-hand
+    side + the linear solve (PCG: 1; direct: factor + substitution) + 1 fused
+    merit, and per refinement round 1 residual + 1 right-hand side + 1 solve
+    (PCG, or the direct substitution) + 1 accumulate."""
+    solve = 1 if linsys == "pcg" else 2
+    return 5 + solve + 4 * refine_steps
+
 
 def _src_sha(path):
     with open(path, "rb") as f:
@@ -193,6 +205,70 @@ def _cpu_baseline(w, budget_s=12.0):
             "pcg_iters_per_sec": sum(r[0] for r in res) / sec}
 
 
+def _time_solver(torch, s, p, d, out, steps, flush, stream):
+    """Device time of `steps` gato_solve_kkt calls (L2 flushed before each):
+    (ms per step, mean stage microseconds, PCG iterations per step)."""
+    def step():
+        out["status"].zero_()
+        s.solve_kkt(p, d, out["dX"], out["dU"], out["lam"], out["iters"], out["merit"],
+                    out["best"], out["status"], stream)
+    for _ in range(3):
+        step()
+    s.set_timing(True)
+    ms, stages, iters = [], {"form": [], "linsys": [], "refine": [], "merit": []}, 0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for k in range(steps):
+        flush.fill_(float(k))
+        a.record(stream)
+        step()
+        b.record(stream)
+        st = s.get_stats()
+        ms.append(a.elapsed_time(b))
+        stages["form"].append(st.form_us)
+        stages["linsys"].append(st.pcg_us)
+        stages["refine"].append(max(st.refine_us, 0.0))
+        stages["merit"].append(st.merit_us)
+        iters += int(out["iters"].sum())
+    s.set_timing(False)
+    bad = int((out["status"] != 0).sum())
+    return (statistics.mean(ms), {k: statistics.mean(v) for k, v in stages.items()},
+            iters / steps, bad)
+
+
+def run_sweep(args, local):
+    """Horizon x batch sweep of the linear solvers (the GATO documentation's
+    PCG-versus-direct comparison that sets BDSV_HORIZON), one JSON line each."""
+    import torch
+
+    from trajectory_optimization_kkt_gb300 import _build, gato
+    from trajectory_optimization_kkt_gb300.workloads import WORKLOADS, make_batch
+    torch.cuda.set_device(local)
+    _build.build()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    base = WORKLOADS[WORKLOAD_INDEX]
+    for N in (32, 64, 128, 256, 512):
+        for M in (1, 16, 256):
+            w = base.with_batch(M, N)
+            prob = make_batch(w, M=M)
+            d = {k: torch.from_numpy(v).to(dev) for k, v in prob.items()}
+            with gato.Solver(M, N, w.n, w.m) as s:
+                out = s.outputs(w.n_alpha)
+                for name, ls in LINSYS.items():
+                    p = gato.default_params(pcg_eps=w.pcg_eps, pcg_max_iters=4000,
+                                            n_alpha=w.n_alpha, beta=w.beta, mu=w.mu,
+                                            refine_steps=w.refine_steps,
+                                            refine_eps=w.refine_eps, linsys=ls)
+                    ms, stages, iters, bad = _time_solver(torch, s, p, d, out, args.steps,
+                                                          flush, stream)
+                    print(json.dumps({"sweep": "linsys", "M": M, "N": N, "n": w.n, "m": w.m,
+                                      "linsys": name, "solves_per_s": M / (ms / 1000.0),
+                                      "ms_per_step": ms, "stage_us": stages,
+                                      "pcg_iters_per_solve": iters / M,
+                                      "status_nonzero_solves": bad}), flush=True)
+
+
 def run_gpu(args, world, rank, local):
     import torch
 
@@ -216,12 +292,11 @@ def run_gpu(args, world, rank, local):
     out = s.outputs(w.n_alpha)
     p = gato.default_params(pcg_eps=w.pcg_eps, pcg_max_iters=w.pcg_max_iters,
                             n_alpha=w.n_alpha, beta=w.beta, mu=w.mu,
-                            refine_steps=w.refine_steps, refine_eps=w.refine_eps)
+                            refine_steps=w.refine_steps, refine_eps=w.refine_eps,
+                            linsys=LINSYS[args.linsys])
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    # 3 formation + 1 right-hand side + 1 PCG + 2 merit, and per refinement
-    # round 1 residual + 1 right-hand side + 1 PCG + 1 accumulate
-    launches_per_step = 7 + 4 * w.refine_steps
+    launches_per_step = launches_per_solve(args.linsys, w.refine_steps)
 
     def step():
         out["status"].zero_()
@@ -310,6 +385,19 @@ def run_gpu(args, world, rank, local):
     sha = _src_sha(os.path.join(_build.CSRC, "pcg.cu"))
     traffic = PCG_TRAFFIC["bytes_per_launch"] if PCG_TRAFFIC["pcg_sha"] == sha else None
 
+    # ---- the same step through the direct solvers (context, not the metric) ----
+    alternatives = {}
+    if args.linsys == "pcg" and not args.no_alternatives and rank == 0:
+        for name in ("bdsv", "bdsv_chrono"):
+            pa = gato.default_params(pcg_eps=w.pcg_eps, pcg_max_iters=w.pcg_max_iters,
+                                     n_alpha=w.n_alpha, beta=w.beta, mu=w.mu,
+                                     refine_steps=w.refine_steps, refine_eps=w.refine_eps,
+                                     linsys=LINSYS[name])
+            ms, stages, _, bad = _time_solver(torch, s, pa, d, out, min(args.steps, 10), flush,
+                                              stream)
+            alternatives[name] = {"solves_per_s": M / (ms / 1000.0), "ms_per_step": ms,
+                                  "stage_us": stages, "status_nonzero_solves": bad}
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -323,7 +411,9 @@ def run_gpu(args, world, rank, local):
                          "refine": statistics.mean(refine_us),
                          "merit": statistics.mean(merit_us)},
             "status_nonzero_solves": status_bad,
-            "roofline": {"bound": "alu", "achieved": achieved_tf, "peak": alu_peak_tf,
+            "linsys": args.linsys,
+            "roofline": None if args.linsys != "pcg" else {
+                         "bound": "alu", "achieved": achieved_tf, "peak": alu_peak_tf,
                          "unit": "TFLOP/s", "frac": achieved_tf / alu_peak_tf,
                          "traffic": traffic, "kernel": "k_pcg_tile (solve + refinement launches)",
                          "peak_basis": f"{n_sm} SMs x {FP32_LANES_PER_SM} FFMA lanes x 2 flop x "
@@ -340,6 +430,8 @@ def run_gpu(args, world, rank, local):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
         }
+        if alternatives:
+            line["linsys_alternatives"] = alternatives
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = _cpu_baseline(w)
         print(json.dumps(line), flush=True)
@@ -357,6 +449,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--linsys", default="pcg", choices=sorted(LINSYS),
+                    help="linear solver of the timed step (default pcg, the metric's)")
+    ap.add_argument("--no-alternatives", action="store_true",
+                    help="skip timing the same step through the direct solvers")
+    ap.add_argument("--sweep", action="store_true",
+                    help="horizon x batch sweep of the three linear solvers instead")
     ap.add_argument("--batch", type=int, default=None,
                     help="solves per GPU (default: the workload's 256); for profiler "
                          "captures of a smaller case")
@@ -364,6 +462,8 @@ def main():
     world, rank, local = _dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.sweep:
+        run_sweep(args, local)
     else:
         run_gpu(args, world, rank, local)
 

@@ -77,6 +77,24 @@ extern "C" {
                                       N <= 128, else the generic kernel            */
 #define GATO_PCG_GENERIC 1         /* always the generic kernel                   */
 
+/* Linear solver of S lambda = gamma (gato_params.linsys).  The direct solver
+ * (bdsv) factors the block-tridiagonal S exactly instead of iterating; the
+ * GATO documentation measures it about linear in the horizon N and faster
+ * than PCG from N = 256 (its BDSV_HORIZON policy), which GATO_LINSYS_AUTO
+ * follows with the threshold gato_params.bdsv_horizon. */
+#define GATO_LINSYS_AUTO 0         /* PCG when N < bdsv_horizon, else the cyclic-
+                                      reduction direct solve (default)            */
+#define GATO_LINSYS_PCG 1          /* always PCG                                  */
+#define GATO_LINSYS_BDSV 2         /* direct solve, cyclic reduction (odd knots
+                                      first, ceil(log2 N) levels)                 */
+#define GATO_LINSYS_BDSV_CHRONO 3  /* direct solve, block Cholesky in
+                                      chronological order (block Thomas)          */
+
+/* direct-solve kernel selection (gato_set_bdsv_kernel) */
+#define GATO_BDSV_KERNEL_AUTO 0    /* register kernel for cyclic reduction when
+                                      n <= 16, else the shared-memory kernel      */
+#define GATO_BDSV_KERNEL_SHARED 1  /* always the shared-memory kernel             */
+
 /* formation kernel selection (gato_set_form_kernel) */
 #define GATO_FORM_AUTO 0           /* register kernels when n, m <= 16, else the
                                       shared-memory kernels                        */
@@ -99,7 +117,8 @@ typedef struct gato_params {
     int pcg_max_iters;   /* PCG iteration cap (default 200)                       */
     int stop_rule;       /* GATO_STOP_* (default GATO_STOP_RESIDUAL)              */
     int refine_steps;    /* gato_solve_kkt only: rounds of iterative refinement of
-                            the KKT solution, residual in fp64 (default 0)         */
+                            the KKT solution, residual in compensated fp32
+                            (default 0)                                            */
     int n_alpha;         /* line-search candidates A (default 8)                  */
     float beta;          /* alpha_i = beta^-i, beta > 1 (default 2)               */
     float mu;            /* L1 penalty weight (default 10)                        */
@@ -108,14 +127,18 @@ typedef struct gato_params {
     float refine_eps;    /* PCG tolerance of each refinement correction; 0 means
                             pcg_eps (default 0.1: a correction only needs a digit) */
     int merit_kernel;    /* GATO_MERIT_FUSED (default) or GATO_MERIT_PER_CANDIDATE */
+    int linsys;          /* GATO_LINSYS_* (default GATO_LINSYS_AUTO)              */
+    int bdsv_horizon;    /* GATO_LINSYS_AUTO: direct solve when N >= bdsv_horizon
+                            (default 256); >= 1                                    */
 } gato_params;
 
 typedef struct gato_stats {
     float form_us;       /* device time of the last call's stages (microseconds), */
     float pcg_us;        /* filled only when timing was enabled with              */
     float refine_us;     /* gato_set_timing; -1 for a stage that did not run.     */
-    float merit_us;      /* pcg_us: the PCG launch of the solve; refine_us: every */
-    float total_us;      /* refinement round (residual, right-hand side, PCG).    */
+    float merit_us;      /* pcg_us: the linear solve (PCG, or the direct solve's  */
+    float total_us;      /* factorisation and substitution); refine_us: every
+                            refinement round (residual, right-hand side, solve).  */
 } gato_stats;
 
 typedef struct gato_handle gato_handle;
@@ -125,8 +148,8 @@ void gato_default_params(gato_params* p);
 
 /* Creates a solver for M solves of N knots, n states and m controls on the
  * current CUDA device and allocates its device workspace (cudaMalloc; about
- * 4 M (8 N n^2 + (N-1)(m^2 + n m) + 11 N n + 4 (N-1) m + 65 N) bytes).  *h receives the handle, which the
- * caller releases with gato_destroy.  Errors: INVALID_ARG (h NULL, M, N, n or
+ * 4 M (11 N n^2 + (N-1)(m^2 + n m) + 13 N n + 4 (N-1) m + 65 N) bytes).  *h
+ * receives the handle, which the caller releases with gato_destroy.  Errors: INVALID_ARG (h NULL, M, N, n or
  * m < 1), UNSUPPORTED (n or m above the limits), NO_MEMORY, CUDA. */
 int gato_create(gato_handle** h, int M, int N, int n, int m);
 
@@ -145,6 +168,11 @@ int gato_get_stats(gato_handle* h, gato_stats* out);
  * Both give the same PCG iterates up to rounding; the generic kernel covers
  * every supported size.  Errors: INVALID_ARG. */
 int gato_set_pcg_kernel(gato_handle* h, int kind);
+
+/* Chooses the direct-solve kernels (GATO_BDSV_KERNEL_AUTO or
+ * GATO_BDSV_KERNEL_SHARED) for later calls; both compute the same
+ * factorisation up to rounding.  Errors: INVALID_ARG. */
+int gato_set_bdsv_kernel(gato_handle* h, int kind);
 
 /* Chooses the formation kernels (GATO_FORM_AUTO or GATO_FORM_SHARED) for later
  * calls; both compute the same blocks up to rounding.  Errors: INVALID_ARG. */
@@ -184,6 +212,21 @@ int gato_pcg_solve(gato_handle* h, const gato_params* p, const float* lambda0,
                    float* lambda, float* dX, float* dU, int32_t* iters,
                    uint32_t* status, void* stream);
 
+/* Direct solve of S lambda = gamma (f1 of the GATO documentation's linear
+ * solvers, "bdsv"): the block-tridiagonal S is factored exactly, in the
+ * block-Jacobi-scaled form S_hat = L^-1 S L^-T (identity diagonal blocks,
+ * coupling blocks L_j^-1 S_{j,j-1} L_{j-1}^-T), by cyclic reduction
+ * (p->linsys = GATO_LINSYS_BDSV or AUTO: odd knots eliminated first, then the
+ * odd ones of the reduced chain, ceil(log2 N) levels, one thread block per
+ * solve) or by block Cholesky in chronological order (GATO_LINSYS_BDSV_CHRONO,
+ * the block Thomas algorithm); then lambda, and dz by eq. (4) as in
+ * gato_pcg_solve.  Outputs as gato_pcg_solve; iters [M] gets 0.  A pivot of a
+ * reduced block that is <= 0 sets GATO_STATUS_NONPOSITIVE_PIVOT, a non-finite
+ * lambda GATO_STATUS_NONFINITE.  Requires a preceding gato_form_schur on the
+ * same handle.  Errors: INVALID_ARG (also p->linsys = GATO_LINSYS_PCG). */
+int gato_bdsv_solve(gato_handle* h, const gato_params* p, float* lambda, float* dX,
+                    float* dU, int32_t* iters, uint32_t* status, void* stream);
+
 /* a5 + a6.  Parallel line search (GATO paper Sec. III-A): for alpha = 0 and
  * alpha_i = beta^-i (i = 0..n_alpha-1), with x = alpha dx, u = alpha du,
  *   M(alpha) = sum_k 1/2 x_k^T Q_k x_k + q_k^T x_k + 1/2 u_k^T R_k u_k + r_k^T u_k
@@ -199,12 +242,14 @@ int gato_linesearch(gato_handle* h, const gato_params* p, const float* Q, const 
                     const float* e, const float* s0, const float* dX, const float* dU,
                     float* merit, int32_t* best, uint32_t* status, void* stream);
 
-/* gato_form_schur + gato_pcg_solve + gato_linesearch on one stream.  With
- * p->refine_steps = k > 0 the KKT solution is refined k times: the residual of
- * the full KKT system is formed in fp64 from the inputs, the correction is
- * solved with the same S and Phi^-1, and added to dz and lambda; iters then
- * counts PCG iterations over all solves of the refinement.  Each correction is
- * solved to p->refine_eps (relative residual of the correction system). */
+/* gato_form_schur + the linear solve (gato_pcg_solve, or gato_bdsv_solve as
+ * p->linsys selects) + gato_linesearch on one stream.  With p->refine_steps =
+ * k > 0 the KKT solution is refined k times: the residual of the full KKT
+ * system is formed from the inputs in compensated fp32 (error-free products
+ * and sums, about as accurate as fp64 accumulation), the correction is solved
+ * with the same S (PCG to p->refine_eps, relative residual of the correction
+ * system; or the direct solve's factors), and added to dz and lambda; iters
+ * then counts PCG iterations over all solves of the refinement. */
 int gato_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const float* R,
                    const float* q, const float* r, const float* A, const float* B,
                    const float* e, const float* s0, float* dX, float* dU, float* lambda,
@@ -225,7 +270,7 @@ int gato_apply_step(gato_handle* h, const gato_params* p, const int32_t* best,
  * n, m); the caller still provides every input and output.  The solver's
  * scratch is one static device array of GATO_NOALLOC_MAX_BYTES that every GPU
  * loading this library holds until the process exits; a problem needs about
- * 4 M (8 N n^2 + (N-1)(m^2 + n m) + 11 N n + 4 (N-1) m + 65 N) bytes of it
+ * 4 M (11 N n^2 + (N-1)(m^2 + n m) + 13 N n + 4 (N-1) m + 65 N) bytes of it
  * (each array rounded up to 64 floats), and larger problems are rejected
  * with GATO_ERR_UNSUPPORTED before
  * anything is launched (use gato_create for those).  The first call on each

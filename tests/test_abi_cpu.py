@@ -32,7 +32,8 @@ def test_header_declares_the_abi():
     for fn in ("gato_create", "gato_destroy", "gato_form_schur", "gato_pcg_solve",
                "gato_linesearch", "gato_solve_kkt", "gato_apply_step", "gato_get_schur",
                "gato_default_params", "gato_set_timing", "gato_get_stats",
-               "gato_set_pcg_kernel", "gato_set_form_kernel", "gato_solve_kkt_noalloc"):
+               "gato_set_pcg_kernel", "gato_set_form_kernel", "gato_solve_kkt_noalloc",
+               "gato_bdsv_solve", "gato_set_bdsv_kernel"):
         assert fn in names
 
 
@@ -49,6 +50,16 @@ def test_default_params(lib):
     assert (p.beta, p.mu) == (2.0, 10.0)
     assert p.refine_eps == pytest.approx(0.1)
     assert p.merit_kernel == gato.GATO_MERIT_FUSED
+    # the GATO documentation's policy: PCG below N = 256, the direct solve from it
+    assert (p.linsys, p.bdsv_horizon) == (gato.GATO_LINSYS_AUTO, 256)
+
+
+def test_params_struct_matches_header():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct gato_params \{(.*?)\} gato_params;", text, re.S).group(1)
+    fields = re.findall(r"\b(int|float)\s+(\w+)\s*;", body)
+    ctype = {"int": ctypes.c_int, "float": ctypes.c_float}
+    assert [(name, ctype[t]) for t, name in fields] == list(gato.GatoParams._fields_)
 
 
 def test_invalid_arguments_rejected_before_cuda(lib):
@@ -66,6 +77,7 @@ def test_invalid_arguments_rejected_before_cuda(lib):
     assert lib.gato_set_timing(None, 1) == gato.GATO_ERR_INVALID_ARG
     assert lib.gato_set_pcg_kernel(None, 0) == gato.GATO_ERR_INVALID_ARG
     assert lib.gato_set_form_kernel(None, 0) == gato.GATO_ERR_INVALID_ARG
+    assert lib.gato_set_bdsv_kernel(None, 0) == gato.GATO_ERR_INVALID_ARG
     assert lib.gato_get_stats(None, None) == gato.GATO_ERR_INVALID_ARG
     null = [None] * 8
     assert lib.gato_form_schur(None, *null, None, None) == gato.GATO_ERR_INVALID_ARG
@@ -74,6 +86,7 @@ def test_invalid_arguments_rejected_before_cuda(lib):
     assert lib.gato_linesearch(None, ctypes.byref(p), *null, *([None] * 5), None) == gato.GATO_ERR_INVALID_ARG
     assert lib.gato_solve_kkt(None, ctypes.byref(p), *null, *([None] * 7), None) == gato.GATO_ERR_INVALID_ARG
     assert lib.gato_apply_step(None, ctypes.byref(p), *([None] * 5), None) == gato.GATO_ERR_INVALID_ARG
+    assert lib.gato_bdsv_solve(None, ctypes.byref(p), *([None] * 5), None) == gato.GATO_ERR_INVALID_ARG
 
 
 def test_generator_is_deterministic_and_distributed():

@@ -33,10 +33,11 @@ def rel(a, b):
     return np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300)
 
 
-def params(w):
+def params(w, linsys=gato.GATO_LINSYS_AUTO):
     return gato.default_params(pcg_eps=w.pcg_eps, pcg_max_iters=w.pcg_max_iters,
                                n_alpha=w.n_alpha, beta=w.beta, mu=w.mu,
-                               refine_steps=w.refine_steps, refine_eps=w.refine_eps)
+                               refine_steps=w.refine_steps, refine_eps=w.refine_eps,
+                               linsys=linsys)
 
 
 def fresh_outputs(M, N, n, m, n_alpha):
@@ -49,13 +50,14 @@ def fresh_outputs(M, N, n, m, n_alpha):
                 status=torch.zeros(M, device="cuda", dtype=torch.int32))
 
 
-@pytest.mark.parametrize("wi", [1, 2])
-def test_noalloc_matches_solve_kkt_on_two_calls(wi):
+@pytest.mark.parametrize("wi,linsys", [(1, gato.GATO_LINSYS_AUTO), (2, gato.GATO_LINSYS_AUTO),
+                                       (2, gato.GATO_LINSYS_BDSV)])
+def test_noalloc_matches_solve_kkt_on_two_calls(wi, linsys):
     w = WORKLOADS[wi]
     M = min(w.M, 16)
     prob = make_batch(w, M=M)
     d = gato.to_device(prob)
-    p = params(w)
+    p = params(w, linsys)
     with gato.Solver(M, w.N, w.n, w.m) as s:
         ref = s.outputs(w.n_alpha)
         s.solve_kkt(p, d, ref["dX"], ref["dU"], ref["lam"], ref["iters"], ref["merit"],

@@ -17,185 +17,14 @@
 //                         the eigenvalue bound 1 / ||L_j^-1||_F^2
 //   k_rows_off   row j:   Nhat_j = L_j^-1 S_{j,j-1} L_{j-1}^-T and the explicit
 //                         Phi^-1 block -S_jj^-1 S_{j,j-1} S_{j-1,j-1}^-1
-#include "gato_internal.cuh"
+#include "rows16.cuh"
 
 namespace gato {
 namespace {
 
-constexpr int NP = 16;          // padded order
+using namespace rows;
+
 constexpr int kKnotsPerBlock = 16;  // 8 warps, two knots each
-
-__device__ __forceinline__ float shfl16(float v, int src)
-{
-    return __shfl_sync(0xffffffffu, v, src, 16);
-}
-
-// a[li] (runtime li) without dynamic register indexing
-__device__ __forceinline__ float pick(const float (&a)[NP], int li)
-{
-    float v = 0.f;
-#pragma unroll
-    for (int j = 0; j < NP; ++j) v = (j == li) ? a[j] : v;
-    return v;
-}
-
-// Row li of a rows x cols row-major global matrix into a (zero beyond cols);
-// rows >= `rows` become identity rows when `ident`, zero rows otherwise.
-__device__ __forceinline__ void load_row(float (&a)[NP], const float* M, int rows, int cols,
-                                         int li, bool ident)
-{
-#pragma unroll
-    for (int j = 0; j < NP; ++j) {
-        float v = 0.f;
-        if (li < rows) {
-            if (j < cols) v = M[li * cols + j];
-        } else if (ident && j == li) {
-            v = 1.f;
-        }
-        a[j] = v;
-    }
-}
-
-__device__ __forceinline__ void store_row(const float (&a)[NP], float* M, int rows, int cols,
-                                          int li, float s = 1.f)
-{
-    if (li < rows) {
-#pragma unroll
-        for (int j = 0; j < NP; ++j)
-            if (j < cols) M[li * cols + j] = s * a[j];
-    }
-}
-
-// publish row li into the 16 x 16 scratch S (row stride 16)
-__device__ __forceinline__ void publish(const float (&a)[NP], float* S, int li)
-{
-    float4* d = reinterpret_cast<float4*>(S + li * NP);
-    d[0] = make_float4(a[0], a[1], a[2], a[3]);
-    d[1] = make_float4(a[4], a[5], a[6], a[7]);
-    d[2] = make_float4(a[8], a[9], a[10], a[11]);
-    d[3] = make_float4(a[12], a[13], a[14], a[15]);
-}
-
-__device__ __forceinline__ void fetch(float (&b)[NP], const float* S, int k)
-{
-    const float4* s = reinterpret_cast<const float4*>(S + k * NP);
-    const float4 s0 = s[0], s1 = s[1], s2 = s[2], s3 = s[3];
-    b[0] = s0.x; b[1] = s0.y; b[2] = s0.z; b[3] = s0.w;
-    b[4] = s1.x; b[5] = s1.y; b[6] = s1.z; b[7] = s1.w;
-    b[8] = s2.x; b[9] = s2.y; b[10] = s2.z; b[11] = s2.w;
-    b[12] = s3.x; b[13] = s3.y; b[14] = s3.z; b[15] = s3.w;
-}
-
-// In-register Cholesky of diag(M, I) (M of order n): a becomes row li of L,
-// strict upper part zeroed.  A pivot <= 0 or not finite is flagged (false)
-// and replaced by 1.
-__device__ bool rows_cholesky(float (&a)[NP], int li, int n)
-{
-    bool ok = true;
-#pragma unroll
-    for (int k = 0; k < NP; ++k) {
-        if (k < n) {
-            const float d = shfl16(a[k], k);
-            const bool bad = !(d > 0.f) || !isfinite(d);
-            ok = ok && !bad;
-            const float s = bad ? 1.f : sqrtf(d);
-            const float inv = 1.f / s;
-            a[k] = (li == k) ? s : (li > k ? a[k] * inv : a[k]);
-#pragma unroll
-            for (int j = k + 1; j < NP; ++j) {
-                if (j < n) {
-                    const float ljk = shfl16(a[k], j);
-                    if (li >= j) a[j] -= a[k] * ljk;
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < NP; ++j)
-        if (j > li) a[j] = 0.f;
-    return ok;
-}
-
-// x = row li of L^-1 (L lower, rows in a); the finished rows of L^-1 end up
-// in the scratch S.
-__device__ void rows_lower_inverse(const float (&a)[NP], float (&x)[NP], int li, int n, float* S)
-{
-#pragma unroll
-    for (int j = 0; j < NP; ++j) x[j] = (j == li) ? 1.f : 0.f;
-    const float inv_diag = 1.f / pick(a, li);
-#pragma unroll
-    for (int k = 0; k < NP; ++k) {
-        if (k < n) {
-            if (li == k) {
-#pragma unroll
-                for (int j = 0; j < NP; ++j) x[j] *= inv_diag;
-                publish(x, S, k);
-            }
-            __syncwarp();
-            if (li > k) {
-                float xk[NP];
-                fetch(xk, S, k);
-                const float lik = a[k];
-#pragma unroll
-                for (int j = 0; j < NP; ++j) x[j] -= lik * xk[j];
-            }
-        }
-    }
-    if (li >= n) publish(x, S, li);  // identity rows, so S holds all of diag(L^-1, I)
-    __syncwarp();
-}
-
-// c = row li of X^T X, the rows of X in the scratch S (X lower triangular)
-__device__ __forceinline__ void rows_gram_lower(const float* S, float (&c)[NP], int li, int n)
-{
-#pragma unroll
-    for (int j = 0; j < NP; ++j) c[j] = 0.f;
-#pragma unroll
-    for (int k = 0; k < NP; ++k) {
-        if (k < n && k >= li) {
-            float xk[NP];
-            fetch(xk, S, k);
-            const float xki = pick(xk, li);
-#pragma unroll
-            for (int j = 0; j < NP; ++j) c[j] += xki * xk[j];
-        }
-    }
-}
-
-// c = s * (row li of A) * B, B's rows (kk of them) in the scratch S
-__device__ __forceinline__ void rows_mul(const float (&a)[NP], const float* S, int kk,
-                                         float (&c)[NP], float s)
-{
-#pragma unroll
-    for (int j = 0; j < NP; ++j) c[j] = 0.f;
-#pragma unroll
-    for (int k = 0; k < NP; ++k) {
-        if (k < kk) {
-            float bk[NP];
-            fetch(bk, S, k);
-            const float ak = s * a[k];
-#pragma unroll
-            for (int j = 0; j < NP; ++j) c[j] += ak * bk[j];
-        }
-    }
-}
-
-// c[j] += s * dot(row li of A, row j of B), B's rows (count of them) in S
-__device__ __forceinline__ void rows_mul_bt(const float (&a)[NP], const float* S, int count,
-                                            float (&c)[NP], float s)
-{
-#pragma unroll
-    for (int j = 0; j < NP; ++j) {
-        if (j < count) {
-            float bj[NP];
-            fetch(bj, S, j);
-            float d = 0.f;
-#pragma unroll
-            for (int k = 0; k < NP; ++k) d += a[k] * bj[k];
-            c[j] += s * d;
-        }
-    }
-}
 
 struct Half {
     int li;        // lane within the half-warp (row index)

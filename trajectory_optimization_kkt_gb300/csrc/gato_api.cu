@@ -8,17 +8,56 @@
 
 using gato::Work;
 
-namespace {
+namespace gato {
 
+namespace {
 size_t round64(size_t x)
 {
     const size_t r = (x + 63) / 64 * 64;
     return r ? r : 64;
 }
+}  // namespace
 
-int cuda_fail(cudaError_t e) { return e == cudaSuccess ? GATO_OK : GATO_ERR_CUDA; }
+size_t carve_workspace(Work& w, int M, int N, int n, int m, float* base)
+{
+    w.M = M; w.N = N; w.n = n; w.m = m;
+    const size_t K = (size_t)(N - 1);
+    w.sNnn = round64((size_t)N * n * n);
+    w.sKnn = round64(K * n * n);
+    w.sKmm = round64(K * m * m);
+    w.sKnm = round64(K * n * m);
+    w.sNn = round64((size_t)N * n);
+    w.sN = round64((size_t)N);
+    w.sKm = round64(K * m);
+    w.sK2 = (size_t)N * (GATO_MAX_ALPHA + 1);  // float2 units
+    // one allocation: (per-solve floats of each array) x M, in this order
+    float** fields[] = {&w.Qinv, &w.Rinv, &w.O, &w.V, &w.D, &w.L, &w.Linv, &w.Pd, &w.Po, &w.Nh,
+                        &w.dlow,
+                        &w.rhs[0].gamma, &w.rhs[0].ghat, &w.rhs[0].avec, &w.rhs[0].bvec,
+                        &w.rhs[1].gamma, &w.rhs[1].ghat, &w.rhs[1].avec, &w.rhs[1].bvec,
+                        &w.q2, &w.r2, &w.e2, &w.s02, &w.dlam, &w.ddX, &w.ddU,
+                        &w.Bd, &w.Be, &w.By, &w.Bv, &w.Bg};
+    const size_t strides[] = {w.sNnn, w.sKmm, w.sKnn, w.sKnm, w.sNnn, w.sNnn, w.sNnn,
+                              w.sNnn, w.sKnn, w.sKnn, w.sN, w.sNn, w.sNn, w.sNn, w.sKm,
+                              w.sNn, w.sNn, w.sNn, w.sKm,
+                              w.sNn, w.sKm, w.sNn, w.sNn, w.sNn, w.sNn, w.sKm,
+                              w.sNnn, w.sNnn, w.sNnn, w.sNn, w.sNn};
+    static_assert(sizeof(fields) / sizeof(fields[0]) == sizeof(strides) / sizeof(strides[0]),
+                  "one stride per workspace array");
+    const int nf = (int)(sizeof(strides) / sizeof(strides[0]));
+    size_t total = 0;
+    for (int i = 0; i < nf; ++i) {
+        if (base) *fields[i] = base + total;
+        total += strides[i] * (size_t)M;
+    }
+    if (base) w.mpart = (float2*)(base + total);
+    total += 2 * w.sK2 * (size_t)M;  // merit partials
+    if (base) w.queue = (int*)(base + total);
+    total += 64;                     // work counters
+    return total * sizeof(float);
+}
 
-bool params_ok(const gato_params* p)
+bool params_valid(const gato_params* p)
 {
     if (!p) return false;
     if (!(p->pcg_eps >= 0.f) || p->pcg_max_iters < 0) return false;
@@ -30,8 +69,78 @@ bool params_ok(const gato_params* p)
     if (!(p->refine_eps >= 0.f)) return false;
     if (p->merit_kernel != GATO_MERIT_FUSED && p->merit_kernel != GATO_MERIT_PER_CANDIDATE)
         return false;
+    if (p->linsys < GATO_LINSYS_AUTO || p->linsys > GATO_LINSYS_BDSV_CHRONO) return false;
+    if (p->bdsv_horizon < 1) return false;
     return true;
 }
+
+int linsys_for(const gato_params* p, int N)
+{
+    if (p->linsys == GATO_LINSYS_AUTO)
+        return N >= p->bdsv_horizon ? GATO_LINSYS_BDSV : GATO_LINSYS_PCG;
+    return p->linsys;
+}
+
+namespace {
+void record(gato_handle* h, int i, cudaStream_t st)
+{
+    if (!h->timing) return;
+    cudaEventRecord(h->ev[i], st);
+    h->ev_used[i] = 1;
+}
+}  // namespace
+
+cudaError_t run_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const float* R,
+                          const float* q, const float* r, const float* A, const float* B,
+                          const float* e, const float* s0, float* dX, float* dU, float* lambda,
+                          int32_t* iters, float* merit, int32_t* best, uint32_t* status,
+                          cudaStream_t st)
+{
+    Work& w = h->w;
+    const int ls = linsys_for(p, w.N);
+    const bool direct = ls != GATO_LINSYS_PCG;
+    cudaError_t err = launch_form_matrices(h, Q, R, A, B, status, st);
+    if (err == cudaSuccess) err = launch_form_rhs(h, 0, q, r, e, s0, (size_t)w.n, st);
+    record(h, 1, st);
+    if (err == cudaSuccess) {
+        if (direct) {
+            err = launch_bdsv_factor(h, ls, status, st);
+            if (err == cudaSuccess)
+                err = launch_bdsv_solve(h, ls, 0, lambda, dX, dU, iters, 0, status, st);
+        } else {
+            err = launch_pcg_ex(h, p, 0, nullptr, lambda, dX, dU, iters, 0, status, st);
+        }
+    }
+    record(h, 2, st);
+    gato_params pc = *p;  // PCG corrections are solved to refine_eps
+    if (p->refine_eps > 0.f) pc.pcg_eps = p->refine_eps;
+    for (int k = 0; k < p->refine_steps && err == cudaSuccess; ++k) {
+        err = launch_kkt_residual(h, Q, R, q, r, A, B, e, s0, dX, dU, lambda, st);
+        if (err == cudaSuccess)
+            err = launch_form_rhs(h, 1, w.q2, w.r2, w.e2, w.s02, (size_t)w.n, st);
+        if (err == cudaSuccess) {
+            if (direct)
+                err = launch_bdsv_solve(h, ls, 1, w.dlam, w.ddX, w.ddU, iters, 1, status, st);
+            else
+                err = launch_pcg_ex(h, &pc, 1, nullptr, w.dlam, w.ddX, w.ddU, iters, 1, status,
+                                    st);
+        }
+        if (err == cudaSuccess) err = launch_accumulate(h, lambda, dX, dU, iters, st);
+    }
+    if (p->refine_steps > 0) record(h, 3, st);
+    if (err == cudaSuccess)
+        err = launch_merit(h, p, Q, R, q, r, A, B, e, s0, dX, dU, merit, best, status, st);
+    record(h, 4, st);
+    return err;
+}
+
+}  // namespace gato
+
+namespace {
+
+using gato::params_valid;
+
+int cuda_fail(cudaError_t e) { return e == cudaSuccess ? GATO_OK : GATO_ERR_CUDA; }
 
 // the [N-1] arrays may be NULL only when N == 1
 bool lq_ok(const gato_handle* h, const float* Q, const float* R, const float* q,
@@ -56,6 +165,12 @@ void begin_timing(gato_handle* h, cudaStream_t st)
     record(h, 0, st);
 }
 
+int unsupported_or_fail(cudaError_t e)
+{
+    if (e == cudaErrorInvalidConfiguration) return GATO_ERR_UNSUPPORTED;
+    return cuda_fail(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -73,6 +188,8 @@ void gato_default_params(gato_params* p)
     p->merit_threads = 64;
     p->refine_eps = 0.1f;
     p->merit_kernel = GATO_MERIT_FUSED;
+    p->linsys = GATO_LINSYS_AUTO;
+    p->bdsv_horizon = 256;
 }
 
 int gato_create(gato_handle** out, int M, int N, int n, int m)
@@ -91,45 +208,13 @@ int gato_create(gato_handle** out, int M, int N, int n, int m)
         free(h);
         return GATO_ERR_CUDA;
     }
-    Work& w = h->w;
-    w.M = M; w.N = N; w.n = n; w.m = m;
-    const size_t K = (size_t)(N - 1);
-    w.sNnn = round64((size_t)N * n * n);
-    w.sKnn = round64(K * n * n);
-    w.sKmm = round64(K * m * m);
-    w.sKnm = round64(K * n * m);
-    w.sNn = round64((size_t)N * n);
-    w.sN = round64((size_t)N);
-    w.sKm = round64(K * m);
-    w.sK2 = (size_t)N * (GATO_MAX_ALPHA + 1);  // float2 units
-    // carve one allocation: (count of per-solve floats) x M
-    float** fields[] = {&w.Qinv, &w.Rinv, &w.O, &w.V, &w.D, &w.L, &w.Linv, &w.Pd, &w.Po, &w.Nh,
-                        &w.dlow,
-                        &w.rhs[0].gamma, &w.rhs[0].ghat, &w.rhs[0].avec, &w.rhs[0].bvec,
-                        &w.rhs[1].gamma, &w.rhs[1].ghat, &w.rhs[1].avec, &w.rhs[1].bvec,
-                        &w.q2, &w.r2, &w.e2, &w.s02, &w.dlam, &w.ddX, &w.ddU};
-    const size_t strides[] = {w.sNnn, w.sKmm, w.sKnn, w.sKnm, w.sNnn, w.sNnn, w.sNnn,
-                              w.sNnn, w.sKnn, w.sKnn, w.sN, w.sNn, w.sNn, w.sNn, w.sKm,
-                              w.sNn, w.sNn, w.sNn, w.sKm,
-                              w.sNn, w.sKm, w.sNn, w.sNn, w.sNn, w.sNn, w.sKm};
-    const int nf = (int)(sizeof(strides) / sizeof(strides[0]));
-    size_t total = 0;
-    for (int i = 0; i < nf; ++i) total += strides[i] * (size_t)M;
-    total += 2 * w.sK2 * (size_t)M;  // merit partials
-    total += 64;                     // work counters
-    h->bytes = total * sizeof(float);
+    h->bytes = gato::carve_workspace(h->w, M, N, n, m, nullptr);
     if (cudaMalloc(&h->base, h->bytes) != cudaSuccess) {
         cudaGetLastError();
         free(h);
         return GATO_ERR_NO_MEMORY;
     }
-    float* cur = (float*)h->base;
-    for (int i = 0; i < nf; ++i) {
-        *fields[i] = cur;
-        cur += strides[i] * (size_t)M;
-    }
-    w.mpart = (float2*)cur;
-    w.queue = (int*)(cur + 2 * w.sK2 * (size_t)M);
+    gato::carve_workspace(h->w, M, N, n, m, (float*)h->base);
     for (int i = 0; i < 5; ++i) {
         if (cudaEventCreate(&h->ev[i]) != cudaSuccess) {
             for (int j = 0; j < i; ++j) cudaEventDestroy(h->ev[j]);
@@ -163,6 +248,14 @@ int gato_set_pcg_kernel(gato_handle* h, int kind)
 {
     if (!h || (kind != GATO_PCG_AUTO && kind != GATO_PCG_GENERIC)) return GATO_ERR_INVALID_ARG;
     h->pcg_kernel = kind;
+    return GATO_OK;
+}
+
+int gato_set_bdsv_kernel(gato_handle* h, int kind)
+{
+    if (!h || (kind != GATO_BDSV_KERNEL_AUTO && kind != GATO_BDSV_KERNEL_SHARED))
+        return GATO_ERR_INVALID_ARG;
+    h->bdsv_kernel = kind;
     return GATO_OK;
 }
 
@@ -241,7 +334,7 @@ int gato_get_schur(gato_handle* h, float* S_diag, float* S_off, float* gamma,
 int gato_pcg_solve(gato_handle* h, const gato_params* p, const float* lambda0, float* lambda,
                    float* dX, float* dU, int32_t* iters, uint32_t* status, void* stream)
 {
-    if (!h || !params_ok(p) || !lambda || !dX || !iters || !status) return GATO_ERR_INVALID_ARG;
+    if (!h || !params_valid(p) || !lambda || !dX || !iters || !status) return GATO_ERR_INVALID_ARG;
     if (h->w.N > 1 && !dU) return GATO_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;
     begin_timing(h, st);
@@ -251,12 +344,29 @@ int gato_pcg_solve(gato_handle* h, const gato_params* p, const float* lambda0, f
     return cuda_fail(err);
 }
 
+int gato_bdsv_solve(gato_handle* h, const gato_params* p, float* lambda, float* dX, float* dU,
+                    int32_t* iters, uint32_t* status, void* stream)
+{
+    if (!h || !params_valid(p) || !lambda || !dX || !iters || !status)
+        return GATO_ERR_INVALID_ARG;
+    if (h->w.N > 1 && !dU) return GATO_ERR_INVALID_ARG;
+    const int ls = p->linsys == GATO_LINSYS_AUTO ? GATO_LINSYS_BDSV : p->linsys;
+    if (ls == GATO_LINSYS_PCG) return GATO_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    begin_timing(h, st);
+    cudaError_t err = gato::launch_bdsv_factor(h, ls, status, st);
+    if (err == cudaSuccess)
+        err = gato::launch_bdsv_solve(h, ls, 0, lambda, dX, dU, iters, 0, status, st);
+    record(h, 2, st);
+    return unsupported_or_fail(err);
+}
+
 int gato_linesearch(gato_handle* h, const gato_params* p, const float* Q, const float* R,
                     const float* q, const float* r, const float* A, const float* B,
                     const float* e, const float* s0, const float* dX, const float* dU,
                     float* merit, int32_t* best, uint32_t* status, void* stream)
 {
-    if (!h || !params_ok(p) || !lq_ok(h, Q, R, q, r, A, B, e, s0) || !dX || !merit || !best ||
+    if (!h || !params_valid(p) || !lq_ok(h, Q, R, q, r, A, B, e, s0) || !dX || !merit || !best ||
         !status)
         return GATO_ERR_INVALID_ARG;
     if (h->w.N > 1 && !dU) return GATO_ERR_INVALID_ARG;
@@ -274,41 +384,20 @@ int gato_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const f
                    int32_t* iters, float* merit, int32_t* best, uint32_t* status,
                    void* stream)
 {
-    if (!h || !params_ok(p) || !lq_ok(h, Q, R, q, r, A, B, e, s0) || !dX || !lambda ||
+    if (!h || !params_valid(p) || !lq_ok(h, Q, R, q, r, A, B, e, s0) || !dX || !lambda ||
         !iters || !merit || !best || !status)
         return GATO_ERR_INVALID_ARG;
     if (h->w.N > 1 && !dU) return GATO_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;
-    Work& w = h->w;
     begin_timing(h, st);
-    cudaError_t err = gato::launch_form_matrices(h, Q, R, A, B, status, st);
-    if (err == cudaSuccess) err = gato::launch_form_rhs(h, 0, q, r, e, s0, (size_t)w.n, st);
-    record(h, 1, st);
-    if (err == cudaSuccess)
-        err = gato::launch_pcg_ex(h, p, 0, nullptr, lambda, dX, dU, iters, 0, status, st);
-    record(h, 2, st);
-    gato_params pc = *p;  // corrections are solved to refine_eps
-    if (p->refine_eps > 0.f) pc.pcg_eps = p->refine_eps;
-    for (int k = 0; k < p->refine_steps && err == cudaSuccess; ++k) {
-        err = gato::launch_kkt_residual(h, Q, R, q, r, A, B, e, s0, dX, dU, lambda, st);
-        if (err == cudaSuccess)
-            err = gato::launch_form_rhs(h, 1, w.q2, w.r2, w.e2, w.s02, (size_t)w.n, st);
-        if (err == cudaSuccess)
-            err = gato::launch_pcg_ex(h, &pc, 1, nullptr, w.dlam, w.ddX, w.ddU, iters, 1, status, st);
-        if (err == cudaSuccess) err = gato::launch_accumulate(h, lambda, dX, dU, iters, st);
-    }
-    if (p->refine_steps > 0) record(h, 3, st);
-    if (err == cudaSuccess)
-        err = gato::launch_merit(h, p, Q, R, q, r, A, B, e, s0, dX, dU, merit, best, status, st);
-    record(h, 4, st);
-    if (err == cudaErrorInvalidConfiguration) return GATO_ERR_UNSUPPORTED;
-    return cuda_fail(err);
+    return unsupported_or_fail(gato::run_solve_kkt(h, p, Q, R, q, r, A, B, e, s0, dX, dU,
+                                                   lambda, iters, merit, best, status, st));
 }
 
 int gato_apply_step(gato_handle* h, const gato_params* p, const int32_t* best, const float* dX,
                     const float* dU, float* X, float* U, void* stream)
 {
-    if (!h || !params_ok(p) || !best || !dX || !X) return GATO_ERR_INVALID_ARG;
+    if (!h || !params_valid(p) || !best || !dX || !X) return GATO_ERR_INVALID_ARG;
     if (h->w.N > 1 && (!dU || !U)) return GATO_ERR_INVALID_ARG;
     return cuda_fail(gato::launch_apply_step(h, p, best, dX, dU, X, U, (cudaStream_t)stream));
 }

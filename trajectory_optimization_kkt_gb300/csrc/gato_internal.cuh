@@ -60,6 +60,19 @@ struct Work {
     float* dlam;   // [N][n]
     float* ddX;    // [N][n]
     float* ddU;    // [N-1][m]
+    // direct block-tridiagonal solve of S_hat lambda_hat = ghat (S_hat =
+    // L^-1 S L^-T: identity diagonal blocks, coupling blocks Nhat_j).
+    // Cyclic reduction: for a knot eliminated at stride s >= 2, Bd holds
+    // F = C^-1 (C C^T its reduced diagonal block), Be X = F E (E its coupling
+    // to the active knot s to the left) and By Y = F E_right^T; knot 0 ends
+    // with F_0 of the last reduced block in Bd.  Chronological order: Bd holds
+    // F_j = C_j^-1 and Be W_j = Nhat_j F_{j-1}^T of S_hat = L L^T, L block
+    // lower bidiagonal with diagonal C_j and sub-diagonal W_j.
+    float* Bd;     // [N] n x n
+    float* Be;     // [N] n x n
+    float* By;     // [N] n x n
+    float* Bv;     // [N][n] vector scratch of the substitution when it does not
+    float* Bg;     // [N][n] fit in shared memory
     // line search partial sums
     float2* mpart; // [(A+1)][N] (cost, violation) per knot and candidate
     int* queue;    // work counters of the persistent kernels (not per solve)
@@ -76,6 +89,7 @@ struct gato_handle {
     size_t bytes;
     int timing;
     int pcg_kernel;         // GATO_PCG_* selected by gato_set_pcg_kernel
+    int bdsv_kernel;        // GATO_BDSV_KERNEL_* selected by gato_set_bdsv_kernel
     int force_smem_form;    // GATO_FORM_SHARED selected by gato_set_form_kernel
     cudaEvent_t ev[5];  // start, after form, after PCG, after refinement, after merit
     int ev_used[5];
@@ -118,6 +132,29 @@ cudaError_t launch_merit(gato_handle* h, const gato_params* p, const float* Q,
 cudaError_t launch_apply_step(gato_handle* h, const gato_params* p, const int32_t* best,
                               const float* dX, const float* dU, float* X, float* U,
                               cudaStream_t st);
+// direct solve (bdsv.cu): factorisation of S_hat in the order `order`
+// (GATO_LINSYS_BDSV or GATO_LINSYS_BDSV_CHRONO), then substitution for the
+// right-hand side set `set` and recovery of dz; iters[] gets 0 (or nothing
+// added when acc_iters)
+cudaError_t launch_bdsv_factor(gato_handle* h, int order, uint32_t* status, cudaStream_t st);
+cudaError_t launch_bdsv_solve(gato_handle* h, int order, int set, float* lambda, float* dX,
+                              float* dU, int32_t* iters, int acc_iters, uint32_t* status,
+                              cudaStream_t st);
+
+// workspace layout shared by gato_create and the allocation-free entry point:
+// sets every pointer of w from base (when base != NULL) and returns the bytes
+size_t carve_workspace(Work& w, int M, int N, int n, int m, float* base);
+bool params_valid(const gato_params* p);
+// the linear solver a call with parameters p uses: GATO_LINSYS_PCG,
+// GATO_LINSYS_BDSV or GATO_LINSYS_BDSV_CHRONO
+int linsys_for(const gato_params* p, int N);
+// the whole gato_solve_kkt sequence on stream st (events recorded when the
+// handle times)
+cudaError_t run_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const float* R,
+                          const float* q, const float* r, const float* A, const float* B,
+                          const float* e, const float* s0, float* dX, float* dU, float* lambda,
+                          int32_t* iters, float* merit, int32_t* best, uint32_t* status,
+                          cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // device helpers
@@ -230,6 +267,57 @@ __device__ inline void warp_gemv(int rows, int cols, const float* M, const float
         y[i] = acc ? y[i] + s * v : s * v;
     }
     __syncwarp();
+}
+
+// Recovery after a solve of S_hat lambda_hat = ghat (GATO paper, eq. (4)):
+// lambda = L^-T lambda_hat, then dx_k = -Q_k^-1 q_k + Q_k^-1 lambda_k
+// + S_{k+1,k}^T lambda_{k+1} and du_k = -R_k^-1 r_k - (B_k R_k^-1)^T
+// lambda_{k+1}, with the -Q^-1 q and -R^-1 r parts taken from the rhs set.
+// Block-wide (all threads of the block, one solve); lhat(j, a) reads
+// lambda_hat; lsm is an N n scratch in shared memory.
+template <typename LhatFn>
+__device__ inline void recover_dz(const Work& w, const Rhs& rhs, float* lambda, float* dX,
+                                  float* dU, int sol, LhatFn lhat, float* lsm)
+{
+    const int N = w.N, n = w.n, m = w.m, Nn = N * n, T = blockDim.x, tid = threadIdx.x;
+    const float* gLi = w.Linv + sol * w.sNnn;
+    for (int i = tid; i < Nn; i += T) {
+        const int j = i / n, a = i - j * n;
+        const float* Li = gLi + (size_t)j * n * n;
+        float x = 0.f;
+        for (int b = a; b < n; ++b) x += Li[b * n + a] * lhat(j, b);
+        lambda[(size_t)sol * Nn + i] = x;
+        lsm[i] = x;
+    }
+    __syncthreads();
+    const float* Qi = w.Qinv + sol * w.sNnn;
+    const float* Ob = w.O + sol * w.sKnn;
+    const float* av = rhs.avec + sol * w.sNn;
+    for (int i = tid; i < Nn; i += T) {
+        const int k = i / n, a = i - k * n;
+        float x = av[i];
+        const float* Qrow = Qi + (size_t)k * n * n + a * n;
+        float t = 0.f;
+        for (int b = 0; b < n; ++b) t += Qrow[b] * lsm[k * n + b];
+        x += t;
+        if (k < N - 1) {
+            const float* Oc = Ob + (size_t)k * n * n + a;  // S_{k+1,k}, column a
+            float u = 0.f;
+            for (int b = 0; b < n; ++b) u += Oc[b * n] * lsm[(k + 1) * n + b];
+            x += u;
+        }
+        dX[(size_t)sol * Nn + i] = x;
+    }
+    const int Km = (N - 1) * m;
+    const float* Vb = w.V + sol * w.sKnm;
+    const float* bv = rhs.bvec + sol * w.sKm;
+    for (int t = tid; t < Km; t += T) {
+        const int k = t / m, c = t - k * m;
+        const float* Vc = Vb + (size_t)k * n * m + c;  // column c of B_k R_k^-1
+        float u = 0.f;
+        for (int b = 0; b < n; ++b) u += Vc[b * m] * lsm[(k + 1) * n + b];
+        dU[(size_t)sol * Km + t] = bv[t] - u;
+    }
 }
 
 #endif  // __CUDACC__

@@ -52,63 +52,6 @@ int scratch_address(int device, void** out)
     return GATO_OK;
 }
 
-size_t round64(size_t x)
-{
-    const size_t r = (x + 63) / 64 * 64;
-    return r ? r : 64;
-}
-
-// The same workspace layout gato_create uses, placed at `base` (or, with
-// base == nullptr, only sized).  Returns the bytes needed.
-size_t carve(Work& w, int M, int N, int n, int m, float* base)
-{
-    w.M = M; w.N = N; w.n = n; w.m = m;
-    const size_t K = (size_t)(N - 1);
-    w.sNnn = round64((size_t)N * n * n);
-    w.sKnn = round64(K * n * n);
-    w.sKmm = round64(K * m * m);
-    w.sKnm = round64(K * n * m);
-    w.sNn = round64((size_t)N * n);
-    w.sN = round64((size_t)N);
-    w.sKm = round64(K * m);
-    w.sK2 = (size_t)N * (GATO_MAX_ALPHA + 1);
-    float** fields[] = {&w.Qinv, &w.Rinv, &w.O, &w.V, &w.D, &w.L, &w.Linv, &w.Pd, &w.Po, &w.Nh,
-                        &w.dlow,
-                        &w.rhs[0].gamma, &w.rhs[0].ghat, &w.rhs[0].avec, &w.rhs[0].bvec,
-                        &w.rhs[1].gamma, &w.rhs[1].ghat, &w.rhs[1].avec, &w.rhs[1].bvec,
-                        &w.q2, &w.r2, &w.e2, &w.s02, &w.dlam, &w.ddX, &w.ddU};
-    const size_t strides[] = {w.sNnn, w.sKmm, w.sKnn, w.sKnm, w.sNnn, w.sNnn, w.sNnn,
-                              w.sNnn, w.sKnn, w.sKnn, w.sN, w.sNn, w.sNn, w.sNn, w.sKm,
-                              w.sNn, w.sNn, w.sNn, w.sKm,
-                              w.sNn, w.sKm, w.sNn, w.sNn, w.sNn, w.sNn, w.sKm};
-    const int nf = (int)(sizeof(strides) / sizeof(strides[0]));
-    size_t total = 0;
-    for (int i = 0; i < nf; ++i) {
-        if (base) *fields[i] = base + total;
-        total += strides[i] * (size_t)M;
-    }
-    if (base) w.mpart = (float2*)(base + total);
-    total += 2 * w.sK2 * (size_t)M;
-    if (base) w.queue = (int*)(base + total);
-    total += 64;  // work counters
-    return total * sizeof(float);
-}
-
-bool params_ok(const gato_params* p)
-{
-    if (!p) return false;
-    if (!(p->pcg_eps >= 0.f) || p->pcg_max_iters < 0) return false;
-    if (p->stop_rule < GATO_STOP_RESIDUAL || p->stop_rule > GATO_STOP_SCALED) return false;
-    if (p->refine_steps < 0 || p->refine_steps > 16) return false;
-    if (p->n_alpha < 1 || p->n_alpha > GATO_MAX_ALPHA) return false;
-    if (!(p->beta > 1.f) || !(p->mu >= 0.f)) return false;
-    if (p->merit_threads < 32 || p->merit_threads > 256 || p->merit_threads % 32) return false;
-    if (!(p->refine_eps >= 0.f)) return false;
-    if (p->merit_kernel != GATO_MERIT_FUSED && p->merit_kernel != GATO_MERIT_PER_CANDIDATE)
-        return false;
-    return true;
-}
-
 }  // namespace
 
 extern "C" int gato_solve_kkt_noalloc(const gato_params* p, int M, int N, int n, int m,
@@ -120,15 +63,15 @@ extern "C" int gato_solve_kkt_noalloc(const gato_params* p, int M, int N, int n,
 {
     if (M < 1 || N < 1 || n < 1 || m < 1) return GATO_ERR_INVALID_ARG;
     if (n > GATO_MAX_STATE || m > GATO_MAX_CONTROL) return GATO_ERR_UNSUPPORTED;
-    if (!params_ok(p) || !Q || !q || !s0 || !dX || !lambda || !iters || !merit || !best ||
-        !status)
+    if (!gato::params_valid(p) || !Q || !q || !s0 || !dX || !lambda || !iters || !merit ||
+        !best || !status)
         return GATO_ERR_INVALID_ARG;
     if (N > 1 && (!R || !r || !A || !B || !e || !dU)) return GATO_ERR_INVALID_ARG;
     Work probe;
-    if (carve(probe, M, N, n, m, nullptr) > (size_t)GATO_NOALLOC_MAX_BYTES)
+    if (gato::carve_workspace(probe, M, N, n, m, nullptr) > (size_t)GATO_NOALLOC_MAX_BYTES)
         return GATO_ERR_UNSUPPORTED;
 
-    gato_handle h{};  // on the stack: nothing is allocated
+    gato_handle h{};  // on the stack: nothing is allocated, no timing events
     if (cudaGetDevice(&h.device) != cudaSuccess ||
         cudaDeviceGetAttribute(&h.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
                                h.device) != cudaSuccess ||
@@ -139,27 +82,10 @@ extern "C" int gato_solve_kkt_noalloc(const gato_params* p, int M, int N, int n,
     const int rc = scratch_address(h.device, &base);
     if (rc != GATO_OK) return rc;
     h.base = base;
-    h.bytes = carve(h.w, M, N, n, m, (float*)base);
+    h.bytes = gato::carve_workspace(h.w, M, N, n, m, (float*)base);
 
-    cudaStream_t st = (cudaStream_t)stream;
-    Work& w = h.w;
-    cudaError_t err = gato::launch_form_matrices(&h, Q, R, A, B, status, st);
-    if (err == cudaSuccess) err = gato::launch_form_rhs(&h, 0, q, r, e, s0, (size_t)n, st);
-    if (err == cudaSuccess)
-        err = gato::launch_pcg_ex(&h, p, 0, nullptr, lambda, dX, dU, iters, 0, status, st);
-    gato_params pc = *p;
-    if (p->refine_eps > 0.f) pc.pcg_eps = p->refine_eps;
-    for (int k = 0; k < p->refine_steps && err == cudaSuccess; ++k) {
-        err = gato::launch_kkt_residual(&h, Q, R, q, r, A, B, e, s0, dX, dU, lambda, st);
-        if (err == cudaSuccess)
-            err = gato::launch_form_rhs(&h, 1, w.q2, w.r2, w.e2, w.s02, (size_t)n, st);
-        if (err == cudaSuccess)
-            err = gato::launch_pcg_ex(&h, &pc, 1, nullptr, w.dlam, w.ddX, w.ddU, iters, 1,
-                                      status, st);
-        if (err == cudaSuccess) err = gato::launch_accumulate(&h, lambda, dX, dU, iters, st);
-    }
-    if (err == cudaSuccess)
-        err = gato::launch_merit(&h, p, Q, R, q, r, A, B, e, s0, dX, dU, merit, best, status, st);
+    const cudaError_t err = gato::run_solve_kkt(&h, p, Q, R, q, r, A, B, e, s0, dX, dU, lambda,
+                                                iters, merit, best, status, (cudaStream_t)stream);
     if (err == cudaErrorInvalidConfiguration) return GATO_ERR_UNSUPPORTED;
     return err == cudaSuccess ? GATO_OK : GATO_ERR_CUDA;
 }

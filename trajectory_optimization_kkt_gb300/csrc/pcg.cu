@@ -92,14 +92,6 @@ __device__ __forceinline__ void post2(float a, float b, float2* buf)
     if ((lane & 15) == 0) slot[hi ? 1 : 0] = keep;
 }
 
-// one value into the .x (y = false) or .y (y = true) field of the warp's slot
-__device__ __forceinline__ void post1(float a, float2* buf, bool y)
-{
-    a = warp_sum(a);
-    float* slot = reinterpret_cast<float*>(buf + (threadIdx.x >> 5));
-    if (lane_id() == 0) slot[y ? 1 : 0] = a;
-}
-
 __device__ __forceinline__ float2 collect2(const float2* buf)
 {
     // the low half-warp sums the .x fields of the (at most 16) warp slots,
@@ -113,55 +105,6 @@ __device__ __forceinline__ float2 collect2(const float2* buf)
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return make_float2(__shfl_sync(0xffffffffu, v, 0), __shfl_sync(0xffffffffu, v, 16));
-}
-
-// ---------------------------------------------------------------------------
-// epilogue shared by both kernels: lambda = L^-T lambda_hat and recovery of
-// dz.  lhat(j, a) reads lambda_hat; lsm is an N n scratch in shared memory.
-// ---------------------------------------------------------------------------
-template <typename LhatFn>
-__device__ __forceinline__ void recover_dz(const PcgArgs& g, int sol, LhatFn lhat, float* lsm)
-{
-    const Work& w = g.w;
-    const int N = w.N, n = w.n, m = w.m, Nn = N * n, T = blockDim.x, tid = threadIdx.x;
-    const float* gLi = w.Linv + sol * w.sNnn;
-    for (int i = tid; i < Nn; i += T) {
-        const int j = i / n, a = i - j * n;
-        const float* Li = gLi + (size_t)j * n * n;
-        float x = 0.f;
-        for (int b = a; b < n; ++b) x += Li[b * n + a] * lhat(j, b);
-        g.lambda[(size_t)sol * Nn + i] = x;
-        lsm[i] = x;
-    }
-    __syncthreads();
-    const float* Qi = w.Qinv + sol * w.sNnn;
-    const float* Ob = w.O + sol * w.sKnn;
-    const float* av = g.rhs.avec + sol * w.sNn;
-    for (int i = tid; i < Nn; i += T) {
-        const int k = i / n, a = i - k * n;
-        float x = av[i];
-        const float* Qrow = Qi + (size_t)k * n * n + a * n;
-        float t = 0.f;
-        for (int b = 0; b < n; ++b) t += Qrow[b] * lsm[k * n + b];
-        x += t;
-        if (k < N - 1) {
-            const float* Oc = Ob + (size_t)k * n * n + a;  // S_{k+1,k}, column a
-            float u = 0.f;
-            for (int b = 0; b < n; ++b) u += Oc[b * n] * lsm[(k + 1) * n + b];
-            x += u;
-        }
-        g.dX[(size_t)sol * Nn + i] = x;
-    }
-    const int Km = (N - 1) * m;
-    const float* Vb = w.V + sol * w.sKnm;
-    const float* bv = g.rhs.bvec + sol * w.sKm;
-    for (int t = tid; t < Km; t += T) {
-        const int k = t / m, c = t - k * m;
-        const float* Vc = Vb + (size_t)k * n * m + c;  // column c of B_k R_k^-1
-        float u = 0.f;
-        for (int b = 0; b < n; ++b) u += Vc[b * m] * lsm[(k + 1) * n + b];
-        g.dU[(size_t)sol * Km + t] = bv[t] - u;
-    }
 }
 
 __device__ __forceinline__ void finish(const PcgArgs& g, int sol, int it, bool done,
@@ -338,7 +281,8 @@ __global__ void __launch_bounds__(512) k_pcg_generic(PcgArgs g)
         __syncthreads();
     }
     __syncthreads();
-    recover_dz(g, sol, [&](int j, int b) { return lam[j * n + b]; }, r);
+    recover_dz(g.w, g.rhs, g.lambda, g.dX, g.dU, sol,
+               [&](int j, int b) { return lam[j * n + b]; }, r);
     finish(g, sol, it, done, nonfinite);
 }
 
@@ -660,7 +604,8 @@ __device__ __forceinline__ void pcg_tile_solve(const PcgArgs& g, int sol)
     __syncthreads();
     if (owner) store4(XP, e0, lam);
     __syncthreads();
-    recover_dz(g, sol, [&](int j, int b) { return XP[j * 16 + (b / H) * 8 + b % H]; }, YR0);
+    recover_dz(g.w, g.rhs, g.lambda, g.dX, g.dU, sol,
+               [&](int j, int b) { return XP[j * 16 + (b / H) * 8 + b % H]; }, YR0);
     finish(g, sol, it, done, nonfinite);
 }
 

@@ -27,6 +27,14 @@ GATO_STATUS_NONFINITE = 8
 GATO_PCG_AUTO = 0
 GATO_PCG_GENERIC = 1
 
+GATO_LINSYS_AUTO = 0
+GATO_LINSYS_PCG = 1
+GATO_LINSYS_BDSV = 2
+GATO_LINSYS_BDSV_CHRONO = 3
+
+GATO_BDSV_KERNEL_AUTO = 0
+GATO_BDSV_KERNEL_SHARED = 1
+
 GATO_FORM_AUTO = 0
 GATO_FORM_SHARED = 1
 
@@ -46,7 +54,8 @@ class GatoParams(ctypes.Structure):
                 ("stop_rule", ctypes.c_int), ("refine_steps", ctypes.c_int),
                 ("n_alpha", ctypes.c_int), ("beta", ctypes.c_float), ("mu", ctypes.c_float),
                 ("merit_threads", ctypes.c_int), ("refine_eps", ctypes.c_float),
-                ("merit_kernel", ctypes.c_int)]
+                ("merit_kernel", ctypes.c_int), ("linsys", ctypes.c_int),
+                ("bdsv_horizon", ctypes.c_int)]
 
 
 class GatoStats(ctypes.Structure):
@@ -87,18 +96,20 @@ def load(path: Optional[str] = None):
     lib.gato_set_timing.argtypes = [vp, ip]
     lib.gato_set_pcg_kernel.argtypes = [vp, ip]
     lib.gato_set_form_kernel.argtypes = [vp, ip]
+    lib.gato_set_bdsv_kernel.argtypes = [vp, ip]
     lib.gato_get_stats.argtypes = [vp, ctypes.POINTER(GatoStats)]
     lib.gato_form_schur.argtypes = [vp] + [vp] * 8 + [vp, vp]
     lib.gato_get_schur.argtypes = [vp] + [vp] * 5 + [vp]
     lib.gato_pcg_solve.argtypes = [vp, P] + [vp] * 6 + [vp]
+    lib.gato_bdsv_solve.argtypes = [vp, P] + [vp] * 5 + [vp]
     lib.gato_linesearch.argtypes = [vp, P] + [vp] * 8 + [vp] * 5 + [vp]
     lib.gato_solve_kkt.argtypes = [vp, P] + [vp] * 8 + [vp] * 7 + [vp]
     lib.gato_apply_step.argtypes = [vp, P] + [vp] * 5 + [vp]
     lib.gato_solve_kkt_noalloc.argtypes = [P, ip, ip, ip, ip] + [vp] * 8 + [vp] * 7 + [vp]
     for fn in ("gato_create", "gato_set_timing", "gato_set_pcg_kernel", "gato_set_form_kernel",
-               "gato_get_stats", "gato_form_schur",
-               "gato_get_schur", "gato_pcg_solve", "gato_linesearch", "gato_solve_kkt",
-               "gato_apply_step", "gato_solve_kkt_noalloc"):
+               "gato_set_bdsv_kernel", "gato_get_stats", "gato_form_schur",
+               "gato_get_schur", "gato_pcg_solve", "gato_bdsv_solve", "gato_linesearch",
+               "gato_solve_kkt", "gato_apply_step", "gato_solve_kkt_noalloc"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -182,6 +193,9 @@ class Solver:
     def set_pcg_kernel(self, kind: int):
         _check("gato_set_pcg_kernel", self.lib.gato_set_pcg_kernel(self.h, kind))
 
+    def set_bdsv_kernel(self, kind: int):
+        _check("gato_set_bdsv_kernel", self.lib.gato_set_bdsv_kernel(self.h, kind))
+
     def set_form_kernel(self, kind: int):
         _check("gato_set_form_kernel", self.lib.gato_set_form_kernel(self.h, kind))
 
@@ -205,6 +219,13 @@ class Solver:
         import torch
         _check("gato_pcg_solve", self.lib.gato_pcg_solve(
             self.h, ctypes.byref(params), _ptr(lambda0), _ptr(lam), _ptr(dX), _ptr(dU),
+            _ptr(iters, torch.int32, "iters"), _ptr(status, torch.int32, "status"),
+            _stream(stream)))
+
+    def bdsv_solve(self, params, lam, dX, dU, iters, status, stream=None):
+        import torch
+        _check("gato_bdsv_solve", self.lib.gato_bdsv_solve(
+            self.h, ctypes.byref(params), _ptr(lam), _ptr(dX), _ptr(dU),
             _ptr(iters, torch.int32, "iters"), _ptr(status, torch.int32, "status"),
             _stream(stream)))
 
@@ -258,4 +279,5 @@ def solve_kkt_noalloc(params, prob, dX, dU, lam, iters, merit, best, status, str
 def to_device(prob, device="cuda"):
     """numpy workload dict -> contiguous float32 CUDA tensors."""
     import torch
-    return {k: torch.as_tensor(v, dtype=torch.float32).contiguous().to(device) for k, v in prob.items()}
+    return {k: torch.as_tensor(v, dtype=torch.float32).contiguous().to(device)
+            for k, v in prob.items()}
