@@ -64,6 +64,7 @@ def _load():
             lib.oracle_merit.restype = d
             lib.oracle_linesearch.argtypes = lq + [_D, _D, i, d, d, _D]
             lib.oracle_solve_kkt.argtypes = lq + [d, i, i, i, d, d, _D, _D, _D, pi, _D, pi]
+            lib.oracle_sqp_linear.argtypes = lq + [i, d, d, d, d, i, d, d, _D, _D, _D, _D, pi, _D]
             _lib = lib
     return _lib
 
@@ -247,3 +248,38 @@ def batch_solve_kkt(prob, solves=None, **kw):
     M = prob["Q"].shape[0]
     solves = range(M) if solves is None else solves
     return [solve_kkt(solve_one(prob, j), **kw) for j in solves]
+
+
+# ----------------------------------------------------------------------------
+# SQP on the linear model (x_{k+1} = A_k x_k + B_k u_k + c_k, x_0 = xs)
+# ----------------------------------------------------------------------------
+
+_MODEL_KEYS = ("Q", "R", "q", "r", "A", "B", "c", "xs")
+
+
+def sqp_linear(model, iters, rho, rho_factor=10.0, rho_min=1e-8, rho_max=10.0, n_alpha=8,
+               beta=2.0, mu=10.0, X0=None, U0=None):
+    """fp64 SQP loop on one linear-model problem (model holds Q, R, q, r, A,
+    B, c, xs of one solve); starts from (X0, U0), zero by default.  Returns
+    dict(X, U, lam, merit_hist [iters+1], best_hist [iters], rho_hist
+    [iters+1], status)."""
+    L = _load()
+    N, n, m = _dims(model, batched=False)
+    arr = [_f64(model[k]) for k in _MODEL_KEYS]
+    X = np.zeros((N, n)) if X0 is None else _f64(X0).copy()
+    U = np.zeros((max(N - 1, 0), m)) if U0 is None else _f64(U0).copy()
+    lam = np.zeros((N, n))
+    hist, rhos = np.zeros(iters + 1), np.zeros(iters + 1)
+    best = np.zeros(iters, dtype=np.int32)
+    status = L.oracle_sqp_linear(N, n, m, *[_p(a) for a in arr], int(iters), float(rho),
+                                 float(rho_factor), float(rho_min), float(rho_max),
+                                 int(n_alpha), float(beta), float(mu), _p(X), _p(U), _p(lam),
+                                 _p(hist), best.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+                                 _p(rhos))
+    return dict(X=X, U=U, lam=lam, merit_hist=hist, best_hist=best, rho_hist=rhos,
+                status=status)
+
+
+def model_one(model, j: int) -> Dict[str, np.ndarray]:
+    """Problem j of a batch of linear models as a single-problem dict."""
+    return {k: model[k][j] for k in _MODEL_KEYS}

@@ -655,3 +655,103 @@ int oracle_solve_kkt(int N, int n, int m, const double *Q, const double *R,
     free(Dg); free(Off); free(Pd); free(Po); free(gamma);
     return status;
 }
+
+/* ------------------------------------------------------------------------ */
+/* SQP on a linear model with rho damping (Sec. II steps 1-3; Sec. IV-C)     */
+/* ------------------------------------------------------------------------ */
+/*
+ * The problem (a linear model in place of the robot dynamics):
+ *   minimize  J(X, U) = sum_k 1/2 x_k^T Q_k x_k + q_k^T x_k
+ *                     + sum_{k<N-1} 1/2 u_k^T R_k u_k + r_k^T u_k
+ *   s.t.      x_0 = xs,   x_{k+1} = A_k x_k + B_k u_k + c_k.
+ * One SQP iteration at the nominal (X, U), in the paper's three steps:
+ *   1. the quadratic program of the expansion along (X, U) -- exact for this
+ *      model: gradients q_k + Q_k x_k and r_k + R_k u_k, defects
+ *      e_k = A_k x_k + B_k u_k + c_k - x_{k+1} and s0 = xs - x_0, with the
+ *      damping rho added to the diagonal of every Q_k (Sec. IV-C);
+ *   2. its KKT solution dz (computed exactly here: Schur complement, block
+ *      Cholesky, recovery);
+ *   3. the line search on the L1 merit of the problem itself (undamped Q):
+ *      oracle_linesearch on the expansion's data gives M(X + a dX, U + a dU)
+ *      - J(X, U), and (X, U) += a* dz when a candidate beats a = 0.
+ * The damping follows the line search (reading of "adjusted after each SQP
+ * iteration based on the status of the line search"): rho <- max(rho / f,
+ * rho_min) after an accepted step, min(rho f, rho_max) after a failed one.
+ * Outputs: X, U updated in place; merit_hist[0] the merit at the start and
+ * merit_hist[t + 1] after iteration t; best_hist[t] the line-search index
+ * (-1 on failure); rho_hist[t] the rho of iteration t and rho_hist[iters] the
+ * final one; lambda the multipliers of the last subproblem.  Returns a
+ * status mask: 2 a non-positive pivot, 4 some line search failed.
+ */
+int oracle_sqp_linear(int N, int n, int m, const double *Q, const double *R,
+                      const double *q, const double *r, const double *A,
+                      const double *B, const double *c, const double *xs, int iters,
+                      double rho, double rho_factor, double rho_min, double rho_max,
+                      int n_alpha, double beta, double mu, double *X, double *U,
+                      double *lambda, double *merit_hist, int *best_hist, double *rho_hist)
+{
+    const int K = N > 1 ? N - 1 : 1;
+    int status = 0;
+    double *Qd = malloc(sizeof(double) * N * n * n);
+    double *qt = malloc(sizeof(double) * N * n), *rt = malloc(sizeof(double) * K * m);
+    double *et = malloc(sizeof(double) * K * n), *s0t = malloc(sizeof(double) * n);
+    double *Dg = malloc(sizeof(double) * N * n * n), *Off = malloc(sizeof(double) * K * n * n);
+    double *gamma = malloc(sizeof(double) * N * n);
+    double *dX = malloc(sizeof(double) * N * n), *dU = malloc(sizeof(double) * K * m);
+    double *merit = malloc(sizeof(double) * (n_alpha + 1));
+    double *t = malloc(sizeof(double) * (n > m ? n : m));
+    for (int it = 0; it < iters; ++it) {
+        /* step 1: expansion along (X, U) and J(X, U) */
+        double J = 0.0;
+        for (int k = 0; k < N; ++k) {
+            const double *x = X + k * n;
+            gemv(n, n, Q + k * n * n, 0, x, t);
+            for (int i = 0; i < n; ++i) qt[k * n + i] = t[i] + q[k * n + i];
+            J += 0.5 * dot(n, x, t) + dot(n, q + k * n, x);
+            for (int i = 0; i < n * n; ++i) Qd[k * n * n + i] = Q[k * n * n + i];
+            for (int i = 0; i < n; ++i) Qd[k * n * n + i * n + i] += rho;
+            if (k < N - 1) {
+                const double *u = U + k * m;
+                gemv(m, m, R + k * m * m, 0, u, t);
+                for (int i = 0; i < m; ++i) rt[k * m + i] = t[i] + r[k * m + i];
+                J += 0.5 * dot(m, u, t) + dot(m, r + k * m, u);
+                for (int i = 0; i < n; ++i) {
+                    double s = c[k * n + i] - X[(k + 1) * n + i];
+                    for (int j = 0; j < n; ++j) s += A[k * n * n + i * n + j] * x[j];
+                    for (int j = 0; j < m; ++j) s += B[k * n * m + i * m + j] * u[j];
+                    et[k * n + i] = s;
+                }
+            }
+        }
+        for (int i = 0; i < n; ++i) s0t[i] = xs[i] - X[i];
+        rho_hist[it] = rho;
+        /* step 2: the damped subproblem's KKT solution */
+        if (oracle_schur(N, n, m, Qd, R, qt, rt, A, B, et, s0t, Dg, Off, gamma) ||
+            oracle_block_cholesky(N, n, Dg, Off, gamma, lambda) ||
+            oracle_recover(N, n, m, Qd, R, qt, rt, A, B, lambda, dX, dU))
+            status |= 2;
+        /* step 3: line search on the problem's own merit */
+        const int best = oracle_linesearch(N, n, m, Q, R, qt, rt, A, B, et, s0t, dX, dU,
+                                           n_alpha, beta, mu, merit);
+        if (it == 0) merit_hist[0] = J + merit[0];
+        best_hist[it] = best;
+        if (best >= 0) {
+            double alpha = 1.0;
+            for (int i = 0; i < best; ++i) alpha /= beta;
+            for (int i = 0; i < N * n; ++i) X[i] += alpha * dX[i];
+            for (int i = 0; i < (N - 1) * m; ++i) U[i] += alpha * dU[i];
+            merit_hist[it + 1] = J + merit[1 + best];
+            rho = rho / rho_factor;
+            if (rho < rho_min) rho = rho_min;
+        } else {
+            status |= 4;
+            merit_hist[it + 1] = J + merit[0];
+            rho = rho * rho_factor;
+            if (rho > rho_max) rho = rho_max;
+        }
+    }
+    rho_hist[iters] = rho;
+    free(Qd); free(qt); free(rt); free(et); free(s0t); free(Dg); free(Off); free(gamma);
+    free(dX); free(dU); free(merit); free(t);
+    return status;
+}

@@ -164,3 +164,38 @@ def random_lq(M: int, N: int, n: int, m: int, seed: int, **kw) -> Dict[str, np.n
     w = Workload(99, "custom", M, N, n, m, **kw)
     solves = [make_solve(w, seed + j) for j in range(M)]
     return {k: np.ascontiguousarray(np.stack([s[k] for s in solves])) for k in solves[0]}
+
+
+# ---------------------------------------------------------------------------
+# linear-model problems for the SQP loop: minimise the quadratic cost subject
+# to x_0 = xs and x_{k+1} = A_k x_k + B_k u_k + c_k.  The affine term c and the
+# initial state xs are the generator's e and s0 draws; at the zero trajectory
+# the SQP loop's first subproblem is therefore exactly the workload's LQ
+# subproblem.
+# ---------------------------------------------------------------------------
+
+def as_linear_model(batch: Dict[str, np.ndarray]) -> Dict[str, np.ndarray]:
+    """An LQ batch read as linear-model problems (e -> c, s0 -> xs)."""
+    out = {k: v for k, v in batch.items() if k not in ("e", "s0")}
+    out["c"], out["xs"] = batch["e"], batch["s0"]
+    return out
+
+
+def linear_models(M: int, N: int, n: int, m: int, seed: int, **kw) -> Dict[str, np.ndarray]:
+    """``M`` linear-model problems of arbitrary sizes, generated like random_lq."""
+    return as_linear_model(random_lq(M, N, n, m, seed, **kw))
+
+
+def replicate(problem: Dict[str, np.ndarray], M: int) -> Dict[str, np.ndarray]:
+    """One problem (arrays without the batch axis) repeated ``M`` times: the
+    batch of a sweep over a solver parameter such as the damping rho."""
+    return {k: np.ascontiguousarray(np.broadcast_to(v, (M,) + v.shape)) for k, v in
+            problem.items()}
+
+
+def rho_logspace(M: int, lo: float = 1e-8, hi: float = 10.0) -> np.ndarray:
+    """Initial damping of a batch of M solves of one problem: log-spaced from
+    lo to hi (GATO paper Sec. IV-C); a single solve starts at 0.1 there."""
+    if M == 1:
+        return np.array([0.1], dtype=np.float32)
+    return np.logspace(np.log10(lo), np.log10(hi), M).astype(np.float32)
