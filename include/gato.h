@@ -132,6 +132,21 @@ typedef struct gato_params {
                             (default 256); >= 1                                    */
 } gato_params;
 
+/* SQP loop on a linear model (gato_sqp_linear). */
+typedef struct gato_sqp_params {
+    int iters;           /* SQP iterations of one call, >= 1 (default 10)          */
+    float rho_factor;    /* > 1: after each line search rho <- max(rho / factor,
+                            rho_min) when a step was accepted, min(rho * factor,
+                            rho_max) when none was (default 10)                    */
+    float rho_min;       /* 0 <= rho_min <= rho_max (default 1e-8)                  */
+    float rho_max;       /* (default 10)                                            */
+    int warm_start;      /* 1: each PCG solve starts from the current lambda (the
+                            caller's on entry, then the previous iteration's);
+                            0: from zero (default 1)                               */
+    int use_graph;       /* 1: one iteration is recorded as a CUDA graph once and
+                            replayed (default); 0: launched kernel by kernel      */
+} gato_sqp_params;
+
 typedef struct gato_stats {
     float form_us;       /* device time of the last call's stages (microseconds), */
     float pcg_us;        /* filled only when timing was enabled with              */
@@ -145,10 +160,11 @@ typedef struct gato_handle gato_handle;
 
 /* Default parameters (values above). */
 void gato_default_params(gato_params* p);
+void gato_default_sqp_params(gato_sqp_params* sp);
 
 /* Creates a solver for M solves of N knots, n states and m controls on the
  * current CUDA device and allocates its device workspace (cudaMalloc; about
- * 4 M (11 N n^2 + (N-1)(m^2 + n m) + 13 N n + 4 (N-1) m + 65 N) bytes).  *h
+ * 4 M (12 N n^2 + (N-1)(m^2 + n m) + 17 N n + 6 (N-1) m + 66 N + 36) bytes).  *h
  * receives the handle, which the caller releases with gato_destroy.  Errors: INVALID_ARG (h NULL, M, N, n or
  * m < 1), UNSUPPORTED (n or m above the limits), NO_MEMORY, CUDA. */
 int gato_create(gato_handle** h, int M, int N, int n, int m);
@@ -262,6 +278,40 @@ int gato_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const f
 int gato_apply_step(gato_handle* h, const gato_params* p, const int32_t* best,
                     const float* dX, const float* dU, float* X, float* U, void* stream);
 
+/* SQP on a linear model (GATO paper Sec. II, the three steps repeated; the
+ * rho damping and its line-search-driven adjustment of Sec. IV-C).  Each of
+ * the M problems is
+ *   minimise  sum_k 1/2 x_k^T Q_k x_k + q_k^T x_k + sum_{k<N-1} 1/2 u_k^T R_k u_k + r_k^T u_k
+ *   s.t.      x_0 = xs,  x_{k+1} = A_k x_k + B_k u_k + c_k,
+ * with c [M][N-1][n] and xs [M][n] in place of e and s0 and the other inputs
+ * laid out as for gato_solve_kkt.  Starting from the trajectories X
+ * [M][N][n], U [M][N-1][m] (updated in place), each iteration
+ *   1. expands the problem along (X, U) (exact for this model): gradients
+ *      Q_k x_k + q_k, R_k u_k + r_k, defects A_k x_k + B_k u_k + c_k - x_{k+1},
+ *      xs - x_0, and adds rho[j] to the diagonal of every Q_k of problem j;
+ *   2. solves that KKT system as gato_solve_kkt does (p->linsys, refinement;
+ *      PCG warm-started from lambda when sp->warm_start);
+ *   3. runs the line search on the problem's own L1 merit (undamped Q) and
+ *      steps (X, U) += alpha* dz when a candidate beats alpha = 0;
+ *   4. divides rho[j] by sp->rho_factor after an accepted step and multiplies
+ *      it after a failed line search, clamped to [rho_min, rho_max].
+ * rho [M] (in/out) is the per-problem damping: for a sweep over rho, give the
+ * M slots the same problem and different initial rho.  lambda [M][N][n]
+ * (in/out) holds the multipliers of the last subproblem.  merit_hist
+ * [M][iters+1] receives the merit J + mu ||c||_1 at the start (column 0) and
+ * after each iteration; iters_hist [M][iters] (may be NULL) the PCG
+ * iterations of each (0 for a direct solve).  status [M] accumulates the
+ * bits of every iteration (4: some line search failed).  Stage timing is not
+ * recorded.  With sp->use_graph, the first call records one iteration as a
+ * CUDA graph on a private stream and later calls with the same arguments
+ * and parameters replay it; any change of a pointer or a parameter records
+ * it again.  Errors: INVALID_ARG (a NULL input, iters < 1, rho bounds). */
+int gato_sqp_linear(gato_handle* h, const gato_params* p, const gato_sqp_params* sp,
+                    const float* Q, const float* R, const float* q, const float* r,
+                    const float* A, const float* B, const float* c, const float* xs,
+                    float* X, float* U, float* lambda, float* rho, float* merit_hist,
+                    int32_t* iters_hist, uint32_t* status, void* stream);
+
 /* gato_solve_kkt without a handle and without allocating anything.  The
  * paper has no counterpart: this entry point exists for callers that cannot
  * allocate device memory while they run, such as a real-time MPC loop whose
@@ -270,7 +320,7 @@ int gato_apply_step(gato_handle* h, const gato_params* p, const int32_t* best,
  * n, m); the caller still provides every input and output.  The solver's
  * scratch is one static device array of GATO_NOALLOC_MAX_BYTES that every GPU
  * loading this library holds until the process exits; a problem needs about
- * 4 M (11 N n^2 + (N-1)(m^2 + n m) + 13 N n + 4 (N-1) m + 65 N) bytes of it
+ * 4 M (12 N n^2 + (N-1)(m^2 + n m) + 17 N n + 6 (N-1) m + 66 N + 36) bytes of it
  * (each array rounded up to 64 floats), and larger problems are rejected
  * with GATO_ERR_UNSUPPORTED before
  * anything is launched (use gato_create for those).  The first call on each

@@ -33,7 +33,8 @@ def test_header_declares_the_abi():
                "gato_linesearch", "gato_solve_kkt", "gato_apply_step", "gato_get_schur",
                "gato_default_params", "gato_set_timing", "gato_get_stats",
                "gato_set_pcg_kernel", "gato_set_form_kernel", "gato_solve_kkt_noalloc",
-               "gato_bdsv_solve", "gato_set_bdsv_kernel"):
+               "gato_bdsv_solve", "gato_set_bdsv_kernel", "gato_sqp_linear",
+               "gato_default_sqp_params"):
         assert fn in names
 
 
@@ -52,6 +53,22 @@ def test_default_params(lib):
     assert p.merit_kernel == gato.GATO_MERIT_FUSED
     # the GATO documentation's policy: PCG below N = 256, the direct solve from it
     assert (p.linsys, p.bdsv_horizon) == (gato.GATO_LINSYS_AUTO, 256)
+
+
+def test_default_sqp_params(lib):
+    sp = gato.default_sqp_params()
+    assert (sp.iters, sp.warm_start, sp.use_graph) == (10, 1, 1)
+    assert (sp.rho_factor, sp.rho_max) == (10.0, 10.0)
+    assert sp.rho_min == pytest.approx(1e-8)
+
+
+def test_sqp_params_struct_matches_header():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct gato_sqp_params \{(.*?)\} gato_sqp_params;", text,
+                     re.S).group(1)
+    fields = re.findall(r"\b(int|float)\s+(\w+)\s*;", body)
+    ctype = {"int": ctypes.c_int, "float": ctypes.c_float}
+    assert [(name, ctype[t]) for t, name in fields] == list(gato.GatoSqpParams._fields_)
 
 
 def test_params_struct_matches_header():
@@ -87,6 +104,9 @@ def test_invalid_arguments_rejected_before_cuda(lib):
     assert lib.gato_solve_kkt(None, ctypes.byref(p), *null, *([None] * 7), None) == gato.GATO_ERR_INVALID_ARG
     assert lib.gato_apply_step(None, ctypes.byref(p), *([None] * 5), None) == gato.GATO_ERR_INVALID_ARG
     assert lib.gato_bdsv_solve(None, ctypes.byref(p), *([None] * 5), None) == gato.GATO_ERR_INVALID_ARG
+    sp = gato.default_sqp_params()
+    assert lib.gato_sqp_linear(None, ctypes.byref(p), ctypes.byref(sp), *null, *([None] * 7),
+                               None) == gato.GATO_ERR_INVALID_ARG
 
 
 def test_generator_is_deterministic_and_distributed():

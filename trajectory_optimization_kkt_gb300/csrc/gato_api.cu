@@ -30,18 +30,23 @@ size_t carve_workspace(Work& w, int M, int N, int n, int m, float* base)
     w.sN = round64((size_t)N);
     w.sKm = round64(K * m);
     w.sK2 = (size_t)N * (GATO_MAX_ALPHA + 1);  // float2 units
+    float* ints = nullptr;  // three int arrays of M (SQP best, iterations, counter)
     // one allocation: (per-solve floats of each array) x M, in this order
     float** fields[] = {&w.Qinv, &w.Rinv, &w.O, &w.V, &w.D, &w.L, &w.Linv, &w.Pd, &w.Po, &w.Nh,
                         &w.dlow,
                         &w.rhs[0].gamma, &w.rhs[0].ghat, &w.rhs[0].avec, &w.rhs[0].bvec,
                         &w.rhs[1].gamma, &w.rhs[1].ghat, &w.rhs[1].avec, &w.rhs[1].bvec,
                         &w.q2, &w.r2, &w.e2, &w.s02, &w.dlam, &w.ddX, &w.ddU,
-                        &w.Bd, &w.Be, &w.By, &w.Bv, &w.Bg};
+                        &w.Bd, &w.Be, &w.By, &w.Bv, &w.Bg,
+                        &w.Qd, &w.qt, &w.rt, &w.et, &w.s0t, &w.Jk, &w.sdX, &w.sdU,
+                        &w.smerit, &ints};
     const size_t strides[] = {w.sNnn, w.sKmm, w.sKnn, w.sKnm, w.sNnn, w.sNnn, w.sNnn,
                               w.sNnn, w.sKnn, w.sKnn, w.sN, w.sNn, w.sNn, w.sNn, w.sKm,
                               w.sNn, w.sNn, w.sNn, w.sKm,
                               w.sNn, w.sKm, w.sNn, w.sNn, w.sNn, w.sNn, w.sKm,
-                              w.sNnn, w.sNnn, w.sNnn, w.sNn, w.sNn};
+                              w.sNnn, w.sNnn, w.sNnn, w.sNn, w.sNn,
+                              w.sNnn, w.sNn, w.sKm, w.sNn, w.sNn, w.sN, w.sNn, w.sKm,
+                              32, 4};
     static_assert(sizeof(fields) / sizeof(fields[0]) == sizeof(strides) / sizeof(strides[0]),
                   "one stride per workspace array");
     const int nf = (int)(sizeof(strides) / sizeof(strides[0]));
@@ -49,6 +54,11 @@ size_t carve_workspace(Work& w, int M, int N, int n, int m, float* base)
     for (int i = 0; i < nf; ++i) {
         if (base) *fields[i] = base + total;
         total += strides[i] * (size_t)M;
+    }
+    if (base) {
+        w.sbest = reinterpret_cast<int*>(ints);
+        w.siters = w.sbest + M;
+        w.sqpt = w.sbest + 2 * M;
     }
     if (base) w.mpart = (float2*)(base + total);
     total += 2 * w.sK2 * (size_t)M;  // merit partials
@@ -90,32 +100,33 @@ void record(gato_handle* h, int i, cudaStream_t st)
 }
 }  // namespace
 
-cudaError_t run_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const float* R,
-                          const float* q, const float* r, const float* A, const float* B,
-                          const float* e, const float* s0, float* dX, float* dU, float* lambda,
-                          int32_t* iters, float* merit, int32_t* best, uint32_t* status,
-                          cudaStream_t st)
+cudaError_t run_kkt_core(gato_handle* h, const gato_params* p, const float* Q_form,
+                         const float* Q_merit, const float* R, const float* q, const float* r,
+                         const float* A, const float* B, const float* e, const float* s0,
+                         const float* lambda0, float* dX, float* dU, float* lambda,
+                         int32_t* iters, float* merit, int32_t* best, uint32_t* status,
+                         cudaStream_t st, bool timed)
 {
     Work& w = h->w;
     const int ls = linsys_for(p, w.N);
     const bool direct = ls != GATO_LINSYS_PCG;
-    cudaError_t err = launch_form_matrices(h, Q, R, A, B, status, st);
+    cudaError_t err = launch_form_matrices(h, Q_form, R, A, B, status, st);
     if (err == cudaSuccess) err = launch_form_rhs(h, 0, q, r, e, s0, (size_t)w.n, st);
-    record(h, 1, st);
+    if (timed) record(h, 1, st);
     if (err == cudaSuccess) {
         if (direct) {
             err = launch_bdsv_factor(h, ls, status, st);
             if (err == cudaSuccess)
                 err = launch_bdsv_solve(h, ls, 0, lambda, dX, dU, iters, 0, status, st);
         } else {
-            err = launch_pcg_ex(h, p, 0, nullptr, lambda, dX, dU, iters, 0, status, st);
+            err = launch_pcg_ex(h, p, 0, lambda0, lambda, dX, dU, iters, 0, status, st);
         }
     }
-    record(h, 2, st);
+    if (timed) record(h, 2, st);
     gato_params pc = *p;  // PCG corrections are solved to refine_eps
     if (p->refine_eps > 0.f) pc.pcg_eps = p->refine_eps;
     for (int k = 0; k < p->refine_steps && err == cudaSuccess; ++k) {
-        err = launch_kkt_residual(h, Q, R, q, r, A, B, e, s0, dX, dU, lambda, st);
+        err = launch_kkt_residual(h, Q_form, R, q, r, A, B, e, s0, dX, dU, lambda, st);
         if (err == cudaSuccess)
             err = launch_form_rhs(h, 1, w.q2, w.r2, w.e2, w.s02, (size_t)w.n, st);
         if (err == cudaSuccess) {
@@ -127,11 +138,21 @@ cudaError_t run_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, 
         }
         if (err == cudaSuccess) err = launch_accumulate(h, lambda, dX, dU, iters, st);
     }
-    if (p->refine_steps > 0) record(h, 3, st);
+    if (timed && p->refine_steps > 0) record(h, 3, st);
     if (err == cudaSuccess)
-        err = launch_merit(h, p, Q, R, q, r, A, B, e, s0, dX, dU, merit, best, status, st);
-    record(h, 4, st);
+        err = launch_merit(h, p, Q_merit, R, q, r, A, B, e, s0, dX, dU, merit, best, status, st);
+    if (timed) record(h, 4, st);
     return err;
+}
+
+cudaError_t run_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const float* R,
+                          const float* q, const float* r, const float* A, const float* B,
+                          const float* e, const float* s0, float* dX, float* dU, float* lambda,
+                          int32_t* iters, float* merit, int32_t* best, uint32_t* status,
+                          cudaStream_t st)
+{
+    return run_kkt_core(h, p, Q, Q, R, q, r, A, B, e, s0, nullptr, dX, dU, lambda, iters, merit,
+                        best, status, st, true);
 }
 
 }  // namespace gato
@@ -171,6 +192,87 @@ int unsupported_or_fail(cudaError_t e)
     return cuda_fail(e);
 }
 
+bool sqp_params_valid(const gato_sqp_params* sp)
+{
+    if (!sp || sp->iters < 1) return false;
+    if (!(sp->rho_factor > 1.f) || !(sp->rho_min >= 0.f) || !(sp->rho_max >= sp->rho_min))
+        return false;
+    return true;
+}
+
+struct SqpArgs {
+    const float *Q, *R, *q, *r, *A, *B, *c, *xs;
+    float *X, *U, *lambda, *rho, *merit_hist;
+    int32_t* iters_hist;
+    uint32_t* status;
+};
+
+// one SQP iteration: expansion, the damped KKT solve, line search, step
+cudaError_t sqp_iteration(gato_handle* h, const gato_params* p, const gato_sqp_params* sp,
+                          const SqpArgs& a, cudaStream_t st)
+{
+    Work& w = h->w;
+    cudaError_t err = gato::launch_sqp_linearize(h, a.Q, a.R, a.q, a.r, a.A, a.B, a.c, a.xs,
+                                                 a.X, a.U, a.rho, st);
+    if (err == cudaSuccess)
+        err = gato::run_kkt_core(h, p, w.Qd, a.Q, a.R, w.qt, w.rt, a.A, a.B, w.et, w.s0t,
+                                 sp->warm_start ? a.lambda : nullptr, w.sdX, w.sdU, a.lambda,
+                                 w.siters, w.smerit, w.sbest, a.status, st, false);
+    if (err == cudaSuccess)
+        err = gato::launch_sqp_step(h, p, sp, a.X, a.U, a.rho, a.merit_hist, a.iters_hist, st);
+    return err;
+}
+
+// everything a recorded iteration depends on (parameters, pointers and the
+// handle's kernel selections), in a zero-padded byte string
+void sqp_key(unsigned char* key, const gato_handle* h, const gato_params* p,
+             const gato_sqp_params* sp, const SqpArgs& a)
+{
+    static_assert(sizeof(gato_params) + sizeof(gato_sqp_params) + sizeof(SqpArgs) +
+                          3 * sizeof(int) <= 512,
+                  "key size");
+    memset(key, 0, 512);
+    const int kinds[3] = {h->pcg_kernel, h->bdsv_kernel, h->force_smem_form};
+    gato_params pk;
+    gato_sqp_params sk;
+    memset(&pk, 0, sizeof(pk));
+    memset(&sk, 0, sizeof(sk));
+    pk = *p;
+    sk = *sp;
+    memcpy(key, &pk, sizeof(pk));
+    memcpy(key + sizeof(pk), &sk, sizeof(sk));
+    memcpy(key + sizeof(pk) + sizeof(sk), &a, sizeof(a));
+    memcpy(key + sizeof(pk) + sizeof(sk) + sizeof(a), kinds, sizeof(kinds));
+}
+
+// records one iteration on the handle's private stream (nothing runs while
+// recording) and instantiates it
+cudaError_t record_sqp_graph(gato_handle* h, const gato_params* p, const gato_sqp_params* sp,
+                             const SqpArgs& a)
+{
+    if (h->sqp_exec) {
+        cudaGraphExecDestroy(h->sqp_exec);
+        h->sqp_exec = nullptr;
+    }
+    cudaError_t err = cudaSuccess;
+    if (!h->capture_stream)
+        err = cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking);
+    if (err != cudaSuccess) return err;
+    err = cudaStreamBeginCapture(h->capture_stream, cudaStreamCaptureModeThreadLocal);
+    if (err != cudaSuccess) return err;
+    err = sqp_iteration(h, p, sp, a, h->capture_stream);
+    cudaGraph_t g = nullptr;
+    const cudaError_t end = cudaStreamEndCapture(h->capture_stream, &g);
+    if (err == cudaSuccess) err = end;
+    if (err == cudaSuccess) err = cudaGraphInstantiate(&h->sqp_exec, g, 0);
+    if (g) cudaGraphDestroy(g);
+    if (err != cudaSuccess) {
+        h->sqp_exec = nullptr;
+        cudaGetLastError();
+    }
+    return err;
+}
+
 }  // namespace
 
 extern "C" {
@@ -190,6 +292,17 @@ void gato_default_params(gato_params* p)
     p->merit_kernel = GATO_MERIT_FUSED;
     p->linsys = GATO_LINSYS_AUTO;
     p->bdsv_horizon = 256;
+}
+
+void gato_default_sqp_params(gato_sqp_params* sp)
+{
+    if (!sp) return;
+    sp->iters = 10;
+    sp->rho_factor = 10.f;
+    sp->rho_min = 1e-8f;
+    sp->rho_max = 10.f;
+    sp->warm_start = 1;
+    sp->use_graph = 1;
 }
 
 int gato_create(gato_handle** out, int M, int N, int n, int m)
@@ -232,6 +345,8 @@ int gato_create(gato_handle** out, int M, int N, int n, int m)
 void gato_destroy(gato_handle* h)
 {
     if (!h) return;
+    if (h->sqp_exec) cudaGraphExecDestroy(h->sqp_exec);
+    if (h->capture_stream) cudaStreamDestroy(h->capture_stream);
     for (int i = 0; i < 5; ++i) cudaEventDestroy(h->ev[i]);
     cudaFree(h->base);
     free(h);
@@ -400,6 +515,37 @@ int gato_apply_step(gato_handle* h, const gato_params* p, const int32_t* best, c
     if (!h || !params_valid(p) || !best || !dX || !X) return GATO_ERR_INVALID_ARG;
     if (h->w.N > 1 && (!dU || !U)) return GATO_ERR_INVALID_ARG;
     return cuda_fail(gato::launch_apply_step(h, p, best, dX, dU, X, U, (cudaStream_t)stream));
+}
+
+int gato_sqp_linear(gato_handle* h, const gato_params* p, const gato_sqp_params* sp,
+                    const float* Q, const float* R, const float* q, const float* r,
+                    const float* A, const float* B, const float* c, const float* xs, float* X,
+                    float* U, float* lambda, float* rho, float* merit_hist, int32_t* iters_hist,
+                    uint32_t* status, void* stream)
+{
+    if (!h || !params_valid(p) || !sqp_params_valid(sp) || !lq_ok(h, Q, R, q, r, A, B, c, xs) ||
+        !X || !lambda || !rho || !merit_hist || !status)
+        return GATO_ERR_INVALID_ARG;
+    if (h->w.N > 1 && !U) return GATO_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    const SqpArgs a{Q, R, q, r, A, B, c, xs, X, U, lambda, rho, merit_hist, iters_hist, status};
+    cudaError_t err = cudaMemsetAsync(h->w.sqpt, 0, sizeof(int) * h->w.M, st);
+    if (err != cudaSuccess) return GATO_ERR_CUDA;
+    if (!sp->use_graph) {
+        for (int k = 0; k < sp->iters && err == cudaSuccess; ++k)
+            err = sqp_iteration(h, p, sp, a, st);
+        return unsupported_or_fail(err);
+    }
+    unsigned char key[sizeof(h->sqp_key)];
+    sqp_key(key, h, p, sp, a);
+    if (!h->sqp_exec || memcmp(key, h->sqp_key, sizeof(key)) != 0) {
+        err = record_sqp_graph(h, p, sp, a);
+        if (err != cudaSuccess) return unsupported_or_fail(err);
+        memcpy(h->sqp_key, key, sizeof(key));
+    }
+    for (int k = 0; k < sp->iters && err == cudaSuccess; ++k)
+        err = cudaGraphLaunch(h->sqp_exec, st);
+    return unsupported_or_fail(err);
 }
 
 }  // extern "C"

@@ -73,6 +73,21 @@ struct Work {
     float* By;     // [N] n x n
     float* Bv;     // [N][n] vector scratch of the substitution when it does not
     float* Bg;     // [N][n] fit in shared memory
+    // SQP loop on the linear model: the expansion along the current
+    // trajectory (dense [M][...] like the caller's arrays), per-knot cost
+    // partials, and the iteration's step, merits and counters
+    float* Qd;     // [N][n][n] Q_k + rho I
+    float* qt;     // [N][n]    Q_k x_k + q_k
+    float* rt;     // [N-1][m]  R_k u_k + r_k
+    float* et;     // [N-1][n]  A_k x_k + B_k u_k + c_k - x_{k+1}
+    float* s0t;    // [n]       xs - x_0
+    float* Jk;     // [N]       cost of knot k at the current trajectory (stride sN)
+    float* sdX;    // [N][n]    the step
+    float* sdU;    // [N-1][m]
+    float* smerit; // [n_alpha + 1] (dense [M][n_alpha + 1])
+    int* sbest;    // [M]
+    int* siters;   // [M]
+    int* sqpt;     // [M] iterations done in the current call
     // line search partial sums
     float2* mpart; // [(A+1)][N] (cost, violation) per knot and candidate
     int* queue;    // work counters of the persistent kernels (not per solve)
@@ -94,6 +109,11 @@ struct gato_handle {
     cudaEvent_t ev[5];  // start, after form, after PCG, after refinement, after merit
     int ev_used[5];
     gato_stats last;
+    // one SQP iteration recorded as a CUDA graph, with the arguments it was
+    // recorded for (replayed while they stay the same)
+    cudaStream_t capture_stream;
+    cudaGraphExec_t sqp_exec;
+    unsigned char sqp_key[512];
 };
 
 namespace gato {
@@ -148,6 +168,23 @@ bool params_valid(const gato_params* p);
 // the linear solver a call with parameters p uses: GATO_LINSYS_PCG,
 // GATO_LINSYS_BDSV or GATO_LINSYS_BDSV_CHRONO
 int linsys_for(const gato_params* p, int N);
+// formation with Q_form, right-hand side, linear solve (from lambda0 when not
+// NULL), refinement rounds and line search with Q_merit, on stream st; the
+// handle's timing events are recorded when `timed`
+cudaError_t run_kkt_core(gato_handle* h, const gato_params* p, const float* Q_form,
+                         const float* Q_merit, const float* R, const float* q, const float* r,
+                         const float* A, const float* B, const float* e, const float* s0,
+                         const float* lambda0, float* dX, float* dU, float* lambda,
+                         int32_t* iters, float* merit, int32_t* best, uint32_t* status,
+                         cudaStream_t st, bool timed);
+// SQP loop kernels (sqp.cu)
+cudaError_t launch_sqp_linearize(gato_handle* h, const float* Q, const float* R, const float* q,
+                                 const float* r, const float* A, const float* B, const float* c,
+                                 const float* xs, const float* X, const float* U,
+                                 const float* rho, cudaStream_t st);
+cudaError_t launch_sqp_step(gato_handle* h, const gato_params* p, const gato_sqp_params* sp,
+                            float* X, float* U, float* rho, float* merit_hist,
+                            int32_t* iters_hist, cudaStream_t st);
 // the whole gato_solve_kkt sequence on stream st (events recorded when the
 // handle times)
 cudaError_t run_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const float* R,

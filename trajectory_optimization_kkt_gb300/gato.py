@@ -58,6 +58,12 @@ class GatoParams(ctypes.Structure):
                 ("bdsv_horizon", ctypes.c_int)]
 
 
+class GatoSqpParams(ctypes.Structure):
+    _fields_ = [("iters", ctypes.c_int), ("rho_factor", ctypes.c_float),
+                ("rho_min", ctypes.c_float), ("rho_max", ctypes.c_float),
+                ("warm_start", ctypes.c_int), ("use_graph", ctypes.c_int)]
+
+
 class GatoStats(ctypes.Structure):
     _fields_ = [("form_us", ctypes.c_float), ("pcg_us", ctypes.c_float),
                 ("refine_us", ctypes.c_float), ("merit_us", ctypes.c_float),
@@ -90,6 +96,10 @@ def load(path: Optional[str] = None):
     P = ctypes.POINTER(GatoParams)
     lib.gato_default_params.argtypes = [P]
     lib.gato_default_params.restype = None
+    SP = ctypes.POINTER(GatoSqpParams)
+    lib.gato_default_sqp_params.argtypes = [SP]
+    lib.gato_default_sqp_params.restype = None
+    lib.gato_sqp_linear.argtypes = [vp, P, SP] + [vp] * 8 + [vp] * 7 + [vp]
     lib.gato_create.argtypes = [ctypes.POINTER(vp), ip, ip, ip, ip]
     lib.gato_destroy.argtypes = [vp]
     lib.gato_destroy.restype = None
@@ -109,7 +119,8 @@ def load(path: Optional[str] = None):
     for fn in ("gato_create", "gato_set_timing", "gato_set_pcg_kernel", "gato_set_form_kernel",
                "gato_set_bdsv_kernel", "gato_get_stats", "gato_form_schur",
                "gato_get_schur", "gato_pcg_solve", "gato_bdsv_solve", "gato_linesearch",
-               "gato_solve_kkt", "gato_apply_step", "gato_solve_kkt_noalloc"):
+               "gato_solve_kkt", "gato_apply_step", "gato_solve_kkt_noalloc",
+               "gato_sqp_linear"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -126,6 +137,14 @@ def default_params(**overrides) -> GatoParams:
     for k, v in overrides.items():
         setattr(p, k, v)
     return p
+
+
+def default_sqp_params(**overrides) -> GatoSqpParams:
+    sp = GatoSqpParams()
+    load().gato_default_sqp_params(ctypes.byref(sp))
+    for k, v in overrides.items():
+        setattr(sp, k, v)
+    return sp
 
 
 def _ptr(t, dtype=None, what="tensor"):
@@ -151,6 +170,7 @@ def _stream(stream):
 
 
 _LQ = ("Q", "R", "q", "r", "A", "B", "e", "s0")
+_MODEL = ("Q", "R", "q", "r", "A", "B", "c", "xs")
 
 
 class Solver:
@@ -242,6 +262,18 @@ class Solver:
             self.h, ctypes.byref(params), *self._lq(prob), _ptr(dX), _ptr(dU), _ptr(lam),
             _ptr(iters, torch.int32, "iters"), _ptr(merit), _ptr(best, torch.int32, "best"),
             _ptr(status, torch.int32, "status"), _stream(stream)))
+
+    def sqp_linear(self, params, sqp_params, model, X, U, lam, rho, merit_hist, status,
+                   iters_hist=None, stream=None):
+        """gato_sqp_linear: model holds Q, R, q, r, A, B, c, xs (CUDA tensors);
+        X, U, lam and rho are updated in place."""
+        import torch
+        _check("gato_sqp_linear", self.lib.gato_sqp_linear(
+            self.h, ctypes.byref(params), ctypes.byref(sqp_params),
+            *[_ptr(model.get(k), what=k) for k in _MODEL],
+            _ptr(X), _ptr(U), _ptr(lam), _ptr(rho), _ptr(merit_hist),
+            _ptr(iters_hist, torch.int32, "iters_hist"), _ptr(status, torch.int32, "status"),
+            _stream(stream)))
 
     def apply_step(self, params, best, dX, dU, X, U, stream=None):
         import torch
