@@ -24,6 +24,8 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -269,6 +271,83 @@ def run_sweep(args, local):
                                       "status_nonzero_solves": bad}), flush=True)
 
 
+def _sqp_timing(torch, gato, model_np, M, iters, linsys, use_graph, dev, stream, flush, reps=3):
+    """Device ms per SQP iteration of a batch of M problems (after one
+    untimed call that records the graph), and the last call's outputs."""
+    N, n = model_np["Q"].shape[1:3]
+    m = model_np["B"].shape[-1]
+    from trajectory_optimization_kkt_gb300.workloads import rho_logspace
+    d = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in model_np.items()}
+    f = dict(device=dev, dtype=torch.float32)
+    p = gato.default_params(pcg_max_iters=2000, refine_steps=1, linsys=LINSYS[linsys])
+    sp = gato.default_sqp_params(iters=iters, use_graph=use_graph)
+    rho0 = torch.from_numpy(rho_logspace(M)).to(dev)
+    with gato.Solver(M, N, n, m) as s:
+        X, U = torch.zeros(M, N, n, **f), torch.zeros(M, N - 1, m, **f)
+        lam, rho = torch.zeros(M, N, n, **f), rho0.clone()
+        hist = torch.zeros(M, iters + 1, **f)
+        status = torch.zeros(M, device=dev, dtype=torch.int32)
+        times = []
+        for rep in range(reps + 1):
+            for t in (X, U, lam, status):
+                t.zero_()
+            rho.copy_(rho0)
+            flush.fill_(float(rep))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            s.sqp_linear(p, sp, d, X, U, lam, rho, hist, status, stream=stream)
+            b.record(stream)
+            b.synchronize()
+            if rep:
+                times.append(a.elapsed_time(b) / iters)
+        return statistics.median(times), hist.cpu().numpy(), status.cpu().numpy()
+
+
+def run_sqp_study(args, local):
+    """The rho-damping case study of the GATO paper (Sec. IV-C) on the linear
+    model: each batch holds one problem M times with rho log-spaced from 1e-8
+    to 10 (a single solve starts at 0.1); merit after each of 100 SQP
+    iterations from the zero trajectory, best over the batch, and the time
+    per iteration with graph replay and with kernel-by-kernel launches."""
+    import torch
+
+    from trajectory_optimization_kkt_gb300 import _build, gato
+    from trajectory_optimization_kkt_gb300.workloads import linear_models, replicate
+    torch.cuda.set_device(local)
+    _build.build()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    N, n, m, iters, problems = 64, 14, 7, 100, 8
+    models = linear_models(problems, N, n, m, seed=9000)
+    for M in (1, 4, 16, 32, 64, 128):
+        best, ms_graph = [], []
+        for j in range(problems):
+            one = {k: v[j] for k, v in models.items()}
+            ms, hist, _ = _sqp_timing(torch, gato, replicate(one, M), M, iters, "pcg", 1, dev,
+                                      stream, flush, reps=1)
+            ms_graph.append(ms)
+            best.append(hist.min(axis=0))  # best merit over the batch after each iteration
+        best = np.array(best)
+        first = replicate({k: v[0] for k, v in models.items()}, M)
+        ms_stream, _, _ = _sqp_timing(torch, gato, first, M, iters, "pcg", 0, dev, stream,
+                                      flush, reps=1)
+        ms_direct, hist_d, _ = _sqp_timing(torch, gato, first, M, iters, "bdsv", 1, dev,
+                                           stream, flush, reps=1)
+        print(json.dumps({"sqp_study": "rho_sweep", "M": M, "N": N, "n": n, "m": m,
+                          "iters": iters, "problems": problems,
+                          "best_merit_over_batch_mean": {
+                              str(t): float(best[:, t].mean()) for t in (0, 1, 2, 5, 10, 20,
+                                                                         50, 100)},
+                          "ms_per_iteration_graph": statistics.median(ms_graph),
+                          "ms_per_iteration_stream": ms_stream,
+                          "ms_per_iteration_direct_solve_graph": ms_direct,
+                          "direct_solve_best_merit_problem0": {
+                              str(t): float(hist_d.min(axis=0)[t]) for t in (0, 1, 2, 100)},
+                          "pcg_best_merit_problem0": {
+                              str(t): float(best[0, t]) for t in (0, 1, 2, 100)}}), flush=True)
+
+
 def run_gpu(args, world, rank, local):
     import torch
 
@@ -385,6 +464,20 @@ def run_gpu(args, world, rank, local):
     sha = _src_sha(os.path.join(_build.CSRC, "pcg.cu"))
     traffic = PCG_TRAFFIC["bytes_per_launch"] if PCG_TRAFFIC["pcg_sha"] == sha else None
 
+    # ---- SQP loop on the linear model (context, not the metric) ----
+    sqp = None
+    if not args.no_alternatives and rank == 0:
+        from trajectory_optimization_kkt_gb300.workloads import linear_models
+        sq_M, sq_N, sq_iters = 128, 64, 20
+        model = linear_models(sq_M, sq_N, w.n, w.m, seed=9100)
+        sqp = {"M": sq_M, "N": sq_N, "n": w.n, "m": w.m, "iters_per_call": sq_iters,
+               "rho0": "log-spaced 1e-8..10", "linsys": "pcg, one refinement round"}
+        for mode, g in (("graph", 1), ("stream", 0)):
+            ms, _, st = _sqp_timing(torch, gato, model, sq_M, sq_iters, "pcg", g, dev, stream,
+                                    flush)
+            sqp[f"ms_per_iteration_{mode}"] = ms
+        sqp["sqp_iterations_per_sec_graph"] = 1000.0 / sqp["ms_per_iteration_graph"]
+
     # ---- the same step through the direct solvers (context, not the metric) ----
     alternatives = {}
     if args.linsys == "pcg" and not args.no_alternatives and rank == 0:
@@ -432,6 +525,8 @@ def run_gpu(args, world, rank, local):
         }
         if alternatives:
             line["linsys_alternatives"] = alternatives
+        if sqp:
+            line["sqp_loop"] = sqp
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = _cpu_baseline(w)
         print(json.dumps(line), flush=True)
@@ -455,6 +550,8 @@ def main():
                     help="skip timing the same step through the direct solvers")
     ap.add_argument("--sweep", action="store_true",
                     help="horizon x batch sweep of the three linear solvers instead")
+    ap.add_argument("--sqp-study", action="store_true",
+                    help="the rho-damping SQP case study on the linear model instead")
     ap.add_argument("--batch", type=int, default=None,
                     help="solves per GPU (default: the workload's 256); for profiler "
                          "captures of a smaller case")
@@ -464,6 +561,8 @@ def main():
         run_reference(args, world, rank)
     elif args.sweep:
         run_sweep(args, local)
+    elif args.sqp_study:
+        run_sqp_study(args, local)
     else:
         run_gpu(args, world, rank, local)
 

@@ -126,9 +126,11 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_factor_rows(Work w, uint32_t* s
             const int k = r0 + half;
             const bool act = k < cnt;
             const int i = act ? 2 * k : 0;
-            float a[NP], c[NP], t[NP];
+            float a[NP], c[NP], t[NP], tl[NP];
+            // all of the round's loads first: one memory latency per round
             load_blk(a, b.nh, i - 1, act && i >= 1, n, li, false);
             load_blk(t, b.nh, i, act && i + 1 < N, n, li, false);
+            load_blk(tl, b.nh, i - 2, act && i >= 2, n, li, false);
             __syncwarp();
             publish(a, S0, li);
             publish(t, S1, li);
@@ -137,9 +139,8 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_factor_rows(Work w, uint32_t* s
             rows_mul_bt(a, S0, n, c, -1.f);
             rows_atb(S1, S1, n, li, c, -1.f);
             if (act) store_row(c, b.D(i), n, n, li);
-            load_blk(t, b.nh, i - 2, act && i >= 2, n, li, false);
             __syncwarp();
-            publish(t, S1, li);
+            publish(tl, S1, li);
             __syncwarp();
             rows_mul(a, S1, n, c, -1.f);
             if (act && i >= 2) store_row(c, b.E(i), n, n, li);
@@ -154,23 +155,21 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_factor_rows(Work w, uint32_t* s
             const int k = r0 + half;
             const bool act = k < cnt;
             const int j = act ? (2 * k + 1) * s : 0;
-            float d[NP], x[NP], e[NP], c[NP];
+            const bool right = act && j + s < N;
+            float d[NP], x[NP], e[NP], er[NP], c[NP];
             load_blk(d, b.bd, j, act, n, li, true);
+            load_blk(e, b.be, j, act, n, li, false);
+            load_blk(er, b.be, j + s, right, n, li, false);
             __syncwarp();
+            publish(e, S1, li);
             const bool okj = rows_cholesky(d, li, n);
             ok = ok && (okj || !act);
-            rows_lower_inverse(d, x, li, n, S0);  // x: row li of F
+            rows_lower_inverse(d, x, li, n, S0);  // x: row li of F (ends with __syncwarp)
             if (act) store_row(x, b.D(j), n, n, li);
-            load_blk(e, b.be, j, act, n, li, false);
-            __syncwarp();
-            publish(e, S1, li);
-            __syncwarp();
             rows_mul(x, S1, n, c, 1.f);  // X = F E_j
             if (act) store_row(c, b.E(j), n, n, li);
-            const bool right = act && j + s < N;
-            load_blk(e, b.be, j + s, right, n, li, false);
             __syncwarp();
-            publish(e, S1, li);
+            publish(er, S1, li);
             __syncwarp();
             set_row(c, li, 0.f);
             rows_mul_bt(x, S1, n, c, 1.f);  // Y = F E_{j+s}^T
@@ -183,10 +182,12 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_factor_rows(Work w, uint32_t* s
             const int k = r0 + half;
             const bool act = k < cnt2;
             const int i = act ? 2 * k * s : 0;
-            float c[NP], y[NP], t[NP];
+            const bool far = act && i >= 2 * s;
+            float c[NP], y[NP], t[NP], tl[NP];
             load_blk(c, b.bd, i, act, n, li, false);
             load_blk(y, b.by, i - s, act && i >= s, n, li, false);
             load_blk(t, b.be, i + s, act && i + s < N, n, li, false);
+            load_blk(tl, b.be, i - s, far, n, li, false);
             __syncwarp();
             publish(y, S0, li);
             publish(t, S1, li);
@@ -194,10 +195,8 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_factor_rows(Work w, uint32_t* s
             rows_atb(S0, S0, n, li, c, -1.f);  // - Y_{i-s}^T Y_{i-s}
             rows_atb(S1, S1, n, li, c, -1.f);  // - X_{i+s}^T X_{i+s}
             if (act) store_row(c, b.D(i), n, n, li);
-            const bool far = act && i >= 2 * s;
-            load_blk(t, b.be, i - s, far, n, li, false);
             __syncwarp();
-            publish(t, S1, li);
+            publish(tl, S1, li);
             __syncwarp();
             set_row(c, li, 0.f);
             rows_atb(S0, S1, n, li, c, -1.f);  // E' = -Y_{i-s}^T X_{i-s}
@@ -357,16 +356,32 @@ __global__ void __launch_bounds__(128) k_bdsv_chrono_factor(Work w, uint32_t* st
 // substitution and recovery (one block per solve)
 // ===========================================================================
 
-// sum_b M[a][b] x[b] (T = false) or sum_b M[b][a] x[b] (T = true); lower
-// (T = false: b <= a; T = true: b >= a) for triangular M
-template <bool T, bool Lower>
+// sum_b M[a][b] x[b] (T = false) or sum_b M[b][a] x[b] (T = true); Lower
+// skips the zero half of a lower-triangular M (T = false: b <= a; T = true:
+// b >= a).  With NPX > 0 (n <= NPX) the loop is unrolled and predicated, so
+// that all of a row's loads are in flight at once.
+template <bool T, bool Lower, int NPX>
 __device__ __forceinline__ float rowdot(const float* M, const float* x, int a, int n)
 {
-    float s = 0.f;
-    const int lo = (Lower && T) ? a : 0;
-    const int hi = (Lower && !T) ? a + 1 : n;
-    for (int c = lo; c < hi; ++c) s += (T ? M[c * n + a] : M[a * n + c]) * x[c];
-    return s;
+    if constexpr (NPX > 0) {
+        float mv[NPX], xv[NPX];
+#pragma unroll
+        for (int c = 0; c < NPX; ++c) {
+            const bool in = c < n && (!Lower || (T ? c >= a : c <= a));
+            mv[c] = in ? (T ? M[c * n + a] : M[a * n + c]) : 0.f;
+            xv[c] = in ? x[c] : 0.f;
+        }
+        float s = 0.f;
+#pragma unroll
+        for (int c = 0; c < NPX; ++c) s = fmaf(mv[c], xv[c], s);
+        return s;
+    } else {
+        float s = 0.f;
+        const int lo = (Lower && T) ? a : 0;
+        const int hi = (Lower && !T) ? a + 1 : n;
+        for (int c = lo; c < hi; ++c) s += (T ? M[c * n + a] : M[a * n + c]) * x[c];
+        return s;
+    }
 }
 
 __device__ __forceinline__ void finish_solve(const BdsvArgs& g, int sol, const float* v)
@@ -383,6 +398,7 @@ __device__ __forceinline__ void finish_solve(const BdsvArgs& g, int sol, const f
 
 // The vectors: v holds ghat, then the reduced right-hand sides, then
 // lambda_hat; G holds g = F gamma of the eliminated knots.
+template <int NPX>
 __global__ void __launch_bounds__(256) k_bdsv_cr_solve(BdsvArgs g)
 {
     extern __shared__ __align__(16) float sm[];
@@ -401,8 +417,8 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_solve(BdsvArgs g)
     for (int t = tid; t < even_multiples(N, 1) * n; t += T) {
         const int i = 2 * (t / n), a = t % n;
         float x = v[i * n + a];
-        if (i >= 1) x -= rowdot<false, false>(b.Nhat(i), v + (i - 1) * n, a, n);
-        if (i + 1 < N) x -= rowdot<true, false>(b.Nhat(i + 1), v + (i + 1) * n, a, n);
+        if (i >= 1) x -= rowdot<false, false, NPX>(b.Nhat(i), v + (i - 1) * n, a, n);
+        if (i + 1 < N) x -= rowdot<true, false, NPX>(b.Nhat(i + 1), v + (i + 1) * n, a, n);
         v[i * n + a] = x;
     }
     __syncthreads();
@@ -411,36 +427,36 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_solve(BdsvArgs g)
         smax = s;
         for (int t = tid; t < odd_multiples(N, s) * n; t += T) {
             const int j = (2 * (t / n) + 1) * s, a = t % n;
-            G[j * n + a] = rowdot<false, true>(b.D(j), v + j * n, a, n);  // F_j v_j
+            G[j * n + a] = rowdot<false, true, NPX>(b.D(j), v + j * n, a, n);  // F_j v_j
         }
         __syncthreads();
         for (int t = tid; t < even_multiples(N, s) * n; t += T) {
             const int i = 2 * (t / n) * s, a = t % n;
             float x = v[i * n + a];
-            if (i >= s) x -= rowdot<true, false>(b.Y(i - s), G + (i - s) * n, a, n);
-            if (i + s < N) x -= rowdot<true, false>(b.E(i + s), G + (i + s) * n, a, n);
+            if (i >= s) x -= rowdot<true, false, NPX>(b.Y(i - s), G + (i - s) * n, a, n);
+            if (i + s < N) x -= rowdot<true, false, NPX>(b.E(i + s), G + (i + s) * n, a, n);
             v[i * n + a] = x;
         }
         __syncthreads();
     }
     // knot 0: v_0 = F_0^T F_0 v_0
-    for (int a = tid; a < n; a += T) G[a] = rowdot<false, true>(b.D(0), v, a, n);
+    for (int a = tid; a < n; a += T) G[a] = rowdot<false, true, NPX>(b.D(0), v, a, n);
     __syncthreads();
-    for (int a = tid; a < n; a += T) v[a] = rowdot<true, true>(b.D(0), G, a, n);
+    for (int a = tid; a < n; a += T) v[a] = rowdot<true, true, NPX>(b.D(0), G, a, n);
     __syncthreads();
     // backward: x_j = F_j^T (g_j - X_j x_{j-s} - Y_j x_{j+s}) for the odd
     // multiples j of s, from the last level down
     for (int s = smax; s >= 2; s >>= 1) {
         for (int t = tid; t < odd_multiples(N, s) * n; t += T) {
             const int j = (2 * (t / n) + 1) * s, a = t % n;
-            float x = G[j * n + a] - rowdot<false, false>(b.E(j), v + (j - s) * n, a, n);
-            if (j + s < N) x -= rowdot<false, false>(b.Y(j), v + (j + s) * n, a, n);
+            float x = G[j * n + a] - rowdot<false, false, NPX>(b.E(j), v + (j - s) * n, a, n);
+            if (j + s < N) x -= rowdot<false, false, NPX>(b.Y(j), v + (j + s) * n, a, n);
             G[j * n + a] = x;
         }
         __syncthreads();
         for (int t = tid; t < odd_multiples(N, s) * n; t += T) {
             const int j = (2 * (t / n) + 1) * s, a = t % n;
-            v[j * n + a] = rowdot<true, true>(b.D(j), G + j * n, a, n);
+            v[j * n + a] = rowdot<true, true, NPX>(b.D(j), G + j * n, a, n);
         }
         __syncthreads();
     }
@@ -448,19 +464,20 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_solve(BdsvArgs g)
     // v_j still holds ghat_j)
     for (int t = tid; t < odd_multiples(N, 1) * n; t += T) {
         const int j = 2 * (t / n) + 1, a = t % n;
-        float x = v[j * n + a] - rowdot<false, false>(b.Nhat(j), v + (j - 1) * n, a, n);
-        if (j + 1 < N) x -= rowdot<true, false>(b.Nhat(j + 1), v + (j + 1) * n, a, n);
+        float x = v[j * n + a] - rowdot<false, false, NPX>(b.Nhat(j), v + (j - 1) * n, a, n);
+        if (j + 1 < N) x -= rowdot<true, false, NPX>(b.Nhat(j + 1), v + (j + 1) * n, a, n);
         v[j * n + a] = x;
     }
     __syncthreads();
     finish_solve(g, sol, v);
-    recover_dz(w, g.rhs, g.lambda, g.dX, g.dU, sol, [&](int j, int c) { return v[j * n + c]; },
-               G);
+    recover_dz<NPX>(w, g.rhs, g.lambda, g.dX, g.dU, sol,
+                    [&](int j, int c) { return v[j * n + c]; }, G);
 }
 
 // Chronological substitution: y_j = F_j (ghat_j - W_j y_{j-1}), then
 // x_j = F_j^T (y_j - W_{j+1}^T x_{j+1}); warp 0 walks the chain, the whole
 // block recovers dz.
+template <int NPX>
 __global__ void __launch_bounds__(128) k_bdsv_chrono_solve(BdsvArgs g)
 {
     extern __shared__ __align__(16) float sm[];
@@ -476,30 +493,30 @@ __global__ void __launch_bounds__(128) k_bdsv_chrono_solve(BdsvArgs g)
         for (int j = 0; j < N; ++j) {
             for (int a = lane; a < n; a += 32) {
                 float x = gh[j * n + a];
-                if (j > 0) x -= rowdot<false, false>(b.E(j), v + (j - 1) * n, a, n);
+                if (j > 0) x -= rowdot<false, false, NPX>(b.E(j), v + (j - 1) * n, a, n);
                 G[j * n + a] = x;
             }
             __syncwarp();
             for (int a = lane; a < n; a += 32)
-                v[j * n + a] = rowdot<false, true>(b.D(j), G + j * n, a, n);
+                v[j * n + a] = rowdot<false, true, NPX>(b.D(j), G + j * n, a, n);
             __syncwarp();
         }
         for (int j = N - 1; j >= 0; --j) {
             for (int a = lane; a < n; a += 32) {
                 float x = v[j * n + a];
-                if (j + 1 < N) x -= rowdot<true, false>(b.E(j + 1), v + (j + 1) * n, a, n);
+                if (j + 1 < N) x -= rowdot<true, false, NPX>(b.E(j + 1), v + (j + 1) * n, a, n);
                 G[j * n + a] = x;
             }
             __syncwarp();
             for (int a = lane; a < n; a += 32)
-                v[j * n + a] = rowdot<true, true>(b.D(j), G + j * n, a, n);
+                v[j * n + a] = rowdot<true, true, NPX>(b.D(j), G + j * n, a, n);
             __syncwarp();
         }
     }
     __syncthreads();
     finish_solve(g, sol, v);
-    recover_dz(w, g.rhs, g.lambda, g.dX, g.dU, sol, [&](int j, int c) { return v[j * n + c]; },
-               G);
+    recover_dz<NPX>(w, g.rhs, g.lambda, g.dX, g.dU, sol,
+                    [&](int j, int c) { return v[j * n + c]; }, G);
 }
 
 // ---------------------------------------------------------------------------
@@ -566,9 +583,14 @@ cudaError_t launch_bdsv_solve(gato_handle* h, int order, int set, float* lambda,
     // recovery needs its N n scratch in shared memory only when the vectors
     // are there too; otherwise it uses Bg in global memory
     const size_t smem = a.vec_smem ? vec : 0;
+    const bool small = w.n <= NP;
     if (order == GATO_LINSYS_BDSV_CHRONO)
-        return launch(k_bdsv_chrono_solve, (unsigned)w.M, kChronoSolveThreads, smem, st, a);
-    return launch(k_bdsv_cr_solve, (unsigned)w.M, kSolveThreads, smem, st, a);
+        return small ? launch(k_bdsv_chrono_solve<NP>, (unsigned)w.M, kChronoSolveThreads, smem,
+                              st, a)
+                     : launch(k_bdsv_chrono_solve<0>, (unsigned)w.M, kChronoSolveThreads, smem,
+                              st, a);
+    return small ? launch(k_bdsv_cr_solve<NP>, (unsigned)w.M, kSolveThreads, smem, st, a)
+                 : launch(k_bdsv_cr_solve<0>, (unsigned)w.M, kSolveThreads, smem, st, a);
 }
 
 }  // namespace gato

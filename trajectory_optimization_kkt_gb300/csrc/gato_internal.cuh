@@ -306,13 +306,36 @@ __device__ inline void warp_gemv(int rows, int cols, const float* M, const float
     __syncwarp();
 }
 
+// sum_{c in [lo, hi)} M[c * stride] x(c): with NPX > 0 (hi <= NPX) unrolled
+// and predicated so that all loads are in flight at once
+template <int NPX, typename XFn>
+__device__ __forceinline__ float strided_dot(const float* M, int stride, XFn x, int lo, int hi)
+{
+    float s = 0.f;
+    if constexpr (NPX > 0) {
+        float mv[NPX], xv[NPX];
+#pragma unroll
+        for (int c = 0; c < NPX; ++c) {
+            const bool in = c >= lo && c < hi;
+            mv[c] = in ? M[c * stride] : 0.f;
+            xv[c] = in ? x(c) : 0.f;
+        }
+#pragma unroll
+        for (int c = 0; c < NPX; ++c) s = fmaf(mv[c], xv[c], s);
+    } else {
+        for (int c = lo; c < hi; ++c) s += M[c * stride] * x(c);
+    }
+    return s;
+}
+
 // Recovery after a solve of S_hat lambda_hat = ghat (GATO paper, eq. (4)):
 // lambda = L^-T lambda_hat, then dx_k = -Q_k^-1 q_k + Q_k^-1 lambda_k
 // + S_{k+1,k}^T lambda_{k+1} and du_k = -R_k^-1 r_k - (B_k R_k^-1)^T
 // lambda_{k+1}, with the -Q^-1 q and -R^-1 r parts taken from the rhs set.
 // Block-wide (all threads of the block, one solve); lhat(j, a) reads
-// lambda_hat; lsm is an N n scratch in shared memory.
-template <typename LhatFn>
+// lambda_hat; lsm is an N n scratch in shared memory.  NPX > 0 (n <= NPX)
+// unrolls the dot products.
+template <int NPX = 0, typename LhatFn>
 __device__ inline void recover_dz(const Work& w, const Rhs& rhs, float* lambda, float* dX,
                                   float* dU, int sol, LhatFn lhat, float* lsm)
 {
@@ -321,8 +344,7 @@ __device__ inline void recover_dz(const Work& w, const Rhs& rhs, float* lambda, 
     for (int i = tid; i < Nn; i += T) {
         const int j = i / n, a = i - j * n;
         const float* Li = gLi + (size_t)j * n * n;
-        float x = 0.f;
-        for (int b = a; b < n; ++b) x += Li[b * n + a] * lhat(j, b);
+        const float x = strided_dot<NPX>(Li + a, n, [&](int b) { return lhat(j, b); }, a, n);
         lambda[(size_t)sol * Nn + i] = x;
         lsm[i] = x;
     }
@@ -332,16 +354,15 @@ __device__ inline void recover_dz(const Work& w, const Rhs& rhs, float* lambda, 
     const float* av = rhs.avec + sol * w.sNn;
     for (int i = tid; i < Nn; i += T) {
         const int k = i / n, a = i - k * n;
+        const float* lk = lsm + k * n;
         float x = av[i];
-        const float* Qrow = Qi + (size_t)k * n * n + a * n;
-        float t = 0.f;
-        for (int b = 0; b < n; ++b) t += Qrow[b] * lsm[k * n + b];
-        x += t;
+        x += strided_dot<NPX>(Qi + (size_t)k * n * n + a * n, 1, [&](int b) { return lk[b]; },
+                              0, n);
         if (k < N - 1) {
-            const float* Oc = Ob + (size_t)k * n * n + a;  // S_{k+1,k}, column a
-            float u = 0.f;
-            for (int b = 0; b < n; ++b) u += Oc[b * n] * lsm[(k + 1) * n + b];
-            x += u;
+            const float* lk1 = lsm + (k + 1) * n;
+            // S_{k+1,k}, column a
+            x += strided_dot<NPX>(Ob + (size_t)k * n * n + a, n, [&](int b) { return lk1[b]; },
+                                  0, n);
         }
         dX[(size_t)sol * Nn + i] = x;
     }
@@ -350,9 +371,10 @@ __device__ inline void recover_dz(const Work& w, const Rhs& rhs, float* lambda, 
     const float* bv = rhs.bvec + sol * w.sKm;
     for (int t = tid; t < Km; t += T) {
         const int k = t / m, c = t - k * m;
-        const float* Vc = Vb + (size_t)k * n * m + c;  // column c of B_k R_k^-1
-        float u = 0.f;
-        for (int b = 0; b < n; ++b) u += Vc[b * m] * lsm[(k + 1) * n + b];
+        const float* lk1 = lsm + (k + 1) * n;
+        // column c of B_k R_k^-1
+        const float u = strided_dot<NPX>(Vb + (size_t)k * n * m + c, m,
+                                         [&](int b) { return lk1[b]; }, 0, n);
         dU[(size_t)sol * Km + t] = bv[t] - u;
     }
 }

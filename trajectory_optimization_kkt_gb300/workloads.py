@@ -189,8 +189,7 @@ def linear_models(M: int, N: int, n: int, m: int, seed: int, **kw) -> Dict[str, 
 def replicate(problem: Dict[str, np.ndarray], M: int) -> Dict[str, np.ndarray]:
     """One problem (arrays without the batch axis) repeated ``M`` times: the
     batch of a sweep over a solver parameter such as the damping rho."""
-    return {k: np.ascontiguousarray(np.broadcast_to(v, (M,) + v.shape)) for k, v in
-            problem.items()}
+    return {k: np.repeat(np.asarray(v)[None], M, axis=0) for k, v in problem.items()}
 
 
 def rho_logspace(M: int, lo: float = 1e-8, hi: float = 10.0) -> np.ndarray:
