@@ -122,10 +122,9 @@ class ClockSampler:
 
 
 def _dist_env():
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return world, rank, local
+    from trajectory_optimization_kkt_gb300.replicas import from_env
+    r = from_env()
+    return r.world, r.rank, r.local
 
 
 def run_reference(args, world, rank):
@@ -364,7 +363,9 @@ def run_gpu(args, world, rank, local):
     if args.batch:
         w = w.with_batch(args.batch)
     M = w.M
-    prob = make_batch(w, M=M, first_solve=rank * M) if rank else make_batch(w, M=M)
+    from trajectory_optimization_kkt_gb300.replicas import Replica, job_throughput, max_over_ranks
+    replica = Replica(world, rank, local)
+    prob = make_batch(w, M=M, first_solve=replica.first_solve(M))
     dev = torch.device("cuda", local)
     d = {k: torch.from_numpy(v).to(dev) for k, v in prob.items()}
     s = gato.Solver(M, w.N, w.n, w.m)
@@ -435,12 +436,9 @@ def run_gpu(args, world, rank, local):
         e2e_ms += e_start.elapsed_time(e_end)
 
     # ---- max over ranks ----
-    t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = float(t[0]), float(t[1])
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dist, dev)
     solves = M * world * args.steps
-    value = solves / (total_ms / 1000.0)
+    value = job_throughput(M * args.steps, world, total_ms)
 
     # ---- roofline of the dominant kernel (PCG) ----
     # The PCG kernel keeps the operator on chip (registers and shared memory),
