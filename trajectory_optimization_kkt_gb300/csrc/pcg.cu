@@ -301,7 +301,12 @@ __global__ void __launch_bounds__(512) k_pcg_generic(PcgArgs g)
 //                           banks)
 //   red [5][32] float2      warp partial sums (four in use)
 //   DL [N]                  1 / ||L_j^-1||_F^2 (eigenvalue lower bounds)
-//   LP [N][n(n+1)/2]        packed Cholesky factors (stopping rule 0)
+//   LP [N][KS]              Cholesky factors for stopping rule 0: row a of
+//                           L_j at j*KS + a*LS, its entries in the padded
+//                           column layout of the vectors (so that a row
+//                           times r_hat_j is four float4 products); LS = 20
+//                           and KS = n*LS (+8 when that is a multiple of 32)
+//                           keep the owners' row loads free of bank conflicts
 // Thread t owns the four padded elements 4t .. 4t+3 (one knot half, one
 // float4) and keeps them in registers; the launch uses T >= 4 N threads.
 
@@ -373,17 +378,58 @@ __device__ __forceinline__ void store4(float* X, int e0, const float (&v)[4])
     *reinterpret_cast<float4*>(X + e0) = make_float4(v[0], v[1], v[2], v[3]);
 }
 
-// ||L_j r_hat_j||^2 contribution of row a of knot j
-template <int H>
-__device__ __forceinline__ float lrow_tile(const float* LP, const float* gL, bool lpacked,
-                                          const float* XR, int j, int a, int n, int tri)
+constexpr int kLS = 20;  // floats per padded row of L in shared memory
+
+__host__ __device__ __forceinline__ int l_knot_stride(int n)
 {
-    const float* row = lpacked ? LP + (size_t)j * tri + a * (a + 1) / 2
-                               : gL + (size_t)j * n * n + a * n;
-    const float* xv = XR + j * 16;
-    float t = 0.f;
-    for (int b = 0; b <= a; ++b) t += row[b] * xv[(b / H) * 8 + b % H];
-    return t * t;
+    return (n * kLS) % 32 == 0 ? n * kLS + 8 : n * kLS;
+}
+
+__device__ __forceinline__ float dot4(const float4 a, const float4 b, float s)
+{
+    s = fmaf(a.x, b.x, s);
+    s = fmaf(a.y, b.y, s);
+    s = fmaf(a.z, b.z, s);
+    return fmaf(a.w, b.w, s);
+}
+
+// sum over the owned valid rows a = ao + u of (L_j r_hat_j)_a^2: from the
+// padded rows in shared memory (four float4 loads per row, the second-half
+// chunks only for rows that reach them), or row by row from global memory
+template <int H>
+__device__ __forceinline__ float lnorm_owned(const float* LP, int KS, const float* gL, bool lsm,
+                                             const float* XR, int j, int ao, int n,
+                                             const bool (&valid)[4])
+{
+    float s = 0.f;
+    if (lsm) {
+        const float4* xv = reinterpret_cast<const float4*>(XR + j * 16);
+        const float4 x0 = xv[0], x1 = xv[1], x2 = xv[2], x3 = xv[3];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (!valid[u]) continue;
+            const float4* row = reinterpret_cast<const float4*>(LP + j * KS + (ao + u) * kLS);
+            float t = dot4(row[0], x0, 0.f);
+            t = dot4(row[1], x1, t);
+            if (ao + u >= H) {  // rows of the first half end before column H
+                t = dot4(row[2], x2, t);
+                t = dot4(row[3], x3, t);
+            }
+            s = fmaf(t, t, s);
+        }
+    } else {
+        const float* xv = XR + j * 16;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (!valid[u]) continue;
+            const int a = ao + u;
+            const float* row = gL + (size_t)j * n * n + a * n;
+            float t = 0.f;
+            for (int b = 0; b <= a; ++b) t += row[b] * xv[(b / H) * 8 + b % H];
+            s = fmaf(t, t, s);
+        }
+    }
+    return s;
 }
 
 template <int H>
@@ -393,9 +439,9 @@ __device__ __forceinline__ void pcg_tile_solve(const PcgArgs& g, int sol)
     const Work& w = g.w;
     const int N = w.N, n = w.n, T = blockDim.x, tid = threadIdx.x;
     const int E = N * 16;  // padded elements
-    const int tri = n * (n + 1) / 2;
     const bool rule0 = g.rule == GATO_STOP_RESIDUAL;
-    const bool lpacked = rule0 && g.l_smem;
+    const bool lsm = rule0 && g.l_smem;
+    const int KS = l_knot_stride(n);
 
     float* XP = sm;
     float* XR = XP + E;
@@ -416,12 +462,13 @@ __device__ __forceinline__ void pcg_tile_solve(const PcgArgs& g, int sol)
     for (int i = tid; i < zero_count; i += T) sm[i] = 0.f;
     for (int j = tid; j < N; j += T) DL[j] = w.dlow[sol * w.sN + j];
     const float* gL = w.L + sol * w.sNnn;
-    if (lpacked) {
-        for (int t = tid; t < N * n; t += T) {
-            const int j = t / n, a = t - j * n;
-            const float* src = gL + (size_t)j * n * n + a * n;
-            float* dst = LP + (size_t)j * tri + a * (a + 1) / 2;
-            for (int b = 0; b <= a; ++b) dst[b] = src[b];
+    if (lsm) {
+        // row a of L_j in the padded column layout, zeros above the diagonal
+        for (int t = tid; t < N * n * 16; t += T) {
+            const int c = t & 15, ja = t >> 4, j = ja / n, a = ja - j * n;
+            const int b = c < 8 ? c : H + (c - 8);
+            const bool in = (c < 8 ? c < H : c - 8 < n - H) && b <= a;
+            LP[j * KS + a * kLS + c] = in ? gL[(size_t)j * n * n + a * n + b] : 0.f;
         }
     }
 
@@ -492,11 +539,7 @@ __device__ __forceinline__ void pcg_tile_solve(const PcgArgs& g, int sol)
     __syncthreads();
     float q = has_tile ? tile_matvec<H>(tile, jb, rt, ct, XR, yr_base, yc_base) : 0.f;
     float lsq = 0.f;
-    if (rule0) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (valid[u]) lsq += lrow_tile<H>(LP, gL, lpacked, XR, jo, ao + u, n, tri);
-    }
+    if (rule0) lsq = lnorm_owned<H>(LP, KS, gL, lsm, XR, jo, ao, n, valid);
     post2(q, lsq, redC);
     __syncthreads();
     float2 sB = collect2(redB), sC = collect2(redC);
@@ -559,11 +602,7 @@ __device__ __forceinline__ void pcg_tile_solve(const PcgArgs& g, int sol)
         for (int u = 0; u < 4; ++u) rr += r[u] * r[u];
         float lsq = 0.f;
         const bool exact = exact_next;
-        if (exact) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (valid[u]) lsq += lrow_tile<H>(LP, gL, lpacked, XR, jo, ao + u, n, tri);
-        }
+        if (exact) lsq = lnorm_owned<H>(LP, KS, gL, lsm, XR, jo, ao, n, valid);
         post2(q, rr, redB);
         post2(dl * rr, lsq, redC);
         __syncthreads();
@@ -575,10 +614,7 @@ __device__ __forceinline__ void pcg_tile_solve(const PcgArgs& g, int sol)
         bool have_exact = exact;
         if (rule0 && !exact && sC.x * 0.999f <= thr) {
             // the bound no longer rules convergence out: evaluate ||L r_hat||
-            lsq = 0.f;
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (valid[u]) lsq += lrow_tile<H>(LP, gL, lpacked, XR, jo, ao + u, n, tri);
+            lsq = lnorm_owned<H>(LP, KS, gL, lsm, XR, jo, ao, n, valid);
             float lv[1] = {lsq};
             block_sum<1>(lv, reinterpret_cast<float4*>(redD));
             lsq_all = lv[0];
@@ -648,7 +684,7 @@ size_t tile_smem_bytes(const Work& w, int l_smem)
     size_t f = 6 * 16 * N + 12;  // XP, XR, YR0/1, YC0/1
     f += 5 * 32 * 2;        // five float2[32] reduction buffers
     f += round4(N);         // DL
-    if (l_smem) f += N * (n * (n + 1) / 2);
+    if (l_smem) f += N * (size_t)l_knot_stride((int)n);
     return f * sizeof(float);
 }
 
