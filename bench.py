@@ -506,7 +506,7 @@ def run_gpu(args, world, rank, local):
             "roofline": None if args.linsys != "pcg" else {
                          "bound": "alu", "achieved": achieved_tf, "peak": alu_peak_tf,
                          "unit": "TFLOP/s", "frac": achieved_tf / alu_peak_tf,
-                         "traffic": traffic, "kernel": "k_pcg_tile (solve + refinement launches)",
+                         "traffic": traffic, "kernel": "k_pcg_wide (solve + refinement launches)",
                          "peak_basis": f"{n_sm} SMs x {FP32_LANES_PER_SM} FFMA lanes x 2 flop x "
                                        f"{sm_mhz:.0f} MHz (max SM clock, {peak_kind})",
                          "flops_per_solve_iteration": flops_it,

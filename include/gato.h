@@ -73,9 +73,14 @@ extern "C" {
                                       block diagonal of S                         */
 
 /* PCG kernel selection (gato_set_pcg_kernel) */
-#define GATO_PCG_AUTO 0            /* register-tiled kernel when 7 <= n <= 16 and
+#define GATO_PCG_AUTO 0            /* the wide-tile kernel when 7 <= n <= 16 and
                                       N <= 128, else the generic kernel            */
 #define GATO_PCG_GENERIC 1         /* always the generic kernel                   */
+#define GATO_PCG_WIDE 2            /* the wide-tile kernel (two threads per
+                                      coupling block, rows over all 2H columns)
+                                      where it applies, else as GATO_PCG_AUTO     */
+#define GATO_PCG_TILE 3            /* the four-thread tile kernel (H x H tiles)
+                                      where it applies, else as GATO_PCG_AUTO     */
 
 /* Linear solver of S lambda = gamma (gato_params.linsys).  The direct solver
  * (bdsv) factors the block-tridiagonal S exactly instead of iterating; the
@@ -180,7 +185,8 @@ int gato_set_timing(gato_handle* h, int on);
 /* Stage times of the last call (see gato_stats). */
 int gato_get_stats(gato_handle* h, gato_stats* out);
 
-/* Chooses the PCG kernel (GATO_PCG_AUTO or GATO_PCG_GENERIC) for later calls.
+/* Chooses the PCG kernel (GATO_PCG_AUTO, GATO_PCG_GENERIC, GATO_PCG_WIDE or
+ * GATO_PCG_TILE) for later calls.
  * Both give the same PCG iterates up to rounding; the generic kernel covers
  * every supported size.  Errors: INVALID_ARG. */
 int gato_set_pcg_kernel(gato_handle* h, int kind);

@@ -169,6 +169,18 @@ CUSTOM = [
     ("N130_n14_m7_generic", 1, 130, 14, 7, 1),
     ("N128_n12_m6_tile", 2, 128, 12, 6, 1),
 ]
+WIDE = [c for c in CUSTOM if 7 <= c[3] <= 16 and c[2] <= 128] + [
+    ("N33_n15_m4", 2, 33, 15, 4, 1), ("N5_n8_m3", 3, 5, 8, 3, 0)]
+
+
+@pytest.mark.parametrize("kind", [gato.GATO_PCG_WIDE, gato.GATO_PCG_TILE], ids=["wide", "tile"])
+@pytest.mark.parametrize("name,M,N,n,m,refine", WIDE, ids=[c[0] for c in WIDE])
+def test_tiled_kernels_custom_sizes(name, M, N, n, m, refine, kind):
+    prob = random_lq(M, N, n, m, seed=600 + N + n)
+    p = gato.default_params(pcg_max_iters=3000, refine_steps=refine)
+    out = solve(prob, p, kind)
+    assert not out["status"].any(), out["status"]
+    check_solution(prob, out, range(M))
 
 
 @pytest.mark.parametrize("name,M,N,n,m,refine", CUSTOM, ids=[c[0] for c in CUSTOM])
@@ -180,10 +192,11 @@ def test_solve_kkt_custom_sizes(name, M, N, n, m, refine):
     check_solution(prob, out, range(M))
 
 
+@pytest.mark.parametrize("kind", [gato.GATO_PCG_WIDE, gato.GATO_PCG_TILE], ids=["wide", "tile"])
 @pytest.mark.parametrize("w", [WORKLOADS[1], WORKLOADS[4]], ids=lambda w: w.name)
-def test_tile_and_generic_kernels_agree(w):
+def test_tiled_and_generic_kernels_agree(w, kind):
     prob = make_batch(w, M=4)
-    a = solve(prob, params_for(w), gato.GATO_PCG_AUTO)
+    a = solve(prob, params_for(w), kind)
     b = solve(prob, params_for(w), gato.GATO_PCG_GENERIC)
     assert np.abs(a["iters"] - b["iters"]).max() <= 0.05 * b["iters"].max() + 2
     for j in range(4):

@@ -14,6 +14,8 @@
 // is r = L r_hat.  Both operator applications per iteration are products with
 // the one matrix Nhat.
 //
+// k_pcg_wide<H>  (7 <= n <= 16, N <= 128; the default there): two threads
+//     per coupling block with ownership aligned to the tiles, see below.
 // k_pcg_tile<H>  (7 <= n <= 16, N <= 128): every coupling block Nhat_j is
 //     split into 2 x 2 tiles of H x H (H = ceil(n/2)); four threads hold one
 //     block's tiles in registers for the whole solve, so a product with Nhat
@@ -249,7 +251,7 @@ __global__ void __launch_bounds__(512) k_pcg_generic(PcgArgs g)
             pv[0] += p[i] * x;
         }
         block_sum<1>(pv, redA);
-        const float alpha = eta / pv[0];
+        const float alpha = __fdividef(eta, pv[0]);
         for (int i = tid; i < Nn; i += T) {
             lam[i] += alpha * p[i];
             r[i] -= alpha * v[i];
@@ -275,7 +277,7 @@ __global__ void __launch_bounds__(512) k_pcg_generic(PcgArgs g)
         }
         done = (g.rule == GATO_STOP_PRECOND ? eta_new : red2[1]) <= thr;
         if (done) break;
-        const float beta = eta_new / eta;
+        const float beta = __fdividef(eta_new, eta);
         for (int i = tid; i < Nn; i += T) p[i] = v[i] + beta * p[i];
         eta = eta_new;
         __syncthreads();
@@ -583,7 +585,7 @@ __device__ __forceinline__ void pcg_tile_solve(const PcgArgs& g, int sol)
         // B: alpha = eta / p^T S_hat p; lambda and r updates (owners)
         const float2 sA = collect2(redA);  // (sum_j p_j^T Nhat_j p_{j-1}, p^T p)
         const float pv = sA.y + 2.f * sA.x;
-        const float alpha = eta / pv;
+        const float alpha = __fdividef(eta, pv);
         if (owner) ysum4(Y, e0, y);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -629,7 +631,7 @@ __device__ __forceinline__ void pcg_tile_solve(const PcgArgs& g, int sol)
         done = (!rule0 || have_exact) && stopq <= thr;
         if (done) break;
         exact_next = rule0 && sC.x <= 1.25f * thr;
-        const float beta = eta_new / eta;
+        const float beta = __fdividef(eta_new, eta);
         if (owner) ysum4(Y, e0, y);
 #pragma unroll
         for (int u = 0; u < 4; ++u) p[u] = valid[u] ? (r[u] - y[u]) + beta * p[u] : 0.f;
@@ -663,6 +665,375 @@ __global__ void __launch_bounds__(512, 1) k_pcg_tile(PcgArgs g)
     }
 }
 
+// ===========================================================================
+// wide-tile kernel: two threads per coupling block, ownership aligned with
+// the tiles
+// ===========================================================================
+//
+// k_pcg_wide<H> (7 <= n <= 16, N <= 128) runs the same iteration as
+// k_pcg_tile<H> with half the threads and about half its shared-memory
+// traffic.  Thread t < 2(N-1) holds rows rt*H .. rt*H+H-1 of Nhat_j over all
+// 2H columns (j = 1 + t/2, rt = t mod 2) and owns the same rows of knot j:
+// its row sums (Nhat_j x_{j-1})_rows are complete and stay in registers, and
+// its own part of x never has to be read back.  Only the transposed
+// products (Nhat_j^T x_j, partial over the two row halves) go through shared
+// memory, to the owners of knot j-1.  Threads 2(N-1) and 2(N-1)+1 own knot 0.
+//
+// Shared memory (floats): XP, XR [N][24] (a knot's first half at +0, its
+// second at +12), YC0, YC1 [N][24] (same layout; YC1 offset by 4 more
+// floats), the reduction slots, the eigenvalue bounds and the padded L.
+// These strides keep every 128-bit access of an iteration free of bank
+// conflicts for N = 16 .. 128.
+
+constexpr int kWS = 24;  // knot stride of the vectors and column sums
+constexpr int kWH = 12;  // offset of a knot's second half
+
+template <int H>
+struct WideTile {
+    float t[H][2 * H];
+};
+
+// logical padded position of unpadded column b (< 2H): halves of 8 slots
+template <int H>
+__host__ __device__ constexpr int pcol(int b)
+{
+    return b < H ? b : 8 + (b - H);
+}
+
+// physical offset of logical slot p within a knot
+__host__ __device__ constexpr int wphys(int p) { return p < 8 ? p : kWH + (p - 8); }
+
+// the 16 logical slots of a knot (four float4 chunks at +0, +4, +12, +16)
+__device__ __forceinline__ void wload16(const float* X, float (&x)[16])
+{
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const float4 v = *reinterpret_cast<const float4*>(X + wphys(4 * c));
+        x[4 * c] = v.x;
+        x[4 * c + 1] = v.y;
+        x[4 * c + 2] = v.z;
+        x[4 * c + 3] = v.w;
+    }
+}
+
+__device__ __forceinline__ void wload8(const float* X, float (&x)[8])
+{
+    const float4 a = *reinterpret_cast<const float4*>(X);
+    const float4 b = *reinterpret_cast<const float4*>(X + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+__device__ __forceinline__ void wstore8(float* X, const float (&v)[8])
+{
+    *reinterpret_cast<float4*>(X) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(X + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// One product with Nhat for the rows (j, rt) held by this thread: rs gets the
+// complete row sums of those rows, the column sums (partial over the row
+// halves) go to yc_base for knot j-1; returns xr^T rs, this thread's share of
+// x^T Nhat x.  xr is the thread's own part of x_j.
+template <int H>
+__device__ __forceinline__ float wide_matvec(const WideTile<H>& T, int j, const float* X,
+                                             const float (&xr)[8], float (&rs)[8],
+                                             float* yc_base)
+{
+    float xc[16];
+    wload16(X + (j - 1) * kWS, xc);
+    float cs[16];
+#pragma unroll
+    for (int a = 0; a < 8; ++a) rs[a] = 0.f;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) cs[c] = 0.f;
+#pragma unroll
+    for (int a = 0; a < H; ++a)
+#pragma unroll
+        for (int b = 0; b < 2 * H; ++b) {
+            const float v = T.t[a][b];
+            rs[a] = fmaf(v, xc[pcol<H>(b)], rs[a]);
+            cs[pcol<H>(b)] = fmaf(v, xr[a], cs[pcol<H>(b)]);
+        }
+    float q = 0.f;
+#pragma unroll
+    for (int a = 0; a < H; ++a) q = fmaf(xr[a], rs[a], q);
+    float* yc = yc_base + (j - 1) * kWS;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<float4*>(yc + wphys(4 * c)) =
+            make_float4(cs[4 * c], cs[4 * c + 1], cs[4 * c + 2], cs[4 * c + 3]);
+    return q;
+}
+
+// (Nhat x) at the eight owned slots: own row sums plus the two column parts
+__device__ __forceinline__ void wide_y(const float (&rs)[8], const float* YC0, const float* YC1,
+                                       int off, float (&y)[8])
+{
+    float c0[8], c1[8];
+    wload8(YC0 + off, c0);
+    wload8(YC1 + off, c1);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) y[k] = rs[k] + c0[k] + c1[k];
+}
+
+// sum over the owned rows a = half*H + k (k < H, valid) of (L_j r_hat_j)_a^2
+template <int H>
+__device__ __forceinline__ float lnorm_half(const float* LP, int KS, const float* gL, bool lsm,
+                                            const float* XR, int j, int half, int n,
+                                            const bool (&valid)[8])
+{
+    float s = 0.f;
+    const float* xk = XR + j * kWS;
+    if (lsm) {
+        const float4 x0 = *reinterpret_cast<const float4*>(xk);
+        const float4 x1 = *reinterpret_cast<const float4*>(xk + 4);
+        const float4 x2 = half ? *reinterpret_cast<const float4*>(xk + kWH)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 x3 = half ? *reinterpret_cast<const float4*>(xk + kWH + 4)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < H; ++k) {
+            if (!valid[k]) continue;
+            const float4* row =
+                reinterpret_cast<const float4*>(LP + j * KS + (half * H + k) * kLS);
+            float t = dot4(row[0], x0, 0.f);
+            t = dot4(row[1], x1, t);
+            if (half) {  // rows of the first half end before column H
+                t = dot4(row[2], x2, t);
+                t = dot4(row[3], x3, t);
+            }
+            s = fmaf(t, t, s);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < H; ++k) {
+            if (!valid[k]) continue;
+            const int a = half * H + k;
+            const float* row = gL + (size_t)j * n * n + a * n;
+            float t = 0.f;
+            for (int b = 0; b <= a; ++b) t += row[b] * xk[wphys(pcol<H>(b))];
+            s = fmaf(t, t, s);
+        }
+    }
+    return s;
+}
+
+template <int H>
+__device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
+{
+    extern __shared__ __align__(16) float sm[];
+    const Work& w = g.w;
+    const int N = w.N, n = w.n, T = blockDim.x, tid = threadIdx.x;
+    const int EX = N * kWS;
+    const bool rule0 = g.rule == GATO_STOP_RESIDUAL;
+    const bool lsm = rule0 && g.l_smem;
+    const int KS = l_knot_stride(n);
+
+    float* XP = sm;
+    float* XR = XP + EX;
+    float* YC0 = XR + EX;
+    float* YC1 = YC0 + EX + 4;
+    const int zero_count = 4 * EX + 8;
+    float2* redA = reinterpret_cast<float2*>(sm + zero_count);
+    float2* redB = redA + 32;
+    float2* redC = redA + 64;
+    float2* redD = redA + 96;  // also used as float4[16] by block_sum
+    float* DL = reinterpret_cast<float*>(redA + 160);
+    float* LP = DL + ((N + 3) & ~3);
+
+    for (int i = tid; i < zero_count; i += T) sm[i] = 0.f;
+    for (int j = tid; j < N; j += T) DL[j] = w.dlow[sol * w.sN + j];
+    const float* gL = w.L + sol * w.sNnn;
+    if (lsm) {
+        for (int t = tid; t < N * n * 16; t += T) {
+            const int c = t & 15, ja = t >> 4, j = ja / n, a = ja - j * n;
+            const int b = c < 8 ? c : H + (c - 8);
+            const bool in = (c < 8 ? c < H : c - 8 < n - H) && b <= a;
+            LP[j * KS + a * kLS + c] = in ? gL[(size_t)j * n * n + a * n + b] : 0.f;
+        }
+    }
+
+    // tile rows (block jb, half rt) and the owned slots (knot jo, same half)
+    const int rt = tid & 1;
+    const bool has_tile = tid < 2 * (N - 1);
+    const int jb = 1 + (tid >> 1);
+    const bool owner = tid < 2 * N;
+    const int jo = has_tile ? jb : 0;
+    const int half = rt;
+    float* yc_base = rt ? YC1 : YC0;
+    WideTile<H> tile;
+    {
+        const float* blk = w.Nh + sol * w.sKnn + (size_t)(has_tile ? jb - 1 : 0) * n * n;
+#pragma unroll
+        for (int a = 0; a < H; ++a)
+#pragma unroll
+            for (int b = 0; b < 2 * H; ++b) {
+                const int ra = rt * H + a;
+                tile.t[a][b] = (has_tile && ra < n && b < n) ? blk[ra * n + b] : 0.f;
+            }
+    }
+    const int xo = jo * kWS + half * kWH;  // owned slots in XP / XR / YC
+    bool valid[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) valid[k] = owner && k < H && half * H + k < n;
+    const int gi0 = jo * n + half * H;  // unpadded index of owned slot k is gi0 + k
+    const float* ghat = g.rhs.ghat + sol * w.sNn;
+    const float* gam = g.rhs.gamma + sol * w.sNn;
+    const float dl = owner ? DL[jo] : 0.f;
+    float lam[8], r[8], p[8], y[8], rs[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) rs[k] = 0.f;
+    __syncthreads();
+
+    // lambda_hat0 = L^T lambda0
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        lam[k] = 0.f;
+        if (valid[k] && g.lambda0) {
+            const int a = half * H + k;
+            const float* Lj = gL + (size_t)jo * n * n;
+            const float* l0 = g.lambda0 + (size_t)sol * N * n + jo * n;
+            float x = 0.f;
+            for (int b = a; b < n; ++b) x += Lj[b * n + a] * l0[b];
+            lam[k] = x;
+        }
+    }
+    if (owner) wstore8(XP + xo, lam);
+    __syncthreads();
+    if (has_tile) wide_matvec<H>(tile, jb, XP, lam, rs, yc_base);
+    __syncthreads();
+    // r_hat = ghat - S_hat lambda_hat
+    float rr = 0.f, gg = 0.f;
+    if (owner) wide_y(rs, YC0, YC1, xo, y);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        r[k] = 0.f;
+        if (valid[k]) {
+            const int i = gi0 + k;
+            r[k] = ghat[i] - lam[k] - y[k];
+            rr += r[k] * r[k];
+            gg += rule0 ? gam[i] * gam[i] : ghat[i] * ghat[i];
+        }
+    }
+    if (owner) wstore8(XR + xo, r);
+    post2(rr, gg, redB);
+    __syncthreads();  // XR complete; the column sums of lambda are read
+    float q = has_tile ? wide_matvec<H>(tile, jb, XR, r, rs, yc_base) : 0.f;
+    float lsq = 0.f;
+    if (rule0) lsq = lnorm_half<H>(LP, KS, gL, lsm, XR, jo, half, n, valid);
+    post2(q, lsq, redC);
+    __syncthreads();
+    float2 sB = collect2(redB), sC = collect2(redC);
+    float eta = sB.x - 2.f * sC.x;  // r^T (I - Nhat) r
+    const float ref = g.rule == GATO_STOP_PRECOND ? eta : sB.y;
+    const float thr = g.eps * g.eps * ref;
+    float stopq = g.rule == GATO_STOP_RESIDUAL ? sC.y : (g.rule == GATO_STOP_SCALED ? sB.x : eta);
+    bool done = stopq <= thr;
+    bool nonfinite = !isfinite(eta) || !isfinite(stopq);
+    if (owner) wide_y(rs, YC0, YC1, xo, y);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) p[k] = valid[k] ? r[k] - y[k] : 0.f;  // z = (I - Nhat) r
+    if (owner) wstore8(XP + xo, p);
+    // the exact ||L r_hat|| is gated as in k_pcg_tile
+    bool exact_next;
+    {
+        float lb = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) lb += dl * r[k] * r[k];
+        float lbv[1] = {lb};
+        block_sum<1>(lbv, reinterpret_cast<float4*>(redD));
+        exact_next = rule0 && lbv[0] <= 1.25f * thr;
+    }
+    __syncthreads();
+
+    int it = 0;
+    while (!done && !nonfinite && it < g.max_iters) {
+        ++it;
+        // A: Nhat p: own row sums, column sums to the owners of knot j-1;
+        // p^T Nhat p and p^T p partials
+        q = has_tile ? wide_matvec<H>(tile, jb, XP, p, rs, yc_base) : 0.f;
+        float pp = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pp = fmaf(p[k], p[k], pp);
+        post2(q, pp, redA);
+        __syncthreads();
+        // B: alpha = eta / p^T S_hat p; lambda and r updates
+        const float2 sA = collect2(redA);
+        const float pv = sA.y + 2.f * sA.x;
+        const float alpha = __fdividef(eta, pv);
+        if (owner) wide_y(rs, YC0, YC1, xo, y);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float v = p[k] + y[k];
+            lam[k] = fmaf(alpha, p[k], lam[k]);
+            r[k] = valid[k] ? fmaf(-alpha, v, r[k]) : 0.f;
+        }
+        if (owner) wstore8(XR + xo, r);
+        __syncthreads();
+        // C: Nhat r; r^T Nhat r and r^T r partials, the lower bound and, when
+        // gated in, ||L r_hat||^2
+        q = has_tile ? wide_matvec<H>(tile, jb, XR, r, rs, yc_base) : 0.f;
+        rr = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) rr = fmaf(r[k], r[k], rr);
+        float lsq = 0.f;
+        const bool exact = exact_next;
+        if (exact) lsq = lnorm_half<H>(LP, KS, gL, lsm, XR, jo, half, n, valid);
+        post2(q, rr, redB);
+        post2(dl * rr, lsq, redC);
+        __syncthreads();
+        // D: eta' = r^T (I - Nhat) r, convergence, p = z + beta p
+        sB = collect2(redB);
+        sC = collect2(redC);
+        const float eta_new = sB.y - 2.f * sB.x;
+        float lsq_all = sC.y;
+        bool have_exact = exact;
+        if (rule0 && !exact && sC.x * 0.999f <= thr) {
+            lsq = lnorm_half<H>(LP, KS, gL, lsm, XR, jo, half, n, valid);
+            float lv[1] = {lsq};
+            block_sum<1>(lv, reinterpret_cast<float4*>(redD));
+            lsq_all = lv[0];
+            have_exact = true;
+        }
+        stopq = g.rule == GATO_STOP_RESIDUAL ? lsq_all
+                                             : (g.rule == GATO_STOP_SCALED ? sB.y : eta_new);
+        if (!isfinite(eta_new + pv + stopq + sC.x)) {  // NaN and Inf propagate
+            nonfinite = true;
+            break;
+        }
+        done = (!rule0 || have_exact) && stopq <= thr;
+        if (done) break;
+        exact_next = rule0 && sC.x <= 1.25f * thr;
+        const float beta = __fdividef(eta_new, eta);
+        if (owner) wide_y(rs, YC0, YC1, xo, y);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) p[k] = valid[k] ? fmaf(beta, p[k], r[k] - y[k]) : 0.f;
+        if (owner) wstore8(XP + xo, p);
+        eta = eta_new;
+        __syncthreads();
+    }
+    __syncthreads();
+    if (owner) wstore8(XP + xo, lam);
+    __syncthreads();
+    recover_dz(g.w, g.rhs, g.lambda, g.dX, g.dU, sol,
+               [&](int j, int b) { return XP[j * kWS + wphys(pcol<H>(b))]; }, YC0);
+    finish(g, sol, it, done, nonfinite);
+}
+
+template <int H>
+__global__ void __launch_bounds__(256, 1) k_pcg_wide(PcgArgs g)
+{
+    __shared__ int s_sol;
+    for (;;) {
+        if (threadIdx.x == 0) s_sol = atomicAdd(g.queue, 1);
+        __syncthreads();
+        const int sol = s_sol;
+        __syncthreads();
+        if (sol >= g.w.M) break;
+        pcg_wide_solve<H>(g, sol);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -675,6 +1046,16 @@ size_t generic_smem_bytes(const Work& w, int nh_smem, int l_smem)
     if (l_smem) f += round4(N * (n * (n + 1) / 2));
     f += 4 * round4(N * n);  // lambda_hat, r_hat, p, v
     f += 64 * 4;             // two float4[32] reduction buffers
+    return f * sizeof(float);
+}
+
+size_t wide_smem_bytes(const Work& w, int l_smem)
+{
+    const size_t n = w.n, N = w.N;
+    size_t f = 4 * kWS * N + 8;  // XP, XR, YC0/1
+    f += 5 * 32 * 2;            // five float2[32] reduction buffers
+    f += round4(N);             // DL
+    if (l_smem) f += N * (size_t)l_knot_stride((int)n);
     return f * sizeof(float);
 }
 
@@ -746,11 +1127,37 @@ cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const f
     const size_t limit = (size_t)h->smem_optin;
     const int want_l = p->stop_rule == GATO_STOP_RESIDUAL;
 
-    // register-tiled kernel: 7 <= n <= 16, four threads per coupling block
     const int H = (w.n + 1) / 2;
+    const bool tiled_n = w.n >= 7 && w.n <= 16;
+
+    // wide-tile kernel: two threads per coupling block
+    int Tw = ((2 * w.N + 31) / 32) * 32;
+    if (Tw < 64) Tw = 64;
+    const int kind = h->pcg_kernel;
+    if ((kind == GATO_PCG_AUTO || kind == GATO_PCG_WIDE) && tiled_n && Tw <= 256) {
+        a.nh_smem = 0;
+        a.l_smem = want_l;
+        size_t smem = wide_smem_bytes(w, a.l_smem);
+        if (smem > limit) {
+            a.l_smem = 0;
+            smem = wide_smem_bytes(w, 0);
+        }
+        if (smem <= limit) {
+            switch (H) {
+                case 4: return launch_persistent(k_pcg_wide<4>, a, Tw, smem, h->num_sms, st);
+                case 5: return launch_persistent(k_pcg_wide<5>, a, Tw, smem, h->num_sms, st);
+                case 6: return launch_persistent(k_pcg_wide<6>, a, Tw, smem, h->num_sms, st);
+                case 7: return launch_persistent(k_pcg_wide<7>, a, Tw, smem, h->num_sms, st);
+                case 8: return launch_persistent(k_pcg_wide<8>, a, Tw, smem, h->num_sms, st);
+                default: break;
+            }
+        }
+    }
+
+    // register-tiled kernel: 7 <= n <= 16, four threads per coupling block
     int T = ((4 * w.N + 31) / 32) * 32;
     if (T < 64) T = 64;
-    if (h->pcg_kernel != GATO_PCG_GENERIC && w.n >= 7 && w.n <= 16 && T <= 512) {
+    if (kind != GATO_PCG_GENERIC && tiled_n && T <= 512) {
         a.nh_smem = 0;
         a.l_smem = want_l;
         size_t smem = tile_smem_bytes(w, a.l_smem);

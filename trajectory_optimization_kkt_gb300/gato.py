@@ -26,6 +26,8 @@ GATO_STATUS_NONFINITE = 8
 
 GATO_PCG_AUTO = 0
 GATO_PCG_GENERIC = 1
+GATO_PCG_WIDE = 2
+GATO_PCG_TILE = 3
 
 GATO_LINSYS_AUTO = 0
 GATO_LINSYS_PCG = 1
