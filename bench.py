@@ -37,8 +37,8 @@ WORKLOAD_INDEX = 4  # M=256, N=128, n=14, m=7
 # solve launch at this workload, from an ncu capture; valid only for the
 # kernel source it was taken on (sha256 prefix of csrc/pcg.cu), null
 # otherwise.  Captured on 152 solves (one block per SM) and scaled
-# by the solves processed to the 256-solve launch (90.04 MB x 256 / 152).
-PCG_TRAFFIC = {"pcg_sha": "31d7c3d2352bf4ad", "bytes_per_launch": 151652460}
+# by the solves processed to the 256-solve launch (90.13 MB x 256 / 152).
+PCG_TRAFFIC = {"pcg_sha": "44a137b49a059c04", "bytes_per_launch": 151796467}
 
 FP32_LANES_PER_SM = 128  # FFMA lanes per SM (4 sub-partitions x 32)
 
