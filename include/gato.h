@@ -129,8 +129,10 @@ typedef struct gato_params {
     float mu;            /* L1 penalty weight (default 10)                        */
     int merit_threads;   /* threads per merit block, 32..256, multiple of 32
                             (default 64); results are bit-identical at any size   */
-    float refine_eps;    /* PCG tolerance of each refinement correction; 0 means
-                            pcg_eps (default 0.1: a correction only needs a digit) */
+    float refine_eps;    /* PCG tolerance of each refinement correction, on the
+                            preconditioned residual sqrt(r^T Phi^-1 r / r0^T Phi^-1
+                            r0); 0 means pcg_eps (default 0.1: a correction only
+                            needs a digit)                                         */
     int merit_kernel;    /* GATO_MERIT_FUSED (default) or GATO_MERIT_PER_CANDIDATE */
     int linsys;          /* GATO_LINSYS_* (default GATO_LINSYS_AUTO)              */
     int bdsv_horizon;    /* GATO_LINSYS_AUTO: direct solve when N >= bdsv_horizon
@@ -269,9 +271,10 @@ int gato_linesearch(gato_handle* h, const gato_params* p, const float* Q, const 
  * k > 0 the KKT solution is refined k times: the residual of the full KKT
  * system is formed from the inputs in compensated fp32 (error-free products
  * and sums, about as accurate as fp64 accumulation), the correction is solved
- * with the same S (PCG to p->refine_eps, relative residual of the correction
- * system; or the direct solve's factors), and added to dz and lambda; iters
- * then counts PCG iterations over all solves of the refinement. */
+ * with the same S (PCG to p->refine_eps on the correction system's relative
+ * preconditioned residual, or the direct solve's factors), and added to dz
+ * and lambda; iters then counts PCG iterations over all solves of the
+ * refinement. */
 int gato_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const float* R,
                    const float* q, const float* r, const float* A, const float* B,
                    const float* e, const float* s0, float* dX, float* dU, float* lambda,

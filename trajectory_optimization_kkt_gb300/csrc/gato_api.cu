@@ -123,8 +123,12 @@ cudaError_t run_kkt_core(gato_handle* h, const gato_params* p, const float* Q_fo
         }
     }
     if (timed) record(h, 2, st);
-    gato_params pc = *p;  // PCG corrections are solved to refine_eps
+    // PCG corrections are solved to refine_eps on the preconditioned residual
+    // (r^T Phi^-1 r): a correction only needs a digit, and that test costs no
+    // residual-norm evaluation
+    gato_params pc = *p;
     if (p->refine_eps > 0.f) pc.pcg_eps = p->refine_eps;
+    pc.stop_rule = GATO_STOP_PRECOND;
     for (int k = 0; k < p->refine_steps && err == cudaSuccess; ++k) {
         err = launch_kkt_residual(h, Q_form, R, q, r, A, B, e, s0, dX, dU, lambda, st);
         if (err == cudaSuccess)
