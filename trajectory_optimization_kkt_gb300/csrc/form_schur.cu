@@ -137,6 +137,9 @@ __global__ void k_form_off(Work w)
 }
 
 // Right-hand side for (q, r, e, s0); s0 of solve i starts at s0 + i * s0_stride.
+// One warp per knot, lanes over rows; with NPX > 0 (n, m <= NPX) every row
+// product is unrolled and predicated so that its loads are in flight at once.
+template <int NPX>
 __global__ void k_form_rhs(Work w, Rhs out, const float* __restrict__ q,
                            const float* __restrict__ r, const float* __restrict__ e,
                            const float* __restrict__ s0, size_t s0_stride)
@@ -144,7 +147,7 @@ __global__ void k_form_rhs(Work w, Rhs out, const float* __restrict__ q,
     extern __shared__ __align__(16) float sm[];
     const int n = w.n, m = w.m, N = w.N;
     const int nn = n * n;
-    const int warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5, wpb = blockDim.x >> 5, lane = lane_id();
     const long g = (long)blockIdx.x * wpb + warp;
     if (g >= (long)w.M * N) return;
     const int sol = (int)(g / N), j = (int)(g % N);
@@ -152,28 +155,38 @@ __global__ void k_form_rhs(Work w, Rhs out, const float* __restrict__ q,
     float* sg = sm + (size_t)warp * n;
     const float* Qi = w.Qinv + sol * w.sNnn + (size_t)j * nn;
     const float* qj = q + ((size_t)sol * N + j) * n;
-
-    if (j == 0) {
-        warp_copy(sg, s0 + sol * s0_stride, n);
-        __syncwarp();
-        warp_gemv<false>(n, n, Qi, qj, sg, 1.f, true);
-    } else {
-        warp_copy(sg, e + ((size_t)sol * K + (j - 1)) * n, n);
-        __syncwarp();
-        warp_gemv<false>(n, n, w.O + sol * w.sKnn + (size_t)(j - 1) * nn,
-                         q + ((size_t)sol * N + (j - 1)) * n, sg, 1.f, true);
-        warp_gemv<false>(n, m, w.V + sol * w.sKnm + (size_t)(j - 1) * n * m,
-                         r + ((size_t)sol * K + (j - 1)) * m, sg, -1.f, true);
-        warp_gemv<false>(n, n, Qi, qj, sg, 1.f, true);
+    const float* qp = q + ((size_t)sol * N + (j > 0 ? j - 1 : 0)) * n;
+    const float* rp = r + ((size_t)sol * K + (j > 0 ? j - 1 : 0)) * m;
+    const float* Op = w.O + sol * w.sKnn + (size_t)(j > 0 ? j - 1 : 0) * nn;
+    const float* Vp = w.V + sol * w.sKnm + (size_t)(j > 0 ? j - 1 : 0) * n * m;
+    auto at = [](const float* v) { return [v](int b) { return v[b]; }; };
+    for (int a = lane; a < n; a += 32) {
+        const float t = strided_dot<NPX>(Qi + a * n, 1, at(qj), 0, n);  // (Q_j^-1 q_j)_a
+        float gv;
+        if (j == 0) {
+            gv = s0[sol * s0_stride + a] + t;
+        } else {
+            gv = e[((size_t)sol * K + (j - 1)) * n + a];
+            gv += strided_dot<NPX>(Op + a * n, 1, at(qp), 0, n);
+            gv -= strided_dot<NPX>(Vp + a * m, 1, at(rp), 0, m);
+            gv += t;
+        }
+        sg[a] = gv;
+        out.gamma[sol * w.sNn + (size_t)j * n + a] = gv;
+        out.avec[sol * w.sNn + (size_t)j * n + a] = -t;
     }
-    warp_copy(out.gamma + sol * w.sNn + (size_t)j * n, sg, n);
-    warp_gemv<false>(n, n, w.Linv + sol * w.sNnn + (size_t)j * nn, sg,
-                     out.ghat + sol * w.sNn + (size_t)j * n, 1.f, false);
-    warp_gemv<false>(n, n, Qi, qj, out.avec + sol * w.sNn + (size_t)j * n, -1.f, false);
-    if (j < N - 1)
-        warp_gemv<false>(m, m, w.Rinv + sol * w.sKmm + (size_t)j * m * m,
-                         r + ((size_t)sol * K + j) * m, out.bvec + sol * w.sKm + (size_t)j * m,
-                         -1.f, false);
+    __syncwarp();
+    const float* Li = w.Linv + sol * w.sNnn + (size_t)j * nn;
+    for (int a = lane; a < n; a += 32)
+        out.ghat[sol * w.sNn + (size_t)j * n + a] =
+            strided_dot<NPX>(Li + a * n, 1, at(sg), 0, a + 1);
+    if (j < N - 1) {
+        const float* Ri = w.Rinv + sol * w.sKmm + (size_t)j * m * m;
+        const float* rj = r + ((size_t)sol * K + j) * m;
+        for (int c = lane; c < m; c += 32)
+            out.bvec[sol * w.sKm + (size_t)j * m + c] =
+                -strided_dot<NPX>(Ri + c * m, 1, at(rj), 0, m);
+    }
 }
 
 // warps per block so that the per-warp slices fit in `budget` bytes
@@ -228,8 +241,13 @@ cudaError_t launch_form_rhs(gato_handle* h, int set, const float* q, const float
                             const float* e, const float* s0, size_t s0_stride, cudaStream_t st)
 {
     const Work& w = h->w;
-    return launch_warp_per_item(k_form_rhs, (long)w.M * w.N, (size_t)w.n * sizeof(float), h,
-                                st, w, w.rhs[set], q, r, e, s0, s0_stride);
+    const long knots = (long)w.M * w.N;
+    const size_t per_warp = (size_t)w.n * sizeof(float);
+    if (w.n <= 16 && w.m <= 16)
+        return launch_warp_per_item(k_form_rhs<16>, knots, per_warp, h, st, w, w.rhs[set], q, r,
+                                    e, s0, s0_stride);
+    return launch_warp_per_item(k_form_rhs<0>, knots, per_warp, h, st, w, w.rhs[set], q, r, e,
+                                s0, s0_stride);
 }
 
 }  // namespace gato

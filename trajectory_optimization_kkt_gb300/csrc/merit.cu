@@ -149,6 +149,7 @@ __global__ void k_merit_reduce(Work w, int A1, float mu, float* merit, int32_t* 
 
 constexpr int kMaxA1 = GATO_MAX_ALPHA + 1;
 
+template <int NPX>
 __global__ void __launch_bounds__(512) k_merit_fused(MeritArgs g, float mu, float* merit,
                                                      int32_t* best, uint32_t* status)
 {
@@ -183,9 +184,10 @@ __global__ void __launch_bounds__(512) k_merit_fused(MeritArgs g, float mu, floa
         __syncwarp();
         const float* Qk = g.Q + ((size_t)sol * N + k) * n * n;
         const float* qk = g.q + ((size_t)sol * N + k) * n;
+        auto xs = [&](int b) { return xv[b]; };
+        auto us = [&](int b) { return uv[b]; };
         for (int a = lane; a < n; a += 32) {
-            float qx = 0.f;
-            for (int b = 0; b < n; ++b) qx += Qk[a * n + b] * xv[b];
+            const float qx = strided_dot<NPX>(Qk + a * n, 1, xs, 0, n);
             c2 += xv[a] * qx;
             c1 += qk[a] * xv[a];
             if (has_u) {
@@ -193,8 +195,8 @@ __global__ void __launch_bounds__(512) k_merit_fused(MeritArgs g, float mu, floa
                 const float* Bk = g.B + ((size_t)sol * K + k) * n * m;
                 const float ea = g.e[((size_t)sol * K + k) * n + a];
                 float wa = -xn[a];
-                for (int b = 0; b < n; ++b) wa += Ak[a * n + b] * xv[b];
-                for (int b = 0; b < m; ++b) wa += Bk[a * m + b] * uv[b];
+                wa += strided_dot<NPX>(Ak + a * n, 1, xs, 0, n);
+                wa += strided_dot<NPX>(Bk + a * m, 1, us, 0, m);
 #pragma unroll
                 for (int i = 0; i < kMaxA1; ++i)
                     if (i < A1) viol[i] += fabsf(ea + alpha[i] * wa);
@@ -209,8 +211,7 @@ __global__ void __launch_bounds__(512) k_merit_fused(MeritArgs g, float mu, floa
             const float* Rk = g.R + ((size_t)sol * K + k) * m * m;
             const float* rk = g.r + ((size_t)sol * K + k) * m;
             for (int c = lane; c < m; c += 32) {
-                float ru = 0.f;
-                for (int b = 0; b < m; ++b) ru += Rk[c * m + b] * uv[b];
+                const float ru = strided_dot<NPX>(Rk + c * m, 1, us, 0, m);
                 c2 += uv[c] * ru;
                 c1 += rk[c] * uv[c];
             }
@@ -297,12 +298,15 @@ cudaError_t launch_merit(gato_handle* h, const gato_params* p, const float* Q,
     a.A1 = p->n_alpha + 1;
     a.beta = p->beta;
     if (p->merit_kernel == GATO_MERIT_FUSED) {
-        int warps = (w.N + 7) / 8;  // about eight knots per warp
+        int warps = (w.N + 3) / 4;  // about four knots per warp
         if (warps > 16) warps = 16;
         if (warps < 1) warps = 1;
         const size_t smem =
             ((size_t)warps * (2 * w.n + w.m) + (size_t)warps * (a.A1 + 2) + a.A1) * sizeof(float);
-        k_merit_fused<<<w.M, 32 * warps, smem, st>>>(a, p->mu, merit, best, status);
+        if (w.n <= 16 && w.m <= 16)
+            k_merit_fused<16><<<w.M, 32 * warps, smem, st>>>(a, p->mu, merit, best, status);
+        else
+            k_merit_fused<0><<<w.M, 32 * warps, smem, st>>>(a, p->mu, merit, best, status);
         return cudaGetLastError();
     }
     const size_t smem = (size_t)(5 * w.n + 2 * w.m) * sizeof(float);
