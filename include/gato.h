@@ -220,7 +220,10 @@ int gato_form_schur(gato_handle* h, const float* Q, const float* R, const float*
 /* Copies the explicit blocks formed by the last gato_form_schur into caller
  * buffers (any may be NULL): S_diag [M][N][n][n], S_off [M][N-1][n][n] (block
  * (j, j-1) at index j-1), gamma [M][N][n], Phi_diag [M][N][n][n], Phi_off
- * [M][N-1][n][n].  Device-to-device copies on `stream`. */
+ * [M][N-1][n][n].  Device-to-device copies on `stream`.  The solve applies
+ * Phi^-1 in factored form, so the explicit Phi^-1 blocks are formed from
+ * those factors on the first request after a formation (two kernels on
+ * `stream`, before the copies). */
 int gato_get_schur(gato_handle* h, float* S_diag, float* S_off, float* gamma,
                    float* Phi_diag, float* Phi_off, void* stream);
 

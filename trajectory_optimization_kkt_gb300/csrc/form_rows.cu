@@ -13,10 +13,12 @@
 //   k_rows_knot  knot k:  Q_k^-1, R_k^-1, S_{k+1,k} = -A_k Q_k^-1,
 //                         V_k = B_k R_k^-1, and theta_k = A_k Q_k^-1 A_k^T +
 //                         V_k B_k^T (stored where S_{k+1,k+1} goes)
-//   k_rows_diag  row j:   S_jj = Q_j^-1 + theta_{j-1}, L_j, L_j^-1, S_jj^-1 and
-//                         the eigenvalue bound 1 / ||L_j^-1||_F^2
-//   k_rows_off   row j:   Nhat_j = L_j^-1 S_{j,j-1} L_{j-1}^-T and the explicit
-//                         Phi^-1 block -S_jj^-1 S_{j,j-1} S_{j-1,j-1}^-1
+//   k_rows_diag  row j:   S_jj = Q_j^-1 + theta_{j-1}, L_j, L_j^-1 and the
+//                         eigenvalue bound 1 / ||L_j^-1||_F^2
+//   k_rows_off   row j:   Nhat_j = L_j^-1 S_{j,j-1} L_{j-1}^-T
+// The solve applies Phi^-1 in that factored form; the explicit blocks
+// S_jj^-1 and -S_jj^-1 S_{j,j-1} S_{j-1,j-1}^-1 are formed only for export
+// (k_rows_phi_diag, k_rows_phi_off, launched by gato_get_schur).
 #include "rows16.cuh"
 
 namespace gato {
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(256) k_rows_diag(Work w, uint32_t* status)
     }
     const bool ok = rows_cholesky(d, li, n);
     if (h.active) store_row(d, w.L + off, n, n, li);
-    float x[NP], c[NP];
+    float x[NP];
     rows_lower_inverse(d, x, li, n, h.S0);
     if (h.active) store_row(x, w.Linv + off, n, n, li);
     // ||L_j^-1||_F^2 = trace(S_jj^-1) >= 1 / lambda_min(S_jj)
@@ -167,8 +169,6 @@ __global__ void __launch_bounds__(256) k_rows_diag(Work w, uint32_t* status)
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) f += __shfl_xor_sync(0xffffffffu, f, o, 16);
     if (h.active && li == 0) w.dlow[sol * w.sN + j] = 1.f / f;
-    rows_gram_lower(h.S0, c, li, n);
-    if (h.active) store_row(c, w.Pd + off, n, n, li);
     if (h.active && !ok && li == 0) atomicOr(status + sol, GATO_STATUS_NONPOSITIVE_PIVOT);
 }
 
@@ -196,8 +196,42 @@ __global__ void __launch_bounds__(256) k_rows_off(Work w)
     for (int c = 0; c < NP; ++c) r[c] = 0.f;
     rows_mul_bt(t, h.S1, n, r, 1.f);
     if (h.active) store_row(r, w.Nh + oj, n, n, li);
-    // Phi^-1 block: -(S_jj^-1 S_{j,j-1}) S_{j-1,j-1}^-1
+}
+
+// The explicit blocks of Phi^-1 for export (the solve applies Phi^-1 in the
+// factored form L^-T (I - Nhat) L^-1): diagonal S_jj^-1 = L_j^-T L_j^-1 ...
+__global__ void __launch_bounds__(256) k_rows_phi_diag(Work w)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int n = w.n, N = w.N;
+    const Half h = half_setup((long)w.M * N, sm);
+    const long item = h.active ? h.item : 0;
+    const int sol = (int)(item / N), j = (int)(item % N);
+    const int li = h.li;
+    const size_t off = sol * w.sNnn + (size_t)j * n * n;
+    float x[NP], c[NP];
+    load_row(x, w.Linv + off, n, n, li, false);
     __syncwarp();
+    publish(x, h.S0, li);
+    __syncwarp();
+    rows_gram_lower(h.S0, c, li, n);
+    if (h.active) store_row(c, w.Pd + off, n, n, li);
+}
+
+// ... and off-diagonal -S_jj^-1 S_{j,j-1} S_{j-1,j-1}^-1
+__global__ void __launch_bounds__(256) k_rows_phi_off(Work w)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int n = w.n, N = w.N, K = N - 1;
+    const Half h = half_setup((long)w.M * K, sm);
+    const long item = h.active ? h.item : 0;
+    const int sol = (int)(item / K), j = 1 + (int)(item % K);
+    const int li = h.li;
+    const size_t dj = sol * w.sNnn + (size_t)j * n * n, dp = dj - (size_t)n * n;
+    const size_t oj = sol * w.sKnn + (size_t)(j - 1) * n * n;
+    float a[NP], t[NP], r[NP];
+    load_row(a, w.O + oj, n, n, li, false);
+    publish(a, h.S0, li);  // S_{j,j-1} rows
     load_row(a, w.Pd + dp, n, n, li, false);
     publish(a, h.S1, li);  // S_{j-1,j-1}^-1 rows
     __syncwarp();
@@ -221,6 +255,14 @@ cudaError_t launch_rows(K kernel, long items, cudaStream_t st, Args... args)
 }  // namespace
 
 bool rows_formation_supported(const Work& w) { return w.n <= NP && w.m <= NP; }
+
+cudaError_t launch_form_phi(gato_handle* h, cudaStream_t st)
+{
+    const Work& w = h->w;
+    cudaError_t e = launch_rows(k_rows_phi_diag, (long)w.M * w.N, st, w);
+    if (e != cudaSuccess) return e;
+    return launch_rows(k_rows_phi_off, (long)w.M * (w.N - 1), st, w);
+}
 
 cudaError_t launch_form_rows(gato_handle* h, const float* Q, const float* R, const float* A,
                              const float* B, uint32_t* status, cudaStream_t st)

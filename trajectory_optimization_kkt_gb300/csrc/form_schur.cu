@@ -223,8 +223,11 @@ cudaError_t launch_form_matrices(gato_handle* h, const float* Q, const float* R,
                                  cudaStream_t st)
 {
     const Work& w = h->w;
-    if (!h->force_smem_form && rows_formation_supported(w))
+    h->phi_pending = 0;
+    if (!h->force_smem_form && rows_formation_supported(w)) {
+        h->phi_pending = 1;
         return launch_form_rows(h, Q, R, A, B, status, st);
+    }
     const size_t n = w.n, m = w.m, f = sizeof(float);
     const long knots = (long)w.M * w.N;
     cudaError_t e;

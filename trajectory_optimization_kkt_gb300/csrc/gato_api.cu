@@ -433,6 +433,10 @@ int gato_get_schur(gato_handle* h, float* S_diag, float* S_off, float* gamma,
     if (!h) return GATO_ERR_INVALID_ARG;
     const Work& w = h->w;
     cudaStream_t st = (cudaStream_t)stream;
+    if ((Phi_diag || Phi_off) && h->phi_pending) {
+        if (gato::launch_form_phi(h, st) != cudaSuccess) return GATO_ERR_CUDA;
+        h->phi_pending = 0;
+    }
     const size_t f = sizeof(float), K = (size_t)(w.N - 1);
     struct Item { float* dst; const float* src; size_t width, stride; } items[] = {
         {S_diag, w.D, (size_t)w.N * w.n * w.n, w.sNnn},

@@ -106,6 +106,7 @@ struct gato_handle {
     int pcg_kernel;         // GATO_PCG_* selected by gato_set_pcg_kernel
     int bdsv_kernel;        // GATO_BDSV_KERNEL_* selected by gato_set_bdsv_kernel
     int force_smem_form;    // GATO_FORM_SHARED selected by gato_set_form_kernel
+    int phi_pending;        // the last formation left the explicit Phi^-1 blocks unformed
     cudaEvent_t ev[5];  // start, after form, after PCG, after refinement, after merit
     int ev_used[5];
     gato_stats last;
@@ -128,6 +129,8 @@ cudaError_t launch_form_matrices(gato_handle* h, const float* Q, const float* R,
 bool rows_formation_supported(const Work& w);
 cudaError_t launch_form_rows(gato_handle* h, const float* Q, const float* R, const float* A,
                              const float* B, uint32_t* status, cudaStream_t st);
+// the explicit Phi^-1 blocks after a register formation (form_rows.cu)
+cudaError_t launch_form_phi(gato_handle* h, cudaStream_t st);
 cudaError_t launch_form_rhs(gato_handle* h, int set, const float* q, const float* r,
                             const float* e, const float* s0, size_t s0_stride, cudaStream_t st);
 cudaError_t launch_pcg(gato_handle* h, const gato_params* p, const float* lambda0,

@@ -395,6 +395,29 @@ __device__ __forceinline__ float dot4(const float4 a, const float4 b, float s)
     return fmaf(a.w, b.w, s);
 }
 
+// Row a of L_j into LP in the padded column layout (zeros above the
+// diagonal and in the padding), one row per thread and pass: its n loads are
+// issued together and it is written as four float4.
+template <int H>
+__device__ __forceinline__ void stage_l_rows(float* LP, int KS, const float* gL, int N, int n)
+{
+    for (int ja = threadIdx.x; ja < N * n; ja += blockDim.x) {
+        const int j = ja / n, a = ja - j * n;
+        const float* src = gL + (size_t)j * n * n + a * n;
+        float v[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const int b = c < 8 ? c : H + (c - 8);
+            const bool in = (c < 8 ? c < H : c - 8 < n - H) && b <= a;
+            v[c] = in ? src[b] : 0.f;
+        }
+        float4* dst = reinterpret_cast<float4*>(LP + j * KS + a * kLS);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+    }
+}
+
 // sum over the owned valid rows a = ao + u of (L_j r_hat_j)_a^2: from the
 // padded rows in shared memory (four float4 loads per row, the second-half
 // chunks only for rows that reach them), or row by row from global memory
@@ -464,15 +487,7 @@ __device__ __forceinline__ void pcg_tile_solve(const PcgArgs& g, int sol)
     for (int i = tid; i < zero_count; i += T) sm[i] = 0.f;
     for (int j = tid; j < N; j += T) DL[j] = w.dlow[sol * w.sN + j];
     const float* gL = w.L + sol * w.sNnn;
-    if (lsm) {
-        // row a of L_j in the padded column layout, zeros above the diagonal
-        for (int t = tid; t < N * n * 16; t += T) {
-            const int c = t & 15, ja = t >> 4, j = ja / n, a = ja - j * n;
-            const int b = c < 8 ? c : H + (c - 8);
-            const bool in = (c < 8 ? c < H : c - 8 < n - H) && b <= a;
-            LP[j * KS + a * kLS + c] = in ? gL[(size_t)j * n * n + a * n + b] : 0.f;
-        }
-    }
+    if (lsm) stage_l_rows<H>(LP, KS, gL, N, n);
 
     // the tile this thread holds: block jb = 1 + tid/4, tile (rt, ct)
     const int jb = 1 + (tid >> 2), rt = (tid >> 1) & 1, ct = tid & 1;
@@ -642,8 +657,8 @@ __device__ __forceinline__ void pcg_tile_solve(const PcgArgs& g, int sol)
     __syncthreads();
     if (owner) store4(XP, e0, lam);
     __syncthreads();
-    recover_dz(g.w, g.rhs, g.lambda, g.dX, g.dU, sol,
-               [&](int j, int b) { return XP[j * 16 + (b / H) * 8 + b % H]; }, YR0);
+    recover_dz<16>(g.w, g.rhs, g.lambda, g.dX, g.dU, sol,
+                   [&](int j, int b) { return XP[j * 16 + (b / H) * 8 + b % H]; }, YR0);
     finish(g, sol, it, done, nonfinite);
 }
 
@@ -844,14 +859,7 @@ __device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
     for (int i = tid; i < zero_count; i += T) sm[i] = 0.f;
     for (int j = tid; j < N; j += T) DL[j] = w.dlow[sol * w.sN + j];
     const float* gL = w.L + sol * w.sNnn;
-    if (lsm) {
-        for (int t = tid; t < N * n * 16; t += T) {
-            const int c = t & 15, ja = t >> 4, j = ja / n, a = ja - j * n;
-            const int b = c < 8 ? c : H + (c - 8);
-            const bool in = (c < 8 ? c < H : c - 8 < n - H) && b <= a;
-            LP[j * KS + a * kLS + c] = in ? gL[(size_t)j * n * n + a * n + b] : 0.f;
-        }
-    }
+    if (lsm) stage_l_rows<H>(LP, KS, gL, N, n);
 
     // tile rows (block jb, half rt) and the owned slots (knot jo, same half)
     const int rt = tid & 1;
@@ -1015,8 +1023,8 @@ __device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
     __syncthreads();
     if (owner) wstore8(XP + xo, lam);
     __syncthreads();
-    recover_dz(g.w, g.rhs, g.lambda, g.dX, g.dU, sol,
-               [&](int j, int b) { return XP[j * kWS + wphys(pcol<H>(b))]; }, YC0);
+    recover_dz<16>(g.w, g.rhs, g.lambda, g.dX, g.dU, sol,
+                   [&](int j, int b) { return XP[j * kWS + wphys(pcol<H>(b))]; }, YC0);
     finish(g, sol, it, done, nonfinite);
 }
 
