@@ -46,8 +46,30 @@ struct Acc2 {
     __device__ __forceinline__ float value() const { return __fadd_rn(s, c); }
 };
 
+// acc += sum_{b < cnt} M[b * stride] x[b]; with NPX > 0 (cnt <= NPX) all the
+// loads are issued first (unrolled, predicated), then the compensated chain
+template <int NPX>
+__device__ __forceinline__ void dot_acc(Acc2& acc, const float* M, int stride, const float* x,
+                                        int cnt)
+{
+    if constexpr (NPX > 0) {
+        float mv[NPX], xv[NPX];
+#pragma unroll
+        for (int b = 0; b < NPX; ++b) {
+            mv[b] = b < cnt ? M[b * stride] : 0.f;
+            xv[b] = b < cnt ? x[b] : 0.f;
+        }
+#pragma unroll
+        for (int b = 0; b < NPX; ++b)
+            if (b < cnt) acc.add_prod(mv[b], xv[b]);
+    } else {
+        for (int b = 0; b < cnt; ++b) acc.add_prod(M[b * stride], x[b]);
+    }
+}
+
 // one warp per knot, lanes over rows, compensated sums; the correction's data
 // (q2, r2, e2, s02) is written densely, like the caller's q, r, e, s0
+template <int NPX>
 __global__ void k_kkt_residual(Work w, const float* __restrict__ Q, const float* __restrict__ R,
                                const float* __restrict__ q, const float* __restrict__ r,
                                const float* __restrict__ A, const float* __restrict__ B,
@@ -68,10 +90,10 @@ __global__ void k_kkt_residual(Work w, const float* __restrict__ Q, const float*
         Acc2 acc;
         acc.add(q[((size_t)sol * N + k) * n + a]);
         acc.add(-l[a]);
-        for (int b = 0; b < n; ++b) acc.add_prod(Qk[a * n + b], x[b]);
+        dot_acc<NPX>(acc, Qk + a * n, 1, x, n);
         if (k < N - 1) {
             const float* Ak = A + ((size_t)sol * K + k) * n * n;
-            for (int b = 0; b < n; ++b) acc.add_prod(Ak[b * n + a], l[n + b]);
+            dot_acc<NPX>(acc, Ak + a, n, l + n, n);
         }
         w.q2[((size_t)sol * N + k) * n + a] = acc.value();
     }
@@ -90,31 +112,33 @@ __global__ void k_kkt_residual(Work w, const float* __restrict__ Q, const float*
         for (int c = lane; c < m; c += 32) {
             Acc2 acc;
             acc.add(r[((size_t)sol * K + k) * m + c]);
-            for (int b = 0; b < m; ++b) acc.add_prod(Rk[c * m + b], u[b]);
-            for (int b = 0; b < n; ++b) acc.add_prod(Bk[b * m + c], l[n + b]);
+            dot_acc<NPX>(acc, Rk + c * m, 1, u, m);
+            dot_acc<NPX>(acc, Bk + c, m, l + n, n);
             w.r2[((size_t)sol * K + k) * m + c] = acc.value();
         }
         for (int a = lane; a < n; a += 32) {
             Acc2 acc;
             acc.add(e[((size_t)sol * K + k) * n + a]);
             acc.add(-x[n + a]);
-            for (int b = 0; b < n; ++b) acc.add_prod(Ak[a * n + b], x[b]);
-            for (int b = 0; b < m; ++b) acc.add_prod(Bk[a * m + b], u[b]);
+            dot_acc<NPX>(acc, Ak + a * n, 1, x, n);
+            dot_acc<NPX>(acc, Bk + a * m, 1, u, m);
             w.e2[((size_t)sol * K + k) * n + a] = acc.value();
         }
     }
 }
 
-__global__ void k_accumulate(Work w, float* lam, float* dX, float* dU)
+// y += d over a dense array (the correction was written densely, [M][N][n]
+// and [M][N-1][m], by the linear solve), grid-stride
+__global__ void k_accumulate(float* lam, const float* dlam, float* dX, const float* ddX,
+                             size_t total_x, float* dU, const float* ddU, size_t total_u)
 {
-    const int sol = blockIdx.x;
-    const size_t Nn = (size_t)w.N * w.n, Km = (size_t)(w.N - 1) * w.m;
-    // the correction was written densely ([M][N][n], [M][N-1][m]) by the PCG kernel
-    for (size_t i = threadIdx.x; i < Nn; i += blockDim.x) {
-        lam[sol * Nn + i] += w.dlam[sol * Nn + i];
-        dX[sol * Nn + i] += w.ddX[sol * Nn + i];
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total_x; i += stride) {
+        lam[i] += dlam[i];
+        dX[i] += ddX[i];
     }
-    for (size_t i = threadIdx.x; i < Km; i += blockDim.x) dU[sol * Km + i] += w.ddU[sol * Km + i];
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total_u; i += stride)
+        dU[i] += ddU[i];
 }
 
 }  // namespace
@@ -128,8 +152,10 @@ cudaError_t launch_kkt_residual(gato_handle* h, const float* Q, const float* R,
     const Work& w = h->w;
     const long knots = (long)w.M * w.N;
     const int wpb = 4;
-    k_kkt_residual<<<(unsigned)((knots + wpb - 1) / wpb), 32 * wpb, 0, st>>>(
-        w, Q, R, q, r, A, B, e, s0, dX, dU, lambda);
+    // the compensated chains are the latency here, not the loads: the
+    // runtime-bounded loops (fewer registers, more warps) are the faster form
+    const unsigned blocks = (unsigned)((knots + wpb - 1) / wpb);
+    k_kkt_residual<0><<<blocks, 32 * wpb, 0, st>>>(w, Q, R, q, r, A, B, e, s0, dX, dU, lambda);
     return cudaGetLastError();
 }
 
@@ -137,7 +163,13 @@ cudaError_t launch_accumulate(gato_handle* h, float* lambda, float* dX, float* d
                               int32_t* iters, cudaStream_t st)
 {
     (void)iters;
-    k_accumulate<<<h->w.M, 256, 0, st>>>(h->w, lambda, dX, dU);
+    const Work& w = h->w;
+    const size_t tx = (size_t)w.M * w.N * w.n, tu = (size_t)w.M * (w.N - 1) * w.m;
+    size_t blocks = (tx + 255) / 256;
+    const size_t cap = (size_t)h->num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    k_accumulate<<<(unsigned)blocks, 256, 0, st>>>(lambda, w.dlam, dX, w.ddX, tx, dU, w.ddU, tu);
     return cudaGetLastError();
 }
 
