@@ -192,6 +192,30 @@ def test_solve_kkt_custom_sizes(name, M, N, n, m, refine):
     check_solution(prob, out, range(M))
 
 
+# horizons beyond 128 knots: the solve split over a cluster of 2 (N <= 256) or
+# 4 (N <= 512) CTAs, ragged splits included
+CLUSTER = [
+    ("N129_n7_m3_c2", 2, 129, 7, 3),
+    ("N200_n13_m5_c2", 2, 200, 13, 5),
+    ("N256_n14_m7_c2", 2, 256, 14, 7),
+    ("N300_n16_m8_c4", 2, 300, 16, 8),
+    ("N512_n14_m7_c4", 1, 512, 14, 7),
+]
+
+
+@pytest.mark.parametrize("name,M,N,n,m", CLUSTER, ids=[c[0] for c in CLUSTER])
+def test_cluster_kernel_long_horizons(name, M, N, n, m):
+    prob = random_lq(M, N, n, m, seed=650 + N + n)
+    p = gato.default_params(pcg_max_iters=4000, refine_steps=1)
+    out = solve(prob, p)
+    assert not out["status"].any(), out["status"]
+    check_solution(prob, out, range(M))
+    ref = solve(prob, p, gato.GATO_PCG_GENERIC)
+    assert np.abs(out["iters"] - ref["iters"]).max() <= 0.05 * ref["iters"].max() + 2
+    for j in range(M):
+        assert rel(out["lam"][j], ref["lam"][j]) < 1e-3
+
+
 @pytest.mark.parametrize("kind", [gato.GATO_PCG_WIDE, gato.GATO_PCG_TILE], ids=["wide", "tile"])
 @pytest.mark.parametrize("w", [WORKLOADS[1], WORKLOADS[4]], ids=lambda w: w.name)
 def test_tiled_and_generic_kernels_agree(w, kind):

@@ -27,10 +27,14 @@
 //     four block barriers per iteration.
 // k_pcg_generic  (any n <= 64): Nhat in shared memory when it fits (else read
 //     from global memory), one thread per vector element.
+#include <cooperative_groups.h>
+
 #include "gato_internal.cuh"
 
 namespace gato {
 namespace {
+
+namespace cg = cooperative_groups;
 
 struct PcgArgs {
     Work w;
@@ -747,15 +751,14 @@ __device__ __forceinline__ void wstore8(float* X, const float (&v)[8])
 
 // One product with Nhat for the rows (j, rt) held by this thread: rs gets the
 // complete row sums of those rows, the column sums (partial over the row
-// halves) go to yc_base for knot j-1; returns xr^T rs, this thread's share of
-// x^T Nhat x.  xr is the thread's own part of x_j.
+// halves) go to yc (knot j-1's slots); returns xr^T rs, this thread's share
+// of x^T Nhat x.  xprev holds x_{j-1}, xr is the thread's own part of x_j.
 template <int H>
-__device__ __forceinline__ float wide_matvec(const WideTile<H>& T, int j, const float* X,
-                                             const float (&xr)[8], float (&rs)[8],
-                                             float* yc_base)
+__device__ __forceinline__ float wide_matvec(const WideTile<H>& T, const float* xprev,
+                                             const float (&xr)[8], float (&rs)[8], float* yc)
 {
     float xc[16];
-    wload16(X + (j - 1) * kWS, xc);
+    wload16(xprev, xc);
     float cs[16];
 #pragma unroll
     for (int a = 0; a < 8; ++a) rs[a] = 0.f;
@@ -772,7 +775,6 @@ __device__ __forceinline__ float wide_matvec(const WideTile<H>& T, int j, const 
     float q = 0.f;
 #pragma unroll
     for (int a = 0; a < H; ++a) q = fmaf(xr[a], rs[a], q);
-    float* yc = yc_base + (j - 1) * kWS;
 #pragma unroll
     for (int c = 0; c < 4; ++c)
         *reinterpret_cast<float4*>(yc + wphys(4 * c)) =
@@ -881,6 +883,8 @@ __device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
             }
     }
     const int xo = jo * kWS + half * kWH;  // owned slots in XP / XR / YC
+    const int pj = (has_tile ? jb - 1 : 0) * kWS;  // knot j-1 of the tile rows
+    float* yc = yc_base + pj;
     bool valid[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) valid[k] = owner && k < H && half * H + k < n;
@@ -908,7 +912,7 @@ __device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
     }
     if (owner) wstore8(XP + xo, lam);
     __syncthreads();
-    if (has_tile) wide_matvec<H>(tile, jb, XP, lam, rs, yc_base);
+    if (has_tile) wide_matvec<H>(tile, XP + pj, lam, rs, yc);
     __syncthreads();
     // r_hat = ghat - S_hat lambda_hat
     float rr = 0.f, gg = 0.f;
@@ -926,7 +930,7 @@ __device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
     if (owner) wstore8(XR + xo, r);
     post2(rr, gg, redB);
     __syncthreads();  // XR complete; the column sums of lambda are read
-    float q = has_tile ? wide_matvec<H>(tile, jb, XR, r, rs, yc_base) : 0.f;
+    float q = has_tile ? wide_matvec<H>(tile, XR + pj, r, rs, yc) : 0.f;
     float lsq = 0.f;
     if (rule0) lsq = lnorm_half<H>(LP, KS, gL, lsm, XR, jo, half, n, valid);
     post2(q, lsq, redC);
@@ -959,7 +963,7 @@ __device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
         ++it;
         // A: Nhat p: own row sums, column sums to the owners of knot j-1;
         // p^T Nhat p and p^T p partials
-        q = has_tile ? wide_matvec<H>(tile, jb, XP, p, rs, yc_base) : 0.f;
+        q = has_tile ? wide_matvec<H>(tile, XP + pj, p, rs, yc) : 0.f;
         float pp = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) pp = fmaf(p[k], p[k], pp);
@@ -980,7 +984,7 @@ __device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
         __syncthreads();
         // C: Nhat r; r^T Nhat r and r^T r partials, the lower bound and, when
         // gated in, ||L r_hat||^2
-        q = has_tile ? wide_matvec<H>(tile, jb, XR, r, rs, yc_base) : 0.f;
+        q = has_tile ? wide_matvec<H>(tile, XR + pj, r, rs, yc) : 0.f;
         rr = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) rr = fmaf(r[k], r[k], rr);
@@ -1042,6 +1046,287 @@ __global__ void __launch_bounds__(256, 1) k_pcg_wide(PcgArgs g)
     }
 }
 
+// ===========================================================================
+// cluster kernel: one solve across the CTAs of a thread-block cluster
+// ===========================================================================
+//
+// k_pcg_cluster<H, C> (7 <= n <= 16, 128 < N <= 128 C) runs the wide-tile
+// iteration with a solve's knots split over the C CTAs of a cluster: CTA c
+// holds knots c*Nc .. c*Nc+Nc-1 (Nc = ceil(N / C)), their rows of Nhat and
+// the owned vector slots, exactly as k_pcg_wide does for a whole solve.  Only
+// a CTA's first block (j = c*Nc, c >= 1) reaches across: it reads x_{j-1}
+// from CTA c-1's shared memory and writes its transposed product there
+// (distributed shared memory).  Block sums add every CTA's warp slots in rank
+// order, so all CTAs hold the same scalars and take the same branches; every
+// phase barrier is a cluster barrier.
+
+template <int C>
+__device__ __forceinline__ float2 cluster_collect2(cg::cluster_group& cl, float2* buf)
+{
+    float2 s = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int rk = 0; rk < C; ++rk) {
+        const float2 v = collect2(cl.map_shared_rank(buf, rk));
+        s.x += v.x;
+        s.y += v.y;
+    }
+    return s;
+}
+
+// lambda = L^-T lambda_hat for this CTA's knots, then (after a cluster
+// barrier, with the neighbours' lambda in global memory) dz by eq. (4)
+template <typename LhatFn>
+__device__ __forceinline__ void cluster_recover(cg::cluster_group& cl, const PcgArgs& g, int sol,
+                                                int k0, int nk, LhatFn lhat)
+{
+    const Work& w = g.w;
+    const int N = w.N, n = w.n, m = w.m, T = blockDim.x, tid = threadIdx.x;
+    const size_t Nn = (size_t)N * n;
+    float* lam = g.lambda + (size_t)sol * Nn;
+    const float* gLi = w.Linv + sol * w.sNnn;
+    for (int i = tid; i < nk * n; i += T) {
+        const int jl = i / n, a = i - jl * n, j = k0 + jl;
+        lam[(size_t)j * n + a] = strided_dot<16>(gLi + (size_t)j * n * n + a, n,
+                                                 [&](int b) { return lhat(jl, b); }, a, n);
+    }
+    cl.sync();
+    const float* Qi = w.Qinv + sol * w.sNnn;
+    const float* Ob = w.O + sol * w.sKnn;
+    const float* av = g.rhs.avec + sol * w.sNn;
+    auto at = [](const float* v) { return [v](int b) { return v[b]; }; };
+    for (int i = tid; i < nk * n; i += T) {
+        const int kl = i / n, a = i - kl * n, k = k0 + kl;
+        float x = av[(size_t)k * n + a];
+        x += strided_dot<16>(Qi + (size_t)k * n * n + a * n, 1, at(lam + (size_t)k * n), 0, n);
+        if (k < N - 1)
+            x += strided_dot<16>(Ob + (size_t)k * n * n + a, n, at(lam + (size_t)(k + 1) * n), 0,
+                                 n);
+        g.dX[(size_t)sol * Nn + (size_t)k * n + a] = x;
+    }
+    const int ku = min(nk, N - 1 - k0);  // this CTA's knots that have a control
+    const float* Vb = w.V + sol * w.sKnm;
+    const float* bv = g.rhs.bvec + sol * w.sKm;
+    for (int t = tid; t < ku * m; t += T) {
+        const int kl = t / m, c = t - kl * m, k = k0 + kl;
+        const float u = strided_dot<16>(Vb + (size_t)k * n * m + c, m,
+                                        at(lam + (size_t)(k + 1) * n), 0, n);
+        g.dU[(size_t)sol * (N - 1) * m + (size_t)k * m + c] = bv[(size_t)k * m + c] - u;
+    }
+}
+
+template <int H, int C>
+__device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
+{
+    extern __shared__ __align__(16) float sm[];
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank();
+    const int sol = blockIdx.x / C;
+    const Work& w = g.w;
+    const int N = w.N, n = w.n, T = blockDim.x, tid = threadIdx.x;
+    const int Nc = (N + C - 1) / C;
+    const int k0 = rank * Nc;          // first knot of this CTA
+    const int nk = min(Nc, N - k0);    // its knot count (>= 1)
+    const int EX = Nc * kWS;
+    const bool rule0 = g.rule == GATO_STOP_RESIDUAL;
+    const bool lsm = rule0 && g.l_smem;
+    const int KS = l_knot_stride(n);
+
+    float* XP = sm;
+    float* XR = XP + EX;
+    float* YC0 = XR + EX;
+    float* YC1 = YC0 + EX + 4;
+    const int zero_count = 4 * EX + 8;
+    float2* redA = reinterpret_cast<float2*>(sm + zero_count);
+    float2* redB = redA + 32;
+    float2* redC = redA + 64;
+    float2* redD = redA + 96;
+    float* DL = reinterpret_cast<float*>(redA + 160);
+    float* LP = DL + ((Nc + 3) & ~3);
+
+    for (int i = tid; i < zero_count; i += T) sm[i] = 0.f;
+    for (int jl = tid; jl < nk; jl += T) DL[jl] = w.dlow[sol * w.sN + k0 + jl];
+    const float* gL = w.L + sol * w.sNnn;
+    if (lsm) stage_l_rows<H>(LP, KS, gL + (size_t)k0 * n * n, nk, n);
+
+    // thread: local knot jl, row half rt; block j = k0 + jl when j >= 1
+    const int jl = tid >> 1, rt = tid & 1, half = rt;
+    const bool owner = jl < nk;
+    const int j = k0 + jl;
+    const bool has_tile = owner && j >= 1;
+    float* yc_base = rt ? YC1 : YC0;
+    WideTile<H> tile;
+    {
+        const float* blk = w.Nh + sol * w.sKnn + (size_t)(has_tile ? j - 1 : 0) * n * n;
+#pragma unroll
+        for (int a = 0; a < H; ++a)
+#pragma unroll
+            for (int b = 0; b < 2 * H; ++b) {
+                const int ra = rt * H + a;
+                tile.t[a][b] = (has_tile && ra < n && b < n) ? blk[ra * n + b] : 0.f;
+            }
+    }
+    // x_{j-1} and the slots for block j's column sums: local knot jl-1, or
+    // the last knot of CTA rank-1 for the CTA's first block
+    const bool edge = has_tile && jl == 0;
+    const int pj = edge ? (Nc - 1) * kWS : (has_tile ? (jl - 1) * kWS : 0);
+    const float* xpp = (edge ? cl.map_shared_rank(XP, rank - 1) : XP) + pj;
+    const float* xrp = (edge ? cl.map_shared_rank(XR, rank - 1) : XR) + pj;
+    float* yc = (edge ? cl.map_shared_rank(yc_base, rank - 1) : yc_base) + pj;
+
+    const int xo = (owner ? jl : 0) * kWS + half * kWH;
+    bool valid[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) valid[k] = owner && k < H && half * H + k < n;
+    const int gi0 = (owner ? j : 0) * n + half * H;
+    const float* ghat = g.rhs.ghat + sol * w.sNn;
+    const float* gam = g.rhs.gamma + sol * w.sNn;
+    const float dl = owner ? DL[jl] : 0.f;
+    float lam[8], r[8], p[8], y[8], rs[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) rs[k] = 0.f;
+    cl.sync();
+
+    // lambda_hat0 = L^T lambda0
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        lam[k] = 0.f;
+        if (valid[k] && g.lambda0) {
+            const int a = half * H + k;
+            const float* Lj = gL + (size_t)j * n * n;
+            const float* l0 = g.lambda0 + (size_t)sol * N * n + (size_t)j * n;
+            float x = 0.f;
+            for (int b = a; b < n; ++b) x += Lj[b * n + a] * l0[b];
+            lam[k] = x;
+        }
+    }
+    if (owner) wstore8(XP + xo, lam);
+    cl.sync();
+    if (has_tile) wide_matvec<H>(tile, xpp, lam, rs, yc);
+    cl.sync();
+    float rr = 0.f, gg = 0.f;
+    if (owner) wide_y(rs, YC0, YC1, xo, y);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        r[k] = 0.f;
+        if (valid[k]) {
+            const int i = gi0 + k;
+            r[k] = ghat[i] - lam[k] - y[k];
+            rr += r[k] * r[k];
+            gg += rule0 ? gam[i] * gam[i] : ghat[i] * ghat[i];
+        }
+    }
+    if (owner) wstore8(XR + xo, r);
+    post2(rr, gg, redB);
+    cl.sync();
+    float q = has_tile ? wide_matvec<H>(tile, xrp, r, rs, yc) : 0.f;
+    float lsq = 0.f;
+    if (rule0 && owner) lsq = lnorm_half<H>(LP, KS, gL + (size_t)k0 * n * n, lsm, XR, jl, half, n,
+                                            valid);
+    post2(q, lsq, redC);
+    cl.sync();
+    float2 sB = cluster_collect2<C>(cl, redB), sC = cluster_collect2<C>(cl, redC);
+    float eta = sB.x - 2.f * sC.x;
+    const float ref = g.rule == GATO_STOP_PRECOND ? eta : sB.y;
+    const float thr = g.eps * g.eps * ref;
+    float stopq = g.rule == GATO_STOP_RESIDUAL ? sC.y : (g.rule == GATO_STOP_SCALED ? sB.x : eta);
+    bool done = stopq <= thr;
+    bool nonfinite = !isfinite(eta) || !isfinite(stopq);
+    if (owner) wide_y(rs, YC0, YC1, xo, y);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) p[k] = valid[k] ? r[k] - y[k] : 0.f;
+    if (owner) wstore8(XP + xo, p);
+    bool exact_next;
+    {
+        float lb = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) lb += dl * r[k] * r[k];
+        post2(lb, 0.f, redD);
+        cl.sync();
+        exact_next = rule0 && cluster_collect2<C>(cl, redD).x <= 1.25f * thr;
+    }
+    cl.sync();
+
+    int it = 0;
+    while (!done && !nonfinite && it < g.max_iters) {
+        ++it;
+        // A: Nhat p, p^T Nhat p and p^T p partials
+        q = has_tile ? wide_matvec<H>(tile, xpp, p, rs, yc) : 0.f;
+        float pp = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pp = fmaf(p[k], p[k], pp);
+        post2(q, pp, redA);
+        cl.sync();
+        // B: alpha; lambda and r updates
+        const float2 sA = cluster_collect2<C>(cl, redA);
+        const float pv = sA.y + 2.f * sA.x;
+        const float alpha = __fdividef(eta, pv);
+        if (owner) wide_y(rs, YC0, YC1, xo, y);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float v = p[k] + y[k];
+            lam[k] = fmaf(alpha, p[k], lam[k]);
+            r[k] = valid[k] ? fmaf(-alpha, v, r[k]) : 0.f;
+        }
+        if (owner) wstore8(XR + xo, r);
+        cl.sync();
+        // C: Nhat r; r^T Nhat r, r^T r, the bound and (gated) ||L r_hat||^2
+        q = has_tile ? wide_matvec<H>(tile, xrp, r, rs, yc) : 0.f;
+        rr = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) rr = fmaf(r[k], r[k], rr);
+        float lsq = 0.f;
+        const bool exact = exact_next;
+        if (exact && owner)
+            lsq = lnorm_half<H>(LP, KS, gL + (size_t)k0 * n * n, lsm, XR, jl, half, n, valid);
+        post2(q, rr, redB);
+        post2(dl * rr, lsq, redC);
+        cl.sync();
+        // D: eta', convergence, p = z + beta p
+        sB = cluster_collect2<C>(cl, redB);
+        sC = cluster_collect2<C>(cl, redC);
+        const float eta_new = sB.y - 2.f * sB.x;
+        float lsq_all = sC.y;
+        bool have_exact = exact;
+        if (rule0 && !exact && sC.x * 0.999f <= thr) {
+            lsq = owner ? lnorm_half<H>(LP, KS, gL + (size_t)k0 * n * n, lsm, XR, jl, half, n,
+                                        valid)
+                        : 0.f;
+            post2(lsq, 0.f, redD);
+            cl.sync();
+            lsq_all = cluster_collect2<C>(cl, redD).x;
+            have_exact = true;
+        }
+        stopq = g.rule == GATO_STOP_RESIDUAL ? lsq_all
+                                             : (g.rule == GATO_STOP_SCALED ? sB.y : eta_new);
+        if (!isfinite(eta_new + pv + stopq + sC.x)) {
+            nonfinite = true;
+            break;
+        }
+        done = (!rule0 || have_exact) && stopq <= thr;
+        if (done) break;
+        exact_next = rule0 && sC.x <= 1.25f * thr;
+        const float beta = __fdividef(eta_new, eta);
+        if (owner) wide_y(rs, YC0, YC1, xo, y);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) p[k] = valid[k] ? fmaf(beta, p[k], r[k] - y[k]) : 0.f;
+        if (owner) wstore8(XP + xo, p);
+        eta = eta_new;
+        cl.sync();
+    }
+    cl.sync();
+    if (owner) wstore8(XP + xo, lam);
+    cl.sync();
+    cluster_recover(cl, g, sol, k0, nk,
+                    [&](int kl, int b) { return XP[kl * kWS + wphys(pcol<H>(b))]; });
+    if (rank == 0) finish(g, sol, it, done, nonfinite);
+}
+
+template <int H, int C>
+__global__ void __launch_bounds__(256, 1) k_pcg_cluster(PcgArgs g)
+{
+    pcg_cluster_solve<H, C>(g);
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -1057,9 +1342,9 @@ size_t generic_smem_bytes(const Work& w, int nh_smem, int l_smem)
     return f * sizeof(float);
 }
 
-size_t wide_smem_bytes(const Work& w, int l_smem)
+size_t wide_smem_bytes(const Work& w, int l_smem, int knots = 0)
 {
-    const size_t n = w.n, N = w.N;
+    const size_t n = w.n, N = knots ? knots : w.N;
     size_t f = 4 * kWS * N + 8;  // XP, XR, YC0/1
     f += 5 * 32 * 2;            // five float2[32] reduction buffers
     f += round4(N);             // DL
@@ -1111,6 +1396,38 @@ cudaError_t launch_persistent(K kernel, const PcgArgs& a, int T, size_t smem, in
     return cudaGetLastError();
 }
 
+// one solve per cluster of C CTAs (grid M C); cudaErrorInvalidConfiguration
+// when no such cluster fits on the device
+template <typename K>
+cudaError_t launch_cluster(K kernel, const PcgArgs& a, int C, int T, size_t smem,
+                           cudaStream_t st)
+{
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.w.M * C), 1, 1);
+    cfg.blockDim = dim3((unsigned)T, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+    if (e != cudaSuccess || clusters < 1) {
+        cudaGetLastError();
+        return cudaErrorInvalidConfiguration;
+    }
+    e = cudaLaunchKernelEx(&cfg, kernel, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const float* lambda0,
@@ -1159,6 +1476,40 @@ cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const f
                 case 8: return launch_persistent(k_pcg_wide<8>, a, Tw, smem, h->num_sms, st);
                 default: break;
             }
+        }
+    }
+
+    // cluster kernel: 128 < N <= 512, the solve split over 2 or 4 CTAs
+    if ((kind == GATO_PCG_AUTO || kind == GATO_PCG_WIDE) && tiled_n && w.N > 128 &&
+        w.N <= 512) {
+        const int C = w.N <= 256 ? 2 : 4;
+        const int Nc = (w.N + C - 1) / C;
+        int Tc = ((2 * Nc + 31) / 32) * 32;
+        if (Tc < 64) Tc = 64;
+        a.nh_smem = 0;
+        a.l_smem = want_l;
+        size_t smem = wide_smem_bytes(w, a.l_smem, Nc);
+        if (smem > limit) {
+            a.l_smem = 0;
+            smem = wide_smem_bytes(w, 0, Nc);
+        }
+        if (smem <= limit) {
+            cudaError_t e = cudaErrorInvalidConfiguration;
+            switch (H * 8 + C) {
+#define GATO_CLUSTER_CASE(HH, CC)                                                    \
+                case HH * 8 + CC:                                                    \
+                    e = launch_cluster(k_pcg_cluster<HH, CC>, a, CC, Tc, smem, st); \
+                    break;
+                GATO_CLUSTER_CASE(4, 2) GATO_CLUSTER_CASE(4, 4)
+                GATO_CLUSTER_CASE(5, 2) GATO_CLUSTER_CASE(5, 4)
+                GATO_CLUSTER_CASE(6, 2) GATO_CLUSTER_CASE(6, 4)
+                GATO_CLUSTER_CASE(7, 2) GATO_CLUSTER_CASE(7, 4)
+                GATO_CLUSTER_CASE(8, 2) GATO_CLUSTER_CASE(8, 4)
+#undef GATO_CLUSTER_CASE
+                default: break;
+            }
+            // a cluster that cannot be placed falls through to the generic kernel
+            if (e != cudaErrorInvalidConfiguration) return e;
         }
     }
 
