@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_factor_rows(Work w, uint32_t* s
             load_blk(er, b.be, j + s, right, n, li, false);
             __syncwarp();
             publish(e, S1, li);
-            const bool okj = rows_cholesky(d, li, n);
+            const bool okj = rows_cholesky(d, li, n, S0);
             ok = ok && (okj || !act);
             rows_lower_inverse(d, x, li, n, S0);  // x: row li of F (ends with __syncwarp)
             if (act) store_row(x, b.D(j), n, n, li);
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_factor_rows(Work w, uint32_t* s
         const bool act = half == 0;
         float d[NP], x[NP];
         load_blk(d, b.bd, 0, act, n, li, true);
-        const bool ok0 = rows_cholesky(d, li, n);
+        const bool ok0 = rows_cholesky(d, li, n, S0);
         ok = ok && (ok0 || !act);
         rows_lower_inverse(d, x, li, n, S0);
         if (act) store_row(x, b.D(0), n, n, li);

@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(256) k_rows_knot(Work w, const float* __restri
     float a[NP], x[NP], c[NP];
     // Q_k^-1
     load_row(a, Q + ((size_t)sol * N + k) * n * n, n, n, li, true);
-    bool ok = rows_cholesky(a, li, n);
+    bool ok = rows_cholesky(a, li, n, h.S0);
     rows_lower_inverse(a, x, li, n, h.S0);
     rows_gram_lower(h.S0, c, li, n);  // row li of Q_k^-1
     if (h.active) store_row(c, w.Qinv + sol * w.sNnn + (size_t)k * n * n, n, n, li);
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(256) k_rows_knot(Work w, const float* __restri
 #pragma unroll
         for (int j = 0; j < NP; ++j) a[j] = (j == li) ? 1.f : 0.f;
     }
-    const bool okr = rows_cholesky(a, li, m);
+    const bool okr = rows_cholesky(a, li, m, h.S0);
     if (has_u) ok = ok && okr;
     __syncwarp();
     rows_lower_inverse(a, x, li, m, h.S0);
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(256) k_rows_diag(Work w, uint32_t* status)
 #pragma unroll
         for (int c = 0; c < NP; ++c) d[c] = (c == li) ? 1.f : 0.f;
     }
-    const bool ok = rows_cholesky(d, li, n);
+    const bool ok = rows_cholesky(d, li, n, h.S0);
     if (h.active) store_row(d, w.L + off, n, n, li);
     float x[NP];
     rows_lower_inverse(d, x, li, n, h.S0);

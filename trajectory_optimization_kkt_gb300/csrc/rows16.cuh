@@ -80,8 +80,10 @@ __device__ __forceinline__ void fetch(float (&b)[NP], const float* S, int k)
 
 // In-register Cholesky of diag(M, I) (M of order n): a becomes row li of L,
 // strict upper part zeroed.  A pivot <= 0 or not finite is flagged (false)
-// and replaced by 1.
-__device__ inline bool rows_cholesky(float (&a)[NP], int li, int n)
+// and replaced by 1.  Column k of L reaches the other lanes through the
+// 32-float scratch col (two alternating 16-float buffers): one store per lane
+// and four broadcast 128-bit loads per step.
+__device__ inline bool rows_cholesky(float (&a)[NP], int li, int n, float* col)
 {
     bool ok = true;
 #pragma unroll
@@ -93,13 +95,14 @@ __device__ inline bool rows_cholesky(float (&a)[NP], int li, int n)
             const float s = bad ? 1.f : sqrtf(d);
             const float inv = 1.f / s;
             a[k] = (li == k) ? s : (li > k ? a[k] * inv : a[k]);
+            float* ck = col + (k & 1) * NP;
+            ck[li] = a[k];
+            __syncwarp();
+            float lk[NP];
+            fetch(lk, ck, 0);
 #pragma unroll
-            for (int j = k + 1; j < NP; ++j) {
-                if (j < n) {
-                    const float ljk = shfl16(a[k], j);
-                    if (li >= j) a[j] -= a[k] * ljk;
-                }
-            }
+            for (int j = k + 1; j < NP; ++j)
+                if (j < n && li >= j) a[j] -= a[k] * lk[j];
         }
     }
 #pragma unroll
@@ -148,7 +151,7 @@ __device__ __forceinline__ void rows_gram_lower(const float* S, float (&c)[NP], 
         if (k < n && k >= li) {
             float xk[NP];
             fetch(xk, S, k);
-            const float xki = pick(xk, li);
+            const float xki = S[k * NP + li];
 #pragma unroll
             for (int j = 0; j < NP; ++j) c[j] += xki * xk[j];
         }
@@ -198,10 +201,9 @@ __device__ __forceinline__ void rows_atb(const float* SA, const float* SB, int k
 #pragma unroll
     for (int k = 0; k < NP; ++k) {
         if (k < kk) {
-            float ak[NP], bk[NP];
-            fetch(ak, SA, k);
+            float bk[NP];
             fetch(bk, SB, k);
-            const float a = s * pick(ak, li);
+            const float a = s * SA[k * NP + li];
 #pragma unroll
             for (int j = 0; j < NP; ++j) c[j] += a * bk[j];
         }
