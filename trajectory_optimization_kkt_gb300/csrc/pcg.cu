@@ -101,16 +101,21 @@ __device__ __forceinline__ void post2(float a, float b, float2* buf)
 __device__ __forceinline__ float2 collect2(const float2* buf)
 {
     // the low half-warp sums the .x fields of the (at most 16) warp slots,
-    // the high half the .y fields; two broadcasts give every lane both totals
+    // the high half the .y fields; the full butterfly leaves every lane of a
+    // half with that half's total (each level adds the same pair in both
+    // lanes, so all lanes agree bit for bit), and one exchange across the
+    // halves gives every lane both totals
     const int lane = lane_id(), q = lane & 15;
+    const bool hi = lane & 16;
     float v = 0.f;
     if (q < (int)(blockDim.x >> 5)) {
         const float2 t = buf[q];
-        v = (lane & 16) ? t.y : t.x;
+        v = hi ? t.y : t.x;
     }
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return make_float2(__shfl_sync(0xffffffffu, v, 0), __shfl_sync(0xffffffffu, v, 16));
+    const float other = __shfl_xor_sync(0xffffffffu, v, 16);
+    return hi ? make_float2(other, v) : make_float2(v, other);
 }
 
 __device__ __forceinline__ void finish(const PcgArgs& g, int sol, int it, bool done,
