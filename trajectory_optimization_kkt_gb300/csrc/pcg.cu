@@ -798,11 +798,10 @@ __device__ __forceinline__ void wide_y(const float (&rs)[8], const float* YC0, c
     for (int k = 0; k < 8; ++k) y[k] = rs[k] + c0[k] + c1[k];
 }
 
-// sum over the owned rows a = half*H + k (k < H, valid) of (L_j r_hat_j)_a^2
+// sum over the owned rows a = half*H + k < n (k < H) of (L_j r_hat_j)_a^2
 template <int H>
 __device__ __forceinline__ float lnorm_half(const float* LP, int KS, const float* gL, bool lsm,
-                                            const float* XR, int j, int half, int n,
-                                            const bool (&valid)[8])
+                                            const float* XR, int j, int half, int n, int owner)
 {
     float s = 0.f;
     const float* xk = XR + j * kWS;
@@ -815,7 +814,7 @@ __device__ __forceinline__ float lnorm_half(const float* LP, int KS, const float
                                : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < H; ++k) {
-            if (!valid[k]) continue;
+            if (!owner || half * H + k >= n) continue;
             const float4* row =
                 reinterpret_cast<const float4*>(LP + j * KS + (half * H + k) * kLS);
             float t = dot4(row[0], x0, 0.f);
@@ -827,13 +826,20 @@ __device__ __forceinline__ float lnorm_half(const float* LP, int KS, const float
             s = fmaf(t, t, s);
         }
     } else {
+        // rows from global memory: the loads of a row are independent, the x
+        // values come from the knot's four float4 chunks
+        float xs[16];
+        wload16(xk, xs);
+        const float* Lj = gL + (size_t)j * n * n;
 #pragma unroll
         for (int k = 0; k < H; ++k) {
-            if (!valid[k]) continue;
             const int a = half * H + k;
-            const float* row = gL + (size_t)j * n * n + a * n;
+            if (!owner || a >= n) continue;
+            const float* row = Lj + a * n;
             float t = 0.f;
-            for (int b = 0; b <= a; ++b) t += row[b] * xk[wphys(pcol<H>(b))];
+#pragma unroll
+            for (int b = 0; b < 2 * H; ++b)
+                if (b <= a) t = fmaf(row[b], xs[pcol<H>(b)], t);
             s = fmaf(t, t, s);
         }
     }
@@ -897,9 +903,12 @@ __device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
     const float* ghat = g.rhs.ghat + sol * w.sNn;
     const float* gam = g.rhs.gamma + sol * w.sNn;
     const float dl = owner ? DL[jo] : 0.f;
+    // slots past n (and all slots of a thread that owns none) start at zero
+    // and stay exactly zero: the padded rows and columns of the tiles are
+    // zero, so the loop needs no masks
     float lam[8], r[8], p[8], y[8], rs[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) rs[k] = 0.f;
+    for (int k = 0; k < 8; ++k) rs[k] = y[k] = 0.f;
     __syncthreads();
 
     // lambda_hat0 = L^T lambda0
@@ -937,7 +946,7 @@ __device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
     __syncthreads();  // XR complete; the column sums of lambda are read
     float q = has_tile ? wide_matvec<H>(tile, XR + pj, r, rs, yc) : 0.f;
     float lsq = 0.f;
-    if (rule0) lsq = lnorm_half<H>(LP, KS, gL, lsm, XR, jo, half, n, valid);
+    if (rule0) lsq = lnorm_half<H>(LP, KS, gL, lsm, XR, jo, half, n, owner);
     post2(q, lsq, redC);
     __syncthreads();
     float2 sB = collect2(redB), sC = collect2(redC);
@@ -949,7 +958,7 @@ __device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
     bool nonfinite = !isfinite(eta) || !isfinite(stopq);
     if (owner) wide_y(rs, YC0, YC1, xo, y);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) p[k] = valid[k] ? r[k] - y[k] : 0.f;  // z = (I - Nhat) r
+    for (int k = 0; k < 8; ++k) p[k] = r[k] - y[k];  // z = (I - Nhat) r
     if (owner) wstore8(XP + xo, p);
     // the exact ||L r_hat|| is gated as in k_pcg_tile
     bool exact_next;
@@ -983,7 +992,7 @@ __device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
         for (int k = 0; k < 8; ++k) {
             const float v = p[k] + y[k];
             lam[k] = fmaf(alpha, p[k], lam[k]);
-            r[k] = valid[k] ? fmaf(-alpha, v, r[k]) : 0.f;
+            r[k] = fmaf(-alpha, v, r[k]);
         }
         if (owner) wstore8(XR + xo, r);
         __syncthreads();
@@ -995,7 +1004,7 @@ __device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
         for (int k = 0; k < 8; ++k) rr = fmaf(r[k], r[k], rr);
         float lsq = 0.f;
         const bool exact = exact_next;
-        if (exact) lsq = lnorm_half<H>(LP, KS, gL, lsm, XR, jo, half, n, valid);
+        if (exact) lsq = lnorm_half<H>(LP, KS, gL, lsm, XR, jo, half, n, owner);
         post2(q, rr, redB);
         post2(dl * rr, lsq, redC);
         __syncthreads();
@@ -1006,7 +1015,7 @@ __device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
         float lsq_all = sC.y;
         bool have_exact = exact;
         if (rule0 && !exact && sC.x * 0.999f <= thr) {
-            lsq = lnorm_half<H>(LP, KS, gL, lsm, XR, jo, half, n, valid);
+            lsq = lnorm_half<H>(LP, KS, gL, lsm, XR, jo, half, n, owner);
             float lv[1] = {lsq};
             block_sum<1>(lv, reinterpret_cast<float4*>(redD));
             lsq_all = lv[0];
@@ -1024,7 +1033,7 @@ __device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
         const float beta = __fdividef(eta_new, eta);
         if (owner) wide_y(rs, YC0, YC1, xo, y);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) p[k] = valid[k] ? fmaf(beta, p[k], r[k] - y[k]) : 0.f;
+        for (int k = 0; k < 8; ++k) p[k] = fmaf(beta, p[k], r[k] - y[k]);
         if (owner) wstore8(XP + xo, p);
         eta = eta_new;
         __syncthreads();
@@ -1186,9 +1195,11 @@ __device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
     const float* ghat = g.rhs.ghat + sol * w.sNn;
     const float* gam = g.rhs.gamma + sol * w.sNn;
     const float dl = owner ? DL[jl] : 0.f;
+    // slots past n (and all slots of a thread that owns none) start at zero
+    // and stay exactly zero, as in k_pcg_wide
     float lam[8], r[8], p[8], y[8], rs[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) rs[k] = 0.f;
+    for (int k = 0; k < 8; ++k) rs[k] = y[k] = 0.f;
     cl.sync();
 
     // lambda_hat0 = L^T lambda0
@@ -1226,7 +1237,7 @@ __device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
     float q = has_tile ? wide_matvec<H>(tile, xrp, r, rs, yc) : 0.f;
     float lsq = 0.f;
     if (rule0 && owner) lsq = lnorm_half<H>(LP, KS, gL + (size_t)k0 * n * n, lsm, XR, jl, half, n,
-                                            valid);
+                                            owner);
     post2(q, lsq, redC);
     cl.sync();
     float2 sB = cluster_collect2<C>(cl, redB), sC = cluster_collect2<C>(cl, redC);
@@ -1238,7 +1249,7 @@ __device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
     bool nonfinite = !isfinite(eta) || !isfinite(stopq);
     if (owner) wide_y(rs, YC0, YC1, xo, y);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) p[k] = valid[k] ? r[k] - y[k] : 0.f;
+    for (int k = 0; k < 8; ++k) p[k] = r[k] - y[k];
     if (owner) wstore8(XP + xo, p);
     bool exact_next;
     {
@@ -1270,7 +1281,7 @@ __device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
         for (int k = 0; k < 8; ++k) {
             const float v = p[k] + y[k];
             lam[k] = fmaf(alpha, p[k], lam[k]);
-            r[k] = valid[k] ? fmaf(-alpha, v, r[k]) : 0.f;
+            r[k] = fmaf(-alpha, v, r[k]);
         }
         if (owner) wstore8(XR + xo, r);
         cl.sync();
@@ -1282,7 +1293,7 @@ __device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
         float lsq = 0.f;
         const bool exact = exact_next;
         if (exact && owner)
-            lsq = lnorm_half<H>(LP, KS, gL + (size_t)k0 * n * n, lsm, XR, jl, half, n, valid);
+            lsq = lnorm_half<H>(LP, KS, gL + (size_t)k0 * n * n, lsm, XR, jl, half, n, owner);
         post2(q, rr, redB);
         post2(dl * rr, lsq, redC);
         cl.sync();
@@ -1294,7 +1305,7 @@ __device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
         bool have_exact = exact;
         if (rule0 && !exact && sC.x * 0.999f <= thr) {
             lsq = owner ? lnorm_half<H>(LP, KS, gL + (size_t)k0 * n * n, lsm, XR, jl, half, n,
-                                        valid)
+                                        owner)
                         : 0.f;
             post2(lsq, 0.f, redD);
             cl.sync();
@@ -1313,7 +1324,7 @@ __device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
         const float beta = __fdividef(eta_new, eta);
         if (owner) wide_y(rs, YC0, YC1, xo, y);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) p[k] = valid[k] ? fmaf(beta, p[k], r[k] - y[k]) : 0.f;
+        for (int k = 0; k < 8; ++k) p[k] = fmaf(beta, p[k], r[k] - y[k]);
         if (owner) wstore8(XP + xo, p);
         eta = eta_new;
         cl.sync();
