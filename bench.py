@@ -37,8 +37,8 @@ WORKLOAD_INDEX = 4  # M=256, N=128, n=14, m=7
 # solve launch at this workload, from an ncu capture; valid only for the
 # kernel source it was taken on (sha256 prefix of csrc/pcg.cu), null
 # otherwise.  Captured on 152 solves (one block per SM) and scaled
-# by the solves processed to the 256-solve launch (90.13 MB x 256 / 152).
-PCG_TRAFFIC = {"pcg_sha": "44a137b49a059c04", "bytes_per_launch": 151796467}
+# by the solves processed to the 256-solve launch (89.78 MB x 256 / 152).
+PCG_TRAFFIC = {"pcg_sha": "2a736ae016406569", "bytes_per_launch": 151210092}
 
 FP32_LANES_PER_SM = 128  # FFMA lanes per SM (4 sub-partitions x 32)
 
@@ -459,6 +459,13 @@ def run_gpu(args, world, rank, local):
     # the pages' streaming model: packed S and Phi^-1 read once per iteration
     bytes_it = 2 * (N * n * (n + 1) // 2 + (N - 1) * n * n) * 4
     stream_gbs = bytes_it * iters_per_step / (pcg_stage_us * 1e-6) / 1e9
+    # merit: the problem data and the step read once, A + 1 merits and the
+    # argmin written, per solve
+    K, m = N - 1, w.m
+    merit_bytes = 4 * M * (N * n * n + K * (m * m + n * n + n * m) + N * n + K * m + K * n + n
+                           + N * n + K * m + (w.n_alpha + 1) + 1)
+    merit_s = statistics.mean(merit_us) * 1e-6
+    merit_gbs = merit_bytes / merit_s / 1e9
     sha = _src_sha(os.path.join(_build.CSRC, "pcg.cu"))
     traffic = PCG_TRAFFIC["bytes_per_launch"] if PCG_TRAFFIC["pcg_sha"] == sha else None
 
@@ -511,6 +518,13 @@ def run_gpu(args, world, rank, local):
                                        f"{sm_mhz:.0f} MHz (max SM clock, {peak_kind})",
                          "flops_per_solve_iteration": flops_it,
                          "iterations_per_step": iters_per_step},
+            "merit_roofline": {"bound": "hbm", "achieved": merit_gbs, "peak": hbm_peak,
+                               "unit": "GB/s", "frac": merit_gbs / hbm_peak,
+                               "peak_kind": peak_kind, "bytes_per_launch": merit_bytes,
+                               "kernel": "k_merit_knots" if n <= 16 and m <= 16
+                                         else "k_merit_fused",
+                               "knot_candidates_per_s":
+                                   M * N * (w.n_alpha + 1) / merit_s},
             "hbm_stream_model": {"achieved": stream_gbs, "peak": hbm_peak, "unit": "GB/s",
                                  "frac": stream_gbs / hbm_peak, "peak_kind": peak_kind,
                                  "note": "S and Phi^-1 bytes per iteration as if streamed; "

@@ -106,8 +106,10 @@ extern "C" {
 #define GATO_FORM_SHARED 1         /* always the shared-memory kernels           */
 
 /* merit kernels (gato_params.merit_kernel) */
-#define GATO_MERIT_FUSED 0         /* one block per solve, knots streamed once,
-                                      candidates in factored form (default)       */
+#define GATO_MERIT_FUSED 0         /* knots read once, candidates in factored
+                                      form (default): a half-warp per knot and the
+                                      blocks of a solve summed in block order when
+                                      n, m <= 16, else one block per solve        */
 #define GATO_MERIT_PER_CANDIDATE 1 /* one block of merit_threads per (knot,
                                       candidate), full formula per candidate      */
 
@@ -171,7 +173,7 @@ void gato_default_sqp_params(gato_sqp_params* sp);
 
 /* Creates a solver for M solves of N knots, n states and m controls on the
  * current CUDA device and allocates its device workspace (cudaMalloc; about
- * 4 M (12 N n^2 + (N-1)(m^2 + n m) + 17 N n + 6 (N-1) m + 66 N + 36) bytes).  *h
+ * 4 M (12 N n^2 + (N-1)(m^2 + n m) + 17 N n + 6 (N-1) m + 66 N + 37) bytes).  *h
  * receives the handle, which the caller releases with gato_destroy.  Errors: INVALID_ARG (h NULL, M, N, n or
  * m < 1), UNSUPPORTED (n or m above the limits), NO_MEMORY, CUDA. */
 int gato_create(gato_handle** h, int M, int N, int n, int m);
@@ -332,7 +334,7 @@ int gato_sqp_linear(gato_handle* h, const gato_params* p, const gato_sqp_params*
  * n, m); the caller still provides every input and output.  The solver's
  * scratch is one static device array of GATO_NOALLOC_MAX_BYTES that every GPU
  * loading this library holds until the process exits; a problem needs about
- * 4 M (12 N n^2 + (N-1)(m^2 + n m) + 17 N n + 6 (N-1) m + 66 N + 36) bytes of it
+ * 4 M (12 N n^2 + (N-1)(m^2 + n m) + 17 N n + 6 (N-1) m + 66 N + 37) bytes of it
  * (each array rounded up to 64 floats), and larger problems are rejected
  * with GATO_ERR_UNSUPPORTED before
  * anything is launched (use gato_create for those).  The first call on each

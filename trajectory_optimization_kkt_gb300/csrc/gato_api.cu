@@ -64,6 +64,8 @@ size_t carve_workspace(Work& w, int M, int N, int n, int m, float* base)
     total += 2 * w.sK2 * (size_t)M;  // merit partials
     if (base) w.queue = (int*)(base + total);
     total += 64;                     // work counters
+    if (base) w.mcount = (int*)(base + total);
+    total += (size_t)M;              // merit: blocks arrived per solve
     return total * sizeof(float);
 }
 

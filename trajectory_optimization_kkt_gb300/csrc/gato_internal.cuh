@@ -91,6 +91,7 @@ struct Work {
     // line search partial sums
     float2* mpart; // [(A+1)][N] (cost, violation) per knot and candidate
     int* queue;    // work counters of the persistent kernels (not per solve)
+    int* mcount;   // [M] merit blocks arrived per solve (zeroed before each launch)
 };
 
 }  // namespace gato

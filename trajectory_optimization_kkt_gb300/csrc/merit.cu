@@ -21,6 +21,14 @@
 //                 + mu sum |e + alpha w| (+ mu sum |alpha x_0 - s0|), the
 //                 factored form of the same merit.  Knot sums in a fixed
 //                 order; the block reduction, argmin and acceptance follow.
+// k_merit_knots   (the fused merit for n, m <= 16) the same factored merit
+//                 with one half-warp per knot (lane = row) and sixteen knots
+//                 per block, grid (ceil(N/16), M): every knot's loads are in
+//                 flight at once.  Each block writes its sums (c1, c2 and the
+//                 candidates' violations) to scratch; the block of a solve
+//                 that arrives last (fence + counter) adds the blocks in
+//                 block order, so the merits do not depend on scheduling, and
+//                 takes the argmin.
 // k_apply_step    X += alpha* dX, U += alpha* dU.
 #include "gato_internal.cuh"
 
@@ -282,6 +290,137 @@ __global__ void k_apply_step(Work w, float beta, const int32_t* best, const floa
         U[sol * Km + i] += alpha * dU[sol * Km + i];
 }
 
+// sum over the owned row li < rows of row li of M (rows x cols, row-major)
+// times v (cols <= 16, from shared memory); loads issued together
+__device__ __forceinline__ float row_dot16(const float* M, int cols, int li, const float* v)
+{
+    const float* row = M + li * cols;
+    float t = 0.f;
+#pragma unroll
+    for (int b = 0; b < 16; ++b)
+        if (b < cols) t = fmaf(row[b], v[b], t);
+    return t;
+}
+
+template <int NA>
+__global__ void __launch_bounds__(256) k_merit_knots(MeritArgs g, float mu, float* merit,
+                                                     int32_t* best, uint32_t* status,
+                                                     int* count)
+{
+    __shared__ __align__(16) float xs[16][48];  // per half-warp: x_k, u_k, x_{k+1}
+    __shared__ float wpart[8][NA + 2];          // per warp: c1, c2, violations
+    __shared__ float smer[NA];
+    __shared__ int s_last;
+    const int N = g.w.N, n = g.w.n, m = g.w.m, A1 = g.A1;
+    const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
+    const int h = tid >> 4, li = tid & 15;
+    const int sol = blockIdx.y, nb = gridDim.x;
+    const int k = blockIdx.x * 16 + h;
+    const bool act = k < N;
+    const bool has_u = act && k < N - 1;
+    const size_t K = (size_t)(N - 1);
+
+    float* xv = xs[h];
+    float* uv = xv + 16;
+    const float* dXs = g.dX + (size_t)sol * N * n;
+    xv[li] = act && li < n ? dXs[(size_t)k * n + li] : 0.f;
+    uv[li] = has_u && li < m ? g.dU[((size_t)sol * K + k) * m + li] : 0.f;
+    const float xnext = has_u && li < n ? dXs[(size_t)(k + 1) * n + li] : 0.f;
+    __syncwarp();
+
+    float alpha[NA];
+#pragma unroll
+    for (int i = 0; i < NA; ++i) alpha[i] = i < A1 ? candidate_alpha(i, g.beta) : 0.f;
+    float viol[NA];
+#pragma unroll
+    for (int i = 0; i < NA; ++i) viol[i] = 0.f;
+    float c1 = 0.f, c2 = 0.f;
+    if (act && li < n) {
+        const float xa = xv[li];
+        const float qx = row_dot16(g.Q + ((size_t)sol * N + k) * n * n, n, li, xv);
+        c2 = xa * qx;
+        c1 = g.q[((size_t)sol * N + k) * n + li] * xa;
+        if (has_u) {
+            float wa = row_dot16(g.A + ((size_t)sol * K + k) * n * n, n, li, xv);
+            wa += row_dot16(g.B + ((size_t)sol * K + k) * n * m, m, li, uv);
+            wa -= xnext;
+            const float ea = g.e[((size_t)sol * K + k) * n + li];
+#pragma unroll
+            for (int i = 0; i < NA; ++i)
+                if (i < A1) viol[i] = fabsf(ea + alpha[i] * wa);
+        }
+        if (k == 0) {
+            const float s0a = g.s0[(size_t)sol * n + li];
+#pragma unroll
+            for (int i = 0; i < NA; ++i)
+                if (i < A1) viol[i] += fabsf(alpha[i] * xa - s0a);
+        }
+    }
+    if (has_u && li < m) {
+        const float ua = uv[li];
+        const float ru = row_dot16(g.R + ((size_t)sol * K + k) * m * m, m, li, uv);
+        c2 = fmaf(ua, ru, c2);
+        c1 = fmaf(g.r[((size_t)sol * K + k) * m + li], ua, c1);
+    }
+    // warp sums (two knots), then the block's sums in warp order
+    c1 = warp_sum(c1);
+    c2 = warp_sum(c2);
+#pragma unroll
+    for (int i = 0; i < NA; ++i)
+        if (i < A1) viol[i] = warp_sum(viol[i]);
+    if (lane == 0) {
+        wpart[warp][0] = c1;
+        wpart[warp][1] = c2;
+#pragma unroll
+        for (int i = 0; i < NA; ++i)
+            if (i < A1) wpart[warp][2 + i] = viol[i];
+    }
+    __syncthreads();
+    float* part = reinterpret_cast<float*>(g.w.mpart) + (size_t)sol * 2 * g.w.sK2;
+    if (tid < A1 + 2) {
+        float t = 0.f;
+        for (int q = 0; q < 8; ++q) t += wpart[q][tid];
+        part[(size_t)blockIdx.x * (A1 + 2) + tid] = t;
+    }
+    // the last block of the solve to arrive adds all blocks in block order
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(count + sol, 1) == nb - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (tid < A1) {
+        float C1 = 0.f, C2 = 0.f, V = 0.f;
+        for (int b = 0; b < nb; ++b) {
+            const float* pb = part + (size_t)b * (A1 + 2);
+            C1 += __ldcg(pb);
+            C2 += __ldcg(pb + 1);
+            V += __ldcg(pb + 2 + tid);
+        }
+        const float a = candidate_alpha(tid, g.beta);
+        const float mv = 0.5f * a * a * C2 + a * C1 + mu * V;
+        smer[tid] = mv;
+        merit[(size_t)sol * A1 + tid] = mv;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int b = 0;
+        bool finite = isfinite(smer[0]);
+        for (int i = 1; i < A1; ++i) {
+            finite = finite && isfinite(smer[i]);
+            if (smer[i] < smer[1 + b]) b = i - 1;
+        }
+        uint32_t st = 0;
+        if (!finite) st |= GATO_STATUS_NONFINITE;
+        if (!(smer[1 + b] < smer[0])) {
+            b = -1;
+            st |= GATO_STATUS_LINESEARCH_FAILED;
+        }
+        best[sol] = b;
+        if (st) atomicOr(status + sol, st);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_merit(gato_handle* h, const gato_params* p, const float* Q,
@@ -297,16 +436,23 @@ cudaError_t launch_merit(gato_handle* h, const gato_params* p, const float* Q,
     a.dX = dX; a.dU = dU;
     a.A1 = p->n_alpha + 1;
     a.beta = p->beta;
+    if (p->merit_kernel == GATO_MERIT_FUSED && w.n <= 16 && w.m <= 16 && w.M <= 65535) {
+        cudaError_t e = cudaMemsetAsync(w.mcount, 0, sizeof(int) * (size_t)w.M, st);
+        if (e != cudaSuccess) return e;
+        const dim3 grid((unsigned)((w.N + 15) / 16), (unsigned)w.M);
+        if (a.A1 <= 9)
+            k_merit_knots<9><<<grid, 256, 0, st>>>(a, p->mu, merit, best, status, w.mcount);
+        else
+            k_merit_knots<kMaxA1><<<grid, 256, 0, st>>>(a, p->mu, merit, best, status, w.mcount);
+        return cudaGetLastError();
+    }
     if (p->merit_kernel == GATO_MERIT_FUSED) {
         int warps = (w.N + 3) / 4;  // about four knots per warp
         if (warps > 16) warps = 16;
         if (warps < 1) warps = 1;
         const size_t smem =
             ((size_t)warps * (2 * w.n + w.m) + (size_t)warps * (a.A1 + 2) + a.A1) * sizeof(float);
-        if (w.n <= 16 && w.m <= 16)
-            k_merit_fused<16><<<w.M, 32 * warps, smem, st>>>(a, p->mu, merit, best, status);
-        else
-            k_merit_fused<0><<<w.M, 32 * warps, smem, st>>>(a, p->mu, merit, best, status);
+        k_merit_fused<0><<<w.M, 32 * warps, smem, st>>>(a, p->mu, merit, best, status);
         return cudaGetLastError();
     }
     const size_t smem = (size_t)(5 * w.n + 2 * w.m) * sizeof(float);
