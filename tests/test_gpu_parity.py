@@ -10,9 +10,10 @@ Tolerances
   S, Phi, gamma  relative Frobenius error per solve <= 1e-5 (fp32 formation:
               about 20 n u with u = 2^-24 for the sizes here)
 The workloads use their own refinement setting (one correction solved to
-0.1, or 0.01 for workload 3): in fp32 the formation of S alone moves dz by
-4e-5 to 1.3e-4 (up to 3e-3 for workload 3), so the unrefined solve sits at
-the tolerance; refinement brings it near 1e-5.  A test below also checks
+0.25, 0.1 for workload 2, 0.01 for workload 3): in fp32 the formation of S
+alone moves dz by 4e-5 to 1.3e-4 (up to 3e-3 for workload 3), so the
+unrefined solve sits at the tolerance; refinement brings the worst solve of
+each workload to 1.5e-5 .. 3.2e-5.  A test below also checks
 the unrefined solve of workload 4.
 """
 import numpy as np

@@ -136,6 +136,61 @@ __global__ void k_form_off(Work w)
     warp_gemm<false, false>(n, n, n, s4, s3, w.Po + oj, -1.f, false);
 }
 
+// n, m <= 16: the same right-hand side with one half-warp per knot (lane =
+// row) and sixteen knots per block, every row product unrolled; the row
+// sums are those of k_form_rhs, in the same order.
+__global__ void __launch_bounds__(256) k_form_rhs_half(Work w, Rhs out, const float* __restrict__ q,
+                                                       const float* __restrict__ r,
+                                                       const float* __restrict__ e,
+                                                       const float* __restrict__ s0,
+                                                       size_t s0_stride)
+{
+    __shared__ __align__(16) float sgs[16][16];
+    const int n = w.n, m = w.m, N = w.N;
+    const int nn = n * n;
+    const int h = threadIdx.x >> 4, li = threadIdx.x & 15;
+    const long g = (long)blockIdx.x * 16 + h;
+    const bool act = g < (long)w.M * N;  // no early return: the warp syncs below
+    const long gi = act ? g : 0;
+    const int sol = (int)(gi / N), j = (int)(gi % N);
+    const size_t K = (size_t)(N - 1);
+    float* sg = sgs[h];
+    auto at = [](const float* v) { return [v](int b) { return v[b]; }; };
+    if (act && li < n) {
+        const float* Qi = w.Qinv + sol * w.sNnn + (size_t)j * nn;
+        const float* qj = q + ((size_t)sol * N + j) * n;
+        const float t = strided_dot<16>(Qi + li * n, 1, at(qj), 0, n);  // (Q_j^-1 q_j)_li
+        float gv;
+        if (j == 0) {
+            gv = s0[sol * s0_stride + li] + t;
+        } else {
+            const float* qp = q + ((size_t)sol * N + (j - 1)) * n;
+            const float* rp = r + ((size_t)sol * K + (j - 1)) * m;
+            const float* Op = w.O + sol * w.sKnn + (size_t)(j - 1) * nn;
+            const float* Vp = w.V + sol * w.sKnm + (size_t)(j - 1) * n * m;
+            gv = e[((size_t)sol * K + (j - 1)) * n + li];
+            gv += strided_dot<16>(Op + li * n, 1, at(qp), 0, n);
+            gv -= strided_dot<16>(Vp + li * m, 1, at(rp), 0, m);
+            gv += t;
+        }
+        sg[li] = gv;
+        out.gamma[sol * w.sNn + (size_t)j * n + li] = gv;
+        out.avec[sol * w.sNn + (size_t)j * n + li] = -t;
+    }
+    __syncwarp();
+    if (act && li < n) {
+        const float* Li = w.Linv + sol * w.sNnn + (size_t)j * nn;
+        out.ghat[sol * w.sNn + (size_t)j * n + li] =
+            strided_dot<16>(Li + li * n, 1, at(sg), 0, li + 1);
+    }
+    if (act && j < N - 1 && li < m) {
+        const float* Ri = w.Rinv + sol * w.sKmm + (size_t)j * m * m;
+        const float* rj = r + ((size_t)sol * K + j) * m;
+        out.bvec[sol * w.sKm + (size_t)j * m + li] =
+            -strided_dot<16>(Ri + li * m, 1, at(rj), 0, m);
+    }
+}
+
 // Right-hand side for (q, r, e, s0); s0 of solve i starts at s0 + i * s0_stride.
 // One warp per knot, lanes over rows; with NPX > 0 (n, m <= NPX) every row
 // product is unrolled and predicated so that its loads are in flight at once.
@@ -246,9 +301,12 @@ cudaError_t launch_form_rhs(gato_handle* h, int set, const float* q, const float
     const Work& w = h->w;
     const long knots = (long)w.M * w.N;
     const size_t per_warp = (size_t)w.n * sizeof(float);
-    if (w.n <= 16 && w.m <= 16)
-        return launch_warp_per_item(k_form_rhs<16>, knots, per_warp, h, st, w, w.rhs[set], q, r,
-                                    e, s0, s0_stride);
+    if (w.n <= 16 && w.m <= 16) {
+        if (knots <= 0) return cudaSuccess;
+        k_form_rhs_half<<<(unsigned)((knots + 15) / 16), 256, 0, st>>>(w, w.rhs[set], q, r, e, s0,
+                                                                       s0_stride);
+        return cudaGetLastError();
+    }
     return launch_warp_per_item(k_form_rhs<0>, knots, per_warp, h, st, w, w.rhs[set], q, r, e,
                                 s0, s0_stride);
 }

@@ -127,6 +127,78 @@ __global__ void k_kkt_residual(Work w, const float* __restrict__ Q, const float*
     }
 }
 
+// n, m <= 16: the same residual with one half-warp per knot (lane = row) and
+// sixteen knots per block; the knot's step and multiplier vectors are staged
+// in shared memory once, and each row's compensated chain adds its terms in
+// the order k_kkt_residual does (bit-identical results).
+__global__ void __launch_bounds__(256) k_kkt_residual_half(
+    Work w, const float* __restrict__ Q, const float* __restrict__ R, const float* __restrict__ q,
+    const float* __restrict__ r, const float* __restrict__ A, const float* __restrict__ B,
+    const float* __restrict__ e, const float* __restrict__ s0, const float* __restrict__ dX,
+    const float* __restrict__ dU, const float* __restrict__ lam)
+{
+    __shared__ __align__(16) float vs[16][80];  // x_k, x_{k+1}, u_k, lambda_k, lambda_{k+1}
+    const int n = w.n, m = w.m, N = w.N;
+    const int h = threadIdx.x >> 4, li = threadIdx.x & 15;
+    const long g = (long)blockIdx.x * 16 + h;
+    const bool act = g < (long)w.M * N;  // no early return: the warp syncs below
+    const long gi = act ? g : 0;
+    const int sol = (int)(gi / N), k = (int)(gi % N);
+    const bool has_u = act && k < N - 1;
+    const size_t K = (size_t)(N - 1);
+    float* x = vs[h];
+    float* xn = x + 16;
+    float* u = x + 32;
+    float* l = x + 48;
+    float* l1 = x + 64;
+    const float* dXk = dX + ((size_t)sol * N + k) * n;
+    const float* lk = lam + ((size_t)sol * N + k) * n;
+    x[li] = act && li < n ? dXk[li] : 0.f;
+    xn[li] = has_u && li < n ? dXk[n + li] : 0.f;
+    l[li] = act && li < n ? lk[li] : 0.f;
+    l1[li] = has_u && li < n ? lk[n + li] : 0.f;
+    u[li] = has_u && li < m ? dU[((size_t)sol * K + k) * m + li] : 0.f;
+    __syncwarp();
+    if (act && li < n) {
+        const float* Qk = Q + ((size_t)sol * N + k) * n * n;
+        Acc2 aq;
+        aq.add(q[((size_t)sol * N + k) * n + li]);
+        aq.add(-l[li]);
+        if (has_u) {
+            const float* Ak = A + ((size_t)sol * K + k) * n * n;
+            const float* Bk = B + ((size_t)sol * K + k) * n * m;
+            Acc2 ae;
+            ae.add(e[((size_t)sol * K + k) * n + li]);
+            ae.add(-xn[li]);
+            for (int b = 0; b < n; ++b) {  // the two rows' chains side by side
+                aq.add_prod(Qk[li * n + b], x[b]);
+                ae.add_prod(Ak[li * n + b], x[b]);
+            }
+            for (int b = 0; b < n; ++b) aq.add_prod(Ak[b * n + li], l1[b]);
+            for (int c = 0; c < m; ++c) ae.add_prod(Bk[li * m + c], u[c]);
+            w.e2[((size_t)sol * K + k) * n + li] = ae.value();
+        } else {
+            for (int b = 0; b < n; ++b) aq.add_prod(Qk[li * n + b], x[b]);
+        }
+        w.q2[((size_t)sol * N + k) * n + li] = aq.value();
+        if (k == 0) {
+            Acc2 a0;
+            a0.add(s0[(size_t)sol * n + li]);
+            a0.add(-x[li]);
+            w.s02[(size_t)sol * n + li] = a0.value();
+        }
+    }
+    if (has_u && li < m) {
+        const float* Rk = R + ((size_t)sol * K + k) * m * m;
+        const float* Bk = B + ((size_t)sol * K + k) * n * m;
+        Acc2 ar;
+        ar.add(r[((size_t)sol * K + k) * m + li]);
+        for (int c = 0; c < m; ++c) ar.add_prod(Rk[li * m + c], u[c]);
+        for (int b = 0; b < n; ++b) ar.add_prod(Bk[b * m + li], l1[b]);
+        w.r2[((size_t)sol * K + k) * m + li] = ar.value();
+    }
+}
+
 // y += d over a dense array (the correction was written densely, [M][N][n]
 // and [M][N-1][m], by the linear solve), grid-stride
 __global__ void k_accumulate(float* lam, const float* dlam, float* dX, const float* ddX,
@@ -151,6 +223,12 @@ cudaError_t launch_kkt_residual(gato_handle* h, const float* Q, const float* R,
 {
     const Work& w = h->w;
     const long knots = (long)w.M * w.N;
+    if (w.n <= 16 && w.m <= 16) {
+        if (knots <= 0) return cudaSuccess;
+        k_kkt_residual_half<<<(unsigned)((knots + 15) / 16), 256, 0, st>>>(w, Q, R, q, r, A, B, e,
+                                                                           s0, dX, dU, lambda);
+        return cudaGetLastError();
+    }
     const int wpb = 4;
     // the compensated chains are the latency here, not the loads: the
     // runtime-bounded loops (fewer registers, more warps) are the faster form

@@ -92,11 +92,13 @@ class Workload:
     n_alpha: int = 8
     beta: float = 2.0
     mu: float = 10.0
-    # one round of KKT iterative refinement (fp64 residual), the correction
-    # solved to refine_eps: fp32 alone leaves dz about 1e-4 from the exact
-    # solution on these workloads
+    # one round of KKT iterative refinement (compensated residual), the
+    # correction solved to refine_eps: fp32 alone leaves dz about 1e-4 from
+    # the exact solution on these workloads.  refine_eps is the loosest of
+    # 0.25 / 0.1 / 0.01 whose worst dz error over the workload's whole batch
+    # stays within a third of the 1e-4 parity tolerance
     refine_steps: int = 1
-    refine_eps: float = 0.1
+    refine_eps: float = 0.25
 
     def with_batch(self, M: int, N: int | None = None) -> "Workload":
         return dataclasses.replace(self, M=M, N=self.N if N is None else N)
@@ -104,13 +106,14 @@ class Workload:
 
 # Iteration caps: workloads 0 and 2 state theirs (200, 500).  The others state
 # only eps = 1e-6; their cap is set high enough for fp32 PCG to reach it.
-# Workload 3 (diagonal scaling over four decades) refines its correction to
-# 1e-2 instead of 1e-1.
+# Correction tolerances by the rule above: 0.25 leaves workload 2 (A = I +
+# 0.05 N(0,1)) at 4.3e-5, so it refines to 1e-1; workload 3 (diagonal
+# scaling over four decades) to 1e-2.
 WORKLOADS = [
     Workload(0, "M1_N16_n14_m7", 1, 16, 14, 7, pcg_max_iters=200),
     Workload(1, "M16_N32_n12_m6", 16, 32, 12, 6, pcg_max_iters=1000),
     Workload(2, "M64_N64_n14_m7_A05_QN10", 64, 64, 14, 7, a_sigma=0.05,
-             terminal_scale=10.0, pcg_max_iters=500),
+             terminal_scale=10.0, pcg_max_iters=500, refine_eps=0.1),
     Workload(3, "M128_N16_n36_m12_logscaled", 128, 16, 36, 12, b_sigma=0.05,
              log_scale=True, pcg_max_iters=4000, refine_eps=0.01),
     Workload(4, "M256_N128_n14_m7", 256, 128, 14, 7, pcg_max_iters=1000),
