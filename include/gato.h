@@ -350,6 +350,38 @@ int gato_solve_kkt_noalloc(const gato_params* p, int M, int N, int n, int m, con
                            float* dU, float* lambda, int32_t* iters, float* merit,
                            int32_t* best, uint32_t* status, void* stream);
 
+/* Largest number of parts gato_solve_kkt_host splits a batch into. */
+#define GATO_HOST_MAX_CHUNKS 8
+
+/* gato_solve_kkt on HOST buffers: every input and output pointer (same
+ * shapes and layouts as gato_solve_kkt) is host memory.  The paper has no
+ * counterpart; it serves callers whose batch lives in host memory.  The call
+ * splits the batch into parts of consecutive solves (gato_set_host_chunks)
+ * and runs each part on an internal stream: copy its inputs to the device,
+ * solve it as gato_solve_kkt does, copy its outputs back.  The copies of one
+ * part overlap the solves of the others.  Each part's arithmetic is that of
+ * gato_solve_kkt on the same solves, so the outputs are identical.
+ * status[M] is in/out here too: it is copied in with the inputs, the bits
+ * are OR-ed into it, and it is copied back.  Host buffers should be pinned
+ * (cudaHostAlloc or cudaHostRegister); with pageable memory the copies are
+ * staged by the driver and do not overlap.  The work is ordered after the
+ * work already on `stream`, and `stream` waits for all of it: synchronise
+ * `stream` before reading the outputs or reusing the inputs.  The first call
+ * allocates device staging buffers for all M solves, one internal stream and
+ * one sub-batch workspace per part (about the size of the handle's own
+ * workspace in total); later calls with the same part count reuse them.  Stage
+ * timing is not recorded.  Errors: INVALID_ARG, NO_MEMORY, CUDA. */
+int gato_solve_kkt_host(gato_handle* h, const gato_params* p, const float* Q, const float* R,
+                        const float* q, const float* r, const float* A, const float* B,
+                        const float* e, const float* s0, float* dX, float* dU, float* lambda,
+                        int32_t* iters, float* merit, int32_t* best, uint32_t* status,
+                        void* stream);
+
+/* Number of parts gato_solve_kkt_host splits the batch into: 1 ..
+ * GATO_HOST_MAX_CHUNKS (capped at M), or 0 for the automatic choice (the
+ * default).  Errors: INVALID_ARG. */
+int gato_set_host_chunks(gato_handle* h, int chunks);
+
 #ifdef __cplusplus
 }
 #endif

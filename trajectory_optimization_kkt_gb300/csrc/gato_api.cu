@@ -351,6 +351,7 @@ int gato_create(gato_handle** out, int M, int N, int n, int m)
 void gato_destroy(gato_handle* h)
 {
     if (!h) return;
+    gato::host_pipe_free(h);
     if (h->sqp_exec) cudaGraphExecDestroy(h->sqp_exec);
     if (h->capture_stream) cudaStreamDestroy(h->capture_stream);
     for (int i = 0; i < 5; ++i) cudaEventDestroy(h->ev[i]);

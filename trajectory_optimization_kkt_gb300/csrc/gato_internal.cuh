@@ -116,7 +116,15 @@ struct gato_handle {
     cudaStream_t capture_stream;
     cudaGraphExec_t sqp_exec;
     unsigned char sqp_key[512];
+    // gato_solve_kkt_host: requested part count (0 = automatic) and the
+    // staging buffers, streams and sub-batch handles of the current one
+    int host_chunks;
+    struct gato_host_pipe* pipe;
 };
+
+namespace gato {
+void host_pipe_free(gato_handle* h);  // releases h->pipe (gato_host.cu)
+}
 
 namespace gato {
 

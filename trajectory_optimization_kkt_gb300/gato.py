@@ -28,6 +28,7 @@ GATO_PCG_AUTO = 0
 GATO_PCG_GENERIC = 1
 GATO_PCG_WIDE = 2
 GATO_PCG_TILE = 3
+GATO_HOST_MAX_CHUNKS = 8
 
 GATO_LINSYS_AUTO = 0
 GATO_LINSYS_PCG = 1
@@ -116,6 +117,8 @@ def load(path: Optional[str] = None):
     lib.gato_bdsv_solve.argtypes = [vp, P] + [vp] * 5 + [vp]
     lib.gato_linesearch.argtypes = [vp, P] + [vp] * 8 + [vp] * 5 + [vp]
     lib.gato_solve_kkt.argtypes = [vp, P] + [vp] * 8 + [vp] * 7 + [vp]
+    lib.gato_solve_kkt_host.argtypes = [vp, P] + [vp] * 8 + [vp] * 7 + [vp]
+    lib.gato_set_host_chunks.argtypes = [vp, ip]
     lib.gato_apply_step.argtypes = [vp, P] + [vp] * 5 + [vp]
     lib.gato_solve_kkt_noalloc.argtypes = [P, ip, ip, ip, ip] + [vp] * 8 + [vp] * 7 + [vp]
     for fn in ("gato_create", "gato_set_timing", "gato_set_pcg_kernel", "gato_set_form_kernel",
@@ -156,6 +159,22 @@ def _ptr(t, dtype=None, what="tensor"):
     import torch
     if not t.is_cuda:
         raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    want = dtype or torch.float32
+    if t.dtype != want:
+        raise ValueError(f"{what} must be {want}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_ptr(t, dtype=None, what="tensor"):
+    """Host pointer of a contiguous CPU tensor (None -> NULL); pin it for
+    copies that overlap the solve."""
+    if t is None:
+        return None
+    import torch
+    if t.is_cuda:
+        raise ValueError(f"{what} must be a CPU tensor")
     if not t.is_contiguous():
         raise ValueError(f"{what} must be contiguous")
     want = dtype or torch.float32
@@ -265,6 +284,20 @@ class Solver:
             _ptr(iters, torch.int32, "iters"), _ptr(merit), _ptr(best, torch.int32, "best"),
             _ptr(status, torch.int32, "status"), _stream(stream)))
 
+    def set_host_chunks(self, chunks: int):
+        _check("gato_set_host_chunks", self.lib.gato_set_host_chunks(self.h, chunks))
+
+    def solve_kkt_host(self, params, prob, dX, dU, lam, iters, merit, best, status,
+                       stream=None):
+        """gato_solve_kkt_host: every array is a (preferably pinned) CPU
+        tensor; synchronise the stream before reading the outputs."""
+        import torch
+        _check("gato_solve_kkt_host", self.lib.gato_solve_kkt_host(
+            self.h, ctypes.byref(params), *[_host_ptr(prob.get(k), what=k) for k in _LQ],
+            _host_ptr(dX), _host_ptr(dU), _host_ptr(lam), _host_ptr(iters, torch.int32, "iters"),
+            _host_ptr(merit), _host_ptr(best, torch.int32, "best"),
+            _host_ptr(status, torch.int32, "status"), _stream(stream)))
+
     def sqp_linear(self, params, sqp_params, model, X, U, lam, rho, merit_hist, status,
                    iters_hist=None, stream=None):
         """gato_sqp_linear: model holds Q, R, q, r, A, B, c, xs (CUDA tensors);
@@ -296,6 +329,24 @@ class Solver:
                     merit=torch.empty(M, n_alpha + 1, **f),
                     best=torch.empty(M, device=dev, dtype=torch.int32),
                     status=torch.zeros(M, device=dev, dtype=torch.int32))
+
+    def host_outputs(self, n_alpha: int = 8):
+        """Pinned CPU output tensors for solve_kkt_host (status zeroed)."""
+        import torch
+        M, N, n, m = self.M, self.N, self.n, self.m
+        f = dict(dtype=torch.float32, pin_memory=True)
+        i = dict(dtype=torch.int32, pin_memory=True)
+        return dict(dX=torch.empty(M, N, n, **f), dU=torch.empty(M, max(N - 1, 0), m, **f),
+                    lam=torch.empty(M, N, n, **f), iters=torch.zeros(M, **i),
+                    merit=torch.empty(M, n_alpha + 1, **f), best=torch.empty(M, **i),
+                    status=torch.zeros(M, **i))
+
+
+def to_host(prob):
+    """numpy workload dict -> contiguous pinned float32 CPU tensors."""
+    import torch
+    return {k: torch.as_tensor(v, dtype=torch.float32).contiguous().pin_memory()
+            for k, v in prob.items()}
 
 
 def solve_kkt_noalloc(params, prob, dX, dU, lam, iters, merit, best, status, stream=None):
