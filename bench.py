@@ -207,15 +207,16 @@ def _cpu_baseline(w, budget_s=12.0):
 
 
 def _time_solver(torch, s, p, d, out, steps, flush, stream):
-    """Device time of `steps` gato_solve_kkt calls (L2 flushed before each):
-    (ms per step, mean stage microseconds, PCG iterations per step)."""
+    """Device time of `steps` gato_solve_kkt calls (L2 flushed before each),
+    with the library's default parts; the stages from a one-part pass of the
+    same steps: (ms per step, mean stage microseconds, PCG iterations per
+    step, solves with a status bit)."""
     def step():
         out["status"].zero_()
         s.solve_kkt(p, d, out["dX"], out["dU"], out["lam"], out["iters"], out["merit"],
                     out["best"], out["status"], stream)
     for _ in range(3):
         step()
-    s.set_timing(True)
     ms, stages, iters = [], {"form": [], "linsys": [], "refine": [], "merit": []}, 0
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for k in range(steps):
@@ -223,14 +224,21 @@ def _time_solver(torch, s, p, d, out, steps, flush, stream):
         a.record(stream)
         step()
         b.record(stream)
-        st = s.get_stats()
+        b.synchronize()
         ms.append(a.elapsed_time(b))
+        iters += int(out["iters"].sum())
+    s.set_parts(1)
+    s.set_timing(True)
+    for k in range(steps):
+        flush.fill_(float(k))
+        step()
+        st = s.get_stats()
         stages["form"].append(st.form_us)
         stages["linsys"].append(st.pcg_us)
         stages["refine"].append(max(st.refine_us, 0.0))
         stages["merit"].append(st.merit_us)
-        iters += int(out["iters"].sum())
     s.set_timing(False)
+    s.set_parts(0)
     bad = int((out["status"] != 0).sum())
     return (statistics.mean(ms), {k: statistics.mean(v) for k, v in stages.items()},
             iters / steps, bad)
@@ -388,10 +396,12 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
 
     # ---- device-resident timing: per-step events, L2 flushed in between ----
-    s.set_timing(True)
+    # the step as the library runs it by default: the batch in parts that run
+    # concurrently on internal streams (gato_set_parts), the events on the
+    # caller's stream bracketing all of them
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    pcg_us, refine_us, form_us, merit_us, iters_total = [], [], [], [], 0
+    iters_total = 0
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -401,19 +411,32 @@ def run_gpu(args, world, rank, local):
             starts[k].record(stream)
             step()
             ends[k].record(stream)
-            st = s.get_stats()  # synchronises on this step's last event
-            pcg_us.append(st.pcg_us)
-            refine_us.append(max(st.refine_us, 0.0))
-            form_us.append(st.form_us)
-            merit_us.append(st.merit_us)
+            ends[k].synchronize()
             iters_total += int(out["iters"].sum())
         torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    s.set_timing(False)
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     total_ms = sum(step_ms)
     status_bad = int((out["status"] != 0).sum())
+    parts = s.get_parts()
+
+    # ---- stage breakdown: the same steps as one part, whose stages are
+    # bracketed by events on one stream; the PCG roofline uses these launches
+    s.set_parts(1)
+    s.set_timing(True)
+    pcg_us, refine_us, form_us, merit_us = [], [], [], []
+    for k in range(args.steps):
+        flush.fill_(float(k))
+        step()
+        st = s.get_stats()  # synchronises on this step's last event
+        pcg_us.append(st.pcg_us)
+        refine_us.append(max(st.refine_us, 0.0))
+        form_us.append(st.form_us)
+        merit_us.append(st.merit_us)
+    torch.cuda.synchronize()
+    s.set_timing(False)
+    s.set_parts(0)
 
     # ---- end to end through the C ABI with host buffers ----
     # gato_solve_kkt_host on pinned host arrays: every step copies the inputs
@@ -520,6 +543,8 @@ def run_gpu(args, world, rank, local):
             "config": _config(w),
             "pcg_iters_per_sec": iters_per_step * world / (total_ms / args.steps / 1000.0),
             "pcg_iters_per_solve": iters_per_step / M,
+            "parts": parts,
+            "stage_us_note": "one-part pass of the same steps (stage events need one stream)",
             "stage_us": {"form": statistics.mean(form_us), "pcg": statistics.mean(pcg_us),
                          "refine": statistics.mean(refine_us),
                          "merit": statistics.mean(merit_us)},

@@ -73,8 +73,10 @@ extern "C" {
                                       block diagonal of S                         */
 
 /* PCG kernel selection (gato_set_pcg_kernel) */
-#define GATO_PCG_AUTO 0            /* the wide-tile kernel when 7 <= n <= 16 and
-                                      N <= 128, else the generic kernel            */
+#define GATO_PCG_AUTO 0            /* for 7 <= n <= 16 the wide-tile kernel when
+                                      N <= 128 and the cluster kernel (2 or 4
+                                      CTAs per solve) when 128 < N <= 512; else
+                                      the generic kernel                          */
 #define GATO_PCG_GENERIC 1         /* always the generic kernel                   */
 #define GATO_PCG_WIDE 2            /* the wide-tile kernel (two threads per
                                       coupling block, rows over all 2H columns)
@@ -279,7 +281,9 @@ int gato_linesearch(gato_handle* h, const gato_params* p, const float* Q, const 
  * with the same S (PCG to p->refine_eps on the correction system's relative
  * preconditioned residual, or the direct solve's factors), and added to dz
  * and lambda; iters then counts PCG iterations over all solves of the
- * refinement. */
+ * refinement.  The batch runs as gato_set_parts parts of consecutive solves,
+ * concurrently on internal streams ordered after the work already on `stream`
+ * (which waits for them); the outputs do not depend on the part count. */
 int gato_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const float* R,
                    const float* q, const float* r, const float* A, const float* B,
                    const float* e, const float* s0, float* dX, float* dU, float* lambda,
@@ -350,16 +354,17 @@ int gato_solve_kkt_noalloc(const gato_params* p, int M, int N, int n, int m, con
                            float* dU, float* lambda, int32_t* iters, float* merit,
                            int32_t* best, uint32_t* status, void* stream);
 
-/* Largest number of parts gato_solve_kkt_host splits a batch into. */
-#define GATO_HOST_MAX_CHUNKS 8
+/* Largest number of parts gato_solve_kkt and gato_solve_kkt_host split a
+ * batch into (gato_set_parts). */
+#define GATO_MAX_PARTS 8
 
 /* gato_solve_kkt on HOST buffers: every input and output pointer (same
  * shapes and layouts as gato_solve_kkt) is host memory.  The paper has no
  * counterpart; it serves callers whose batch lives in host memory.  The call
- * splits the batch into parts of consecutive solves (gato_set_host_chunks)
- * and runs each part on an internal stream: copy its inputs to the device,
- * solve it as gato_solve_kkt does, copy its outputs back.  The copies of one
- * part overlap the solves of the others.  Each part's arithmetic is that of
+ * splits the batch into parts of consecutive solves (gato_set_parts) and
+ * runs each part on an internal stream: copy its inputs to the device, solve
+ * it as gato_solve_kkt does, copy its outputs back.  The copies of one part
+ * overlap the solves of the others.  Each part's arithmetic is that of
  * gato_solve_kkt on the same solves, so the outputs are identical.
  * status[M] is in/out here too: it is copied in with the inputs, the bits
  * are OR-ed into it, and it is copied back.  Host buffers should be pinned
@@ -370,17 +375,26 @@ int gato_solve_kkt_noalloc(const gato_params* p, int M, int N, int n, int m, con
  * allocates device staging buffers for all M solves, one internal stream and
  * one sub-batch workspace per part (about the size of the handle's own
  * workspace in total); later calls with the same part count reuse them.  Stage
- * timing is not recorded.  Errors: INVALID_ARG, NO_MEMORY, CUDA. */
+ * timing is recorded only for a single part.  Errors: INVALID_ARG, NO_MEMORY,
+ * CUDA. */
 int gato_solve_kkt_host(gato_handle* h, const gato_params* p, const float* Q, const float* R,
                         const float* q, const float* r, const float* A, const float* B,
                         const float* e, const float* s0, float* dX, float* dU, float* lambda,
                         int32_t* iters, float* merit, int32_t* best, uint32_t* status,
                         void* stream);
 
-/* Number of parts gato_solve_kkt_host splits the batch into: 1 ..
- * GATO_HOST_MAX_CHUNKS (capped at M), or 0 for the automatic choice (the
- * default).  Errors: INVALID_ARG. */
-int gato_set_host_chunks(gato_handle* h, int chunks);
+/* Number of parts gato_solve_kkt and gato_solve_kkt_host split a batch into:
+ * 1 .. GATO_MAX_PARTS (capped at M), or 0 for the automatic choice (the
+ * default: one part per 64 solves, at most 4).  The parts of a call run
+ * concurrently on internal streams, each on its own sub-batch workspace, so
+ * the kernels of one part fill the SMs that another part's leave idle (the
+ * last wave of its PCG, its shorter stages).  Errors: INVALID_ARG. */
+int gato_set_parts(gato_handle* h, int parts);
+
+/* The number of parts the next gato_solve_kkt or gato_solve_kkt_host call on
+ * this handle runs (the setting resolved for the handle's M) into *parts.
+ * Errors: INVALID_ARG. */
+int gato_get_parts(const gato_handle* h, int* parts);
 
 #ifdef __cplusplus
 }

@@ -34,7 +34,8 @@ def test_header_declares_the_abi():
                "gato_default_params", "gato_set_timing", "gato_get_stats",
                "gato_set_pcg_kernel", "gato_set_form_kernel", "gato_solve_kkt_noalloc",
                "gato_bdsv_solve", "gato_set_bdsv_kernel", "gato_sqp_linear",
-               "gato_default_sqp_params"):
+               "gato_default_sqp_params", "gato_solve_kkt_host", "gato_set_parts",
+               "gato_get_parts"):
         assert fn in names
 
 
@@ -102,6 +103,9 @@ def test_invalid_arguments_rejected_before_cuda(lib):
     assert lib.gato_pcg_solve(None, ctypes.byref(p), *([None] * 6), None) == gato.GATO_ERR_INVALID_ARG
     assert lib.gato_linesearch(None, ctypes.byref(p), *null, *([None] * 5), None) == gato.GATO_ERR_INVALID_ARG
     assert lib.gato_solve_kkt(None, ctypes.byref(p), *null, *([None] * 7), None) == gato.GATO_ERR_INVALID_ARG
+    assert lib.gato_solve_kkt_host(None, ctypes.byref(p), *null, *([None] * 7), None) == gato.GATO_ERR_INVALID_ARG
+    assert lib.gato_set_parts(None, 1) == gato.GATO_ERR_INVALID_ARG
+    assert lib.gato_get_parts(None, None) == gato.GATO_ERR_INVALID_ARG
     assert lib.gato_apply_step(None, ctypes.byref(p), *([None] * 5), None) == gato.GATO_ERR_INVALID_ARG
     assert lib.gato_bdsv_solve(None, ctypes.byref(p), *([None] * 5), None) == gato.GATO_ERR_INVALID_ARG
     sp = gato.default_sqp_params()

@@ -1,0 +1,146 @@
+"""The batch in parts: gato_solve_kkt and gato_solve_kkt_host split a batch
+into parts of consecutive solves that run concurrently on internal streams
+(gato_set_parts), the host entry also copying each part's slice in and out.
+Each part runs the one-part path's arithmetic on its solves, so every output
+must equal the one-part gato_solve_kkt's bit for bit, for every part count
+(ragged parts included), and be within the oracle's tolerance."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from trajectory_optimization_kkt_gb300 import gato  # noqa: E402
+from trajectory_optimization_kkt_gb300.workloads import WORKLOADS, make_batch, random_lq  # noqa: E402
+
+from test_gpu_parity import check_solution, params_for  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def device_solve(s, p, prob, parts):
+    s.set_parts(parts)
+    d = gato.to_device(prob)
+    out = s.outputs(p.n_alpha)
+    s.solve_kkt(p, d, out["dX"], out["dU"], out["lam"], out["iters"], out["merit"], out["best"],
+                out["status"])
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def host_solve(s, p, prob, parts, status0=None):
+    s.set_parts(parts)
+    hp = gato.to_host(prob)
+    out = s.host_outputs(p.n_alpha)
+    if status0 is not None:
+        out["status"].copy_(torch.as_tensor(status0, dtype=torch.int32))
+    stream = torch.cuda.current_stream()
+    s.solve_kkt_host(p, hp, out["dX"], out["dU"], out["lam"], out["iters"], out["merit"],
+                     out["best"], out["status"], stream)
+    stream.synchronize()
+    return {k: v.numpy().copy() for k, v in out.items()}
+
+
+def same(a, b):
+    for k in b:
+        assert np.array_equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("parts", [0, 1, 2, 3, 7])
+def test_parts_equal_one_part(parts):
+    w = WORKLOADS[4]
+    M = 23  # ragged parts for 2, 3 and 7
+    prob = make_batch(w, M=M)
+    p = params_for(w)
+    with gato.Solver(M, w.N, w.n, w.m) as s:
+        ref = device_solve(s, p, prob, 1)
+        dev = device_solve(s, p, prob, parts)
+        host = host_solve(s, p, prob, parts)
+    same(dev, ref)
+    same(host, ref)
+    check_solution(prob, host, [0, 11, 22], w.n_alpha, w.beta, w.mu)
+
+
+def test_default_parts_at_the_benchmark_batch():
+    """256 solves run as four parts by default; a sample against the oracle
+    and every output against the one-part run."""
+    w = WORKLOADS[4]
+    prob = make_batch(w)
+    p = params_for(w)
+    with gato.Solver(w.M, w.N, w.n, w.m) as s:
+        s.set_parts(0)
+        assert s.get_parts() == 4
+        ref = device_solve(s, p, prob, 1)
+        dev = device_solve(s, p, prob, 0)
+        host = host_solve(s, p, prob, 0)
+    same(dev, ref)
+    same(host, ref)
+    assert not ref["status"].any()
+    check_solution(prob, dev, [0, 63, 64, 191, 255], w.n_alpha, w.beta, w.mu)
+
+
+def test_parts_are_reused_and_rebuilt():
+    w = WORKLOADS[1]
+    prob = make_batch(w, M=9)
+    p = params_for(w)
+    with gato.Solver(9, w.N, w.n, w.m) as s:
+        ref = device_solve(s, p, prob, 1)
+        runs = [host_solve(s, p, prob, k) for k in (2, 2, 4, 1)]
+        runs += [device_solve(s, p, prob, k) for k in (4, 3, 3)]
+    for out in runs:
+        same(out, ref)
+
+
+def test_host_status_is_in_out_and_single_knot_problems():
+    prob = random_lq(5, 1, 6, 3, seed=901)  # N = 1: no R, A, B, e, no controls
+    prob = {k: v for k, v in prob.items() if k in ("Q", "q", "s0")}
+    p = gato.default_params()
+    with gato.Solver(5, 1, 6, 3) as s:
+        out = host_solve(s, p, prob, 2, status0=[0, 64, 0, 0, 64])
+        ref = device_solve(s, p, prob, 1)
+        dev = device_solve(s, p, prob, 2)
+    # the bit set before the call survives; the solver's own bits are the one-part run's
+    assert list(out["status"] & 64) == [0, 64, 0, 0, 64]
+    assert np.array_equal(out["status"] & ~64, ref["status"])
+    for k in ("dX", "lam", "merit", "best", "iters"):
+        assert np.array_equal(out[k], ref[k]), k
+        assert np.array_equal(dev[k], ref[k]), k
+
+
+def test_stage_timing_only_for_one_part():
+    w = WORKLOADS[1]
+    prob = make_batch(w, M=8)
+    p = params_for(w)
+    d = gato.to_device(prob)
+    with gato.Solver(8, w.N, w.n, w.m) as s:
+        o = s.outputs(p.n_alpha)
+        s.set_timing(True)
+        for parts, timed in ((2, False), (1, True)):
+            s.set_parts(parts)
+            s.solve_kkt(p, d, o["dX"], o["dU"], o["lam"], o["iters"], o["merit"], o["best"],
+                        o["status"])
+            st = s.get_stats()
+            assert (st.pcg_us > 0) == timed and (st.total_us > 0) == timed
+
+
+def test_parts_reject_bad_arguments():
+    w = WORKLOADS[1]
+    prob = make_batch(w, M=2)
+    p = params_for(w)
+    with gato.Solver(2, w.N, w.n, w.m) as s:
+        for bad in (-1, gato.GATO_MAX_PARTS + 1):
+            with pytest.raises(gato.GatoError) as e:
+                s.set_parts(bad)
+            assert e.value.code == gato.GATO_ERR_INVALID_ARG
+        s.set_parts(gato.GATO_MAX_PARTS)
+        assert s.get_parts() == 2  # capped at M
+        out = s.host_outputs(p.n_alpha)
+        with pytest.raises(ValueError):  # device tensors are refused by the binding
+            s.solve_kkt_host(p, gato.to_device(prob), out["dX"], out["dU"], out["lam"],
+                             out["iters"], out["merit"], out["best"], out["status"])

@@ -351,7 +351,7 @@ int gato_create(gato_handle** out, int M, int N, int n, int m)
 void gato_destroy(gato_handle* h)
 {
     if (!h) return;
-    gato::host_pipe_free(h);
+    gato::parts_free(h);
     if (h->sqp_exec) cudaGraphExecDestroy(h->sqp_exec);
     if (h->capture_stream) cudaStreamDestroy(h->capture_stream);
     for (int i = 0; i < 5; ++i) cudaEventDestroy(h->ev[i]);
@@ -515,6 +515,11 @@ int gato_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const f
         return GATO_ERR_INVALID_ARG;
     if (h->w.N > 1 && !dU) return GATO_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;
+    if (gato::parts_for(h) > 1) {
+        h->ev_used[0] = 0;  // no stage timing for a call in parts
+        return gato::run_parts(h, p, Q, R, q, r, A, B, e, s0, dX, dU, lambda, iters, merit,
+                               best, status, st, false);
+    }
     begin_timing(h, st);
     return unsupported_or_fail(gato::run_solve_kkt(h, p, Q, R, q, r, A, B, e, s0, dX, dU,
                                                    lambda, iters, merit, best, status, st));

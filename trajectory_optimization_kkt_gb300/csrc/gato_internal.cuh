@@ -116,14 +116,24 @@ struct gato_handle {
     cudaStream_t capture_stream;
     cudaGraphExec_t sqp_exec;
     unsigned char sqp_key[512];
-    // gato_solve_kkt_host: requested part count (0 = automatic) and the
-    // staging buffers, streams and sub-batch handles of the current one
-    int host_chunks;
-    struct gato_host_pipe* pipe;
+    // gato_set_parts: requested part count (0 = automatic), and the streams,
+    // sub-batch handles and (host entry only) staging buffers of the current
+    // one
+    int parts;
+    struct gato_parts* pipe;
 };
 
 namespace gato {
-void host_pipe_free(gato_handle* h);  // releases h->pipe (gato_host.cu)
+// gato_parts.cu
+void parts_free(gato_handle* h);  // releases h->pipe
+int parts_for(const gato_handle* h);
+// gato_solve_kkt on parts of the batch, concurrently on internal streams;
+// with `host`, every pointer is host memory and is staged through device
+// buffers.  Returns a GATO_* code.
+int run_parts(gato_handle* h, const gato_params* p, const float* Q, const float* R,
+              const float* q, const float* r, const float* A, const float* B, const float* e,
+              const float* s0, float* dX, float* dU, float* lambda, int32_t* iters, float* merit,
+              int32_t* best, uint32_t* status, cudaStream_t user, bool host);
 }
 
 namespace gato {

@@ -1,0 +1,269 @@
+// gato_parts.cu -- the KKT solve of a batch as concurrent parts, from device
+// buffers (gato_solve_kkt) or host buffers (gato_solve_kkt_host).  Not on the
+// GATO pages; a GB300-side scheduling choice.
+//
+// The batch is split into parts of consecutive solves.  Each part has its own
+// internal stream and its own sub-batch handle (workspace, work counters and
+// merit counters), so the parts share no scratch and their kernels run
+// concurrently: one part's formation, right-hand side and merit fill the SMs
+// that another part's PCG leaves idle in its last wave.  From host buffers,
+// part c also copies its slice of the inputs into device staging buffers
+// first and its slice of the outputs back last, so the copies of one part
+// overlap the kernels of the others.  A solve's arithmetic does not depend on
+// its position in the batch, so the outputs do not depend on the part count.
+#include <stdlib.h>
+
+#include "gato_internal.cuh"
+
+struct gato_parts {
+    int count_parts;
+    int first[GATO_MAX_PARTS], count[GATO_MAX_PARTS];
+    gato_handle* sub[GATO_MAX_PARTS];
+    cudaStream_t st[GATO_MAX_PARTS];
+    cudaEvent_t done[GATO_MAX_PARTS];
+    cudaEvent_t entry;
+    void* dev;  // host entry: staging for the inputs and outputs of all M solves
+    // per-solve sizes (elements) of the caller's arrays and, for the staging,
+    // their offsets (bytes)
+    size_t n_Q, n_R, n_q, n_r, n_A, n_B, n_e, n_s0, n_dX, n_dU, n_lam;
+    size_t o_Q, o_R, o_q, o_r, o_A, o_B, o_e, o_s0, o_dX, o_dU, o_lam, o_merit, o_iters, o_best,
+        o_status;
+};
+
+namespace gato {
+namespace {
+
+size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+void release(gato_parts* pp)
+{
+    if (!pp) return;
+    for (int c = 0; c < pp->count_parts; ++c) {
+        if (pp->sub[c]) gato_destroy(pp->sub[c]);
+        if (pp->st[c]) cudaStreamDestroy(pp->st[c]);
+        if (pp->done[c]) cudaEventDestroy(pp->done[c]);
+    }
+    if (pp->entry) cudaEventDestroy(pp->entry);
+    if (pp->dev) cudaFree(pp->dev);
+    free(pp);
+}
+
+// k parts for the handle's sizes (no staging yet); NO_MEMORY / CUDA on failure
+int create(const gato_handle* h, int k, gato_parts** out)
+{
+    const Work& w = h->w;
+    const size_t M = w.M, N = w.N, n = w.n, m = w.m, K = N - 1;
+    gato_parts* pp = (gato_parts*)calloc(1, sizeof(gato_parts));
+    if (!pp) return GATO_ERR_NO_MEMORY;
+    pp->count_parts = k;
+    pp->n_Q = N * n * n;
+    pp->n_R = K * m * m;
+    pp->n_q = N * n;
+    pp->n_r = K * m;
+    pp->n_A = K * n * n;
+    pp->n_B = K * n * m;
+    pp->n_e = K * n;
+    pp->n_s0 = n;
+    pp->n_dX = N * n;
+    pp->n_dU = K * m;
+    pp->n_lam = N * n;
+    int rc = GATO_OK;
+    if (cudaEventCreateWithFlags(&pp->entry, cudaEventDisableTiming) != cudaSuccess)
+        rc = GATO_ERR_CUDA;
+    int first = 0;
+    for (int c = 0; c < k && rc == GATO_OK; ++c) {
+        const int cnt = (int)(M / k) + (c < (int)(M % k) ? 1 : 0);
+        pp->first[c] = first;
+        pp->count[c] = cnt;
+        first += cnt;
+        if (cudaStreamCreateWithFlags(&pp->st[c], cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&pp->done[c], cudaEventDisableTiming) != cudaSuccess) {
+            rc = GATO_ERR_CUDA;
+            break;
+        }
+        rc = gato_create(&pp->sub[c], cnt, w.N, w.n, w.m);
+    }
+    if (rc != GATO_OK) {
+        release(pp);
+        return rc;
+    }
+    *out = pp;
+    return GATO_OK;
+}
+
+// the host entry's device staging, allocated at its first use
+int ensure_staging(gato_parts* pp, int M)
+{
+    if (pp->dev) return GATO_OK;
+    const size_t f = sizeof(float), i4 = sizeof(int32_t);
+    size_t off = 0;
+    auto place = [&](size_t& o, size_t per_solve_bytes) {
+        o = off;
+        off += align256(per_solve_bytes * (size_t)M);
+    };
+    place(pp->o_Q, pp->n_Q * f);
+    place(pp->o_R, pp->n_R * f);
+    place(pp->o_q, pp->n_q * f);
+    place(pp->o_r, pp->n_r * f);
+    place(pp->o_A, pp->n_A * f);
+    place(pp->o_B, pp->n_B * f);
+    place(pp->o_e, pp->n_e * f);
+    place(pp->o_s0, pp->n_s0 * f);
+    place(pp->o_dX, pp->n_dX * f);
+    place(pp->o_dU, pp->n_dU * f);
+    place(pp->o_lam, pp->n_lam * f);
+    place(pp->o_merit, (GATO_MAX_ALPHA + 1) * f);
+    place(pp->o_iters, i4);
+    place(pp->o_best, i4);
+    place(pp->o_status, i4);
+    if (cudaMalloc(&pp->dev, off) != cudaSuccess) {
+        cudaGetLastError();
+        pp->dev = nullptr;
+        return GATO_ERR_NO_MEMORY;
+    }
+    return GATO_OK;
+}
+
+}  // namespace
+
+// one part per 64 solves, between 1 and 4, or the caller's choice (capped at M)
+int parts_for(const gato_handle* h)
+{
+    const int M = h->w.M;
+    int k = h->parts;
+    if (k <= 0) {
+        k = M / 64;
+        if (k > 4) k = 4;
+        if (k < 1) k = 1;
+    }
+    if (k > M) k = M;
+    return k;
+}
+
+void parts_free(gato_handle* h)
+{
+    if (!h) return;
+    release(h->pipe);
+    h->pipe = nullptr;
+}
+
+int run_parts(gato_handle* h, const gato_params* p, const float* Q, const float* R,
+              const float* q, const float* r, const float* A, const float* B, const float* e,
+              const float* s0, float* dX, float* dU, float* lambda, int32_t* iters, float* merit,
+              int32_t* best, uint32_t* status, cudaStream_t user, bool host)
+{
+    const int k = parts_for(h);
+    if (h->pipe && h->pipe->count_parts != k) parts_free(h);
+    if (!h->pipe) {
+        const int rc = create(h, k, &h->pipe);
+        if (rc != GATO_OK) return rc;
+    }
+    gato_parts* pp = h->pipe;
+    if (host) {
+        const int rc = ensure_staging(pp, h->w.M);
+        if (rc != GATO_OK) return rc;
+    }
+    char* dev = (char*)pp->dev;
+    const size_t f = sizeof(float), i4 = sizeof(int32_t);
+    const size_t A1 = (size_t)p->n_alpha + 1;  // merit row stride of the caller's array
+    cudaError_t err = cudaEventRecord(pp->entry, user);
+    for (int c = 0; c < k && err == cudaSuccess; ++c) {
+        cudaStream_t st = pp->st[c];
+        gato_handle* sh = pp->sub[c];
+        sh->pcg_kernel = h->pcg_kernel;
+        sh->bdsv_kernel = h->bdsv_kernel;
+        sh->force_smem_form = h->force_smem_form;
+        sh->timing = 0;
+        const size_t f0 = (size_t)pp->first[c], cnt = (size_t)pp->count[c];
+        // the part's slice of an array with `per` elements of `es` bytes per
+        // solve: in the staging (host entry) or in the caller's array
+        auto part = [&](size_t o, size_t per, size_t es, const void* caller) {
+            return host ? (void*)(dev + o + f0 * per * es)
+                        : (caller ? (void*)((const char*)caller + f0 * per * es) : nullptr);
+        };
+        auto h2d = [&](size_t o, size_t per, size_t es, const void* src) {
+            if (!host || err != cudaSuccess || per == 0) return;
+            err = cudaMemcpyAsync(part(o, per, es, nullptr), (const char*)src + f0 * per * es,
+                                  cnt * per * es, cudaMemcpyHostToDevice, st);
+        };
+        auto d2h = [&](size_t o, size_t per, size_t es, void* dst) {
+            if (!host || err != cudaSuccess || per == 0) return;
+            err = cudaMemcpyAsync((char*)dst + f0 * per * es, part(o, per, es, nullptr),
+                                  cnt * per * es, cudaMemcpyDeviceToHost, st);
+        };
+        err = cudaStreamWaitEvent(st, pp->entry, 0);
+        h2d(pp->o_Q, pp->n_Q, f, Q);
+        h2d(pp->o_R, pp->n_R, f, R);
+        h2d(pp->o_q, pp->n_q, f, q);
+        h2d(pp->o_r, pp->n_r, f, r);
+        h2d(pp->o_A, pp->n_A, f, A);
+        h2d(pp->o_B, pp->n_B, f, B);
+        h2d(pp->o_e, pp->n_e, f, e);
+        h2d(pp->o_s0, pp->n_s0, f, s0);
+        h2d(pp->o_status, 1, i4, status);
+        if (err == cudaSuccess)
+            err = run_solve_kkt(sh, p, (const float*)part(pp->o_Q, pp->n_Q, f, Q),
+                                (const float*)part(pp->o_R, pp->n_R, f, R),
+                                (const float*)part(pp->o_q, pp->n_q, f, q),
+                                (const float*)part(pp->o_r, pp->n_r, f, r),
+                                (const float*)part(pp->o_A, pp->n_A, f, A),
+                                (const float*)part(pp->o_B, pp->n_B, f, B),
+                                (const float*)part(pp->o_e, pp->n_e, f, e),
+                                (const float*)part(pp->o_s0, pp->n_s0, f, s0),
+                                (float*)part(pp->o_dX, pp->n_dX, f, dX),
+                                (float*)part(pp->o_dU, pp->n_dU, f, dU),
+                                (float*)part(pp->o_lam, pp->n_lam, f, lambda),
+                                (int32_t*)part(pp->o_iters, 1, i4, iters),
+                                (float*)part(pp->o_merit, A1, f, merit),
+                                (int32_t*)part(pp->o_best, 1, i4, best),
+                                (uint32_t*)part(pp->o_status, 1, i4, status), st);
+        d2h(pp->o_dX, pp->n_dX, f, dX);
+        d2h(pp->o_dU, pp->n_dU, f, dU);
+        d2h(pp->o_lam, pp->n_lam, f, lambda);
+        d2h(pp->o_iters, 1, i4, iters);
+        d2h(pp->o_merit, A1, f, merit);
+        d2h(pp->o_best, 1, i4, best);
+        d2h(pp->o_status, 1, i4, status);
+        // the caller's stream waits for whatever this part enqueued
+        if (cudaEventRecord(pp->done[c], st) == cudaSuccess)
+            cudaStreamWaitEvent(user, pp->done[c], 0);
+    }
+    if (err == cudaErrorInvalidConfiguration) return GATO_ERR_UNSUPPORTED;
+    return err == cudaSuccess ? GATO_OK : GATO_ERR_CUDA;
+}
+
+}  // namespace gato
+
+extern "C" {
+
+int gato_set_parts(gato_handle* h, int parts)
+{
+    if (!h || parts < 0 || parts > GATO_MAX_PARTS) return GATO_ERR_INVALID_ARG;
+    h->parts = parts;
+    return GATO_OK;
+}
+
+int gato_get_parts(const gato_handle* h, int* parts)
+{
+    if (!h || !parts) return GATO_ERR_INVALID_ARG;
+    *parts = gato::parts_for(h);
+    return GATO_OK;
+}
+
+int gato_solve_kkt_host(gato_handle* h, const gato_params* p, const float* Q, const float* R,
+                        const float* q, const float* r, const float* A, const float* B,
+                        const float* e, const float* s0, float* dX, float* dU, float* lambda,
+                        int32_t* iters, float* merit, int32_t* best, uint32_t* status,
+                        void* stream)
+{
+    using namespace gato;
+    if (!h || !params_valid(p) || !Q || !q || !s0 || !dX || !lambda || !iters || !merit ||
+        !best || !status)
+        return GATO_ERR_INVALID_ARG;
+    if (h->w.N > 1 && (!R || !r || !A || !B || !e || !dU)) return GATO_ERR_INVALID_ARG;
+    h->ev_used[0] = 0;  // no stage timing for a call in parts
+    return run_parts(h, p, Q, R, q, r, A, B, e, s0, dX, dU, lambda, iters, merit, best, status,
+                     (cudaStream_t)stream, true);
+}
+
+}  // extern "C"

@@ -28,7 +28,7 @@ GATO_PCG_AUTO = 0
 GATO_PCG_GENERIC = 1
 GATO_PCG_WIDE = 2
 GATO_PCG_TILE = 3
-GATO_HOST_MAX_CHUNKS = 8
+GATO_MAX_PARTS = 8
 
 GATO_LINSYS_AUTO = 0
 GATO_LINSYS_PCG = 1
@@ -118,7 +118,8 @@ def load(path: Optional[str] = None):
     lib.gato_linesearch.argtypes = [vp, P] + [vp] * 8 + [vp] * 5 + [vp]
     lib.gato_solve_kkt.argtypes = [vp, P] + [vp] * 8 + [vp] * 7 + [vp]
     lib.gato_solve_kkt_host.argtypes = [vp, P] + [vp] * 8 + [vp] * 7 + [vp]
-    lib.gato_set_host_chunks.argtypes = [vp, ip]
+    lib.gato_set_parts.argtypes = [vp, ip]
+    lib.gato_get_parts.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
     lib.gato_apply_step.argtypes = [vp, P] + [vp] * 5 + [vp]
     lib.gato_solve_kkt_noalloc.argtypes = [P, ip, ip, ip, ip] + [vp] * 8 + [vp] * 7 + [vp]
     for fn in ("gato_create", "gato_set_timing", "gato_set_pcg_kernel", "gato_set_form_kernel",
@@ -284,8 +285,13 @@ class Solver:
             _ptr(iters, torch.int32, "iters"), _ptr(merit), _ptr(best, torch.int32, "best"),
             _ptr(status, torch.int32, "status"), _stream(stream)))
 
-    def set_host_chunks(self, chunks: int):
-        _check("gato_set_host_chunks", self.lib.gato_set_host_chunks(self.h, chunks))
+    def set_parts(self, parts: int):
+        _check("gato_set_parts", self.lib.gato_set_parts(self.h, parts))
+
+    def get_parts(self) -> int:
+        v = ctypes.c_int(0)
+        _check("gato_get_parts", self.lib.gato_get_parts(self.h, ctypes.byref(v)))
+        return v.value
 
     def solve_kkt_host(self, params, prob, dX, dU, lam, iters, merit, best, status,
                        stream=None):
