@@ -572,7 +572,7 @@ def run_gpu(args, world, rank, local):
             "e2e": None if args.no_e2e else {
                 "value": solves / (e2e_ms / 1000.0), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step * args.steps,
+            "gpu_launches": launches_per_step * parts * args.steps,  # each part launches all
             "clocks": clk.summary(),
         }
         if alternatives:
