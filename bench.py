@@ -183,6 +183,26 @@ def _config(w, **extra):
     return c
 
 
+def _cpu_model():
+    """The host CPU's model name from /proc/cpuinfo (or the machine type)."""
+    import platform
+    ids = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+                if key in ("cpu implementer", "cpu part") and key not in ids:
+                    ids[key] = line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    if ids:  # Arm kernels name the core by implementer and part codes
+        return (f"{platform.machine()} (implementer {ids.get('cpu implementer', '?')}, "
+                f"part {ids.get('cpu part', '?')})")
+    return platform.machine()
+
+
 def _cpu_baseline(w, budget_s=12.0):
     """Oracle on a bounded sample of the workload, spawn pool on all cores."""
     import multiprocessing as mp
@@ -201,9 +221,15 @@ def _cpu_baseline(w, budget_s=12.0):
         t0 = time.perf_counter()
         res = pool.starmap(_oracle_solve, [(s, kw) for s in solves])
         sec = time.perf_counter() - t0
+    # one thread: the first two solves in this process
+    t0 = time.perf_counter()
+    for s_ in solves[:2]:
+        _oracle_solve(s_, kw)
+    one = 2 / (time.perf_counter() - t0)
     return {"value": sample / sec, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"first {sample} of the {w.M} solves, fp64 C oracle, spawn pool",
-            "pcg_iters_per_sec": sum(r[0] for r in res) / sec}
+            "pcg_iters_per_sec": sum(r[0] for r in res) / sec,
+            "single_thread_solves_per_s": one, "cpu_model": _cpu_model()}
 
 
 def _time_solver(torch, s, p, d, out, steps, flush, stream):
@@ -276,6 +302,47 @@ def run_sweep(args, local):
                                       "ms_per_step": ms, "stage_us": stages,
                                       "pcg_iters_per_solve": iters / M,
                                       "status_nonzero_solves": bad}), flush=True)
+
+
+def run_throughput_sweep(args, local):
+    """The benchmark workload's throughput sweep: M in {1, 8, 16, 64, 256} x
+    N in {16, 32, 64, 128} at n = 14, m = 7, the default PCG path; solves/s
+    and PCG iterations/s of whole calls (default parts), the merit's
+    microseconds per launch and (knot, candidate) pairs per second from the
+    one-part stage pass; one JSON line per cell."""
+    import torch
+
+    from trajectory_optimization_kkt_gb300 import _build, gato
+    from trajectory_optimization_kkt_gb300.workloads import WORKLOADS, make_batch
+    torch.cuda.set_device(local)
+    _build.build()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    base = WORKLOADS[WORKLOAD_INDEX]
+    for N in (16, 32, 64, 128):
+        for M in (1, 8, 16, 64, 256):
+            w = base.with_batch(M, N)
+            prob = make_batch(w, M=M)
+            d = {k: torch.from_numpy(v).to(dev) for k, v in prob.items()}
+            with gato.Solver(M, N, w.n, w.m) as s:
+                out = s.outputs(w.n_alpha)
+                p = gato.default_params(pcg_eps=w.pcg_eps, pcg_max_iters=w.pcg_max_iters,
+                                        n_alpha=w.n_alpha, beta=w.beta, mu=w.mu,
+                                        refine_steps=w.refine_steps, refine_eps=w.refine_eps,
+                                        linsys=LINSYS["pcg"])
+                ms, stages, iters, bad = _time_solver(torch, s, p, d, out, args.steps, flush,
+                                                      stream)
+                print(json.dumps({"sweep": "throughput", "M": M, "N": N, "n": w.n, "m": w.m,
+                                  "parts": s.get_parts(), "solves_per_s": M / (ms / 1000.0),
+                                  "ms_per_step": ms,
+                                  "pcg_iters_per_sec": iters / (ms / 1000.0),
+                                  "pcg_iters_per_solve": iters / M,
+                                  "merit_us_per_launch": stages["merit"],
+                                  "knot_candidates_per_s":
+                                      M * N * (w.n_alpha + 1) / (stages["merit"] * 1e-6),
+                                  "stage_us": stages, "status_nonzero_solves": bad}),
+                      flush=True)
 
 
 def _sqp_timing(torch, gato, model_np, M, iters, linsys, use_graph, dev, stream, flush, reps=3):
@@ -602,6 +669,8 @@ def main():
                     help="skip timing the same step through the direct solvers")
     ap.add_argument("--sweep", action="store_true",
                     help="horizon x batch sweep of the three linear solvers instead")
+    ap.add_argument("--throughput-sweep", action="store_true",
+                    help="the workload's M x N throughput sweep (solves/s, merit us) instead")
     ap.add_argument("--sqp-study", action="store_true",
                     help="the rho-damping SQP case study on the linear model instead")
     ap.add_argument("--batch", type=int, default=None,
@@ -613,6 +682,8 @@ def main():
         run_reference(args, world, rank)
     elif args.sweep:
         run_sweep(args, local)
+    elif args.throughput_sweep:
+        run_throughput_sweep(args, local)
     elif args.sqp_study:
         run_sqp_study(args, local)
     else:
