@@ -385,7 +385,7 @@ int gato_solve_kkt_host(gato_handle* h, const gato_params* p, const float* Q, co
 
 /* Number of parts gato_solve_kkt and gato_solve_kkt_host split a batch into:
  * 1 .. GATO_MAX_PARTS (capped at M), or 0 for the automatic choice (the
- * default: one part per 64 solves, at most 4).  The parts of a call run
+ * default: one part below 64 solves, two below 128, four from 128).  The parts of a call run
  * concurrently on internal streams, each on its own sub-batch workspace, so
  * the kernels of one part fill the SMs that another part's leave idle (the
  * last wave of its PCG, its shorter stages).  Errors: INVALID_ARG. */
