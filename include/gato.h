@@ -115,7 +115,7 @@ extern "C" {
 #define GATO_MERIT_PER_CANDIDATE 1 /* one block of merit_threads per (knot,
                                       candidate), full formula per candidate      */
 
-/* Limits of this build. */
+/* Limits of the library. */
 #define GATO_MAX_STATE 64          /* n <= 64 */
 #define GATO_MAX_CONTROL 64        /* m <= 64 */
 #define GATO_MAX_ALPHA 31          /* n_alpha <= 31 */
