@@ -283,7 +283,10 @@ int gato_linesearch(gato_handle* h, const gato_params* p, const float* Q, const 
  * and lambda; iters then counts PCG iterations over all solves of the
  * refinement.  The batch runs as gato_set_parts parts of consecutive solves,
  * concurrently on internal streams ordered after the work already on `stream`
- * (which waits for them); the outputs do not depend on the part count. */
+ * (which waits for them); the outputs do not depend on the part count.  With
+ * more than one part the parts use their own workspaces, so the handle's
+ * formation (what gato_get_schur, gato_pcg_solve and gato_bdsv_solve use)
+ * stays that of the last gato_form_schur. */
 int gato_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const float* R,
                    const float* q, const float* r, const float* A, const float* B,
                    const float* e, const float* s0, float* dX, float* dU, float* lambda,
