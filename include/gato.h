@@ -283,10 +283,11 @@ int gato_linesearch(gato_handle* h, const gato_params* p, const float* Q, const 
  * and lambda; iters then counts PCG iterations over all solves of the
  * refinement.  The batch runs as gato_set_parts parts of consecutive solves,
  * concurrently on internal streams ordered after the work already on `stream`
- * (which waits for them); the outputs do not depend on the part count.  With
- * more than one part the parts use their own workspaces, so the handle's
- * formation (what gato_get_schur, gato_pcg_solve and gato_bdsv_solve use)
- * stays that of the last gato_form_schur. */
+ * (which waits for them); the outputs do not depend on the part count.  The
+ * parts' workspaces are views into the handle's own allocation (nothing is
+ * allocated by the call, which can be captured into a CUDA graph), so a call
+ * in parts overwrites the handle's formation: call gato_form_schur again
+ * before gato_get_schur, gato_pcg_solve or gato_bdsv_solve. */
 int gato_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const float* R,
                    const float* q, const float* r, const float* A, const float* B,
                    const float* e, const float* s0, float* dX, float* dU, float* lambda,
@@ -375,10 +376,9 @@ int gato_solve_kkt_noalloc(const gato_params* p, int M, int N, int n, int m, con
  * staged by the driver and do not overlap.  The work is ordered after the
  * work already on `stream`, and `stream` waits for all of it: synchronise
  * `stream` before reading the outputs or reusing the inputs.  The first call
- * allocates device staging buffers for all M solves, one internal stream and
- * one sub-batch workspace per part (about the size of the handle's own
- * workspace in total); later calls with the same part count reuse them.  Stage
- * timing is recorded only for a single part.  Errors: INVALID_ARG, NO_MEMORY,
+ * allocates device staging buffers for the inputs and outputs of all M
+ * solves; later calls reuse them.  Stage timing is recorded only for a
+ * single part.  Errors: INVALID_ARG, NO_MEMORY,
  * CUDA. */
 int gato_solve_kkt_host(gato_handle* h, const gato_params* p, const float* Q, const float* R,
                         const float* q, const float* r, const float* A, const float* B,

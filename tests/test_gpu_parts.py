@@ -144,3 +144,36 @@ def test_parts_reject_bad_arguments():
         with pytest.raises(ValueError):  # device tensors are refused by the binding
             s.solve_kkt_host(p, gato.to_device(prob), out["dX"], out["dU"], out["lam"],
                              out["iters"], out["merit"], out["best"], out["status"])
+
+
+def test_call_in_parts_allocates_nothing_and_can_be_captured():
+    """The parts are views into the handle's own allocation: a call that
+    re-partitions the batch leaves the free device memory unchanged, and a
+    call captured into a CUDA graph replays to the same outputs."""
+    w = WORKLOADS[4]
+    M = 128
+    prob = make_batch(w, M=M)
+    p = params_for(w)
+    d = gato.to_device(prob)
+    with gato.Solver(M, w.N, w.n, w.m) as s:
+        ref = device_solve(s, p, prob, 1)  # loads every kernel once
+        same(device_solve(s, p, prob, 4), ref)  # and uses every part's stream
+        s.set_parts(2)
+        out = s.outputs(p.n_alpha)
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        s.solve_kkt(p, d, out["dX"], out["dU"], out["lam"], out["iters"], out["merit"],
+                    out["best"], out["status"])
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0
+        same({k: v.cpu().numpy() for k, v in out.items()}, ref)
+        s.set_parts(0)
+        assert s.get_parts() == 4
+        cap = s.outputs(p.n_alpha)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            s.solve_kkt(p, d, cap["dX"], cap["dU"], cap["lam"], cap["iters"], cap["merit"],
+                        cap["best"], cap["status"])
+        g.replay()
+        torch.cuda.synchronize()
+        same({k: v.cpu().numpy() for k, v in cap.items()}, ref)

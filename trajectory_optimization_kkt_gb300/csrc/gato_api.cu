@@ -327,7 +327,9 @@ int gato_create(gato_handle** out, int M, int N, int n, int m)
         free(h);
         return GATO_ERR_CUDA;
     }
-    h->bytes = gato::carve_workspace(h->w, M, N, n, m, nullptr);
+    // room for the handle's workspace and for any partition of the batch into
+    // parts, which are views into the same allocation
+    h->bytes = gato::carve_workspace(h->w, M, N, n, m, nullptr) + gato::parts_extra_bytes();
     if (cudaMalloc(&h->base, h->bytes) != cudaSuccess) {
         cudaGetLastError();
         free(h);
@@ -344,6 +346,13 @@ int gato_create(gato_handle** out, int M, int N, int n, int m)
     }
     h->last.form_us = h->last.pcg_us = h->last.refine_us = h->last.merit_us = h->last.total_us =
         -1.f;
+    const int prc = gato::parts_init(h);
+    if (prc != GATO_OK) {
+        for (int i = 0; i < 5; ++i) cudaEventDestroy(h->ev[i]);
+        cudaFree(h->base);
+        free(h);
+        return prc;
+    }
     *out = h;
     return GATO_OK;
 }

@@ -125,6 +125,8 @@ struct gato_handle {
 
 namespace gato {
 // gato_parts.cu
+size_t parts_extra_bytes();       // allocation beyond the handle's own workspace
+int parts_init(gato_handle* h);   // streams and events of the parts (gato_create)
 void parts_free(gato_handle* h);  // releases h->pipe
 int parts_for(const gato_handle* h);
 // gato_solve_kkt on parts of the batch, concurrently on internal streams;

@@ -12,13 +12,15 @@
 // overlap the kernels of the others.  A solve's arithmetic does not depend on
 // its position in the batch, so the outputs do not depend on the part count.
 #include <stdlib.h>
+#include <string.h>
 
 #include "gato_internal.cuh"
 
 struct gato_parts {
-    int count_parts;
+    int nstreams;     // streams and events created (min(M, GATO_MAX_PARTS))
+    int count_parts;  // parts of the current partition (0: none yet)
     int first[GATO_MAX_PARTS], count[GATO_MAX_PARTS];
-    gato_handle* sub[GATO_MAX_PARTS];
+    gato_handle sub[GATO_MAX_PARTS];  // views into the handle's workspace
     cudaStream_t st[GATO_MAX_PARTS];
     cudaEvent_t done[GATO_MAX_PARTS];
     cudaEvent_t entry;
@@ -38,8 +40,7 @@ size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 void release(gato_parts* pp)
 {
     if (!pp) return;
-    for (int c = 0; c < pp->count_parts; ++c) {
-        if (pp->sub[c]) gato_destroy(pp->sub[c]);
+    for (int c = 0; c < pp->nstreams; ++c) {
         if (pp->st[c]) cudaStreamDestroy(pp->st[c]);
         if (pp->done[c]) cudaEventDestroy(pp->done[c]);
     }
@@ -48,47 +49,33 @@ void release(gato_parts* pp)
     free(pp);
 }
 
-// k parts for the handle's sizes (no staging yet); NO_MEMORY / CUDA on failure
-int create(const gato_handle* h, int k, gato_parts** out)
+// the parts as views into the handle's workspace: part c takes the next
+// 256-byte-aligned region of the size carve_workspace gives for its solves
+// (the handle's allocation has room for any partition, see
+// parts_extra_bytes); no allocation
+void partition(gato_handle* h, int k)
 {
+    gato_parts* pp = h->pipe;
     const Work& w = h->w;
-    const size_t M = w.M, N = w.N, n = w.n, m = w.m, K = N - 1;
-    gato_parts* pp = (gato_parts*)calloc(1, sizeof(gato_parts));
-    if (!pp) return GATO_ERR_NO_MEMORY;
-    pp->count_parts = k;
-    pp->n_Q = N * n * n;
-    pp->n_R = K * m * m;
-    pp->n_q = N * n;
-    pp->n_r = K * m;
-    pp->n_A = K * n * n;
-    pp->n_B = K * n * m;
-    pp->n_e = K * n;
-    pp->n_s0 = n;
-    pp->n_dX = N * n;
-    pp->n_dU = K * m;
-    pp->n_lam = N * n;
-    int rc = GATO_OK;
-    if (cudaEventCreateWithFlags(&pp->entry, cudaEventDisableTiming) != cudaSuccess)
-        rc = GATO_ERR_CUDA;
+    size_t off = 0;
     int first = 0;
-    for (int c = 0; c < k && rc == GATO_OK; ++c) {
-        const int cnt = (int)(M / k) + (c < (int)(M % k) ? 1 : 0);
+    for (int c = 0; c < k; ++c) {
+        const int cnt = w.M / k + (c < w.M % k ? 1 : 0);
         pp->first[c] = first;
         pp->count[c] = cnt;
         first += cnt;
-        if (cudaStreamCreateWithFlags(&pp->st[c], cudaStreamNonBlocking) != cudaSuccess ||
-            cudaEventCreateWithFlags(&pp->done[c], cudaEventDisableTiming) != cudaSuccess) {
-            rc = GATO_ERR_CUDA;
-            break;
-        }
-        rc = gato_create(&pp->sub[c], cnt, w.N, w.n, w.m);
+        gato_handle& sh = pp->sub[c];
+        memset(&sh, 0, sizeof(sh));
+        sh.device = h->device;
+        sh.smem_optin = h->smem_optin;
+        sh.num_sms = h->num_sms;
+        sh.base = (char*)h->base + off;
+        sh.bytes = carve_workspace(sh.w, cnt, w.N, w.n, w.m, nullptr);
+        carve_workspace(sh.w, cnt, w.N, w.n, w.m, (float*)sh.base);
+        sh.parts = 1;
+        off += align256(sh.bytes);
     }
-    if (rc != GATO_OK) {
-        release(pp);
-        return rc;
-    }
-    *out = pp;
-    return GATO_OK;
+    pp->count_parts = k;
 }
 
 // the host entry's device staging, allocated at its first use
@@ -126,6 +113,44 @@ int ensure_staging(gato_parts* pp, int M)
 
 }  // namespace
 
+// beyond the handle's own workspace, the parts need one work-counter block
+// each, and each part's region starts on a 256-byte boundary
+size_t parts_extra_bytes() { return (size_t)GATO_MAX_PARTS * 512; }
+
+// streams and events for up to min(M, GATO_MAX_PARTS) parts, at gato_create
+int parts_init(gato_handle* h)
+{
+    const Work& w = h->w;
+    const size_t N = w.N, n = w.n, m = w.m, K = N - 1;
+    gato_parts* pp = (gato_parts*)calloc(1, sizeof(gato_parts));
+    if (!pp) return GATO_ERR_NO_MEMORY;
+    pp->n_Q = N * n * n;
+    pp->n_R = K * m * m;
+    pp->n_q = N * n;
+    pp->n_r = K * m;
+    pp->n_A = K * n * n;
+    pp->n_B = K * n * m;
+    pp->n_e = K * n;
+    pp->n_s0 = n;
+    pp->n_dX = N * n;
+    pp->n_dU = K * m;
+    pp->n_lam = N * n;
+    pp->nstreams = w.M < GATO_MAX_PARTS ? w.M : GATO_MAX_PARTS;
+    int rc = GATO_OK;
+    if (cudaEventCreateWithFlags(&pp->entry, cudaEventDisableTiming) != cudaSuccess)
+        rc = GATO_ERR_CUDA;
+    for (int c = 0; c < pp->nstreams && rc == GATO_OK; ++c)
+        if (cudaStreamCreateWithFlags(&pp->st[c], cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&pp->done[c], cudaEventDisableTiming) != cudaSuccess)
+            rc = GATO_ERR_CUDA;
+    if (rc != GATO_OK) {
+        release(pp);
+        return rc;
+    }
+    h->pipe = pp;
+    return GATO_OK;
+}
+
 // the caller's choice (capped at M), else by batch size: one part below 64
 // solves, two below 128, four from there (measured at N = 128: two parts
 // gain 3-4% at 64-96 solves, four 1-4% from 128; below 64 one is best)
@@ -151,12 +176,9 @@ int run_parts(gato_handle* h, const gato_params* p, const float* Q, const float*
               int32_t* best, uint32_t* status, cudaStream_t user, bool host)
 {
     const int k = parts_for(h);
-    if (h->pipe && h->pipe->count_parts != k) parts_free(h);
-    if (!h->pipe) {
-        const int rc = create(h, k, &h->pipe);
-        if (rc != GATO_OK) return rc;
-    }
     gato_parts* pp = h->pipe;
+    if (!pp || k > pp->nstreams) return GATO_ERR_INVALID_ARG;
+    if (pp->count_parts != k) partition(h, k);
     if (host) {
         const int rc = ensure_staging(pp, h->w.M);
         if (rc != GATO_OK) return rc;
@@ -167,7 +189,7 @@ int run_parts(gato_handle* h, const gato_params* p, const float* Q, const float*
     cudaError_t err = cudaEventRecord(pp->entry, user);
     for (int c = 0; c < k && err == cudaSuccess; ++c) {
         cudaStream_t st = pp->st[c];
-        gato_handle* sh = pp->sub[c];
+        gato_handle* sh = &pp->sub[c];
         sh->pcg_kernel = h->pcg_kernel;
         sh->bdsv_kernel = h->bdsv_kernel;
         sh->force_smem_form = h->force_smem_form;
