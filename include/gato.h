@@ -368,7 +368,9 @@ int gato_solve_kkt_noalloc(const gato_params* p, int M, int N, int n, int m, con
  * splits the batch into parts of consecutive solves (gato_set_parts) and
  * runs each part on an internal stream: copy its inputs to the device, solve
  * it as gato_solve_kkt does, copy its outputs back.  The copies of one part
- * overlap the solves of the others.  Each part's arithmetic is that of
+ * overlap the solves of the others; nothing overlaps the first part's input
+ * copy, so with three parts or more that part is about half the size of the
+ * others.  Each part's arithmetic is that of
  * gato_solve_kkt on the same solves, so the outputs are identical.
  * status[M] is in/out here too: it is copied in with the inputs, the bits
  * are OR-ed into it, and it is copied back.  Host buffers should be pinned

@@ -19,6 +19,7 @@
 struct gato_parts {
     int nstreams;     // streams and events created (min(M, GATO_MAX_PARTS))
     int count_parts;  // parts of the current partition (0: none yet)
+    int small_first;  // the current partition's first part is the short one
     int first[GATO_MAX_PARTS], count[GATO_MAX_PARTS];
     gato_handle sub[GATO_MAX_PARTS];  // views into the handle's workspace
     cudaStream_t st[GATO_MAX_PARTS];
@@ -52,15 +53,21 @@ void release(gato_parts* pp)
 // the parts as views into the handle's workspace: part c takes the next
 // 256-byte-aligned region of the size carve_workspace gives for its solves
 // (the handle's allocation has room for any partition, see
-// parts_extra_bytes); no allocation
-void partition(gato_handle* h, int k)
+// parts_extra_bytes); no allocation.  Equal parts, or with small_first and
+// three parts or more a first part of about half the others' size (from host
+// buffers nothing overlaps the first part's input copy, so it is kept short;
+// with two parts the other part would carry three quarters of the batch)
+void partition(gato_handle* h, int k, bool small_first)
 {
     gato_parts* pp = h->pipe;
     const Work& w = h->w;
+    const int c0 = (small_first && k > 2) ? (w.M / (2 * k) > 0 ? w.M / (2 * k) : 1) : 0;
+    const int rest = w.M - c0, kr = c0 ? k - 1 : k;
     size_t off = 0;
     int first = 0;
     for (int c = 0; c < k; ++c) {
-        const int cnt = w.M / k + (c < w.M % k ? 1 : 0);
+        const int r = c0 ? c - 1 : c;
+        const int cnt = (c0 && c == 0) ? c0 : rest / kr + (r < rest % kr ? 1 : 0);
         pp->first[c] = first;
         pp->count[c] = cnt;
         first += cnt;
@@ -76,6 +83,7 @@ void partition(gato_handle* h, int k)
         off += align256(sh.bytes);
     }
     pp->count_parts = k;
+    pp->small_first = small_first ? 1 : 0;
 }
 
 // the host entry's device staging, allocated at its first use
@@ -178,7 +186,7 @@ int run_parts(gato_handle* h, const gato_params* p, const float* Q, const float*
     const int k = parts_for(h);
     gato_parts* pp = h->pipe;
     if (!pp || k > pp->nstreams) return GATO_ERR_INVALID_ARG;
-    if (pp->count_parts != k) partition(h, k);
+    if (pp->count_parts != k || pp->small_first != (host ? 1 : 0)) partition(h, k, host);
     if (host) {
         const int rc = ensure_staging(pp, h->w.M);
         if (rc != GATO_OK) return rc;
