@@ -452,3 +452,35 @@ def test_stage_timing():
         st = s.get_stats()
     assert st.form_us > 0 and st.pcg_us > 0 and st.merit_us > 0
     assert st.total_us >= st.pcg_us
+
+
+def test_batch_beyond_the_grid_yz_limit():
+    """70000 solves, more than a grid's y or z extent holds (65535): the
+    per-candidate merit is launched in slices, the factored merit runs one
+    block per solve for a single part, its per-knot form per part of four.
+    All give the same steps; samples are checked against the oracle."""
+    base = random_lq(7, 2, 2, 1, seed=991)
+    M = 70000
+    prob = {k: np.ascontiguousarray(np.tile(v, (M // 7,) + (1,) * (v.ndim - 1)))
+            for k, v in base.items()}
+    d = gato.to_device(prob)
+    runs = {}
+    with gato.Solver(M, 2, 2, 1) as s:
+        for name, kind, parts in (("fused, one part", gato.GATO_MERIT_FUSED, 1),
+                                  ("fused, four parts", gato.GATO_MERIT_FUSED, 4),
+                                  ("per candidate", gato.GATO_MERIT_PER_CANDIDATE, 1)):
+            s.set_parts(parts)
+            p = gato.default_params(pcg_max_iters=200, merit_kernel=kind)
+            out = s.outputs(p.n_alpha)
+            s.solve_kkt(p, d, out["dX"], out["dU"], out["lam"], out["iters"], out["merit"],
+                        out["best"], out["status"])
+            torch.cuda.synchronize()
+            runs[name] = {k: v.cpu().numpy() for k, v in out.items()}
+    ref = runs["fused, one part"]
+    for name, out in runs.items():
+        assert np.array_equal(out["dX"], ref["dX"]), name
+        assert np.array_equal(out["best"], ref["best"]), name
+        scale = np.abs(ref["merit"]).max(axis=1, keepdims=True)
+        assert (np.abs(out["merit"] - ref["merit"]) <= TOL_MERIT * scale).all(), name
+    assert not ref["status"].any()
+    check_solution(prob, ref, [0, 35000, 65534, 65535, 69999])

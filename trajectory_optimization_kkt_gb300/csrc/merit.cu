@@ -40,6 +40,7 @@ struct MeritArgs {
     const float *Q, *R, *q, *r, *A, *B, *e, *s0, *dX, *dU;
     int A1;      // candidates including alpha = 0
     float beta;
+    int sol0;    // k_merit: first solve of the launch (grids of at most 65535 solves)
 };
 
 // alpha of candidate c: 0 for c = 0, beta^-(c-1) otherwise (repeated division)
@@ -55,7 +56,7 @@ __global__ void k_merit(MeritArgs g)
 {
     extern __shared__ __align__(16) float sm[];
     const int N = g.w.N, n = g.w.n, m = g.w.m;
-    const int k = blockIdx.x, c = blockIdx.y, sol = blockIdx.z;
+    const int k = blockIdx.x, c = blockIdx.y, sol = g.sol0 + (int)blockIdx.z;
     const int T = blockDim.x, tid = threadIdx.x;
     const bool has_u = k < N - 1;
     const size_t K = (size_t)(N - 1);
@@ -436,6 +437,7 @@ cudaError_t launch_merit(gato_handle* h, const gato_params* p, const float* Q,
     a.dX = dX; a.dU = dU;
     a.A1 = p->n_alpha + 1;
     a.beta = p->beta;
+    a.sol0 = 0;
     if (p->merit_kernel == GATO_MERIT_FUSED && w.n <= 16 && w.m <= 16 && w.M <= 65535) {
         cudaError_t e = cudaMemsetAsync(w.mcount, 0, sizeof(int) * (size_t)w.M, st);
         if (e != cudaSuccess) return e;
@@ -456,10 +458,15 @@ cudaError_t launch_merit(gato_handle* h, const gato_params* p, const float* Q,
         return cudaGetLastError();
     }
     const size_t smem = (size_t)(5 * w.n + 2 * w.m) * sizeof(float);
-    dim3 grid(w.N, a.A1, w.M);
-    k_merit<<<grid, p->merit_threads, smem, st>>>(a);
-    cudaError_t e2 = cudaGetLastError();
-    if (e2 != cudaSuccess) return e2;
+    // the grid's z extent is limited to 65535: launch the solves in slices
+    for (int s0 = 0; s0 < w.M; s0 += 65535) {
+        a.sol0 = s0;
+        const int cnt = w.M - s0 < 65535 ? w.M - s0 : 65535;
+        dim3 grid(w.N, a.A1, cnt);
+        k_merit<<<grid, p->merit_threads, smem, st>>>(a);
+        cudaError_t e2 = cudaGetLastError();
+        if (e2 != cudaSuccess) return e2;
+    }
     k_merit_reduce<<<w.M, 32 * a.A1, 0, st>>>(w, a.A1, p->mu, merit, best, status);
     return cudaGetLastError();
 }
