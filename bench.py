@@ -333,8 +333,14 @@ def run_throughput_sweep(args, local):
                                         linsys=LINSYS["pcg"])
                 ms, stages, iters, bad = _time_solver(torch, s, p, d, out, args.steps, flush,
                                                       stream)
+                # one part: the PCG stage (solve) plus the refinement stage (its
+                # correction solve and small kernels) over the iterations of both;
+                # at M = 1 this is the latency of one iteration of one solve
+                pcg_us_it = (stages["linsys"] + stages["refine"]) / max(iters / M, 1.0)
                 print(json.dumps({"sweep": "throughput", "M": M, "N": N, "n": w.n, "m": w.m,
                                   "parts": s.get_parts(), "solves_per_s": M / (ms / 1000.0),
+                                  "pcg_us_per_iteration": pcg_us_it,
+                                  "pcg_warps_per_sm": max(2, (2 * N + 31) // 32),
                                   "ms_per_step": ms,
                                   "pcg_iters_per_sec": iters / (ms / 1000.0),
                                   "pcg_iters_per_solve": iters / M,
