@@ -484,3 +484,38 @@ def test_batch_beyond_the_grid_yz_limit():
         assert (np.abs(out["merit"] - ref["merit"]) <= TOL_MERIT * scale).all(), name
     assert not ref["status"].any()
     check_solution(prob, ref, [0, 35000, 65534, 65535, 69999])
+
+
+@pytest.mark.parametrize("w", [WORKLOADS[1], WORKLOADS[4]], ids=lambda w: w.name)
+def test_default_stop_rule_reaches_the_relative_residual(w):
+    """The default rule stops on ||gamma - S lambda|| <= eps ||gamma|| of the
+    updated residual: the true residual of the returned lambda, against the S
+    and gamma the GPU formed (exported, evaluated in fp64), stays within a
+    small multiple of eps, and the iteration count tracks the fp64 oracle's."""
+    M = 3
+    prob = make_batch(w, M=M)
+    p = params_for(w, refine_steps=0)
+    d = gato.to_device(prob)
+    N, n = w.N, w.n
+    f = dict(device="cuda", dtype=torch.float32)
+    with gato.Solver(M, N, n, w.m) as s:
+        o = s.outputs(p.n_alpha)
+        s.form_schur(d, o["status"])
+        s.pcg_solve(p, o["lam"], o["dX"], o["dU"], o["iters"], o["status"])
+        D = torch.empty(M, N, n, n, **f)
+        O = torch.empty(M, N - 1, n, n, **f)
+        g = torch.empty(M, N, n, **f)
+        s.get_schur(D, O, g)
+        torch.cuda.synchronize()
+        lam, iters = o["lam"].cpu().numpy(), o["iters"].cpu().numpy()
+        D, O, g = D.cpu().numpy(), O.cpu().numpy(), g.cpu().numpy()
+    assert not o["status"].cpu().numpy().any()
+    for j in range(M):
+        S = oracle.bt_dense(D[j], O[j])
+        gj = g[j].astype(np.float64).ravel()
+        res = np.linalg.norm(gj - S @ lam[j].astype(np.float64).ravel()) / np.linalg.norm(gj)
+        assert res <= 10 * w.pcg_eps, (j, res)
+        Dj, Oj, gam, _ = oracle.schur(oracle.solve_one(prob, j))
+        Pd, Po, _ = oracle.stair(Dj, Oj)
+        _, it, ok = oracle.pcg(Dj, Oj, Pd, Po, gam, w.pcg_eps, 5000, stop_rule=0)
+        assert ok and it * 0.9 - 3 <= int(iters[j]) <= it * 1.2 + 5, (j, it, iters[j])
