@@ -177,3 +177,31 @@ def test_call_in_parts_allocates_nothing_and_can_be_captured():
         g.replay()
         torch.cuda.synchronize()
         same({k: v.cpu().numpy() for k, v in cap.items()}, ref)
+
+
+def test_faults_stay_with_their_solve_across_parts():
+    """An indefinite Q in one solve and a NaN in another set status bits for
+    those solves only, the same in parts, through the host entry and as one
+    part; the other solves' outputs are unchanged."""
+    w = WORKLOADS[1]
+    M = 9
+    prob = make_batch(w, M=M)
+    bad = {k: v.copy() for k, v in prob.items()}
+    bad["Q"][4, 3] = -np.eye(w.n, dtype=np.float32)  # indefinite block: pivot <= 0
+    bad["q"][7, 5, 2] = np.nan
+    p = params_for(w)
+    with gato.Solver(M, w.N, w.n, w.m) as s:
+        clean = device_solve(s, p, prob, 1)
+        ref = device_solve(s, p, bad, 1)
+        dev = device_solve(s, p, bad, 3)
+        host = host_solve(s, p, bad, 3)
+    assert ref["status"][4] & gato.GATO_STATUS_NONPOSITIVE_PIVOT
+    assert ref["status"][7] & gato.GATO_STATUS_NONFINITE
+    others = [j for j in range(M) if j not in (4, 7)]
+    assert not ref["status"][others].any()
+    for k in ("dX", "dU", "lam", "merit", "best", "iters"):
+        assert np.array_equal(ref[k][others], clean[k][others]), k
+    for out in (dev, host):
+        assert np.array_equal(out["status"], ref["status"])
+        for k in ("dX", "dU", "lam", "merit", "best", "iters"):
+            assert np.array_equal(out[k], ref[k], equal_nan=True), k
