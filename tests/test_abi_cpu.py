@@ -39,6 +39,27 @@ def test_header_declares_the_abi():
         assert fn in names
 
 
+
+def header_constants():
+    """Every integer #define GATO_* of the header, its value evaluated from the
+    (parenthesised, unsigned-suffixed, multiplied) literal."""
+    out = {}
+    for name, expr in re.findall(r"^#define (GATO_\w+)[ \t]+([^/\n]+)", open(HEADER).read(), re.M):
+        expr = re.sub(r"(\d+)u\b", r"\1", expr.strip())
+        if re.fullmatch(r"[\d\s()*+-]+", expr):
+            out[name] = eval(expr)  # digits, parentheses and arithmetic only
+    return out
+
+
+def test_binding_constants_equal_the_header():
+    consts = header_constants()
+    assert len(consts) >= 30, sorted(consts)
+    missing = [k for k in consts if not hasattr(gato, k)]
+    assert not missing, missing
+    for k, v in consts.items():
+        assert getattr(gato, k) == v, (k, getattr(gato, k), v)
+
+
 def test_library_exports_every_declared_symbol(lib):
     missing = [fn for fn in declared_functions() if not hasattr(lib, fn)]
     assert not missing, missing

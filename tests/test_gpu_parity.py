@@ -169,6 +169,7 @@ CUSTOM = [
     ("N6_n40_m12_generic", 2, 6, 40, 12, 1),
     ("N130_n14_m7_generic", 1, 130, 14, 7, 1),
     ("N128_n12_m6_tile", 2, 128, 12, 6, 1),
+    ("N4_n64_m64_generic", 1, 4, 64, 64, 1),  # the largest state and control sizes
 ]
 WIDE = [c for c in CUSTOM if 7 <= c[3] <= 16 and c[2] <= 128] + [
     ("N33_n15_m4", 2, 33, 15, 4, 1), ("N5_n8_m3", 3, 5, 8, 3, 0)]
@@ -303,6 +304,34 @@ def test_merit_kernels_agree(w):
         assert np.abs(a["merit"][j] - b["merit"][j]).max() <= TOL_MERIT * scale
     np.testing.assert_array_equal(a["best"], b["best"])
     np.testing.assert_array_equal(a["dX"], b["dX"])
+
+
+
+# candidate counts 1..GATO_MAX_ALPHA, each merit kernel, on sizes that take the
+# per-knot kernel (n, m <= 16: instantiations for up to 9 and up to 32 values
+# of alpha) and the per-solve fused kernel (n > 16)
+MERIT_COUNTS = [(1, 2.0, 10.0), (8, 2.0, 10.0), (9, 1.5, 3.0), (20, 1.25, 0.5),
+                (gato.GATO_MAX_ALPHA, 2.0, 100.0)]
+
+
+@pytest.mark.parametrize("kernel", [gato.GATO_MERIT_FUSED, gato.GATO_MERIT_PER_CANDIDATE],
+                         ids=["fused", "per_candidate"])
+@pytest.mark.parametrize("M,N,n,m", [(3, 32, 12, 6), (2, 9, 20, 8)], ids=["n12", "n20"])
+@pytest.mark.parametrize("n_alpha,beta,mu", MERIT_COUNTS,
+                         ids=[f"A{c[0]}" for c in MERIT_COUNTS])
+def test_merit_candidate_counts(n_alpha, beta, mu, M, N, n, m, kernel):
+    """Merit values of alpha = 0 and alpha_i = beta^-i, i < n_alpha, and the
+    selected step against the oracle's line search on the GPU's own step."""
+    prob = random_lq(M, N, n, m, seed=700 + n_alpha + n)
+    out = solve(prob, gato.default_params(pcg_max_iters=3000, refine_steps=1, n_alpha=n_alpha,
+                                          beta=beta, mu=mu, merit_kernel=kernel))
+    assert out["merit"].shape == (M, n_alpha + 1)
+    assert not out["status"].any(), out["status"]
+    check_solution(prob, out, range(M), n_alpha, beta, mu)
+    for j in range(M):  # alpha = 0 in closed form: mu times the L1 norm of (s0, e)
+        ref0 = mu * (np.abs(prob["s0"][j]).astype(np.float64).sum()
+                     + np.abs(prob["e"][j]).astype(np.float64).sum())
+        assert abs(out["merit"][j, 0] - ref0) <= TOL_MERIT * ref0
 
 
 def test_deterministic_and_batch_position_invariant():

@@ -29,6 +29,10 @@ GATO_PCG_GENERIC = 1
 GATO_PCG_WIDE = 2
 GATO_PCG_TILE = 3
 GATO_MAX_PARTS = 8
+GATO_MAX_STATE = 64
+GATO_MAX_CONTROL = 64
+GATO_MAX_ALPHA = 31
+GATO_NOALLOC_MAX_BYTES = 32 * 1024 * 1024
 
 GATO_LINSYS_AUTO = 0
 GATO_LINSYS_PCG = 1
