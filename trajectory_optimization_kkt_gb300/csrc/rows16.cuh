@@ -17,27 +17,33 @@ namespace rows {
 
 constexpr int NP = 16;  // padded order
 
+// 128-bit chunks that hold the first P columns of a row
+template <int P>
+__host__ __device__ constexpr int chunks() { return (P + 3) / 4; }
+
 __device__ __forceinline__ float shfl16(float v, int src)
 {
     return __shfl_sync(0xffffffffu, v, src, 16);
 }
 
 // a[li] (runtime li) without dynamic register indexing
+template <int P = NP>
 __device__ __forceinline__ float pick(const float (&a)[NP], int li)
 {
     float v = 0.f;
 #pragma unroll
-    for (int j = 0; j < NP; ++j) v = (j == li) ? a[j] : v;
+    for (int j = 0; j < P; ++j) v = (j == li) ? a[j] : v;
     return v;
 }
 
 // Row li of a rows x cols row-major global matrix into a (zero beyond cols);
 // rows >= `rows` become identity rows when `ident`, zero rows otherwise.
+template <int P = NP>
 __device__ __forceinline__ void load_row(float (&a)[NP], const float* M, int rows, int cols,
                                          int li, bool ident)
 {
 #pragma unroll
-    for (int j = 0; j < NP; ++j) {
+    for (int j = 0; j < P; ++j) {
         float v = 0.f;
         if (li < rows) {
             if (j < cols) v = M[li * cols + j];
@@ -48,46 +54,54 @@ __device__ __forceinline__ void load_row(float (&a)[NP], const float* M, int row
     }
 }
 
+template <int P = NP>
 __device__ __forceinline__ void store_row(const float (&a)[NP], float* M, int rows, int cols,
                                           int li, float s = 1.f)
 {
     if (li < rows) {
 #pragma unroll
-        for (int j = 0; j < NP; ++j)
+        for (int j = 0; j < P; ++j)
             if (j < cols) M[li * cols + j] = s * a[j];
     }
 }
 
-// publish row li into the 16 x 16 scratch S (row stride 16)
+// publish the first P columns of row li into the 16 x 16 scratch S (row
+// stride 16; the rest of the last 128-bit chunk written as zeros)
+template <int P = NP>
 __device__ __forceinline__ void publish(const float (&a)[NP], float* S, int li)
 {
     float4* d = reinterpret_cast<float4*>(S + li * NP);
-    d[0] = make_float4(a[0], a[1], a[2], a[3]);
-    d[1] = make_float4(a[4], a[5], a[6], a[7]);
-    d[2] = make_float4(a[8], a[9], a[10], a[11]);
-    d[3] = make_float4(a[12], a[13], a[14], a[15]);
+#pragma unroll
+    for (int c = 0; c < chunks<P>(); ++c)
+        d[c] = make_float4(4 * c < P ? a[4 * c] : 0.f, 4 * c + 1 < P ? a[4 * c + 1] : 0.f,
+                           4 * c + 2 < P ? a[4 * c + 2] : 0.f, 4 * c + 3 < P ? a[4 * c + 3] : 0.f);
 }
 
+template <int P = NP>
 __device__ __forceinline__ void fetch(float (&b)[NP], const float* S, int k)
 {
     const float4* s = reinterpret_cast<const float4*>(S + k * NP);
-    const float4 s0 = s[0], s1 = s[1], s2 = s[2], s3 = s[3];
-    b[0] = s0.x; b[1] = s0.y; b[2] = s0.z; b[3] = s0.w;
-    b[4] = s1.x; b[5] = s1.y; b[6] = s1.z; b[7] = s1.w;
-    b[8] = s2.x; b[9] = s2.y; b[10] = s2.z; b[11] = s2.w;
-    b[12] = s3.x; b[13] = s3.y; b[14] = s3.z; b[15] = s3.w;
+#pragma unroll
+    for (int c = 0; c < chunks<P>(); ++c) {
+        const float4 t = s[c];
+        b[4 * c] = t.x;
+        b[4 * c + 1] = t.y;
+        b[4 * c + 2] = t.z;
+        b[4 * c + 3] = t.w;
+    }
 }
 
-// In-register Cholesky of diag(M, I) (M of order n): a becomes row li of L,
-// strict upper part zeroed.  A pivot <= 0 or not finite is flagged (false)
+// In-register Cholesky of diag(M, I) (M of order n <= P): a becomes row li of
+// L, strict upper part zeroed.  A pivot <= 0 or not finite is flagged (false)
 // and replaced by 1.  Column k of L reaches the other lanes through the
 // 32-float scratch col (two alternating 16-float buffers): one store per lane
-// and four broadcast 128-bit loads per step.
+// and broadcast 128-bit loads per step.
+template <int P = NP>
 __device__ inline bool rows_cholesky(float (&a)[NP], int li, int n, float* col)
 {
     bool ok = true;
 #pragma unroll
-    for (int k = 0; k < NP; ++k) {
+    for (int k = 0; k < P; ++k) {
         if (k < n) {
             const float d = shfl16(a[k], k);
             const bool bad = !(d > 0.f) || !isfinite(d);
@@ -99,113 +113,121 @@ __device__ inline bool rows_cholesky(float (&a)[NP], int li, int n, float* col)
             ck[li] = a[k];
             __syncwarp();
             float lk[NP];
-            fetch(lk, ck, 0);
+            fetch<P>(lk, ck, 0);
 #pragma unroll
-            for (int j = k + 1; j < NP; ++j)
+            for (int j = k + 1; j < P; ++j)
                 if (j < n && li >= j) a[j] -= a[k] * lk[j];
         }
     }
 #pragma unroll
-    for (int j = 0; j < NP; ++j)
+    for (int j = 0; j < P; ++j)
         if (j > li) a[j] = 0.f;
     return ok;
 }
 
-// x = row li of L^-1 (L lower, rows in a); the finished rows of L^-1 end up
-// in the scratch S.
+// x = row li of L^-1 (L lower of order n <= P, rows in a); the finished rows
+// of L^-1 end up in the scratch S.
+template <int P = NP>
 __device__ inline void rows_lower_inverse(const float (&a)[NP], float (&x)[NP], int li, int n,
                                           float* S)
 {
 #pragma unroll
-    for (int j = 0; j < NP; ++j) x[j] = (j == li) ? 1.f : 0.f;
-    const float inv_diag = 1.f / pick(a, li);
+    for (int j = 0; j < P; ++j) x[j] = (j == li) ? 1.f : 0.f;
+    const float inv_diag = 1.f / pick<P>(a, li);
 #pragma unroll
-    for (int k = 0; k < NP; ++k) {
+    for (int k = 0; k < P; ++k) {
         if (k < n) {
             if (li == k) {
 #pragma unroll
-                for (int j = 0; j < NP; ++j) x[j] *= inv_diag;
-                publish(x, S, k);
+                for (int j = 0; j < P; ++j) x[j] *= inv_diag;
+                publish<P>(x, S, k);
             }
             __syncwarp();
             if (li > k) {
                 float xk[NP];
-                fetch(xk, S, k);
+                fetch<P>(xk, S, k);
                 const float lik = a[k];
 #pragma unroll
-                for (int j = 0; j < NP; ++j) x[j] -= lik * xk[j];
+                for (int j = 0; j < P; ++j) x[j] -= lik * xk[j];
             }
         }
     }
-    if (li >= n) publish(x, S, li);  // identity rows, so S holds all of diag(L^-1, I)
+    if (li >= n) publish<P>(x, S, li);  // identity rows, so S holds all of diag(L^-1, I)
     __syncwarp();
 }
 
-// c = row li of X^T X, the rows of X in the scratch S (X lower triangular)
+// c = row li of X^T X, the rows of X in the scratch S (X lower triangular of
+// order n <= P)
+template <int P = NP>
 __device__ __forceinline__ void rows_gram_lower(const float* S, float (&c)[NP], int li, int n)
 {
 #pragma unroll
-    for (int j = 0; j < NP; ++j) c[j] = 0.f;
+    for (int j = 0; j < P; ++j) c[j] = 0.f;
 #pragma unroll
-    for (int k = 0; k < NP; ++k) {
+    for (int k = 0; k < P; ++k) {
         if (k < n && k >= li) {
             float xk[NP];
-            fetch(xk, S, k);
+            fetch<P>(xk, S, k);
             const float xki = S[k * NP + li];
 #pragma unroll
-            for (int j = 0; j < NP; ++j) c[j] += xki * xk[j];
+            for (int j = 0; j < P; ++j) c[j] += xki * xk[j];
         }
     }
 }
 
-// c = s * (row li of A) * B, B's rows (kk of them) in the scratch S
+// c = s * (row li of A) * B, B's rows (kk <= PK of them, PJ columns) in the
+// scratch S
+template <int PK = NP, int PJ = NP>
 __device__ __forceinline__ void rows_mul(const float (&a)[NP], const float* S, int kk,
                                          float (&c)[NP], float s)
 {
 #pragma unroll
-    for (int j = 0; j < NP; ++j) c[j] = 0.f;
+    for (int j = 0; j < PJ; ++j) c[j] = 0.f;
 #pragma unroll
-    for (int k = 0; k < NP; ++k) {
+    for (int k = 0; k < PK; ++k) {
         if (k < kk) {
             float bk[NP];
-            fetch(bk, S, k);
+            fetch<PJ>(bk, S, k);
             const float ak = s * a[k];
 #pragma unroll
-            for (int j = 0; j < NP; ++j) c[j] += ak * bk[j];
+            for (int j = 0; j < PJ; ++j) c[j] += ak * bk[j];
         }
     }
 }
 
-// c[j] += s * dot(row li of A, row j of B), B's rows (count of them) in S
+// c[j] += s * dot(row li of A, row j of B), B's rows (count <= PJ of them, PK
+// columns) in S
+template <int PK = NP, int PJ = NP>
 __device__ __forceinline__ void rows_mul_bt(const float (&a)[NP], const float* S, int count,
                                             float (&c)[NP], float s)
 {
 #pragma unroll
-    for (int j = 0; j < NP; ++j) {
+    for (int j = 0; j < PJ; ++j) {
         if (j < count) {
             float bj[NP];
-            fetch(bj, S, j);
+            fetch<PK>(bj, S, j);
             float d = 0.f;
 #pragma unroll
-            for (int k = 0; k < NP; ++k) d += a[k] * bj[k];
+            for (int k = 0; k < PK; ++k) d += a[k] * bj[k];
             c[j] += s * d;
         }
     }
 }
 
 // c += s * (A^T B)[li][:] = s * sum_k A[k][li] * (row k of B), the rows of A
-// in SA and those of B in SB (kk rows each)
+// in SA and those of B in SB (kk <= PK rows each, PJ columns of B)
+template <int PK = NP, int PJ = NP>
 __device__ __forceinline__ void rows_atb(const float* SA, const float* SB, int kk, int li,
                                          float (&c)[NP], float s)
 {
 #pragma unroll
-    for (int k = 0; k < NP; ++k) {
+    for (int k = 0; k < PK; ++k) {
         if (k < kk) {
             float bk[NP];
-            fetch(bk, SB, k);
+            fetch<PJ>(bk, SB, k);
             const float a = s * SA[k * NP + li];
 #pragma unroll
-            for (int j = 0; j < NP; ++j) c[j] += a * bk[j];
+            for (int j = 0; j < PJ; ++j) c[j] += a * bk[j];
         }
     }
 }
