@@ -40,7 +40,8 @@ struct Half {
     float* S2;
 };
 
-__device__ __forceinline__ Half half_setup(long items, float* sm)
+// a half's scratch: nmat 16 x 16 matrices (S0, S1, S2 as far as nmat goes)
+__device__ __forceinline__ Half half_setup(long items, float* sm, int nmat)
 {
     Half h;
     const int lane = lane_id(), warp = threadIdx.x >> 5;
@@ -48,9 +49,9 @@ __device__ __forceinline__ Half half_setup(long items, float* sm)
     h.li = lane & 15;
     h.item = (long)blockIdx.x * kKnotsPerBlock + half;
     h.active = h.item < items;
-    h.S0 = sm + (size_t)half * 3 * NP * NP;
-    h.S1 = h.S0 + NP * NP;
-    h.S2 = h.S1 + NP * NP;
+    h.S0 = sm + (size_t)half * nmat * NP * NP;
+    h.S1 = nmat > 1 ? h.S0 + NP * NP : nullptr;
+    h.S2 = nmat > 2 ? h.S0 + 2 * NP * NP : nullptr;
     return h;
 }
 
@@ -64,7 +65,7 @@ __global__ void __launch_bounds__(256, 3) k_rows_knot(Work w, const float* __res
 {
     extern __shared__ __align__(16) float sm[];
     const int n = w.n, m = w.m, N = w.N;
-    const Half h = half_setup((long)w.M * N, sm);
+    const Half h = half_setup((long)w.M * N, sm, 3);
     // inactive halves run the same code on identity data so that every lane
     // of the warp takes part in the shuffles and barriers; they store nothing
     const long item = h.active ? h.item : 0;
@@ -150,7 +151,7 @@ __global__ void __launch_bounds__(256) k_rows_diag(Work w, uint32_t* status)
 {
     extern __shared__ __align__(16) float sm[];
     const int n = w.n, N = w.N;
-    const Half h = half_setup((long)w.M * N, sm);
+    const Half h = half_setup((long)w.M * N, sm, 1);
     const long item = h.active ? h.item : 0;
     const int sol = (int)(item / N), j = (int)(item % N);
     const int li = h.li;
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(256) k_rows_off(Work w)
 {
     extern __shared__ __align__(16) float sm[];
     const int n = w.n, N = w.N, K = N - 1;
-    const Half h = half_setup((long)w.M * K, sm);
+    const Half h = half_setup((long)w.M * K, sm, 2);
     const long item = h.active ? h.item : 0;
     const int sol = (int)(item / K), j = 1 + (int)(item % K);
     const int li = h.li;
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(256) k_rows_phi_diag(Work w)
 {
     extern __shared__ __align__(16) float sm[];
     const int n = w.n, N = w.N;
-    const Half h = half_setup((long)w.M * N, sm);
+    const Half h = half_setup((long)w.M * N, sm, 1);
     const long item = h.active ? h.item : 0;
     const int sol = (int)(item / N), j = (int)(item % N);
     const int li = h.li;
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(256) k_rows_phi_off(Work w)
 {
     extern __shared__ __align__(16) float sm[];
     const int n = w.n, N = w.N, K = N - 1;
-    const Half h = half_setup((long)w.M * K, sm);
+    const Half h = half_setup((long)w.M * K, sm, 2);
     const long item = h.active ? h.item : 0;
     const int sol = (int)(item / K), j = 1 + (int)(item % K);
     const int li = h.li;
@@ -260,11 +261,12 @@ __global__ void __launch_bounds__(256) k_rows_phi_off(Work w)
     if (h.active) store_row<PN>(r, w.Po + oj, n, n, li);
 }
 
+// nmat: the kernel's scratch matrices per half-warp (16 KB per block each)
 template <typename K, typename... Args>
-cudaError_t launch_rows(K kernel, long items, cudaStream_t st, Args... args)
+cudaError_t launch_rows(K kernel, int nmat, long items, cudaStream_t st, Args... args)
 {
     if (items <= 0) return cudaSuccess;
-    const size_t smem = (size_t)kKnotsPerBlock * 3 * NP * NP * sizeof(float);  // 48 KB
+    const size_t smem = (size_t)kKnotsPerBlock * nmat * NP * NP * sizeof(float);
     const long blocks = (items + kKnotsPerBlock - 1) / kKnotsPerBlock;
     kernel<<<(unsigned)blocks, 256, smem, st>>>(args...);
     return cudaGetLastError();
@@ -279,9 +281,9 @@ namespace {
 template <int PN>
 cudaError_t form_phi_w(const Work& w, cudaStream_t st)
 {
-    cudaError_t e = launch_rows(k_rows_phi_diag<PN>, (long)w.M * w.N, st, w);
+    cudaError_t e = launch_rows(k_rows_phi_diag<PN>, 1, (long)w.M * w.N, st, w);
     if (e != cudaSuccess) return e;
-    return launch_rows(k_rows_phi_off<PN>, (long)w.M * (w.N - 1), st, w);
+    return launch_rows(k_rows_phi_off<PN>, 2, (long)w.M * (w.N - 1), st, w);
 }
 
 template <int PN, int PM>
@@ -289,11 +291,11 @@ cudaError_t form_rows_w(const Work& w, const float* Q, const float* R, const flo
                         const float* B, uint32_t* status, cudaStream_t st)
 {
     const long knots = (long)w.M * w.N;
-    cudaError_t e = launch_rows(k_rows_knot<PN, PM>, knots, st, w, Q, R, A, B, status);
+    cudaError_t e = launch_rows(k_rows_knot<PN, PM>, 3, knots, st, w, Q, R, A, B, status);
     if (e != cudaSuccess) return e;
-    e = launch_rows(k_rows_diag<PN>, knots, st, w, status);
+    e = launch_rows(k_rows_diag<PN>, 1, knots, st, w, status);
     if (e != cudaSuccess) return e;
-    return launch_rows(k_rows_off<PN>, (long)w.M * (w.N - 1), st, w);
+    return launch_rows(k_rows_off<PN>, 2, (long)w.M * (w.N - 1), st, w);
 }
 
 template <int PN>

@@ -131,6 +131,7 @@ template <int P = NP>
 __device__ inline void rows_lower_inverse(const float (&a)[NP], float (&x)[NP], int li, int n,
                                           float* S)
 {
+    __syncwarp();  // S may still be read by the routine before (rows_cholesky's column)
 #pragma unroll
     for (int j = 0; j < P; ++j) x[j] = (j == li) ? 1.f : 0.f;
     const float inv_diag = 1.f / pick<P>(a, li);
