@@ -116,6 +116,10 @@ FORM_CASES = [(w.name, make_batch(w, M=min(w.M, 6))) for w in WORKLOADS] + [
     ("N1_n14", random_lq(2, 1, 14, 7, seed=502)),
     ("n3_m2", random_lq(2, 11, 3, 2, seed=503)),
     ("n64_m64", random_lq(1, 4, 64, 64, seed=504)),
+    # register-row widths: controls wider than 8 (PM = 16) and every state width
+    ("n9_m12", random_lq(2, 9, 9, 12, seed=505)),
+    ("n16_m16", random_lq(2, 6, 16, 16, seed=506)),
+    ("n11_m9", random_lq(2, 13, 11, 9, seed=507)),
 ]
 
 
@@ -170,6 +174,8 @@ CUSTOM = [
     ("N130_n14_m7_generic", 1, 130, 14, 7, 1),
     ("N128_n12_m6_tile", 2, 128, 12, 6, 1),
     ("N4_n64_m64_generic", 1, 4, 64, 64, 1),  # the largest state and control sizes
+    ("N9_n9_m12", 2, 9, 9, 12, 1),  # controls wider than the state
+    ("N7_n16_m16", 2, 7, 16, 16, 1),
 ]
 WIDE = [c for c in CUSTOM if 7 <= c[3] <= 16 and c[2] <= 128] + [
     ("N33_n15_m4", 2, 33, 15, 4, 1), ("N5_n8_m3", 3, 5, 8, 3, 0)]

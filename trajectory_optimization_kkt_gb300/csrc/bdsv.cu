@@ -83,27 +83,31 @@ __host__ __device__ __forceinline__ int even_multiples(int N, int s)
 
 // row li of block idx (n x n at base + idx n^2) when valid, else the zero
 // row or, with ident, the identity row
+template <int P>
 __device__ __forceinline__ void load_blk(float (&a)[NP], const float* base, int idx, bool valid,
                                          int n, int li, bool ident)
 {
     if (valid) {
-        load_row(a, base + (size_t)idx * n * n, n, n, li, ident);
+        load_row<P>(a, base + (size_t)idx * n * n, n, n, li, ident);
     } else {
 #pragma unroll
-        for (int j = 0; j < NP; ++j) a[j] = (ident && j == li) ? 1.f : 0.f;
+        for (int j = 0; j < P; ++j) a[j] = (ident && j == li) ? 1.f : 0.f;
     }
 }
 
+template <int P>
 __device__ __forceinline__ void set_row(float (&c)[NP], int li, float diag)
 {
 #pragma unroll
-    for (int j = 0; j < NP; ++j) c[j] = (j == li) ? diag : 0.f;
+    for (int j = 0; j < P; ++j) c[j] = (j == li) ? diag : 0.f;
 }
 
 // One solve per block of 256 threads (16 half-warps).  Every phase runs in
 // rounds that all half-warps take part in (uniform control flow for the
 // shuffles); a half-warp without a knot in a round computes on zero or
-// identity rows and stores nothing.
+// identity rows and stores nothing.  Rows are PN >= n columns wide (the
+// columns past n are padding zeros).
+template <int PN>
 __global__ void __launch_bounds__(256) k_bdsv_cr_factor_rows(Work w, uint32_t* status)
 {
     extern __shared__ __align__(16) float sm[];
@@ -128,22 +132,22 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_factor_rows(Work w, uint32_t* s
             const int i = act ? 2 * k : 0;
             float a[NP], c[NP], t[NP], tl[NP];
             // all of the round's loads first: one memory latency per round
-            load_blk(a, b.nh, i - 1, act && i >= 1, n, li, false);
-            load_blk(t, b.nh, i, act && i + 1 < N, n, li, false);
-            load_blk(tl, b.nh, i - 2, act && i >= 2, n, li, false);
+            load_blk<PN>(a, b.nh, i - 1, act && i >= 1, n, li, false);
+            load_blk<PN>(t, b.nh, i, act && i + 1 < N, n, li, false);
+            load_blk<PN>(tl, b.nh, i - 2, act && i >= 2, n, li, false);
             __syncwarp();
-            publish(a, S0, li);
-            publish(t, S1, li);
+            publish<PN>(a, S0, li);
+            publish<PN>(t, S1, li);
             __syncwarp();
-            set_row(c, li, 1.f);
-            rows_mul_bt(a, S0, n, c, -1.f);
-            rows_atb(S1, S1, n, li, c, -1.f);
-            if (act) store_row(c, b.D(i), n, n, li);
+            set_row<PN>(c, li, 1.f);
+            rows_mul_bt<PN, PN>(a, S0, n, c, -1.f);
+            rows_atb<PN, PN>(S1, S1, n, li, c, -1.f);
+            if (act) store_row<PN>(c, b.D(i), n, n, li);
             __syncwarp();
-            publish(tl, S1, li);
+            publish<PN>(tl, S1, li);
             __syncwarp();
-            rows_mul(a, S1, n, c, -1.f);
-            if (act && i >= 2) store_row(c, b.E(i), n, n, li);
+            rows_mul<PN, PN>(a, S1, n, c, -1.f);
+            if (act && i >= 2) store_row<PN>(c, b.E(i), n, n, li);
         }
     }
     __syncthreads();
@@ -157,23 +161,23 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_factor_rows(Work w, uint32_t* s
             const int j = act ? (2 * k + 1) * s : 0;
             const bool right = act && j + s < N;
             float d[NP], x[NP], e[NP], er[NP], c[NP];
-            load_blk(d, b.bd, j, act, n, li, true);
-            load_blk(e, b.be, j, act, n, li, false);
-            load_blk(er, b.be, j + s, right, n, li, false);
+            load_blk<PN>(d, b.bd, j, act, n, li, true);
+            load_blk<PN>(e, b.be, j, act, n, li, false);
+            load_blk<PN>(er, b.be, j + s, right, n, li, false);
             __syncwarp();
-            publish(e, S1, li);
-            const bool okj = rows_cholesky(d, li, n, S0);
+            publish<PN>(e, S1, li);
+            const bool okj = rows_cholesky<PN>(d, li, n, S0);
             ok = ok && (okj || !act);
-            rows_lower_inverse(d, x, li, n, S0);  // x: row li of F (ends with __syncwarp)
-            if (act) store_row(x, b.D(j), n, n, li);
-            rows_mul(x, S1, n, c, 1.f);  // X = F E_j
-            if (act) store_row(c, b.E(j), n, n, li);
+            rows_lower_inverse<PN>(d, x, li, n, S0);  // x: row li of F (ends with __syncwarp)
+            if (act) store_row<PN>(x, b.D(j), n, n, li);
+            rows_mul<PN, PN>(x, S1, n, c, 1.f);  // X = F E_j
+            if (act) store_row<PN>(c, b.E(j), n, n, li);
             __syncwarp();
-            publish(er, S1, li);
+            publish<PN>(er, S1, li);
             __syncwarp();
-            set_row(c, li, 0.f);
-            rows_mul_bt(x, S1, n, c, 1.f);  // Y = F E_{j+s}^T
-            if (right) store_row(c, b.Y(j), n, n, li);
+            set_row<PN>(c, li, 0.f);
+            rows_mul_bt<PN, PN>(x, S1, n, c, 1.f);  // Y = F E_{j+s}^T
+            if (right) store_row<PN>(c, b.Y(j), n, n, li);
         }
         __syncthreads();
         // update the even multiples i of s
@@ -184,23 +188,23 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_factor_rows(Work w, uint32_t* s
             const int i = act ? 2 * k * s : 0;
             const bool far = act && i >= 2 * s;
             float c[NP], y[NP], t[NP], tl[NP];
-            load_blk(c, b.bd, i, act, n, li, false);
-            load_blk(y, b.by, i - s, act && i >= s, n, li, false);
-            load_blk(t, b.be, i + s, act && i + s < N, n, li, false);
-            load_blk(tl, b.be, i - s, far, n, li, false);
+            load_blk<PN>(c, b.bd, i, act, n, li, false);
+            load_blk<PN>(y, b.by, i - s, act && i >= s, n, li, false);
+            load_blk<PN>(t, b.be, i + s, act && i + s < N, n, li, false);
+            load_blk<PN>(tl, b.be, i - s, far, n, li, false);
             __syncwarp();
-            publish(y, S0, li);
-            publish(t, S1, li);
+            publish<PN>(y, S0, li);
+            publish<PN>(t, S1, li);
             __syncwarp();
-            rows_atb(S0, S0, n, li, c, -1.f);  // - Y_{i-s}^T Y_{i-s}
-            rows_atb(S1, S1, n, li, c, -1.f);  // - X_{i+s}^T X_{i+s}
-            if (act) store_row(c, b.D(i), n, n, li);
+            rows_atb<PN, PN>(S0, S0, n, li, c, -1.f);  // - Y_{i-s}^T Y_{i-s}
+            rows_atb<PN, PN>(S1, S1, n, li, c, -1.f);  // - X_{i+s}^T X_{i+s}
+            if (act) store_row<PN>(c, b.D(i), n, n, li);
             __syncwarp();
-            publish(tl, S1, li);
+            publish<PN>(tl, S1, li);
             __syncwarp();
-            set_row(c, li, 0.f);
-            rows_atb(S0, S1, n, li, c, -1.f);  // E' = -Y_{i-s}^T X_{i-s}
-            if (far) store_row(c, b.E(i), n, n, li);
+            set_row<PN>(c, li, 0.f);
+            rows_atb<PN, PN>(S0, S1, n, li, c, -1.f);  // E' = -Y_{i-s}^T X_{i-s}
+            if (far) store_row<PN>(c, b.E(i), n, n, li);
         }
         __syncthreads();
     }
@@ -209,11 +213,11 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_factor_rows(Work w, uint32_t* s
     if (warp == 0) {
         const bool act = half == 0;
         float d[NP], x[NP];
-        load_blk(d, b.bd, 0, act, n, li, true);
-        const bool ok0 = rows_cholesky(d, li, n, S0);
+        load_blk<PN>(d, b.bd, 0, act, n, li, true);
+        const bool ok0 = rows_cholesky<PN>(d, li, n, S0);
         ok = ok && (ok0 || !act);
-        rows_lower_inverse(d, x, li, n, S0);
-        if (act) store_row(x, b.D(0), n, n, li);
+        rows_lower_inverse<PN>(d, x, li, n, S0);
+        if (act) store_row<PN>(x, b.D(0), n, n, li);
     }
     if (!ok && li == 0) atomicOr(status + sol, GATO_STATUS_NONPOSITIVE_PIVOT);
 }
@@ -556,7 +560,11 @@ cudaError_t launch_bdsv_factor(gato_handle* h, int order, uint32_t* status, cuda
     }
     if (h->bdsv_kernel != GATO_BDSV_KERNEL_SHARED && w.n <= NP) {
         const size_t smem = (kRowsThreads / 16) * 2 * NP * NP * sizeof(float);  // 32 KB
-        return launch(k_bdsv_cr_factor_rows, (unsigned)w.M, kRowsThreads, smem, st, w, status);
+        auto kernel = w.n <= 8    ? k_bdsv_cr_factor_rows<8>
+                      : w.n <= 12 ? k_bdsv_cr_factor_rows<12>
+                      : w.n <= 14 ? k_bdsv_cr_factor_rows<14>
+                                  : k_bdsv_cr_factor_rows<16>;
+        return launch(kernel, (unsigned)w.M, kRowsThreads, smem, st, w, status);
     }
     int nw = (int)(limit / per_warp);
     if (nw > kSmemWarps) nw = kSmemWarps;
@@ -583,14 +591,23 @@ cudaError_t launch_bdsv_solve(gato_handle* h, int order, int set, float* lambda,
     // recovery needs its N n scratch in shared memory only when the vectors
     // are there too; otherwise it uses Bg in global memory
     const size_t smem = a.vec_smem ? vec : 0;
-    const bool small = w.n <= NP;
-    if (order == GATO_LINSYS_BDSV_CHRONO)
-        return small ? launch(k_bdsv_chrono_solve<NP>, (unsigned)w.M, kChronoSolveThreads, smem,
-                              st, a)
-                     : launch(k_bdsv_chrono_solve<0>, (unsigned)w.M, kChronoSolveThreads, smem,
-                              st, a);
-    return small ? launch(k_bdsv_cr_solve<NP>, (unsigned)w.M, kSolveThreads, smem, st, a)
-                 : launch(k_bdsv_cr_solve<0>, (unsigned)w.M, kSolveThreads, smem, st, a);
+    // the row products unrolled to the state width (8, 12, 14 or 16), or
+    // looped beyond 16
+    const unsigned M = (unsigned)w.M;
+    if (order == GATO_LINSYS_BDSV_CHRONO) {
+        auto kernel = w.n <= 8    ? k_bdsv_chrono_solve<8>
+                      : w.n <= 12 ? k_bdsv_chrono_solve<12>
+                      : w.n <= 14 ? k_bdsv_chrono_solve<14>
+                      : w.n <= NP ? k_bdsv_chrono_solve<NP>
+                                  : k_bdsv_chrono_solve<0>;
+        return launch(kernel, M, kChronoSolveThreads, smem, st, a);
+    }
+    auto kernel = w.n <= 8    ? k_bdsv_cr_solve<8>
+                  : w.n <= 12 ? k_bdsv_cr_solve<12>
+                  : w.n <= 14 ? k_bdsv_cr_solve<14>
+                  : w.n <= NP ? k_bdsv_cr_solve<NP>
+                              : k_bdsv_cr_solve<0>;
+    return launch(kernel, M, kSolveThreads, smem, st, a);
 }
 
 }  // namespace gato

@@ -226,7 +226,9 @@ __device__ __forceinline__ void rows_atb(const float* SA, const float* SB, int k
         if (k < kk) {
             float bk[NP];
             fetch<PJ>(bk, SB, k);
-            const float a = s * SA[k * NP + li];
+            // rows of SA were published PJ columns wide: lanes past that hold
+            // padding rows of the result
+            const float a = li < PJ ? s * SA[k * NP + li] : 0.f;
 #pragma unroll
             for (int j = 0; j < PJ; ++j) c[j] += a * bk[j];
         }
