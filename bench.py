@@ -351,6 +351,75 @@ def run_throughput_sweep(args, local):
                       flush=True)
 
 
+def run_merit_sweep(args, local):
+    """The merit variants (the GATO line-search table's fused / unfused
+    comparison): device microseconds per gato_linesearch call for the factored
+    default (one launch) and the per-candidate kernel (one block per (knot,
+    candidate), then the reduction) at 32, 64, 128 and 256 threads, over
+    (n, m) in {(12, 6), (14, 7), (36, 12)}, N in {16, 32, 64, 128} and M in
+    {1, 8, 16, 256}.  Twenty calls are recorded in a CUDA graph and replayed,
+    so the time is the device's per call without the host's call overhead;
+    the inputs stay in L2 from one call to the next.  One JSON line per
+    cell."""
+    import torch
+
+    from trajectory_optimization_kkt_gb300 import _build, gato
+    from trajectory_optimization_kkt_gb300.workloads import normals, random_lq
+    torch.cuda.set_device(local)
+    _build.build()
+    dev = torch.device("cuda", local)
+    calls, reps = 20, 5
+
+    def per_call_us(s, p, d, dX, dU, out):
+        def run():
+            for _ in range(calls):
+                s.linesearch(p, d, dX, dU, out["merit"], out["best"], out["status"])
+        run()  # loads the kernels before the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            run()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        b.synchronize()
+        return a.elapsed_time(b) * 1000.0 / (calls * reps)
+
+    for n, m in ((12, 6), (14, 7), (36, 12)):
+        for N in (16, 32, 64, 128):
+            for M in (1, 8, 16, 256):
+                prob = random_lq(M, N, n, m, seed=4000 + N + M)
+                d = {k: torch.from_numpy(v).to(dev) for k, v in prob.items()}
+                # a step of the problem's size (the kernels' time does not
+                # depend on its values)
+                dX = torch.from_numpy(0.1 * normals(5000 + N + M, 1, M * N * n)
+                                      .reshape(M, N, n).astype(np.float32)).to(dev)
+                dU = torch.from_numpy(0.1 * normals(5000 + N + M, 2, M * (N - 1) * m)
+                                      .reshape(M, N - 1, m).astype(np.float32)).to(dev)
+                row = {"sweep": "merit", "n": n, "m": m, "N": N, "M": M, "n_alpha": 8}
+                with gato.Solver(M, N, n, m) as s:
+                    out = s.outputs(8)
+                    p = gato.default_params(merit_kernel=gato.GATO_MERIT_FUSED)
+                    row["fused_us"] = per_call_us(s, p, d, dX, dU, out)
+                    row["fused_kernel"] = ("k_merit_knots" if n <= 16 and m <= 16
+                                           else "k_merit_fused")
+                    unf = {}
+                    for t in (32, 64, 128, 256):
+                        p = gato.default_params(merit_kernel=gato.GATO_MERIT_PER_CANDIDATE,
+                                                merit_threads=t)
+                        unf[str(t)] = per_call_us(s, p, d, dX, dU, out)
+                row["per_candidate_us"] = unf
+                best = min(unf.values())
+                row["fused_over_unfused_256"] = row["fused_us"] / unf["256"]
+                row["fused_over_best_unfused"] = row["fused_us"] / best
+                row["knot_candidates_per_s_fused"] = M * N * 9 / (row["fused_us"] * 1e-6)
+                print(json.dumps(row), flush=True)
+
+
 def _sqp_timing(torch, gato, model_np, M, iters, linsys, use_graph, dev, stream, flush, reps=3):
     """Device ms per SQP iteration of a batch of M problems (after one
     untimed call that records the graph), and the last call's outputs."""
@@ -677,6 +746,9 @@ def main():
                     help="horizon x batch sweep of the three linear solvers instead")
     ap.add_argument("--throughput-sweep", action="store_true",
                     help="the workload's M x N throughput sweep (solves/s, merit us) instead")
+    ap.add_argument("--merit-sweep", action="store_true",
+                    help="the merit variants' sweep (fused / per-candidate at 32-256 "
+                         "threads) instead")
     ap.add_argument("--sqp-study", action="store_true",
                     help="the rho-damping SQP case study on the linear model instead")
     ap.add_argument("--batch", type=int, default=None,
@@ -690,6 +762,8 @@ def main():
         run_sweep(args, local)
     elif args.throughput_sweep:
         run_throughput_sweep(args, local)
+    elif args.merit_sweep:
+        run_merit_sweep(args, local)
     elif args.sqp_study:
         run_sqp_study(args, local)
     else:
