@@ -16,12 +16,15 @@
 //   k_rows_diag  row j:   S_jj = Q_j^-1 + theta_{j-1}, L_j, L_j^-1 and the
 //                         eigenvalue bound 1 / ||L_j^-1||_F^2
 //   k_rows_off   row j:   Nhat_j = L_j^-1 S_{j,j-1} L_{j-1}^-T
-// Every kernel is compiled for column widths PN >= n and PM >= m (8, 12, 14
-// or 16; 8 or 16): columns past the width are padding zeros, so the narrower
-// rows do the same arithmetic on the real entries with fewer operations.
 // The solve applies Phi^-1 in that factored form; the explicit blocks
 // S_jj^-1 and -S_jj^-1 S_{j,j-1} S_{j-1,j-1}^-1 are formed only for export
 // (k_rows_phi_diag, k_rows_phi_off, launched by gato_get_schur).
+//
+// Every kernel is compiled for column widths PN >= n (8, 12, 14 or 16) and
+// PM >= m (8 or 16), and its row routines touch only that many columns.  The
+// columns from n (or m) up to the width are padding zeros, whose products add
+// exact zeros, so the results equal those of 16-wide rows with fewer
+// operations.
 #include "rows16.cuh"
 
 namespace gato {
