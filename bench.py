@@ -351,6 +351,63 @@ def run_throughput_sweep(args, local):
                       flush=True)
 
 
+def run_workloads(args, local):
+    """The five synthetic workloads at their own sizes and settings: solves/s
+    and PCG iterations/s of whole gato_solve_kkt calls (default parts, L2
+    flushed before each), the PCG stage against the fp32 FMA roofline and the
+    merit against measured HBM (from the one-part stage pass), next to the
+    fp64 oracle on the host's cores for the same batch.  One JSON line per
+    workload."""
+    import torch
+
+    from trajectory_optimization_kkt_gb300 import _build, gato
+    from trajectory_optimization_kkt_gb300.workloads import WORKLOADS, make_batch
+    torch.cuda.set_device(local)
+    _build.build()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    hbm_peak, peak_kind, sm_mhz = _peaks()
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak_tf = n_sm * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    steps = min(args.steps, 10)
+    for w in WORKLOADS:
+        M, N, n, m = w.M, w.N, w.n, w.m
+        prob = make_batch(w)
+        d = {k: torch.from_numpy(v).to(dev) for k, v in prob.items()}
+        p = gato.default_params(pcg_eps=w.pcg_eps, pcg_max_iters=w.pcg_max_iters,
+                                n_alpha=w.n_alpha, beta=w.beta, mu=w.mu,
+                                refine_steps=w.refine_steps, refine_eps=w.refine_eps)
+        with gato.Solver(M, N, n, m) as s:
+            out = s.outputs(w.n_alpha)
+            ms, stages, iters, bad = _time_solver(torch, s, p, d, out, steps, flush, stream)
+            parts = s.get_parts()
+        flops_it = 2 * 2 * (3 * N - 2) * n * n + 12 * N * n
+        pcg_us = stages["linsys"] + stages["refine"]
+        achieved_tf = flops_it * iters / (pcg_us * 1e-6) / 1e12
+        K = N - 1
+        merit_bytes = 4 * M * (N * n * n + K * (m * m + n * n + n * m) + N * n + K * m + K * n
+                               + n + N * n + K * m + (w.n_alpha + 1) + 1)
+        merit_gbs = merit_bytes / (stages["merit"] * 1e-6) / 1e9
+        pcg_kernel = ("k_pcg_wide" if 7 <= n <= 16 and N <= 128 else
+                      "k_pcg_cluster" if 7 <= n <= 16 else "k_pcg_generic")
+        row = {"workload": w.name, "M": M, "N": N, "n": n, "m": m, "parts": parts,
+               "solves_per_s": M / (ms / 1000.0), "ms_per_call": ms,
+               "pcg_iters_per_sec": iters / (ms / 1000.0), "pcg_iters_per_solve": iters / M,
+               "stage_us": stages, "status_nonzero_solves": bad,
+               "pcg_roofline": {"bound": "alu", "kernel": pcg_kernel, "achieved": achieved_tf,
+                                "peak": alu_peak_tf, "unit": "TFLOP/s",
+                                "frac": achieved_tf / alu_peak_tf},
+               "merit_roofline": {"bound": "hbm", "achieved": merit_gbs, "peak": hbm_peak,
+                                  "unit": "GB/s", "frac": merit_gbs / hbm_peak,
+                                  "peak_kind": peak_kind,
+                                  "knot_candidates_per_s":
+                                      M * N * (w.n_alpha + 1) / (stages["merit"] * 1e-6)}}
+        if not args.no_cpu_baseline:
+            row["cpu_baseline"] = _cpu_baseline(w)
+        print(json.dumps(row), flush=True)
+
+
 def run_merit_sweep(args, local):
     """The merit variants (the GATO line-search table's fused / unfused
     comparison): device microseconds per gato_linesearch call for the factored
@@ -746,6 +803,9 @@ def main():
                     help="horizon x batch sweep of the three linear solvers instead")
     ap.add_argument("--throughput-sweep", action="store_true",
                     help="the workload's M x N throughput sweep (solves/s, merit us) instead")
+    ap.add_argument("--workloads", action="store_true",
+                    help="the five synthetic workloads at their own sizes, each next to the "
+                         "oracle on the host's cores, instead")
     ap.add_argument("--merit-sweep", action="store_true",
                     help="the merit variants' sweep (fused / per-candidate at 32-256 "
                          "threads) instead")
@@ -762,6 +822,8 @@ def main():
         run_sweep(args, local)
     elif args.throughput_sweep:
         run_throughput_sweep(args, local)
+    elif args.workloads:
+        run_workloads(args, local)
     elif args.merit_sweep:
         run_merit_sweep(args, local)
     elif args.sqp_study:

@@ -75,14 +75,21 @@ extern "C" {
 /* PCG kernel selection (gato_set_pcg_kernel) */
 #define GATO_PCG_AUTO 0            /* for 7 <= n <= 16 the wide-tile kernel when
                                       N <= 128 and the cluster kernel (2 or 4
-                                      CTAs per solve) when 128 < N <= 512; else
-                                      the generic kernel                          */
+                                      CTAs per solve) when 128 < N <= 512; for
+                                      16 < n <= 64 the register-row kernel when
+                                      its block fits (N ceil(n/R) threads within
+                                      the register budget: N <= 17 at n = 36);
+                                      else the generic kernel                     */
 #define GATO_PCG_GENERIC 1         /* always the generic kernel                   */
 #define GATO_PCG_WIDE 2            /* the wide-tile kernel (two threads per
                                       coupling block, rows over all 2H columns)
                                       where it applies, else as GATO_PCG_AUTO     */
 #define GATO_PCG_TILE 3            /* the four-thread tile kernel (H x H tiles)
                                       where it applies, else as GATO_PCG_AUTO     */
+#define GATO_PCG_ROWS 4            /* the register-row kernel (whole rows of the
+                                      two coupling blocks around a knot per
+                                      thread) for any n <= 64 where its block
+                                      fits, else as GATO_PCG_AUTO                 */
 
 /* Linear solver of S lambda = gamma (gato_params.linsys).  The direct solver
  * (bdsv) factors the block-tridiagonal S exactly instead of iterating; the
@@ -191,8 +198,8 @@ int gato_set_timing(gato_handle* h, int on);
 /* Stage times of the last call (see gato_stats). */
 int gato_get_stats(gato_handle* h, gato_stats* out);
 
-/* Chooses the PCG kernel (GATO_PCG_AUTO, GATO_PCG_GENERIC, GATO_PCG_WIDE or
- * GATO_PCG_TILE) for later calls.
+/* Chooses the PCG kernel (GATO_PCG_AUTO, GATO_PCG_GENERIC, GATO_PCG_WIDE,
+ * GATO_PCG_TILE or GATO_PCG_ROWS) for later calls.
  * Both give the same PCG iterates up to rounding; the generic kernel covers
  * every supported size.  Errors: INVALID_ARG. */
 int gato_set_pcg_kernel(gato_handle* h, int kind);

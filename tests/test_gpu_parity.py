@@ -224,6 +224,59 @@ def test_cluster_kernel_long_horizons(name, M, N, n, m):
         assert rel(out["lam"][j], ref["lam"][j]) < 1e-3
 
 
+# the register-row kernel (16 < n <= 64, and any n when chosen): every row
+# width instantiation, ragged rows per thread, N = 1, and a block too large
+# for it (the default then takes the generic kernel)
+ROWS = [
+    ("n17_m5", 3, 9, 17, 5), ("n20_m20", 2, 10, 20, 20), ("n24_m8", 2, 12, 24, 8),
+    ("n27_m9", 2, 11, 27, 9), ("n32_m4", 2, 8, 32, 4), ("n36_m12", 2, 16, 36, 12),
+    ("n40_m10", 1, 6, 40, 10), ("n45_m7", 1, 5, 45, 7), ("n53_m3", 1, 4, 53, 3),
+    ("n64_m16", 1, 4, 64, 16), ("N1_n36", 2, 1, 36, 12), ("n36_N40_generic", 1, 40, 36, 12),
+]
+
+
+@pytest.mark.parametrize("name,M,N,n,m", ROWS, ids=[c[0] for c in ROWS])
+def test_rows_kernel_matches_oracle_and_generic(name, M, N, n, m):
+    prob = random_lq(M, N, n, m, seed=800 + N + n)
+    p = gato.default_params(pcg_max_iters=5000, refine_steps=1)
+    out = solve(prob, p)
+    assert not out["status"].any(), out["status"]
+    check_solution(prob, out, range(M))
+    ref = solve(prob, p, gato.GATO_PCG_GENERIC)
+    assert np.abs(out["iters"] - ref["iters"]).max() <= 0.05 * ref["iters"].max() + 2
+    for j in range(M):
+        assert rel(out["lam"][j], ref["lam"][j]) < 1e-3
+
+
+@pytest.mark.parametrize("rule", [gato.GATO_STOP_RESIDUAL, gato.GATO_STOP_PRECOND,
+                                  gato.GATO_STOP_SCALED], ids=["residual", "precond", "scaled"])
+def test_rows_kernel_stopping_rules(rule):
+    """Each stopping rule stops the row kernel where it stops the generic one
+    (workload 3's sizes, unrefined), and its lambda is as close to the fp64
+    direct solution as the generic kernel's (the workload is ill-conditioned:
+    about 1700 iterations, so the two kernels' rounding alone moves lambda
+    by about 1e-3)."""
+    w = WORKLOADS[3]
+    prob = make_batch(w, M=3)
+    p = params_for(w, stop_rule=rule, refine_steps=0)
+    a = solve(prob, p, gato.GATO_PCG_ROWS)
+    b = solve(prob, p, gato.GATO_PCG_GENERIC)
+    assert not a["status"].any() and not b["status"].any()
+    assert np.abs(a["iters"] - b["iters"]).max() <= 0.05 * b["iters"].max() + 2
+    for j in range(3):
+        lam = oracle.direct_solve(oracle.solve_one(prob, j))[2]
+        assert rel(a["lam"][j], lam) <= 2 * rel(b["lam"][j], lam) + 1e-5
+
+
+def test_rows_kernel_chosen_for_small_states():
+    """GATO_PCG_ROWS also runs n <= 16 (the narrowest row width)."""
+    w = WORKLOADS[1]
+    prob = make_batch(w, M=4)
+    out = solve(prob, params_for(w), gato.GATO_PCG_ROWS)
+    assert not out["status"].any()
+    check_solution(prob, out, range(4), w.n_alpha, w.beta, w.mu)
+
+
 @pytest.mark.parametrize("kind", [gato.GATO_PCG_WIDE, gato.GATO_PCG_TILE], ids=["wide", "tile"])
 @pytest.mark.parametrize("w", [WORKLOADS[1], WORKLOADS[4]], ids=lambda w: w.name)
 def test_tiled_and_generic_kernels_agree(w, kind):

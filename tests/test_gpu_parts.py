@@ -205,3 +205,24 @@ def test_faults_stay_with_their_solve_across_parts():
         assert np.array_equal(out["status"], ref["status"])
         for k in ("dX", "dU", "lam", "merit", "best", "iters"):
             assert np.array_equal(out[k], ref[k], equal_nan=True), k
+
+
+def test_host_entry_takes_pageable_buffers():
+    """Pageable (unpinned) host arrays are copied without overlap but give
+    the same outputs as pinned ones."""
+    w = WORKLOADS[1]
+    M = 11
+    prob = make_batch(w, M=M)
+    p = params_for(w)
+    with gato.Solver(M, w.N, w.n, w.m) as s:
+        ref = host_solve(s, p, prob, 3)
+        s.set_parts(3)
+        hp = {k: torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)) for k, v in prob.items()}
+        assert not any(t.is_pinned() for t in hp.values())
+        out = {k: torch.zeros(v.shape, dtype=v.dtype) for k, v in s.host_outputs(p.n_alpha).items()}
+        assert not any(t.is_pinned() for t in out.values())
+        stream = torch.cuda.current_stream()
+        s.solve_kkt_host(p, hp, out["dX"], out["dU"], out["lam"], out["iters"], out["merit"],
+                         out["best"], out["status"], stream)
+        stream.synchronize()
+    same({k: v.numpy() for k, v in out.items()}, ref)

@@ -377,7 +377,7 @@ int gato_set_timing(gato_handle* h, int on)
 
 int gato_set_pcg_kernel(gato_handle* h, int kind)
 {
-    if (!h || kind < GATO_PCG_AUTO || kind > GATO_PCG_TILE) return GATO_ERR_INVALID_ARG;
+    if (!h || kind < GATO_PCG_AUTO || kind > GATO_PCG_ROWS) return GATO_ERR_INVALID_ARG;
     h->pcg_kernel = kind;
     return GATO_OK;
 }

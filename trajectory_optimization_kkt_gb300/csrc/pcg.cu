@@ -27,59 +27,16 @@
 //     four block barriers per iteration.
 // k_pcg_generic  (any n <= 64): Nhat in shared memory when it fits (else read
 //     from global memory), one thread per vector element.
+// k_pcg_rows<NP, R> (pcg_rows.cu; the default for 16 < n <= 64 where its
+//     block fits): whole rows of the coupling blocks in registers.
 #include <cooperative_groups.h>
 
-#include "gato_internal.cuh"
+#include "pcg_common.cuh"
 
 namespace gato {
 namespace {
 
 namespace cg = cooperative_groups;
-
-struct PcgArgs {
-    Work w;
-    Rhs rhs;
-    const float* lambda0;  // original variables, [M][N][n], may be NULL
-    float* lambda;
-    float* dX;
-    float* dU;
-    int32_t* iters;
-    uint32_t* status;
-    float eps;
-    int max_iters;
-    int rule;
-    int nh_smem;     // generic kernel: Nhat staged in shared memory
-    int l_smem;      // packed L staged in shared memory (rule 0 only)
-    int acc_iters;   // add to iters instead of storing
-    int* queue;      // tiled kernel: next-solve counter, zero at launch
-};
-
-__host__ __device__ __forceinline__ size_t round4(size_t x) { return (x + 3) & ~(size_t)3; }
-
-template <int K>
-__device__ __forceinline__ void block_sum(float (&v)[K], float4* buf)
-{
-    static_assert(K >= 1 && K <= 3, "block_sum reduces up to three values");
-#pragma unroll
-    for (int k = 0; k < K; ++k) v[k] = warp_sum(v[k]);
-    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    if (lane_id() == 0) {
-        float4 t = make_float4(v[0], 0.f, 0.f, 0.f);
-        if (K > 1) t.y = v[K > 1 ? 1 : 0];
-        if (K > 2) t.z = v[K > 2 ? 2 : 0];
-        buf[w] = t;
-    }
-    __syncthreads();
-    float s[3] = {0.f, 0.f, 0.f};
-    for (int q = 0; q < nw; ++q) {
-        const float4 t = buf[q];
-        s[0] += t.x;
-        s[1] += t.y;
-        s[2] += t.z;
-    }
-#pragma unroll
-    for (int k = 0; k < K; ++k) v[k] = s[k];
-}
 
 // Warp partial sums written before a barrier and summed by every thread after
 // it, in a fixed order (deterministic).  buf holds up to 16 float2 (one per
@@ -118,20 +75,6 @@ __device__ __forceinline__ float2 collect2(const float2* buf)
     return hi ? make_float2(other, v) : make_float2(v, other);
 }
 
-__device__ __forceinline__ void finish(const PcgArgs& g, int sol, int it, bool done,
-                                       bool nonfinite)
-{
-    if (threadIdx.x == 0) {
-        if (g.acc_iters)
-            g.iters[sol] += it;
-        else
-            g.iters[sol] = it;
-        uint32_t st = 0;
-        if (!done && !nonfinite) st |= GATO_STATUS_PCG_MAX_ITERS;
-        if (nonfinite) st |= GATO_STATUS_NONFINITE;
-        if (st) atomicOr(g.status + sol, st);
-    }
-}
 
 // ===========================================================================
 // generic kernel
@@ -1474,7 +1417,14 @@ cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const f
     // wide-tile kernel: two threads per coupling block
     int Tw = ((2 * w.N + 31) / 32) * 32;
     if (Tw < 64) Tw = 64;
-    const int kind = h->pcg_kernel;
+    int kind = h->pcg_kernel;
+    // register-row kernel (pcg_rows.cu): the default for 16 < n <= 64 where its
+    // block fits, any n <= 64 when chosen; where it does not fit, as AUTO
+    if (kind == GATO_PCG_ROWS || (kind == GATO_PCG_AUTO && w.n > 16)) {
+        cudaError_t e = launch_pcg_rows(a, limit, st);
+        if (e != cudaErrorInvalidConfiguration) return e;
+        kind = GATO_PCG_AUTO;
+    }
     if ((kind == GATO_PCG_AUTO || kind == GATO_PCG_WIDE) && tiled_n && Tw <= 256) {
         a.nh_smem = 0;
         a.l_smem = want_l;

@@ -1,0 +1,75 @@
+// pcg_common.cuh -- what the PCG kernels of pcg.cu and pcg_rows.cu share: the
+// kernel arguments, the block reduction and the per-solve epilogue (iteration
+// count and status bits).
+#pragma once
+
+#include "gato_internal.cuh"
+
+namespace gato {
+
+struct PcgArgs {
+    Work w;
+    Rhs rhs;
+    const float* lambda0;  // original variables, [M][N][n], may be NULL
+    float* lambda;
+    float* dX;
+    float* dU;
+    int32_t* iters;
+    uint32_t* status;
+    float eps;
+    int max_iters;
+    int rule;
+    int nh_smem;     // generic kernel: Nhat staged in shared memory
+    int l_smem;      // packed L staged in shared memory (rule 0 only)
+    int acc_iters;   // add to iters instead of storing
+    int* queue;      // tiled kernel: next-solve counter, zero at launch
+};
+
+__host__ __device__ __forceinline__ size_t round4(size_t x) { return (x + 3) & ~(size_t)3; }
+
+template <int K>
+__device__ __forceinline__ void block_sum(float (&v)[K], float4* buf)
+{
+    static_assert(K >= 1 && K <= 3, "block_sum reduces up to three values");
+#pragma unroll
+    for (int k = 0; k < K; ++k) v[k] = warp_sum(v[k]);
+    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (lane_id() == 0) {
+        float4 t = make_float4(v[0], 0.f, 0.f, 0.f);
+        if (K > 1) t.y = v[K > 1 ? 1 : 0];
+        if (K > 2) t.z = v[K > 2 ? 2 : 0];
+        buf[w] = t;
+    }
+    __syncthreads();
+    float s[3] = {0.f, 0.f, 0.f};
+    for (int q = 0; q < nw; ++q) {
+        const float4 t = buf[q];
+        s[0] += t.x;
+        s[1] += t.y;
+        s[2] += t.z;
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) v[k] = s[k];
+}
+
+__device__ __forceinline__ void finish(const PcgArgs& g, int sol, int it, bool done,
+                                       bool nonfinite)
+{
+    if (threadIdx.x == 0) {
+        if (g.acc_iters)
+            g.iters[sol] += it;
+        else
+            g.iters[sol] = it;
+        uint32_t st = 0;
+        if (!done && !nonfinite) st |= GATO_STATUS_PCG_MAX_ITERS;
+        if (nonfinite) st |= GATO_STATUS_NONFINITE;
+        if (st) atomicOr(g.status + sol, st);
+    }
+}
+
+// the register-row kernel (pcg_rows.cu): launched when it applies to the
+// sizes, else cudaErrorInvalidConfiguration (the caller then takes another
+// kernel)
+cudaError_t launch_pcg_rows(const PcgArgs& a, size_t smem_limit, cudaStream_t st);
+
+}  // namespace gato

@@ -1,0 +1,327 @@
+// pcg_rows.cu -- batched PCG on S lambda = gamma with the symmetric stair
+// preconditioner for larger states (17 <= n <= 64), and recovery of dz (GATO
+// paper, Sec. II and eq. (4); Sec. III: one thread block per linear system,
+// block-tridiagonal matrix-vector products, block reductions).
+//
+// The same iteration as the kernels of pcg.cu, in the block-Jacobi-scaled
+// variables lambda_hat = L^T lambda, where S_hat = I + Nhat and the stair
+// preconditioner is I - Nhat: both products of an iteration are products
+// with the block-tridiagonal Nhat (coupling blocks Nhat_j, block (j, j-1)).
+//
+// k_pcg_rows<NP, R>: thread t owns rows a = q R .. q R + R - 1 of knot j
+// (j = t / TPK, q = t % TPK, TPK = ceil(n / R) threads per knot) and keeps
+// in registers those rows of the two coupling blocks around its knot: row a
+// of Nhat_j (multiplies x_{j-1}) and row a of Nhat_{j+1}^T (column a of
+// Nhat_{j+1}, multiplies x_{j+1}).  Its rows of Nhat x are then complete
+// in registers: a product reads only the two neighbouring knots' vectors,
+// broadcast from shared memory as 128-bit loads, and nothing else is
+// exchanged.  NP is n padded to a multiple of 4 (the vectors' knot stride,
+// padding slots zero), R keeps the two row tiles within 144 floats.  The
+// vectors live in registers with their owners and in shared memory for the
+// neighbours; a guard knot of zeros before knot 0 and after knot N-1 stands
+// for the missing neighbours.
+//
+// Stopping rule 0 (||L r_hat|| <= eps ||gamma||) is evaluated only when the
+// per-knot lower bound sum_j lambda_min-bound_j ||r_hat_j||^2 no longer rules
+// convergence out, as in the kernels of pcg.cu: gated by the previous
+// iteration's bound (within 1.25 of the threshold), with a fallback
+// evaluation in the same iteration, so the stop is exact.
+#include "pcg_common.cuh"
+
+namespace gato {
+namespace {
+
+// rows per thread: the two tiles (2 R NP floats) within 144 registers
+constexpr int rows_for(int NP) { return 144 / (2 * NP) > 0 ? 144 / (2 * NP) : 1; }
+
+// threads per block the registers allow: 64K registers over the tiles plus
+// about 56 for the rest, in whole warps
+constexpr int max_threads_for(int NP)
+{
+    return (65536 / (2 * rows_for(NP) * NP + 56)) / 32 * 32 > 1024
+               ? 1024
+               : (65536 / (2 * rows_for(NP) * NP + 56)) / 32 * 32;
+}
+
+template <int NP, int R>
+struct RowTiles {
+    float lo[R][NP];  // rows of Nhat_j        (times x_{j-1})
+    float up[R][NP];  // rows of Nhat_{j+1}^T  (times x_{j+1})
+};
+
+// y[i] = (Nhat x)_a for the thread's rows; X holds the vector with knot j at
+// X + (j + 1) NP (guard knots of zeros at both ends)
+template <int NP, int R>
+__device__ __forceinline__ void rows_matvec(const RowTiles<NP, R>& T, const float* X, int j,
+                                            float (&y)[R])
+{
+    const float4* xm = reinterpret_cast<const float4*>(X + j * NP);        // x_{j-1}
+    const float4* xp = reinterpret_cast<const float4*>(X + (j + 2) * NP);  // x_{j+1}
+    float sl[R], su[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) sl[i] = su[i] = 0.f;
+#pragma unroll
+    for (int c = 0; c < NP / 4; ++c) {
+        const float4 a = xm[c], b = xp[c];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            sl[i] = fmaf(T.lo[i][4 * c], a.x, sl[i]);
+            sl[i] = fmaf(T.lo[i][4 * c + 1], a.y, sl[i]);
+            sl[i] = fmaf(T.lo[i][4 * c + 2], a.z, sl[i]);
+            sl[i] = fmaf(T.lo[i][4 * c + 3], a.w, sl[i]);
+            su[i] = fmaf(T.up[i][4 * c], b.x, su[i]);
+            su[i] = fmaf(T.up[i][4 * c + 1], b.y, su[i]);
+            su[i] = fmaf(T.up[i][4 * c + 2], b.z, su[i]);
+            su[i] = fmaf(T.up[i][4 * c + 3], b.w, su[i]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i) y[i] = sl[i] + su[i];
+}
+
+// sum over the thread's valid rows of (L_j r_hat_j)_a^2, L_j from global memory
+// (read only in the iterations where the exact norm is needed)
+template <int NP, int R>
+__device__ __forceinline__ float rows_lnorm(const float* Lj, const float* X, int j, int a0,
+                                            int n, const bool (&valid)[R])
+{
+    const float* xr = X + (j + 1) * NP;
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        if (valid[i]) {
+            const int a = a0 + i;
+            const float* row = Lj + (size_t)a * n;
+            float t = 0.f;
+            for (int b = 0; b <= a; ++b) t = fmaf(row[b], xr[b], t);
+            s = fmaf(t, t, s);
+        }
+    }
+    return s;
+}
+
+template <int NP, int R>
+__device__ __forceinline__ void rows_store(float* X, int j, int a0, const bool (&valid)[R],
+                                           const float (&v)[R])
+{
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+        if (valid[i]) X[(j + 1) * NP + a0 + i] = v[i];
+}
+
+template <int NP, int R>
+__global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
+{
+    extern __shared__ __align__(16) float sm[];
+    const Work& w = g.w;
+    const int N = w.N, n = w.n, T = blockDim.x, tid = threadIdx.x;
+    const int sol = blockIdx.x;
+    const int TPK = (n + R - 1) / R;
+    const int XS = (N + 2) * NP;  // one vector with its guard knots
+    const bool rule0 = g.rule == GATO_STOP_RESIDUAL;
+
+    float* XP = sm;                 // p (and lambda_hat at the end)
+    float* XR = XP + XS;            // r
+    float* lsm = XR + XS;           // recovery scratch, N n
+    float4* redA = reinterpret_cast<float4*>(lsm + round4((size_t)N * n));
+    float4* redB = redA + 32;
+    float4* redC = redA + 64;
+    for (int i = tid; i < 2 * XS; i += T) sm[i] = 0.f;
+
+    const int j = tid / TPK, q = tid - j * TPK;
+    const int a0 = q * R;
+    const bool owner = j < N;
+    bool valid[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) valid[i] = owner && a0 + i < n;
+    const int jj = owner ? j : 0;  // a safe knot for threads past the last one
+
+    // the thread's rows of Nhat_j and Nhat_{j+1}^T (zero where there is no
+    // block, no row, or no column)
+    RowTiles<NP, R> tile;
+    {
+        const float* nh = w.Nh + sol * w.sKnn;
+        const size_t nn = (size_t)n * n;
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int a = a0 + i;
+            const bool has_lo = valid[i] && jj >= 1;
+            const bool has_up = valid[i] && jj + 1 < N;
+            const float* lo = nh + (size_t)(jj >= 1 ? jj - 1 : 0) * nn + (size_t)a * n;
+            const float* up = nh + (size_t)jj * nn + a;
+#pragma unroll
+            for (int b = 0; b < NP; ++b) {
+                tile.lo[i][b] = (has_lo && b < n) ? lo[b] : 0.f;
+                tile.up[i][b] = (has_up && b < n) ? up[(size_t)b * n] : 0.f;
+            }
+        }
+    }
+    const float dl = owner ? w.dlow[sol * w.sN + jj] : 0.f;
+    const float* ghat = g.rhs.ghat + sol * w.sNn;
+    const float* gam = g.rhs.gamma + sol * w.sNn;
+    const float* gL = w.L + sol * w.sNnn;
+    const float* Lj = gL + (size_t)jj * n * n;
+
+    float lam[R], r[R], p[R], y[R];
+    // lambda_hat0 = L^T lambda0
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        lam[i] = 0.f;
+        if (valid[i] && g.lambda0) {
+            const int a = a0 + i;
+            const float* l0 = g.lambda0 + (size_t)sol * N * n + (size_t)jj * n;
+            float x = 0.f;
+            for (int b = a; b < n; ++b) x += Lj[(size_t)b * n + a] * l0[b];
+            lam[i] = x;
+        }
+    }
+    __syncthreads();  // the zeroed vectors
+    rows_store<NP, R>(XP, jj, a0, valid, lam);
+    __syncthreads();
+    // r_hat = ghat - S_hat lambda_hat, then z = (I - Nhat) r_hat = p
+    rows_matvec<NP, R>(tile, XP, jj, y);
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+        r[i] = valid[i] ? ghat[jj * n + a0 + i] - lam[i] - y[i] : 0.f;
+    rows_store<NP, R>(XR, jj, a0, valid, r);
+    __syncthreads();
+    rows_matvec<NP, R>(tile, XR, jj, y);
+    float red3[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        p[i] = r[i] - y[i];
+        red3[0] = fmaf(r[i], p[i], red3[0]);
+        if (valid[i]) {
+            const int gi = jj * n + a0 + i;
+            if (rule0)
+                red3[2] = fmaf(gam[gi], gam[gi], red3[2]);
+            else if (g.rule == GATO_STOP_SCALED) {
+                red3[1] = fmaf(r[i], r[i], red3[1]);
+                red3[2] = fmaf(ghat[gi], ghat[gi], red3[2]);
+            }
+        }
+    }
+    if (rule0) red3[1] = rows_lnorm<NP, R>(Lj, XR, jj, a0, n, valid);
+    rows_store<NP, R>(XP, jj, a0, valid, p);
+    block_sum<3>(red3, redA);  // also orders the p stores before the first product
+    float eta = red3[0];
+    const float ref = g.rule == GATO_STOP_PRECOND ? eta : red3[2];
+    const float thr = g.eps * g.eps * ref;
+    bool done = (g.rule == GATO_STOP_PRECOND ? eta : red3[1]) <= thr;
+    bool nonfinite = !isfinite(eta) || !isfinite(red3[1]);
+    bool exact_next = false;
+    if (rule0) {
+        float lb = 0.f;
+#pragma unroll
+        for (int i = 0; i < R; ++i) lb = fmaf(dl * r[i], r[i], lb);
+        float lv[1] = {lb};
+        block_sum<1>(lv, redB);
+        exact_next = lv[0] <= 1.25f * thr;
+    }
+    __syncthreads();
+
+    int it = 0;
+    while (!done && !nonfinite && it < g.max_iters) {
+        ++it;
+        // v = S_hat p, alpha = eta / p^T v; lambda and r updates
+        rows_matvec<NP, R>(tile, XP, jj, y);
+        float pv[1] = {0.f};
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            y[i] += p[i];
+            pv[0] = fmaf(p[i], y[i], pv[0]);
+        }
+        block_sum<1>(pv, redA);
+        const float alpha = __fdividef(eta, pv[0]);
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            lam[i] = fmaf(alpha, p[i], lam[i]);
+            r[i] = fmaf(-alpha, y[i], r[i]);
+        }
+        rows_store<NP, R>(XR, jj, a0, valid, r);
+        __syncthreads();
+        // z = (I - Nhat) r, eta' = r^T z; the stopping quantities
+        rows_matvec<NP, R>(tile, XR, jj, y);
+        float red[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            y[i] = r[i] - y[i];
+            red[0] = fmaf(r[i], y[i], red[0]);
+            red[1] = fmaf(r[i], r[i], red[1]);
+        }
+        if (rule0) red[1] *= dl;  // the lower bound's share
+        const bool exact = exact_next;
+        if (exact) red[2] = rows_lnorm<NP, R>(Lj, XR, jj, a0, n, valid);
+        block_sum<3>(red, redB);
+        const float eta_new = red[0];
+        float lsq = red[2];
+        bool have_exact = exact;
+        if (rule0 && !exact && red[1] * 0.999f <= thr) {
+            float lv[1] = {rows_lnorm<NP, R>(Lj, XR, jj, a0, n, valid)};
+            block_sum<1>(lv, redC);
+            lsq = lv[0];
+            have_exact = true;
+        }
+        const float stopq = rule0 ? lsq : (g.rule == GATO_STOP_SCALED ? red[1] : eta_new);
+        if (!isfinite(eta_new + pv[0] + stopq + red[1])) {  // NaN and Inf propagate
+            nonfinite = true;
+            break;
+        }
+        done = (!rule0 || have_exact) && stopq <= thr;
+        if (done) break;
+        exact_next = rule0 && red[1] <= 1.25f * thr;
+        const float beta = __fdividef(eta_new, eta);
+#pragma unroll
+        for (int i = 0; i < R; ++i) p[i] = fmaf(beta, p[i], y[i]);
+        rows_store<NP, R>(XP, jj, a0, valid, p);
+        eta = eta_new;
+        __syncthreads();
+    }
+    __syncthreads();
+    rows_store<NP, R>(XP, jj, a0, valid, lam);
+    __syncthreads();
+    recover_dz(g.w, g.rhs, g.lambda, g.dX, g.dU, sol,
+               [&](int k, int b) { return XP[(k + 1) * NP + b]; }, lsm);
+    finish(g, sol, it, done, nonfinite);
+}
+
+template <int NP>
+cudaError_t launch_rows_np(const PcgArgs& a, size_t limit, cudaStream_t st)
+{
+    constexpr int R = rows_for(NP);
+    const Work& w = a.w;
+    const int TPK = (w.n + R - 1) / R;
+    int T = ((w.N * TPK + 31) / 32) * 32;
+    if (T < 64) T = 64;
+    if (T > max_threads_for(NP)) return cudaErrorInvalidConfiguration;
+    const size_t smem = sizeof(float) * (2 * (size_t)(w.N + 2) * NP + round4((size_t)w.N * w.n)) +
+                        96 * sizeof(float4);
+    if (smem > limit) return cudaErrorInvalidConfiguration;
+    auto kernel = k_pcg_rows<NP, R>;
+    if (smem > 48 * 1024) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    kernel<<<w.M, T, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_pcg_rows(const PcgArgs& a, size_t limit, cudaStream_t st)
+{
+    const int n = a.w.n;
+    if (n <= 20) return launch_rows_np<20>(a, limit, st);
+    if (n <= 24) return launch_rows_np<24>(a, limit, st);
+    if (n <= 28) return launch_rows_np<28>(a, limit, st);
+    if (n <= 32) return launch_rows_np<32>(a, limit, st);
+    if (n <= 36) return launch_rows_np<36>(a, limit, st);
+    if (n <= 40) return launch_rows_np<40>(a, limit, st);
+    if (n <= 48) return launch_rows_np<48>(a, limit, st);
+    if (n <= 56) return launch_rows_np<56>(a, limit, st);
+    if (n <= 64) return launch_rows_np<64>(a, limit, st);
+    return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace gato

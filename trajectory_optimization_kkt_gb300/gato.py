@@ -28,6 +28,7 @@ GATO_PCG_AUTO = 0
 GATO_PCG_GENERIC = 1
 GATO_PCG_WIDE = 2
 GATO_PCG_TILE = 3
+GATO_PCG_ROWS = 4
 GATO_MAX_PARTS = 8
 GATO_MAX_STATE = 64
 GATO_MAX_CONTROL = 64
