@@ -100,6 +100,33 @@ __device__ __forceinline__ float rows_lnorm(const float* Lj, const float* X, int
     return s;
 }
 
+// the same from the rows of L staged in shared memory (row a of L_j at
+// LS + (j n + a) NP, zero above the diagonal and past n): 128-bit products
+template <int NP, int R>
+__device__ __forceinline__ float rows_lnorm_smem(const float* LS, const float* X, int j, int a0,
+                                                 int n, const bool (&valid)[R])
+{
+    const float4* xr = reinterpret_cast<const float4*>(X + (j + 1) * NP);
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        if (valid[i]) {
+            const float4* row = reinterpret_cast<const float4*>(LS + ((size_t)j * n + a0 + i) * NP);
+            float t = 0.f;
+#pragma unroll
+            for (int c = 0; c < NP / 4; ++c) {
+                const float4 l = row[c], x = xr[c];
+                t = fmaf(l.x, x.x, t);
+                t = fmaf(l.y, x.y, t);
+                t = fmaf(l.z, x.z, t);
+                t = fmaf(l.w, x.w, t);
+            }
+            s = fmaf(t, t, s);
+        }
+    }
+    return s;
+}
+
 template <int NP, int R>
 __device__ __forceinline__ void rows_store(float* X, int j, int a0, const bool (&valid)[R],
                                            const float (&v)[R])
@@ -126,6 +153,7 @@ __global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
     float4* redA = reinterpret_cast<float4*>(lsm + round4((size_t)N * n));
     float4* redB = redA + 32;
     float4* redC = redA + 64;
+    float* LS = reinterpret_cast<float*>(redA + 96);  // rule 0 with l_smem: the rows of L
     for (int i = tid; i < 2 * XS; i += T) sm[i] = 0.f;
 
     const int j = tid / TPK, q = tid - j * TPK;
@@ -161,6 +189,13 @@ __global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
     const float* gam = g.rhs.gamma + sol * w.sNn;
     const float* gL = w.L + sol * w.sNnn;
     const float* Lj = gL + (size_t)jj * n * n;
+    const bool l_staged = rule0 && g.l_smem;
+    if (l_staged) {  // every row padded to NP (the factor's upper part is stored as zeros)
+        for (int t = tid; t < N * n * NP; t += T) {
+            const int row = t / NP, b = t - row * NP;
+            LS[t] = b < n ? gL[(size_t)row * n + b] : 0.f;
+        }
+    }
 
     float lam[R], r[R], p[R], y[R];
     // lambda_hat0 = L^T lambda0
@@ -201,7 +236,9 @@ __global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
             }
         }
     }
-    if (rule0) red3[1] = rows_lnorm<NP, R>(Lj, XR, jj, a0, n, valid);
+    if (rule0)
+        red3[1] = l_staged ? rows_lnorm_smem<NP, R>(LS, XR, jj, a0, n, valid)
+                      : rows_lnorm<NP, R>(Lj, XR, jj, a0, n, valid);
     rows_store<NP, R>(XP, jj, a0, valid, p);
     block_sum<3>(red3, redA);  // also orders the p stores before the first product
     float eta = red3[0];
@@ -251,13 +288,16 @@ __global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
         }
         if (rule0) red[1] *= dl;  // the lower bound's share
         const bool exact = exact_next;
-        if (exact) red[2] = rows_lnorm<NP, R>(Lj, XR, jj, a0, n, valid);
+        if (exact)
+            red[2] = l_staged ? rows_lnorm_smem<NP, R>(LS, XR, jj, a0, n, valid)
+                         : rows_lnorm<NP, R>(Lj, XR, jj, a0, n, valid);
         block_sum<3>(red, redB);
         const float eta_new = red[0];
         float lsq = red[2];
         bool have_exact = exact;
         if (rule0 && !exact && red[1] * 0.999f <= thr) {
-            float lv[1] = {rows_lnorm<NP, R>(Lj, XR, jj, a0, n, valid)};
+            float lv[1] = {l_staged ? rows_lnorm_smem<NP, R>(LS, XR, jj, a0, n, valid)
+                               : rows_lnorm<NP, R>(Lj, XR, jj, a0, n, valid)};
             block_sum<1>(lv, redC);
             lsq = lv[0];
             have_exact = true;
@@ -294,16 +334,21 @@ cudaError_t launch_rows_np(const PcgArgs& a, size_t limit, cudaStream_t st)
     int T = ((w.N * TPK + 31) / 32) * 32;
     if (T < 64) T = 64;
     if (T > max_threads_for(NP)) return cudaErrorInvalidConfiguration;
-    const size_t smem = sizeof(float) * (2 * (size_t)(w.N + 2) * NP + round4((size_t)w.N * w.n)) +
-                        96 * sizeof(float4);
+    size_t smem = sizeof(float) * (2 * (size_t)(w.N + 2) * NP + round4((size_t)w.N * w.n)) +
+                  96 * sizeof(float4);
     if (smem > limit) return cudaErrorInvalidConfiguration;
+    // rule 0: the rows of L in shared memory where they fit
+    PcgArgs b = a;
+    const size_t l_bytes = sizeof(float) * (size_t)w.N * w.n * NP;
+    b.l_smem = a.rule == GATO_STOP_RESIDUAL && smem + l_bytes <= limit;
+    if (b.l_smem) smem += l_bytes;
     auto kernel = k_pcg_rows<NP, R>;
     if (smem > 48 * 1024) {
         cudaError_t e =
             cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    kernel<<<w.M, T, smem, st>>>(a);
+    kernel<<<w.M, T, smem, st>>>(b);
     return cudaGetLastError();
 }
 
