@@ -212,7 +212,10 @@ def _cpu_baseline(w):
     cores = os.cpu_count() or 1
     oracle.build()
     kw = dict(eps=w.pcg_eps, max_iters=w.pcg_max_iters, n_alpha=w.n_alpha, beta=w.beta, mu=w.mu)
-    sample = w.M  # the whole batch: about 8 s of CPU work at workload 4 (34 solves/s a core)
+    # the whole batch (about 8 s of CPU work at workload 4, 34 solves/s a core);
+    # for batches smaller than four solves a core, that many solves of the same
+    # recipe, so that the pool's dispatch does not dominate
+    sample = max(w.M, 4 * cores)
     prob = make_batch(w, M=sample)
     solves = [oracle.solve_one(prob, j) for j in range(sample)]
     ctx = mp.get_context("spawn")
@@ -227,7 +230,9 @@ def _cpu_baseline(w):
         _oracle_solve(s_, kw)
     one = 2 / (time.perf_counter() - t0)
     return {"value": sample / sec, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"all {sample} solves of the batch, fp64 C oracle, spawn pool of {cores}",
+            "sample": (f"all {sample} solves of the batch" if sample == w.M else
+                       f"{sample} solves of the workload's recipe (batch of {w.M})")
+                      + f", fp64 C oracle, spawn pool of {cores}",
             "pcg_iters_per_sec": sum(r[0] for r in res) / sec,
             "single_thread_solves_per_s": one, "cpu_model": _cpu_model()}
 
@@ -351,6 +356,22 @@ def run_throughput_sweep(args, local):
                       flush=True)
 
 
+def _pcg_kernel_name(N, n):
+    """The PCG kernel GATO_PCG_AUTO picks for these sizes (the rules of
+    launch_pcg_ex and launch_pcg_rows: the register-row kernel's rows per
+    thread keep its two row tiles within 144 floats, and its block within
+    the registers)."""
+    if 7 <= n <= 16:
+        return "k_pcg_wide" if N <= 128 else ("k_pcg_cluster" if N <= 512 else "k_pcg_generic")
+    if 16 < n <= 64:
+        NP = next(p for p in (20, 24, 28, 32, 36, 40, 48, 56, 64) if n <= p)
+        R = max(1, 144 // (2 * NP))
+        T = max(64, (N * -(-n // R) + 31) // 32 * 32)
+        if T <= min(1024, 65536 // (2 * R * NP + 56) // 32 * 32):
+            return "k_pcg_rows"
+    return "k_pcg_generic"
+
+
 def run_workloads(args, local):
     """The five synthetic workloads at their own sizes and settings: solves/s
     and PCG iterations/s of whole gato_solve_kkt calls (default parts, L2
@@ -389,8 +410,7 @@ def run_workloads(args, local):
         merit_bytes = 4 * M * (N * n * n + K * (m * m + n * n + n * m) + N * n + K * m + K * n
                                + n + N * n + K * m + (w.n_alpha + 1) + 1)
         merit_gbs = merit_bytes / (stages["merit"] * 1e-6) / 1e9
-        pcg_kernel = ("k_pcg_wide" if 7 <= n <= 16 and N <= 128 else
-                      "k_pcg_cluster" if 7 <= n <= 16 else "k_pcg_generic")
+        pcg_kernel = _pcg_kernel_name(N, n)
         row = {"workload": w.name, "M": M, "N": N, "n": n, "m": m, "parts": parts,
                "solves_per_s": M / (ms / 1000.0), "ms_per_call": ms,
                "pcg_iters_per_sec": iters / (ms / 1000.0), "pcg_iters_per_solve": iters / M,
