@@ -469,13 +469,24 @@ def test_apply_step():
     np.testing.assert_array_equal(U.cpu().numpy(), U0 + alpha[:, None, None] * out["dU"])
 
 
-def test_warm_start_at_solution_needs_no_iterations():
-    w = WORKLOADS[1]
-    prob = make_batch(w, M=2)
+WARM = [("n12_auto", 12, gato.GATO_PCG_AUTO), ("n12_generic", 12, gato.GATO_PCG_GENERIC),
+        ("n12_tile", 12, gato.GATO_PCG_TILE), ("n36_rows", 36, gato.GATO_PCG_AUTO),
+        ("n36_generic", 36, gato.GATO_PCG_GENERIC)]
+
+
+def _warm_problem(n):
+    return make_batch(WORKLOADS[1], M=2) if n == 12 else random_lq(2, 8, 36, 12, seed=910)
+
+
+@pytest.mark.parametrize("name,n,kind", WARM, ids=[c[0] for c in WARM])
+def test_warm_start_at_solution_needs_no_iterations(name, n, kind):
+    prob = _warm_problem(n)
+    M, N, n_, m = 2, prob["Q"].shape[1], n, prob["R"].shape[-1]
     lam = np.stack([oracle.direct_solve(oracle.solve_one(prob, j))[2] for j in range(2)])
     d = gato.to_device(prob)
-    p = params_for(w, pcg_eps=1e-3)
-    with gato.Solver(2, w.N, w.n, w.m) as s:
+    p = gato.default_params(pcg_eps=1e-3, pcg_max_iters=3000)
+    with gato.Solver(M, N, n_, m) as s:
+        s.set_pcg_kernel(kind)
         o = s.outputs(p.n_alpha)
         s.form_schur(d, o["status"])
         s.pcg_solve(p, o["lam"], o["dX"], o["dU"], o["iters"], o["status"],
@@ -484,6 +495,30 @@ def test_warm_start_at_solution_needs_no_iterations():
         assert (o["iters"].cpu().numpy() == 0).all()
         for j in range(2):
             assert rel(o["lam"][j].cpu().numpy(), lam[j]) < 1e-4
+
+
+@pytest.mark.parametrize("name,n,kind", WARM, ids=[c[0] for c in WARM])
+def test_warm_start_from_a_partial_solution(name, n, kind):
+    """From half the solution every kernel converges to it, in fewer
+    iterations than from zero."""
+    prob = _warm_problem(n)
+    M, N, m = 2, prob["Q"].shape[1], prob["R"].shape[-1]
+    lam = np.stack([oracle.direct_solve(oracle.solve_one(prob, j))[2] for j in range(2)])
+    d = gato.to_device(prob)
+    p = gato.default_params(pcg_eps=1e-6, pcg_max_iters=5000)
+    with gato.Solver(M, N, n, m) as s:
+        s.set_pcg_kernel(kind)
+        o = s.outputs(p.n_alpha)
+        s.form_schur(d, o["status"])
+        s.pcg_solve(p, o["lam"], o["dX"], o["dU"], o["iters"], o["status"])
+        cold = o["iters"].cpu().numpy().copy()
+        s.pcg_solve(p, o["lam"], o["dX"], o["dU"], o["iters"], o["status"],
+                    lambda0=torch.tensor(0.5 * lam, dtype=torch.float32, device="cuda"))
+        torch.cuda.synchronize()
+        assert not o["status"].cpu().numpy().any()
+        assert (o["iters"].cpu().numpy() <= cold).all()
+        for j in range(2):
+            assert rel(o["lam"][j].cpu().numpy(), lam[j]) < 1e-3
 
 
 # --------------------------------------------------------------------------
