@@ -135,7 +135,7 @@ def run_reference(args, world, rank):
 
     import oracle
     from trajectory_optimization_kkt_gb300.workloads import WORKLOADS, make_batch
-    w = WORKLOADS[WORKLOAD_INDEX]
+    w = WORKLOADS[args.workload]
     cores = os.cpu_count() or 1
     per_step = max(cores, 16)  # solves per timed step: a bounded sample of the batch
     prob = make_batch(w, M=per_step)
@@ -586,7 +586,7 @@ def run_gpu(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     _build.build()
-    w = WORKLOADS[WORKLOAD_INDEX]
+    w = WORKLOADS[args.workload]
     if args.batch:
         w = w.with_batch(args.batch)
     M = w.M
@@ -724,7 +724,10 @@ def run_gpu(args, world, rank, local):
     merit_s = statistics.mean(merit_us) * 1e-6
     merit_gbs = merit_bytes / merit_s / 1e9
     sha = _src_sha(os.path.join(_build.CSRC, "pcg.cu"))
-    traffic = PCG_TRAFFIC["bytes_per_launch"] if PCG_TRAFFIC["pcg_sha"] == sha else None
+    # the ncu capture behind the traffic figure is of the default workload
+    traffic = (PCG_TRAFFIC["bytes_per_launch"]
+               if PCG_TRAFFIC["pcg_sha"] == sha and args.workload == WORKLOAD_INDEX
+               and not args.batch else None)
 
     # ---- SQP loop on the linear model (context, not the metric) ----
     sqp = None
@@ -772,7 +775,8 @@ def run_gpu(args, world, rank, local):
             "roofline": None if args.linsys != "pcg" else {
                          "bound": "alu", "achieved": achieved_tf, "peak": alu_peak_tf,
                          "unit": "TFLOP/s", "frac": achieved_tf / alu_peak_tf,
-                         "traffic": traffic, "kernel": "k_pcg_wide (solve + refinement launches)",
+                         "traffic": traffic,
+                         "kernel": _pcg_kernel_name(N, n) + " (solve + refinement launches)",
                          "peak_basis": f"{n_sm} SMs x {FP32_LANES_PER_SM} FFMA lanes x 2 flop x "
                                        f"{sm_mhz:.0f} MHz (max SM clock, {peak_kind})",
                          "flops_per_solve_iteration": flops_it,
@@ -831,6 +835,10 @@ def main():
                          "threads) instead")
     ap.add_argument("--sqp-study", action="store_true",
                     help="the rho-damping SQP case study on the linear model instead")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX, choices=range(5),
+                    help="the workload of the timed step (default 4, the metric's: "
+                         "M=256, N=128, n=14, m=7); the others are parity cases, run "
+                         "here for profiler captures")
     ap.add_argument("--batch", type=int, default=None,
                     help="solves per GPU (default: the workload's 256); for profiler "
                          "captures of a smaller case")

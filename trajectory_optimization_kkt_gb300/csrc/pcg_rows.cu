@@ -43,20 +43,52 @@ constexpr int max_threads_for(int NP)
                : (65536 / (2 * rows_for(NP) * NP + 56)) / 32 * 32;
 }
 
+// The registers per thread the launch bound leaves: 64K over the warps of
+// the fullest SM sub-partition (a quarter of the block's warps, rounded up),
+// in steps of 8.
+constexpr int reg_cap_for(int NP)
+{
+    return (16384 / (((max_threads_for(NP) / 32 + 3) / 4) * 32)) / 8 * 8 > 255
+               ? 255
+               : (16384 / (((max_threads_for(NP) / 32 + 3) / 4) * 32)) / 8 * 8;
+}
+
+// 128-bit column chunks of the tile rows kept in registers: as many as fit
+// beside about 56 other registers; the remaining chunks live in shared
+// memory (read once per product, a float4 per thread, conflict-free), so
+// that nothing is spilled to local memory
+constexpr int reg_chunks_for(int NP)
+{
+    return (reg_cap_for(NP) - 56) / (2 * rows_for(NP) * 4) >= NP / 4
+               ? NP / 4
+               : (reg_cap_for(NP) - 56) / (2 * rows_for(NP) * 4);
+}
+
 template <int NP, int R>
 struct RowTiles {
-    float lo[R][NP];  // rows of Nhat_j        (times x_{j-1})
-    float up[R][NP];  // rows of Nhat_{j+1}^T  (times x_{j+1})
+    static constexpr int RC = reg_chunks_for(NP);  // chunks in registers
+    float lo[R][4 * RC];  // rows of Nhat_j        (times x_{j-1})
+    float up[R][4 * RC];  // rows of Nhat_{j+1}^T  (times x_{j+1})
 };
+
+// shared-memory chunk s (the chunks from RC on) of tile k (0: lo, 1: up), row
+// i of thread tid, in a block of T threads
+template <int R>
+__device__ __forceinline__ int ts_index(int s, int i, int k, int tid, int T)
+{
+    return ((s * R + i) * 2 + k) * T + tid;
+}
 
 // y[i] = (Nhat x)_a for the thread's rows; X holds the vector with knot j at
 // X + (j + 1) NP (guard knots of zeros at both ends)
 template <int NP, int R>
-__device__ __forceinline__ void rows_matvec(const RowTiles<NP, R>& T, const float* X, int j,
-                                            float (&y)[R])
+__device__ __forceinline__ void rows_matvec(const RowTiles<NP, R>& T, const float4* TS,
+                                            const float* X, int j, float (&y)[R])
 {
+    constexpr int RC = RowTiles<NP, R>::RC;
     const float4* xm = reinterpret_cast<const float4*>(X + j * NP);        // x_{j-1}
     const float4* xp = reinterpret_cast<const float4*>(X + (j + 2) * NP);  // x_{j+1}
+    const int tid = threadIdx.x, nt = blockDim.x;
     float sl[R], su[R];
 #pragma unroll
     for (int i = 0; i < R; ++i) sl[i] = su[i] = 0.f;
@@ -65,14 +97,24 @@ __device__ __forceinline__ void rows_matvec(const RowTiles<NP, R>& T, const floa
         const float4 a = xm[c], b = xp[c];
 #pragma unroll
         for (int i = 0; i < R; ++i) {
-            sl[i] = fmaf(T.lo[i][4 * c], a.x, sl[i]);
-            sl[i] = fmaf(T.lo[i][4 * c + 1], a.y, sl[i]);
-            sl[i] = fmaf(T.lo[i][4 * c + 2], a.z, sl[i]);
-            sl[i] = fmaf(T.lo[i][4 * c + 3], a.w, sl[i]);
-            su[i] = fmaf(T.up[i][4 * c], b.x, su[i]);
-            su[i] = fmaf(T.up[i][4 * c + 1], b.y, su[i]);
-            su[i] = fmaf(T.up[i][4 * c + 2], b.z, su[i]);
-            su[i] = fmaf(T.up[i][4 * c + 3], b.w, su[i]);
+            float4 l, u;
+            if (c < RC) {
+                l = make_float4(T.lo[i][4 * c], T.lo[i][4 * c + 1], T.lo[i][4 * c + 2],
+                                T.lo[i][4 * c + 3]);
+                u = make_float4(T.up[i][4 * c], T.up[i][4 * c + 1], T.up[i][4 * c + 2],
+                                T.up[i][4 * c + 3]);
+            } else {
+                l = TS[ts_index<R>(c - RC, i, 0, tid, nt)];
+                u = TS[ts_index<R>(c - RC, i, 1, tid, nt)];
+            }
+            sl[i] = fmaf(l.x, a.x, sl[i]);
+            sl[i] = fmaf(l.y, a.y, sl[i]);
+            sl[i] = fmaf(l.z, a.z, sl[i]);
+            sl[i] = fmaf(l.w, a.w, sl[i]);
+            su[i] = fmaf(u.x, b.x, su[i]);
+            su[i] = fmaf(u.y, b.y, su[i]);
+            su[i] = fmaf(u.z, b.z, su[i]);
+            su[i] = fmaf(u.w, b.w, su[i]);
         }
     }
 #pragma unroll
@@ -153,7 +195,11 @@ __global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
     float4* redA = reinterpret_cast<float4*>(lsm + round4((size_t)N * n));
     float4* redB = redA + 32;
     float4* redC = redA + 64;
-    float* LS = reinterpret_cast<float*>(redA + 96);  // rule 0 with l_smem: the rows of L
+    // the tile chunks past the registers' share, then (rule 0 with l_smem) the
+    // rows of L
+    constexpr int SC = NP / 4 - RowTiles<NP, R>::RC;
+    float4* TS = redA + 96;
+    float* LS = reinterpret_cast<float*>(TS + (size_t)SC * R * 2 * T);
     for (int i = tid; i < 2 * XS; i += T) sm[i] = 0.f;
 
     const int j = tid / TPK, q = tid - j * TPK;
@@ -178,9 +224,21 @@ __global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
             const float* lo = nh + (size_t)(jj >= 1 ? jj - 1 : 0) * nn + (size_t)a * n;
             const float* up = nh + (size_t)jj * nn + a;
 #pragma unroll
-            for (int b = 0; b < NP; ++b) {
+            for (int b = 0; b < 4 * RowTiles<NP, R>::RC; ++b) {
                 tile.lo[i][b] = (has_lo && b < n) ? lo[b] : 0.f;
                 tile.up[i][b] = (has_up && b < n) ? up[(size_t)b * n] : 0.f;
+            }
+#pragma unroll
+            for (int sc = 0; sc < SC; ++sc) {
+                float vl[4], vu[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int b = 4 * (RowTiles<NP, R>::RC + sc) + e;
+                    vl[e] = (has_lo && b < n) ? lo[b] : 0.f;
+                    vu[e] = (has_up && b < n) ? up[(size_t)b * n] : 0.f;
+                }
+                TS[ts_index<R>(sc, i, 0, tid, T)] = make_float4(vl[0], vl[1], vl[2], vl[3]);
+                TS[ts_index<R>(sc, i, 1, tid, T)] = make_float4(vu[0], vu[1], vu[2], vu[3]);
             }
         }
     }
@@ -214,13 +272,13 @@ __global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
     rows_store<NP, R>(XP, jj, a0, valid, lam);
     __syncthreads();
     // r_hat = ghat - S_hat lambda_hat, then z = (I - Nhat) r_hat = p
-    rows_matvec<NP, R>(tile, XP, jj, y);
+    rows_matvec<NP, R>(tile, TS, XP, jj, y);
 #pragma unroll
     for (int i = 0; i < R; ++i)
         r[i] = valid[i] ? ghat[jj * n + a0 + i] - lam[i] - y[i] : 0.f;
     rows_store<NP, R>(XR, jj, a0, valid, r);
     __syncthreads();
-    rows_matvec<NP, R>(tile, XR, jj, y);
+    rows_matvec<NP, R>(tile, TS, XR, jj, y);
     float red3[3] = {0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < R; ++i) {
@@ -261,7 +319,7 @@ __global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
     while (!done && !nonfinite && it < g.max_iters) {
         ++it;
         // v = S_hat p, alpha = eta / p^T v; lambda and r updates
-        rows_matvec<NP, R>(tile, XP, jj, y);
+        rows_matvec<NP, R>(tile, TS, XP, jj, y);
         float pv[1] = {0.f};
 #pragma unroll
         for (int i = 0; i < R; ++i) {
@@ -278,7 +336,7 @@ __global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
         rows_store<NP, R>(XR, jj, a0, valid, r);
         __syncthreads();
         // z = (I - Nhat) r, eta' = r^T z; the stopping quantities
-        rows_matvec<NP, R>(tile, XR, jj, y);
+        rows_matvec<NP, R>(tile, TS, XR, jj, y);
         float red[3] = {0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < R; ++i) {
@@ -334,8 +392,9 @@ cudaError_t launch_rows_np(const PcgArgs& a, size_t limit, cudaStream_t st)
     int T = ((w.N * TPK + 31) / 32) * 32;
     if (T < 64) T = 64;
     if (T > max_threads_for(NP)) return cudaErrorInvalidConfiguration;
+    constexpr int SC = NP / 4 - RowTiles<NP, R>::RC;
     size_t smem = sizeof(float) * (2 * (size_t)(w.N + 2) * NP + round4((size_t)w.N * w.n)) +
-                  96 * sizeof(float4);
+                  (96 + (size_t)SC * R * 2 * T) * sizeof(float4);
     if (smem > limit) return cudaErrorInvalidConfiguration;
     // rule 0: the rows of L in shared memory where they fit
     PcgArgs b = a;
