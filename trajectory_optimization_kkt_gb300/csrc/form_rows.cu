@@ -314,6 +314,7 @@ cudaError_t form_rows_m(const Work& w, const float* Q, const float* R, const flo
 cudaError_t launch_form_phi(gato_handle* h, cudaStream_t st)
 {
     const Work& w = h->w;
+    if (h->phi_smem) return launch_form_phi_smem(h, st);
     if (w.n <= 8) return form_phi_w<8>(w, st);
     if (w.n <= 12) return form_phi_w<12>(w, st);
     if (w.n <= 14) return form_phi_w<14>(w, st);

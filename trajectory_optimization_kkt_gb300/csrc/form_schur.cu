@@ -7,10 +7,12 @@
 // synchronisations the block-local formation needs:
 //   k_form_inv   knot k:  Q_k^-1, R_k^-1, S_{k+1,k} = -A_k Q_k^-1, V_k = B_k R_k^-1
 //   k_form_diag  row j:   S_jj = Q_j^-1 + A_{j-1} Q_{j-1}^-1 A_{j-1}^T + V_{j-1} B_{j-1}^T,
-//                         its Cholesky factor L_j, L_j^-1, S_jj^-1 and the
-//                         eigenvalue bound 1 / ||L_j^-1||_F^2
-//   k_form_off   row j:   Nhat_j = L_j^-1 S_{j,j-1} L_{j-1}^-T and the explicit
-//                         Phi^-1 block -S_jj^-1 S_{j,j-1} S_{j-1,j-1}^-1
+//                         its Cholesky factor L_j, L_j^-1 and the eigenvalue
+//                         bound 1 / ||L_j^-1||_F^2
+//   k_form_off   row j:   Nhat_j = L_j^-1 S_{j,j-1} L_{j-1}^-T
+// The solve applies Phi^-1 in that factored form; the explicit blocks
+// S_jj^-1 and -S_jj^-1 S_{j,j-1} S_{j-1,j-1}^-1 are formed only for export
+// (k_form_phi_diag, k_form_phi_off, launched by gato_get_schur).
 // and a fourth for the right-hand side (also used by iterative refinement):
 //   k_form_rhs   row j:   gamma_j, L_j^-1 gamma_j, -Q_j^-1 q_j, -R_j^-1 r_j
 #include "gato_internal.cuh"
@@ -102,8 +104,6 @@ __global__ void k_form_diag(Work w, const float* __restrict__ A, const float* __
         f = warp_sum(f);
         if (lane_id() == 0) w.dlow[sol * w.sN + j] = 1.f / f;
     }
-    warp_gram_lower(sA, sO, n);
-    warp_copy(w.Pd + off, sO, nn);
     if (!ok && lane_id() == 0) atomicOr(status + sol, GATO_STATUS_NONPOSITIVE_PIVOT);
 }
 
@@ -129,7 +129,43 @@ __global__ void k_form_off(Work w)
     __syncwarp();
     warp_gemm<false, false>(n, n, n, s1, s2, s4, 1.f, false);
     warp_gemm<false, true>(n, n, n, s4, s3, w.Nh + oj, 1.f, false);
+}
+
+// The explicit Phi^-1 blocks for export: S_jj^-1 = L_j^-T L_j^-1 ...
+__global__ void k_form_phi_diag(Work w)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int n = w.n, N = w.N, nn = n * n;
+    const int warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+    const long g = (long)blockIdx.x * wpb + warp;
+    if (g >= (long)w.M * N) return;
+    const int sol = (int)(g / N), j = (int)(g % N);
+    float* sA = sm + (size_t)warp * 2 * nn;
+    float* sO = sA + nn;
+    const size_t off = sol * w.sNnn + (size_t)j * nn;
+    warp_copy(sA, w.Linv + off, nn);
+    __syncwarp();
+    warp_gram_lower(sA, sO, n);
+    warp_copy(w.Pd + off, sO, nn);
+}
+
+// ... and -S_jj^-1 S_{j,j-1} S_{j-1,j-1}^-1
+__global__ void k_form_phi_off(Work w)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int n = w.n, N = w.N, K = N - 1, nn = n * n;
+    const int warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+    const long g = (long)blockIdx.x * wpb + warp;
+    if (K < 1 || g >= (long)w.M * K) return;
+    const int sol = (int)(g / K), j = 1 + (int)(g % K);
+    float* s1 = sm + (size_t)warp * 4 * nn;
+    float* s2 = s1 + nn;
+    float* s3 = s2 + nn;
+    float* s4 = s3 + nn;
+    const size_t dj = sol * w.sNnn + (size_t)j * nn, dp = dj - nn;
+    const size_t oj = sol * w.sKnn + (size_t)(j - 1) * nn;
     warp_copy(s1, w.Pd + dj, nn);
+    warp_copy(s2, w.O + oj, nn);
     warp_copy(s3, w.Pd + dp, nn);
     __syncwarp();
     warp_gemm<false, false>(n, n, n, s1, s2, s4, 1.f, false);
@@ -278,11 +314,11 @@ cudaError_t launch_form_matrices(gato_handle* h, const float* Q, const float* R,
                                  cudaStream_t st)
 {
     const Work& w = h->w;
-    h->phi_pending = 0;
-    if (!h->force_smem_form && rows_formation_supported(w)) {
-        h->phi_pending = 1;
+    h->phi_pending = 1;  // formed on demand by gato_get_schur
+    h->phi_smem = 0;
+    if (!h->force_smem_form && rows_formation_supported(w))
         return launch_form_rows(h, Q, R, A, B, status, st);
-    }
+    h->phi_smem = 1;
     const size_t n = w.n, m = w.m, f = sizeof(float);
     const long knots = (long)w.M * w.N;
     cudaError_t e;
@@ -293,6 +329,15 @@ cudaError_t launch_form_matrices(gato_handle* h, const float* Q, const float* R,
                              status);
     if (e != cudaSuccess) return e;
     return launch_warp_per_item(k_form_off, (long)w.M * (w.N - 1), 4 * n * n * f, h, st, w);
+}
+
+cudaError_t launch_form_phi_smem(gato_handle* h, cudaStream_t st)
+{
+    const Work& w = h->w;
+    const size_t nn = (size_t)w.n * w.n * sizeof(float);
+    cudaError_t e = launch_warp_per_item(k_form_phi_diag, (long)w.M * w.N, 2 * nn, h, st, w);
+    if (e != cudaSuccess) return e;
+    return launch_warp_per_item(k_form_phi_off, (long)w.M * (w.N - 1), 4 * nn, h, st, w);
 }
 
 cudaError_t launch_form_rhs(gato_handle* h, int set, const float* q, const float* r,

@@ -108,6 +108,7 @@ struct gato_handle {
     int bdsv_kernel;        // GATO_BDSV_KERNEL_* selected by gato_set_bdsv_kernel
     int force_smem_form;    // GATO_FORM_SHARED selected by gato_set_form_kernel
     int phi_pending;        // the last formation left the explicit Phi^-1 blocks unformed
+    int phi_smem;           // ... and it ran the shared-memory kernels (form them there)
     cudaEvent_t ev[5];  // start, after form, after PCG, after refinement, after merit
     int ev_used[5];
     gato_stats last;
@@ -152,6 +153,7 @@ cudaError_t launch_form_rows(gato_handle* h, const float* Q, const float* R, con
                              const float* B, uint32_t* status, cudaStream_t st);
 // the explicit Phi^-1 blocks after a register formation (form_rows.cu)
 cudaError_t launch_form_phi(gato_handle* h, cudaStream_t st);
+cudaError_t launch_form_phi_smem(gato_handle* h, cudaStream_t st);
 cudaError_t launch_form_rhs(gato_handle* h, int set, const float* q, const float* r,
                             const float* e, const float* s0, size_t s0_stride, cudaStream_t st);
 cudaError_t launch_pcg(gato_handle* h, const gato_params* p, const float* lambda0,
