@@ -251,21 +251,24 @@ def test_rows_kernel_matches_oracle_and_generic(name, M, N, n, m):
 @pytest.mark.parametrize("rule", [gato.GATO_STOP_RESIDUAL, gato.GATO_STOP_PRECOND,
                                   gato.GATO_STOP_SCALED], ids=["residual", "precond", "scaled"])
 def test_rows_kernel_stopping_rules(rule):
-    """Each stopping rule stops the row kernel where it stops the generic one
-    (workload 3's sizes, unrefined), and its lambda is as close to the fp64
-    direct solution as the generic kernel's (the workload is ill-conditioned:
-    about 1700 iterations, so the two kernels' rounding alone moves lambda
-    by about 1e-3)."""
+    """Each stopping rule stops the row kernel with a lambda as close to the
+    fp64 direct solution as the generic kernel's, at about the same iteration
+    (workload 3's sizes, unrefined).  The workload is ill-conditioned (1300
+    to 1700 iterations): near fp32's attainable accuracy the iteration at
+    which the recursive residual crosses eps depends on rounding, and the two
+    kernels, which sum in different orders, differ by up to 12% there and
+    move lambda by about 1e-3; hence 15% here against 5% on the well
+    conditioned sizes."""
     w = WORKLOADS[3]
     prob = make_batch(w, M=3)
     p = params_for(w, stop_rule=rule, refine_steps=0)
     a = solve(prob, p, gato.GATO_PCG_ROWS)
     b = solve(prob, p, gato.GATO_PCG_GENERIC)
     assert not a["status"].any() and not b["status"].any()
-    assert np.abs(a["iters"] - b["iters"]).max() <= 0.05 * b["iters"].max() + 2
     for j in range(3):
         lam = oracle.direct_solve(oracle.solve_one(prob, j))[2]
         assert rel(a["lam"][j], lam) <= 2 * rel(b["lam"][j], lam) + 1e-5
+    assert np.abs(a["iters"] - b["iters"]).max() <= 0.15 * b["iters"].max() + 2
 
 
 def test_rows_kernel_chosen_for_small_states():
@@ -609,12 +612,15 @@ def test_batch_beyond_the_grid_yz_limit():
     check_solution(prob, ref, [0, 35000, 65534, 65535, 69999])
 
 
-@pytest.mark.parametrize("w", [WORKLOADS[1], WORKLOADS[4]], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [WORKLOADS[1], WORKLOADS[3], WORKLOADS[4]], ids=lambda w: w.name)
 def test_default_stop_rule_reaches_the_relative_residual(w):
     """The default rule stops on ||gamma - S lambda|| <= eps ||gamma|| of the
     updated residual: the true residual of the returned lambda, against the S
     and gamma the GPU formed (exported, evaluated in fp64), stays within a
-    small multiple of eps, and the iteration count tracks the fp64 oracle's."""
+    small multiple of eps, and the iteration count tracks the fp64 oracle's.
+    On the ill-conditioned workload 3 fp32 CG loses orthogonality and needs
+    20 to 35% more iterations than fp64 CG (any kernel: the generic one
+    too), so its upper bound is 1.5 times the oracle's."""
     M = 3
     prob = make_batch(w, M=M)
     p = params_for(w, refine_steps=0)
@@ -641,4 +647,5 @@ def test_default_stop_rule_reaches_the_relative_residual(w):
         Dj, Oj, gam, _ = oracle.schur(oracle.solve_one(prob, j))
         Pd, Po, _ = oracle.stair(Dj, Oj)
         _, it, ok = oracle.pcg(Dj, Oj, Pd, Po, gam, w.pcg_eps, 5000, stop_rule=0)
-        assert ok and it * 0.9 - 3 <= int(iters[j]) <= it * 1.2 + 5, (j, it, iters[j])
+        upper = 1.5 if w.index == 3 else 1.2
+        assert ok and it * 0.9 - 3 <= int(iters[j]) <= it * upper + 5, (j, it, iters[j])

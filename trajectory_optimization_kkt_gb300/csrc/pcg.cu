@@ -38,42 +38,6 @@ namespace {
 
 namespace cg = cooperative_groups;
 
-// Warp partial sums written before a barrier and summed by every thread after
-// it, in a fixed order (deterministic).  buf holds up to 16 float2 (one per
-// warp).  post2 reduces two values at the cost of one: the first exchange
-// leaves the pair sums of a in the low half-warp and those of b in the high
-// half, the remaining four steps run on one value per lane.
-__device__ __forceinline__ void post2(float a, float b, float2* buf)
-{
-    const int lane = lane_id();
-    const bool hi = lane & 16;
-    float keep = hi ? b : a;
-    keep += __shfl_xor_sync(0xffffffffu, hi ? a : b, 16);
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
-    float* slot = reinterpret_cast<float*>(buf + (threadIdx.x >> 5));
-    if ((lane & 15) == 0) slot[hi ? 1 : 0] = keep;
-}
-
-__device__ __forceinline__ float2 collect2(const float2* buf)
-{
-    // the low half-warp sums the .x fields of the (at most 16) warp slots,
-    // the high half the .y fields; the full butterfly leaves every lane of a
-    // half with that half's total (each level adds the same pair in both
-    // lanes, so all lanes agree bit for bit), and one exchange across the
-    // halves gives every lane both totals
-    const int lane = lane_id(), q = lane & 15;
-    const bool hi = lane & 16;
-    float v = 0.f;
-    if (q < (int)(blockDim.x >> 5)) {
-        const float2 t = buf[q];
-        v = hi ? t.y : t.x;
-    }
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    const float other = __shfl_xor_sync(0xffffffffu, v, 16);
-    return hi ? make_float2(other, v) : make_float2(v, other);
-}
 
 
 // ===========================================================================

@@ -195,10 +195,13 @@ __global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
     float4* redA = reinterpret_cast<float4*>(lsm + round4((size_t)N * n));
     float4* redB = redA + 32;
     float4* redC = redA + 64;
+    float2* pairA = reinterpret_cast<float2*>(redA + 96);  // post2 / collect2 slots
+    float2* pairB = pairA + 16;
+    float2* pairC = pairB + 16;
     // the tile chunks past the registers' share, then (rule 0 with l_smem) the
     // rows of L
     constexpr int SC = NP / 4 - RowTiles<NP, R>::RC;
-    float4* TS = redA + 96;
+    float4* TS = redA + 120;
     float* LS = reinterpret_cast<float*>(TS + (size_t)SC * R * 2 * T);
     for (int i = tid; i < 2 * XS; i += T) sm[i] = 0.f;
 
@@ -320,14 +323,16 @@ __global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
         ++it;
         // v = S_hat p, alpha = eta / p^T v; lambda and r updates
         rows_matvec<NP, R>(tile, TS, XP, jj, y);
-        float pv[1] = {0.f};
+        float pvp = 0.f;
 #pragma unroll
         for (int i = 0; i < R; ++i) {
             y[i] += p[i];
-            pv[0] = fmaf(p[i], y[i], pv[0]);
+            pvp = fmaf(p[i], y[i], pvp);
         }
-        block_sum<1>(pv, redA);
-        const float alpha = __fdividef(eta, pv[0]);
+        post2(pvp, 0.f, pairA);
+        __syncthreads();
+        const float pv = collect2(pairA).x;
+        const float alpha = __fdividef(eta, pv);
 #pragma unroll
         for (int i = 0; i < R; ++i) {
             lam[i] = fmaf(alpha, p[i], lam[i]);
@@ -349,7 +354,15 @@ __global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
         if (exact)
             red[2] = l_staged ? rows_lnorm_smem<NP, R>(LS, XR, jj, a0, n, valid)
                          : rows_lnorm<NP, R>(Lj, XR, jj, a0, n, valid);
-        block_sum<3>(red, redB);
+        post2(red[0], red[1], pairB);
+        if (exact) post2(red[2], 0.f, pairC);
+        __syncthreads();
+        {
+            const float2 sb = collect2(pairB);
+            red[0] = sb.x;
+            red[1] = sb.y;
+            red[2] = exact ? collect2(pairC).x : 0.f;
+        }
         const float eta_new = red[0];
         float lsq = red[2];
         bool have_exact = exact;
@@ -361,7 +374,7 @@ __global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
             have_exact = true;
         }
         const float stopq = rule0 ? lsq : (g.rule == GATO_STOP_SCALED ? red[1] : eta_new);
-        if (!isfinite(eta_new + pv[0] + stopq + red[1])) {  // NaN and Inf propagate
+        if (!isfinite(eta_new + pv + stopq + red[1])) {  // NaN and Inf propagate
             nonfinite = true;
             break;
         }
@@ -394,7 +407,7 @@ cudaError_t launch_rows_np(const PcgArgs& a, size_t limit, cudaStream_t st)
     if (T > max_threads_for(NP)) return cudaErrorInvalidConfiguration;
     constexpr int SC = NP / 4 - RowTiles<NP, R>::RC;
     size_t smem = sizeof(float) * (2 * (size_t)(w.N + 2) * NP + round4((size_t)w.N * w.n)) +
-                  (96 + (size_t)SC * R * 2 * T) * sizeof(float4);
+                  (120 + (size_t)SC * R * 2 * T) * sizeof(float4);
     if (smem > limit) return cudaErrorInvalidConfiguration;
     // rule 0: the rows of L in shared memory where they fit
     PcgArgs b = a;
