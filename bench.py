@@ -38,7 +38,7 @@ WORKLOAD_INDEX = 4  # M=256, N=128, n=14, m=7
 # kernel source it was taken on (sha256 prefix of csrc/pcg.cu), null
 # otherwise.  Captured on 152 solves (one block per SM) and scaled
 # by the solves processed to the 256-solve launch (89.78 MB x 256 / 152).
-PCG_TRAFFIC = {"pcg_sha": "2a736ae016406569", "bytes_per_launch": 151210092}
+PCG_TRAFFIC = {"pcg_sha": "34571eb583c1e516", "bytes_per_launch": 150718572}
 
 FP32_LANES_PER_SM = 128  # FFMA lanes per SM (4 sub-partitions x 32)
 
@@ -55,9 +55,12 @@ def launches_per_solve(linsys, refine_steps):
     return 5 + solve + 4 * refine_steps
 
 
-def _src_sha(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def _src_sha(*paths):
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def _peaks():
@@ -723,7 +726,7 @@ def run_gpu(args, world, rank, local):
                            + N * n + K * m + (w.n_alpha + 1) + 1)
     merit_s = statistics.mean(merit_us) * 1e-6
     merit_gbs = merit_bytes / merit_s / 1e9
-    sha = _src_sha(os.path.join(_build.CSRC, "pcg.cu"))
+    sha = _src_sha(os.path.join(_build.CSRC, "pcg.cu"), os.path.join(_build.CSRC, "pcg_common.cuh"))
     # the ncu capture behind the traffic figure is of the default workload
     traffic = (PCG_TRAFFIC["bytes_per_launch"]
                if PCG_TRAFFIC["pcg_sha"] == sha and args.workload == WORKLOAD_INDEX
