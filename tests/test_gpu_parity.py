@@ -156,6 +156,23 @@ def test_solve_kkt_matches_oracle(w):
     check_solution(prob, out, range(M), w.n_alpha, w.beta, w.mu)
 
 
+@pytest.mark.parametrize("w", [WORKLOADS[1], WORKLOADS[2], WORKLOADS[3]], ids=lambda w: w.name)
+def test_full_batch_in_the_benchmark_configuration(w):
+    """Each workload at its full batch with the default kernels and parts (as
+    bench.py --workloads times it), sampled against the oracle at both ends
+    of every part."""
+    prob = make_batch(w)
+    out = solve(prob, params_for(w))
+    assert not (out["status"] & ~gato.GATO_STATUS_PCG_MAX_ITERS).any(), out["status"]
+    parts = 1 if w.M < 64 else (2 if w.M < 128 else 4)
+    edges = sorted({j for c in range(parts) for j in (c * w.M // parts, (c + 1) * w.M // parts - 1)})
+    # workload 2's cap (500 iterations) can stop a few solves: those are the
+    # cap tests' concern; every other solve at a part edge is checked
+    ok = [j for j in edges if not out["status"][j]]
+    assert 2 * len(ok) >= len(edges)
+    check_solution(prob, out, ok, w.n_alpha, w.beta, w.mu)
+
+
 def test_unrefined_solve_of_workload4():
     w = WORKLOADS[4]
     prob = make_batch(w, M=8)
