@@ -362,15 +362,17 @@ def run_throughput_sweep(args, local):
 def _pcg_kernel_name(N, n):
     """The PCG kernel GATO_PCG_AUTO picks for these sizes (the rules of
     launch_pcg_ex and launch_pcg_rows: the register-row kernel's rows per
-    thread keep its two row tiles within 144 floats, and its block within
-    the registers)."""
+    thread keep its two row tiles within 216 floats, and its block within
+    the registers, at most 256 threads with more than one row per thread)."""
     if 7 <= n <= 16:
         return "k_pcg_wide" if N <= 128 else ("k_pcg_cluster" if N <= 512 else "k_pcg_generic")
     if 16 < n <= 64:
         NP = next(p for p in (20, 24, 28, 32, 36, 40, 48, 56, 64) if n <= p)
-        R = max(1, 144 // (2 * NP))
+        R = max(1, 216 // (2 * NP))
+        raw = 65536 // (2 * R * NP + 56) // 32 * 32
+        limit = min(256, raw) if R > 1 else min(1024, raw)
         T = max(64, (N * -(-n // R) + 31) // 32 * 32)
-        if T <= min(1024, 65536 // (2 * R * NP + 56) // 32 * 32):
+        if T <= limit:
             return "k_pcg_rows"
     return "k_pcg_generic"
 

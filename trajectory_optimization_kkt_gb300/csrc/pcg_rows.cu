@@ -16,7 +16,7 @@
 // in registers: a product reads only the two neighbouring knots' vectors,
 // broadcast from shared memory as 128-bit loads, and nothing else is
 // exchanged.  NP is n padded to a multiple of 4 (the vectors' knot stride,
-// padding slots zero), R keeps the two row tiles within 144 floats.  The
+// padding slots zero), R keeps the two row tiles within 216 floats.  The
 // vectors live in registers with their owners and in shared memory for the
 // neighbours; a guard knot of zeros before knot 0 and after knot N-1 stands
 // for the missing neighbours.
@@ -31,16 +31,19 @@
 namespace gato {
 namespace {
 
-// rows per thread: the two tiles (2 R NP floats) within 144 registers
-constexpr int rows_for(int NP) { return 144 / (2 * NP) > 0 ? 144 / (2 * NP) : 1; }
+// rows per thread: the two tiles (2 R NP floats) within 216 registers
+constexpr int rows_for(int NP) { return 216 / (2 * NP) > 0 ? 216 / (2 * NP) : 1; }
 
 // threads per block the registers allow: 64K registers over the tiles plus
-// about 56 for the rest, in whole warps
+// about 56 for the rest, in whole warps; with more than one row per thread
+// at most 256 threads, so that no SM sub-partition holds more than two warps
+// and a thread may use 255 registers (fewer, fuller threads measured faster
+// than more threads with spilled tiles)
+constexpr int max_threads_raw(int NP) { return (65536 / (2 * rows_for(NP) * NP + 56)) / 32 * 32; }
 constexpr int max_threads_for(int NP)
 {
-    return (65536 / (2 * rows_for(NP) * NP + 56)) / 32 * 32 > 1024
-               ? 1024
-               : (65536 / (2 * rows_for(NP) * NP + 56)) / 32 * 32;
+    return rows_for(NP) > 1 ? (max_threads_raw(NP) > 256 ? 256 : max_threads_raw(NP))
+                            : (max_threads_raw(NP) > 1024 ? 1024 : max_threads_raw(NP));
 }
 
 // The registers per thread the launch bound leaves: 64K over the warps of
