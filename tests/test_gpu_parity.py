@@ -249,6 +249,9 @@ ROWS = [
     ("n27_m9", 2, 11, 27, 9), ("n32_m4", 2, 8, 32, 4), ("n36_m12", 2, 16, 36, 12),
     ("n40_m10", 1, 6, 40, 10), ("n45_m7", 1, 5, 45, 7), ("n53_m3", 1, 4, 53, 3),
     ("n64_m16", 1, 4, 64, 16), ("N1_n36", 2, 1, 36, 12), ("n36_N40_generic", 1, 40, 36, 12),
+    # the largest blocks the register budget allows, and one knot past them
+    ("n36_N18_max", 1, 18, 36, 12), ("n36_N19_generic", 1, 19, 36, 12),
+    ("n24_N42_max", 1, 42, 24, 8), ("n64_N5_max", 1, 5, 64, 8),
 ]
 
 
