@@ -20,6 +20,14 @@
 namespace gato {
 namespace {
 
+// floats per warp of k_form_inv: sQ (n x n) and a second slice that holds
+// L^-1, later the R part (3 m^2 + n m) and A (n^2)
+__host__ __device__ __forceinline__ int form_inv_floats(int n, int m)
+{
+    const int rest = 3 * m * m + n * m > n * n ? 3 * m * m + n * m : n * n;
+    return (n * n + rest + 3) & ~3;
+}
+
 __global__ void k_form_inv(Work w, const float* __restrict__ Q, const float* __restrict__ R,
                            const float* __restrict__ A, const float* __restrict__ B,
                            uint32_t* status)
@@ -31,10 +39,11 @@ __global__ void k_form_inv(Work w, const float* __restrict__ Q, const float* __r
     const long g = (long)blockIdx.x * wpb + warp;
     if (g >= (long)w.M * N) return;
     const int sol = (int)(g / N), k = (int)(g % N);
-    float* sQ = sm + (size_t)warp * (3 * nn + 3 * mm + nm);
+    // two n x n slices per warp (more warps per SM): L and then Q^-1 in sQ;
+    // L^-1 in sT, then the R part (R's factor, R^-1 rows, R^-1, B), then A
+    float* sQ = sm + (size_t)warp * form_inv_floats(n, m);
     float* sT = sQ + nn;
-    float* sQi = sT + nn;
-    float* sR = sQi + nn;
+    float* sR = sT;
     float* sRt = sR + mm;
     float* sRi = sRt + mm;
     float* sB = sRi + mm;
@@ -42,7 +51,8 @@ __global__ void k_form_inv(Work w, const float* __restrict__ Q, const float* __r
     warp_copy(sQ, Q + ((size_t)sol * N + k) * nn, nn);
     bool ok = warp_cholesky(sQ, n);
     warp_lower_inverse(sQ, sT, n);
-    warp_gram_lower(sT, sQi, n);
+    warp_gram_lower(sT, sQ, n);  // Q^-1 over L (read no more)
+    float* sQi = sQ;
     warp_copy(w.Qinv + sol * w.sNnn + (size_t)k * nn, sQi, nn);
     if (k < N - 1) {
         const size_t K = (size_t)(N - 1);
@@ -51,11 +61,12 @@ __global__ void k_form_inv(Work w, const float* __restrict__ Q, const float* __r
         warp_lower_inverse(sR, sRt, m);
         warp_gram_lower(sRt, sRi, m);
         warp_copy(w.Rinv + sol * w.sKmm + (size_t)k * mm, sRi, mm);
-        warp_copy(sQ, A + ((size_t)sol * K + k) * nn, nn);  // sQ now holds A_k
         warp_copy(sB, B + ((size_t)sol * K + k) * nm, nm);
         __syncwarp();
-        warp_gemm<false, false>(n, n, n, sQ, sQi, w.O + sol * w.sKnn + (size_t)k * nn, -1.f, false);
         warp_gemm<false, false>(n, m, m, sB, sRi, w.V + sol * w.sKnm + (size_t)k * nm, 1.f, false);
+        warp_copy(sT, A + ((size_t)sol * K + k) * nn, nn);  // the R part is done: A_k
+        __syncwarp();
+        warp_gemm<false, false>(n, n, n, sT, sQi, w.O + sol * w.sKnn + (size_t)k * nn, -1.f, false);
     }
     if (!ok && lane_id() == 0) atomicOr(status + sol, GATO_STATUS_NONPOSITIVE_PIVOT);
 }
@@ -116,19 +127,19 @@ __global__ void k_form_off(Work w)
     const long g = (long)blockIdx.x * wpb + warp;
     if (K < 1 || g >= (long)w.M * K) return;
     const int sol = (int)(g / K), j = 1 + (int)(g % K);
-    float* s1 = sm + (size_t)warp * 4 * nn;
+    float* s1 = sm + (size_t)warp * 3 * nn;
     float* s2 = s1 + nn;
-    float* s3 = s2 + nn;
-    float* s4 = s3 + nn;
+    float* s4 = s2 + nn;
     const size_t dj = sol * w.sNnn + (size_t)j * nn, dp = dj - nn;
     const size_t oj = sol * w.sKnn + (size_t)(j - 1) * nn;
 
     warp_copy(s1, w.Linv + dj, nn);
     warp_copy(s2, w.O + oj, nn);
-    warp_copy(s3, w.Linv + dp, nn);
     __syncwarp();
     warp_gemm<false, false>(n, n, n, s1, s2, s4, 1.f, false);
-    warp_gemm<false, true>(n, n, n, s4, s3, w.Nh + oj, 1.f, false);
+    warp_copy(s1, w.Linv + dp, nn);  // L_j^-1 is read no more: L_{j-1}^-1
+    __syncwarp();
+    warp_gemm<false, true>(n, n, n, s4, s1, w.Nh + oj, 1.f, false);
 }
 
 // The explicit Phi^-1 blocks for export: S_jj^-1 = L_j^-T L_j^-1 ...
@@ -322,13 +333,13 @@ cudaError_t launch_form_matrices(gato_handle* h, const float* Q, const float* R,
     const size_t n = w.n, m = w.m, f = sizeof(float);
     const long knots = (long)w.M * w.N;
     cudaError_t e;
-    e = launch_warp_per_item(k_form_inv, knots, (3 * n * n + 3 * m * m + n * m) * f, h, st,
-                             w, Q, R, A, B, status);
+    e = launch_warp_per_item(k_form_inv, knots, form_inv_floats((int)n, (int)m) * f, h, st, w,
+                             Q, R, A, B, status);
     if (e != cudaSuccess) return e;
     e = launch_warp_per_item(k_form_diag, knots, (4 * n * n + 2 * n * m) * f, h, st, w, A, B,
                              status);
     if (e != cudaSuccess) return e;
-    return launch_warp_per_item(k_form_off, (long)w.M * (w.N - 1), 4 * n * n * f, h, st, w);
+    return launch_warp_per_item(k_form_off, (long)w.M * (w.N - 1), 3 * n * n * f, h, st, w);
 }
 
 cudaError_t launch_form_phi_smem(gato_handle* h, cudaStream_t st)
