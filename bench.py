@@ -124,6 +124,32 @@ class ClockSampler:
                 "samples": len(self.rows)}
 
 
+def _fp32_probe(torch, gato, dev, local):
+    """Measured fp32 FMA throughput of this GPU (TFLOP/s, 2 flops per FMA):
+    the library's probe kernel (independent FMA chains in every thread of
+    four 256-thread blocks per SM), scalar fma.rn.f32 and packed
+    fma.rn.f32x2, best of five launches of about 3 ms each after warm-up,
+    timed with CUDA events; SM clocks sampled meanwhile."""
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, threads, trips = 4 * n_sm, 256, 4096
+    sink = torch.zeros(blocks, dtype=torch.float32, device=dev)
+    res = {}
+    with ClockSampler(local) as clk:
+        for name, packed in (("ffma", 0), ("ffma2", 1)):
+            best = 0.0
+            for k in range(8):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                flops = gato.probe_fp32(packed, blocks, threads, trips, sink)
+                b.record()
+                b.synchronize()
+                if k >= 3:
+                    best = max(best, flops / (a.elapsed_time(b) * 1e-3) / 1e12)
+            res[name] = best
+    res["clocks"] = clk.summary()
+    return res
+
+
 def _dist_env():
     from trajectory_optimization_kkt_gb300.replicas import from_env
     r = from_env()
@@ -140,7 +166,7 @@ def run_reference(args, world, rank):
     from trajectory_optimization_kkt_gb300.workloads import WORKLOADS, make_batch
     w = WORKLOADS[args.workload]
     cores = os.cpu_count() or 1
-    per_step = max(cores, 16)  # solves per timed step: a bounded sample of the batch
+    per_step = w.M  # every step solves the whole batch, as the GPU arm's step does
     prob = make_batch(w, M=per_step)
     oracle.build()
     solves = [oracle.solve_one(prob, j) for j in range(per_step)]
@@ -162,9 +188,10 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * sec / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "pcg_iters_per_sec": iters / sec,
-        "config": _config(w, per_step_solves=per_step),
+        "config": _config(w),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"{per_step} of the {w.M} solves per step, spawn pool of {cores}"},
+                         "sample": f"the whole batch of {w.M} solves per step, spawn pool of "
+                                   f"{cores}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -181,6 +208,7 @@ def _config(w, **extra):
          "pcg_max_iters": w.pcg_max_iters, "stop_rule": "relative residual ||r||<=eps||gamma||",
          "n_alpha": w.n_alpha, "beta": w.beta, "mu": w.mu,
          "refine_steps": w.refine_steps, "refine_eps": w.refine_eps,
+         "pcg_precision": "double-float" if w.pcg_precision else "fp32",
          "l2": "flushed before every timed step (256 MB write)"}
     c.update(extra)
     return c
@@ -299,10 +327,8 @@ def run_sweep(args, local):
             with gato.Solver(M, N, w.n, w.m) as s:
                 out = s.outputs(w.n_alpha)
                 for name, ls in LINSYS.items():
-                    p = gato.default_params(pcg_eps=w.pcg_eps, pcg_max_iters=4000,
-                                            n_alpha=w.n_alpha, beta=w.beta, mu=w.mu,
-                                            refine_steps=w.refine_steps,
-                                            refine_eps=w.refine_eps, linsys=ls)
+                    p = gato.default_params(**{**w.solver_settings(), "pcg_max_iters": 4000},
+                                            linsys=ls)
                     ms, stages, iters, bad = _time_solver(torch, s, p, d, out, args.steps,
                                                           flush, stream)
                     print(json.dumps({"sweep": "linsys", "M": M, "N": N, "n": w.n, "m": w.m,
@@ -335,10 +361,7 @@ def run_throughput_sweep(args, local):
             d = {k: torch.from_numpy(v).to(dev) for k, v in prob.items()}
             with gato.Solver(M, N, w.n, w.m) as s:
                 out = s.outputs(w.n_alpha)
-                p = gato.default_params(pcg_eps=w.pcg_eps, pcg_max_iters=w.pcg_max_iters,
-                                        n_alpha=w.n_alpha, beta=w.beta, mu=w.mu,
-                                        refine_steps=w.refine_steps, refine_eps=w.refine_eps,
-                                        linsys=LINSYS["pcg"])
+                p = gato.default_params(**w.solver_settings(), linsys=LINSYS["pcg"])
                 ms, stages, iters, bad = _time_solver(torch, s, p, d, out, args.steps, flush,
                                                       stream)
                 # one part: the PCG stage (solve) plus the refinement stage (its
@@ -359,11 +382,16 @@ def run_throughput_sweep(args, local):
                       flush=True)
 
 
-def _pcg_kernel_name(N, n):
+def _pcg_kernel_name(N, n, precision=0):
     """The PCG kernel GATO_PCG_AUTO picks for these sizes (the rules of
     launch_pcg_ex and launch_pcg_rows: the register-row kernel's rows per
     thread keep its two row tiles within 216 floats, and its block within
-    the registers, at most 256 threads with more than one row per thread)."""
+    the registers, at most 256 threads with more than one row per thread);
+    the double-float kernel for the main solve when that precision is set
+    (the refinement's corrections then run in the fp32 kernel named after
+    the plus sign)."""
+    if precision:
+        return "k_pcg_ff + " + _pcg_kernel_name(N, n)
     if 7 <= n <= 16:
         return "k_pcg_wide" if N <= 128 else ("k_pcg_cluster" if N <= 512 else "k_pcg_generic")
     if 16 < n <= 64:
@@ -394,16 +422,14 @@ def run_workloads(args, local):
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     hbm_peak, peak_kind, sm_mhz = _peaks()
-    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
-    alu_peak_tf = n_sm * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    probe = _fp32_probe(torch, gato, dev, local)
+    alu_peak_tf = max(probe["ffma"], probe["ffma2"])
     steps = min(args.steps, 10)
     for w in WORKLOADS:
         M, N, n, m = w.M, w.N, w.n, w.m
         prob = make_batch(w)
         d = {k: torch.from_numpy(v).to(dev) for k, v in prob.items()}
-        p = gato.default_params(pcg_eps=w.pcg_eps, pcg_max_iters=w.pcg_max_iters,
-                                n_alpha=w.n_alpha, beta=w.beta, mu=w.mu,
-                                refine_steps=w.refine_steps, refine_eps=w.refine_eps)
+        p = gato.default_params(**w.solver_settings())
         with gato.Solver(M, N, n, m) as s:
             out = s.outputs(w.n_alpha)
             ms, stages, iters, bad = _time_solver(torch, s, p, d, out, steps, flush, stream)
@@ -415,14 +441,15 @@ def run_workloads(args, local):
         merit_bytes = 4 * M * (N * n * n + K * (m * m + n * n + n * m) + N * n + K * m + K * n
                                + n + N * n + K * m + (w.n_alpha + 1) + 1)
         merit_gbs = merit_bytes / (stages["merit"] * 1e-6) / 1e9
-        pcg_kernel = _pcg_kernel_name(N, n)
+        pcg_kernel = _pcg_kernel_name(N, n, w.pcg_precision)
         row = {"workload": w.name, "M": M, "N": N, "n": n, "m": m, "parts": parts,
                "solves_per_s": M / (ms / 1000.0), "ms_per_call": ms,
                "pcg_iters_per_sec": iters / (ms / 1000.0), "pcg_iters_per_solve": iters / M,
                "stage_us": stages, "status_nonzero_solves": bad,
                "pcg_roofline": {"bound": "alu", "kernel": pcg_kernel, "achieved": achieved_tf,
                                 "peak": alu_peak_tf, "unit": "TFLOP/s",
-                                "frac": achieved_tf / alu_peak_tf},
+                                "frac": achieved_tf / alu_peak_tf,
+                                "peak_basis": "fp32 FMA probe in this run, of measured"},
                "merit_roofline": {"bound": "hbm", "achieved": merit_gbs, "peak": hbm_peak,
                                   "unit": "GB/s", "frac": merit_gbs / hbm_peak,
                                   "peak_kind": peak_kind,
@@ -602,10 +629,7 @@ def run_gpu(args, world, rank, local):
     d = {k: torch.from_numpy(v).to(dev) for k, v in prob.items()}
     s = gato.Solver(M, w.N, w.n, w.m)
     out = s.outputs(w.n_alpha)
-    p = gato.default_params(pcg_eps=w.pcg_eps, pcg_max_iters=w.pcg_max_iters,
-                            n_alpha=w.n_alpha, beta=w.beta, mu=w.mu,
-                            refine_steps=w.refine_steps, refine_eps=w.refine_eps,
-                            linsys=LINSYS[args.linsys])
+    p = gato.default_params(**w.solver_settings(), linsys=LINSYS[args.linsys])
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     launches_per_step = launches_per_solve(args.linsys, w.refine_steps)
@@ -717,7 +741,10 @@ def run_gpu(args, world, rank, local):
     achieved_tf = flops_it * iters_per_step / (pcg_stage_us * 1e-6) / 1e12
     hbm_peak, peak_kind, sm_mhz = _peaks()
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
-    alu_peak_tf = n_sm * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    nominal_tf = n_sm * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    probe = _fp32_probe(torch, gato, dev, local)
+    # the roofline's peak: the faster of the two measured FMA forms
+    alu_peak_tf = max(probe["ffma"], probe["ffma2"])
     # the pages' streaming model: packed S and Phi^-1 read once per iteration
     bytes_it = 2 * (N * n * (n + 1) // 2 + (N - 1) * n * n) * 4
     stream_gbs = bytes_it * iters_per_step / (pcg_stage_us * 1e-6) / 1e9
@@ -752,10 +779,7 @@ def run_gpu(args, world, rank, local):
     alternatives = {}
     if args.linsys == "pcg" and not args.no_alternatives and rank == 0:
         for name in ("bdsv", "bdsv_chrono"):
-            pa = gato.default_params(pcg_eps=w.pcg_eps, pcg_max_iters=w.pcg_max_iters,
-                                     n_alpha=w.n_alpha, beta=w.beta, mu=w.mu,
-                                     refine_steps=w.refine_steps, refine_eps=w.refine_eps,
-                                     linsys=LINSYS[name])
+            pa = gato.default_params(**w.solver_settings(), linsys=LINSYS[name])
             ms, stages, _, bad = _time_solver(torch, s, pa, d, out, min(args.steps, 10), flush,
                                               stream)
             alternatives[name] = {"solves_per_s": M / (ms / 1000.0), "ms_per_step": ms,
@@ -781,9 +805,19 @@ def run_gpu(args, world, rank, local):
                          "bound": "alu", "achieved": achieved_tf, "peak": alu_peak_tf,
                          "unit": "TFLOP/s", "frac": achieved_tf / alu_peak_tf,
                          "traffic": traffic,
-                         "kernel": _pcg_kernel_name(N, n) + " (solve + refinement launches)",
-                         "peak_basis": f"{n_sm} SMs x {FP32_LANES_PER_SM} FFMA lanes x 2 flop x "
-                                       f"{sm_mhz:.0f} MHz (max SM clock, {peak_kind})",
+                         "kernel": _pcg_kernel_name(N, n, w.pcg_precision)
+                                   + " (solve + refinement launches)",
+                         "peak_basis": "measured in this run: fp32 FMA probe "
+                                       "(gato_probe_fp32), faster of scalar and packed form; "
+                                       "of measured",
+                         "peak_probe": {"ffma_tflops": probe["ffma"],
+                                        "ffma2_tflops": probe["ffma2"],
+                                        "sm_mhz_median": probe["clocks"].get("sm_mhz"),
+                                        "reasons": probe["clocks"].get("reasons")},
+                         "peak_nominal": nominal_tf,
+                         "peak_nominal_basis": f"{n_sm} SMs x {FP32_LANES_PER_SM} FFMA lanes x "
+                                               f"2 flop x {sm_mhz:.0f} MHz (max SM clock)",
+                         "frac_of_nominal": achieved_tf / nominal_tf,
                          "flops_per_solve_iteration": flops_it,
                          "iterations_per_step": iters_per_step},
             "merit_roofline": {"bound": "hbm", "achieved": merit_gbs, "peak": hbm_peak,
@@ -793,10 +827,13 @@ def run_gpu(args, world, rank, local):
                                          else "k_merit_fused",
                                "knot_candidates_per_s":
                                    M * N * (w.n_alpha + 1) / merit_s},
-            "hbm_stream_model": {"achieved": stream_gbs, "peak": hbm_peak, "unit": "GB/s",
-                                 "frac": stream_gbs / hbm_peak, "peak_kind": peak_kind,
-                                 "note": "S and Phi^-1 bytes per iteration as if streamed; "
-                                         "the kernel keeps them on chip"},
+            "hbm_stream_model": {"equivalent_gbs": stream_gbs, "hbm_gbs": hbm_peak,
+                                 "equivalent_over_hbm": stream_gbs / hbm_peak,
+                                 "note": "the rate at which the pages' design would have to "
+                                         "stream packed S and Phi^-1 from memory to match "
+                                         "this step; not a roofline fraction: the kernel "
+                                         "keeps the operator on chip and moves none of "
+                                         "these bytes"},
             "e2e": None if args.no_e2e else {
                 "value": solves / (e2e_ms / 1000.0), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

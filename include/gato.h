@@ -65,6 +65,10 @@ extern "C" {
 #define GATO_STATUS_LINESEARCH_FAILED 4u  /* no candidate beat M(0); best = -1     */
 #define GATO_STATUS_NONFINITE 8u          /* a NaN/Inf reached a PCG reduction or
                                              a merit value                          */
+#define GATO_STATUS_BOUNDS 16u            /* library built with GATO_DEBUG_BOUNDS
+                                             only: a device index check failed and
+                                             the access was skipped (never set by
+                                             the normal build)                      */
 
 /* PCG stopping rules (GATO paper Sec. II: "up to tolerance eps") */
 #define GATO_STOP_RESIDUAL 0       /* ||gamma - S lambda||_2 <= eps ||gamma||_2   */
@@ -90,6 +94,23 @@ extern "C" {
                                       two coupling blocks around a knot per
                                       thread) for any n <= 64 where its block
                                       fits, else as GATO_PCG_AUTO                 */
+
+/* Arithmetic of the main PCG solve (gato_params.pcg_precision).  The
+ * iteration count of CG in finite precision grows with the rounding unit:
+ * on long, poorly conditioned horizons fp32 PCG needs 3-25 % more iterations
+ * than fp64 PCG to reach the same relative residual, and a stated
+ * iteration cap can stop it first.  The double-float kernel carries the
+ * vectors, products, inner products and CG scalars as pairs of floats
+ * (about 48 significand bits), at fp32 instruction speed, on the operator
+ * formed in fp32; it follows the fp64 iteration count closely and costs
+ * several times the fp32 kernels' time per iteration. */
+#define GATO_PCG_PRECISION_FP32 0  /* fp32 vectors and sums (default)           */
+#define GATO_PCG_PRECISION_FF 1    /* double-float: one block per solve, one
+                                      thread per row of S (two when N n > 1024),
+                                      any n <= 64 with N n <= 2048 (N n <= 1024
+                                      when n > 16) and the blocks in shared
+                                      memory; larger sizes are rejected with
+                                      GATO_ERR_UNSUPPORTED                       */
 
 /* Linear solver of S lambda = gamma (gato_params.linsys).  The direct solver
  * (bdsv) factors the block-tridiagonal S exactly instead of iterating; the
@@ -148,6 +169,9 @@ typedef struct gato_params {
     int linsys;          /* GATO_LINSYS_* (default GATO_LINSYS_AUTO)              */
     int bdsv_horizon;    /* GATO_LINSYS_AUTO: direct solve when N >= bdsv_horizon
                             (default 256); >= 1                                    */
+    int pcg_precision;   /* GATO_PCG_PRECISION_* of the main PCG solve (default
+                            GATO_PCG_PRECISION_FP32); refinement corrections are
+                            always solved in fp32                                  */
 } gato_params;
 
 /* SQP loop on a linear model (gato_sqp_linear). */
@@ -181,9 +205,10 @@ void gato_default_params(gato_params* p);
 void gato_default_sqp_params(gato_sqp_params* sp);
 
 /* Creates a solver for M solves of N knots, n states and m controls on the
- * current CUDA device and allocates its device workspace (cudaMalloc; about
- * 4 M (12 N n^2 + (N-1)(m^2 + n m) + 17 N n + 6 (N-1) m + 66 N + 37) bytes).  *h
- * receives the handle, which the caller releases with gato_destroy.  Errors: INVALID_ARG (h NULL, M, N, n or
+ * current CUDA device and allocates its device workspace (one cudaMalloc of
+ * the bytes given at gato_solve_kkt_noalloc below, plus 512 bytes for each of
+ * GATO_MAX_PARTS possible parts).  *h receives the handle, which the caller
+ * releases with gato_destroy.  Errors: INVALID_ARG (h NULL, M, N, n or
  * m < 1), UNSUPPORTED (n or m above the limits), NO_MEMORY, CUDA. */
 int gato_create(gato_handle** h, int M, int N, int n, int m);
 
@@ -348,13 +373,17 @@ int gato_sqp_linear(gato_handle* h, const gato_params* p, const gato_sqp_params*
  * allocation.  Arguments are those of gato_solve_kkt plus the sizes (M, N,
  * n, m); the caller still provides every input and output.  The solver's
  * scratch is one static device array of GATO_NOALLOC_MAX_BYTES that every GPU
- * loading this library holds until the process exits; a problem needs about
- * 4 M (12 N n^2 + (N-1)(m^2 + n m) + 17 N n + 6 (N-1) m + 66 N + 37) bytes of it
- * (each array rounded up to 64 floats), and larger problems are rejected
- * with GATO_ERR_UNSUPPORTED before
+ * loading this library holds until the process exits; a problem needs
+ *   4 (M (9 r(N n^2) + 3 r((N-1) n^2) + r((N-1) m^2) + r((N-1) n m) + 17 r(N n)
+ *        + 6 r((N-1) m) + 2 r(N) + 64 N + 36) + M + 64) bytes of it,
+ *   r(x) = max(64, x rounded up to a multiple of 64)
+ * (exactly; for instance 46 solves of N = 64, n = 14, m = 7 fit and 47 do
+ * not), and larger problems are rejected with GATO_ERR_UNSUPPORTED before
  * anything is launched (use gato_create for those).  The first call on each
  * device looks up the array's device address; make that first call before
- * any stream capture.  All calls share the array and it keeps the previous
+ * any stream capture.  The address is cached with the identifier of the
+ * device's CUDA context and looked up again when that changes (after a
+ * cudaDeviceReset).  All calls share the array and it keeps the previous
  * call's contents (every entry is written before it is read, so nothing needs
  * clearing); calls that overlap on the GPU race on it, so the caller must
  * serialise them.  Never calls cudaMalloc, cudaFree or any allocating
@@ -364,6 +393,20 @@ int gato_solve_kkt_noalloc(const gato_params* p, int M, int N, int n, int m, con
                            const float* B, const float* e, const float* s0, float* dX,
                            float* dU, float* lambda, int32_t* iters, float* merit,
                            int32_t* best, uint32_t* status, void* stream);
+
+/* fp32 FMA throughput probe (a measurement helper; the paper has no
+ * counterpart).  The PCG kernels keep their operator on chip, so the bound
+ * of their roofline is the SM's fp32 FMA rate, which this probe measures
+ * rather than assuming the nominal unit count.  Launches `blocks` blocks of
+ * `threads` threads (a multiple of 32, at most 1024) on `stream`; every
+ * thread runs eight independent FMA chains for 16 `trips` FMAs each, as
+ * scalar fma.rn.f32 (packed = 0) or as half as many packed two-lane
+ * fma.rn.f32x2 instructions (packed = 1).  sink [blocks] floats of device
+ * memory is never written in practice (only under a condition that cannot
+ * hold).  Returns the floating-point operations of the launch (2 per FMA),
+ * or a negative GATO_ERR_* (INVALID_ARG, CUDA).  The caller times it. */
+long long gato_probe_fp32(int packed, int blocks, int threads, int trips, float* sink,
+                          void* stream);
 
 /* Largest number of parts gato_solve_kkt and gato_solve_kkt_host split a
  * batch into (gato_set_parts). */

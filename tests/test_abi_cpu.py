@@ -35,7 +35,7 @@ def test_header_declares_the_abi():
                "gato_set_pcg_kernel", "gato_set_form_kernel", "gato_solve_kkt_noalloc",
                "gato_bdsv_solve", "gato_set_bdsv_kernel", "gato_sqp_linear",
                "gato_default_sqp_params", "gato_solve_kkt_host", "gato_set_parts",
-               "gato_get_parts"):
+               "gato_get_parts", "gato_probe_fp32"):
         assert fn in names
 
 

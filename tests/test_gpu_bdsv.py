@@ -3,8 +3,9 @@ and chronological block Cholesky, against the fp64 oracle.
 
 The oracle's reference is the same as for PCG: its direct fp64 solution
 (Schur complement, block Cholesky, recovery by eq. (4)); the direct solve's
-result is unique, so dz, lambda and the merits are compared with the PCG
-tolerances (dz 1e-4 relative L2 per solve, merit 1e-5 of max|merit|).
+result is unique, so dX, dU, lambda and the merits are compared with the PCG
+tolerances (dX and dU each 1e-4 relative L2 per solve, merits 1e-5 per value
+as in test_gpu_parity).
 """
 import numpy as np
 import pytest
@@ -61,10 +62,18 @@ def test_direct_solve_matches_oracle(w, order):
 
 
 @pytest.mark.parametrize("order", [CR, CHRONO], ids=["cyclic", "chrono"])
-def test_unrefined_direct_solve_of_workload4(order):
+def test_refined_direct_solve_of_workload4(order):
+    """The exact solve of the fp32-formed system leaves dX 2e-4 to 4e-4 from
+    the exact solution (the formation's rounding); one refinement round, its
+    correction solved with the same factors, brings every solve within 1e-4."""
     w = WORKLOADS[4]
     prob = make_batch(w, M=8)
-    out = solve(prob, params_for(w, linsys=order, refine_steps=0))
+    raw = solve(prob, params_for(w, linsys=order, refine_steps=0))
+    assert not raw["status"].any()
+    worst = max(rel(raw["dX"][j], oracle.direct_solve(oracle.solve_one(prob, j))[0])
+                for j in range(8))
+    assert TOL_DZ < worst < 6e-4, worst
+    out = solve(prob, params_for(w, linsys=order, refine_steps=1))
     assert not out["status"].any()
     check_solution(prob, out, range(8), w.n_alpha, w.beta, w.mu)
 
@@ -103,7 +112,7 @@ def test_direct_solve_sizes(name, M, N, n, m, order):
                          ids=[SIZES[i][0] for i in (3, 4, 7, 11)])
 def test_register_and_shared_kernels_agree(name, M, N, n, m):
     prob = random_lq(M, N, n, m, seed=800 + N)
-    p = gato.default_params(linsys=CR, refine_steps=0)
+    p = gato.default_params(linsys=CR, refine_steps=1)
     a = solve(prob, p, gato.GATO_BDSV_KERNEL_AUTO)
     b = solve(prob, p, gato.GATO_BDSV_KERNEL_SHARED)
     for j in range(M):
@@ -116,8 +125,9 @@ def test_auto_policy_follows_the_horizon():
     """GATO_LINSYS_AUTO: PCG below bdsv_horizon (iterations counted), the
     direct solve from it (no iterations)."""
     prob = random_lq(2, 40, 14, 7, seed=901)
-    below = solve(prob, gato.default_params(bdsv_horizon=41, pcg_max_iters=2000))
-    at = solve(prob, gato.default_params(bdsv_horizon=40))
+    below = solve(prob, gato.default_params(bdsv_horizon=41, pcg_max_iters=2000,
+                                            refine_steps=1))
+    at = solve(prob, gato.default_params(bdsv_horizon=40, refine_steps=1))
     assert (below["iters"] > 0).all() and (at["iters"] == 0).all()
     for out in (below, at):
         assert not out["status"].any()

@@ -1,20 +1,25 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
 
 Tolerances
-  dz          relative L2 of the stacked dz = (dX, dU) per solve <= 1e-4 against
-              the oracle's direct fp64 solution, PCG stopped at eps = 1e-6
-  merit       |merit_gpu - merit_oracle| <= 1e-5 max|merit| per solve, the oracle
-              evaluating the GPU's own dz
+  dX, dU      relative L2 error of dX and, separately, of dU per solve <= 1e-4
+              against the oracle's direct fp64 solution, PCG stopped at
+              eps = 1e-6; every solve of every workload at its full batch
+  merit       per value: |merit_gpu - merit_oracle| <= 1e-5 max(|merit_oracle|,
+              1e-2 max|merit| of the solve), the oracle evaluating the GPU's own
+              dz.  A merit 100 times below the solve's largest one is a sum
+              whose terms cancelled by more than 100x; its fp32 rounding error
+              scales with the terms, not with the value, so the value's
+              magnitude is floored at 1 % of the solve's scale
   best        identical, unless the oracle's two best candidates are within
               1e-5 |M_best| of each other (then either of the two)
   S, Phi, gamma  relative Frobenius error per solve <= 1e-5 (fp32 formation:
               about 20 n u with u = 2^-24 for the sizes here)
+  status      0 on every solve of the workloads: workloads 0 and 2 meet their
+              stated iteration caps (200, 500) with the double-float PCG
 The workloads use their own refinement setting (one correction solved to
-0.25, 0.1 for workload 2, 0.01 for workload 3): in fp32 the formation of S
-alone moves dz by 4e-5 to 1.3e-4 (up to 3e-3 for workload 3), so the
-unrefined solve sits at the tolerance; refinement brings the worst solve of
-each workload to 1.5e-5 .. 3.2e-5.  A test below also checks
-the unrefined solve of workload 4.
+0.25 for workload 0, 0.1 for workloads 1, 2 and 4, two corrections solved to
+0.01 for workload 3): fp32 formation alone moves dX by 2e-4 to 1e-2, and
+refinement brings the worst dX of each workload's batch to 1e-5 .. 6e-5.
 """
 import numpy as np
 import pytest
@@ -28,6 +33,7 @@ from trajectory_optimization_kkt_gb300.workloads import WORKLOADS, make_batch, r
 
 TOL_DZ = 1e-4
 TOL_MERIT = 1e-5
+MERIT_NEAR_ZERO = 1e-2
 TOL_FORM = 1e-5
 
 
@@ -45,10 +51,7 @@ def rel(a, b):
 
 
 def params_for(w, **kw):
-    p = dict(pcg_eps=w.pcg_eps, pcg_max_iters=w.pcg_max_iters, n_alpha=w.n_alpha,
-             beta=w.beta, mu=w.mu, refine_steps=w.refine_steps, refine_eps=w.refine_eps)
-    p.update(kw)
-    return gato.default_params(**p)
+    return gato.default_params(**{**w.solver_settings(), **kw})
 
 
 def solve(prob, params, kernel=gato.GATO_PCG_AUTO, form_kind=gato.GATO_FORM_AUTO):
@@ -65,21 +68,29 @@ def solve(prob, params, kernel=gato.GATO_PCG_AUTO, form_kind=gato.GATO_FORM_AUTO
         return {k: v.cpu().numpy() for k, v in out.items()}
 
 
+def dz_errors(prob, out, j):
+    """Relative L2 errors of dX and dU (0 when there is no control) of solve j
+    against the oracle's direct fp64 solution."""
+    dX, dU, _ = oracle.direct_solve(oracle.solve_one(prob, j))
+    ex = rel(out["dX"][j], dX)
+    eu = rel(out["dU"][j], dU) if dU.size else 0.0
+    return ex, eu
+
+
 def check_solution(prob, out, solves, n_alpha=8, beta=2.0, mu=10.0, tol_dz=TOL_DZ):
     for j in solves:
+        ex, eu = dz_errors(prob, out, j)
+        assert ex <= tol_dz and eu <= tol_dz, (j, ex, eu)
         pj = oracle.solve_one(prob, j)
-        dX, dU, lam = oracle.direct_solve(pj)
-        z = np.concatenate([out["dX"][j].ravel(), out["dU"][j].ravel()])
-        zr = np.concatenate([dX.ravel(), dU.ravel()])
-        assert rel(z, zr) <= tol_dz, (j, rel(z, zr))
         check_merit(pj, out["dX"][j], out["dU"][j], out["merit"][j], out["best"][j],
                     n_alpha, beta, mu)
 
 
 def check_merit(pj, dX, dU, merit, best, n_alpha, beta, mu):
     ref, ref_best = oracle.linesearch(pj, dX, dU, n_alpha, beta, mu)
-    scale = np.abs(ref).max()
-    assert np.abs(merit - ref).max() <= TOL_MERIT * scale, (merit, ref)
+    floor = MERIT_NEAR_ZERO * np.abs(ref).max()
+    tol = TOL_MERIT * np.maximum(np.abs(ref), floor)
+    assert (np.abs(merit - ref) <= tol).all(), (merit, ref)
     cand = ref[1:]
     order = np.argsort(cand, kind="stable")
     gap = cand[order[1]] - cand[order[0]] if len(cand) > 1 else np.inf
@@ -149,36 +160,36 @@ def test_solve_kkt_matches_oracle(w):
     M = min(w.M, 8)
     prob = make_batch(w, M=M)
     out = solve(prob, params_for(w))
-    # workloads 0 and 2 state their caps (200, 500), which fp32 PCG can reach
-    assert not (out["status"] & ~gato.GATO_STATUS_PCG_MAX_ITERS).any(), out["status"]
-    if w.index not in (0, 2):
-        assert not out["status"].any()
+    assert not out["status"].any(), out["status"]
     check_solution(prob, out, range(M), w.n_alpha, w.beta, w.mu)
 
 
-@pytest.mark.parametrize("w", [WORKLOADS[1], WORKLOADS[2], WORKLOADS[3]], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", WORKLOADS, ids=lambda w: w.name)
 def test_full_batch_in_the_benchmark_configuration(w):
     """Each workload at its full batch with the default kernels and parts (as
-    bench.py --workloads times it), sampled against the oracle at both ends
-    of every part."""
+    bench.py times it): every solve ends with status 0 (workloads 0 and 2
+    within their stated caps of 200 and 500 iterations per PCG solve) and
+    every solve matches the oracle (dX, dU, merits, best)."""
     prob = make_batch(w)
     out = solve(prob, params_for(w))
-    assert not (out["status"] & ~gato.GATO_STATUS_PCG_MAX_ITERS).any(), out["status"]
-    parts = 1 if w.M < 64 else (2 if w.M < 128 else 4)
-    edges = sorted({j for c in range(parts) for j in (c * w.M // parts, (c + 1) * w.M // parts - 1)})
-    # workload 2's cap (500 iterations) can stop a few solves: those are the
-    # cap tests' concern; every other solve at a part edge is checked
-    ok = [j for j in edges if not out["status"][j]]
-    assert 2 * len(ok) >= len(edges)
-    check_solution(prob, out, ok, w.n_alpha, w.beta, w.mu)
+    assert not out["status"].any(), np.nonzero(out["status"])
+    check_solution(prob, out, range(w.M), w.n_alpha, w.beta, w.mu)
+    assert (out["best"] >= 0).all()
 
 
-def test_unrefined_solve_of_workload4():
-    w = WORKLOADS[4]
-    prob = make_batch(w, M=8)
-    out = solve(prob, params_for(w, refine_steps=0))
-    assert not out["status"].any()
-    check_solution(prob, out, range(8), w.n_alpha, w.beta, w.mu)
+@pytest.mark.parametrize("w", [WORKLOADS[1], WORKLOADS[4]], ids=lambda w: w.name)
+def test_refinement_removes_the_fp32_formation_error(w):
+    """Without refinement the fp32 formation of S (inverses and products
+    rounded to fp32) leaves dX 2e-4 to 4e-4 from the exact solution; one
+    correction round brings every solve within the 1e-4 tolerance."""
+    M = 16
+    prob = make_batch(w, M=M)
+    raw = solve(prob, params_for(w, refine_steps=0))
+    refined = solve(prob, params_for(w))
+    assert not raw["status"].any() and not refined["status"].any()
+    worst_raw = max(dz_errors(prob, raw, j)[0] for j in range(M))
+    assert TOL_DZ < worst_raw < 6e-4, worst_raw
+    check_solution(prob, refined, range(M), w.n_alpha, w.beta, w.mu)
 
 
 CUSTOM = [
@@ -195,7 +206,7 @@ CUSTOM = [
     ("N7_n16_m16", 2, 7, 16, 16, 1),
 ]
 WIDE = [c for c in CUSTOM if 7 <= c[3] <= 16 and c[2] <= 128] + [
-    ("N33_n15_m4", 2, 33, 15, 4, 1), ("N5_n8_m3", 3, 5, 8, 3, 0)]
+    ("N33_n15_m4", 2, 33, 15, 4, 1), ("N5_n8_m3", 3, 5, 8, 3, 2)]
 
 
 @pytest.mark.parametrize("kind", [gato.GATO_PCG_WIDE, gato.GATO_PCG_TILE], ids=["wide", "tile"])
@@ -338,20 +349,136 @@ def test_other_stop_rules(rule):
 
 
 # --------------------------------------------------------------------------
-# full sizes, launch configuration of the benchmark, sampled solves
+# the double-float PCG (GATO_PCG_PRECISION_FF)
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("w", [WORKLOADS[2], WORKLOADS[3], WORKLOADS[4]], ids=lambda w: w.name)
-def test_full_size_sampled(w):
+FF = gato.GATO_PCG_PRECISION_FF
+
+
+def pcg_only(prob, p, lambda0=None):
+    """gato_form_schur + gato_pcg_solve; also returns the S and gamma the GPU
+    formed (exported) for a true-residual check."""
+    M, N, n = prob["Q"].shape[:3]
+    m = prob["B"].shape[-1]
+    d = gato.to_device(prob)
+    f = dict(device="cuda", dtype=torch.float32)
+    with gato.Solver(M, N, n, m) as s:
+        o = s.outputs(p.n_alpha)
+        s.form_schur(d, o["status"])
+        l0 = None if lambda0 is None else torch.tensor(lambda0, **f)
+        s.pcg_solve(p, o["lam"], o["dX"], o["dU"], o["iters"], o["status"], lambda0=l0)
+        D, g = torch.empty(M, N, n, n, **f), torch.empty(M, N, n, **f)
+        O = torch.empty(M, N - 1, n, n, **f) if N > 1 else None
+        s.get_schur(D, O, g)
+        torch.cuda.synchronize()
+        out = {k: v.cpu().numpy() for k, v in o.items()}
+        out.update(D=D.cpu().numpy(), O=None if O is None else O.cpu().numpy(), g=g.cpu().numpy())
+        return out
+
+
+def true_relative_residual(out, j):
+    """||gamma - S lambda|| / ||gamma|| of the returned lambda on the S and
+    gamma the GPU formed (fp64), and the same for the exact solution of that
+    system rounded to fp32: the floor that an fp32 lambda can reach."""
+    N, n = out["g"].shape[1:]
+    O = out["O"][j] if out["O"] is not None else np.zeros((0, n, n))
+    S = oracle.bt_dense(out["D"][j], O)
+    g = out["g"][j].astype(np.float64).ravel()
+    exact = np.linalg.solve(S, g).astype(np.float32).astype(np.float64)
+    res = lambda lam: np.linalg.norm(g - S @ lam) / np.linalg.norm(g)
+    return res(out["lam"][j].astype(np.float64).ravel()), res(exact)
+
+
+@pytest.mark.parametrize("w", [WORKLOADS[0], WORKLOADS[2]], ids=lambda w: w.name)
+def test_double_float_pcg_meets_the_stated_cap(w):
+    """Workloads 0 and 2 state caps of 200 and 500 iterations.  The double-
+    float main solve stops on ||gamma - S lambda|| <= eps ||gamma|| within
+    them on every solve, and its iteration count follows the fp64 oracle's
+    (which needs up to 185 and 490) within 3 %.  The true residual of the
+    returned lambda on the exported S and gamma stays within the fp32
+    kernels' bound of 10 eps: it also carries the rounding of lambda to fp32
+    and the fp32 formation's mismatch between the scaled blocks the solve
+    uses and the exported S (measured 1.8e-6 and at most 2.7e-6 here)."""
     prob = make_batch(w)
-    out = solve(prob, params_for(w))
-    if w.index == 2:  # stated cap of 500 iterations
-        assert not (out["status"] & ~gato.GATO_STATUS_PCG_MAX_ITERS).any()
-    else:
-        assert not out["status"].any(), np.nonzero(out["status"])
-    samples = sorted(set(np.linspace(0, w.M - 1, 12).astype(int).tolist()))
-    check_solution(prob, out, samples, w.n_alpha, w.beta, w.mu)
-    assert (out["best"] >= 0).all()
+    out = pcg_only(prob, params_for(w, refine_steps=0))
+    assert not out["status"].any(), np.nonzero(out["status"])
+    assert out["iters"].max() <= w.pcg_max_iters
+    for j in range(w.M):
+        res, floor = true_relative_residual(out, j)
+        assert res <= 10 * w.pcg_eps, (j, res, floor)
+        D, O, gam, _ = oracle.schur(oracle.solve_one(prob, j))
+        Pd, Po, _ = oracle.stair(D, O)
+        _, it, ok = oracle.pcg(D, O, Pd, Po, gam, w.pcg_eps, 5000, stop_rule=0)
+        assert ok and it * 0.95 - 3 <= out["iters"][j] <= it * 1.03 + 3, (j, it, out["iters"][j])
+
+
+FF_SIZES = [
+    ("N1_n14_m7", 2, 1, 14, 7),
+    ("N2_n3_m2", 2, 2, 3, 2),
+    ("N37_n13_m5", 2, 37, 13, 5),
+    ("N16_n36_m12", 2, 16, 36, 12),
+    ("N4_n64_m16", 1, 4, 64, 16),
+    ("N100_n14_m7_two_rows", 2, 100, 14, 7),   # 1400 rows: two per thread
+    ("N128_n16_m8_two_rows", 1, 128, 16, 8),   # 2048 rows, the largest
+]
+
+
+@pytest.mark.parametrize("name,M,N,n,m", FF_SIZES, ids=[c[0] for c in FF_SIZES])
+def test_double_float_pcg_sizes(name, M, N, n, m):
+    """Every size class of the double-float kernel (one and two rows per
+    thread, n up to 64, N = 1) against the oracle, and against the fp32
+    kernel's lambda."""
+    prob = random_lq(M, N, n, m, seed=950 + N + n)
+    p = gato.default_params(pcg_max_iters=5000, refine_steps=1, pcg_precision=FF)
+    out = solve(prob, p)
+    assert not out["status"].any(), out["status"]
+    check_solution(prob, out, range(M))
+    ref = solve(prob, gato.default_params(pcg_max_iters=5000, refine_steps=1))
+    for j in range(M):
+        assert rel(out["lam"][j], ref["lam"][j]) < 1e-3
+
+
+@pytest.mark.parametrize("rule", [gato.GATO_STOP_PRECOND, gato.GATO_STOP_SCALED],
+                         ids=["precond", "scaled"])
+def test_double_float_pcg_other_stop_rules(rule):
+    """The other stopping rules stop the double-float solve where the fp64
+    oracle's same rule stops (within 3 %)."""
+    w = WORKLOADS[2]
+    prob = make_batch(w, M=4)
+    out = pcg_only(prob, params_for(w, stop_rule=rule, refine_steps=0))
+    assert not out["status"].any()
+    for j in range(4):
+        D, O, gam, _ = oracle.schur(oracle.solve_one(prob, j))
+        Pd, Po, _ = oracle.stair(D, O)
+        _, it, ok = oracle.pcg(D, O, Pd, Po, gam, w.pcg_eps, 5000, stop_rule=rule)
+        assert ok and it * 0.97 - 3 <= out["iters"][j] <= it * 1.03 + 3, (j, it, out["iters"][j])
+
+
+def test_double_float_pcg_warm_start():
+    """From the exact multipliers no iteration is needed; from half of them
+    fewer than from zero."""
+    w = WORKLOADS[0]
+    prob = make_batch(w, M=2, N=24)
+    lam = np.stack([oracle.direct_solve(oracle.solve_one(prob, j))[2] for j in range(2)])
+    p = params_for(w, refine_steps=0, pcg_max_iters=1000)
+    at = pcg_only(prob, gato.default_params(pcg_eps=1e-3, pcg_precision=FF), lambda0=lam)
+    assert (at["iters"] == 0).all()
+    cold = pcg_only(prob, p)
+    half = pcg_only(prob, p, lambda0=0.5 * lam)
+    assert not cold["status"].any() and not half["status"].any()
+    assert (half["iters"] <= cold["iters"]).all()
+    for j in range(2):
+        assert rel(half["lam"][j], lam[j]) < 1e-3
+
+
+def test_double_float_pcg_rejects_sizes_beyond_it():
+    """More than 2048 rows (or more than 1024 with n > 16): rejected as
+    unsupported rather than solved at a lower precision."""
+    for (N, n, m) in ((150, 14, 7), (30, 36, 12)):
+        prob = random_lq(1, N, n, m, seed=990)
+        with pytest.raises(gato.GatoError) as e:
+            solve(prob, gato.default_params(pcg_max_iters=100, pcg_precision=FF))
+        assert e.value.code == gato.GATO_ERR_UNSUPPORTED
 
 
 # --------------------------------------------------------------------------
@@ -580,7 +707,8 @@ def test_invalid_parameters_rejected():
     w = WORKLOADS[0]
     prob = make_batch(w, M=1)
     for bad in (dict(merit_threads=48), dict(n_alpha=0), dict(beta=1.0), dict(stop_rule=7),
-                dict(pcg_max_iters=-1), dict(merit_kernel=5), dict(refine_eps=-1.0)):
+                dict(pcg_max_iters=-1), dict(merit_kernel=5), dict(refine_eps=-1.0),
+                dict(pcg_precision=2), dict(pcg_precision=-1)):
         with pytest.raises(gato.GatoError) as e:
             solve(prob, params_for(w, **bad))
         assert e.value.code == gato.GATO_ERR_INVALID_ARG

@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_factor_rows(Work w, uint32_t* s
     const int lane = lane_id(), warp = threadIdx.x >> 5;
     const int half = (warp << 1) | (lane >> 4), li = lane & 15;
     const int H = blockDim.x >> 4;
+    if (!gb_smem((size_t)H * 2 * NP * NP * sizeof(float), w.status, sol)) return;  // uniform
     float* S0 = sm + (size_t)half * 2 * NP * NP;
     float* S1 = S0 + NP * NP;
     const Blocks b(w, sol);
@@ -252,6 +253,7 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_factor_smem(Work w, uint32_t* s
     const int sol = blockIdx.x;
     const int n = w.n, N = w.N, n2 = n * n;
     const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (!gb_smem((size_t)nw * 3 * n2 * sizeof(float), w.status, sol)) return;  // uniform
     float* Ta = sm + (size_t)warp * 3 * n2;
     float* Tb = Ta + n2;
     float* Tc = Tb + n2;
@@ -336,6 +338,7 @@ __global__ void __launch_bounds__(128) k_bdsv_chrono_factor(Work w, uint32_t* st
     const int sol = blockIdx.x * (blockDim.x >> 5) + warp;
     if (sol >= w.M) return;  // whole warps leave together
     const int n = w.n, N = w.N, n2 = n * n;
+    if (!gb_smem((size_t)(warp + 1) * 3 * n2 * sizeof(float), w.status, sol)) return;  // warp
     float* Ta = sm + (size_t)warp * 3 * n2;
     float* Tf = Ta + n2;  // F_{j-1}, then F_j
     float* Tw = Tf + n2;
@@ -409,6 +412,7 @@ __global__ void __launch_bounds__(256) k_bdsv_cr_solve(BdsvArgs g)
     const Work& w = g.w;
     const int sol = blockIdx.x;
     const int n = w.n, N = w.N, Nn = N * n, T = blockDim.x, tid = threadIdx.x;
+    if (g.vec_smem && !gb_smem(2 * (size_t)Nn * sizeof(float), w.status, sol)) return;  // uniform
     float* v = g.vec_smem ? sm : w.Bv + sol * w.sNn;
     float* G = g.vec_smem ? sm + Nn : w.Bg + sol * w.sNn;
     const Blocks b(w, sol);
@@ -488,6 +492,7 @@ __global__ void __launch_bounds__(128) k_bdsv_chrono_solve(BdsvArgs g)
     const Work& w = g.w;
     const int sol = blockIdx.x;
     const int n = w.n, N = w.N, Nn = N * n;
+    if (g.vec_smem && !gb_smem(2 * (size_t)Nn * sizeof(float), w.status, sol)) return;  // uniform
     float* v = g.vec_smem ? sm : w.Bv + sol * w.sNn;
     float* G = g.vec_smem ? sm + Nn : w.Bg + sol * w.sNn;
     const Blocks b(w, sol);

@@ -58,6 +58,13 @@ __device__ __forceinline__ Half half_setup(long items, float* sm, int nmat)
     return h;
 }
 
+// debug build: the block's sixteen scratches fit its dynamic shared memory
+// (the same for every half, so a failed check returns the whole block)
+__device__ __forceinline__ bool rows_scratch_ok(int nmat, const Work& w, int sol)
+{
+    return gb_smem((size_t)kKnotsPerBlock * nmat * NP * NP * sizeof(float), w.status, sol);
+}
+
 // three blocks per SM at 80 registers (no spills at PN = 14, PM = 8; a few at
 // 16 x 16)
 template <int PN, int PM>
@@ -73,6 +80,7 @@ __global__ void __launch_bounds__(256, 3) k_rows_knot(Work w, const float* __res
     // of the warp takes part in the shuffles and barriers; they store nothing
     const long item = h.active ? h.item : 0;
     const int sol = (int)(item / N), k = (int)(item % N);
+    if (!rows_scratch_ok(3, w, sol)) return;
     const size_t K = (size_t)(N - 1);
     // the last knot has no control: its half still runs the control part (on
     // knot 0's data of the same solve, when there is one) so that the warp's
@@ -157,6 +165,7 @@ __global__ void __launch_bounds__(256) k_rows_diag(Work w, uint32_t* status)
     const Half h = half_setup((long)w.M * N, sm, 1);
     const long item = h.active ? h.item : 0;
     const int sol = (int)(item / N), j = (int)(item % N);
+    if (!rows_scratch_ok(1, w, sol)) return;
     const int li = h.li;
     const size_t off = sol * w.sNnn + (size_t)j * n * n;
 
@@ -199,6 +208,7 @@ __global__ void __launch_bounds__(256) k_rows_off(Work w)
     const Half h = half_setup((long)w.M * K, sm, 2);
     const long item = h.active ? h.item : 0;
     const int sol = (int)(item / K), j = 1 + (int)(item % K);
+    if (!rows_scratch_ok(2, w, sol)) return;
     const int li = h.li;
     const size_t dj = sol * w.sNnn + (size_t)j * n * n, dp = dj - (size_t)n * n;
     const size_t oj = sol * w.sKnn + (size_t)(j - 1) * n * n;
@@ -228,6 +238,7 @@ __global__ void __launch_bounds__(256) k_rows_phi_diag(Work w)
     const Half h = half_setup((long)w.M * N, sm, 1);
     const long item = h.active ? h.item : 0;
     const int sol = (int)(item / N), j = (int)(item % N);
+    if (!rows_scratch_ok(1, w, sol)) return;
     const int li = h.li;
     const size_t off = sol * w.sNnn + (size_t)j * n * n;
     float x[NP], c[NP];
@@ -248,6 +259,7 @@ __global__ void __launch_bounds__(256) k_rows_phi_off(Work w)
     const Half h = half_setup((long)w.M * K, sm, 2);
     const long item = h.active ? h.item : 0;
     const int sol = (int)(item / K), j = 1 + (int)(item % K);
+    if (!rows_scratch_ok(2, w, sol)) return;
     const int li = h.li;
     const size_t dj = sol * w.sNnn + (size_t)j * n * n, dp = dj - (size_t)n * n;
     const size_t oj = sol * w.sKnn + (size_t)(j - 1) * n * n;

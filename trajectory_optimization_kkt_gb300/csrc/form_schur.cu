@@ -39,6 +39,8 @@ __global__ void k_form_inv(Work w, const float* __restrict__ Q, const float* __r
     const long g = (long)blockIdx.x * wpb + warp;
     if (g >= (long)w.M * N) return;
     const int sol = (int)(g / N), k = (int)(g % N);
+    if (!gb_smem((size_t)(warp + 1) * form_inv_floats(n, m) * sizeof(float), w.status, sol))
+        return;  // the warp's slice (warp-uniform)
     // two n x n slices per warp (more warps per SM): L and then Q^-1 in sQ;
     // L^-1 in sT, then the R part (R's factor, R^-1 rows, R^-1, B), then A
     float* sQ = sm + (size_t)warp * form_inv_floats(n, m);
@@ -81,6 +83,8 @@ __global__ void k_form_diag(Work w, const float* __restrict__ A, const float* __
     const long g = (long)blockIdx.x * wpb + warp;
     if (g >= (long)w.M * N) return;
     const int sol = (int)(g / N), j = (int)(g % N);
+    if (!gb_smem((size_t)(warp + 1) * (4 * nn + 2 * nm) * sizeof(float), w.status, sol))
+        return;  // the warp's slice (warp-uniform)
     float* sD = sm + (size_t)warp * (4 * nn + 2 * nm);
     float* sO = sD + nn;
     float* sA = sO + nn;
@@ -127,6 +131,8 @@ __global__ void k_form_off(Work w)
     const long g = (long)blockIdx.x * wpb + warp;
     if (K < 1 || g >= (long)w.M * K) return;
     const int sol = (int)(g / K), j = 1 + (int)(g % K);
+    if (!gb_smem((size_t)(warp + 1) * 3 * nn * sizeof(float), w.status, sol))
+        return;  // the warp's slice (warp-uniform)
     float* s1 = sm + (size_t)warp * 3 * nn;
     float* s2 = s1 + nn;
     float* s4 = s2 + nn;
@@ -151,6 +157,8 @@ __global__ void k_form_phi_diag(Work w)
     const long g = (long)blockIdx.x * wpb + warp;
     if (g >= (long)w.M * N) return;
     const int sol = (int)(g / N), j = (int)(g % N);
+    if (!gb_smem((size_t)(warp + 1) * 2 * nn * sizeof(float), w.status, sol))
+        return;  // the warp's slice (warp-uniform)
     float* sA = sm + (size_t)warp * 2 * nn;
     float* sO = sA + nn;
     const size_t off = sol * w.sNnn + (size_t)j * nn;
@@ -169,6 +177,8 @@ __global__ void k_form_phi_off(Work w)
     const long g = (long)blockIdx.x * wpb + warp;
     if (K < 1 || g >= (long)w.M * K) return;
     const int sol = (int)(g / K), j = 1 + (int)(g % K);
+    if (!gb_smem((size_t)(warp + 1) * 4 * nn * sizeof(float), w.status, sol))
+        return;  // the warp's slice (warp-uniform)
     float* s1 = sm + (size_t)warp * 4 * nn;
     float* s2 = s1 + nn;
     float* s3 = s2 + nn;
@@ -254,6 +264,7 @@ __global__ void k_form_rhs(Work w, Rhs out, const float* __restrict__ q,
     if (g >= (long)w.M * N) return;
     const int sol = (int)(g / N), j = (int)(g % N);
     const size_t K = (size_t)(N - 1);
+    if (!gb_smem((size_t)(warp + 1) * n * sizeof(float), w.status, sol)) return;
     float* sg = sm + (size_t)warp * n;
     const float* Qi = w.Qinv + sol * w.sNnn + (size_t)j * nn;
     const float* qj = q + ((size_t)sol * N + j) * n;

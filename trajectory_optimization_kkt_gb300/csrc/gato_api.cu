@@ -21,6 +21,7 @@ size_t round64(size_t x)
 size_t carve_workspace(Work& w, int M, int N, int n, int m, float* base)
 {
     w.M = M; w.N = N; w.n = n; w.m = m;
+    w.status = nullptr;
     const size_t K = (size_t)(N - 1);
     w.sNnn = round64((size_t)N * n * n);
     w.sKnn = round64(K * n * n);
@@ -83,7 +84,16 @@ bool params_valid(const gato_params* p)
         return false;
     if (p->linsys < GATO_LINSYS_AUTO || p->linsys > GATO_LINSYS_BDSV_CHRONO) return false;
     if (p->bdsv_horizon < 1) return false;
+    if (p->pcg_precision != GATO_PCG_PRECISION_FP32 && p->pcg_precision != GATO_PCG_PRECISION_FF)
+        return false;
     return true;
+}
+
+bool sizes_supported(const Work& w, const gato_params* p, int smem_limit)
+{
+    if (p->pcg_precision != GATO_PCG_PRECISION_FF) return true;
+    if (linsys_for(p, w.N) != GATO_LINSYS_PCG) return true;
+    return pcg_ff_fits(w.N, w.n, (size_t)smem_limit);
 }
 
 int linsys_for(const gato_params* p, int N)
@@ -110,6 +120,7 @@ cudaError_t run_kkt_core(gato_handle* h, const gato_params* p, const float* Q_fo
                          cudaStream_t st, bool timed)
 {
     Work& w = h->w;
+    w.status = status;
     const int ls = linsys_for(p, w.N);
     const bool direct = ls != GATO_LINSYS_PCG;
     cudaError_t err = launch_form_matrices(h, Q_form, R, A, B, status, st);
@@ -131,6 +142,7 @@ cudaError_t run_kkt_core(gato_handle* h, const gato_params* p, const float* Q_fo
     gato_params pc = *p;
     if (p->refine_eps > 0.f) pc.pcg_eps = p->refine_eps;
     pc.stop_rule = GATO_STOP_PRECOND;
+    pc.pcg_precision = GATO_PCG_PRECISION_FP32;
     for (int k = 0; k < p->refine_steps && err == cudaSuccess; ++k) {
         err = launch_kkt_residual(h, Q_form, R, q, r, A, B, e, s0, dX, dU, lambda, st);
         if (err == cudaSuccess)
@@ -218,6 +230,7 @@ cudaError_t sqp_iteration(gato_handle* h, const gato_params* p, const gato_sqp_p
                           const SqpArgs& a, cudaStream_t st)
 {
     Work& w = h->w;
+    w.status = a.status;
     cudaError_t err = gato::launch_sqp_linearize(h, a.Q, a.R, a.q, a.r, a.A, a.B, a.c, a.xs,
                                                  a.X, a.U, a.rho, st);
     if (err == cudaSuccess)
@@ -298,6 +311,7 @@ void gato_default_params(gato_params* p)
     p->merit_kernel = GATO_MERIT_FUSED;
     p->linsys = GATO_LINSYS_AUTO;
     p->bdsv_horizon = 256;
+    p->pcg_precision = GATO_PCG_PRECISION_FP32;
 }
 
 void gato_default_sqp_params(gato_sqp_params* sp)
@@ -430,6 +444,7 @@ int gato_form_schur(gato_handle* h, const float* Q, const float* R, const float*
                     const float* s0, uint32_t* status, void* stream)
 {
     if (!h || !status || !lq_ok(h, Q, R, q, r, A, B, e, s0)) return GATO_ERR_INVALID_ARG;
+    h->w.status = status;
     cudaStream_t st = (cudaStream_t)stream;
     begin_timing(h, st);
     cudaError_t err = gato::launch_form_matrices(h, Q, R, A, B, status, st);
@@ -443,6 +458,7 @@ int gato_get_schur(gato_handle* h, float* S_diag, float* S_off, float* gamma,
                    float* Phi_diag, float* Phi_off, void* stream)
 {
     if (!h) return GATO_ERR_INVALID_ARG;
+    h->w.status = nullptr;
     const Work& w = h->w;
     cudaStream_t st = (cudaStream_t)stream;
     if ((Phi_diag || Phi_off) && h->phi_pending) {
@@ -471,6 +487,10 @@ int gato_pcg_solve(gato_handle* h, const gato_params* p, const float* lambda0, f
 {
     if (!h || !params_valid(p) || !lambda || !dX || !iters || !status) return GATO_ERR_INVALID_ARG;
     if (h->w.N > 1 && !dU) return GATO_ERR_INVALID_ARG;
+    if (p->pcg_precision == GATO_PCG_PRECISION_FF &&
+        !gato::pcg_ff_fits(h->w.N, h->w.n, (size_t)h->smem_optin))
+        return GATO_ERR_UNSUPPORTED;
+    h->w.status = status;
     cudaStream_t st = (cudaStream_t)stream;
     begin_timing(h, st);
     cudaError_t err = gato::launch_pcg(h, p, lambda0, lambda, dX, dU, iters, status, st);
@@ -487,6 +507,7 @@ int gato_bdsv_solve(gato_handle* h, const gato_params* p, float* lambda, float* 
     if (h->w.N > 1 && !dU) return GATO_ERR_INVALID_ARG;
     const int ls = p->linsys == GATO_LINSYS_AUTO ? GATO_LINSYS_BDSV : p->linsys;
     if (ls == GATO_LINSYS_PCG) return GATO_ERR_INVALID_ARG;
+    h->w.status = status;
     cudaStream_t st = (cudaStream_t)stream;
     begin_timing(h, st);
     cudaError_t err = gato::launch_bdsv_factor(h, ls, status, st);
@@ -505,6 +526,7 @@ int gato_linesearch(gato_handle* h, const gato_params* p, const float* Q, const 
         !status)
         return GATO_ERR_INVALID_ARG;
     if (h->w.N > 1 && !dU) return GATO_ERR_INVALID_ARG;
+    h->w.status = status;
     cudaStream_t st = (cudaStream_t)stream;
     begin_timing(h, st);
     cudaError_t err =
@@ -523,6 +545,7 @@ int gato_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const f
         !iters || !merit || !best || !status)
         return GATO_ERR_INVALID_ARG;
     if (h->w.N > 1 && !dU) return GATO_ERR_INVALID_ARG;
+    if (!gato::sizes_supported(h->w, p, h->smem_optin)) return GATO_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
     if (gato::parts_for(h) > 1) {
         h->ev_used[0] = 0;  // no stage timing for a call in parts
@@ -539,6 +562,7 @@ int gato_apply_step(gato_handle* h, const gato_params* p, const int32_t* best, c
 {
     if (!h || !params_valid(p) || !best || !dX || !X) return GATO_ERR_INVALID_ARG;
     if (h->w.N > 1 && (!dU || !U)) return GATO_ERR_INVALID_ARG;
+    h->w.status = nullptr;
     return cuda_fail(gato::launch_apply_step(h, p, best, dX, dU, X, U, (cudaStream_t)stream));
 }
 
@@ -552,6 +576,7 @@ int gato_sqp_linear(gato_handle* h, const gato_params* p, const gato_sqp_params*
         !X || !lambda || !rho || !merit_hist || !status)
         return GATO_ERR_INVALID_ARG;
     if (h->w.N > 1 && !U) return GATO_ERR_INVALID_ARG;
+    if (!gato::sizes_supported(h->w, p, h->smem_optin)) return GATO_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
     const SqpArgs a{Q, R, q, r, A, B, c, xs, X, U, lambda, rho, merit_hist, iters_hist, status};
     cudaError_t err = cudaMemsetAsync(h->w.sqpt, 0, sizeof(int) * h->w.M, st);

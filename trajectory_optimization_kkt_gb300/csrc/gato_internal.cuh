@@ -92,6 +92,10 @@ struct Work {
     float2* mpart; // [(A+1)][N] (cost, violation) per knot and candidate
     int* queue;    // work counters of the persistent kernels (not per solve)
     int* mcount;   // [M] merit blocks arrived per solve (zeroed before each launch)
+    // the current call's status[M] (may be NULL): where the index checks of
+    // the debug build record GATO_STATUS_BOUNDS; set by every entry point
+    // before it launches
+    uint32_t* status;
 };
 
 }  // namespace gato
@@ -191,6 +195,13 @@ cudaError_t launch_bdsv_solve(gato_handle* h, int order, int set, float* lambda,
 // sets every pointer of w from base (when base != NULL) and returns the bytes
 size_t carve_workspace(Work& w, int M, int N, int n, int m, float* base);
 bool params_valid(const gato_params* p);
+// the double-float PCG kernel takes N knots of n states within smem_limit
+// bytes of shared memory per block (pcg_ff.cu)
+bool pcg_ff_fits(int N, int n, size_t smem_limit);
+// the kernels p asks for take the sizes of w: false when p asks for the
+// double-float PCG and the linear solver is PCG but the kernel cannot take
+// them (checked before anything is launched)
+bool sizes_supported(const Work& w, const gato_params* p, int smem_limit);
 // the linear solver a call with parameters p uses: GATO_LINSYS_PCG,
 // GATO_LINSYS_BDSV or GATO_LINSYS_BDSV_CHRONO
 int linsys_for(const gato_params* p, int N);
@@ -223,6 +234,50 @@ cudaError_t run_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, 
 // device helpers
 // ---------------------------------------------------------------------------
 #ifdef __CUDACC__
+
+// ---------------------------------------------------------------------------
+// index checks of the debug build (compiled with -DGATO_DEBUG_BOUNDS=1, the
+// stand-in for a memory checker): an index outside its array, or a layout
+// that does not fit the block's dynamic shared memory, is recorded as
+// GATO_STATUS_BOUNDS in the call's status[sol] and the check returns false,
+// so that the caller skips the access.  Nothing traps.  In the normal build
+// both checks are the constant true and vanish.
+// ---------------------------------------------------------------------------
+#ifndef GATO_DEBUG_BOUNDS
+#define GATO_DEBUG_BOUNDS 0
+#endif
+
+__device__ __forceinline__ bool gb_ok(long long idx, long long limit, uint32_t* status, int sol)
+{
+#if GATO_DEBUG_BOUNDS
+    if (idx >= 0 && idx < limit) return true;
+    if (status) atomicOr(status + sol, GATO_STATUS_BOUNDS);
+    return false;
+#else
+    (void)idx;
+    (void)limit;
+    (void)status;
+    (void)sol;
+    return true;
+#endif
+}
+
+// the block's layout needs `bytes` of dynamic shared memory
+__device__ __forceinline__ bool gb_smem(size_t bytes, uint32_t* status, int sol)
+{
+#if GATO_DEBUG_BOUNDS
+    unsigned dyn;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    if (bytes <= dyn) return true;
+    if (status) atomicOr(status + sol, GATO_STATUS_BOUNDS);
+    return false;
+#else
+    (void)bytes;
+    (void)status;
+    (void)sol;
+    return true;
+#endif
+}
 
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 

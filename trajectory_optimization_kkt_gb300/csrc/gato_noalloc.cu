@@ -13,8 +13,12 @@
 // Host code must not pass the array's name to a kernel: on the host it is a
 // stand-in symbol, not a device address.  The first call on each device,
 // with that device current, asks the runtime for the array's device address
-// (cudaGetSymbolAddress) and caches it; that first call should therefore be
-// made before any stream capture begins.
+// (cudaGetSymbolAddress) and caches it together with the identifier of the
+// CUDA context it belongs to; that first call should therefore be made
+// before any stream capture begins.  A device reset (cudaDeviceReset)
+// destroys that context and the module is loaded again, possibly elsewhere,
+// in the next one: a later call sees a different context identifier and
+// looks the address up again instead of passing a stale pointer.
 //
 // All calls share the one array and it keeps whatever the last call left in
 // it.  The solve writes every scratch entry before reading it, so nothing
@@ -33,22 +37,62 @@ static __device__ __align__(256) unsigned char g_scratch[GATO_NOALLOC_MAX_BYTES]
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-void* g_scratch_addr[kMaxDevices];
+struct Cached {
+    unsigned long long ctx_id;  // context the address belongs to (0: none yet)
+    void* addr;
+};
+Cached g_cache[kMaxDevices];
 
-// device address of g_scratch on the current device (cached per device)
+// the driver's current-context queries, reached through the runtime so that
+// the library needs no link against the driver library
+using CtxGetCurrentFn = int (*)(void** ctx);
+using CtxGetIdFn = int (*)(void* ctx, unsigned long long* id);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// identifier of the current context, 0 when there is none or it cannot be read
+unsigned long long current_context_id()
+{
+    if (!g_ctx_get_current || !g_ctx_get_id) {
+        cudaDriverEntryPointQueryResult q1, q2;
+        void* f1 = nullptr;
+        void* f2 = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault,
+                                             &q1) != cudaSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) !=
+                cudaSuccess ||
+            q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 || !f2) {
+            cudaGetLastError();
+            return 0;
+        }
+        g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+        g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f2);
+    }
+    void* ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_get_current(&ctx) != 0 || !ctx || g_ctx_get_id(ctx, &id) != 0) return 0;
+    return id;
+}
+
+// device address of g_scratch on the current device: cached per device and
+// looked up again when the device's context has changed since
 int scratch_address(int device, void** out)
 {
     if (device < 0 || device >= kMaxDevices) return GATO_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_addr[device]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) {
-            cudaGetLastError();
-            return GATO_ERR_CUDA;
-        }
-        g_scratch_addr[device] = p;
+    Cached& c = g_cache[device];
+    if (c.addr && c.ctx_id != 0 && current_context_id() == c.ctx_id) {
+        *out = c.addr;
+        return GATO_OK;
     }
-    *out = g_scratch_addr[device];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return GATO_ERR_CUDA;
+    }
+    c.addr = p;
+    c.ctx_id = current_context_id();  // the lookup made the context current
+    *out = p;
     return GATO_OK;
 }
 
@@ -78,6 +122,7 @@ extern "C" int gato_solve_kkt_noalloc(const gato_params* p, int M, int N, int n,
         cudaDeviceGetAttribute(&h.num_sms, cudaDevAttrMultiProcessorCount, h.device) !=
             cudaSuccess)
         return GATO_ERR_CUDA;
+    if (!gato::sizes_supported(probe, p, h.smem_optin)) return GATO_ERR_UNSUPPORTED;
     void* base = nullptr;
     const int rc = scratch_address(h.device, &base);
     if (rc != GATO_OK) return rc;

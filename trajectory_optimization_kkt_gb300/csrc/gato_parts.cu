@@ -289,6 +289,7 @@ int gato_solve_kkt_host(gato_handle* h, const gato_params* p, const float* Q, co
         !best || !status)
         return GATO_ERR_INVALID_ARG;
     if (h->w.N > 1 && (!R || !r || !A || !B || !e || !dU)) return GATO_ERR_INVALID_ARG;
+    if (!sizes_supported(h->w, p, h->smem_optin)) return GATO_ERR_UNSUPPORTED;
     h->ev_used[0] = 0;  // no stage timing for a call in parts
     return run_parts(h, p, Q, R, q, r, A, B, e, s0, dX, dU, lambda, iters, merit, best, status,
                      (cudaStream_t)stream, true);

@@ -67,6 +67,9 @@ __global__ void k_merit(MeritArgs g)
     float* u = xn + n;       // m
     float* tc = u + m;       // n + m  cost terms
     float* tv = tc + n + m;  // 2n     violation terms (dynamics rows, then x_0 rows)
+    if (!gb_smem((size_t)(5 * n + 2 * m) * sizeof(float), g.w.status, sol) ||
+        !gb_ok((long long)c * N + k, (long long)g.w.sK2, g.w.status, sol))
+        return;  // block-uniform
 
     const float* dXs = g.dX + (size_t)sol * N * n;
     for (int i = tid; i < n; i += T) {
@@ -171,6 +174,8 @@ __global__ void __launch_bounds__(512) k_merit_fused(MeritArgs g, float mu, floa
     float* xn = xv + n;
     float* uv = xn + n;
     float* part = sm + (size_t)nw * (2 * n + m);  // [nw][A1 + 2] warp partials
+    if (!gb_smem(((size_t)nw * (2 * n + m + A1 + 2) + A1) * sizeof(float), g.w.status, sol))
+        return;  // block-uniform
 
     float alpha[kMaxA1];
 #pragma unroll
@@ -378,7 +383,9 @@ __global__ void __launch_bounds__(256) k_merit_knots(MeritArgs g, float mu, floa
     }
     __syncthreads();
     float* part = reinterpret_cast<float*>(g.w.mpart) + (size_t)sol * 2 * g.w.sK2;
-    if (tid < A1 + 2) {
+    // the block's A1 + 2 sums, in the solve's 2 sK2 floats of scratch
+    if (tid < A1 + 2 &&
+        gb_ok((long long)blockIdx.x * (A1 + 2) + tid, 2 * (long long)g.w.sK2, g.w.status, sol)) {
         float t = 0.f;
         for (int q = 0; q < 8; ++q) t += wpart[q][tid];
         part[(size_t)blockIdx.x * (A1 + 2) + tid] = t;

@@ -104,6 +104,10 @@ __global__ void __launch_bounds__(512) k_pcg_generic(PcgArgs g)
     off += round4(Nn);
     float4* redA = reinterpret_cast<float4*>(sm + off);
     float4* redB = redA + 32;
+    if (!gb_smem((off + 64 * 4) * sizeof(float), w.status, sol) ||
+        (nh_count > 0 && !gb_ok((long long)nh_count - 1, (long long)w.sKnn, w.status, sol)) ||
+        !gb_ok((long long)Nn - 1, (long long)w.sNn, w.status, sol))
+        return;  // block-uniform
 
     const float* gNh = w.Nh + sol * w.sKnn;
     const float* gL = w.L + sol * w.sNnn;
@@ -398,6 +402,11 @@ __device__ __forceinline__ void pcg_tile_solve(const PcgArgs& g, int sol)
     float* DL = reinterpret_cast<float*>(redA + 160);
     float* LP = DL + ((N + 3) & ~3);
     const Y4 Y{YR0, YR1, YC0, YC1};
+    if (!gb_smem((size_t)(LP - sm + (lsm ? (size_t)N * KS : 0)) * sizeof(float), w.status,
+                 sol)) {
+        finish(g, sol, 0, false, false);
+        return;  // block-uniform
+    }
 
     // zero vectors and partial sums (padding and missing blocks stay 0)
     for (int i = tid; i < zero_count; i += T) sm[i] = 0.f;
@@ -407,7 +416,8 @@ __device__ __forceinline__ void pcg_tile_solve(const PcgArgs& g, int sol)
 
     // the tile this thread holds: block jb = 1 + tid/4, tile (rt, ct)
     const int jb = 1 + (tid >> 2), rt = (tid >> 1) & 1, ct = tid & 1;
-    const bool has_tile = jb <= N - 1;
+    // a tile's row and column sums go to knot jb's and jb-1's 16 slots
+    const bool has_tile = jb <= N - 1 && gb_ok((long long)jb * 16 + 15, E, w.status, sol);
     float* yr_base = ct ? YR1 : YR0;
     float* yc_base = rt ? YC1 : YC0;
     Tile<H> tile;
@@ -775,17 +785,27 @@ __device__ __forceinline__ void pcg_wide_solve(const PcgArgs& g, int sol)
     float2* redD = redA + 96;  // also used as float4[16] by block_sum
     float* DL = reinterpret_cast<float*>(redA + 160);
     float* LP = DL + ((N + 3) & ~3);
+    if (!gb_smem((size_t)(LP - sm + (lsm ? (size_t)N * KS : 0)) * sizeof(float), w.status,
+                 sol)) {
+        finish(g, sol, 0, false, false);
+        return;  // block-uniform
+    }
 
     for (int i = tid; i < zero_count; i += T) sm[i] = 0.f;
     for (int j = tid; j < N; j += T) DL[j] = w.dlow[sol * w.sN + j];
     const float* gL = w.L + sol * w.sNnn;
     if (lsm) stage_l_rows<H>(LP, KS, gL, N, n);
 
-    // tile rows (block jb, half rt) and the owned slots (knot jo, same half)
+    // tile rows (block jb, half rt) and the owned slots (knot jo, same half);
+    // the tile reads x_{j-1} (knot jb-1's 20 floats) and writes its column
+    // sums there, the owner its 8 slots of knot jo
     const int rt = tid & 1;
-    const bool has_tile = tid < 2 * (N - 1);
     const int jb = 1 + (tid >> 1);
-    const bool owner = tid < 2 * N;
+    const bool has_tile =
+        tid < 2 * (N - 1) && gb_ok((long long)(jb - 1) * kWS + 19, EX, w.status, sol);
+    const bool owner =
+        tid < 2 * N && gb_ok((long long)(tid < 2 * (N - 1) ? jb : 0) * kWS + (tid & 1) * kWH + 7,
+                             EX, w.status, sol);
     const int jo = has_tile ? jb : 0;
     const int half = rt;
     float* yc_base = rt ? YC1 : YC0;
@@ -1063,6 +1083,13 @@ __device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
     float2* redD = redA + 96;
     float* DL = reinterpret_cast<float*>(redA + 160);
     float* LP = DL + ((Nc + 3) & ~3);
+    // the layout is the same in every CTA of the cluster, so they all leave
+    // together (no cluster barrier is left waiting)
+    if (!gb_smem((size_t)(LP - sm + (lsm ? (size_t)Nc * KS : 0)) * sizeof(float), w.status,
+                 sol)) {
+        if (rank == 0) finish(g, sol, 0, false, false);
+        return;
+    }
 
     for (int i = tid; i < zero_count; i += T) sm[i] = 0.f;
     for (int jl = tid; jl < nk; jl += T) DL[jl] = w.dlow[sol * w.sN + k0 + jl];
@@ -1071,7 +1098,7 @@ __device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
 
     // thread: local knot jl, row half rt; block j = k0 + jl when j >= 1
     const int jl = tid >> 1, rt = tid & 1, half = rt;
-    const bool owner = jl < nk;
+    const bool owner = jl < nk && gb_ok((long long)jl * kWS + half * kWH + 7, EX, w.status, sol);
     const int j = k0 + jl;
     const bool has_tile = owner && j >= 1;
     float* yc_base = rt ? YC1 : YC0;
@@ -1374,6 +1401,14 @@ cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const f
     a.queue = w.queue;
     const size_t limit = (size_t)h->smem_optin;
     const int want_l = p->stop_rule == GATO_STOP_RESIDUAL;
+
+    // double-float arithmetic (pcg_ff.cu) when asked for; sizes beyond that
+    // kernel are rejected rather than solved at a lower precision
+    if (p->pcg_precision == GATO_PCG_PRECISION_FF) {
+        a.nh_smem = 0;
+        a.l_smem = 0;
+        return launch_pcg_ff(a, limit, st);
+    }
 
     const int H = (w.n + 1) / 2;
     const bool tiled_n = w.n >= 7 && w.n <= 16;

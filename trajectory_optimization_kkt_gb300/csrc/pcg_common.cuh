@@ -109,4 +109,9 @@ __device__ __forceinline__ void finish(const PcgArgs& g, int sol, int it, bool d
 // kernel)
 cudaError_t launch_pcg_rows(const PcgArgs& a, size_t smem_limit, cudaStream_t st);
 
+// the double-float kernel (pcg_ff.cu): cudaErrorInvalidConfiguration when the
+// sizes are beyond it (more than 2048 rows N n, more than 1024 when n > 16, or
+// its shared memory above smem_limit)
+cudaError_t launch_pcg_ff(const PcgArgs& a, size_t smem_limit, cudaStream_t st);
+
 }  // namespace gato

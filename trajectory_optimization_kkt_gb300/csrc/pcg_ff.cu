@@ -1,0 +1,448 @@
+// pcg_ff.cu -- batched PCG on S lambda = gamma with the symmetric stair
+// preconditioner in double-float arithmetic, and recovery of dz (GATO paper,
+// Sec. II and eq. (4): PCG refines lambda up to the tolerance eps; Sec. III:
+// one thread block per linear system, block-tridiagonal products, block
+// reductions).
+//
+// Why: the iteration count of CG in finite precision grows as the rounding
+// unit grows (the computed residuals lose their orthogonality and the
+// method re-explores converged directions).  On the horizons and conditioning
+// of the benchmark problems with stated iteration caps, fp32 PCG needs
+// 3-25 % more iterations than fp64 PCG to reach a relative residual of 1e-6,
+// and every fp32 rounding in the iteration (the product's input, its
+// accumulation, its output, the vector updates and the inner products)
+// contributes on its own: the count falls by about one iteration per extra
+// significand bit.  This kernel carries the vectors, the products' sums, the
+// inner products and the CG scalars as double-float values (about 48 bits);
+// the operator (the scaled coupling blocks Nhat_j, formed in fp32) and the
+// right-hand side stay as formed.  Its iterates are those of the fp32
+// kernels' iteration (same variables, same recurrence, same stopping rules),
+// computed more accurately.
+//
+// The iteration runs in the block-Jacobi-scaled variables lambda_hat =
+// L^T lambda, where S_hat = I + Nhat and the stair preconditioner is I - Nhat
+// (see pcg.cu).  Thread t owns the rows t, t + T, ... (R of them) of the
+// solve's N n rows; row a of knot j needs row a of Nhat_j (times x_{j-1}) and
+// column a of Nhat_{j+1} (times x_{j+1}), read from one copy of the blocks in
+// shared memory framed by two zero blocks, so that the first and last knot
+// need no branch.  The vectors p and r live in shared memory as high and low
+// arrays with a guard knot of zeros at each end.  Four block barriers per
+// iteration, as in the fp32 kernels; every block reduction sums the warps'
+// double-float partials in a fixed order, so results do not depend on
+// scheduling.
+#include "ff.cuh"
+#include "pcg_common.cuh"
+
+namespace gato {
+namespace {
+
+constexpr int kFFMaxThreads = 1024;
+
+// (Nhat x)_a for row a of knot j: row a of Nhat_j times x_{j-1} plus column a
+// of Nhat_{j+1} times x_{j+1}, two compensated chains.  NB holds the blocks
+// (block j at NB + j n^2: zero, Nhat_1 .. Nhat_{N-1}, zero), XH / XL the
+// vector with knot j at (j + 1) NP.
+template <int NP>
+__device__ __forceinline__ ff ff_row(const float* NB, int n, int nn, int j, int a,
+                                     const float* XH, const float* XL)
+{
+    const float* lo = NB + (size_t)j * nn + a * n;
+    const float* up = NB + (size_t)(j + 1) * nn + a;
+    const float4* mh = reinterpret_cast<const float4*>(XH + j * NP);
+    const float4* ml = reinterpret_cast<const float4*>(XL + j * NP);
+    const float4* ph = reinterpret_cast<const float4*>(XH + (j + 2) * NP);
+    const float4* pl = reinterpret_cast<const float4*>(XL + (j + 2) * NP);
+    Dot2 c1, c2;
+#pragma unroll
+    for (int q = 0; q < NP / 4; ++q) {
+        const float4 a4 = mh[q], b4 = ml[q], c4 = ph[q], d4 = pl[q];
+        const float xmh[4] = {a4.x, a4.y, a4.z, a4.w};
+        const float xml[4] = {b4.x, b4.y, b4.z, b4.w};
+        const float xph[4] = {c4.x, c4.y, c4.z, c4.w};
+        const float xpl[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int b = 4 * q + e;
+            if (b < n) {
+                c1.add(lo[b], xmh[e], xml[e]);
+                c2.add(up[b * n], xph[e], xpl[e]);
+            }
+        }
+    }
+    return ff_add(c1.value(), c2.value());
+}
+
+// sum over the block of one double-float and two floats per thread; every
+// thread returns the totals (fixed order: the warps' butterflies, then one
+// butterfly over the warp slots)
+__device__ __forceinline__ void ff_warp_reduce(ff& v, float& f1, float& f2)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const ff u{__shfl_xor_sync(0xffffffffu, v.h, o), __shfl_xor_sync(0xffffffffu, v.l, o)};
+        v = ff_add(v, u);
+        f1 += __shfl_xor_sync(0xffffffffu, f1, o);
+        f2 += __shfl_xor_sync(0xffffffffu, f2, o);
+    }
+}
+
+__device__ __forceinline__ void ff_post(ff v, float f1, float f2, float4* slots)
+{
+    ff_warp_reduce(v, f1, f2);
+    if (lane_id() == 0) slots[threadIdx.x >> 5] = make_float4(v.h, v.l, f1, f2);
+}
+
+__device__ __forceinline__ void ff_collect(const float4* slots, ff& v, float& f1, float& f2)
+{
+    const int lane = lane_id();
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane < (int)(blockDim.x >> 5)) t = slots[lane];
+    v = ff{t.x, t.y};
+    f1 = t.z;
+    f2 = t.w;
+    ff_warp_reduce(v, f1, f2);
+}
+
+// (L_j r_hat_j)_a^2 from the high parts of r (fp32: only the stopping test
+// reads it); L_j lower triangular, full n x n in global memory
+__device__ __forceinline__ float ff_lrow_sq(const float* Lj, const float* RH, int NP, int j, int a,
+                                            int n)
+{
+    const float* row = Lj + (size_t)a * n;
+    const float* x = RH + (j + 1) * NP;
+    float t = 0.f;
+    for (int b = 0; b <= a; ++b) t = fmaf(row[b], x[b], t);
+    return t * t;
+}
+
+template <int NP, int R>
+__global__ void __launch_bounds__(kFFMaxThreads, 1) k_pcg_ff(PcgArgs g)
+{
+    extern __shared__ __align__(16) float sm[];
+    const Work& w = g.w;
+    const int N = w.N, n = w.n, nn = n * n, T = blockDim.x, tid = threadIdx.x;
+    const int sol = blockIdx.x;
+    const int XS = (N + 2) * NP;
+    const int rule = g.rule;
+    const bool rule0 = rule == GATO_STOP_RESIDUAL;
+
+    float* PH = sm;
+    float* PL = PH + XS;
+    float* RH = PL + XS;
+    float* RL = RH + XS;
+    float4* slotA = reinterpret_cast<float4*>(RL + XS);
+    float4* slotC = slotA + 32;
+    float4* slotD = slotA + 64;
+    float* NB = reinterpret_cast<float*>(slotA + 96);
+    {
+        const size_t blocks = (size_t)(N + 1) * nn, scratch = (size_t)N * n;
+        if (!gb_smem((size_t)(NB - sm + round4(blocks > scratch ? blocks : scratch)) *
+                         sizeof(float),
+                     w.status, sol)) {
+            finish(g, sol, 0, false, false);
+            return;  // block-uniform
+        }
+    }
+
+    for (int i = tid; i < 4 * XS; i += T) sm[i] = 0.f;
+    {
+        const float* gN = w.Nh + sol * w.sKnn;
+        const int nb = (N - 1) * nn;
+        for (int i = tid; i < nn; i += T) {
+            NB[i] = 0.f;
+            NB[(size_t)N * nn + i] = 0.f;
+        }
+        for (int i = tid; i < nb; i += T) NB[nn + i] = gN[i];
+    }
+
+    // the thread's rows
+    int jr[R], ar[R];
+    bool valid[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        const int row = tid + i * T;
+        // a row's products read knots j - 1 .. j + 1 (the guarded vectors)
+        // and blocks j, j + 1 (the framed copy of Nhat)
+        valid[i] = row < N * n && gb_ok((long long)(row / n + 2) * NP + NP - 1, XS, w.status, sol) &&
+                   gb_ok((long long)(row / n + 2) * nn - 1, (long long)(N + 1) * nn, w.status, sol);
+        jr[i] = valid[i] ? row / n : 0;
+        ar[i] = valid[i] ? row - jr[i] * n : 0;
+    }
+    const float* ghat = g.rhs.ghat + sol * w.sNn;
+    const float* gam = g.rhs.gamma + sol * w.sNn;
+    const float* gL = w.L + sol * w.sNnn;
+    const float* dlow = w.dlow + sol * w.sN;
+
+    ff lam[R], r[R], p[R], v[R];
+    // lambda_hat0 = L^T lambda0 (compensated)
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        lam[i] = ff_of(0.f);
+        if (valid[i] && g.lambda0) {
+            const int j = jr[i], a = ar[i];
+            const float* Lj = gL + (size_t)j * nn;
+            const float* l0 = g.lambda0 + (size_t)sol * N * n + (size_t)j * n;
+            Dot2 d;
+            for (int b = a; b < n; ++b) d.add(Lj[(size_t)b * n + a], l0[b], 0.f);
+            lam[i] = d.value();
+        }
+    }
+    __syncthreads();  // zeroed vectors and copied blocks
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+        if (valid[i]) {
+            PH[(jr[i] + 1) * NP + ar[i]] = lam[i].h;
+            PL[(jr[i] + 1) * NP + ar[i]] = lam[i].l;
+        }
+    __syncthreads();
+    // r_hat = ghat - lambda_hat - Nhat lambda_hat
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        r[i] = ff_of(0.f);
+        if (valid[i]) {
+            const ff y = ff_row<NP>(NB, n, nn, jr[i], ar[i], PH, PL);
+            r[i] = ff_sub(ff_sub(ff_of(ghat[jr[i] * n + ar[i]]), lam[i]), y);
+            RH[(jr[i] + 1) * NP + ar[i]] = r[i].h;
+            RL[(jr[i] + 1) * NP + ar[i]] = r[i].l;
+        }
+    }
+    __syncthreads();
+    // z = (I - Nhat) r = p; eta = r^T z; the stopping reference and quantity
+    ff eta_part = ff_of(0.f);
+    float ref_part = 0.f, q_part = 0.f;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        p[i] = ff_of(0.f);
+        if (valid[i]) {
+            const int j = jr[i], a = ar[i], gi = j * n + a;
+            const ff y = ff_row<NP>(NB, n, nn, j, a, RH, RL);
+            p[i] = ff_sub(r[i], y);
+            eta_part = ff_add(eta_part, ff_mul(r[i], p[i]));
+            if (rule0) {
+                ref_part = fmaf(gam[gi], gam[gi], ref_part);
+                q_part += ff_lrow_sq(gL + (size_t)j * nn, RH, NP, j, a, n);
+            } else if (rule == GATO_STOP_SCALED) {
+                ref_part = fmaf(ghat[gi], ghat[gi], ref_part);
+                q_part = fmaf(r[i].h, r[i].h, q_part);
+            }
+        }
+    }
+    ff_post(eta_part, ref_part, q_part, slotA);
+    __syncthreads();
+    ff eta;
+    float ref, stopq;
+    ff_collect(slotA, eta, ref, stopq);
+    if (rule == GATO_STOP_PRECOND) {
+        ref = eta.h;
+        stopq = eta.h;
+    }
+    const float thr = g.eps * g.eps * ref;
+    bool done = stopq <= thr;
+    bool nonfinite = !isfinite(eta.h) || !isfinite(stopq);
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+        if (valid[i]) {
+            PH[(jr[i] + 1) * NP + ar[i]] = p[i].h;
+            PL[(jr[i] + 1) * NP + ar[i]] = p[i].l;
+        }
+    // the exact ||L r_hat|| of rule 0 is evaluated only once the per-knot
+    // lower bound sum_j dlow_j ||r_hat_j||^2 comes within 1.25 of the
+    // threshold (as in the fp32 kernels); a fallback evaluates it in the
+    // iteration where the bound drops below the threshold without it
+    bool exact_next = false;
+    if (rule0) {
+        float lb = 0.f;
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+            if (valid[i]) lb = fmaf(dlow[jr[i]] * r[i].h, r[i].h, lb);
+        float z0 = 0.f;
+        ff zf = ff_of(0.f);
+        ff_post(zf, lb, z0, slotC);
+        __syncthreads();
+        ff_collect(slotC, zf, lb, z0);
+        exact_next = lb <= 1.25f * thr;
+    }
+    __syncthreads();
+
+    int it = 0;
+    while (!done && !nonfinite && it < g.max_iters) {
+        ++it;
+        // A: v = S_hat p = p + Nhat p, p^T v
+        ff pv_part = ff_of(0.f);
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            v[i] = ff_of(0.f);
+            if (valid[i]) {
+                v[i] = ff_add(p[i], ff_row<NP>(NB, n, nn, jr[i], ar[i], PH, PL));
+                pv_part = ff_add(pv_part, ff_mul(p[i], v[i]));
+            }
+        }
+        ff_post(pv_part, 0.f, 0.f, slotA);
+        __syncthreads();
+        // B: alpha = eta / p^T v; lambda and r updates
+        ff pv;
+        float u1, u2;
+        ff_collect(slotA, pv, u1, u2);
+        const ff alpha = ff_div(eta, pv);
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+            if (valid[i]) {
+                lam[i] = ff_add(lam[i], ff_mul(alpha, p[i]));
+                r[i] = ff_sub(r[i], ff_mul(alpha, v[i]));
+                RH[(jr[i] + 1) * NP + ar[i]] = r[i].h;
+                RL[(jr[i] + 1) * NP + ar[i]] = r[i].l;
+            }
+        __syncthreads();
+        // C: z = (I - Nhat) r (kept in v), eta' = r^T z; the lower bound's
+        // and (gated in) the exact norm's shares
+        ff eta_part2 = ff_of(0.f);
+        float lb_part = 0.f, lsq_part = 0.f;
+        const bool exact = exact_next;
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+            if (valid[i]) {
+                const int j = jr[i], a = ar[i];
+                v[i] = ff_sub(r[i], ff_row<NP>(NB, n, nn, j, a, RH, RL));
+                eta_part2 = ff_add(eta_part2, ff_mul(r[i], v[i]));
+                if (rule0) {
+                    lb_part = fmaf(dlow[j] * r[i].h, r[i].h, lb_part);
+                    if (exact) lsq_part += ff_lrow_sq(gL + (size_t)j * nn, RH, NP, j, a, n);
+                } else if (rule == GATO_STOP_SCALED) {
+                    lb_part = fmaf(r[i].h, r[i].h, lb_part);
+                }
+            }
+        ff_post(eta_part2, lb_part, lsq_part, slotC);
+        __syncthreads();
+        // D: convergence, beta = eta' / eta, p = z + beta p
+        ff eta_new;
+        float lb, lsq;
+        ff_collect(slotC, eta_new, lb, lsq);
+        bool have_exact = exact;
+        if (rule0 && !exact && lb * 0.999f <= thr) {
+            float part = 0.f, z0 = 0.f;
+#pragma unroll
+            for (int i = 0; i < R; ++i)
+                if (valid[i]) part += ff_lrow_sq(gL + (size_t)jr[i] * nn, RH, NP, jr[i], ar[i], n);
+            ff zf = ff_of(0.f);
+            ff_post(zf, part, z0, slotD);
+            __syncthreads();
+            ff_collect(slotD, zf, lsq, z0);
+            have_exact = true;
+        }
+        stopq = rule0 ? lsq : (rule == GATO_STOP_SCALED ? lb : eta_new.h);
+        if (!isfinite(eta_new.h + pv.h + stopq + lb)) {  // NaN and Inf propagate
+            nonfinite = true;
+            break;
+        }
+        done = (!rule0 || have_exact) && stopq <= thr;
+        if (done) break;
+        exact_next = rule0 && lb <= 1.25f * thr;
+        const ff beta = ff_div(eta_new, eta);
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+            if (valid[i]) {
+                p[i] = ff_add(v[i], ff_mul(beta, p[i]));
+                PH[(jr[i] + 1) * NP + ar[i]] = p[i].h;
+                PL[(jr[i] + 1) * NP + ar[i]] = p[i].l;
+            }
+        eta = eta_new;
+        __syncthreads();
+    }
+    __syncthreads();
+    // lambda_hat to fp32 (h is the rounded sum of h + l), then lambda and dz;
+    // the recovery's scratch reuses the blocks' space
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+        if (valid[i]) PH[(jr[i] + 1) * NP + ar[i]] = lam[i].h;
+    __syncthreads();
+    recover_dz(g.w, g.rhs, g.lambda, g.dX, g.dU, sol,
+               [&](int k, int b) { return PH[(k + 1) * NP + b]; }, NB);
+    finish(g, sol, it, done, nonfinite);
+}
+
+// row width of the vectors: n padded to a multiple of 4 (the instantiations)
+int ff_np(int n)
+{
+    static const int widths[] = {4, 8, 12, 16, 20, 24, 28, 32, 36, 40, 48, 56, 64};
+    for (int v : widths)
+        if (n <= v) return v;
+    return 0;
+}
+
+// shared memory of one block: p and r (high and low) with guard knots, the
+// reduction slots, and the N + 1 coupling blocks (which the recovery reuses
+// as its N n scratch)
+size_t ff_smem_bytes(int N, int n, int NP)
+{
+    const size_t blocks = (size_t)(N + 1) * n * n;
+    const size_t scratch = (size_t)N * n;
+    return sizeof(float) *
+           (4 * (size_t)(N + 2) * NP + 96 * 4 + round4(blocks > scratch ? blocks : scratch));
+}
+
+// rows per thread: 1 up to 1024 rows, 2 up to 2048 when n <= 16; 0 beyond
+int ff_rows_per_thread(int N, int n)
+{
+    const long rows = (long)N * n;
+    if (rows <= kFFMaxThreads) return 1;
+    if (rows <= 2 * kFFMaxThreads && n <= 16) return 2;
+    return 0;
+}
+
+template <int NP, int R>
+cudaError_t launch_ff(const PcgArgs& a, int T, size_t limit, cudaStream_t st)
+{
+    const Work& w = a.w;
+    const size_t smem = ff_smem_bytes(w.N, w.n, NP);
+    if (smem > limit) return cudaErrorInvalidConfiguration;
+    auto kernel = k_pcg_ff<NP, R>;
+    if (smem > 48 * 1024) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    kernel<<<w.M, T, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int NP>
+cudaError_t launch_ff_np(const PcgArgs& a, size_t limit, cudaStream_t st)
+{
+    const int rows = a.w.N * a.w.n;
+    const int R = ff_rows_per_thread(a.w.N, a.w.n);
+    if (R == 0) return cudaErrorInvalidConfiguration;
+    int T = ((rows + R - 1) / R + 31) / 32 * 32;
+    if (T < 32) T = 32;
+    if (R == 1) return launch_ff<NP, 1>(a, T, limit, st);
+    if constexpr (NP <= 16) return launch_ff<NP, 2>(a, T, limit, st);
+    return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace
+
+bool pcg_ff_fits(int N, int n, size_t smem_limit)
+{
+    const int NP = ff_np(n);
+    return NP > 0 && ff_rows_per_thread(N, n) > 0 && ff_smem_bytes(N, n, NP) <= smem_limit;
+}
+
+cudaError_t launch_pcg_ff(const PcgArgs& a, size_t limit, cudaStream_t st)
+{
+    const int n = a.w.n;
+    if (n <= 4) return launch_ff_np<4>(a, limit, st);
+    if (n <= 8) return launch_ff_np<8>(a, limit, st);
+    if (n <= 12) return launch_ff_np<12>(a, limit, st);
+    if (n <= 16) return launch_ff_np<16>(a, limit, st);
+    if (n <= 20) return launch_ff_np<20>(a, limit, st);
+    if (n <= 24) return launch_ff_np<24>(a, limit, st);
+    if (n <= 28) return launch_ff_np<28>(a, limit, st);
+    if (n <= 32) return launch_ff_np<32>(a, limit, st);
+    if (n <= 36) return launch_ff_np<36>(a, limit, st);
+    if (n <= 40) return launch_ff_np<40>(a, limit, st);
+    if (n <= 48) return launch_ff_np<48>(a, limit, st);
+    if (n <= 56) return launch_ff_np<56>(a, limit, st);
+    if (n <= 64) return launch_ff_np<64>(a, limit, st);
+    return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace gato

@@ -206,11 +206,20 @@ __global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
     constexpr int SC = NP / 4 - RowTiles<NP, R>::RC;
     float4* TS = redA + 120;
     float* LS = reinterpret_cast<float*>(TS + (size_t)SC * R * 2 * T);
+    const bool l_staged_sm = g.rule == GATO_STOP_RESIDUAL && g.l_smem;
+    if (!gb_smem((size_t)(LS - sm + (l_staged_sm ? (size_t)N * n * NP : 0)) * sizeof(float),
+                 w.status, sol)) {
+        finish(g, sol, 0, false, false);
+        return;  // block-uniform
+    }
     for (int i = tid; i < 2 * XS; i += T) sm[i] = 0.f;
 
     const int j = tid / TPK, q = tid - j * TPK;
     const int a0 = q * R;
-    const bool owner = j < N;
+    // the thread's rows are stored at knot j's slots (j + 1) NP + a0 .. + R - 1
+    // and its products read knots j - 1 .. j + 1 of the guarded vector
+    const bool owner = j < N && gb_ok((long long)(j + 2) * NP + NP - 1, XS, w.status, sol) &&
+                       gb_ok(a0, n, w.status, sol);
     bool valid[R];
 #pragma unroll
     for (int i = 0; i < R; ++i) valid[i] = owner && a0 + i < n;

@@ -23,6 +23,7 @@ GATO_STATUS_PCG_MAX_ITERS = 1
 GATO_STATUS_NONPOSITIVE_PIVOT = 2
 GATO_STATUS_LINESEARCH_FAILED = 4
 GATO_STATUS_NONFINITE = 8
+GATO_STATUS_BOUNDS = 16
 
 GATO_PCG_AUTO = 0
 GATO_PCG_GENERIC = 1
@@ -49,6 +50,9 @@ GATO_FORM_SHARED = 1
 GATO_MERIT_FUSED = 0
 GATO_MERIT_PER_CANDIDATE = 1
 
+GATO_PCG_PRECISION_FP32 = 0
+GATO_PCG_PRECISION_FF = 1
+
 GATO_STOP_RESIDUAL = 0
 GATO_STOP_PRECOND = 1
 GATO_STOP_SCALED = 2
@@ -63,7 +67,7 @@ class GatoParams(ctypes.Structure):
                 ("n_alpha", ctypes.c_int), ("beta", ctypes.c_float), ("mu", ctypes.c_float),
                 ("merit_threads", ctypes.c_int), ("refine_eps", ctypes.c_float),
                 ("merit_kernel", ctypes.c_int), ("linsys", ctypes.c_int),
-                ("bdsv_horizon", ctypes.c_int)]
+                ("bdsv_horizon", ctypes.c_int), ("pcg_precision", ctypes.c_int)]
 
 
 class GatoSqpParams(ctypes.Structure):
@@ -88,15 +92,16 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    """libgato.so, or libgato_bounds.so when GATO_DEBUG_BOUNDS=1 is set."""
+    return _build.library_path()
 
 
 def load(path: Optional[str] = None):
-    """Load libgato.so (built by __graft_entry__.build()); raises if absent."""
+    """Load the library (built by __graft_entry__.build()); raises if absent."""
     global _lib
     if _lib is not None:
         return _lib
-    path = path or _build.LIB_PATH
+    path = path or library_path()
     if not os.path.exists(path):
         raise RuntimeError(f"CUDA library not built: {path} is missing (run build())")
     lib = ctypes.CDLL(path)
@@ -127,6 +132,8 @@ def load(path: Optional[str] = None):
     lib.gato_get_parts.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
     lib.gato_apply_step.argtypes = [vp, P] + [vp] * 5 + [vp]
     lib.gato_solve_kkt_noalloc.argtypes = [P, ip, ip, ip, ip] + [vp] * 8 + [vp] * 7 + [vp]
+    lib.gato_probe_fp32.argtypes = [ip, ip, ip, ip, vp, vp]
+    lib.gato_probe_fp32.restype = ctypes.c_longlong
     for fn in ("gato_create", "gato_set_timing", "gato_set_pcg_kernel", "gato_set_form_kernel",
                "gato_set_bdsv_kernel", "gato_get_stats", "gato_form_schur",
                "gato_get_schur", "gato_pcg_solve", "gato_bdsv_solve", "gato_linesearch",
@@ -360,12 +367,17 @@ def to_host(prob):
             for k, v in prob.items()}
 
 
-def solve_kkt_noalloc(params, prob, dX, dU, lam, iters, merit, best, status, stream=None):
+def solve_kkt_noalloc(params, prob, dX, dU, lam, iters, merit, best, status, stream=None,
+                      dims=None):
     """gato_solve_kkt_noalloc: the whole solve with the library's static scratch
-    (no handle, no device allocation by the library)."""
+    (no handle, no device allocation by the library).  dims = (M, N, n, m);
+    by default read from the shapes of Q and B (give it when B is None)."""
     import torch
-    M, N, n = prob["Q"].shape[:3]
-    m = prob["B"].shape[-1]
+    if dims is None:
+        M, N, n = prob["Q"].shape[:3]
+        m = prob["B"].shape[-1]
+    else:
+        M, N, n, m = dims
     _check("gato_solve_kkt_noalloc", load().gato_solve_kkt_noalloc(
         ctypes.byref(params), M, N, n, m, *[_ptr(prob.get(k), what=k) for k in _LQ],
         _ptr(dX), _ptr(dU), _ptr(lam), _ptr(iters, torch.int32, "iters"), _ptr(merit),
@@ -377,3 +389,15 @@ def to_device(prob, device="cuda"):
     import torch
     return {k: torch.as_tensor(v, dtype=torch.float32).contiguous().to(device)
             for k, v in prob.items()}
+
+
+def probe_fp32(packed: bool, blocks: int, threads: int, trips: int, sink, stream=None) -> int:
+    """Launch the fp32 FMA throughput probe (gato_probe_fp32) on ``stream``
+    (default: torch's current stream); returns the launch's flops."""
+    import torch
+    st = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    rc = load().gato_probe_fp32(int(bool(packed)), int(blocks), int(threads), int(trips),
+                                _ptr(sink, what="sink"), st)
+    if rc < 0:
+        raise GatoError("gato_probe_fp32", int(rc))
+    return int(rc)
