@@ -37,8 +37,8 @@ WORKLOAD_INDEX = 4  # M=256, N=128, n=14, m=7
 # solve launch at this workload, from an ncu capture; valid only for the
 # kernel source it was taken on (sha256 prefix of csrc/pcg.cu), null
 # otherwise.  Captured on 152 solves (one block per SM) and scaled
-# by the solves processed to the 256-solve launch (89.78 MB x 256 / 152).
-PCG_TRAFFIC = {"pcg_sha": "34571eb583c1e516", "bytes_per_launch": 150718572}
+# by the solves processed to the 256-solve launch (90.12 MB x 256 / 152).
+PCG_TRAFFIC = {"pcg_sha": "c31b70593b9ae9e0", "bytes_per_launch": 151774909}
 
 FP32_LANES_PER_SM = 128  # FFMA lanes per SM (4 sub-partitions x 32)
 
