@@ -382,7 +382,20 @@ def run_throughput_sweep(args, local):
                       flush=True)
 
 
-def _pcg_kernel_name(N, n, precision=0):
+def _ff_kernel_name(M, N, n, n_sm):
+    """The double-float kernel launch_pcg_ff picks: a cluster of two CTAs per
+    solve when the batch is at most half of the SMs (n <= 16, each CTA with at
+    least 256 rows, the CTAs' warps within one 32-lane butterfly), else one CTA
+    per solve."""
+    if n <= 16:
+        Nc = -(-N // 2)
+        warps = -(-(Nc * n) // 32)
+        if M * 2 <= n_sm and Nc < N and 2 * warps <= 32 and Nc * n >= 256:
+            return "k_pcg_ff_cluster<2>"
+    return "k_pcg_ff"
+
+
+def _pcg_kernel_name(N, n, precision=0, M=None, n_sm=152):
     """The PCG kernel GATO_PCG_AUTO picks for these sizes (the rules of
     launch_pcg_ex and launch_pcg_rows: the register-row kernel's rows per
     thread keep its two row tiles within 216 floats, and its block within
@@ -391,7 +404,7 @@ def _pcg_kernel_name(N, n, precision=0):
     (the refinement's corrections then run in the fp32 kernel named after
     the plus sign)."""
     if precision:
-        return "k_pcg_ff + " + _pcg_kernel_name(N, n)
+        return _ff_kernel_name(M or 1, N, n, n_sm) + " + " + _pcg_kernel_name(N, n)
     if 7 <= n <= 16:
         return "k_pcg_wide" if N <= 128 else ("k_pcg_cluster" if N <= 512 else "k_pcg_generic")
     if 16 < n <= 64:
@@ -441,7 +454,8 @@ def run_workloads(args, local):
         merit_bytes = 4 * M * (N * n * n + K * (m * m + n * n + n * m) + N * n + K * m + K * n
                                + n + N * n + K * m + (w.n_alpha + 1) + 1)
         merit_gbs = merit_bytes / (stages["merit"] * 1e-6) / 1e9
-        pcg_kernel = _pcg_kernel_name(N, n, w.pcg_precision)
+        pcg_kernel = _pcg_kernel_name(N, n, w.pcg_precision, M,
+                                      torch.cuda.get_device_properties(dev).multi_processor_count)
         row = {"workload": w.name, "M": M, "N": N, "n": n, "m": m, "parts": parts,
                "solves_per_s": M / (ms / 1000.0), "ms_per_call": ms,
                "pcg_iters_per_sec": iters / (ms / 1000.0), "pcg_iters_per_solve": iters / M,
@@ -805,7 +819,7 @@ def run_gpu(args, world, rank, local):
                          "bound": "alu", "achieved": achieved_tf, "peak": alu_peak_tf,
                          "unit": "TFLOP/s", "frac": achieved_tf / alu_peak_tf,
                          "traffic": traffic,
-                         "kernel": _pcg_kernel_name(N, n, w.pcg_precision)
+                         "kernel": _pcg_kernel_name(N, n, w.pcg_precision, M, n_sm)
                                    + " (solve + refinement launches)",
                          "peak_basis": "measured in this run: fp32 FMA probe "
                                        "(gato_probe_fp32), faster of scalar and packed form; "

@@ -420,14 +420,15 @@ FF_SIZES = [
     ("N4_n64_m16", 1, 4, 64, 16),
     ("N100_n14_m7_two_rows", 2, 100, 14, 7),   # 1400 rows: two per thread
     ("N128_n16_m8_two_rows", 1, 128, 16, 8),   # 2048 rows, the largest
+    ("N45_n12_m4_cluster", 2, 45, 12, 4),      # two CTAs per solve, 23 + 22 knots
 ]
 
 
 @pytest.mark.parametrize("name,M,N,n,m", FF_SIZES, ids=[c[0] for c in FF_SIZES])
 def test_double_float_pcg_sizes(name, M, N, n, m):
     """Every size class of the double-float kernel (one and two rows per
-    thread, n up to 64, N = 1) against the oracle, and against the fp32
-    kernel's lambda."""
+    thread, n up to 64, N = 1, a solve split over two CTAs of a cluster with a
+    ragged split) against the oracle, and against the fp32 kernel's lambda."""
     prob = random_lq(M, N, n, m, seed=950 + N + n)
     p = gato.default_params(pcg_max_iters=5000, refine_steps=1, pcg_precision=FF)
     out = solve(prob, p)
@@ -454,11 +455,12 @@ def test_double_float_pcg_other_stop_rules(rule):
         assert ok and it * 0.97 - 3 <= out["iters"][j] <= it * 1.03 + 3, (j, it, out["iters"][j])
 
 
-def test_double_float_pcg_warm_start():
+@pytest.mark.parametrize("wi,N", [(0, 24), (2, 64)], ids=["one_cta", "cluster"])
+def test_double_float_pcg_warm_start(wi, N):
     """From the exact multipliers no iteration is needed; from half of them
-    fewer than from zero."""
-    w = WORKLOADS[0]
-    prob = make_batch(w, M=2, N=24)
+    fewer than from zero (one CTA per solve, and two CTAs of a cluster)."""
+    w = WORKLOADS[wi]
+    prob = make_batch(w, M=2, N=N)
     lam = np.stack([oracle.direct_solve(oracle.solve_one(prob, j))[2] for j in range(2)])
     p = params_for(w, refine_steps=0, pcg_max_iters=1000)
     at = pcg_only(prob, gato.default_params(pcg_eps=1e-3, pcg_precision=FF), lambda0=lam)

@@ -29,16 +29,10 @@
 //     from global memory), one thread per vector element.
 // k_pcg_rows<NP, R> (pcg_rows.cu; the default for 16 < n <= 64 where its
 //     block fits): whole rows of the coupling blocks in registers.
-#include <cooperative_groups.h>
-
 #include "pcg_common.cuh"
 
 namespace gato {
 namespace {
-
-namespace cg = cooperative_groups;
-
-
 
 // ===========================================================================
 // generic kernel
@@ -1014,47 +1008,6 @@ __device__ __forceinline__ float2 cluster_collect2(cg::cluster_group& cl, float2
     return s;
 }
 
-// lambda = L^-T lambda_hat for this CTA's knots, then (after a cluster
-// barrier, with the neighbours' lambda in global memory) dz by eq. (4)
-template <typename LhatFn>
-__device__ __forceinline__ void cluster_recover(cg::cluster_group& cl, const PcgArgs& g, int sol,
-                                                int k0, int nk, LhatFn lhat)
-{
-    const Work& w = g.w;
-    const int N = w.N, n = w.n, m = w.m, T = blockDim.x, tid = threadIdx.x;
-    const size_t Nn = (size_t)N * n;
-    float* lam = g.lambda + (size_t)sol * Nn;
-    const float* gLi = w.Linv + sol * w.sNnn;
-    for (int i = tid; i < nk * n; i += T) {
-        const int jl = i / n, a = i - jl * n, j = k0 + jl;
-        lam[(size_t)j * n + a] = strided_dot<16>(gLi + (size_t)j * n * n + a, n,
-                                                 [&](int b) { return lhat(jl, b); }, a, n);
-    }
-    cl.sync();
-    const float* Qi = w.Qinv + sol * w.sNnn;
-    const float* Ob = w.O + sol * w.sKnn;
-    const float* av = g.rhs.avec + sol * w.sNn;
-    auto at = [](const float* v) { return [v](int b) { return v[b]; }; };
-    for (int i = tid; i < nk * n; i += T) {
-        const int kl = i / n, a = i - kl * n, k = k0 + kl;
-        float x = av[(size_t)k * n + a];
-        x += strided_dot<16>(Qi + (size_t)k * n * n + a * n, 1, at(lam + (size_t)k * n), 0, n);
-        if (k < N - 1)
-            x += strided_dot<16>(Ob + (size_t)k * n * n + a, n, at(lam + (size_t)(k + 1) * n), 0,
-                                 n);
-        g.dX[(size_t)sol * Nn + (size_t)k * n + a] = x;
-    }
-    const int ku = min(nk, N - 1 - k0);  // this CTA's knots that have a control
-    const float* Vb = w.V + sol * w.sKnm;
-    const float* bv = g.rhs.bvec + sol * w.sKm;
-    for (int t = tid; t < ku * m; t += T) {
-        const int kl = t / m, c = t - kl * m, k = k0 + kl;
-        const float u = strided_dot<16>(Vb + (size_t)k * n * m + c, m,
-                                        at(lam + (size_t)(k + 1) * n), 0, n);
-        g.dU[(size_t)sol * (N - 1) * m + (size_t)k * m + c] = bv[(size_t)k * m + c] - u;
-    }
-}
-
 template <int H, int C>
 __device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
 {
@@ -1407,7 +1360,7 @@ cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const f
     if (p->pcg_precision == GATO_PCG_PRECISION_FF) {
         a.nh_smem = 0;
         a.l_smem = 0;
-        return launch_pcg_ff(a, limit, st);
+        return launch_pcg_ff(a, limit, h->num_sms, st);
     }
 
     const int H = (w.n + 1) / 2;

@@ -3,9 +3,13 @@
 // count and status bits).
 #pragma once
 
+#include <cooperative_groups.h>
+
 #include "gato_internal.cuh"
 
 namespace gato {
+
+namespace cg = cooperative_groups;
 
 struct PcgArgs {
     Work w;
@@ -104,6 +108,47 @@ __device__ __forceinline__ void finish(const PcgArgs& g, int sol, int it, bool d
     }
 }
 
+// lambda = L^-T lambda_hat for this CTA's knots, then (after a cluster
+// barrier, with the neighbours' lambda in global memory) dz by eq. (4)
+template <typename LhatFn>
+__device__ __forceinline__ void cluster_recover(cg::cluster_group& cl, const PcgArgs& g, int sol,
+                                                int k0, int nk, LhatFn lhat)
+{
+    const Work& w = g.w;
+    const int N = w.N, n = w.n, m = w.m, T = blockDim.x, tid = threadIdx.x;
+    const size_t Nn = (size_t)N * n;
+    float* lam = g.lambda + (size_t)sol * Nn;
+    const float* gLi = w.Linv + sol * w.sNnn;
+    for (int i = tid; i < nk * n; i += T) {
+        const int jl = i / n, a = i - jl * n, j = k0 + jl;
+        lam[(size_t)j * n + a] = strided_dot<16>(gLi + (size_t)j * n * n + a, n,
+                                                 [&](int b) { return lhat(jl, b); }, a, n);
+    }
+    cl.sync();
+    const float* Qi = w.Qinv + sol * w.sNnn;
+    const float* Ob = w.O + sol * w.sKnn;
+    const float* av = g.rhs.avec + sol * w.sNn;
+    auto at = [](const float* v) { return [v](int b) { return v[b]; }; };
+    for (int i = tid; i < nk * n; i += T) {
+        const int kl = i / n, a = i - kl * n, k = k0 + kl;
+        float x = av[(size_t)k * n + a];
+        x += strided_dot<16>(Qi + (size_t)k * n * n + a * n, 1, at(lam + (size_t)k * n), 0, n);
+        if (k < N - 1)
+            x += strided_dot<16>(Ob + (size_t)k * n * n + a, n, at(lam + (size_t)(k + 1) * n), 0,
+                                 n);
+        g.dX[(size_t)sol * Nn + (size_t)k * n + a] = x;
+    }
+    const int ku = min(nk, N - 1 - k0);  // this CTA's knots that have a control
+    const float* Vb = w.V + sol * w.sKnm;
+    const float* bv = g.rhs.bvec + sol * w.sKm;
+    for (int t = tid; t < ku * m; t += T) {
+        const int kl = t / m, c = t - kl * m, k = k0 + kl;
+        const float u = strided_dot<16>(Vb + (size_t)k * n * m + c, m,
+                                        at(lam + (size_t)(k + 1) * n), 0, n);
+        g.dU[(size_t)sol * (N - 1) * m + (size_t)k * m + c] = bv[(size_t)k * m + c] - u;
+    }
+}
+
 // the register-row kernel (pcg_rows.cu): launched when it applies to the
 // sizes, else cudaErrorInvalidConfiguration (the caller then takes another
 // kernel)
@@ -111,7 +156,8 @@ cudaError_t launch_pcg_rows(const PcgArgs& a, size_t smem_limit, cudaStream_t st
 
 // the double-float kernel (pcg_ff.cu): cudaErrorInvalidConfiguration when the
 // sizes are beyond it (more than 2048 rows N n, more than 1024 when n > 16, or
-// its shared memory above smem_limit)
-cudaError_t launch_pcg_ff(const PcgArgs& a, size_t smem_limit, cudaStream_t st);
+// its shared memory above smem_limit); a batch of at most half the SM count
+// runs each solve over a cluster of two CTAs when each keeps enough rows
+cudaError_t launch_pcg_ff(const PcgArgs& a, size_t smem_limit, int num_sms, cudaStream_t st);
 
 }  // namespace gato

@@ -37,6 +37,10 @@ namespace gato {
 namespace {
 
 constexpr int kFFMaxThreads = 1024;
+// rows per CTA from which a solve is split over a cluster of two CTAs: measured
+// on workload 2's sizes (448 rows per CTA) the split saves a quarter of the
+// solve, with 56 rows per CTA (four CTAs at N = 16, n = 14) it costs 14 %
+constexpr int kFFClusterRows = 256;
 
 // (Nhat x)_a for row a of knot j: row a of Nhat_j times x_{j-1} plus column a
 // of Nhat_{j+1} times x_{j+1}, two compensated chains.  NB holds the blocks
@@ -360,6 +364,252 @@ __global__ void __launch_bounds__(kFFMaxThreads, 1) k_pcg_ff(PcgArgs g)
     finish(g, sol, it, done, nonfinite);
 }
 
+// ---------------------------------------------------------------------------
+// The same solve split over a cluster of C CTAs (when the batch leaves SMs
+// idle and the CTAs keep enough rows): CTA c owns knots c Nc .. c Nc + nk - 1 (Nc = ceil(N / C)) with one
+// row per thread, and holds the coupling blocks of its knots plus the one
+// that couples its last knot to the next CTA's first.  A vector update
+// writes the CTA's first and last knots also into the guard slots of the
+// neighbouring CTAs (distributed shared memory), so the products read only
+// local memory.  Every barrier is a cluster barrier; a block reduction adds
+// all CTAs' warp slots in rank order, so every CTA holds the same scalars and
+// takes the same branches.
+// ---------------------------------------------------------------------------
+
+// the double-float totals of the C CTAs' warp slots (C nw <= 32 slots)
+template <int C>
+__device__ __forceinline__ void ff_collect_cluster(cg::cluster_group& cl, float4* slots,
+                                                   ff& v, float& f1, float& f2)
+{
+    const int lane = lane_id(), nw = (int)(blockDim.x >> 5);
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane < C * nw) {
+        const float4* rs = cl.map_shared_rank(slots, lane / nw);
+        t = rs[lane % nw];
+    }
+    v = ff{t.x, t.y};
+    f1 = t.z;
+    f2 = t.w;
+    ff_warp_reduce(v, f1, f2);
+}
+
+// a CTA of a cluster has at most 1024 / C threads (its warp slots and the
+// other CTAs' fit one 32-lane butterfly), which leaves more registers
+template <int NP, int C>
+__global__ void __launch_bounds__(kFFMaxThreads / C, 1) k_pcg_ff_cluster(PcgArgs g)
+{
+    extern __shared__ __align__(16) float sm[];
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank();
+    const int sol = (int)(blockIdx.x / C);
+    const Work& w = g.w;
+    const int N = w.N, n = w.n, nn = n * n, T = blockDim.x, tid = threadIdx.x;
+    const int Nc = (N + C - 1) / C;
+    const int k0 = rank * Nc;        // first knot of this CTA
+    const int nk = min(Nc, N - k0);  // its knots (>= 1: the launcher checks)
+    const int XS = (Nc + 2) * NP;
+    const int rule = g.rule;
+    const bool rule0 = rule == GATO_STOP_RESIDUAL;
+
+    float* PH = sm;
+    float* PL = PH + XS;
+    float* RH = PL + XS;
+    float* RL = RH + XS;
+    float4* slotA = reinterpret_cast<float4*>(RL + XS);
+    float4* slotC = slotA + 32;
+    float4* slotD = slotA + 64;
+    float* NB = reinterpret_cast<float*>(slotA + 96);
+    {
+        const size_t blocks = (size_t)(Nc + 1) * nn, scratch = (size_t)Nc * n;
+        // the same layout in every CTA: all leave together
+        if (!gb_smem((size_t)(NB - sm + round4(blocks > scratch ? blocks : scratch)) *
+                         sizeof(float),
+                     w.status, sol)) {
+            if (rank == 0) finish(g, sol, 0, false, false);
+            return;
+        }
+    }
+    // the neighbours' vectors (for the guard-slot writes)
+    float* nPH[2] = {nullptr, nullptr};
+    float* nPL[2] = {nullptr, nullptr};
+    float* nRH[2] = {nullptr, nullptr};
+    float* nRL[2] = {nullptr, nullptr};
+    if (rank > 0) {
+        nPH[0] = cl.map_shared_rank(PH, rank - 1);
+        nPL[0] = cl.map_shared_rank(PL, rank - 1);
+        nRH[0] = cl.map_shared_rank(RH, rank - 1);
+        nRL[0] = cl.map_shared_rank(RL, rank - 1);
+    }
+    if (rank < C - 1) {
+        nPH[1] = cl.map_shared_rank(PH, rank + 1);
+        nPL[1] = cl.map_shared_rank(PL, rank + 1);
+        nRH[1] = cl.map_shared_rank(RH, rank + 1);
+        nRL[1] = cl.map_shared_rank(RL, rank + 1);
+    }
+
+    for (int i = tid; i < 4 * XS; i += T) sm[i] = 0.f;
+    {
+        // block jl (jl = 0 .. Nc) is Nhat_{k0 + jl} where it exists, else zero
+        const float* gN = w.Nh + sol * w.sKnn;
+        for (int i = tid; i < (Nc + 1) * nn; i += T) {
+            const int jl = i / nn, j = k0 + jl;
+            NB[i] = (jl <= nk && j >= 1 && j <= N - 1) ? gN[(size_t)(j - 1) * nn + (i - jl * nn)]
+                                                       : 0.f;
+        }
+    }
+    const int row = tid;
+    const bool valid = row < nk * n && gb_ok((long long)(row / n + 2) * NP + NP - 1, XS,
+                                             w.status, sol);
+    const int jl = valid ? row / n : 0, a = valid ? row - jl * n : 0, j = k0 + jl;
+    // a value of this thread's row into p or r, and into a neighbour's guard
+    // slot when the row is a boundary knot's
+    auto put = [&](float* XH, float* XL, float* const (&nH)[2], float* const (&nL)[2], ff v) {
+        if (!valid) return;
+        XH[(jl + 1) * NP + a] = v.h;
+        XL[(jl + 1) * NP + a] = v.l;
+        if (jl == 0 && rank > 0) {
+            nH[0][(Nc + 1) * NP + a] = v.h;
+            nL[0][(Nc + 1) * NP + a] = v.l;
+        }
+        if (jl == nk - 1 && rank < C - 1) {
+            nH[1][a] = v.h;
+            nL[1][a] = v.l;
+        }
+    };
+    const float* ghat = g.rhs.ghat + sol * w.sNn;
+    const float* gam = g.rhs.gamma + sol * w.sNn;
+    const float* gL = w.L + sol * w.sNnn;
+    const float* dlow = w.dlow + sol * w.sN;
+    const float dl = valid ? dlow[j] : 0.f;
+
+    ff lam = ff_of(0.f), r = ff_of(0.f), p = ff_of(0.f), v = ff_of(0.f);
+    if (valid && g.lambda0) {
+        const float* Lj = gL + (size_t)j * nn;
+        const float* l0 = g.lambda0 + (size_t)sol * N * n + (size_t)j * n;
+        Dot2 d;
+        for (int b = a; b < n; ++b) d.add(Lj[(size_t)b * n + a], l0[b], 0.f);
+        lam = d.value();
+    }
+    cl.sync();  // zeroed vectors and blocks in every CTA
+    put(PH, PL, nPH, nPL, lam);
+    cl.sync();
+    if (valid) {
+        r = ff_sub(ff_sub(ff_of(ghat[j * n + a]), lam), ff_row<NP>(NB, n, nn, jl, a, PH, PL));
+        put(RH, RL, nRH, nRL, r);
+    }
+    cl.sync();
+    ff eta_part = ff_of(0.f);
+    float ref_part = 0.f, q_part = 0.f;
+    if (valid) {
+        const int gi = j * n + a;
+        p = ff_sub(r, ff_row<NP>(NB, n, nn, jl, a, RH, RL));
+        eta_part = ff_mul(r, p);
+        if (rule0) {
+            ref_part = gam[gi] * gam[gi];
+            q_part = ff_lrow_sq(gL + (size_t)j * nn, RH, NP, jl, a, n);
+        } else if (rule == GATO_STOP_SCALED) {
+            ref_part = ghat[gi] * ghat[gi];
+            q_part = r.h * r.h;
+        }
+    }
+    ff_post(eta_part, ref_part, q_part, slotA);
+    cl.sync();
+    ff eta;
+    float ref, stopq;
+    ff_collect_cluster<C>(cl, slotA, eta, ref, stopq);
+    if (rule == GATO_STOP_PRECOND) {
+        ref = eta.h;
+        stopq = eta.h;
+    }
+    const float thr = g.eps * g.eps * ref;
+    bool done = stopq <= thr;
+    bool nonfinite = !isfinite(eta.h) || !isfinite(stopq);
+    put(PH, PL, nPH, nPL, p);
+    bool exact_next = false;
+    if (rule0) {
+        float lb = valid ? dl * r.h * r.h : 0.f, z0 = 0.f;
+        ff zf = ff_of(0.f);
+        ff_post(zf, lb, z0, slotC);
+        cl.sync();
+        ff_collect_cluster<C>(cl, slotC, zf, lb, z0);
+        exact_next = lb <= 1.25f * thr;
+    }
+    cl.sync();
+
+    int it = 0;
+    while (!done && !nonfinite && it < g.max_iters) {
+        ++it;
+        // A: v = p + Nhat p, p^T v
+        ff pv_part = ff_of(0.f);
+        if (valid) {
+            v = ff_add(p, ff_row<NP>(NB, n, nn, jl, a, PH, PL));
+            pv_part = ff_mul(p, v);
+        }
+        ff_post(pv_part, 0.f, 0.f, slotA);
+        cl.sync();
+        // B: alpha; lambda and r
+        ff pv;
+        float u1, u2;
+        ff_collect_cluster<C>(cl, slotA, pv, u1, u2);
+        const ff alpha = ff_div(eta, pv);
+        if (valid) {
+            lam = ff_add(lam, ff_mul(alpha, p));
+            r = ff_sub(r, ff_mul(alpha, v));
+            put(RH, RL, nRH, nRL, r);
+        }
+        cl.sync();
+        // C: z = r - Nhat r, eta' = r^T z, the bound's and the exact norm's shares
+        ff eta_part2 = ff_of(0.f);
+        float lb_part = 0.f, lsq_part = 0.f;
+        const bool exact = exact_next;
+        if (valid) {
+            v = ff_sub(r, ff_row<NP>(NB, n, nn, jl, a, RH, RL));
+            eta_part2 = ff_mul(r, v);
+            if (rule0) {
+                lb_part = dl * r.h * r.h;
+                if (exact) lsq_part = ff_lrow_sq(gL + (size_t)j * nn, RH, NP, jl, a, n);
+            } else if (rule == GATO_STOP_SCALED) {
+                lb_part = r.h * r.h;
+            }
+        }
+        ff_post(eta_part2, lb_part, lsq_part, slotC);
+        cl.sync();
+        // D: convergence, beta, p
+        ff eta_new;
+        float lb, lsq;
+        ff_collect_cluster<C>(cl, slotC, eta_new, lb, lsq);
+        bool have_exact = exact;
+        if (rule0 && !exact && lb * 0.999f <= thr) {
+            float part = valid ? ff_lrow_sq(gL + (size_t)j * nn, RH, NP, jl, a, n) : 0.f, z0 = 0.f;
+            ff zf = ff_of(0.f);
+            ff_post(zf, part, z0, slotD);
+            cl.sync();
+            ff_collect_cluster<C>(cl, slotD, zf, lsq, z0);
+            have_exact = true;
+        }
+        stopq = rule0 ? lsq : (rule == GATO_STOP_SCALED ? lb : eta_new.h);
+        if (!isfinite(eta_new.h + pv.h + stopq + lb)) {  // NaN and Inf propagate
+            nonfinite = true;
+            break;
+        }
+        done = (!rule0 || have_exact) && stopq <= thr;
+        if (done) break;
+        exact_next = rule0 && lb <= 1.25f * thr;
+        const ff beta = ff_div(eta_new, eta);
+        if (valid) {
+            p = ff_add(v, ff_mul(beta, p));
+            put(PH, PL, nPH, nPL, p);
+        }
+        eta = eta_new;
+        cl.sync();
+    }
+    cl.sync();
+    if (valid) PH[(jl + 1) * NP + a] = lam.h;
+    cl.sync();
+    cluster_recover(cl, g, sol, k0, nk, [&](int kl, int b) { return PH[(kl + 1) * NP + b]; });
+    if (rank == 0) finish(g, sol, it, done, nonfinite);
+}
+
 // row width of the vectors: n padded to a multiple of 4 (the instantiations)
 int ff_np(int n)
 {
@@ -405,9 +655,60 @@ cudaError_t launch_ff(const PcgArgs& a, int T, size_t limit, cudaStream_t st)
     return cudaGetLastError();
 }
 
-template <int NP>
-cudaError_t launch_ff_np(const PcgArgs& a, size_t limit, cudaStream_t st)
+// one solve per cluster of C CTAs (grid M C); cudaErrorInvalidConfiguration
+// when the split does not apply or no such cluster fits
+template <int NP, int C>
+cudaError_t launch_ff_cluster(const PcgArgs& a, size_t limit, cudaStream_t st)
 {
+    const Work& w = a.w;
+    const int Nc = (w.N + C - 1) / C;
+    if ((C - 1) * Nc >= w.N) return cudaErrorInvalidConfiguration;  // a CTA without knots
+    const int rows = Nc * w.n;
+    int T = (rows + 31) / 32 * 32;
+    if (T < 32) T = 32;
+    if (T > kFFMaxThreads || C * (T / 32) > 32) return cudaErrorInvalidConfiguration;
+    const size_t smem = ff_smem_bytes(Nc, w.n, NP);
+    if (smem > limit) return cudaErrorInvalidConfiguration;
+    auto kernel = k_pcg_ff_cluster<NP, C>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(w.M * C), 1, 1);
+    cfg.blockDim = dim3((unsigned)T, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+    if (e != cudaSuccess || clusters < 1) {
+        cudaGetLastError();
+        return cudaErrorInvalidConfiguration;
+    }
+    e = cudaLaunchKernelEx(&cfg, kernel, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <int NP>
+cudaError_t launch_ff_np(const PcgArgs& a, size_t limit, int num_sms, cudaStream_t st)
+{
+    // a batch of at most half the SMs: each solve over two CTAs (n <= 16),
+    // when each keeps at least kFFClusterRows rows; below that the cluster
+    // barriers and the remote reductions cost more than the halved work
+    if constexpr (NP <= 16) {
+        const int Nc = (a.w.N + 1) / 2;
+        if (a.w.M * 2 <= num_sms && Nc * a.w.n >= kFFClusterRows) {
+            const cudaError_t e = launch_ff_cluster<NP, 2>(a, limit, st);
+            if (e != cudaErrorInvalidConfiguration) return e;
+        }
+    }
     const int rows = a.w.N * a.w.n;
     const int R = ff_rows_per_thread(a.w.N, a.w.n);
     if (R == 0) return cudaErrorInvalidConfiguration;
@@ -426,22 +727,22 @@ bool pcg_ff_fits(int N, int n, size_t smem_limit)
     return NP > 0 && ff_rows_per_thread(N, n) > 0 && ff_smem_bytes(N, n, NP) <= smem_limit;
 }
 
-cudaError_t launch_pcg_ff(const PcgArgs& a, size_t limit, cudaStream_t st)
+cudaError_t launch_pcg_ff(const PcgArgs& a, size_t limit, int num_sms, cudaStream_t st)
 {
     const int n = a.w.n;
-    if (n <= 4) return launch_ff_np<4>(a, limit, st);
-    if (n <= 8) return launch_ff_np<8>(a, limit, st);
-    if (n <= 12) return launch_ff_np<12>(a, limit, st);
-    if (n <= 16) return launch_ff_np<16>(a, limit, st);
-    if (n <= 20) return launch_ff_np<20>(a, limit, st);
-    if (n <= 24) return launch_ff_np<24>(a, limit, st);
-    if (n <= 28) return launch_ff_np<28>(a, limit, st);
-    if (n <= 32) return launch_ff_np<32>(a, limit, st);
-    if (n <= 36) return launch_ff_np<36>(a, limit, st);
-    if (n <= 40) return launch_ff_np<40>(a, limit, st);
-    if (n <= 48) return launch_ff_np<48>(a, limit, st);
-    if (n <= 56) return launch_ff_np<56>(a, limit, st);
-    if (n <= 64) return launch_ff_np<64>(a, limit, st);
+    if (n <= 4) return launch_ff_np<4>(a, limit, num_sms, st);
+    if (n <= 8) return launch_ff_np<8>(a, limit, num_sms, st);
+    if (n <= 12) return launch_ff_np<12>(a, limit, num_sms, st);
+    if (n <= 16) return launch_ff_np<16>(a, limit, num_sms, st);
+    if (n <= 20) return launch_ff_np<20>(a, limit, num_sms, st);
+    if (n <= 24) return launch_ff_np<24>(a, limit, num_sms, st);
+    if (n <= 28) return launch_ff_np<28>(a, limit, num_sms, st);
+    if (n <= 32) return launch_ff_np<32>(a, limit, num_sms, st);
+    if (n <= 36) return launch_ff_np<36>(a, limit, num_sms, st);
+    if (n <= 40) return launch_ff_np<40>(a, limit, num_sms, st);
+    if (n <= 48) return launch_ff_np<48>(a, limit, num_sms, st);
+    if (n <= 56) return launch_ff_np<56>(a, limit, num_sms, st);
+    if (n <= 64) return launch_ff_np<64>(a, limit, num_sms, st);
     return cudaErrorInvalidConfiguration;
 }
 
