@@ -395,16 +395,17 @@ def _ff_kernel_name(M, N, n, n_sm):
     return "k_pcg_ff"
 
 
-def _pcg_kernel_name(N, n, precision=0, M=None, n_sm=152):
+def _pcg_kernel_name(N, n, precision=0, M=None, n_sm=152, refine_solver=0):
     """The PCG kernel GATO_PCG_AUTO picks for these sizes (the rules of
     launch_pcg_ex and launch_pcg_rows: the register-row kernel's rows per
     thread keep its two row tiles within 216 floats, and its block within
     the registers, at most 256 threads with more than one row per thread);
     the double-float kernel for the main solve when that precision is set
     (the refinement's corrections then run in the fp32 kernel named after
-    the plus sign)."""
+    the plus sign, unless they are direct)."""
     if precision:
-        return _ff_kernel_name(M or 1, N, n, n_sm) + " + " + _pcg_kernel_name(N, n)
+        main = _ff_kernel_name(M or 1, N, n, n_sm)
+        return main if refine_solver else main + " + " + _pcg_kernel_name(N, n)
     if 7 <= n <= 16:
         return "k_pcg_wide" if N <= 128 else ("k_pcg_cluster" if N <= 512 else "k_pcg_generic")
     if 16 < n <= 64:
@@ -448,14 +449,16 @@ def run_workloads(args, local):
             ms, stages, iters, bad = _time_solver(torch, s, p, d, out, steps, flush, stream)
             parts = s.get_parts()
         flops_it = 2 * 2 * (3 * N - 2) * n * n + 12 * N * n
-        pcg_us = stages["linsys"] + stages["refine"]
+        # with direct corrections the refinement stage runs no PCG iteration
+        pcg_us = stages["linsys"] + (0.0 if w.refine_solver else stages["refine"])
         achieved_tf = flops_it * iters / (pcg_us * 1e-6) / 1e12
         K = N - 1
         merit_bytes = 4 * M * (N * n * n + K * (m * m + n * n + n * m) + N * n + K * m + K * n
                                + n + N * n + K * m + (w.n_alpha + 1) + 1)
         merit_gbs = merit_bytes / (stages["merit"] * 1e-6) / 1e9
         pcg_kernel = _pcg_kernel_name(N, n, w.pcg_precision, M,
-                                      torch.cuda.get_device_properties(dev).multi_processor_count)
+                                      torch.cuda.get_device_properties(dev).multi_processor_count,
+                                      w.refine_solver)
         row = {"workload": w.name, "M": M, "N": N, "n": n, "m": m, "parts": parts,
                "solves_per_s": M / (ms / 1000.0), "ms_per_call": ms,
                "pcg_iters_per_sec": iters / (ms / 1000.0), "pcg_iters_per_solve": iters / M,
@@ -751,7 +754,9 @@ def run_gpu(args, world, rank, local):
     N, n = w.N, w.n
     flops_it = 2 * 2 * (3 * N - 2) * n * n + 12 * N * n
     iters_per_step = iters_total / args.steps
-    pcg_stage_us = statistics.mean(a + b for a, b in zip(pcg_us, refine_us))
+    # with direct corrections the refinement stage runs no PCG iteration
+    pcg_stage_us = statistics.mean(a + (0.0 if w.refine_solver else b)
+                                   for a, b in zip(pcg_us, refine_us))
     achieved_tf = flops_it * iters_per_step / (pcg_stage_us * 1e-6) / 1e12
     hbm_peak, peak_kind, sm_mhz = _peaks()
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -819,7 +824,8 @@ def run_gpu(args, world, rank, local):
                          "bound": "alu", "achieved": achieved_tf, "peak": alu_peak_tf,
                          "unit": "TFLOP/s", "frac": achieved_tf / alu_peak_tf,
                          "traffic": traffic,
-                         "kernel": _pcg_kernel_name(N, n, w.pcg_precision, M, n_sm)
+                         "kernel": _pcg_kernel_name(N, n, w.pcg_precision, M, n_sm,
+                                                    w.refine_solver)
                                    + " (solve + refinement launches)",
                          "peak_basis": "measured in this run: fp32 FMA probe "
                                        "(gato_probe_fp32), faster of scalar and packed form; "

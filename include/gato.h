@@ -112,6 +112,16 @@ extern "C" {
                                       memory; larger sizes are rejected with
                                       GATO_ERR_UNSUPPORTED                       */
 
+/* How refinement corrections are solved (gato_params.refine_solver). */
+#define GATO_REFINE_SOLVER_SAME 0    /* with the main solve's solver: PCG to
+                                        refine_eps, or the direct solve's factors
+                                        (default)                                 */
+#define GATO_REFINE_SOLVER_DIRECT 1  /* with the cyclic-reduction factorisation of
+                                        the same S (bdsv), factored once per call
+                                        when the main solve is PCG: each correction
+                                        is then a substitution, exact for the
+                                        fp32-formed S                             */
+
 /* Linear solver of S lambda = gamma (gato_params.linsys).  The direct solver
  * (bdsv) factors the block-tridiagonal S exactly instead of iterating; the
  * GATO documentation measures it about linear in the horizon N and faster
@@ -172,6 +182,7 @@ typedef struct gato_params {
     int pcg_precision;   /* GATO_PCG_PRECISION_* of the main PCG solve (default
                             GATO_PCG_PRECISION_FP32); refinement corrections are
                             always solved in fp32                                  */
+    int refine_solver;   /* GATO_REFINE_SOLVER_* (default GATO_REFINE_SOLVER_SAME) */
 } gato_params;
 
 /* SQP loop on a linear model (gato_sqp_linear). */
@@ -311,9 +322,11 @@ int gato_linesearch(gato_handle* h, const gato_params* p, const float* Q, const 
  * system is formed from the inputs in compensated fp32 (error-free products
  * and sums, about as accurate as fp64 accumulation), the correction is solved
  * with the same S (PCG to p->refine_eps on the correction system's relative
- * preconditioned residual, or the direct solve's factors), and added to dz
- * and lambda; iters then counts PCG iterations over all solves of the
- * refinement.  The batch runs as gato_set_parts parts of consecutive solves,
+ * preconditioned residual, or the direct solve's factors: those of a direct
+ * main solve, or with p->refine_solver = GATO_REFINE_SOLVER_DIRECT the
+ * cyclic-reduction factorisation formed once after a PCG main solve), and
+ * added to dz and lambda; iters then counts the PCG iterations of every solve
+ * of the call (a direct correction adds none).  The batch runs as gato_set_parts parts of consecutive solves,
  * concurrently on internal streams ordered after the work already on `stream`
  * (which waits for them); the outputs do not depend on the part count.  The
  * parts' workspaces are views into the handle's own allocation (nothing is

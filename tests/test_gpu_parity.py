@@ -16,10 +16,11 @@ Tolerances
               about 20 n u with u = 2^-24 for the sizes here)
   status      0 on every solve of the workloads: workloads 0 and 2 meet their
               stated iteration caps (200, 500) with the double-float PCG
-The workloads use their own refinement setting (one correction solved to
-0.25 for workload 0, 0.1 for workloads 1, 2 and 4, two corrections solved to
-0.01 for workload 3): fp32 formation alone moves dX by 2e-4 to 1e-2, and
-refinement brings the worst dX of each workload's batch to 1e-5 .. 6e-5.
+The workloads use their own refinement setting (one PCG correction solved to
+0.25 for workload 0 and to 0.1 for workload 4; one correction by substitution
+with a direct factorisation of the same S for workloads 1 and 2, two for
+workload 3): fp32 formation alone moves dX by 2e-4 to 1e-2, and refinement
+brings the worst dX of each workload's batch to 1e-7 .. 5e-5.
 """
 import numpy as np
 import pytest
@@ -346,6 +347,27 @@ def test_other_stop_rules(rule):
         # the same stopping quantity: fp32 iterations of the first solve track
         # the fp64 count (the refinement adds a short second solve)
         assert ok and it * 0.9 - 3 <= int(out["iters"][j]) <= it * 1.2 + 150
+
+
+# --------------------------------------------------------------------------
+# refinement corrections by substitution (GATO_REFINE_SOLVER_DIRECT)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("wi,M,steps", [(1, 16, 1), (3, 16, 2), (4, 8, 1)],
+                         ids=["M16_N32_n12", "M16_N16_n36", "M8_N128_n14"])
+def test_direct_refinement_after_pcg(wi, M, steps):
+    """The main solve is PCG; the corrections are solved with the cyclic-
+    reduction factorisation of the same S, formed once: every solve matches
+    the oracle, and iters counts the main solve's PCG iterations only (those
+    of the unrefined call)."""
+    w = WORKLOADS[wi]
+    prob = make_batch(w, M=M)
+    out = solve(prob, params_for(w, refine_solver=gato.GATO_REFINE_SOLVER_DIRECT,
+                                 refine_steps=steps))
+    assert not out["status"].any(), out["status"]
+    check_solution(prob, out, range(M), w.n_alpha, w.beta, w.mu)
+    raw = solve(prob, params_for(w, refine_steps=0))
+    np.testing.assert_array_equal(out["iters"], raw["iters"])
 
 
 # --------------------------------------------------------------------------
@@ -710,7 +732,7 @@ def test_invalid_parameters_rejected():
     prob = make_batch(w, M=1)
     for bad in (dict(merit_threads=48), dict(n_alpha=0), dict(beta=1.0), dict(stop_rule=7),
                 dict(pcg_max_iters=-1), dict(merit_kernel=5), dict(refine_eps=-1.0),
-                dict(pcg_precision=2), dict(pcg_precision=-1)):
+                dict(pcg_precision=2), dict(pcg_precision=-1), dict(refine_solver=2)):
         with pytest.raises(gato.GatoError) as e:
             solve(prob, params_for(w, **bad))
         assert e.value.code == gato.GATO_ERR_INVALID_ARG

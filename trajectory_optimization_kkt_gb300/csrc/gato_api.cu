@@ -86,6 +86,9 @@ bool params_valid(const gato_params* p)
     if (p->bdsv_horizon < 1) return false;
     if (p->pcg_precision != GATO_PCG_PRECISION_FP32 && p->pcg_precision != GATO_PCG_PRECISION_FF)
         return false;
+    if (p->refine_solver != GATO_REFINE_SOLVER_SAME &&
+        p->refine_solver != GATO_REFINE_SOLVER_DIRECT)
+        return false;
     return true;
 }
 
@@ -143,13 +146,22 @@ cudaError_t run_kkt_core(gato_handle* h, const gato_params* p, const float* Q_fo
     if (p->refine_eps > 0.f) pc.pcg_eps = p->refine_eps;
     pc.stop_rule = GATO_STOP_PRECOND;
     pc.pcg_precision = GATO_PCG_PRECISION_FP32;
+    // corrections by substitution with the direct solve's factors: those of the
+    // main solve, or (GATO_REFINE_SOLVER_DIRECT after a PCG solve) the
+    // cyclic-reduction factorisation of the same S, formed once here
+    const bool direct_ref =
+        direct || (p->refine_solver == GATO_REFINE_SOLVER_DIRECT && p->refine_steps > 0);
+    const int ls_ref = direct ? ls : GATO_LINSYS_BDSV;
+    if (err == cudaSuccess && direct_ref && !direct)
+        err = launch_bdsv_factor(h, ls_ref, status, st);
     for (int k = 0; k < p->refine_steps && err == cudaSuccess; ++k) {
         err = launch_kkt_residual(h, Q_form, R, q, r, A, B, e, s0, dX, dU, lambda, st);
         if (err == cudaSuccess)
             err = launch_form_rhs(h, 1, w.q2, w.r2, w.e2, w.s02, (size_t)w.n, st);
         if (err == cudaSuccess) {
-            if (direct)
-                err = launch_bdsv_solve(h, ls, 1, w.dlam, w.ddX, w.ddU, iters, 1, status, st);
+            if (direct_ref)
+                err = launch_bdsv_solve(h, ls_ref, 1, w.dlam, w.ddX, w.ddU, iters, 1, status,
+                                        st);
             else
                 err = launch_pcg_ex(h, &pc, 1, nullptr, w.dlam, w.ddX, w.ddU, iters, 1, status,
                                     st);
@@ -312,6 +324,7 @@ void gato_default_params(gato_params* p)
     p->linsys = GATO_LINSYS_AUTO;
     p->bdsv_horizon = 256;
     p->pcg_precision = GATO_PCG_PRECISION_FP32;
+    p->refine_solver = GATO_REFINE_SOLVER_SAME;
 }
 
 void gato_default_sqp_params(gato_sqp_params* sp)

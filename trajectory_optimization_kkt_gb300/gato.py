@@ -53,6 +53,9 @@ GATO_MERIT_PER_CANDIDATE = 1
 GATO_PCG_PRECISION_FP32 = 0
 GATO_PCG_PRECISION_FF = 1
 
+GATO_REFINE_SOLVER_SAME = 0
+GATO_REFINE_SOLVER_DIRECT = 1
+
 GATO_STOP_RESIDUAL = 0
 GATO_STOP_PRECOND = 1
 GATO_STOP_SCALED = 2
@@ -67,7 +70,8 @@ class GatoParams(ctypes.Structure):
                 ("n_alpha", ctypes.c_int), ("beta", ctypes.c_float), ("mu", ctypes.c_float),
                 ("merit_threads", ctypes.c_int), ("refine_eps", ctypes.c_float),
                 ("merit_kernel", ctypes.c_int), ("linsys", ctypes.c_int),
-                ("bdsv_horizon", ctypes.c_int), ("pcg_precision", ctypes.c_int)]
+                ("bdsv_horizon", ctypes.c_int), ("pcg_precision", ctypes.c_int),
+                ("refine_solver", ctypes.c_int)]
 
 
 class GatoSqpParams(ctypes.Structure):

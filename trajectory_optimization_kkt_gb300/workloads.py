@@ -93,17 +93,22 @@ class Workload:
     beta: float = 2.0
     mu: float = 10.0
     # rounds of KKT iterative refinement (compensated residual), each
-    # correction solved to refine_eps: fp32 formation alone leaves dX 2e-4 to
-    # 1e-2 from the exact solution on these workloads.  The setting is the
-    # cheapest of one round at 0.25 / 0.1 / 0.01, then two rounds at 0.1 /
-    # 0.01, whose worst dX and worst dU error over the workload's whole batch
-    # stay below 3/4 of the 1e-4 parity tolerance
+    # correction solved by PCG to refine_eps or by substitution with a direct
+    # factorisation of the same S (refine_solver): fp32 formation alone leaves
+    # dX 2e-4 to 1e-2 from the exact solution on these workloads.  The setting
+    # is the fastest of one or two rounds, PCG corrections at 0.25 / 0.1 /
+    # 0.01 or direct ones, whose worst dX and worst dU error over the
+    # workload's whole batch stay below 3/4 of the 1e-4 parity tolerance
     refine_steps: int = 1
     refine_eps: float = 0.1
     # arithmetic of the main PCG solve: 0 fp32, 1 double-float (the value of
     # GATO_PCG_PRECISION_FF), for the workloads whose stated iteration cap
     # fp32 PCG cannot meet
     pcg_precision: int = 0
+    # how the refinement corrections are solved: 0 with the main solve's
+    # solver, 1 by substitution with a direct factorisation of the same S
+    # (the value of GATO_REFINE_SOLVER_DIRECT)
+    refine_solver: int = 0
 
     def solver_settings(self) -> Dict[str, float]:
         """The gato_params fields this workload sets (keyword arguments of
@@ -111,7 +116,7 @@ class Workload:
         return dict(pcg_eps=self.pcg_eps, pcg_max_iters=self.pcg_max_iters,
                     n_alpha=self.n_alpha, beta=self.beta, mu=self.mu,
                     refine_steps=self.refine_steps, refine_eps=self.refine_eps,
-                    pcg_precision=self.pcg_precision)
+                    pcg_precision=self.pcg_precision, refine_solver=self.refine_solver)
 
     def with_batch(self, M: int, N: int | None = None) -> "Workload":
         return dataclasses.replace(self, M=M, N=self.N if N is None else N)
@@ -121,18 +126,19 @@ class Workload:
 # 180 and up to 487 iterations there, fp32 PCG 227 and up to 504, so these two
 # run the main solve in double-float arithmetic (about 48 bits: 186 and up to
 # 491).  The others state only eps = 1e-6; their cap is set high enough for
-# fp32 PCG to reach it.  Refinement by the rule above: 0.25 for workload 0
-# (dX 3.3e-5), 0.1 for workloads 1, 2 and 4 (5.5e-5, 4.0e-5, 4.6e-5), two
-# rounds at 0.01 for workload 3 (diagonal scaling over four decades: one
-# round leaves dX at 5.6e-4, two at 0.1 at 5.0e-4).
+# fp32 PCG to reach it.  Refinement by the rule above: one PCG correction at
+# 0.25 for workload 0 (dX 3.3e-5) and at 0.1 for workload 4 (4.6e-5); one
+# direct correction for workloads 1 and 2 (about 1e-7); two direct ones for
+# workload 3 (diagonal scaling over four decades: one leaves dX at 8.4e-5,
+# two at 3e-6).
 WORKLOADS = [
     Workload(0, "M1_N16_n14_m7", 1, 16, 14, 7, pcg_max_iters=200, refine_eps=0.25,
              pcg_precision=1),
-    Workload(1, "M16_N32_n12_m6", 16, 32, 12, 6, pcg_max_iters=1000),
+    Workload(1, "M16_N32_n12_m6", 16, 32, 12, 6, pcg_max_iters=1000, refine_solver=1),
     Workload(2, "M64_N64_n14_m7_A05_QN10", 64, 64, 14, 7, a_sigma=0.05,
-             terminal_scale=10.0, pcg_max_iters=500, pcg_precision=1),
+             terminal_scale=10.0, pcg_max_iters=500, pcg_precision=1, refine_solver=1),
     Workload(3, "M128_N16_n36_m12_logscaled", 128, 16, 36, 12, b_sigma=0.05,
-             log_scale=True, pcg_max_iters=4000, refine_steps=2, refine_eps=0.01),
+             log_scale=True, pcg_max_iters=4000, refine_steps=2, refine_solver=1),
     Workload(4, "M256_N128_n14_m7", 256, 128, 14, 7, pcg_max_iters=1000),
 ]
 
