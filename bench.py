@@ -37,8 +37,8 @@ WORKLOAD_INDEX = 4  # M=256, N=128, n=14, m=7
 # solve launch at this workload, from an ncu capture; valid only for the
 # kernel source it was taken on (sha256 prefix of csrc/pcg.cu), null
 # otherwise.  Captured on 152 solves (one block per SM) and scaled
-# by the solves processed to the 256-solve launch (90.12 MB x 256 / 152).
-PCG_TRAFFIC = {"pcg_sha": "c31b70593b9ae9e0", "bytes_per_launch": 151774909}
+# by the solves processed to the 256-solve launch (89.91 MB x 256 / 152).
+PCG_TRAFFIC = {"pcg_sha": "1f8d5864afd6735f", "bytes_per_launch": 151428258}
 
 FP32_LANES_PER_SM = 128  # FFMA lanes per SM (4 sub-partitions x 32)
 
@@ -46,13 +46,15 @@ FP32_LANES_PER_SM = 128  # FFMA lanes per SM (4 sub-partitions x 32)
 LINSYS = {"pcg": 1, "bdsv": 2, "bdsv_chrono": 3}
 
 
-def launches_per_solve(linsys, refine_steps):
+def launches_per_solve(linsys, refine_steps, refine_solver=0):
     """Kernel launches of one gato_solve_kkt call: 3 formation + 1 right-hand
     side + the linear solve (PCG: 1; direct: factor + substitution) + 1 fused
     merit, and per refinement round 1 residual + 1 right-hand side + 1 solve
-    (PCG, or the direct substitution) + 1 accumulate."""
+    (PCG, or the direct substitution) + 1 accumulate; direct corrections after
+    a PCG solve add the factorisation once."""
     solve = 1 if linsys == "pcg" else 2
-    return 5 + solve + 4 * refine_steps
+    factor = 1 if (linsys == "pcg" and refine_solver and refine_steps) else 0
+    return 5 + solve + 4 * refine_steps + factor
 
 
 def _src_sha(*paths):
@@ -649,7 +651,7 @@ def run_gpu(args, world, rank, local):
     p = gato.default_params(**w.solver_settings(), linsys=LINSYS[args.linsys])
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    launches_per_step = launches_per_solve(args.linsys, w.refine_steps)
+    launches_per_step = launches_per_solve(args.linsys, w.refine_steps, w.refine_solver)
 
     def step():
         out["status"].zero_()
