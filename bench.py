@@ -304,6 +304,7 @@ def _time_solver(torch, s, p, d, out, steps, flush, stream):
     s.set_timing(False)
     s.set_parts(0)
     bad = int((out["status"] != 0).sum())
+    _time_solver.last_stats = st
     return (statistics.mean(ms), {k: statistics.mean(v) for k, v in stages.items()},
             iters / steps, bad)
 
@@ -397,28 +398,22 @@ def _ff_kernel_name(M, N, n, n_sm):
     return "k_pcg_ff"
 
 
-def _pcg_kernel_name(N, n, precision=0, M=None, n_sm=152, refine_solver=0):
-    """The PCG kernel GATO_PCG_AUTO picks for these sizes (the rules of
-    launch_pcg_ex and launch_pcg_rows: the register-row kernel's rows per
-    thread keep its two row tiles within 216 floats, and its block within
-    the registers, at most 256 threads with more than one row per thread);
-    the double-float kernel for the main solve when that precision is set
-    (the refinement's corrections then run in the fp32 kernel named after
-    the plus sign, unless they are direct)."""
-    if precision:
-        main = _ff_kernel_name(M or 1, N, n, n_sm)
-        return main if refine_solver else main + " + " + _pcg_kernel_name(N, n)
-    if 7 <= n <= 16:
-        return "k_pcg_wide" if N <= 128 else ("k_pcg_cluster" if N <= 512 else "k_pcg_generic")
-    if 16 < n <= 64:
-        NP = next(p for p in (20, 24, 28, 32, 36, 40, 48, 56, 64) if n <= p)
-        R = max(1, 216 // (2 * NP))
-        raw = 65536 // (2 * R * NP + 56) // 32 * 32
-        limit = min(256, raw) if R > 1 else min(1024, raw)
-        T = max(64, (N * -(-n // R) + 31) // 32 * 32)
-        if T <= limit:
-            return "k_pcg_rows"
-    return "k_pcg_generic"
+KERNEL_NAMES = {gato.GATO_PCG_GENERIC: "k_pcg_generic", gato.GATO_PCG_WIDE: "k_pcg_wide",
+                gato.GATO_PCG_TILE: "k_pcg_tile", gato.GATO_PCG_ROWS: "k_pcg_rows",
+                gato.GATO_PCG_QUAD: "k_pcg_quad", gato.GATO_PCG_CLUSTER: "k_pcg_cluster",
+                gato.GATO_PCG_DOUBLE_FLOAT: "k_pcg_ff"}
+
+
+def _pcg_kernel_label(st, M, N, n, n_sm):
+    """The PCG kernels a call ran, as the library reports them in its stats
+    (gato_stats.pcg_kernel, refine_kernel): the main solve's, then, after a
+    plus sign, the refinement corrections' when they ran another PCG kernel;
+    the double-float kernel's cluster form by launch_pcg_ff's rule."""
+    main = KERNEL_NAMES.get(st.pcg_kernel, "none")
+    if st.pcg_kernel == gato.GATO_PCG_DOUBLE_FLOAT:
+        main = _ff_kernel_name(M, N, n, n_sm)
+    ref = KERNEL_NAMES.get(st.refine_kernel)
+    return main if ref is None or ref == main else main + " + " + ref
 
 
 def run_workloads(args, local):
@@ -458,9 +453,8 @@ def run_workloads(args, local):
         merit_bytes = 4 * M * (N * n * n + K * (m * m + n * n + n * m) + N * n + K * m + K * n
                                + n + N * n + K * m + (w.n_alpha + 1) + 1)
         merit_gbs = merit_bytes / (stages["merit"] * 1e-6) / 1e9
-        pcg_kernel = _pcg_kernel_name(N, n, w.pcg_precision, M,
-                                      torch.cuda.get_device_properties(dev).multi_processor_count,
-                                      w.refine_solver)
+        pcg_kernel = _pcg_kernel_label(_time_solver.last_stats, M, N, n,
+                                       torch.cuda.get_device_properties(dev).multi_processor_count)
         row = {"workload": w.name, "M": M, "N": N, "n": n, "m": m, "parts": parts,
                "solves_per_s": M / (ms / 1000.0), "ms_per_call": ms,
                "pcg_iters_per_sec": iters / (ms / 1000.0), "pcg_iters_per_solve": iters / M,
@@ -697,6 +691,7 @@ def run_gpu(args, world, rank, local):
         flush.fill_(float(k))
         step()
         st = s.get_stats()  # synchronises on this step's last event
+        stage_stats = st
         pcg_us.append(st.pcg_us)
         refine_us.append(max(st.refine_us, 0.0))
         form_us.append(st.form_us)
@@ -826,8 +821,7 @@ def run_gpu(args, world, rank, local):
                          "bound": "alu", "achieved": achieved_tf, "peak": alu_peak_tf,
                          "unit": "TFLOP/s", "frac": achieved_tf / alu_peak_tf,
                          "traffic": traffic,
-                         "kernel": _pcg_kernel_name(N, n, w.pcg_precision, M, n_sm,
-                                                    w.refine_solver)
+                         "kernel": _pcg_kernel_label(stage_stats, M, N, n, n_sm)
                                    + " (solve + refinement launches)",
                          "peak_basis": "measured in this run: fp32 FMA probe "
                                        "(gato_probe_fp32), faster of scalar and packed form; "

@@ -94,6 +94,21 @@ extern "C" {
                                       two coupling blocks around a knot per
                                       thread) for any n <= 64 where its block
                                       fits, else as GATO_PCG_AUTO                 */
+#define GATO_PCG_QUAD 5            /* the four-thread kernel with row quarters
+                                      over all n columns (7 <= n <= 16,
+                                      N <= 128; column sums reduced by warp
+                                      shuffles within the quad) where it
+                                      applies, else as GATO_PCG_AUTO.  AUTO
+                                      takes it where the wide-tile kernel would
+                                      leave each SM with at most four working
+                                      warps (2N threads per solve, as many
+                                      solves per SM as the batch and the
+                                      occupancy give)                             */
+/* reported in gato_stats.pcg_kernel only (not choices of gato_set_pcg_kernel) */
+#define GATO_PCG_CLUSTER 6         /* the wide-tile iteration over a cluster of
+                                      2 or 4 CTAs per solve (128 < N <= 512)      */
+#define GATO_PCG_DOUBLE_FLOAT 7    /* the double-float kernel (pcg_precision FF),
+                                      one CTA or a cluster of two per solve       */
 
 /* Arithmetic of the main PCG solve (gato_params.pcg_precision).  The
  * iteration count of CG in finite precision grows with the rounding unit:
@@ -207,6 +222,13 @@ typedef struct gato_stats {
     float merit_us;      /* pcg_us: the linear solve (PCG, or the direct solve's  */
     float total_us;      /* factorisation and substitution); refine_us: every
                             refinement round (residual, right-hand side, solve).  */
+    int pcg_kernel;      /* the kernel the last call's main PCG solve ran: a
+                            GATO_PCG_* value other than AUTO (WIDE, TILE, QUAD,
+                            ROWS, GENERIC, CLUSTER or DOUBLE_FLOAT); 0 when the
+                            call ran no PCG solve.  Filled with or without
+                            timing.                                              */
+    int refine_kernel;   /* the same for the refinement corrections' PCG solves
+                            (0 when they were direct or did not run)             */
 } gato_stats;
 
 typedef struct gato_handle gato_handle;
@@ -235,7 +257,7 @@ int gato_set_timing(gato_handle* h, int on);
 int gato_get_stats(gato_handle* h, gato_stats* out);
 
 /* Chooses the PCG kernel (GATO_PCG_AUTO, GATO_PCG_GENERIC, GATO_PCG_WIDE,
- * GATO_PCG_TILE or GATO_PCG_ROWS) for later calls.
+ * GATO_PCG_TILE, GATO_PCG_ROWS or GATO_PCG_QUAD) for later calls.
  * Both give the same PCG iterates up to rounding; the generic kernel covers
  * every supported size.  Errors: INVALID_ARG. */
 int gato_set_pcg_kernel(gato_handle* h, int kind);

@@ -210,7 +210,11 @@ WIDE = [c for c in CUSTOM if 7 <= c[3] <= 16 and c[2] <= 128] + [
     ("N33_n15_m4", 2, 33, 15, 4, 1), ("N5_n8_m3", 3, 5, 8, 3, 2)]
 
 
-@pytest.mark.parametrize("kind", [gato.GATO_PCG_WIDE, gato.GATO_PCG_TILE], ids=["wide", "tile"])
+TILED_KINDS = [gato.GATO_PCG_WIDE, gato.GATO_PCG_TILE, gato.GATO_PCG_QUAD]
+TILED_IDS = ["wide", "tile", "quad"]
+
+
+@pytest.mark.parametrize("kind", TILED_KINDS, ids=TILED_IDS)
 @pytest.mark.parametrize("name,M,N,n,m,refine", WIDE, ids=[c[0] for c in WIDE])
 def test_tiled_kernels_custom_sizes(name, M, N, n, m, refine, kind):
     prob = random_lq(M, N, n, m, seed=600 + N + n)
@@ -218,6 +222,108 @@ def test_tiled_kernels_custom_sizes(name, M, N, n, m, refine, kind):
     out = solve(prob, p, kind)
     assert not out["status"].any(), out["status"]
     check_solution(prob, out, range(M))
+
+
+# the quad kernel's remaining row counts (n = 10, 11: three rows per lane,
+# ragged last lanes), its largest block (N = 128: 512 threads), and more
+# solves than resident blocks (each block takes several from the queue)
+QUAD = [("N21_n10_m4", 3, 21, 10, 4, 1), ("N17_n11_m5", 3, 17, 11, 5, 1),
+        ("N128_n14_m7_max", 2, 128, 14, 7, 1), ("N120_n16_m8", 2, 120, 16, 8, 1),
+        ("N8_n14_m7_M400", 400, 8, 14, 7, 1)]
+
+
+@pytest.mark.parametrize("name,M,N,n,m,refine", QUAD, ids=[c[0] for c in QUAD])
+def test_quad_kernel_sizes(name, M, N, n, m, refine):
+    prob = random_lq(M, N, n, m, seed=700 + N + n)
+    p = gato.default_params(pcg_max_iters=3000, refine_steps=refine)
+    out = solve(prob, p, gato.GATO_PCG_QUAD)
+    assert not out["status"].any(), out["status"]
+    check = range(M) if M <= 8 else [0, 1, M // 2, M - 2, M - 1]
+    check_solution(prob, out, check)
+    # the wide kernel runs the same iteration in another summation order; in
+    # fp32 the iteration at which the residual crosses eps moves with the
+    # rounding, by a few percent on the average and up to about 10 % on the
+    # rare solve of a large batch
+    ref = solve(prob, p, gato.GATO_PCG_WIDE)
+    diff = np.abs(out["iters"] - ref["iters"])
+    assert diff.mean() <= 0.02 * ref["iters"].mean() + 1
+    assert diff.max() <= 0.1 * ref["iters"].max() + 2
+
+
+@pytest.mark.parametrize("rule", [gato.GATO_STOP_RESIDUAL, gato.GATO_STOP_PRECOND,
+                                  gato.GATO_STOP_SCALED], ids=["residual", "precond", "scaled"])
+def test_quad_kernel_stopping_rules(rule):
+    """Each stopping rule stops the quad kernel where it stops the wide
+    kernel (the same iteration in another summation order), with lambda as
+    close to the fp64 direct solution (workload 4's sizes, unrefined)."""
+    w = WORKLOADS[4]
+    prob = make_batch(w, M=3)
+    p = params_for(w, stop_rule=rule, refine_steps=0)
+    a = solve(prob, p, gato.GATO_PCG_QUAD)
+    b = solve(prob, p, gato.GATO_PCG_WIDE)
+    assert not a["status"].any() and not b["status"].any()
+    for j in range(3):
+        lam = oracle.direct_solve(oracle.solve_one(prob, j))[2]
+        assert rel(a["lam"][j], lam) <= 2 * rel(b["lam"][j], lam) + 1e-5
+    assert np.abs(a["iters"] - b["iters"]).max() <= 0.05 * b["iters"].max() + 2
+
+
+def ran_kernels(prob, p, kernel=gato.GATO_PCG_AUTO, parts=0):
+    """gato_stats.pcg_kernel and refine_kernel after one gato_solve_kkt."""
+    M, N, n = prob["Q"].shape[:3]
+    m = prob["B"].shape[-1]
+    d = gato.to_device(prob)
+    with gato.Solver(M, N, n, m) as s:
+        s.set_pcg_kernel(kernel)
+        s.set_parts(parts)
+        out = s.outputs(p.n_alpha)
+        s.solve_kkt(p, d, out["dX"], out["dU"], out["lam"], out["iters"], out["merit"],
+                    out["best"], out["status"])
+        torch.cuda.synchronize()
+        st = s.get_stats()
+        assert not out["status"].cpu().numpy().any()
+        return st.pcg_kernel, st.refine_kernel
+
+
+Q, W, C, FF = gato.GATO_PCG_QUAD, gato.GATO_PCG_WIDE, gato.GATO_PCG_CLUSTER, \
+    gato.GATO_PCG_DOUBLE_FLOAT
+# (name, M, N, n, m, settings, expected main kernel, expected correction kernel);
+# the wide kernel's working warps per SM are 2N/32 per solve times the solves
+# an SM holds (the whole batch's, by the SM count, at most its occupancy)
+AUTO_CHOICE = [
+    ("M16_N32_n12_quad", 16, 32, 12, 6, {}, Q, Q),        # 2 warps per SM
+    ("M16_N64_n14_quad", 16, 64, 14, 7, {}, Q, Q),        # 4
+    ("M16_N96_n14_wide", 16, 96, 14, 7, {}, W, W),        # 6
+    ("M256_N128_n14_wide", 256, 128, 14, 7, {}, W, W),    # 8, in four parts
+    # four parts of 80: one part alone would leave 2 warps per SM, the whole
+    # batch (3 solves per SM) leaves 6
+    ("M320_N32_n14_parts", 320, 32, 14, 7, {}, W, W),
+    ("M2_N200_n14_cluster", 2, 200, 14, 7, {}, C, C),
+    ("M2_N16_n36_rows", 2, 16, 36, 12, {}, gato.GATO_PCG_ROWS, gato.GATO_PCG_ROWS),
+    ("M2_N16_n14_ff", 2, 16, 14, 7, {"pcg_precision": 1, "refine_eps": 0.25}, FF, Q),
+    ("M2_N32_n12_direct_corr", 2, 32, 12, 6, {"refine_solver": 1}, Q, 0),
+    ("M2_N16_n14_no_refine", 2, 16, 14, 7, {"refine_steps": 0}, Q, 0),
+]
+
+
+@pytest.mark.parametrize("name,M,N,n,m,kw,main,corr", AUTO_CHOICE,
+                         ids=[c[0] for c in AUTO_CHOICE])
+def test_automatic_kernel_choice_is_reported(name, M, N, n, m, kw, main, corr):
+    if M > 16 and torch.cuda.get_device_properties(0).multi_processor_count < 128:
+        pytest.skip("the expected choice assumes at least 128 SMs")
+    prob = random_lq(M, N, n, m, seed=760 + N + n)
+    p = gato.default_params(pcg_max_iters=3000, **{"refine_steps": 1, **kw})
+    assert ran_kernels(prob, p) == (main, corr)
+
+
+def test_chosen_kernels_are_reported():
+    prob = random_lq(2, 16, 14, 7, seed=771)
+    p = gato.default_params(pcg_max_iters=3000, refine_steps=1)
+    for kind in (gato.GATO_PCG_GENERIC, gato.GATO_PCG_WIDE, gato.GATO_PCG_TILE,
+                 gato.GATO_PCG_QUAD, gato.GATO_PCG_ROWS):
+        assert ran_kernels(prob, p, kind) == (kind, kind)
+    # a direct solve runs no PCG kernel
+    assert ran_kernels(prob, gato.default_params(linsys=gato.GATO_LINSYS_BDSV)) == (0, 0)
 
 
 @pytest.mark.parametrize("name,M,N,n,m,refine", CUSTOM, ids=[c[0] for c in CUSTOM])
@@ -312,7 +418,7 @@ def test_rows_kernel_chosen_for_small_states():
     check_solution(prob, out, range(4), w.n_alpha, w.beta, w.mu)
 
 
-@pytest.mark.parametrize("kind", [gato.GATO_PCG_WIDE, gato.GATO_PCG_TILE], ids=["wide", "tile"])
+@pytest.mark.parametrize("kind", TILED_KINDS, ids=TILED_IDS)
 @pytest.mark.parametrize("w", [WORKLOADS[1], WORKLOADS[4]], ids=lambda w: w.name)
 def test_tiled_and_generic_kernels_agree(w, kind):
     prob = make_batch(w, M=4)
@@ -644,7 +750,8 @@ def test_apply_step():
 
 
 WARM = [("n12_auto", 12, gato.GATO_PCG_AUTO), ("n12_generic", 12, gato.GATO_PCG_GENERIC),
-        ("n12_tile", 12, gato.GATO_PCG_TILE), ("n36_rows", 36, gato.GATO_PCG_AUTO),
+        ("n12_tile", 12, gato.GATO_PCG_TILE), ("n12_quad", 12, gato.GATO_PCG_QUAD),
+        ("n36_rows", 36, gato.GATO_PCG_AUTO),
         ("n36_generic", 36, gato.GATO_PCG_GENERIC)]
 
 

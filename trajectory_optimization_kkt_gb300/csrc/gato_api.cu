@@ -124,6 +124,7 @@ cudaError_t run_kkt_core(gato_handle* h, const gato_params* p, const float* Q_fo
 {
     Work& w = h->w;
     w.status = status;
+    h->pcg_ran = h->refine_ran = 0;
     const int ls = linsys_for(p, w.N);
     const bool direct = ls != GATO_LINSYS_PCG;
     cudaError_t err = launch_form_matrices(h, Q_form, R, A, B, status, st);
@@ -211,6 +212,7 @@ void record(gato_handle* h, int i, cudaStream_t st)
 
 void begin_timing(gato_handle* h, cudaStream_t st)
 {
+    h->pcg_ran = h->refine_ran = 0;
     if (!h->timing) return;
     for (int i = 0; i < 5; ++i) h->ev_used[i] = 0;
     record(h, 0, st);
@@ -404,7 +406,7 @@ int gato_set_timing(gato_handle* h, int on)
 
 int gato_set_pcg_kernel(gato_handle* h, int kind)
 {
-    if (!h || kind < GATO_PCG_AUTO || kind > GATO_PCG_ROWS) return GATO_ERR_INVALID_ARG;
+    if (!h || kind < GATO_PCG_AUTO || kind > GATO_PCG_QUAD) return GATO_ERR_INVALID_ARG;
     h->pcg_kernel = kind;
     return GATO_OK;
 }
@@ -429,6 +431,8 @@ int gato_get_stats(gato_handle* h, gato_stats* out)
     if (!h || !out) return GATO_ERR_INVALID_ARG;
     gato_stats s;
     s.form_us = s.pcg_us = s.refine_us = s.merit_us = s.total_us = -1.f;
+    s.pcg_kernel = h->pcg_ran;
+    s.refine_kernel = h->refine_ran;
     if (h->timing && h->ev_used[0]) {
         int last = 0;
         for (int i = 4; i > 0; --i)

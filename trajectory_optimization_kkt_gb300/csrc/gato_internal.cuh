@@ -109,6 +109,10 @@ struct gato_handle {
     size_t bytes;
     int timing;
     int pcg_kernel;         // GATO_PCG_* selected by gato_set_pcg_kernel
+    int pcg_ran;            // GATO_PCG_* kernel of the last main PCG launch (0: none)
+    int refine_ran;         // ... and of the last correction PCG launch
+    int batch_M;            // solves running at the same time as this handle's: the
+                            // whole batch when the handle is one part of it (0: w.M)
     int bdsv_kernel;        // GATO_BDSV_KERNEL_* selected by gato_set_bdsv_kernel
     int force_smem_form;    // GATO_FORM_SHARED selected by gato_set_form_kernel
     int phi_pending;        // the last formation left the explicit Phi^-1 blocks unformed

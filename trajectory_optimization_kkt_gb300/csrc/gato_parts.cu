@@ -80,6 +80,7 @@ void partition(gato_handle* h, int k, bool small_first)
         sh.bytes = carve_workspace(sh.w, cnt, w.N, w.n, w.m, nullptr);
         carve_workspace(sh.w, cnt, w.N, w.n, w.m, (float*)sh.base);
         sh.parts = 1;
+        sh.batch_M = w.M;  // the parts run concurrently
         off += align256(sh.bytes);
     }
     pp->count_parts = k;
@@ -202,6 +203,7 @@ int run_parts(gato_handle* h, const gato_params* p, const float* Q, const float*
         sh->bdsv_kernel = h->bdsv_kernel;
         sh->force_smem_form = h->force_smem_form;
         sh->timing = 0;
+        sh->pcg_ran = sh->refine_ran = 0;
         const size_t f0 = (size_t)pp->first[c], cnt = (size_t)pp->count[c];
         // the part's slice of an array with `per` elements of `es` bytes per
         // solve: in the staging (host entry) or in the caller's array
@@ -255,6 +257,11 @@ int run_parts(gato_handle* h, const gato_params* p, const float* Q, const float*
         // the caller's stream waits for whatever this part enqueued
         if (cudaEventRecord(pp->done[c], st) == cudaSuccess)
             cudaStreamWaitEvent(user, pp->done[c], 0);
+    }
+    // every part takes the same kernel (the choice counts the whole batch)
+    if (err == cudaSuccess) {
+        h->pcg_ran = pp->sub[k - 1].pcg_ran;
+        h->refine_ran = pp->sub[k - 1].refine_ran;
     }
     if (err == cudaErrorInvalidConfiguration) return GATO_ERR_UNSUPPORTED;
     return err == cudaSuccess ? GATO_OK : GATO_ERR_CUDA;

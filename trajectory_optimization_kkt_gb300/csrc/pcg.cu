@@ -1333,9 +1333,65 @@ cudaError_t launch_cluster(K kernel, const PcgArgs& a, int C, int T, size_t smem
 
 }  // namespace
 
-cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const float* lambda0,
-                          float* lambda, float* dX, float* dU, int32_t* iters, int acc_iters,
-                          uint32_t* status, cudaStream_t st)
+namespace {
+
+// blocks of a kernel an SM can hold with T threads and smem bytes of dynamic
+// shared memory (the opt-in above 48 KB set first, as for its launch); 0 on
+// error
+template <typename K>
+int blocks_per_sm(K kernel, int T, size_t smem)
+{
+    int per_sm = 0;
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, T, smem);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return per_sm;
+}
+
+int wide_blocks_per_sm(int H, int T, size_t smem)
+{
+    switch (H) {
+        case 4: return blocks_per_sm(k_pcg_wide<4>, T, smem);
+        case 5: return blocks_per_sm(k_pcg_wide<5>, T, smem);
+        case 6: return blocks_per_sm(k_pcg_wide<6>, T, smem);
+        case 7: return blocks_per_sm(k_pcg_wide<7>, T, smem);
+        case 8: return blocks_per_sm(k_pcg_wide<8>, T, smem);
+        default: return 0;
+    }
+}
+
+// The automatic choice between the wide-tile and the quad kernel: the quad
+// kernel where the wide one would leave each SM at most four working warps
+// (a solve's 2N threads, times the solves an SM holds: those of the whole
+// concurrent batch per SM, at most the wide kernel's occupancy).  There the
+// quad's twice as many warps hide latency that the few wide warps leave
+// exposed (3 to 42 % less time per PCG solve measured for n = 12, 14, 16 and
+// N = 16 .. 64); with eight or more working warps per SM the quad's 1.5 times
+// as many instructions make it up to 13 % slower.
+bool quad_preferred(const gato_handle* h, int H, int Tw, size_t smem_wide)
+{
+    const Work& w = h->w;
+    const int conc = h->batch_M > 0 ? h->batch_M : w.M;
+    int per_sm = (conc + h->num_sms - 1) / h->num_sms;
+    const int occ = wide_blocks_per_sm(H, Tw, smem_wide);
+    if (occ < 1) return false;
+    if (per_sm > occ) per_sm = occ;
+    const int warps_per_solve = (2 * w.N + 31) / 32;
+    return warps_per_solve * per_sm <= 4;
+}
+
+}  // namespace
+
+// launches the PCG kernel for these sizes and parameters; ran gets its
+// GATO_PCG_* value
+static cudaError_t launch_pcg_pick(gato_handle* h, const gato_params* p, int set,
+                                   const float* lambda0, float* lambda, float* dX, float* dU,
+                                   int32_t* iters, int acc_iters, uint32_t* status,
+                                   cudaStream_t st, int& ran)
 {
     const Work& w = h->w;
     PcgArgs a;
@@ -1360,6 +1416,7 @@ cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const f
     if (p->pcg_precision == GATO_PCG_PRECISION_FF) {
         a.nh_smem = 0;
         a.l_smem = 0;
+        ran = GATO_PCG_DOUBLE_FLOAT;
         return launch_pcg_ff(a, limit, h->num_sms, st);
     }
 
@@ -1373,11 +1430,13 @@ cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const f
     // register-row kernel (pcg_rows.cu): the default for 16 < n <= 64 where its
     // block fits, any n <= 64 when chosen; where it does not fit, as AUTO
     if (kind == GATO_PCG_ROWS || (kind == GATO_PCG_AUTO && w.n > 16)) {
+        ran = GATO_PCG_ROWS;
         cudaError_t e = launch_pcg_rows(a, limit, st);
         if (e != cudaErrorInvalidConfiguration) return e;
         kind = GATO_PCG_AUTO;
     }
-    if ((kind == GATO_PCG_AUTO || kind == GATO_PCG_WIDE) && tiled_n && Tw <= 256) {
+    if ((kind == GATO_PCG_AUTO || kind == GATO_PCG_WIDE || kind == GATO_PCG_QUAD) && tiled_n &&
+        Tw <= 256) {
         a.nh_smem = 0;
         a.l_smem = want_l;
         size_t smem = wide_smem_bytes(w, a.l_smem);
@@ -1385,6 +1444,15 @@ cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const f
             a.l_smem = 0;
             smem = wide_smem_bytes(w, 0);
         }
+        // quad kernel (pcg_quad.cu): four threads per coupling block, when
+        // chosen or by the automatic rule above
+        if (kind == GATO_PCG_QUAD ||
+            (kind == GATO_PCG_AUTO && smem <= limit && quad_preferred(h, H, Tw, smem))) {
+            ran = GATO_PCG_QUAD;
+            cudaError_t e = launch_pcg_quad(a, limit, h->num_sms, st);
+            if (e != cudaErrorInvalidConfiguration) return e;
+        }
+        ran = GATO_PCG_WIDE;
         if (smem <= limit) {
             switch (H) {
                 case 4: return launch_persistent(k_pcg_wide<4>, a, Tw, smem, h->num_sms, st);
@@ -1412,6 +1480,7 @@ cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const f
             smem = wide_smem_bytes(w, 0, Nc);
         }
         if (smem <= limit) {
+            ran = GATO_PCG_CLUSTER;
             cudaError_t e = cudaErrorInvalidConfiguration;
             switch (H * 8 + C) {
 #define GATO_CLUSTER_CASE(HH, CC)                                                    \
@@ -1443,6 +1512,7 @@ cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const f
             smem = tile_smem_bytes(w, 0);
         }
         if (smem <= limit) {
+            ran = GATO_PCG_TILE;
             switch (H) {
                 case 4: return launch_persistent(k_pcg_tile<4>, a, T, smem, h->num_sms, st);
                 case 5: return launch_persistent(k_pcg_tile<5>, a, T, smem, h->num_sms, st);
@@ -1467,11 +1537,25 @@ cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const f
         smem = generic_smem_bytes(w, a.nh_smem, a.l_smem);
     }
     if (smem > limit) return cudaErrorInvalidConfiguration;
+    ran = GATO_PCG_GENERIC;
     const int Nn = w.N * w.n;
     T = ((Nn + 1) / 2 + 31) / 32 * 32;
     if (T < 64) T = 64;
     if (T > 512) T = 512;
     return launch_k(k_pcg_generic, a, T, smem, st);
+}
+
+// the kernel is recorded for gato_stats: pcg_kernel for a main solve (set 0),
+// refine_kernel for a correction (set 1)
+cudaError_t launch_pcg_ex(gato_handle* h, const gato_params* p, int set, const float* lambda0,
+                          float* lambda, float* dX, float* dU, int32_t* iters, int acc_iters,
+                          uint32_t* status, cudaStream_t st)
+{
+    int ran = 0;
+    const cudaError_t e = launch_pcg_pick(h, p, set, lambda0, lambda, dX, dU, iters, acc_iters,
+                                          status, st, ran);
+    if (e == cudaSuccess) (set == 0 ? h->pcg_ran : h->refine_ran) = ran;
+    return e;
 }
 
 cudaError_t launch_pcg(gato_handle* h, const gato_params* p, const float* lambda0,

@@ -160,4 +160,9 @@ cudaError_t launch_pcg_rows(const PcgArgs& a, size_t smem_limit, cudaStream_t st
 // runs each solve over a cluster of two CTAs when each keeps enough rows
 cudaError_t launch_pcg_ff(const PcgArgs& a, size_t smem_limit, int num_sms, cudaStream_t st);
 
+// the four-thread quad kernel (pcg_quad.cu): 7 <= n <= 16 and N <= 128 with
+// its shared memory within smem_limit, else cudaErrorInvalidConfiguration
+bool pcg_quad_fits(int N, int n, int rule, size_t smem_limit);
+cudaError_t launch_pcg_quad(const PcgArgs& a, size_t smem_limit, int num_sms, cudaStream_t st);
+
 }  // namespace gato

@@ -30,6 +30,9 @@ GATO_PCG_GENERIC = 1
 GATO_PCG_WIDE = 2
 GATO_PCG_TILE = 3
 GATO_PCG_ROWS = 4
+GATO_PCG_QUAD = 5
+GATO_PCG_CLUSTER = 6  # reported in the stats only
+GATO_PCG_DOUBLE_FLOAT = 7  # reported in the stats only
 GATO_MAX_PARTS = 8
 GATO_MAX_STATE = 64
 GATO_MAX_CONTROL = 64
@@ -83,7 +86,8 @@ class GatoSqpParams(ctypes.Structure):
 class GatoStats(ctypes.Structure):
     _fields_ = [("form_us", ctypes.c_float), ("pcg_us", ctypes.c_float),
                 ("refine_us", ctypes.c_float), ("merit_us", ctypes.c_float),
-                ("total_us", ctypes.c_float)]
+                ("total_us", ctypes.c_float), ("pcg_kernel", ctypes.c_int),
+                ("refine_kernel", ctypes.c_int)]
 
 
 class GatoError(RuntimeError):
