@@ -341,6 +341,63 @@ def run_sweep(args, local):
                                       "status_nonzero_solves": bad}), flush=True)
 
 
+def run_pcg_kernel_sweep(args, local):
+    """PCG-only time of the wide-tile and quad kernels and of the automatic
+    choice, n in {12, 14, 16} x N in {16, 32, 64, 128} x M in {16, 152, 256,
+    1024}: gato_pcg_solve after one gato_form_schur (stop rule 0, eps 1e-6),
+    L2 flushed before each launch, the median of 6 launches after 2; the
+    batch is 16 generated solves (workload 4's generator at these sizes)
+    repeated to M, so every solve of a cell takes the iterations of one of
+    16.  One JSON line per cell, with the kernel each call ran as the
+    library reports it."""
+    import dataclasses
+
+    import torch
+
+    from trajectory_optimization_kkt_gb300 import _build, gato
+    from trajectory_optimization_kkt_gb300.workloads import WORKLOADS, make_batch
+    torch.cuda.set_device(local)
+    _build.build()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    kinds = {"wide": gato.GATO_PCG_WIDE, "quad": gato.GATO_PCG_QUAD, "auto": gato.GATO_PCG_AUTO}
+    base = WORKLOADS[WORKLOAD_INDEX]
+    for n in (12, 14, 16):
+        for N in (16, 32, 64, 128):
+            w = dataclasses.replace(base, n=n, m=n // 2, N=N)
+            one = make_batch(w, M=16)
+            for M in (16, 152, 256, 1024):
+                prob = {k: np.ascontiguousarray(np.concatenate([v] * (M // 16))[:M])
+                        for k, v in one.items()}
+                d = {k: torch.from_numpy(v).to(dev) for k, v in prob.items()}
+                p = gato.default_params(pcg_eps=1e-6, pcg_max_iters=2000)
+                row = {"sweep": "pcg_kernels", "n": n, "N": N, "M": M}
+                with gato.Solver(M, N, n, n // 2) as s:
+                    out = s.outputs(p.n_alpha)
+                    s.form_schur(d, out["status"], stream)
+                    for name, kind in kinds.items():
+                        s.set_pcg_kernel(kind)
+                        ts = []
+                        for k in range(8):
+                            flush.fill_(float(k))
+                            a = torch.cuda.Event(enable_timing=True)
+                            b = torch.cuda.Event(enable_timing=True)
+                            a.record(stream)
+                            s.pcg_solve(p, out["lam"], out["dX"], out["dU"], out["iters"],
+                                        out["status"], stream=stream)
+                            b.record(stream)
+                            b.synchronize()
+                            if k >= 2:
+                                ts.append(a.elapsed_time(b))
+                        row[name] = {"us": 1000.0 * statistics.median(ts),
+                                     "iters_per_solve": float(out["iters"].float().mean()),
+                                     "ran": _kernel_names().get(s.get_stats().pcg_kernel),
+                                     "status_nonzero_solves": int((out["status"] != 0).sum())}
+                row["quad_over_wide"] = row["quad"]["us"] / row["wide"]["us"]
+                print(json.dumps(row), flush=True)
+
+
 def run_throughput_sweep(args, local):
     """The benchmark workload's throughput sweep: M in {1, 8, 16, 64, 256} x
     N in {16, 32, 64, 128} at n = 14, m = 7, the default PCG path; solves/s
@@ -374,7 +431,10 @@ def run_throughput_sweep(args, local):
                 print(json.dumps({"sweep": "throughput", "M": M, "N": N, "n": w.n, "m": w.m,
                                   "parts": s.get_parts(), "solves_per_s": M / (ms / 1000.0),
                                   "pcg_us_per_iteration": pcg_us_it,
-                                  "pcg_warps_per_sm": max(2, (2 * N + 31) // 32),
+                                  "pcg_kernel": _pcg_kernel_label(
+                                      _time_solver.last_stats, M, N, w.n,
+                                      torch.cuda.get_device_properties(dev)
+                                      .multi_processor_count),
                                   "ms_per_step": ms,
                                   "pcg_iters_per_sec": iters / (ms / 1000.0),
                                   "pcg_iters_per_solve": iters / M,
@@ -398,10 +458,13 @@ def _ff_kernel_name(M, N, n, n_sm):
     return "k_pcg_ff"
 
 
-KERNEL_NAMES = {gato.GATO_PCG_GENERIC: "k_pcg_generic", gato.GATO_PCG_WIDE: "k_pcg_wide",
-                gato.GATO_PCG_TILE: "k_pcg_tile", gato.GATO_PCG_ROWS: "k_pcg_rows",
-                gato.GATO_PCG_QUAD: "k_pcg_quad", gato.GATO_PCG_CLUSTER: "k_pcg_cluster",
-                gato.GATO_PCG_DOUBLE_FLOAT: "k_pcg_ff"}
+def _kernel_names():
+    """Kernel names of the GATO_PCG_* values gato_stats reports."""
+    from trajectory_optimization_kkt_gb300 import gato
+    return {gato.GATO_PCG_GENERIC: "k_pcg_generic", gato.GATO_PCG_WIDE: "k_pcg_wide",
+            gato.GATO_PCG_TILE: "k_pcg_tile", gato.GATO_PCG_ROWS: "k_pcg_rows",
+            gato.GATO_PCG_QUAD: "k_pcg_quad", gato.GATO_PCG_CLUSTER: "k_pcg_cluster",
+            gato.GATO_PCG_DOUBLE_FLOAT: "k_pcg_ff"}
 
 
 def _pcg_kernel_label(st, M, N, n, n_sm):
@@ -409,10 +472,12 @@ def _pcg_kernel_label(st, M, N, n, n_sm):
     (gato_stats.pcg_kernel, refine_kernel): the main solve's, then, after a
     plus sign, the refinement corrections' when they ran another PCG kernel;
     the double-float kernel's cluster form by launch_pcg_ff's rule."""
-    main = KERNEL_NAMES.get(st.pcg_kernel, "none")
+    from trajectory_optimization_kkt_gb300 import gato
+    names = _kernel_names()
+    main = names.get(st.pcg_kernel, "none")
     if st.pcg_kernel == gato.GATO_PCG_DOUBLE_FLOAT:
         main = _ff_kernel_name(M, N, n, n_sm)
-    ref = KERNEL_NAMES.get(st.refine_kernel)
+    ref = names.get(st.refine_kernel)
     return main if ref is None or ref == main else main + " + " + ref
 
 
@@ -883,6 +948,8 @@ def main():
                     help="skip timing the same step through the direct solvers")
     ap.add_argument("--sweep", action="store_true",
                     help="horizon x batch sweep of the three linear solvers instead")
+    ap.add_argument("--pcg-kernel-sweep", action="store_true",
+                    help="PCG-only time of the wide and quad kernels and AUTO over n x N x M")
     ap.add_argument("--throughput-sweep", action="store_true",
                     help="the workload's M x N throughput sweep (solves/s, merit us) instead")
     ap.add_argument("--workloads", action="store_true",
@@ -906,6 +973,8 @@ def main():
         run_reference(args, world, rank)
     elif args.sweep:
         run_sweep(args, local)
+    elif args.pcg_kernel_sweep:
+        run_pcg_kernel_sweep(args, local)
     elif args.throughput_sweep:
         run_throughput_sweep(args, local)
     elif args.workloads:

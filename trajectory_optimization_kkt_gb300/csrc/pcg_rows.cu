@@ -34,42 +34,43 @@ namespace {
 // rows per thread: the two tiles (2 R NP floats) within 216 registers
 constexpr int rows_for(int NP) { return 216 / (2 * NP) > 0 ? 216 / (2 * NP) : 1; }
 
-// threads per block the registers allow: 64K registers over the tiles plus
-// about 56 for the rest, in whole warps; with more than one row per thread
-// at most 256 threads, so that no SM sub-partition holds more than two warps
-// and a thread may use 255 registers (fewer, fuller threads measured faster
-// than more threads with spilled tiles)
-constexpr int max_threads_raw(int NP) { return (65536 / (2 * rows_for(NP) * NP + 56)) / 32 * 32; }
-constexpr int max_threads_for(int NP)
+// threads per block the registers allow with R rows per thread: 64K
+// registers over the tiles plus about 56 for the rest, in whole warps; with
+// more than one row per thread at most 256 threads, so that no SM
+// sub-partition holds more than two warps and a thread may use 255 registers
+// (fewer, fuller threads measured faster than more threads with spilled
+// tiles)
+constexpr int max_threads_raw(int NP, int R) { return (65536 / (2 * R * NP + 56)) / 32 * 32; }
+constexpr int max_threads_for(int NP, int R)
 {
-    return rows_for(NP) > 1 ? (max_threads_raw(NP) > 256 ? 256 : max_threads_raw(NP))
-                            : (max_threads_raw(NP) > 1024 ? 1024 : max_threads_raw(NP));
+    return R > 1 ? (max_threads_raw(NP, R) > 256 ? 256 : max_threads_raw(NP, R))
+                 : (max_threads_raw(NP, R) > 1024 ? 1024 : max_threads_raw(NP, R));
 }
 
 // The registers per thread the launch bound leaves: 64K over the warps of
 // the fullest SM sub-partition (a quarter of the block's warps, rounded up),
 // in steps of 8.
-constexpr int reg_cap_for(int NP)
+constexpr int reg_cap_for(int NP, int R)
 {
-    return (16384 / (((max_threads_for(NP) / 32 + 3) / 4) * 32)) / 8 * 8 > 255
+    return (16384 / (((max_threads_for(NP, R) / 32 + 3) / 4) * 32)) / 8 * 8 > 255
                ? 255
-               : (16384 / (((max_threads_for(NP) / 32 + 3) / 4) * 32)) / 8 * 8;
+               : (16384 / (((max_threads_for(NP, R) / 32 + 3) / 4) * 32)) / 8 * 8;
 }
 
 // 128-bit column chunks of the tile rows kept in registers: as many as fit
 // beside about 56 other registers; the remaining chunks live in shared
 // memory (read once per product, a float4 per thread, conflict-free), so
 // that nothing is spilled to local memory
-constexpr int reg_chunks_for(int NP)
+constexpr int reg_chunks_for(int NP, int R)
 {
-    return (reg_cap_for(NP) - 56) / (2 * rows_for(NP) * 4) >= NP / 4
+    return (reg_cap_for(NP, R) - 56) / (2 * R * 4) >= NP / 4
                ? NP / 4
-               : (reg_cap_for(NP) - 56) / (2 * rows_for(NP) * 4);
+               : (reg_cap_for(NP, R) - 56) / (2 * R * 4);
 }
 
 template <int NP, int R>
 struct RowTiles {
-    static constexpr int RC = reg_chunks_for(NP);  // chunks in registers
+    static constexpr int RC = reg_chunks_for(NP, R);  // chunks in registers
     float lo[R][4 * RC];  // rows of Nhat_j        (times x_{j-1})
     float up[R][4 * RC];  // rows of Nhat_{j+1}^T  (times x_{j+1})
 };
@@ -182,7 +183,7 @@ __device__ __forceinline__ void rows_store(float* X, int j, int a0, const bool (
 }
 
 template <int NP, int R>
-__global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
+__global__ void __launch_bounds__(max_threads_for(NP, R)) k_pcg_rows(PcgArgs g)
 {
     extern __shared__ __align__(16) float sm[];
     const Work& w = g.w;
@@ -408,15 +409,14 @@ __global__ void __launch_bounds__(max_threads_for(NP)) k_pcg_rows(PcgArgs g)
     finish(g, sol, it, done, nonfinite);
 }
 
-template <int NP>
+template <int NP, int R = rows_for(NP)>
 cudaError_t launch_rows_np(const PcgArgs& a, size_t limit, cudaStream_t st)
 {
-    constexpr int R = rows_for(NP);
     const Work& w = a.w;
     const int TPK = (w.n + R - 1) / R;
     int T = ((w.N * TPK + 31) / 32) * 32;
     if (T < 64) T = 64;
-    if (T > max_threads_for(NP)) return cudaErrorInvalidConfiguration;
+    if (T > max_threads_for(NP, R)) return cudaErrorInvalidConfiguration;
     constexpr int SC = NP / 4 - RowTiles<NP, R>::RC;
     size_t smem = sizeof(float) * (2 * (size_t)(w.N + 2) * NP + round4((size_t)w.N * w.n)) +
                   (120 + (size_t)SC * R * 2 * T) * sizeof(float4);
