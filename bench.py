@@ -42,6 +42,9 @@ PCG_TRAFFIC = {"pcg_sha": "1f8d5864afd6735f", "bytes_per_launch": 151428258}
 
 FP32_LANES_PER_SM = 128  # FFMA lanes per SM (4 sub-partitions x 32)
 
+# gato_set_pcg_kernel choices by name (the values of include/gato.h)
+PCG_KERNELS = {"auto": 0, "generic": 1, "wide": 2, "tile": 3, "rows": 4, "quad": 5}
+
 # linear solvers of S lambda = gamma (gato_params.linsys)
 LINSYS = {"pcg": 1, "bdsv": 2, "bdsv_chrono": 3}
 
@@ -368,7 +371,7 @@ def run_pcg_kernel_sweep(args, local):
             w = dataclasses.replace(base, n=n, m=n // 2, N=N)
             one = make_batch(w, M=16)
             for M in (16, 152, 256, 1024):
-                prob = {k: np.ascontiguousarray(np.concatenate([v] * (M // 16))[:M])
+                prob = {k: np.ascontiguousarray(np.concatenate([v] * -(-M // 16))[:M])
                         for k, v in one.items()}
                 d = {k: torch.from_numpy(v).to(dev) for k, v in prob.items()}
                 p = gato.default_params(pcg_eps=1e-6, pcg_max_iters=2000)
@@ -706,6 +709,7 @@ def run_gpu(args, world, rank, local):
     dev = torch.device("cuda", local)
     d = {k: torch.from_numpy(v).to(dev) for k, v in prob.items()}
     s = gato.Solver(M, w.N, w.n, w.m)
+    s.set_pcg_kernel(PCG_KERNELS[args.pcg_kernel])
     out = s.outputs(w.n_alpha)
     p = gato.default_params(**w.solver_settings(), linsys=LINSYS[args.linsys])
     stream = torch.cuda.current_stream()
@@ -840,7 +844,7 @@ def run_gpu(args, world, rank, local):
     # the ncu capture behind the traffic figure is of the default workload
     traffic = (PCG_TRAFFIC["bytes_per_launch"]
                if PCG_TRAFFIC["pcg_sha"] == sha and args.workload == WORKLOAD_INDEX
-               and not args.batch else None)
+               and not args.batch and args.pcg_kernel == "auto" else None)
 
     # ---- SQP loop on the linear model (context, not the metric) ----
     sqp = None
@@ -872,7 +876,8 @@ def run_gpu(args, world, rank, local):
             "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded generator, workload recipe of the benchmark configs)",
-            "config": _config(w),
+            "config": _config(w, **({} if args.pcg_kernel == "auto"
+                                    else {"pcg_kernel": args.pcg_kernel})),
             "pcg_iters_per_sec": iters_per_step * world / (total_ms / args.steps / 1000.0),
             "pcg_iters_per_solve": iters_per_step / M,
             "parts": parts,
@@ -964,6 +969,9 @@ def main():
                     help="the workload of the timed step (default 4, the metric's: "
                          "M=256, N=128, n=14, m=7); the others are parity cases, run "
                          "here for profiler captures")
+    ap.add_argument("--pcg-kernel", default="auto", choices=sorted(PCG_KERNELS),
+                    help="the PCG kernel of the timed step (default: the library's "
+                         "automatic choice); for comparisons and profiler captures")
     ap.add_argument("--batch", type=int, default=None,
                     help="solves per GPU (default: the workload's 256); for profiler "
                          "captures of a smaller case")

@@ -53,3 +53,33 @@ def test_launches_per_call():
     assert bench.launches_per_solve("pcg", 1, refine_solver=1) == 11
     assert bench.launches_per_solve("pcg", 2, refine_solver=1) == 15
     assert bench.launches_per_solve("bdsv", 1) == 11
+
+
+# --------------------------------------------------------------------------
+# the binding's size checks (host side)
+# --------------------------------------------------------------------------
+
+def test_binding_sizes_follow_the_header_layouts():
+    z = gato.sizes(3, 5, 4, 2, n_alpha=6)
+    assert z["Q"] == 3 * 5 * 16 and z["R"] == 3 * 4 * 4 and z["A"] == 3 * 4 * 16
+    assert z["B"] == 3 * 4 * 4 * 2 and z["e"] == 3 * 4 * 4 and z["s0"] == 3 * 4
+    assert z["dX"] == 3 * 5 * 4 and z["dU"] == 3 * 4 * 2 and z["merit"] == 3 * 7
+    # one knot: no controls, no couplings
+    z1 = gato.sizes(2, 1, 4, 2)
+    assert z1["R"] == z1["A"] == z1["B"] == z1["dU"] == 0
+
+
+def test_binding_rejects_a_short_array_before_any_call():
+    torch = pytest.importorskip("torch")
+    t = torch.zeros(10)
+    assert gato._host_ptr(t, what="Q", numel=10) is not None
+    with pytest.raises(ValueError, match="Q holds 10 elements"):
+        gato._host_ptr(t, what="Q", numel=11)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        gato._ptr(t, what="Q", numel=10)
+
+
+def test_pcg_kernel_names_match_the_header():
+    assert bench.PCG_KERNELS == {"auto": gato.GATO_PCG_AUTO, "generic": gato.GATO_PCG_GENERIC,
+                                 "wide": gato.GATO_PCG_WIDE, "tile": gato.GATO_PCG_TILE,
+                                 "rows": gato.GATO_PCG_ROWS, "quad": gato.GATO_PCG_QUAD}

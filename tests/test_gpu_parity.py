@@ -268,6 +268,32 @@ def test_quad_kernel_stopping_rules(rule):
     assert np.abs(a["iters"] - b["iters"]).max() <= 0.05 * b["iters"].max() + 2
 
 
+def test_a_short_input_array_is_rejected_before_launch():
+    prob = random_lq(4, 8, 14, 7, seed=790)
+    d = gato.to_device(prob)
+    d["A"] = d["A"][:3].contiguous()  # three solves of A for a batch of four
+    p = gato.default_params(pcg_max_iters=500)
+    with gato.Solver(4, 8, 14, 7) as s:
+        out = s.outputs(p.n_alpha)
+        with pytest.raises(ValueError, match="A holds"):
+            s.solve_kkt(p, d, out["dX"], out["dU"], out["lam"], out["iters"], out["merit"],
+                        out["best"], out["status"])
+
+
+def test_kernel_choice_between_sizes_keeps_launches_valid():
+    """The automatic choice queries the wide kernel's occupancy at each call's
+    sizes; a later launch of that kernel at other sizes (its shared memory
+    under the 48 KB default, above the size queried) still launches."""
+    p = gato.default_params(pcg_max_iters=3000, refine_steps=0)
+    small = random_lq(16, 16, 12, 6, seed=791)
+    mid = random_lq(2, 32, 12, 6, seed=792)
+    assert ran_kernels(small, p)[0] == gato.GATO_PCG_QUAD
+    assert ran_kernels(mid, p, gato.GATO_PCG_WIDE)[0] == gato.GATO_PCG_WIDE
+    out = solve(mid, gato.default_params(pcg_max_iters=3000, refine_steps=1), gato.GATO_PCG_WIDE)
+    assert not out["status"].any()
+    check_solution(mid, out, range(2))
+
+
 def ran_kernels(prob, p, kernel=gato.GATO_PCG_AUTO, parts=0):
     """gato_stats.pcg_kernel and refine_kernel after one gato_solve_kkt."""
     M, N, n = prob["Q"].shape[:3]

@@ -167,7 +167,9 @@ def test_invalid_sqp_parameters_rejected():
     model = gato.to_device(linear_models(1, 4, 3, 2, seed=49))
     f = dict(device="cuda", dtype=torch.float32)
     X, U, lam = torch.zeros(1, 4, 3, **f), torch.zeros(1, 3, 2, **f), torch.zeros(1, 4, 3, **f)
-    rho, hist = torch.ones(1, **f), torch.zeros(1, 2, **f)
+    # the history holds the default iteration count's columns, so that the
+    # library's own parameter checks are reached
+    rho, hist = torch.ones(1, **f), torch.zeros(1, gato.default_sqp_params().iters + 1, **f)
     status = torch.zeros(1, device="cuda", dtype=torch.int32)
     with gato.Solver(1, 4, 3, 2) as s:
         for bad in (dict(iters=0), dict(rho_factor=1.0), dict(rho_min=-1.0),

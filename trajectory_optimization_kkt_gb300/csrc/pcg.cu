@@ -1336,14 +1336,16 @@ cudaError_t launch_cluster(K kernel, const PcgArgs& a, int C, int T, size_t smem
 namespace {
 
 // blocks of a kernel an SM can hold with T threads and smem bytes of dynamic
-// shared memory (the opt-in above 48 KB set first, as for its launch); 0 on
-// error
+// shared memory; 0 on error.  Above 48 KB the opt-in is raised first, as for
+// a launch; it is never set below 48 KB, which every launch of at most 48 KB
+// relies on without setting it
 template <typename K>
 int blocks_per_sm(K kernel, int T, size_t smem)
 {
     int per_sm = 0;
-    cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaSuccess;
+    if (smem > 48 * 1024)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, T, smem);
     if (e != cudaSuccess) {
         cudaGetLastError();

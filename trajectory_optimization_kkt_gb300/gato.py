@@ -173,8 +173,16 @@ def default_sqp_params(**overrides) -> GatoSqpParams:
     return sp
 
 
-def _ptr(t, dtype=None, what="tensor"):
-    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+def _check_numel(t, numel, what):
+    # the library reads or writes numel elements from the pointer: a shorter
+    # tensor would be overrun
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{what} holds {t.numel()} elements, the call needs {numel}")
+
+
+def _ptr(t, dtype=None, what="tensor", numel=None):
+    """Device pointer of a contiguous CUDA tensor of at least numel elements
+    (None -> NULL)."""
     if t is None:
         return None
     import torch
@@ -185,12 +193,13 @@ def _ptr(t, dtype=None, what="tensor"):
     want = dtype or torch.float32
     if t.dtype != want:
         raise ValueError(f"{what} must be {want}, got {t.dtype}")
+    _check_numel(t, numel, what)
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _host_ptr(t, dtype=None, what="tensor"):
-    """Host pointer of a contiguous CPU tensor (None -> NULL); pin it for
-    copies that overlap the solve."""
+def _host_ptr(t, dtype=None, what="tensor", numel=None):
+    """Host pointer of a contiguous CPU tensor of at least numel elements
+    (None -> NULL); pin it for copies that overlap the solve."""
     if t is None:
         return None
     import torch
@@ -201,7 +210,20 @@ def _host_ptr(t, dtype=None, what="tensor"):
     want = dtype or torch.float32
     if t.dtype != want:
         raise ValueError(f"{what} must be {want}, got {t.dtype}")
+    _check_numel(t, numel, what)
     return ctypes.c_void_p(t.data_ptr())
+
+
+def sizes(M: int, N: int, n: int, m: int, n_alpha: int = 8) -> dict:
+    """Elements of every array argument of the entry points, by name, for a
+    batch of M solves (the layouts include/gato.h gives)."""
+    K = max(N - 1, 0)
+    return dict(Q=M * N * n * n, R=M * K * m * m, q=M * N * n, r=M * K * m, A=M * K * n * n,
+                B=M * K * n * m, e=M * K * n, s0=M * n, c=M * K * n, xs=M * n,
+                dX=M * N * n, dU=M * K * m, lam=M * N * n, lambda0=M * N * n, iters=M,
+                merit=M * (n_alpha + 1), best=M, status=M, X=M * N * n, U=M * K * m, rho=M,
+                S_diag=M * N * n * n, S_off=M * K * n * n, gamma=M * N * n,
+                Phi_diag=M * N * n * n, Phi_off=M * K * n * n)
 
 
 def _stream(stream):
@@ -245,8 +267,12 @@ class Solver:
         self.close()
 
     # -- helpers --------------------------------------------------------------
-    def _lq(self, prob):
-        return [_ptr(prob.get(k), what=k) for k in _LQ]
+    def _sz(self, params=None):
+        return sizes(self.M, self.N, self.n, self.m, params.n_alpha if params else 8)
+
+    def _lq(self, prob, keys=_LQ):
+        sz = self._sz()
+        return [_ptr(prob.get(k), what=k, numel=sz[k]) for k in keys]
 
     # -- entry points ---------------------------------------------------------
     def set_timing(self, on: bool):
@@ -273,37 +299,52 @@ class Solver:
 
     def get_schur(self, S_diag=None, S_off=None, gamma=None, Phi_diag=None, Phi_off=None,
                   stream=None):
+        z = self._sz()
         _check("gato_get_schur", self.lib.gato_get_schur(
-            self.h, _ptr(S_diag), _ptr(S_off), _ptr(gamma), _ptr(Phi_diag), _ptr(Phi_off),
-            _stream(stream)))
+            self.h, _ptr(S_diag, what="S_diag", numel=z["S_diag"]),
+            _ptr(S_off, what="S_off", numel=z["S_off"]),
+            _ptr(gamma, what="gamma", numel=z["gamma"]),
+            _ptr(Phi_diag, what="Phi_diag", numel=z["Phi_diag"]),
+            _ptr(Phi_off, what="Phi_off", numel=z["Phi_off"]), _stream(stream)))
 
     def pcg_solve(self, params, lam, dX, dU, iters, status, lambda0=None, stream=None):
         import torch
+        z = self._sz(params)
         _check("gato_pcg_solve", self.lib.gato_pcg_solve(
-            self.h, ctypes.byref(params), _ptr(lambda0), _ptr(lam), _ptr(dX), _ptr(dU),
-            _ptr(iters, torch.int32, "iters"), _ptr(status, torch.int32, "status"),
-            _stream(stream)))
+            self.h, ctypes.byref(params), _ptr(lambda0, what="lambda0", numel=z["lambda0"]),
+            _ptr(lam, what="lam", numel=z["lam"]), _ptr(dX, what="dX", numel=z["dX"]),
+            _ptr(dU, what="dU", numel=z["dU"]),
+            _ptr(iters, torch.int32, "iters", z["iters"]),
+            _ptr(status, torch.int32, "status", z["status"]), _stream(stream)))
 
     def bdsv_solve(self, params, lam, dX, dU, iters, status, stream=None):
         import torch
+        z = self._sz(params)
         _check("gato_bdsv_solve", self.lib.gato_bdsv_solve(
-            self.h, ctypes.byref(params), _ptr(lam), _ptr(dX), _ptr(dU),
-            _ptr(iters, torch.int32, "iters"), _ptr(status, torch.int32, "status"),
-            _stream(stream)))
+            self.h, ctypes.byref(params), _ptr(lam, what="lam", numel=z["lam"]),
+            _ptr(dX, what="dX", numel=z["dX"]), _ptr(dU, what="dU", numel=z["dU"]),
+            _ptr(iters, torch.int32, "iters", z["iters"]),
+            _ptr(status, torch.int32, "status", z["status"]), _stream(stream)))
 
     def linesearch(self, params, prob, dX, dU, merit, best, status, stream=None):
         import torch
+        z = self._sz(params)
         _check("gato_linesearch", self.lib.gato_linesearch(
-            self.h, ctypes.byref(params), *self._lq(prob), _ptr(dX), _ptr(dU), _ptr(merit),
-            _ptr(best, torch.int32, "best"), _ptr(status, torch.int32, "status"),
-            _stream(stream)))
+            self.h, ctypes.byref(params), *self._lq(prob), _ptr(dX, what="dX", numel=z["dX"]),
+            _ptr(dU, what="dU", numel=z["dU"]), _ptr(merit, what="merit", numel=z["merit"]),
+            _ptr(best, torch.int32, "best", z["best"]),
+            _ptr(status, torch.int32, "status", z["status"]), _stream(stream)))
 
     def solve_kkt(self, params, prob, dX, dU, lam, iters, merit, best, status, stream=None):
         import torch
+        z = self._sz(params)
         _check("gato_solve_kkt", self.lib.gato_solve_kkt(
-            self.h, ctypes.byref(params), *self._lq(prob), _ptr(dX), _ptr(dU), _ptr(lam),
-            _ptr(iters, torch.int32, "iters"), _ptr(merit), _ptr(best, torch.int32, "best"),
-            _ptr(status, torch.int32, "status"), _stream(stream)))
+            self.h, ctypes.byref(params), *self._lq(prob), _ptr(dX, what="dX", numel=z["dX"]),
+            _ptr(dU, what="dU", numel=z["dU"]), _ptr(lam, what="lam", numel=z["lam"]),
+            _ptr(iters, torch.int32, "iters", z["iters"]),
+            _ptr(merit, what="merit", numel=z["merit"]),
+            _ptr(best, torch.int32, "best", z["best"]),
+            _ptr(status, torch.int32, "status", z["status"]), _stream(stream)))
 
     def set_parts(self, parts: int):
         _check("gato_set_parts", self.lib.gato_set_parts(self.h, parts))
@@ -318,29 +359,39 @@ class Solver:
         """gato_solve_kkt_host: every array is a (preferably pinned) CPU
         tensor; synchronise the stream before reading the outputs."""
         import torch
+        z = self._sz(params)
         _check("gato_solve_kkt_host", self.lib.gato_solve_kkt_host(
-            self.h, ctypes.byref(params), *[_host_ptr(prob.get(k), what=k) for k in _LQ],
-            _host_ptr(dX), _host_ptr(dU), _host_ptr(lam), _host_ptr(iters, torch.int32, "iters"),
-            _host_ptr(merit), _host_ptr(best, torch.int32, "best"),
-            _host_ptr(status, torch.int32, "status"), _stream(stream)))
+            self.h, ctypes.byref(params),
+            *[_host_ptr(prob.get(k), what=k, numel=z[k]) for k in _LQ],
+            _host_ptr(dX, what="dX", numel=z["dX"]), _host_ptr(dU, what="dU", numel=z["dU"]),
+            _host_ptr(lam, what="lam", numel=z["lam"]),
+            _host_ptr(iters, torch.int32, "iters", z["iters"]),
+            _host_ptr(merit, what="merit", numel=z["merit"]),
+            _host_ptr(best, torch.int32, "best", z["best"]),
+            _host_ptr(status, torch.int32, "status", z["status"]), _stream(stream)))
 
     def sqp_linear(self, params, sqp_params, model, X, U, lam, rho, merit_hist, status,
                    iters_hist=None, stream=None):
         """gato_sqp_linear: model holds Q, R, q, r, A, B, c, xs (CUDA tensors);
         X, U, lam and rho are updated in place."""
         import torch
+        z = self._sz(params)
         _check("gato_sqp_linear", self.lib.gato_sqp_linear(
-            self.h, ctypes.byref(params), ctypes.byref(sqp_params),
-            *[_ptr(model.get(k), what=k) for k in _MODEL],
-            _ptr(X), _ptr(U), _ptr(lam), _ptr(rho), _ptr(merit_hist),
-            _ptr(iters_hist, torch.int32, "iters_hist"), _ptr(status, torch.int32, "status"),
+            self.h, ctypes.byref(params), ctypes.byref(sqp_params), *self._lq(model, _MODEL),
+            _ptr(X, what="X", numel=z["X"]), _ptr(U, what="U", numel=z["U"]),
+            _ptr(lam, what="lam", numel=z["lam"]), _ptr(rho, what="rho", numel=z["rho"]),
+            _ptr(merit_hist, what="merit_hist", numel=self.M * (sqp_params.iters + 1)),
+            _ptr(iters_hist, torch.int32, "iters_hist", self.M * sqp_params.iters),
+            _ptr(status, torch.int32, "status", z["status"]),
             _stream(stream)))
 
     def apply_step(self, params, best, dX, dU, X, U, stream=None):
         import torch
+        z = self._sz(params)
         _check("gato_apply_step", self.lib.gato_apply_step(
-            self.h, ctypes.byref(params), _ptr(best, torch.int32, "best"), _ptr(dX), _ptr(dU),
-            _ptr(X), _ptr(U), _stream(stream)))
+            self.h, ctypes.byref(params), _ptr(best, torch.int32, "best", z["best"]),
+            _ptr(dX, what="dX", numel=z["dX"]), _ptr(dU, what="dU", numel=z["dU"]),
+            _ptr(X, what="X", numel=z["X"]), _ptr(U, what="U", numel=z["U"]), _stream(stream)))
 
     # -- convenience ------------------------------------------------------------
     def outputs(self, n_alpha: int = 8):
@@ -386,10 +437,14 @@ def solve_kkt_noalloc(params, prob, dX, dU, lam, iters, merit, best, status, str
         m = prob["B"].shape[-1]
     else:
         M, N, n, m = dims
+    z = sizes(M, N, n, m, params.n_alpha)
     _check("gato_solve_kkt_noalloc", load().gato_solve_kkt_noalloc(
-        ctypes.byref(params), M, N, n, m, *[_ptr(prob.get(k), what=k) for k in _LQ],
-        _ptr(dX), _ptr(dU), _ptr(lam), _ptr(iters, torch.int32, "iters"), _ptr(merit),
-        _ptr(best, torch.int32, "best"), _ptr(status, torch.int32, "status"), _stream(stream)))
+        ctypes.byref(params), M, N, n, m,
+        *[_ptr(prob.get(k), what=k, numel=z[k]) for k in _LQ],
+        _ptr(dX, what="dX", numel=z["dX"]), _ptr(dU, what="dU", numel=z["dU"]),
+        _ptr(lam, what="lam", numel=z["lam"]), _ptr(iters, torch.int32, "iters", z["iters"]),
+        _ptr(merit, what="merit", numel=z["merit"]), _ptr(best, torch.int32, "best", z["best"]),
+        _ptr(status, torch.int32, "status", z["status"]), _stream(stream)))
 
 
 def to_device(prob, device="cuda"):
