@@ -37,8 +37,8 @@ WORKLOAD_INDEX = 4  # M=256, N=128, n=14, m=7
 # solve launch at this workload, from an ncu capture; valid only for the
 # kernel source it was taken on (sha256 prefix of csrc/pcg.cu), null
 # otherwise.  Captured on 152 solves (one block per SM) and scaled
-# by the solves processed to the 256-solve launch (89.91 MB x 256 / 152).
-PCG_TRAFFIC = {"pcg_sha": "1f8d5864afd6735f", "bytes_per_launch": 151428258}
+# by the solves processed to the 256-solve launch (89.70 MB x 256 / 152).
+PCG_TRAFFIC = {"pcg_sha": "e4383d03ee4f9796", "bytes_per_launch": 151081175}
 
 FP32_LANES_PER_SM = 128  # FFMA lanes per SM (4 sub-partitions x 32)
 
@@ -346,8 +346,8 @@ def run_sweep(args, local):
 
 def run_pcg_kernel_sweep(args, local):
     """PCG-only time of the wide-tile and quad kernels and of the automatic
-    choice, n in {12, 14, 16} x N in {16, 32, 64, 128} x M in {16, 152, 256,
-    1024}: gato_pcg_solve after one gato_form_schur (stop rule 0, eps 1e-6),
+    choice, n in {8, 10, 12, 14, 16} x N in {16, 32, 64, 128} x M in {16, 152,
+    256, 1024}: gato_pcg_solve after one gato_form_schur (stop rule 0, eps 1e-6),
     L2 flushed before each launch, the median of 6 launches after 2; the
     batch is 16 generated solves (workload 4's generator at these sizes)
     repeated to M, so every solve of a cell takes the iterations of one of
@@ -366,7 +366,7 @@ def run_pcg_kernel_sweep(args, local):
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     kinds = {"wide": gato.GATO_PCG_WIDE, "quad": gato.GATO_PCG_QUAD, "auto": gato.GATO_PCG_AUTO}
     base = WORKLOADS[WORKLOAD_INDEX]
-    for n in (12, 14, 16):
+    for n in (8, 10, 12, 14, 16):
         for N in (16, 32, 64, 128):
             w = dataclasses.replace(base, n=n, m=n // 2, N=N)
             one = make_batch(w, M=16)
