@@ -212,7 +212,9 @@ def _config(w, **extra):
     c = {"workload": w.name, "M": w.M, "N": w.N, "n": w.n, "m": w.m, "pcg_eps": w.pcg_eps,
          "pcg_max_iters": w.pcg_max_iters, "stop_rule": "relative residual ||r||<=eps||gamma||",
          "n_alpha": w.n_alpha, "beta": w.beta, "mu": w.mu,
-         "refine_steps": w.refine_steps, "refine_eps": w.refine_eps,
+         "refine_steps": w.refine_steps,
+         "refine_solver": "direct (cyclic-reduction factors of the same S)" if w.refine_solver
+                          else f"pcg to {w.refine_eps}",
          "pcg_precision": "double-float" if w.pcg_precision else "fp32",
          "l2": "flushed before every timed step (256 MB write)"}
     c.update(extra)
@@ -815,8 +817,10 @@ def run_gpu(args, world, rank, local):
     # solve-iteration are those of the method's iteration on the explicit
     # block-tridiagonal S and Phi^-1: two products with 3N-2 blocks of n^2
     # (2 flops per entry each) plus 12 N n of vector updates and dots.  Every
-    # PCG iteration of the step (solve and refinement correction) counts; the
-    # time is the two PCG launches plus the refinement's small kernels.
+    # PCG iteration of the step counts.  With PCG corrections the time is the
+    # two PCG launches plus the refinement's small kernels; with direct
+    # corrections (substitutions, no PCG iteration) it is the main PCG launch
+    # alone.
     N, n = w.N, w.n
     flops_it = 2 * 2 * (3 * N - 2) * n * n + 12 * N * n
     iters_per_step = iters_total / args.steps
@@ -892,7 +896,8 @@ def run_gpu(args, world, rank, local):
                          "unit": "TFLOP/s", "frac": achieved_tf / alu_peak_tf,
                          "traffic": traffic,
                          "kernel": _pcg_kernel_label(stage_stats, M, N, n, n_sm)
-                                   + " (solve + refinement launches)",
+                                   + (" (main solve; direct corrections)" if w.refine_solver
+                                      else " (solve + refinement launches)"),
                          "peak_basis": "measured in this run: fp32 FMA probe "
                                        "(gato_probe_fp32), faster of scalar and packed form; "
                                        "of measured",

@@ -94,11 +94,16 @@ def test_rho_sweep_matches_oracle(linsys, use_graph):
             assert (out["iters"][j] == 0).all()
 
 
-def test_graph_and_stream_paths_are_bit_identical():
+@pytest.mark.parametrize("refine_solver", [0, 1], ids=["pcg_corrections", "direct_corrections"])
+def test_graph_and_stream_paths_are_bit_identical(refine_solver):
+    """Also with direct corrections, whose factorisation runs on a side stream
+    forked from the iteration's stream and joined back (inside the recorded
+    graph as dependencies)."""
     model = linear_models(4, 16, 14, 7, seed=43)
     rho0 = np.array([1e-6, 1e-3, 0.1, 3.0], dtype=np.float32)
-    a = run(model, rho0, 5, params(), gato.default_sqp_params(use_graph=1))
-    b = run(model, rho0, 5, params(), gato.default_sqp_params(use_graph=0))
+    p = params(refine_solver=refine_solver)
+    a = run(model, rho0, 5, p, gato.default_sqp_params(use_graph=1))
+    b = run(model, rho0, 5, p, gato.default_sqp_params(use_graph=0))
     for k in a:
         assert np.array_equal(a[k], b[k], equal_nan=True), k
 

@@ -160,3 +160,21 @@ def test_noalloc_rejects_problems_beyond_its_scratch(wi, M):
                                o["merit"], o["best"], o["status"])
     assert e.value.code == gato.GATO_ERR_UNSUPPORTED
     assert (o["iters"].cpu().numpy() == -7).all()  # nothing ran
+
+
+@pytest.mark.parametrize("wi,M", [(1, 16), (2, 40)])
+def test_forked_factorisation_gives_the_serial_results(wi, M):
+    """With direct corrections after a PCG solve, gato_solve_kkt forms the
+    corrections' factorisation on a low-priority side stream beside the main
+    solve; the allocation-free entry has no side stream and forms it in
+    stream order.  The same kernels on the same data: bit-identical outputs
+    (workload 2 at 40 solves runs one part in both, and its double-float main
+    solve over clusters of two CTAs)."""
+    w = WORKLOADS[wi]
+    prob = make_batch(w, M=M)
+    p = params(w)
+    assert p.refine_solver == gato.GATO_REFINE_SOLVER_DIRECT and p.refine_steps >= 1
+    d, ref = reference(prob, p)
+    o = call_noalloc(p, d, M, w.N, w.n, w.m)
+    for k in ref:
+        np.testing.assert_array_equal(o[k], ref[k], err_msg=k)

@@ -127,6 +127,18 @@ cudaError_t run_kkt_core(gato_handle* h, const gato_params* p, const float* Q_fo
     h->pcg_ran = h->refine_ran = 0;
     const int ls = linsys_for(p, w.N);
     const bool direct = ls != GATO_LINSYS_PCG;
+    // corrections by substitution with the direct solve's factors: those of the
+    // main solve, or (GATO_REFINE_SOLVER_DIRECT after a PCG solve) the
+    // cyclic-reduction factorisation of the same S, formed once.  That
+    // factorisation needs only the formation's blocks, so with a side stream
+    // it is forked off once the main PCG is launched and runs on the SMs the
+    // PCG leaves idle (its stream has the lowest priority); the corrections
+    // join it before their first substitution
+    const bool direct_ref =
+        direct || (p->refine_solver == GATO_REFINE_SOLVER_DIRECT && p->refine_steps > 0);
+    const int ls_ref = direct ? ls : GATO_LINSYS_BDSV;
+    const bool fork_factor = direct_ref && !direct && h->side;
+    bool joined = false;
     cudaError_t err = launch_form_matrices(h, Q_form, R, A, B, status, st);
     if (err == cudaSuccess) err = launch_form_rhs(h, 0, q, r, e, s0, (size_t)w.n, st);
     if (timed) record(h, 1, st);
@@ -136,7 +148,14 @@ cudaError_t run_kkt_core(gato_handle* h, const gato_params* p, const float* Q_fo
             if (err == cudaSuccess)
                 err = launch_bdsv_solve(h, ls, 0, lambda, dX, dU, iters, 0, status, st);
         } else {
-            err = launch_pcg_ex(h, p, 0, lambda0, lambda, dX, dU, iters, 0, status, st);
+            if (fork_factor) err = cudaEventRecord(h->ev_fork, st);
+            if (err == cudaSuccess)
+                err = launch_pcg_ex(h, p, 0, lambda0, lambda, dX, dU, iters, 0, status, st);
+            if (err == cudaSuccess && fork_factor) {
+                err = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
+                if (err == cudaSuccess) err = launch_bdsv_factor(h, ls_ref, status, h->side);
+                if (err == cudaSuccess) err = cudaEventRecord(h->ev_join, h->side);
+            }
         }
     }
     if (timed) record(h, 2, st);
@@ -147,18 +166,16 @@ cudaError_t run_kkt_core(gato_handle* h, const gato_params* p, const float* Q_fo
     if (p->refine_eps > 0.f) pc.pcg_eps = p->refine_eps;
     pc.stop_rule = GATO_STOP_PRECOND;
     pc.pcg_precision = GATO_PCG_PRECISION_FP32;
-    // corrections by substitution with the direct solve's factors: those of the
-    // main solve, or (GATO_REFINE_SOLVER_DIRECT after a PCG solve) the
-    // cyclic-reduction factorisation of the same S, formed once here
-    const bool direct_ref =
-        direct || (p->refine_solver == GATO_REFINE_SOLVER_DIRECT && p->refine_steps > 0);
-    const int ls_ref = direct ? ls : GATO_LINSYS_BDSV;
-    if (err == cudaSuccess && direct_ref && !direct)
+    if (err == cudaSuccess && direct_ref && !direct && !fork_factor)
         err = launch_bdsv_factor(h, ls_ref, status, st);
     for (int k = 0; k < p->refine_steps && err == cudaSuccess; ++k) {
         err = launch_kkt_residual(h, Q_form, R, q, r, A, B, e, s0, dX, dU, lambda, st);
         if (err == cudaSuccess)
             err = launch_form_rhs(h, 1, w.q2, w.r2, w.e2, w.s02, (size_t)w.n, st);
+        if (err == cudaSuccess && fork_factor && k == 0) {
+            err = cudaStreamWaitEvent(st, h->ev_join, 0);
+            joined = err == cudaSuccess;
+        }
         if (err == cudaSuccess) {
             if (direct_ref)
                 err = launch_bdsv_solve(h, ls_ref, 1, w.dlam, w.ddX, w.ddU, iters, 1, status,
@@ -169,6 +186,10 @@ cudaError_t run_kkt_core(gato_handle* h, const gato_params* p, const float* Q_fo
         }
         if (err == cudaSuccess) err = launch_accumulate(h, lambda, dX, dU, iters, st);
     }
+    // after an error the caller's stream still waits for the side stream, so
+    // that nothing of this call runs on after it (the event completes at once
+    // when nothing was recorded)
+    if (fork_factor && !joined) cudaStreamWaitEvent(st, h->ev_join, 0);
     if (timed && p->refine_steps > 0) record(h, 3, st);
     if (err == cudaSuccess)
         err = launch_merit(h, p, Q_merit, R, q, r, A, B, e, s0, dX, dU, merit, best, status, st);
@@ -375,8 +396,14 @@ int gato_create(gato_handle** out, int M, int N, int n, int m)
     }
     h->last.form_us = h->last.pcg_us = h->last.refine_us = h->last.merit_us = h->last.total_us =
         -1.f;
-    const int prc = gato::parts_init(h);
+    int prc = gato::side_stream_create(&h->side, &h->ev_fork, &h->ev_join) == cudaSuccess
+                  ? GATO_OK
+                  : GATO_ERR_CUDA;
+    if (prc == GATO_OK) prc = gato::parts_init(h);
     if (prc != GATO_OK) {
+        if (h->side) cudaStreamDestroy(h->side);
+        if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+        if (h->ev_join) cudaEventDestroy(h->ev_join);
         for (int i = 0; i < 5; ++i) cudaEventDestroy(h->ev[i]);
         cudaFree(h->base);
         free(h);
@@ -392,6 +419,9 @@ void gato_destroy(gato_handle* h)
     gato::parts_free(h);
     if (h->sqp_exec) cudaGraphExecDestroy(h->sqp_exec);
     if (h->capture_stream) cudaStreamDestroy(h->capture_stream);
+    if (h->side) cudaStreamDestroy(h->side);
+    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+    if (h->ev_join) cudaEventDestroy(h->ev_join);
     for (int i = 0; i < 5; ++i) cudaEventDestroy(h->ev[i]);
     cudaFree(h->base);
     free(h);

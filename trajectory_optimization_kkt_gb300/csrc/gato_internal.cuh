@@ -113,6 +113,12 @@ struct gato_handle {
     int refine_ran;         // ... and of the last correction PCG launch
     int batch_M;            // solves running at the same time as this handle's: the
                             // whole batch when the handle is one part of it (0: w.M)
+    // a low-priority stream, and the events that fork work onto it and join
+    // it back, for work that may run beside the main solve (the corrections'
+    // factorisation); side is NULL where there is none (the allocation-free
+    // entry), and that work then runs in stream order
+    cudaStream_t side;
+    cudaEvent_t ev_fork, ev_join;
     int bdsv_kernel;        // GATO_BDSV_KERNEL_* selected by gato_set_bdsv_kernel
     int force_smem_form;    // GATO_FORM_SHARED selected by gato_set_form_kernel
     int phi_pending;        // the last formation left the explicit Phi^-1 blocks unformed
@@ -138,6 +144,10 @@ size_t parts_extra_bytes();       // allocation beyond the handle's own workspac
 int parts_init(gato_handle* h);   // streams and events of the parts (gato_create)
 void parts_free(gato_handle* h);  // releases h->pipe
 int parts_for(const gato_handle* h);
+// a stream of the device's lowest priority (work that fills idle SMs) or
+// highest (the solve's own stages), and the two fork/join events
+cudaError_t side_stream_create(cudaStream_t* st, cudaEvent_t* fork, cudaEvent_t* join);
+cudaError_t priority_stream_create(cudaStream_t* st, bool highest);
 // gato_solve_kkt on parts of the batch, concurrently on internal streams;
 // with `host`, every pointer is host memory and is staged through device
 // buffers.  Returns a GATO_* code.

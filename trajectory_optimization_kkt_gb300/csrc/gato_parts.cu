@@ -24,6 +24,9 @@ struct gato_parts {
     gato_handle sub[GATO_MAX_PARTS];  // views into the handle's workspace
     cudaStream_t st[GATO_MAX_PARTS];
     cudaEvent_t done[GATO_MAX_PARTS];
+    // each part's low-priority side stream and its fork/join events
+    cudaStream_t side[GATO_MAX_PARTS];
+    cudaEvent_t fork[GATO_MAX_PARTS], join[GATO_MAX_PARTS];
     cudaEvent_t entry;
     void* dev;  // host entry: staging for the inputs and outputs of all M solves
     // per-solve sizes (elements) of the caller's arrays and, for the staging,
@@ -44,6 +47,9 @@ void release(gato_parts* pp)
     for (int c = 0; c < pp->nstreams; ++c) {
         if (pp->st[c]) cudaStreamDestroy(pp->st[c]);
         if (pp->done[c]) cudaEventDestroy(pp->done[c]);
+        if (pp->side[c]) cudaStreamDestroy(pp->side[c]);
+        if (pp->fork[c]) cudaEventDestroy(pp->fork[c]);
+        if (pp->join[c]) cudaEventDestroy(pp->join[c]);
     }
     if (pp->entry) cudaEventDestroy(pp->entry);
     if (pp->dev) cudaFree(pp->dev);
@@ -81,6 +87,9 @@ void partition(gato_handle* h, int k, bool small_first)
         carve_workspace(sh.w, cnt, w.N, w.n, w.m, (float*)sh.base);
         sh.parts = 1;
         sh.batch_M = w.M;  // the parts run concurrently
+        sh.side = pp->side[c];
+        sh.ev_fork = pp->fork[c];
+        sh.ev_join = pp->join[c];
         off += align256(sh.bytes);
     }
     pp->count_parts = k;
@@ -126,6 +135,22 @@ int ensure_staging(gato_parts* pp, int M)
 // each, and each part's region starts on a 256-byte boundary
 size_t parts_extra_bytes() { return (size_t)GATO_MAX_PARTS * 512; }
 
+cudaError_t priority_stream_create(cudaStream_t* st, bool highest)
+{
+    int least = 0, greatest = 0;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e != cudaSuccess) return e;
+    return cudaStreamCreateWithPriority(st, cudaStreamNonBlocking, highest ? greatest : least);
+}
+
+cudaError_t side_stream_create(cudaStream_t* st, cudaEvent_t* fork, cudaEvent_t* join)
+{
+    cudaError_t e = priority_stream_create(st, false);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(join, cudaEventDisableTiming);
+    return e;
+}
+
 // streams and events for up to min(M, GATO_MAX_PARTS) parts, at gato_create
 int parts_init(gato_handle* h)
 {
@@ -148,9 +173,12 @@ int parts_init(gato_handle* h)
     int rc = GATO_OK;
     if (cudaEventCreateWithFlags(&pp->entry, cudaEventDisableTiming) != cudaSuccess)
         rc = GATO_ERR_CUDA;
+    // the parts' own streams at the highest priority, so that the blocks of
+    // their stages are dispatched before those of their side streams
     for (int c = 0; c < pp->nstreams && rc == GATO_OK; ++c)
-        if (cudaStreamCreateWithFlags(&pp->st[c], cudaStreamNonBlocking) != cudaSuccess ||
-            cudaEventCreateWithFlags(&pp->done[c], cudaEventDisableTiming) != cudaSuccess)
+        if (priority_stream_create(&pp->st[c], true) != cudaSuccess ||
+            cudaEventCreateWithFlags(&pp->done[c], cudaEventDisableTiming) != cudaSuccess ||
+            side_stream_create(&pp->side[c], &pp->fork[c], &pp->join[c]) != cudaSuccess)
             rc = GATO_ERR_CUDA;
     if (rc != GATO_OK) {
         release(pp);

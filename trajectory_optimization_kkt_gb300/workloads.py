@@ -126,20 +126,21 @@ class Workload:
 # 180 and up to 487 iterations there, fp32 PCG 227 and up to 504, so these two
 # run the main solve in double-float arithmetic (about 48 bits: 186 and up to
 # 491).  The others state only eps = 1e-6; their cap is set high enough for
-# fp32 PCG to reach it.  Refinement by the rule above: one PCG correction at
-# 0.25 for workload 0 (dX 3.3e-5) and at 0.1 for workload 4 (4.6e-5); one
-# direct correction for workloads 1 and 2 (about 1e-7); two direct ones for
-# workload 3 (diagonal scaling over four decades: one leaves dX at 8.4e-5,
-# two at 3e-6).
+# fp32 PCG to reach it.  Refinement by the rule above: one direct correction
+# for workloads 0, 1, 2 and 4 (dX about 1e-7; its factorisation runs beside
+# the main PCG on the SMs that solve leaves idle, which made it the faster
+# choice for workloads 0 and 4 too, against PCG corrections at 0.25 and 0.1);
+# two direct ones for workload 3 (diagonal scaling over four decades: one
+# leaves dX at 8.4e-5, two at 3e-6).
 WORKLOADS = [
-    Workload(0, "M1_N16_n14_m7", 1, 16, 14, 7, pcg_max_iters=200, refine_eps=0.25,
-             pcg_precision=1),
+    Workload(0, "M1_N16_n14_m7", 1, 16, 14, 7, pcg_max_iters=200, pcg_precision=1,
+             refine_solver=1),
     Workload(1, "M16_N32_n12_m6", 16, 32, 12, 6, pcg_max_iters=1000, refine_solver=1),
     Workload(2, "M64_N64_n14_m7_A05_QN10", 64, 64, 14, 7, a_sigma=0.05,
              terminal_scale=10.0, pcg_max_iters=500, pcg_precision=1, refine_solver=1),
     Workload(3, "M128_N16_n36_m12_logscaled", 128, 16, 36, 12, b_sigma=0.05,
              log_scale=True, pcg_max_iters=4000, refine_steps=2, refine_solver=1),
-    Workload(4, "M256_N128_n14_m7", 256, 128, 14, 7, pcg_max_iters=1000),
+    Workload(4, "M256_N128_n14_m7", 256, 128, 14, 7, pcg_max_iters=1000, refine_solver=1),
 ]
 
 
