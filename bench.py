@@ -296,6 +296,7 @@ def _time_solver(torch, s, p, d, out, steps, flush, stream):
         b.synchronize()
         ms.append(a.elapsed_time(b))
         iters += int(out["iters"].sum())
+    _time_solver.last_parts = s.get_parts()  # the parts the timed calls ran
     s.set_parts(1)
     s.set_timing(True)
     for k in range(steps):
@@ -434,7 +435,8 @@ def run_throughput_sweep(args, local):
                 # at M = 1 this is the latency of one iteration of one solve
                 pcg_us_it = (stages["linsys"] + stages["refine"]) / max(iters / M, 1.0)
                 print(json.dumps({"sweep": "throughput", "M": M, "N": N, "n": w.n, "m": w.m,
-                                  "parts": s.get_parts(), "solves_per_s": M / (ms / 1000.0),
+                                  "parts": _time_solver.last_parts,
+                                  "solves_per_s": M / (ms / 1000.0),
                                   "pcg_us_per_iteration": pcg_us_it,
                                   "pcg_kernel": _pcg_kernel_label(
                                       _time_solver.last_stats, M, N, w.n,
@@ -514,7 +516,7 @@ def run_workloads(args, local):
         with gato.Solver(M, N, n, m) as s:
             out = s.outputs(w.n_alpha)
             ms, stages, iters, bad = _time_solver(torch, s, p, d, out, steps, flush, stream)
-            parts = s.get_parts()
+            parts = _time_solver.last_parts
         flops_it = 2 * 2 * (3 * N - 2) * n * n + 12 * N * n
         # with direct corrections the refinement stage runs no PCG iteration
         pcg_us = stages["linsys"] + (0.0 if w.refine_solver else stages["refine"])

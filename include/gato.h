@@ -475,14 +475,20 @@ int gato_solve_kkt_host(gato_handle* h, const gato_params* p, const float* Q, co
 
 /* Number of parts gato_solve_kkt and gato_solve_kkt_host split a batch into:
  * 1 .. GATO_MAX_PARTS (capped at M), or 0 for the automatic choice (the
- * default: one part below 64 solves, two below 128, four from 128).  The parts of a call run
- * concurrently on internal streams, each on its own sub-batch workspace, so
- * the kernels of one part fill the SMs that another part's leave idle (the
- * last wave of its PCG, its shorter stages).  Errors: INVALID_ARG. */
+ * default): one part below 64 solves, two below 128, four from 128; but for
+ * gato_solve_kkt with direct corrections after a PCG main solve
+ * (refine_solver = GATO_REFINE_SOLVER_DIRECT, refine_steps > 0), whose
+ * factorisation already runs beside the PCG on a low-priority stream, one
+ * part below 128 solves and two from 128.  The parts of a call run
+ * concurrently on internal streams of the highest priority, each on its own
+ * sub-batch workspace, so the kernels of one part fill the SMs that another
+ * part's leave idle (the last wave of its PCG, its shorter stages).
+ * Errors: INVALID_ARG. */
 int gato_set_parts(gato_handle* h, int parts);
 
-/* The number of parts the next gato_solve_kkt or gato_solve_kkt_host call on
- * this handle runs (the setting resolved for the handle's M) into *parts.
+/* The number of parts the last gato_solve_kkt or gato_solve_kkt_host call on
+ * this handle ran into *parts; before any such call, the number a
+ * gato_solve_kkt call with the default parameters would run.
  * Errors: INVALID_ARG. */
 int gato_get_parts(const gato_handle* h, int* parts);
 

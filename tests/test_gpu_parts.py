@@ -68,19 +68,28 @@ def test_parts_equal_one_part(parts):
 
 
 def test_default_parts_at_the_benchmark_batch():
-    """256 solves run as four parts by default; a sample against the oracle
-    and every output against the one-part run."""
+    """256 solves: four parts by default, two on device buffers with the
+    workload's direct corrections (their factorisation runs beside the PCG),
+    four from host buffers; a sample against the oracle and every output
+    against the one-part run."""
     w = WORKLOADS[4]
     prob = make_batch(w)
     p = params_for(w)
+    assert p.refine_solver == gato.GATO_REFINE_SOLVER_DIRECT
     with gato.Solver(w.M, w.N, w.n, w.m) as s:
         s.set_parts(0)
-        assert s.get_parts() == 4
+        assert s.get_parts() == 4  # no call yet: the default parameters
         ref = device_solve(s, p, prob, 1)
+        assert s.get_parts() == 1
         dev = device_solve(s, p, prob, 0)
+        assert s.get_parts() == 2
+        pcg_corr = device_solve(s, params_for(w, refine_solver=0), prob, 0)
+        assert s.get_parts() == 4
         host = host_solve(s, p, prob, 0)
+        assert s.get_parts() == 4
     same(dev, ref)
     same(host, ref)
+    assert not pcg_corr["status"].any()
     assert not ref["status"].any()
     check_solution(prob, dev, [0, 63, 64, 191, 255], w.n_alpha, w.beta, w.mu)
 
@@ -168,7 +177,6 @@ def test_call_in_parts_allocates_nothing_and_can_be_captured():
         assert torch.cuda.mem_get_info()[0] == free0
         same({k: v.cpu().numpy() for k, v in out.items()}, ref)
         s.set_parts(0)
-        assert s.get_parts() == 4
         cap = s.outputs(p.n_alpha)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, capture_error_mode="thread_local"):
@@ -176,6 +184,7 @@ def test_call_in_parts_allocates_nothing_and_can_be_captured():
                         cap["best"], cap["status"])
         g.replay()
         torch.cuda.synchronize()
+        assert s.get_parts() == 2  # 128 solves, direct corrections
         same({k: v.cpu().numpy() for k, v in cap.items()}, ref)
 
 

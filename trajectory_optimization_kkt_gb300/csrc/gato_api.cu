@@ -594,11 +594,12 @@ int gato_solve_kkt(gato_handle* h, const gato_params* p, const float* Q, const f
     if (h->w.N > 1 && !dU) return GATO_ERR_INVALID_ARG;
     if (!gato::sizes_supported(h->w, p, h->smem_optin)) return GATO_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
-    if (gato::parts_for(h) > 1) {
+    if (gato::parts_for(h, p, false) > 1) {
         h->ev_used[0] = 0;  // no stage timing for a call in parts
         return gato::run_parts(h, p, Q, R, q, r, A, B, e, s0, dX, dU, lambda, iters, merit,
                                best, status, st, false);
     }
+    h->parts_last = 1;
     begin_timing(h, st);
     return unsupported_or_fail(gato::run_solve_kkt(h, p, Q, R, q, r, A, B, e, s0, dX, dU,
                                                    lambda, iters, merit, best, status, st));

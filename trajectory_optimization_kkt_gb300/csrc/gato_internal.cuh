@@ -135,6 +135,7 @@ struct gato_handle {
     // sub-batch handles and (host entry only) staging buffers of the current
     // one
     int parts;
+    int parts_last;  // parts the last gato_solve_kkt / _host call ran (0: none yet)
     struct gato_parts* pipe;
 };
 
@@ -143,7 +144,7 @@ namespace gato {
 size_t parts_extra_bytes();       // allocation beyond the handle's own workspace
 int parts_init(gato_handle* h);   // streams and events of the parts (gato_create)
 void parts_free(gato_handle* h);  // releases h->pipe
-int parts_for(const gato_handle* h);
+int parts_for(const gato_handle* h, const gato_params* p, bool host);
 // a stream of the device's lowest priority (work that fills idle SMs) or
 // highest (the solve's own stages), and the two fork/join events
 cudaError_t side_stream_create(cudaStream_t* st, cudaEvent_t* fork, cudaEvent_t* join);

@@ -188,14 +188,25 @@ int parts_init(gato_handle* h)
     return GATO_OK;
 }
 
-// the caller's choice (capped at M), else by batch size: one part below 64
-// solves, two below 128, four from there (measured at N = 128: two parts
-// gain 3-4% at 64-96 solves, four 1-4% from 128; below 64 one is best)
-int parts_for(const gato_handle* h)
+// The caller's choice (capped at M), else by batch size and call: one part
+// below 64 solves, two below 128, four from there (measured at N = 128 with
+// PCG corrections: two parts gain 3-4% at 64-96 solves, four 1-4% from 128;
+// below 64 one is best).  A call on device buffers whose corrections are
+// direct after a PCG main solve already overlaps its longest short stage
+// (the factorisation, on the side stream) with the PCG, and fewer parts do
+// better there: one below 128 solves, two from 128 (measured: 64 solves of
+// N = 64 2.70 against 2.75 ms in two parts; 256 of N = 128 1.91 against
+// 1.93 ms in four; 128 of N = 16, n = 36 3.69 against 3.71 ms in four).  The
+// host entry keeps the first rule: its parts also hide the input copies.
+int parts_for(const gato_handle* h, const gato_params* p, bool host)
 {
     const int M = h->w.M;
     int k = h->parts;
-    if (k <= 0) k = M >= 128 ? 4 : (M >= 64 ? 2 : 1);
+    if (k <= 0) {
+        const bool forked = !host && p && p->refine_solver == GATO_REFINE_SOLVER_DIRECT &&
+                            p->refine_steps > 0 && linsys_for(p, h->w.N) == GATO_LINSYS_PCG;
+        k = forked ? (M >= 128 ? 2 : 1) : (M >= 128 ? 4 : (M >= 64 ? 2 : 1));
+    }
     if (k > M) k = M;
     return k;
 }
@@ -212,7 +223,8 @@ int run_parts(gato_handle* h, const gato_params* p, const float* Q, const float*
               const float* s0, float* dX, float* dU, float* lambda, int32_t* iters, float* merit,
               int32_t* best, uint32_t* status, cudaStream_t user, bool host)
 {
-    const int k = parts_for(h);
+    const int k = parts_for(h, p, host);
+    h->parts_last = k;
     gato_parts* pp = h->pipe;
     if (!pp || k > pp->nstreams) return GATO_ERR_INVALID_ARG;
     if (pp->count_parts != k || pp->small_first != (host ? 1 : 0)) partition(h, k, host);
@@ -309,7 +321,7 @@ int gato_set_parts(gato_handle* h, int parts)
 int gato_get_parts(const gato_handle* h, int* parts)
 {
     if (!h || !parts) return GATO_ERR_INVALID_ARG;
-    *parts = gato::parts_for(h);
+    *parts = h->parts_last > 0 ? h->parts_last : gato::parts_for(h, nullptr, false);
     return GATO_OK;
 }
 
