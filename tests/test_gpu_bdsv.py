@@ -91,6 +91,8 @@ SIZES = [
     ("N17_n12_m6", 2, 17, 12, 6),
     ("N37_n13_m5", 3, 37, 13, 5),
     ("N64_n17_m4_smem", 2, 64, 17, 4),
+    ("N20_n24_m8_smem", 2, 20, 24, 8),  # the substitution's rows unrolled to 24
+    ("N11_n30_m10_smem", 2, 11, 30, 10),  # ... and to 36, predicated
     ("N33_n36_m12_smem", 2, 33, 36, 12),
     ("N6_n64_m8_smem", 1, 6, 64, 8),
     ("N129_n14_m7", 2, 129, 14, 7),
@@ -108,8 +110,10 @@ def test_direct_solve_sizes(name, M, N, n, m, order):
     check_solution(prob, out, range(M))
 
 
-@pytest.mark.parametrize("name,M,N,n,m", [SIZES[i] for i in (3, 4, 7, 11)],
-                         ids=[SIZES[i][0] for i in (3, 4, 7, 11)])
+REG_SIZES = [c for c in SIZES if c[0] in ("N5_n14_m7", "N8_n16_m8", "N37_n13_m5", "N129_n14_m7")]
+
+
+@pytest.mark.parametrize("name,M,N,n,m", REG_SIZES, ids=[c[0] for c in REG_SIZES])
 def test_register_and_shared_kernels_agree(name, M, N, n, m):
     prob = random_lq(M, N, n, m, seed=800 + N)
     p = gato.default_params(linsys=CR, refine_steps=1)

@@ -604,13 +604,20 @@ cudaError_t launch_bdsv_solve(gato_handle* h, int order, int set, float* lambda,
                       : w.n <= 12 ? k_bdsv_chrono_solve<12>
                       : w.n <= 14 ? k_bdsv_chrono_solve<14>
                       : w.n <= NP ? k_bdsv_chrono_solve<NP>
+                      : w.n <= 24 ? k_bdsv_chrono_solve<24>
+                      : w.n <= 36 ? k_bdsv_chrono_solve<36>
                                   : k_bdsv_chrono_solve<0>;
         return launch(kernel, M, kChronoSolveThreads, smem, st, a);
     }
+    // beyond 16 the rows are unrolled to 24 and 36 as well (the row products
+    // of a substitution level are dependent global loads: unrolled, a row's
+    // loads are all in flight at once; looped, they follow one another)
     auto kernel = w.n <= 8    ? k_bdsv_cr_solve<8>
                   : w.n <= 12 ? k_bdsv_cr_solve<12>
                   : w.n <= 14 ? k_bdsv_cr_solve<14>
                   : w.n <= NP ? k_bdsv_cr_solve<NP>
+                  : w.n <= 24 ? k_bdsv_cr_solve<24>
+                  : w.n <= 36 ? k_bdsv_cr_solve<36>
                               : k_bdsv_cr_solve<0>;
     return launch(kernel, M, kSolveThreads, smem, st, a);
 }
