@@ -304,11 +304,43 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
-// dst[0..count) = s * src[0..count), lanes over elements
+// dst[0..count) = s * src[0..count), lanes over elements.  The loads are
+// issued in batches (eight per lane, 128-bit when both ends are 16-byte
+// aligned and count is a multiple of 4) before their stores, so that a
+// matrix copied from global memory costs a few memory latencies rather than
+// one per 32 elements.
 __device__ __forceinline__ void warp_copy(float* dst, const float* src, int count,
                                           float s = 1.f)
 {
-    for (int i = lane_id(); i < count; i += 32) dst[i] = s * src[i];
+    const int lane = lane_id();
+    if ((((uintptr_t)dst | (uintptr_t)src) & 15) == 0 && (count & 3) == 0) {
+        const float4* s4 = reinterpret_cast<const float4*>(src);
+        float4* d4 = reinterpret_cast<float4*>(dst);
+        const int c4 = count >> 2;
+        int i = lane;
+        for (; i + 7 * 32 < c4; i += 8 * 32) {
+            float4 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = s4[i + 32 * k];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                d4[i + 32 * k] = make_float4(s * v[k].x, s * v[k].y, s * v[k].z, s * v[k].w);
+        }
+        for (; i < c4; i += 32) {
+            const float4 v = s4[i];
+            d4[i] = make_float4(s * v.x, s * v.y, s * v.z, s * v.w);
+        }
+        return;
+    }
+    int i = lane;
+    for (; i + 7 * 32 < count; i += 8 * 32) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = src[i + 32 * k];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dst[i + 32 * k] = s * v[k];
+    }
+    for (; i < count; i += 32) dst[i] = s * src[i];
 }
 
 // In-place lower Cholesky a = L L^T of the n x n row-major matrix in shared
