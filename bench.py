@@ -350,7 +350,9 @@ def run_sweep(args, local):
 def run_pcg_kernel_sweep(args, local):
     """PCG-only time of the wide-tile and quad kernels and of the automatic
     choice, n in {8, 10, 12, 14, 16} x N in {16, 32, 64, 128} x M in {16, 152,
-    256, 1024}: gato_pcg_solve after one gato_form_schur (stop rule 0, eps 1e-6),
+    256, 1024}, then of the register-row kernel (its cluster form where one
+    CTA cannot hold a solve) against the generic kernel, n in {24, 36} x N in
+    {16, 32, 64, 128} x M in {16, 128}: gato_pcg_solve after one gato_form_schur (stop rule 0, eps 1e-6),
     L2 flushed before each launch, the median of 6 launches after 2; the
     batch is 16 generated solves (workload 4's generator at these sizes)
     repeated to M, so every solve of a cell takes the iterations of one of
@@ -401,6 +403,41 @@ def run_pcg_kernel_sweep(args, local):
                                      "ran": _kernel_names().get(s.get_stats().pcg_kernel),
                                      "status_nonzero_solves": int((out["status"] != 0).sum())}
                 row["quad_over_wide"] = row["quad"]["us"] / row["wide"]["us"]
+                print(json.dumps(row), flush=True)
+    # n > 16: the register-row kernel (one CTA per solve where its block fits,
+    # else its cluster form) against the generic kernel
+    kinds = {"rows": gato.GATO_PCG_ROWS, "generic": gato.GATO_PCG_GENERIC}
+    for n in (24, 36):
+        for N in (16, 32, 64, 128):
+            w = dataclasses.replace(base, n=n, m=n // 3, N=N)
+            one = make_batch(w, M=16)
+            for M in (16, 128):
+                prob = {k: np.ascontiguousarray(np.concatenate([v] * -(-M // 16))[:M])
+                        for k, v in one.items()}
+                d = {k: torch.from_numpy(v).to(dev) for k, v in prob.items()}
+                p = gato.default_params(pcg_eps=1e-6, pcg_max_iters=4000)
+                row = {"sweep": "pcg_rows", "n": n, "N": N, "M": M}
+                with gato.Solver(M, N, n, n // 3) as s:
+                    out = s.outputs(p.n_alpha)
+                    s.form_schur(d, out["status"], stream)
+                    for name, kind in kinds.items():
+                        s.set_pcg_kernel(kind)
+                        ts = []
+                        for k in range(8):
+                            flush.fill_(float(k))
+                            a = torch.cuda.Event(enable_timing=True)
+                            b = torch.cuda.Event(enable_timing=True)
+                            a.record(stream)
+                            s.pcg_solve(p, out["lam"], out["dX"], out["dU"], out["iters"],
+                                        out["status"], stream=stream)
+                            b.record(stream)
+                            b.synchronize()
+                            if k >= 2:
+                                ts.append(a.elapsed_time(b))
+                        row[name] = {"us": 1000.0 * statistics.median(ts),
+                                     "iters_per_solve": float(out["iters"].float().mean()),
+                                     "status_nonzero_solves": int((out["status"] != 0).sum())}
+                row["generic_over_rows"] = row["generic"]["us"] / row["rows"]["us"]
                 print(json.dumps(row), flush=True)
 
 

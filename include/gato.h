@@ -80,10 +80,11 @@ extern "C" {
 #define GATO_PCG_AUTO 0            /* for 7 <= n <= 16 the wide-tile kernel when
                                       N <= 128 and the cluster kernel (2 or 4
                                       CTAs per solve) when 128 < N <= 512; for
-                                      16 < n <= 64 the register-row kernel when
-                                      its block fits (N ceil(n/R) threads within
-                                      the register budget: N <= 17 at n = 36);
-                                      else the generic kernel                     */
+                                      16 < n <= 64 the register-row kernel, with
+                                      a solve over a cluster of 2, 4 or 8 CTAs
+                                      where one CTA cannot hold it (N ceil(n/R)
+                                      threads beyond the register budget: N > 18
+                                      at n = 36); else the generic kernel         */
 #define GATO_PCG_GENERIC 1         /* always the generic kernel                   */
 #define GATO_PCG_WIDE 2            /* the wide-tile kernel (two threads per
                                       coupling block, rows over all 2H columns)
@@ -92,8 +93,9 @@ extern "C" {
                                       where it applies, else as GATO_PCG_AUTO     */
 #define GATO_PCG_ROWS 4            /* the register-row kernel (whole rows of the
                                       two coupling blocks around a knot per
-                                      thread) for any n <= 64 where its block
-                                      fits, else as GATO_PCG_AUTO                 */
+                                      thread) for any n <= 64, one CTA per solve
+                                      or its cluster form (up to 8 CTAs), else
+                                      as GATO_PCG_AUTO                            */
 #define GATO_PCG_QUAD 5            /* the four-thread kernel with row quarters
                                       over all n columns (7 <= n <= 16,
                                       N <= 128; column sums reduced by warp

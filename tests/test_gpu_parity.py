@@ -392,10 +392,15 @@ ROWS = [
     ("n17_m5", 3, 9, 17, 5), ("n20_m20", 2, 10, 20, 20), ("n24_m8", 2, 12, 24, 8),
     ("n27_m9", 2, 11, 27, 9), ("n32_m4", 2, 8, 32, 4), ("n36_m12", 2, 16, 36, 12),
     ("n40_m10", 1, 6, 40, 10), ("n45_m7", 1, 5, 45, 7), ("n53_m3", 1, 4, 53, 3),
-    ("n64_m16", 1, 4, 64, 16), ("N1_n36", 2, 1, 36, 12), ("n36_N40_generic", 1, 40, 36, 12),
+    ("n64_m16", 1, 4, 64, 16), ("N1_n36", 2, 1, 36, 12),
     # the largest blocks the register budget allows, and one knot past them
-    ("n36_N18_max", 1, 18, 36, 12), ("n36_N19_generic", 1, 19, 36, 12),
+    # (the cluster form: a solve's knots over 2, 4 or 8 CTAs)
+    ("n36_N18_max", 1, 18, 36, 12), ("n36_N19_cluster2", 1, 19, 36, 12),
     ("n24_N42_max", 1, 42, 24, 8), ("n64_N5_max", 1, 5, 64, 8),
+    ("n36_N40_cluster4", 1, 40, 36, 12), ("n36_N32_cluster2", 2, 32, 36, 12),
+    ("n36_N37_cluster4_ragged", 2, 37, 36, 12), ("n24_N64_cluster2", 2, 64, 24, 8),
+    ("n17_N100_cluster2", 1, 100, 17, 5), ("n64_N12_cluster4", 1, 12, 64, 8),
+    ("n36_N128_cluster8", 1, 128, 36, 12),
 ]
 
 
@@ -433,6 +438,35 @@ def test_rows_kernel_stopping_rules(rule):
         lam = oracle.direct_solve(oracle.solve_one(prob, j))[2]
         assert rel(a["lam"][j], lam) <= 2 * rel(b["lam"][j], lam) + 1e-5
     assert np.abs(a["iters"] - b["iters"]).max() <= 0.15 * b["iters"].max() + 2
+
+
+@pytest.mark.parametrize("rule", [gato.GATO_STOP_RESIDUAL, gato.GATO_STOP_PRECOND,
+                                  gato.GATO_STOP_SCALED], ids=["residual", "precond", "scaled"])
+def test_rows_cluster_form_stopping_rules_and_warm_start(rule):
+    """The cluster form (n = 36, N = 32: two CTAs of 16 knots) under each
+    stopping rule, against the oracle and the generic kernel, and warm-started
+    from half the solution."""
+    prob = random_lq(2, 32, 36, 12, seed=831)
+    p = gato.default_params(pcg_max_iters=5000, refine_steps=1, stop_rule=rule)
+    out = solve(prob, p)
+    ref = solve(prob, p, gato.GATO_PCG_GENERIC)
+    assert not out["status"].any() and not ref["status"].any()
+    check_solution(prob, out, range(2))
+    assert np.abs(out["iters"] - ref["iters"]).max() <= 0.05 * ref["iters"].max() + 2
+    lam = np.stack([oracle.direct_solve(oracle.solve_one(prob, j))[2] for j in range(2)])
+    d = gato.to_device(prob)
+    with gato.Solver(2, 32, 36, 12) as s:
+        o = s.outputs(p.n_alpha)
+        s.form_schur(d, o["status"])
+        q = gato.default_params(pcg_max_iters=5000, stop_rule=rule)
+        s.pcg_solve(q, o["lam"], o["dX"], o["dU"], o["iters"], o["status"])
+        cold = o["iters"].cpu().numpy().copy()
+        s.pcg_solve(q, o["lam"], o["dX"], o["dU"], o["iters"], o["status"],
+                    lambda0=torch.tensor(0.5 * lam, dtype=torch.float32, device="cuda"))
+        torch.cuda.synchronize()
+        assert not o["status"].cpu().numpy().any()
+        assert (o["iters"].cpu().numpy() <= cold).all()
+        assert s.get_stats().pcg_kernel == gato.GATO_PCG_ROWS
 
 
 def test_rows_kernel_chosen_for_small_states():

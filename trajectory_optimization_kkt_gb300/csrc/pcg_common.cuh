@@ -109,8 +109,9 @@ __device__ __forceinline__ void finish(const PcgArgs& g, int sol, int it, bool d
 }
 
 // lambda = L^-T lambda_hat for this CTA's knots, then (after a cluster
-// barrier, with the neighbours' lambda in global memory) dz by eq. (4)
-template <typename LhatFn>
+// barrier, with the neighbours' lambda in global memory) dz by eq. (4); the
+// dot products unrolled to NPX >= n (0: loops for any n)
+template <int NPX = 16, typename LhatFn>
 __device__ __forceinline__ void cluster_recover(cg::cluster_group& cl, const PcgArgs& g, int sol,
                                                 int k0, int nk, LhatFn lhat)
 {
@@ -121,7 +122,7 @@ __device__ __forceinline__ void cluster_recover(cg::cluster_group& cl, const Pcg
     const float* gLi = w.Linv + sol * w.sNnn;
     for (int i = tid; i < nk * n; i += T) {
         const int jl = i / n, a = i - jl * n, j = k0 + jl;
-        lam[(size_t)j * n + a] = strided_dot<16>(gLi + (size_t)j * n * n + a, n,
+        lam[(size_t)j * n + a] = strided_dot<NPX>(gLi + (size_t)j * n * n + a, n,
                                                  [&](int b) { return lhat(jl, b); }, a, n);
     }
     cl.sync();
@@ -132,9 +133,9 @@ __device__ __forceinline__ void cluster_recover(cg::cluster_group& cl, const Pcg
     for (int i = tid; i < nk * n; i += T) {
         const int kl = i / n, a = i - kl * n, k = k0 + kl;
         float x = av[(size_t)k * n + a];
-        x += strided_dot<16>(Qi + (size_t)k * n * n + a * n, 1, at(lam + (size_t)k * n), 0, n);
+        x += strided_dot<NPX>(Qi + (size_t)k * n * n + a * n, 1, at(lam + (size_t)k * n), 0, n);
         if (k < N - 1)
-            x += strided_dot<16>(Ob + (size_t)k * n * n + a, n, at(lam + (size_t)(k + 1) * n), 0,
+            x += strided_dot<NPX>(Ob + (size_t)k * n * n + a, n, at(lam + (size_t)(k + 1) * n), 0,
                                  n);
         g.dX[(size_t)sol * Nn + (size_t)k * n + a] = x;
     }
@@ -143,7 +144,7 @@ __device__ __forceinline__ void cluster_recover(cg::cluster_group& cl, const Pcg
     const float* bv = g.rhs.bvec + sol * w.sKm;
     for (int t = tid; t < ku * m; t += T) {
         const int kl = t / m, c = t - kl * m, k = k0 + kl;
-        const float u = strided_dot<16>(Vb + (size_t)k * n * m + c, m,
+        const float u = strided_dot<NPX>(Vb + (size_t)k * n * m + c, m,
                                         at(lam + (size_t)(k + 1) * n), 0, n);
         g.dU[(size_t)sol * (N - 1) * m + (size_t)k * m + c] = bv[(size_t)k * m + c] - u;
     }

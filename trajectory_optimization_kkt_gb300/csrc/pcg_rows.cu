@@ -409,6 +409,365 @@ __global__ void __launch_bounds__(max_threads_for(NP, R)) k_pcg_rows(PcgArgs g)
     finish(g, sol, it, done, nonfinite);
 }
 
+// ===========================================================================
+// cluster form: one solve over the C CTAs of a thread-block cluster
+// ===========================================================================
+//
+// k_pcg_rows_cluster<NP, R> runs the same iteration with a solve's knots
+// split over the CTAs of a cluster (C = 2, 4 or 8, the cluster's size at
+// launch): CTA c owns knots c Nc .. c Nc + Nc - 1 (Nc = ceil(N / C)) with
+// their rows of the two coupling blocks, exactly as k_pcg_rows does for a
+// whole solve.  A CTA's vectors keep the same guard slots, which here hold
+// the neighbouring CTAs' boundary knots: the owners of a CTA's first and
+// last knot also write their rows into the previous and next CTA's guards
+// (distributed shared memory).  Block sums add every CTA's warp slots in rank
+// order, so all CTAs hold the same scalars and take the same branches; every
+// barrier is a cluster barrier.  The recovery is cluster_recover's.
+
+// the sums of post2's slots of every CTA, in rank order
+__device__ __forceinline__ float2 rows_cluster_collect2(cg::cluster_group& cl, float2* buf)
+{
+    float2 s = make_float2(0.f, 0.f);
+    const int C = (int)cl.num_blocks();
+    for (int rk = 0; rk < C; ++rk) {
+        const float2 v = collect2(cl.map_shared_rank(buf, rk));
+        s.x += v.x;
+        s.y += v.y;
+    }
+    return s;
+}
+
+// block_sum over the whole cluster: warp sums to this CTA's slots, a cluster
+// barrier, then every thread adds all CTAs' slots in rank order
+template <int K>
+__device__ __forceinline__ void rows_cluster_sum(cg::cluster_group& cl, float (&v)[K],
+                                                 float4* buf)
+{
+#pragma unroll
+    for (int k = 0; k < K; ++k) v[k] = warp_sum(v[k]);
+    const int wi = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (lane_id() == 0)
+        buf[wi] = make_float4(v[0], K > 1 ? v[K > 1 ? 1 : 0] : 0.f,
+                              K > 2 ? v[K > 2 ? 2 : 0] : 0.f, 0.f);
+    cl.sync();
+    float s[3] = {0.f, 0.f, 0.f};
+    const int C = (int)cl.num_blocks();
+    for (int rk = 0; rk < C; ++rk) {
+        const float4* b = cl.map_shared_rank(buf, rk);
+        for (int q = 0; q < nw; ++q) {
+            const float4 t = b[q];
+            s[0] += t.x;
+            s[1] += t.y;
+            s[2] += t.z;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) v[k] = s[k];
+}
+
+template <int NP, int R>
+__global__ void __launch_bounds__(max_threads_for(NP, R)) k_pcg_rows_cluster(PcgArgs g)
+{
+    extern __shared__ __align__(16) float sm[];
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank(), C = (int)cl.num_blocks();
+    const Work& w = g.w;
+    const int N = w.N, n = w.n, T = blockDim.x, tid = threadIdx.x;
+    const int sol = blockIdx.x / C;
+    const int Nc = (N + C - 1) / C;
+    const int k0 = rank * Nc;         // first knot of this CTA
+    const int nk = min(Nc, N - k0);   // its knot count (>= 1 by the launch)
+    const int TPK = (n + R - 1) / R;
+    const int XS = (Nc + 2) * NP;     // one vector with its guard knots
+    const bool rule0 = g.rule == GATO_STOP_RESIDUAL;
+
+    float* XP = sm;
+    float* XR = XP + XS;
+    float4* redA = reinterpret_cast<float4*>(XR + XS);
+    float4* redB = redA + 32;
+    float4* redC = redA + 64;
+    float2* pairA = reinterpret_cast<float2*>(redA + 96);
+    float2* pairB = pairA + 16;
+    float2* pairC = pairB + 16;
+    constexpr int SC = NP / 4 - RowTiles<NP, R>::RC;
+    float4* TS = redA + 120;
+    float* LS = reinterpret_cast<float*>(TS + (size_t)SC * R * 2 * T);
+    const bool l_staged = rule0 && g.l_smem;
+    // the layout is the same in every CTA, so they all leave together
+    if (!gb_smem((size_t)(LS - sm + (l_staged ? (size_t)Nc * n * NP : 0)) * sizeof(float),
+                 w.status, sol)) {
+        if (rank == 0) finish(g, sol, 0, false, false);
+        return;
+    }
+    for (int i = tid; i < 2 * XS; i += T) sm[i] = 0.f;
+
+    const int jl = tid / TPK, q = tid - jl * TPK;
+    const int a0 = q * R;
+    const bool owner = jl < nk && gb_ok((long long)(jl + 2) * NP + NP - 1, XS, w.status, sol) &&
+                       gb_ok(a0, n, w.status, sol);
+    bool valid[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) valid[i] = owner && a0 + i < n;
+    const int jjl = owner ? jl : 0;  // a safe local knot for threads past the last one
+    const int jj = k0 + jjl;         // its global index
+    // the neighbours' guard slots this thread also writes: the previous CTA's
+    // slot after its last knot (Nc + 1) for the CTA's first knot, the next
+    // CTA's slot 0 for its last knot
+    float* prevXP = (owner && jl == 0 && rank > 0) ? cl.map_shared_rank(XP, rank - 1) : nullptr;
+    float* prevXR = prevXP ? cl.map_shared_rank(XR, rank - 1) : nullptr;
+    float* nextXP = (owner && jl == nk - 1 && rank + 1 < C) ? cl.map_shared_rank(XP, rank + 1)
+                                                             : nullptr;
+    float* nextXR = nextXP ? cl.map_shared_rank(XR, rank + 1) : nullptr;
+    auto store = [&](float* X, float* Xprev, float* Xnext, const float(&v)[R]) {
+        rows_store<NP, R>(X, jjl, a0, valid, v);
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            if (!valid[i]) continue;
+            if (Xprev) Xprev[(Nc + 1) * NP + a0 + i] = v[i];
+            if (Xnext) Xnext[a0 + i] = v[i];
+        }
+    };
+
+    RowTiles<NP, R> tile;
+    {
+        const float* nh = w.Nh + sol * w.sKnn;
+        const size_t nn = (size_t)n * n;
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int a = a0 + i;
+            const bool has_lo = valid[i] && jj >= 1;
+            const bool has_up = valid[i] && jj + 1 < N;
+            const float* lo = nh + (size_t)(jj >= 1 ? jj - 1 : 0) * nn + (size_t)a * n;
+            const float* up = nh + (size_t)(jj + 1 < N ? jj : 0) * nn + a;
+#pragma unroll
+            for (int b = 0; b < 4 * RowTiles<NP, R>::RC; ++b) {
+                tile.lo[i][b] = (has_lo && b < n) ? lo[b] : 0.f;
+                tile.up[i][b] = (has_up && b < n) ? up[(size_t)b * n] : 0.f;
+            }
+#pragma unroll
+            for (int sc = 0; sc < SC; ++sc) {
+                float vl[4], vu[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int b = 4 * (RowTiles<NP, R>::RC + sc) + e;
+                    vl[e] = (has_lo && b < n) ? lo[b] : 0.f;
+                    vu[e] = (has_up && b < n) ? up[(size_t)b * n] : 0.f;
+                }
+                TS[ts_index<R>(sc, i, 0, tid, T)] = make_float4(vl[0], vl[1], vl[2], vl[3]);
+                TS[ts_index<R>(sc, i, 1, tid, T)] = make_float4(vu[0], vu[1], vu[2], vu[3]);
+            }
+        }
+    }
+    const float dl = owner ? w.dlow[sol * w.sN + jj] : 0.f;
+    const float* ghat = g.rhs.ghat + sol * w.sNn;
+    const float* gam = g.rhs.gamma + sol * w.sNn;
+    const float* gL = w.L + sol * w.sNnn;
+    const float* Lj = gL + (size_t)jj * n * n;
+    if (l_staged) {  // this CTA's knots' rows of L, padded to NP
+        const float* gLc = gL + (size_t)k0 * n * n;
+        for (int t = tid; t < nk * n * NP; t += T) {
+            const int row = t / NP, b = t - row * NP;
+            LS[t] = b < n ? gLc[(size_t)row * n + b] : 0.f;
+        }
+    }
+
+    float lam[R], r[R], p[R], y[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        lam[i] = 0.f;
+        if (valid[i] && g.lambda0) {
+            const int a = a0 + i;
+            const float* l0 = g.lambda0 + (size_t)sol * N * n + (size_t)jj * n;
+            float x = 0.f;
+            for (int b = a; b < n; ++b) x += Lj[(size_t)b * n + a] * l0[b];
+            lam[i] = x;
+        }
+    }
+    cl.sync();  // every CTA's vectors zeroed before any guard is written
+    store(XP, prevXP, nextXP, lam);
+    cl.sync();
+    rows_matvec<NP, R>(tile, TS, XP, jjl, y);
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+        r[i] = valid[i] ? ghat[jj * n + a0 + i] - lam[i] - y[i] : 0.f;
+    store(XR, prevXR, nextXR, r);
+    cl.sync();
+    rows_matvec<NP, R>(tile, TS, XR, jjl, y);
+    float red3[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        p[i] = r[i] - y[i];
+        red3[0] = fmaf(r[i], p[i], red3[0]);
+        if (valid[i]) {
+            const int gi = jj * n + a0 + i;
+            if (rule0)
+                red3[2] = fmaf(gam[gi], gam[gi], red3[2]);
+            else if (g.rule == GATO_STOP_SCALED) {
+                red3[1] = fmaf(r[i], r[i], red3[1]);
+                red3[2] = fmaf(ghat[gi], ghat[gi], red3[2]);
+            }
+        }
+    }
+    if (rule0)
+        red3[1] = l_staged ? rows_lnorm_smem<NP, R>(LS, XR, jjl, a0, n, valid)
+                           : rows_lnorm<NP, R>(Lj, XR, jjl, a0, n, valid);
+    store(XP, prevXP, nextXP, p);
+    rows_cluster_sum<3>(cl, red3, redA);  // also orders the p stores before the first product
+    float eta = red3[0];
+    const float ref = g.rule == GATO_STOP_PRECOND ? eta : red3[2];
+    const float thr = g.eps * g.eps * ref;
+    bool done = (g.rule == GATO_STOP_PRECOND ? eta : red3[1]) <= thr;
+    bool nonfinite = !isfinite(eta) || !isfinite(red3[1]);
+    bool exact_next = false;
+    if (rule0) {
+        float lb = 0.f;
+#pragma unroll
+        for (int i = 0; i < R; ++i) lb = fmaf(dl * r[i], r[i], lb);
+        float lv[1] = {lb};
+        rows_cluster_sum<1>(cl, lv, redB);
+        exact_next = lv[0] <= 1.25f * thr;
+    }
+    cl.sync();
+
+    int it = 0;
+    while (!done && !nonfinite && it < g.max_iters) {
+        ++it;
+        rows_matvec<NP, R>(tile, TS, XP, jjl, y);
+        float pvp = 0.f;
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            y[i] += p[i];
+            pvp = fmaf(p[i], y[i], pvp);
+        }
+        post2(pvp, 0.f, pairA);
+        cl.sync();
+        const float pv = rows_cluster_collect2(cl, pairA).x;
+        const float alpha = __fdividef(eta, pv);
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            lam[i] = fmaf(alpha, p[i], lam[i]);
+            r[i] = fmaf(-alpha, y[i], r[i]);
+        }
+        store(XR, prevXR, nextXR, r);
+        cl.sync();
+        rows_matvec<NP, R>(tile, TS, XR, jjl, y);
+        float red[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            y[i] = r[i] - y[i];
+            red[0] = fmaf(r[i], y[i], red[0]);
+            red[1] = fmaf(r[i], r[i], red[1]);
+        }
+        if (rule0) red[1] *= dl;
+        const bool exact = exact_next;
+        if (exact)
+            red[2] = l_staged ? rows_lnorm_smem<NP, R>(LS, XR, jjl, a0, n, valid)
+                              : rows_lnorm<NP, R>(Lj, XR, jjl, a0, n, valid);
+        post2(red[0], red[1], pairB);
+        if (exact) post2(red[2], 0.f, pairC);
+        cl.sync();
+        {
+            const float2 sb = rows_cluster_collect2(cl, pairB);
+            red[0] = sb.x;
+            red[1] = sb.y;
+            red[2] = exact ? rows_cluster_collect2(cl, pairC).x : 0.f;
+        }
+        const float eta_new = red[0];
+        float lsq = red[2];
+        bool have_exact = exact;
+        if (rule0 && !exact && red[1] * 0.999f <= thr) {
+            float lv[1] = {l_staged ? rows_lnorm_smem<NP, R>(LS, XR, jjl, a0, n, valid)
+                                    : rows_lnorm<NP, R>(Lj, XR, jjl, a0, n, valid)};
+            rows_cluster_sum<1>(cl, lv, redC);
+            lsq = lv[0];
+            have_exact = true;
+        }
+        const float stopq = rule0 ? lsq : (g.rule == GATO_STOP_SCALED ? red[1] : eta_new);
+        if (!isfinite(eta_new + pv + stopq + red[1])) {  // NaN and Inf propagate
+            nonfinite = true;
+            break;
+        }
+        done = (!rule0 || have_exact) && stopq <= thr;
+        if (done) break;
+        exact_next = rule0 && red[1] <= 1.25f * thr;
+        const float beta = __fdividef(eta_new, eta);
+#pragma unroll
+        for (int i = 0; i < R; ++i) p[i] = fmaf(beta, p[i], y[i]);
+        store(XP, prevXP, nextXP, p);
+        eta = eta_new;
+        cl.sync();
+    }
+    cl.sync();
+    rows_store<NP, R>(XP, jjl, a0, valid, lam);
+    cl.sync();
+    cluster_recover<NP>(cl, g, sol, k0, nk, [&](int kl, int b) { return XP[(kl + 1) * NP + b]; });
+    if (rank == 0) finish(g, sol, it, done, nonfinite);
+    cl.sync();  // no CTA leaves while another may still read its shared memory
+}
+
+// one solve per cluster of C CTAs (grid M C); cudaErrorInvalidConfiguration
+// when no such cluster fits on the device
+template <typename K>
+cudaError_t launch_rows_cluster_k(K kernel, const PcgArgs& a, int C, int T, size_t smem,
+                                  cudaStream_t st)
+{
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (C > 8) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.w.M * C), 1, 1);
+    cfg.blockDim = dim3((unsigned)T, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+    if (e != cudaSuccess || clusters < 1) {
+        cudaGetLastError();
+        return cudaErrorInvalidConfiguration;
+    }
+    e = cudaLaunchKernelEx(&cfg, kernel, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+// the cluster form where one CTA cannot hold the solve: the smallest C in
+// {2, 4, 8} whose Nc = ceil(N / C) knots fit a CTA and leave every CTA at
+// least one knot
+template <int NP, int R>
+cudaError_t launch_rows_cluster_np(const PcgArgs& a, size_t limit, cudaStream_t st)
+{
+    const Work& w = a.w;
+    const int TPK = (w.n + R - 1) / R;
+    for (int C = 2; C <= 8; C *= 2) {
+        const int Nc = (w.N + C - 1) / C;
+        if ((C - 1) * Nc >= w.N) break;  // a CTA would hold no knot
+        int T = ((Nc * TPK + 31) / 32) * 32;
+        if (T < 64) T = 64;
+        if (T > max_threads_for(NP, R)) continue;
+        constexpr int SC = NP / 4 - RowTiles<NP, R>::RC;
+        size_t smem = sizeof(float) * 2 * (size_t)(Nc + 2) * NP +
+                      (120 + (size_t)SC * R * 2 * T) * sizeof(float4);
+        if (smem > limit) return cudaErrorInvalidConfiguration;
+        PcgArgs b = a;
+        const size_t l_bytes = sizeof(float) * (size_t)Nc * w.n * NP;
+        b.l_smem = a.rule == GATO_STOP_RESIDUAL && smem + l_bytes <= limit;
+        if (b.l_smem) smem += l_bytes;
+        return launch_rows_cluster_k(k_pcg_rows_cluster<NP, R>, b, C, T, smem, st);
+    }
+    return cudaErrorInvalidConfiguration;
+}
+
 template <int NP, int R = rows_for(NP)>
 cudaError_t launch_rows_np(const PcgArgs& a, size_t limit, cudaStream_t st)
 {
@@ -416,7 +775,7 @@ cudaError_t launch_rows_np(const PcgArgs& a, size_t limit, cudaStream_t st)
     const int TPK = (w.n + R - 1) / R;
     int T = ((w.N * TPK + 31) / 32) * 32;
     if (T < 64) T = 64;
-    if (T > max_threads_for(NP, R)) return cudaErrorInvalidConfiguration;
+    if (T > max_threads_for(NP, R)) return launch_rows_cluster_np<NP, R>(a, limit, st);
     constexpr int SC = NP / 4 - RowTiles<NP, R>::RC;
     size_t smem = sizeof(float) * (2 * (size_t)(w.N + 2) * NP + round4((size_t)w.N * w.n)) +
                   (120 + (size_t)SC * R * 2 * T) * sizeof(float4);
