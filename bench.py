@@ -37,8 +37,8 @@ WORKLOAD_INDEX = 4  # M=256, N=128, n=14, m=7
 # solve launch at this workload, from an ncu capture; valid only for the
 # kernel source it was taken on (sha256 prefix of csrc/pcg.cu), null
 # otherwise.  Captured on 152 solves (one block per SM) and scaled
-# by the solves processed to the 256-solve launch (89.70 MB x 256 / 152).
-PCG_TRAFFIC = {"pcg_sha": "e4383d03ee4f9796", "bytes_per_launch": 151081175}
+# by the solves processed to the 256-solve launch (89.81 MB x 256 / 152).
+PCG_TRAFFIC = {"pcg_sha": "64c4297d7876aa67", "bytes_per_launch": 151251482}
 
 FP32_LANES_PER_SM = 128  # FFMA lanes per SM (4 sub-partitions x 32)
 
@@ -741,8 +741,8 @@ def run_gpu(args, world, rank, local):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     _build.build()
     w = WORKLOADS[args.workload]
-    if args.batch:
-        w = w.with_batch(args.batch)
+    if args.batch or args.horizon:
+        w = w.with_batch(args.batch or w.M, args.horizon)
     M = w.M
     from trajectory_optimization_kkt_gb300.replicas import Replica, job_throughput, max_over_ranks
     replica = Replica(world, rank, local)
@@ -887,7 +887,8 @@ def run_gpu(args, world, rank, local):
     # the ncu capture behind the traffic figure is of the default workload
     traffic = (PCG_TRAFFIC["bytes_per_launch"]
                if PCG_TRAFFIC["pcg_sha"] == sha and args.workload == WORKLOAD_INDEX
-               and not args.batch and args.pcg_kernel == "auto" else None)
+               and not args.batch and not args.horizon and args.pcg_kernel == "auto"
+               else None)
 
     # ---- SQP loop on the linear model (context, not the metric) ----
     sqp = None
@@ -1016,6 +1017,9 @@ def main():
     ap.add_argument("--pcg-kernel", default="auto", choices=sorted(PCG_KERNELS),
                     help="the PCG kernel of the timed step (default: the library's "
                          "automatic choice); for comparisons and profiler captures")
+    ap.add_argument("--horizon", type=int, default=None,
+                    help="knots N (default: the workload's); for profiler captures of "
+                         "other horizons")
     ap.add_argument("--batch", type=int, default=None,
                     help="solves per GPU (default: the workload's 256); for profiler "
                          "captures of a smaller case")
