@@ -467,10 +467,12 @@ def run_throughput_sweep(args, local):
                 p = gato.default_params(**w.solver_settings(), linsys=LINSYS["pcg"])
                 ms, stages, iters, bad = _time_solver(torch, s, p, d, out, args.steps, flush,
                                                       stream)
-                # one part: the PCG stage (solve) plus the refinement stage (its
-                # correction solve and small kernels) over the iterations of both;
-                # at M = 1 this is the latency of one iteration of one solve
-                pcg_us_it = (stages["linsys"] + stages["refine"]) / max(iters / M, 1.0)
+                # one part: the PCG stage over the iterations of a solve (with PCG
+                # corrections also the refinement stage, its correction solve and
+                # small kernels, over the iterations of both); at M = 1 this is
+                # the latency of one iteration of one solve
+                pcg_us_it = ((stages["linsys"] + (0.0 if w.refine_solver else stages["refine"]))
+                             / max(iters / M, 1.0))
                 print(json.dumps({"sweep": "throughput", "M": M, "N": N, "n": w.n, "m": w.m,
                                   "parts": _time_solver.last_parts,
                                   "solves_per_s": M / (ms / 1000.0),
