@@ -348,9 +348,11 @@ int gato_linesearch(gato_handle* h, const gato_params* p, const float* Q, const 
  * with the same S (PCG to p->refine_eps on the correction system's relative
  * preconditioned residual, or the direct solve's factors: those of a direct
  * main solve, or with p->refine_solver = GATO_REFINE_SOLVER_DIRECT the
- * cyclic-reduction factorisation formed once after a PCG main solve), and
- * added to dz and lambda; iters then counts the PCG iterations of every solve
- * of the call (a direct correction adds none).  The batch runs as gato_set_parts parts of consecutive solves,
+ * cyclic-reduction factorisation of the same S, formed once beside the PCG
+ * main solve on an internal stream of the lowest priority and joined before
+ * the first correction), and added to dz and lambda; iters then counts the
+ * PCG iterations of every solve of the call (a direct correction adds none).
+ * The batch runs as gato_set_parts parts of consecutive solves,
  * concurrently on internal streams ordered after the work already on `stream`
  * (which waits for them); the outputs do not depend on the part count.  The
  * parts' workspaces are views into the handle's own allocation (nothing is
