@@ -93,6 +93,49 @@ __device__ __forceinline__ float2 collect2(const float2* buf)
     return hi ? make_float2(other, v) : make_float2(v, other);
 }
 
+// Four values at the cost of six exchanges (two post2 calls take ten): the
+// exchange across the halves keeps (a, b) in the low half-warp and (c, d) in
+// the high one, the next across the quarters one value per quarter, three
+// more finish it.  Every value is summed in post2's tree, so a pair of post2
+// slots and one post4 slot hold the same bits.  buf holds up to 16 float4.
+__device__ __forceinline__ void post4(float a, float b, float c, float d, float4* buf)
+{
+    const int lane = lane_id();
+    const bool hi = lane & 16, odd = lane & 8;
+    float k0 = hi ? c : a, k1 = hi ? d : b;
+    k0 += __shfl_xor_sync(0xffffffffu, hi ? a : c, 16);
+    k1 += __shfl_xor_sync(0xffffffffu, hi ? b : d, 16);
+    float keep = odd ? k1 : k0;
+    keep += __shfl_xor_sync(0xffffffffu, odd ? k0 : k1, 8);
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+    float* slot = reinterpret_cast<float*>(buf + (threadIdx.x >> 5));
+    if ((lane & 7) == 0) slot[lane >> 3] = keep;
+}
+
+// The four totals of post4's slots, in collect2's order: the eight lanes of
+// quarter k sum field k, lane q adding warps q and q + 8 (collect2's first
+// level) before the butterfly over the quarter; three independent exchanges
+// then give every lane the other quarters' totals (one shuffle level fewer
+// than collect2).
+__device__ __forceinline__ float4 collect4(const float4* buf)
+{
+    const int lane = lane_id(), q = lane & 7, k = lane >> 3;
+    const int nw = blockDim.x >> 5;
+    const float* f = reinterpret_cast<const float*>(buf);
+    float v = q < nw ? f[4 * q + k] : 0.f;
+    v += q + 8 < nw ? f[4 * (q + 8) + k] : 0.f;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const float v1 = __shfl_xor_sync(0xffffffffu, v, 8);   // field k ^ 1
+    const float v2 = __shfl_xor_sync(0xffffffffu, v, 16);  // field k ^ 2
+    const float v3 = __shfl_xor_sync(0xffffffffu, v, 24);  // field k ^ 3
+    const bool b0 = k & 1, b1 = k & 2;
+    const float lo0 = b0 ? v1 : v, lo1 = b0 ? v : v1;   // fields (k & 2), (k & 2) + 1
+    const float hi0 = b0 ? v3 : v2, hi1 = b0 ? v2 : v3;  // the other pair
+    return b1 ? make_float4(hi0, hi1, lo0, lo1) : make_float4(lo0, lo1, hi0, hi1);
+}
+
 __device__ __forceinline__ void finish(const PcgArgs& g, int sol, int it, bool done,
                                        bool nonfinite)
 {
