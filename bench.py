@@ -35,10 +35,11 @@ WORKLOAD_INDEX = 4  # M=256, N=128, n=14, m=7
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one PCG
 # solve launch at this workload, from an ncu capture; valid only for the
-# kernel source it was taken on (sha256 prefix of csrc/pcg.cu), null
-# otherwise.  Captured on 152 solves (one block per SM) and scaled
-# by the solves processed to the 256-solve launch (89.81 MB x 256 / 152).
-PCG_TRAFFIC = {"pcg_sha": "64c4297d7876aa67", "bytes_per_launch": 151251482}
+# kernel source it was taken on (sha256 prefix of csrc/pcg.cu and
+# csrc/pcg_common.cuh), null otherwise.  Captured on 152 solves (one block
+# per SM) and scaled by the solves processed to the 256-solve launch
+# (89.89 MB x 256 / 152).
+PCG_TRAFFIC = {"pcg_sha": "3397d7b6c65d75c7", "bytes_per_launch": 151397214}
 
 FP32_LANES_PER_SM = 128  # FFMA lanes per SM (4 sub-partitions x 32)
 
@@ -80,14 +81,17 @@ def _peaks():
 
 
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    """Samples SM clocks and throttle reasons with nvidia-smi while running:
+    every 50 ms, the first sample taken before the region it brackets starts
+    (waiting at most two seconds for it)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, interval_ms: int = 50):
         self.index = index
+        self.interval_ms = interval_ms
         self.rows = []
         self.proc = None
 
@@ -95,10 +99,13 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.monotonic()
+            while not self.rows and self.proc.poll() is None and time.monotonic() - t0 < 2.0:
+                time.sleep(0.005)
         except Exception:
             self.proc = None
         return self
@@ -988,7 +995,7 @@ def run_gpu(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gato", choices=["gato", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
