@@ -996,13 +996,37 @@ __global__ void __launch_bounds__(256, 1) k_pcg_wide(PcgArgs g)
 // order, so all CTAs hold the same scalars and take the same branches; every
 // phase barrier is a cluster barrier.
 
+// post2's pair pushed into slot rank * 8 + w of every CTA of the cluster (at
+// most eight warps a CTA and four CTAs: the 32 slots of a buffer), stored
+// before the cluster barrier that publishes it, so that the collect reads
+// only local shared memory; every lane of a half-warp holds its half's total
 template <int C>
-__device__ __forceinline__ float2 cluster_collect2(cg::cluster_group& cl, float2* buf)
+__device__ __forceinline__ void cluster_post2(cg::cluster_group& cl, float a, float b,
+                                              float2* buf)
+{
+    static_assert(C <= 4, "32 slots hold four CTAs of at most eight warps");
+    const int lane = lane_id();
+    const bool hi = lane & 16;
+    float keep = hi ? b : a;
+    keep += __shfl_xor_sync(0xffffffffu, hi ? a : b, 16);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+    const int rk = lane & 15, rank = (int)cl.block_rank();
+    if (rk < C) {
+        float2* dst = rk == rank ? buf : cl.map_shared_rank(buf, rk);
+        reinterpret_cast<float*>(dst + rank * 8 + (int)(threadIdx.x >> 5))[hi ? 1 : 0] = keep;
+    }
+}
+
+// the pushed pairs of every CTA, each CTA's warps in collect2's tree, the
+// CTAs added in rank order (the same bits in every CTA)
+template <int C>
+__device__ __forceinline__ float2 cluster_collect2(const float2* buf)
 {
     float2 s = make_float2(0.f, 0.f);
 #pragma unroll
     for (int rk = 0; rk < C; ++rk) {
-        const float2 v = collect2(cl.map_shared_rank(buf, rk));
+        const float2 v = collect2(buf + rk * 8);
         s.x += v.x;
         s.y += v.y;
     }
@@ -1120,15 +1144,15 @@ __device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
         }
     }
     if (owner) wstore8(XR + xo, r);
-    post2(rr, gg, redB);
+    cluster_post2<C>(cl, rr, gg, redB);
     cl.sync();
     float q = has_tile ? wide_matvec<H>(tile, xrp, r, rs, yc) : 0.f;
     float lsq = 0.f;
     if (rule0 && owner) lsq = lnorm_half<H>(LP, KS, gL + (size_t)k0 * n * n, lsm, XR, jl, half, n,
                                             owner);
-    post2(q, lsq, redC);
+    cluster_post2<C>(cl, q, lsq, redC);
     cl.sync();
-    float2 sB = cluster_collect2<C>(cl, redB), sC = cluster_collect2<C>(cl, redC);
+    float2 sB = cluster_collect2<C>(redB), sC = cluster_collect2<C>(redC);
     float eta = sB.x - 2.f * sC.x;
     const float ref = g.rule == GATO_STOP_PRECOND ? eta : sB.y;
     const float thr = g.eps * g.eps * ref;
@@ -1144,9 +1168,9 @@ __device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
         float lb = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) lb += dl * r[k] * r[k];
-        post2(lb, 0.f, redD);
+        cluster_post2<C>(cl, lb, 0.f, redD);
         cl.sync();
-        exact_next = rule0 && cluster_collect2<C>(cl, redD).x <= 1.25f * thr;
+        exact_next = rule0 && cluster_collect2<C>(redD).x <= 1.25f * thr;
     }
     cl.sync();
 
@@ -1158,10 +1182,10 @@ __device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
         float pp = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) pp = fmaf(p[k], p[k], pp);
-        post2(q, pp, redA);
+        cluster_post2<C>(cl, q, pp, redA);
         cl.sync();
         // B: alpha; lambda and r updates
-        const float2 sA = cluster_collect2<C>(cl, redA);
+        const float2 sA = cluster_collect2<C>(redA);
         const float pv = sA.y + 2.f * sA.x;
         const float alpha = __fdividef(eta, pv);
         if (owner) wide_y(rs, YC0, YC1, xo, y);
@@ -1182,12 +1206,12 @@ __device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
         const bool exact = exact_next;
         if (exact && owner)
             lsq = lnorm_half<H>(LP, KS, gL + (size_t)k0 * n * n, lsm, XR, jl, half, n, owner);
-        post2(q, rr, redB);
-        post2(dl * rr, lsq, redC);
+        cluster_post2<C>(cl, q, rr, redB);
+        cluster_post2<C>(cl, dl * rr, lsq, redC);
         cl.sync();
         // D: eta', convergence, p = z + beta p
-        sB = cluster_collect2<C>(cl, redB);
-        sC = cluster_collect2<C>(cl, redC);
+        sB = cluster_collect2<C>(redB);
+        sC = cluster_collect2<C>(redC);
         const float eta_new = sB.y - 2.f * sB.x;
         float lsq_all = sC.y;
         bool have_exact = exact;
@@ -1195,9 +1219,9 @@ __device__ __forceinline__ void pcg_cluster_solve(const PcgArgs& g)
             lsq = owner ? lnorm_half<H>(LP, KS, gL + (size_t)k0 * n * n, lsm, XR, jl, half, n,
                                         owner)
                         : 0.f;
-            post2(lsq, 0.f, redD);
+            cluster_post2<C>(cl, lsq, 0.f, redD);
             cl.sync();
-            lsq_all = cluster_collect2<C>(cl, redD).x;
+            lsq_all = cluster_collect2<C>(redD).x;
             have_exact = true;
         }
         stopq = g.rule == GATO_STOP_RESIDUAL ? lsq_all

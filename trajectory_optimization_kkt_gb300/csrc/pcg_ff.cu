@@ -376,17 +376,32 @@ __global__ void __launch_bounds__(kFFMaxThreads, 1) k_pcg_ff(PcgArgs g)
 // takes the same branches.
 // ---------------------------------------------------------------------------
 
-// the double-float totals of the C CTAs' warp slots (C nw <= 32 slots)
+// A warp's partial sums go into slot rank * nw + w of every CTA of the cluster
+// (distributed shared memory, stored before the barrier that publishes them),
+// so the collect after it reads only local shared memory: no remote load on
+// the critical path.  Every lane holds the warp's total after the butterfly.
 template <int C>
-__device__ __forceinline__ void ff_collect_cluster(cg::cluster_group& cl, float4* slots,
-                                                   ff& v, float& f1, float& f2)
+__device__ __forceinline__ void ff_post_cluster(cg::cluster_group& cl, ff v, float f1, float f2,
+                                                float4* slots)
+{
+    ff_warp_reduce(v, f1, f2);
+    const int lane = lane_id(), rank = (int)cl.block_rank();
+    if (lane < C) {
+        float4* dst = lane == rank ? slots : cl.map_shared_rank(slots, lane);
+        dst[rank * (int)(blockDim.x >> 5) + (int)(threadIdx.x >> 5)] =
+            make_float4(v.h, v.l, f1, f2);
+    }
+}
+
+// the double-float totals of the C CTAs' warp slots (C nw <= 32 slots), added
+// in rank-major order, the same in every CTA
+template <int C>
+__device__ __forceinline__ void ff_collect_cluster(const float4* slots, ff& v, float& f1,
+                                                   float& f2)
 {
     const int lane = lane_id(), nw = (int)(blockDim.x >> 5);
     float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lane < C * nw) {
-        const float4* rs = cl.map_shared_rank(slots, lane / nw);
-        t = rs[lane % nw];
-    }
+    if (lane < C * nw) t = slots[lane];
     v = ff{t.x, t.y};
     f1 = t.z;
     f2 = t.w;
@@ -512,11 +527,11 @@ __global__ void __launch_bounds__(kFFMaxThreads / C, 1) k_pcg_ff_cluster(PcgArgs
             q_part = r.h * r.h;
         }
     }
-    ff_post(eta_part, ref_part, q_part, slotA);
+    ff_post_cluster<C>(cl, eta_part, ref_part, q_part, slotA);
     cl.sync();
     ff eta;
     float ref, stopq;
-    ff_collect_cluster<C>(cl, slotA, eta, ref, stopq);
+    ff_collect_cluster<C>(slotA, eta, ref, stopq);
     if (rule == GATO_STOP_PRECOND) {
         ref = eta.h;
         stopq = eta.h;
@@ -529,9 +544,9 @@ __global__ void __launch_bounds__(kFFMaxThreads / C, 1) k_pcg_ff_cluster(PcgArgs
     if (rule0) {
         float lb = valid ? dl * r.h * r.h : 0.f, z0 = 0.f;
         ff zf = ff_of(0.f);
-        ff_post(zf, lb, z0, slotC);
+        ff_post_cluster<C>(cl, zf, lb, z0, slotC);
         cl.sync();
-        ff_collect_cluster<C>(cl, slotC, zf, lb, z0);
+        ff_collect_cluster<C>(slotC, zf, lb, z0);
         exact_next = lb <= 1.25f * thr;
     }
     cl.sync();
@@ -545,12 +560,12 @@ __global__ void __launch_bounds__(kFFMaxThreads / C, 1) k_pcg_ff_cluster(PcgArgs
             v = ff_add(p, ff_row<NP>(NB, n, nn, jl, a, PH, PL));
             pv_part = ff_mul(p, v);
         }
-        ff_post(pv_part, 0.f, 0.f, slotA);
+        ff_post_cluster<C>(cl, pv_part, 0.f, 0.f, slotA);
         cl.sync();
         // B: alpha; lambda and r
         ff pv;
         float u1, u2;
-        ff_collect_cluster<C>(cl, slotA, pv, u1, u2);
+        ff_collect_cluster<C>(slotA, pv, u1, u2);
         const ff alpha = ff_div(eta, pv);
         if (valid) {
             lam = ff_add(lam, ff_mul(alpha, p));
@@ -572,19 +587,19 @@ __global__ void __launch_bounds__(kFFMaxThreads / C, 1) k_pcg_ff_cluster(PcgArgs
                 lb_part = r.h * r.h;
             }
         }
-        ff_post(eta_part2, lb_part, lsq_part, slotC);
+        ff_post_cluster<C>(cl, eta_part2, lb_part, lsq_part, slotC);
         cl.sync();
         // D: convergence, beta, p
         ff eta_new;
         float lb, lsq;
-        ff_collect_cluster<C>(cl, slotC, eta_new, lb, lsq);
+        ff_collect_cluster<C>(slotC, eta_new, lb, lsq);
         bool have_exact = exact;
         if (rule0 && !exact && lb * 0.999f <= thr) {
             float part = valid ? ff_lrow_sq(gL + (size_t)j * nn, RH, NP, jl, a, n) : 0.f, z0 = 0.f;
             ff zf = ff_of(0.f);
-            ff_post(zf, part, z0, slotD);
+            ff_post_cluster<C>(cl, zf, part, z0, slotD);
             cl.sync();
-            ff_collect_cluster<C>(cl, slotD, zf, lsq, z0);
+            ff_collect_cluster<C>(slotD, zf, lsq, z0);
             have_exact = true;
         }
         stopq = rule0 ? lsq : (rule == GATO_STOP_SCALED ? lb : eta_new.h);

@@ -34,6 +34,10 @@ namespace {
 // rows per thread: the two tiles (2 R NP floats) within 216 registers
 constexpr int rows_for(int NP) { return 216 / (2 * NP) > 0 ? 216 / (2 * NP) : 1; }
 
+// float4s before the tile chunks in the cluster kernel's shared memory: three
+// block-sum buffers of 32 and three pushed-pair buffers of 64 float2
+constexpr int kRowsClusterHead = 96 + 3 * 32;
+
 // threads per block the registers allow with R rows per thread: 64K
 // registers over the tiles plus about 56 for the rest, in whole warps; with
 // more than one row per thread at most 256 threads, so that no SM
@@ -424,13 +428,34 @@ __global__ void __launch_bounds__(max_threads_for(NP, R)) k_pcg_rows(PcgArgs g)
 // order, so all CTAs hold the same scalars and take the same branches; every
 // barrier is a cluster barrier.  The recovery is cluster_recover's.
 
-// the sums of post2's slots of every CTA, in rank order
-__device__ __forceinline__ float2 rows_cluster_collect2(cg::cluster_group& cl, float2* buf)
+// post2's pair pushed into slot rank * 8 + w of every CTA of the cluster (at
+// most eight warps a CTA and eight CTAs: 64 slots), stored before the
+// cluster barrier that publishes it, so that the collect reads only local
+// shared memory; every lane of a half-warp holds its half's total
+__device__ __forceinline__ void rows_cluster_post2(cg::cluster_group& cl, float a, float b,
+                                                   float2* buf)
+{
+    const int lane = lane_id();
+    const bool hi = lane & 16;
+    float keep = hi ? b : a;
+    keep += __shfl_xor_sync(0xffffffffu, hi ? a : b, 16);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+    const int rk = lane & 15, rank = (int)cl.block_rank();
+    if (rk < (int)cl.num_blocks()) {
+        float2* dst = rk == rank ? buf : cl.map_shared_rank(buf, rk);
+        reinterpret_cast<float*>(dst + rank * 8 + (int)(threadIdx.x >> 5))[hi ? 1 : 0] = keep;
+    }
+}
+
+// the pushed pairs of every CTA, each CTA's warps in collect2's tree, the
+// CTAs added in rank order (the same bits in every CTA)
+__device__ __forceinline__ float2 rows_cluster_collect2(cg::cluster_group& cl, const float2* buf)
 {
     float2 s = make_float2(0.f, 0.f);
     const int C = (int)cl.num_blocks();
     for (int rk = 0; rk < C; ++rk) {
-        const float2 v = collect2(cl.map_shared_rank(buf, rk));
+        const float2 v = collect2(buf + rk * 8);
         s.x += v.x;
         s.y += v.y;
     }
@@ -486,11 +511,11 @@ __global__ void __launch_bounds__(max_threads_for(NP, R)) k_pcg_rows_cluster(Pcg
     float4* redA = reinterpret_cast<float4*>(XR + XS);
     float4* redB = redA + 32;
     float4* redC = redA + 64;
-    float2* pairA = reinterpret_cast<float2*>(redA + 96);
-    float2* pairB = pairA + 16;
-    float2* pairC = pairB + 16;
+    float2* pairA = reinterpret_cast<float2*>(redA + 96);  // 64 pushed slots each
+    float2* pairB = pairA + 64;
+    float2* pairC = pairB + 64;
     constexpr int SC = NP / 4 - RowTiles<NP, R>::RC;
-    float4* TS = redA + 120;
+    float4* TS = redA + kRowsClusterHead;
     float* LS = reinterpret_cast<float*>(TS + (size_t)SC * R * 2 * T);
     const bool l_staged = rule0 && g.l_smem;
     // the layout is the same in every CTA, so they all leave together
@@ -639,7 +664,7 @@ __global__ void __launch_bounds__(max_threads_for(NP, R)) k_pcg_rows_cluster(Pcg
             y[i] += p[i];
             pvp = fmaf(p[i], y[i], pvp);
         }
-        post2(pvp, 0.f, pairA);
+        rows_cluster_post2(cl, pvp, 0.f, pairA);
         cl.sync();
         const float pv = rows_cluster_collect2(cl, pairA).x;
         const float alpha = __fdividef(eta, pv);
@@ -663,8 +688,8 @@ __global__ void __launch_bounds__(max_threads_for(NP, R)) k_pcg_rows_cluster(Pcg
         if (exact)
             red[2] = l_staged ? rows_lnorm_smem<NP, R>(LS, XR, jjl, a0, n, valid)
                               : rows_lnorm<NP, R>(Lj, XR, jjl, a0, n, valid);
-        post2(red[0], red[1], pairB);
-        if (exact) post2(red[2], 0.f, pairC);
+        rows_cluster_post2(cl, red[0], red[1], pairB);
+        if (exact) rows_cluster_post2(cl, red[2], 0.f, pairC);
         cl.sync();
         {
             const float2 sb = rows_cluster_collect2(cl, pairB);
@@ -757,7 +782,7 @@ cudaError_t launch_rows_cluster_np(const PcgArgs& a, size_t limit, cudaStream_t 
         if (T > max_threads_for(NP, R)) continue;
         constexpr int SC = NP / 4 - RowTiles<NP, R>::RC;
         size_t smem = sizeof(float) * 2 * (size_t)(Nc + 2) * NP +
-                      (120 + (size_t)SC * R * 2 * T) * sizeof(float4);
+                      (kRowsClusterHead + (size_t)SC * R * 2 * T) * sizeof(float4);
         if (smem > limit) return cudaErrorInvalidConfiguration;
         PcgArgs b = a;
         const size_t l_bytes = sizeof(float) * (size_t)Nc * w.n * NP;
