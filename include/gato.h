@@ -483,10 +483,11 @@ int gato_solve_kkt_host(gato_handle* h, const gato_params* p, const float* Q, co
  * gato_solve_kkt with direct corrections after a PCG main solve
  * (refine_solver = GATO_REFINE_SOLVER_DIRECT, refine_steps > 0), whose
  * factorisation already runs beside the PCG on a low-priority stream, one
- * part below 128 solves and two from 128.  The parts of a call run
- * concurrently on internal streams of the highest priority, each on its own
- * sub-batch workspace, so the kernels of one part fill the SMs that another
- * part's leave idle (the last wave of its PCG, its shorter stages).
+ * part while the batch has at most one solve per SM and two beyond.  The
+ * parts of a call run concurrently on internal streams of the highest
+ * priority, each on its own sub-batch workspace, so the kernels of one part
+ * fill the SMs that another part's leave idle (the last wave of its PCG, its
+ * shorter stages).
  * Errors: INVALID_ARG. */
 int gato_set_parts(gato_handle* h, int parts);
 

@@ -94,6 +94,23 @@ def test_default_parts_at_the_benchmark_batch():
     check_solution(prob, dev, [0, 63, 64, 191, 255], w.n_alpha, w.beta, w.mu)
 
 
+def test_default_parts_by_batch_size():
+    """With direct corrections on device buffers: one part while the batch has
+    at most one solve per SM, two beyond; the outputs equal the one-part run's."""
+    w = WORKLOADS[1]
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    p = params_for(w)
+    assert p.refine_solver == gato.GATO_REFINE_SOLVER_DIRECT
+    for M, expect in ((n_sm, 1), (n_sm + 1, 2)):
+        prob = make_batch(w, M=M)
+        with gato.Solver(M, w.N, w.n, w.m) as s:
+            ref = device_solve(s, p, prob, 1)
+            out = device_solve(s, p, prob, 0)
+            assert s.get_parts() == expect
+        same(out, ref)
+        assert not out["status"].any()
+
+
 def test_parts_are_reused_and_rebuilt():
     w = WORKLOADS[1]
     prob = make_batch(w, M=9)
@@ -160,7 +177,8 @@ def test_call_in_parts_allocates_nothing_and_can_be_captured():
     re-partitions the batch leaves the free device memory unchanged, and a
     call captured into a CUDA graph replays to the same outputs."""
     w = WORKLOADS[4]
-    M = 128
+    # one solve more than the SMs, so that the automatic choice runs two parts
+    M = torch.cuda.get_device_properties(0).multi_processor_count + 1
     prob = make_batch(w, M=M)
     p = params_for(w)
     d = gato.to_device(prob)
@@ -184,7 +202,7 @@ def test_call_in_parts_allocates_nothing_and_can_be_captured():
                         cap["best"], cap["status"])
         g.replay()
         torch.cuda.synchronize()
-        assert s.get_parts() == 2  # 128 solves, direct corrections
+        assert s.get_parts() == 2  # more solves than SMs, direct corrections
         same({k: v.cpu().numpy() for k, v in cap.items()}, ref)
 
 
