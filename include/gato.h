@@ -483,7 +483,9 @@ int gato_solve_kkt_host(gato_handle* h, const gato_params* p, const float* Q, co
  * gato_solve_kkt with direct corrections after a PCG main solve
  * (refine_solver = GATO_REFINE_SOLVER_DIRECT, refine_steps > 0), whose
  * factorisation already runs beside the PCG on a low-priority stream, one
- * part while the batch has at most one solve per SM and two beyond.  The
+ * part while the PCG kernel holds the whole batch at once (its resident
+ * blocks over the device: one solve per SM at N = 128, n = 14, more at
+ * shorter horizons) and two beyond.  The
  * parts of a call run concurrently on internal streams of the highest
  * priority, each on its own sub-batch workspace, so the kernels of one part
  * fill the SMs that another part's leave idle (the last wave of its PCG, its

@@ -95,18 +95,21 @@ def test_default_parts_at_the_benchmark_batch():
 
 
 def test_default_parts_by_batch_size():
-    """With direct corrections on device buffers: one part while the batch has
-    at most one solve per SM, two beyond; the outputs equal the one-part run's."""
-    w = WORKLOADS[1]
+    """With direct corrections on device buffers: one part while the PCG holds
+    the whole batch at once, two beyond.  At N = 128, n = 14 the wide-tile
+    kernel holds one solve per SM; at N = 32 an SM holds several, so one more
+    solve than SMs still runs as one part.  The outputs equal the one-part
+    run's."""
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
-    p = params_for(w)
-    assert p.refine_solver == gato.GATO_REFINE_SOLVER_DIRECT
-    for M, expect in ((n_sm, 1), (n_sm + 1, 2)):
+    for wi, M, expect in ((4, n_sm, 1), (4, n_sm + 1, 2), (1, n_sm + 1, 1)):
+        w = WORKLOADS[wi]
+        p = params_for(w)
+        assert p.refine_solver == gato.GATO_REFINE_SOLVER_DIRECT
         prob = make_batch(w, M=M)
         with gato.Solver(M, w.N, w.n, w.m) as s:
             ref = device_solve(s, p, prob, 1)
             out = device_solve(s, p, prob, 0)
-            assert s.get_parts() == expect
+            assert s.get_parts() == expect, (wi, M)
         same(out, ref)
         assert not out["status"].any()
 

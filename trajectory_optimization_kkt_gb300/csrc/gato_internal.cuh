@@ -220,6 +220,8 @@ bool sizes_supported(const Work& w, const gato_params* p, int smem_limit);
 // the linear solver a call with parameters p uses: GATO_LINSYS_PCG,
 // GATO_LINSYS_BDSV or GATO_LINSYS_BDSV_CHRONO
 int linsys_for(const gato_params* p, int N);
+// solves one PCG launch over the handle's whole batch holds at once (pcg.cu)
+int pcg_solves_per_wave(const gato_handle* h, const gato_params* p);
 // formation with Q_form, right-hand side, linear solve (from lambda0 when not
 // NULL), refinement rounds and line search with Q_merit, on stream st; the
 // handle's timing events are recorded when `timed`

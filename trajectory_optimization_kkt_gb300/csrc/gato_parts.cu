@@ -194,12 +194,13 @@ int parts_init(gato_handle* h)
 // below 64 one is best).  A call on device buffers whose corrections are
 // direct after a PCG main solve already overlaps its longest short stage
 // (the factorisation, on the side stream) with the PCG, and fewer parts do
-// better there: one while the batch has at most one solve per SM, two
-// beyond (measured: 128 solves of N = 128 1.09 ms in one part against 1.18
-// in two, 152 1.20 against 1.21, 200 1.90 against 1.86, 256 1.97 against
-// 1.91; 128 of N = 16, n = 36 3.49 against 3.56 ms; 128 of N = 32, n = 12
-// 0.44 against 0.50 ms).  The host entry keeps the first rule: its parts
-// also hide the input copies.
+// better there: one while the PCG holds the whole batch at once (one wave),
+// two beyond (measured: 128 solves of N = 128 1.09 ms in one part against
+// 1.18 in two, 152 1.20 against 1.21, 200 1.90 against 1.86, 256 1.97
+// against 1.91; 256 of N = 64 1.01 against 1.07, of N = 32 0.64 against
+// 0.73, of N = 16 0.39 against 0.47; 608 of N = 16 0.52 against 0.56; 128 of
+// N = 16, n = 36 3.49 against 3.56 ms).  The host entry keeps the first
+// rule: its parts also hide the input copies.
 int parts_for(const gato_handle* h, const gato_params* p, bool host)
 {
     const int M = h->w.M;
@@ -207,7 +208,8 @@ int parts_for(const gato_handle* h, const gato_params* p, bool host)
     if (k <= 0) {
         const bool forked = !host && p && p->refine_solver == GATO_REFINE_SOLVER_DIRECT &&
                             p->refine_steps > 0 && linsys_for(p, h->w.N) == GATO_LINSYS_PCG;
-        k = forked ? (M > h->num_sms ? 2 : 1) : (M >= 128 ? 4 : (M >= 64 ? 2 : 1));
+        k = forked ? (M > pcg_solves_per_wave(h, p) ? 2 : 1)
+                   : (M >= 128 ? 4 : (M >= 64 ? 2 : 1));
     }
     if (k > M) k = M;
     return k;

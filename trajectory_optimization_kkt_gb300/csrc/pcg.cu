@@ -1413,6 +1413,32 @@ bool quad_preferred(const gato_handle* h, int H, int Tw, size_t smem_wide)
 
 }  // namespace
 
+// Solves a PCG launch over the handle's whole batch holds at once: for the
+// fp32 kernels at 7 <= n <= 16, N <= 128 the wide-tile kernel's resident
+// blocks per SM times the SMs (the quad kernel the automatic rule may take
+// instead holds at least as many), otherwise one solve per SM (the
+// register-row, double-float and generic kernels hold one at the sizes they
+// serve).
+int pcg_solves_per_wave(const gato_handle* h, const gato_params* p)
+{
+    const Work& w = h->w;
+    const int kind = h->pcg_kernel;
+    if (p && p->pcg_precision != GATO_PCG_PRECISION_FF && w.n >= 7 && w.n <= 16 &&
+        w.N <= 128 &&
+        (kind == GATO_PCG_AUTO || kind == GATO_PCG_WIDE || kind == GATO_PCG_QUAD)) {
+        int Tw = ((2 * w.N + 31) / 32) * 32;
+        if (Tw < 64) Tw = 64;
+        const size_t limit = (size_t)h->smem_optin;
+        size_t smem = wide_smem_bytes(w, p->stop_rule == GATO_STOP_RESIDUAL);
+        if (smem > limit) smem = wide_smem_bytes(w, 0);
+        if (Tw <= 256 && smem <= limit) {
+            const int occ = wide_blocks_per_sm((w.n + 1) / 2, Tw, smem);
+            if (occ > 0) return occ * h->num_sms;
+        }
+    }
+    return h->num_sms;
+}
+
 // launches the PCG kernel for these sizes and parameters; ran gets its
 // GATO_PCG_* value
 static cudaError_t launch_pcg_pick(gato_handle* h, const gato_params* p, int set,
