@@ -100,9 +100,19 @@ __global__ void k_form_diag(Work w, const float* __restrict__ A, const float* __
         warp_copy(sV, w.V + sol * w.sKnm + (size_t)(j - 1) * nm, nm);
         warp_copy(sB, B + ((size_t)sol * K + (j - 1)) * nm, nm);
         __syncwarp();
-        // theta: A Q^-1 A^T = -S_{j,j-1} A^T, plus B R^-1 B^T = V B^T
-        warp_gemm<false, true>(n, n, n, sO, sA, sD, -1.f, true);
-        warp_gemm<false, true>(n, n, m, sV, sB, sD, 1.f, true);
+        // theta: A Q^-1 A^T = -S_{j,j-1} A^T, plus B R^-1 B^T = V B^T; A^T (and
+        // B^T where m <= n, so that it fits) is staged in sL (free until the
+        // factorisation) so that the products take warp_gemm's 128-bit path
+        // (the transposed operand's strided reads would conflict on the
+        // banks); the sums are the same
+        warp_transpose(sA, n, n, sL);
+        warp_gemm<false, false>(n, n, n, sO, sL, sD, -1.f, true);
+        if (m <= n) {
+            warp_transpose(sB, n, m, sL);
+            warp_gemm<false, false>(n, n, m, sV, sL, sD, 1.f, true);
+        } else {
+            warp_gemm<false, true>(n, n, m, sV, sB, sD, 1.f, true);
+        }
     }
     __syncwarp();
     const size_t off = sol * w.sNnn + (size_t)j * nn;
@@ -145,7 +155,9 @@ __global__ void k_form_off(Work w)
     warp_gemm<false, false>(n, n, n, s1, s2, s4, 1.f, false);
     warp_copy(s1, w.Linv + dp, nn);  // L_j^-1 is read no more: L_{j-1}^-1
     __syncwarp();
-    warp_gemm<false, true>(n, n, n, s4, s1, w.Nh + oj, 1.f, false);
+    // L_{j-1}^-T staged in s2 (O is read no more) for warp_gemm's 128-bit path
+    warp_transpose(s1, n, n, s2);
+    warp_gemm<false, false>(n, n, n, s4, s2, w.Nh + oj, 1.f, false);
 }
 
 // The explicit Phi^-1 blocks for export: S_jj^-1 = L_j^-T L_j^-1 ...

@@ -403,6 +403,17 @@ __device__ inline void warp_gram_lower(const float* Linv, float* out, int n)
     __syncwarp();
 }
 
+// dst (cols x rows, row-major) = src^T for a row-major rows x cols src: the
+// reads are contiguous, the writes strided (once per element)
+__device__ inline void warp_transpose(const float* src, int rows, int cols, float* dst)
+{
+    for (int t = lane_id(); t < rows * cols; t += 32) {
+        const int i = t / cols, j = t - i * cols;
+        dst[j * rows + i] = src[t];
+    }
+    __syncwarp();
+}
+
 // C (r x c) = s * op(A) op(B) (+ C when acc).  op(A) is r x kk: A row-major
 // r x kk, or kk x r when TA.  op(B) is kk x c: B row-major kk x c, or c x kk
 // when TB.  Any of the pointers may be global or shared.
