@@ -38,8 +38,8 @@ WORKLOAD_INDEX = 4  # M=256, N=128, n=14, m=7
 # kernel source it was taken on (sha256 prefix of csrc/pcg.cu and
 # csrc/pcg_common.cuh), null otherwise.  Captured on 152 solves (one block
 # per SM) and scaled by the solves processed to the 256-solve launch
-# (89.70 MB x 256 / 152).
-PCG_TRAFFIC = {"pcg_sha": "c85f6baf43f3322f", "bytes_per_launch": 151079451}
+# (89.86 MB x 256 / 152).
+PCG_TRAFFIC = {"pcg_sha": "bf17afc3f87af630", "bytes_per_launch": 151340301}
 
 FP32_LANES_PER_SM = 128  # FFMA lanes per SM (4 sub-partitions x 32)
 

@@ -101,11 +101,11 @@ extern "C" {
                                       N <= 128; column sums reduced by warp
                                       shuffles within the quad) where it
                                       applies, else as GATO_PCG_AUTO.  AUTO
-                                      takes it where the wide-tile kernel would
-                                      leave each SM with at most four working
-                                      warps (2N threads per solve, as many
-                                      solves per SM as the batch and the
-                                      occupancy give)                             */
+                                      takes it at n = 12, and elsewhere where
+                                      the wide-tile kernel would leave each SM
+                                      with at most four working warps (2N
+                                      threads per solve, as many solves per SM
+                                      as the batch and the occupancy give)        */
 /* reported in gato_stats.pcg_kernel only (not choices of gato_set_pcg_kernel) */
 #define GATO_PCG_CLUSTER 6         /* the wide-tile iteration over a cluster of
                                       2 or 4 CTAs per solve (128 < N <= 512)      */

@@ -321,6 +321,7 @@ AUTO_CHOICE = [
     ("M16_N64_n14_quad", 16, 64, 14, 7, {}, Q, Q),        # 4
     ("M16_N96_n14_wide", 16, 96, 14, 7, {}, W, W),        # 6
     ("M256_N128_n14_wide", 256, 128, 14, 7, {}, W, W),    # 8, in four parts
+    ("M256_N128_n12_quad", 256, 128, 12, 6, {}, Q, Q),    # n = 12: the quad kernel
     # four parts of 80: one part alone would leave 2 warps per SM, the whole
     # batch (3 solves per SM) leaves 6
     ("M320_N32_n14_parts", 320, 32, 14, 7, {}, W, W),
