@@ -402,6 +402,10 @@ ROWS = [
     ("n36_N37_cluster4_ragged", 2, 37, 36, 12), ("n24_N64_cluster2", 2, 64, 24, 8),
     ("n17_N100_cluster2", 1, 100, 17, 5), ("n64_N12_cluster4", 1, 12, 64, 8),
     ("n36_N128_cluster8", 1, 128, 36, 12),
+    # one row per thread (n > 48): CTAs of 10 to 11 warps, whose pushed block
+    # sums take more than eight slots per CTA
+    ("n64_N10_cluster2_10warps", 1, 10, 64, 8), ("n56_N24_cluster4_11warps", 1, 24, 56, 8),
+    ("n64_N40_cluster8_10warps", 1, 40, 64, 8),
 ]
 
 

@@ -34,9 +34,13 @@ namespace {
 // rows per thread: the two tiles (2 R NP floats) within 216 registers
 constexpr int rows_for(int NP) { return 216 / (2 * NP) > 0 ? 216 / (2 * NP) : 1; }
 
+// pushed pair slots per buffer in the cluster kernel: C CTAs of nw warps each
+// (C <= 8; nw <= 12 for the blocks max_threads_for allows)
+constexpr int kRowsClusterSlots = 128;
 // float4s before the tile chunks in the cluster kernel's shared memory: three
-// block-sum buffers of 32 and three pushed-pair buffers of 64 float2
-constexpr int kRowsClusterHead = 96 + 3 * 32;
+// block-sum buffers of 32 and three pushed-pair buffers of kRowsClusterSlots
+// float2
+constexpr int kRowsClusterHead = 96 + 3 * kRowsClusterSlots / 2;
 
 // threads per block the registers allow with R rows per thread: 64K
 // registers over the tiles plus about 56 for the rest, in whole warps; with
@@ -428,9 +432,9 @@ __global__ void __launch_bounds__(max_threads_for(NP, R)) k_pcg_rows(PcgArgs g)
 // order, so all CTAs hold the same scalars and take the same branches; every
 // barrier is a cluster barrier.  The recovery is cluster_recover's.
 
-// post2's pair pushed into slot rank * 8 + w of every CTA of the cluster (at
-// most eight warps a CTA and eight CTAs: 64 slots), stored before the
-// cluster barrier that publishes it, so that the collect reads only local
+// post2's pair pushed into slot rank * nw + w of every CTA of the cluster (nw
+// warps a CTA; the launch keeps C nw within kRowsClusterSlots), stored before
+// the cluster barrier that publishes it, so that the collect reads only local
 // shared memory; every lane of a half-warp holds its half's total
 __device__ __forceinline__ void rows_cluster_post2(cg::cluster_group& cl, float a, float b,
                                                    float2* buf)
@@ -444,7 +448,8 @@ __device__ __forceinline__ void rows_cluster_post2(cg::cluster_group& cl, float 
     const int rk = lane & 15, rank = (int)cl.block_rank();
     if (rk < (int)cl.num_blocks()) {
         float2* dst = rk == rank ? buf : cl.map_shared_rank(buf, rk);
-        reinterpret_cast<float*>(dst + rank * 8 + (int)(threadIdx.x >> 5))[hi ? 1 : 0] = keep;
+        reinterpret_cast<float*>(dst + rank * (int)(blockDim.x >> 5) +
+                                 (int)(threadIdx.x >> 5))[hi ? 1 : 0] = keep;
     }
 }
 
@@ -453,9 +458,9 @@ __device__ __forceinline__ void rows_cluster_post2(cg::cluster_group& cl, float 
 __device__ __forceinline__ float2 rows_cluster_collect2(cg::cluster_group& cl, const float2* buf)
 {
     float2 s = make_float2(0.f, 0.f);
-    const int C = (int)cl.num_blocks();
+    const int C = (int)cl.num_blocks(), nw = (int)(blockDim.x >> 5);
     for (int rk = 0; rk < C; ++rk) {
-        const float2 v = collect2(buf + rk * 8);
+        const float2 v = collect2(buf + rk * nw);
         s.x += v.x;
         s.y += v.y;
     }
@@ -511,9 +516,9 @@ __global__ void __launch_bounds__(max_threads_for(NP, R)) k_pcg_rows_cluster(Pcg
     float4* redA = reinterpret_cast<float4*>(XR + XS);
     float4* redB = redA + 32;
     float4* redC = redA + 64;
-    float2* pairA = reinterpret_cast<float2*>(redA + 96);  // 64 pushed slots each
-    float2* pairB = pairA + 64;
-    float2* pairC = pairB + 64;
+    float2* pairA = reinterpret_cast<float2*>(redA + 96);  // kRowsClusterSlots each
+    float2* pairB = pairA + kRowsClusterSlots;
+    float2* pairC = pairB + kRowsClusterSlots;
     constexpr int SC = NP / 4 - RowTiles<NP, R>::RC;
     float4* TS = redA + kRowsClusterHead;
     float* LS = reinterpret_cast<float*>(TS + (size_t)SC * R * 2 * T);
@@ -780,6 +785,7 @@ cudaError_t launch_rows_cluster_np(const PcgArgs& a, size_t limit, cudaStream_t 
         int T = ((Nc * TPK + 31) / 32) * 32;
         if (T < 64) T = 64;
         if (T > max_threads_for(NP, R)) continue;
+        if (C * (T / 32) > kRowsClusterSlots) continue;  // the pushed pair slots
         constexpr int SC = NP / 4 - RowTiles<NP, R>::RC;
         size_t smem = sizeof(float) * 2 * (size_t)(Nc + 2) * NP +
                       (kRowsClusterHead + (size_t)SC * R * 2 * T) * sizeof(float4);
